@@ -1,0 +1,442 @@
+"""Benchmark of libpk's persistent Jacobi sweep on one GB300 (or N replicas).
+
+Default workload: Laplace fp32 on a 16384 x 16384 interior grid (two 1 GiB
+ping-pong buffers, field uniform [0,1) from seed 3), 100 sweeps per step, run
+as ONE persistent cooperative kernel per step (pk_run_sweeps).  The field is
+2 GiB, larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``value`` is whole-job cell-updates/s from
+CUDA events recorded on the launching stream around each kernel (libpk
+records them; pk_run_info.device_us); ``e2e`` is the same metric through the
+public C ABI with host buffers (pinned H2D copy of the field, the sweeps, a
+D2H copy of the result) on the host clock.  ``roofline`` reports the
+dominant kernel's algorithmic HBM bytes (8 B per cell-update: read the
+previous iterate once, write the new one once) per launch over its event
+time, against the measured copy bandwidth.  ``cpu_baseline`` times the CPU
+oracle on a bounded sample of the same workload, single-threaded.
+
+``--impl reference`` runs the CPU oracle arm instead (the only reference for
+this method), on the same config and metric.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the method runs on one GPU; nothing is exchanged on the data path); host
+timing is combined with a gloo max-reduction.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "us/sweep (persistent vs per-launch) and cell-updates/s; HBM GB/s vs peak"
+UNIT = "cell-updates/s"
+
+WORKLOADS = {
+    # name: (n, seed, sweeps, poisson, tol, check_every)
+    "laplace-16384x16384-100sweeps": (16384, 3, 100, False, 0.0, 0),
+    "poisson-4096x4096-2000sweeps-res10": (4096, 2, 2000, True, 1e-4, 10),
+    "laplace-512x512-1000sweeps": (512, 1, 1000, False, 0.0, 0),
+    "laplace-64x64-topedge-100sweeps": (64, None, 100, False, 0.0, 0),
+}
+DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
+
+# DRAM traffic of one launch of the dominant kernel, from the ncu capture
+# summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum,
+# scaled to this workload's launch); valid only while the kernel source
+# hash matches.
+TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for name in ("pk_kernels.cu", "pk_device.cuh", "pk_internal.h"):
+        with open(os.path.join(ROOT, "iterative_stencil_solver_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            d = json.load(fh)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def make_workload(name):
+    from iterative_stencil_solver_gb300 import inputs
+    n, seed, sweeps, poisson, tol, ce = WORKLOADS[name]
+    if name.startswith("laplace-64x64-topedge"):
+        w = inputs.workload_laplace_top_edge(n)
+    elif poisson:
+        w = inputs.workload_poisson_random_source(n, seed)
+    else:
+        w = inputs.workload_laplace_random(n, seed)
+    w.update(sweeps=sweeps, tol=tol, check_every=ce)
+    return w
+
+
+# ---- distributed plumbing (replicas only) -------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group("gloo", rank=rank, world_size=world)
+    return world, rank, local
+
+
+def dist_barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def dist_max(world, value):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_sum(world, value):
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---- clocks -------------------------------------------------------------------
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % self.index)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], 0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax = max(smax, float(parts[2]))
+                except ValueError:
+                    continue
+                for name, flag in zip(names, parts[5:9]):
+                    if flag.lower() == "active":
+                        reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---- CPU oracle timing ---------------------------------------------------------
+
+def oracle_sample(w, target_s=10.0, max_rows=None):
+    """Time the single-threaded oracle on a band of the workload's rows.
+
+    The band keeps the full row width; its top and bottom rows act as its
+    ring.  Returns (cell-updates/s, description, seconds)."""
+    import oracle
+    nx = w["nx"]
+    ny = w["ny"] if max_rows is None else min(w["ny"], max_rows)
+    band = np.ascontiguousarray(w["u0"][:ny + 2])
+    f = None if w["f"] is None else np.ascontiguousarray(w["f"][:ny])
+    h2 = oracle.h2(nx)
+    t0 = time.perf_counter()
+    oracle.jacobi_run(band, f=f, n=2, h2v=h2, threads=1)
+    per_sweep = max((time.perf_counter() - t0) / 2.0, 1e-6)
+    sweeps = int(max(1, min(w["sweeps"], target_s / per_sweep)))
+    t0 = time.perf_counter()
+    oracle.jacobi_run(band, f=f, n=sweeps, h2v=h2, threads=1)
+    dt = time.perf_counter() - t0
+    updates = float(nx) * ny * sweeps
+    desc = "%d sweeps over a %d x %d band of the %d x %d workload, 1 thread" % (
+        sweeps, nx, ny, w["nx"], w["ny"])
+    return updates / dt, desc, dt
+
+
+def reference_arm(args, world, rank):
+    if rank != 0:
+        return
+    w = make_workload(args.workload)
+    import oracle  # noqa: F401
+    rows = min(w["ny"], max(1, int(4e7 // w["nx"])))  # ~4e7 cells per sweep sample
+    values = []
+    for step in range(args.warmup + args.steps):
+        v, desc, _ = oracle_sample(w, target_s=1.0, max_rows=rows)
+        if step >= args.warmup:
+            values.append(v)
+    value = statistics.median(values)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- supplementary measurements (rank 0) ------------------------------------------
+
+def latency_extras(pk):
+    """512^2 persistent vs per-launch (1000 sweeps), floors, barrier costs, and
+    the task-queue round trip (10,000 tasks)."""
+    from iterative_stencil_solver_gb300 import inputs
+    out = {}
+    w = inputs.workload_laplace_random(512, 1)
+    ctx = pk.pk_create(512, 512, w["u0"], None)
+    try:
+        plan = pk.pk_get_plan(ctx)
+        for _ in range(3):
+            pk.pk_run_sweeps(ctx, 1000)
+            pk.pk_run_sweeps_launch(ctx, 1000)
+        pers = [pk.pk_run_sweeps(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
+        launch = [pk.pk_run_sweeps_launch(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
+        sync_each, queued = pk.pk_bench_launch_floor(ctx, 2000)
+        nb = 10000
+        b0 = pk.pk_bench_barrier(ctx, 0, 0, 0)
+        ours = (pk.pk_bench_barrier(ctx, 0, 0, nb) - b0) / nb
+        c0 = pk.pk_bench_barrier(ctx, 1, 0, 0)
+        cgs = (pk.pk_bench_barrier(ctx, 1, 0, nb) - c0) / nb
+        p_med, l_med = statistics.median(pers), statistics.median(launch)
+        out["laplace_512_1000sweeps"] = {
+            "persistent_us_per_sweep": p_med, "launch_us_per_sweep": l_med,
+            "persistent_speedup": l_med / p_med, "grid": plan["grid"],
+            "variant": "direct" if plan["variant"] == 1 else "stream",
+            "persistent_cell_updates_per_s": 512 * 512 / (p_med * 1e-6),
+            "floors_us": {"empty_launch_sync_each": sync_each, "empty_launch_queued": queued,
+                          "grid_barrier": ours, "cg_grid_sync": cgs},
+            "persistent_sweep_in_barriers": p_med / ours if ours > 0 else None,
+            "persistent_sweep_in_queued_launches": p_med / queued if queued > 0 else None,
+        }
+    finally:
+        pk.pk_destroy(ctx)
+    w = inputs.workload_laplace_top_edge(64)
+    ctx = pk.pk_create(64, 64, w["u0"], None)
+    try:
+        for _ in range(3):
+            pk.pk_run_sweeps(ctx, 100)
+            pk.pk_run_sweeps_launch(ctx, 100)
+        pers = statistics.median(pk.pk_run_sweeps(ctx, 100)["device_us"] / 100 for _ in range(5))
+        launch = statistics.median(pk.pk_run_sweeps_launch(ctx, 100)["device_us"] / 100
+                                   for _ in range(5))
+        out["laplace_64_topedge_100sweeps"] = {"persistent_us_per_sweep": pers,
+                                               "launch_us_per_sweep": launch,
+                                               "persistent_speedup": launch / pers}
+    finally:
+        pk.pk_destroy(ctx)
+    # task queue: 10,000 tasks alternating 1-sweep Jacobi (256^2) and axpy (65,536)
+    import torch
+    w = inputs.workload_task_queue(256, 65536, 4)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    x = torch.from_numpy(w["x"]).to(dev)
+    y = torch.from_numpy(w["y"]).to(dev)
+    torch.cuda.synchronize()
+    tasks = [pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=1),
+             pk.make_task(pk.PK_TASK_AXPY, a=0.5, x=x.data_ptr(), y=y.data_ptr(),
+                          length=x.numel())]
+    ctx = pk.pk_create(256, 256, w["u0"], None)
+    try:
+        mb = pk.pk_bench_tasks(ctx, 0, tasks, 10100)[100:] / 1e3
+        pk.pk_shutdown(ctx)
+        ln = pk.pk_bench_tasks(ctx, 1, tasks, 10100)[100:] / 1e3
+        out["task_queue_10000"] = {
+            "mailbox_round_trip_us": {"p50": float(np.percentile(mb, 50)),
+                                      "p99": float(np.percentile(mb, 99))},
+            "launch_sync_round_trip_us": {"p50": float(np.percentile(ln, 50)),
+                                          "p99": float(np.percentile(ln, 99))},
+            "task_grid": pk.pk_get_plan(ctx)["task_grid"],
+        }
+    finally:
+        pk.pk_destroy(ctx)
+    # Poisson 4096^2 with the in-kernel residual every 10 sweeps
+    w = make_workload("poisson-4096x4096-2000sweeps-res10")
+    ctx = pk.pk_create(4096, 4096, w["u0"], w["f"])
+    try:
+        info = pk.pk_run_sweeps(ctx, 2000, 1e-4, 10)
+        us = info["device_us"] / max(1, info["sweeps_done"])
+        out["poisson_4096_res10"] = {
+            "us_per_sweep": us, "sweeps_done": info["sweeps_done"],
+            "res_ratio": info["res_last"] / info["res0"] if info["res0"] else None,
+            "hbm_gbs_algorithmic": 12.0 * 4096 * 4096 / (us * 1e-6) / 1e9,
+            "n_checks": info["n_checks"],
+        }
+    finally:
+        pk.pk_destroy(ctx)
+    return out
+
+
+# ---- main arm ----------------------------------------------------------------------
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["pk", "reference"], default="pk")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true", help="skip the supplementary measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+        return
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (there is no CPU fallback)")
+    torch.cuda.set_device(local)
+    from iterative_stencil_solver_gb300 import build_ext
+    build_ext.build()
+    from iterative_stencil_solver_gb300 import pk
+
+    w = make_workload(args.workload)
+    nx, ny, sweeps = w["nx"], w["ny"], w["sweeps"]
+    cells = nx * ny
+    ctx = pk.pk_create(nx, ny, w["u0"], w["f"])
+    try:
+        plan = pk.pk_get_plan(ctx)
+        for _ in range(args.warmup):
+            pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+        clocks = ClockSampler(local)
+        clocks.start()
+        dist_barrier(world)
+        torch.cuda.synchronize()
+        dev_us, updates = [], 0
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+            dev_us.append(info["device_us"])
+            updates += cells * info["sweeps_done"]
+        torch.cuda.synchronize()
+        host_s = time.perf_counter() - t0
+        dist_barrier(world)
+        clk = clocks.stop()
+        dev_s = sum(dev_us) * 1e-6
+        dev_s_max = dist_max(world, dev_s)
+        updates_all = dist_sum(world, updates)
+        value = updates_all / dev_s_max
+        ms_per_step = dev_s_max * 1e3 / args.steps
+        us_per_sweep = dev_s * 1e6 / (updates / cells)
+
+        # e2e through the public API with pinned host buffers
+        host_in = torch.from_numpy(w["u0"]).pin_memory().numpy()
+        host_out = torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory().numpy()
+        pk.pk_set_field(ctx, host_in)
+        pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+        pk.pk_get_field(ctx, host_out)
+        dist_barrier(world)
+        e2e_updates = 0
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            pk.pk_set_field(ctx, host_in)
+            info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+            pk.pk_get_field(ctx, host_out)
+            e2e_updates += cells * info["sweeps_done"]
+        e2e_s = dist_max(world, time.perf_counter() - t0)
+        e2e_value = dist_sum(world, e2e_updates) / e2e_s
+    finally:
+        pk.pk_destroy(ctx)
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    bytes_per_update = 12.0 if w["f"] is not None else 8.0
+    launch_us = statistics.median(dev_us)
+    alg_bytes = bytes_per_update * cells * sweeps
+    achieved = alg_bytes / (launch_us * 1e-6) / 1e9
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha"] == kernel_source_sha() else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "nx": nx, "ny": ny, "sweeps_per_step": sweeps,
+                   "variant": "stream" if plan["variant"] == 2 else "direct",
+                   "grid": plan["grid"], "l2": "inputs larger than L2 (2 x field > 129 MB)"
+                   if 2 * 4 * cells > 129e6 else "L2-resident",
+                   "parallelism": "replicas" if world > 1 else "single-gpu"},
+        "us_per_sweep": us_per_sweep,
+        "hbm_gbs_algorithmic": achieved,
+        "host_s": host_s,
+        "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": peak_kind,
+                     "kernel": "k_persistent_stream<laplace>" if plan["variant"] == 2
+                     else "k_persistent_direct",
+                     "algorithmic_bytes_per_launch": alg_bytes},
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": int(w["u0"].nbytes),
+                "d2h_bytes_per_step": int(w["u0"].nbytes)},
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        v, desc, dt = oracle_sample(w, target_s=10.0, max_rows=min(ny, 2048))
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": desc, "seconds": dt}
+    if not args.no_extras:
+        line["extras"] = latency_extras(pk)
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,251 @@
+/*
+ * pk.h -- C ABI of libpk, a persistent Jacobi 5-point Laplace/Poisson solver
+ * for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources (page title -- section):
+ *   [P1] "Persistent Kernels: Bridging GPU-CPU Execution"
+ *   [P2] "Grid-Wide Barriers and Persistent Work Queues"
+ *   [P3] "CUDA persist kernel" (finaltheory, "Persistent Thread")
+ *   [P4] "@persistent" (phobos-lang docs)
+ *
+ * Problem ([P1] "The problem (another PDE solver)"): Poisson's equation
+ * u_xx + u_yy = f on the unit square with Dirichlet values on the boundary,
+ * discretised by central differences on nx x ny interior points with
+ * spacing h = 1/(nx+1).  One Jacobi sweep ([P1] "Implementation details and
+ * correctness") computes every interior point from the previous iterate
+ * into the other buffer of a ping-pong pair ([P3] "Ping-Pong Buffer"):
+ *
+ *     u'[j][i] = 0.25f * (((W + E) + (S + N)) - g[j][i]),   g = fl32(h^2 * f)
+ *
+ * with W = u[j][i-1], E = u[j][i+1], S = u[j-1][i], N = u[j+1][i].  Every
+ * operation is one binary32 operation rounded to nearest even in exactly
+ * this order (no FMA contraction, no flush to zero), so results are the same
+ * bit for bit as a plain sequential CPU implementation.  For Laplace (f
+ * absent) the "- g" step is skipped.
+ *
+ * Field layout.  A field has (ny+2) rows of (nx+2) cells including the
+ * Dirichlet ring (rows 0 and ny+1, columns 0 and nx+1), which is never
+ * written.  Host arrays (pk_create, pk_get_field, pk_set_field) are packed
+ * row-major, (ny+2)*(nx+2) floats.  Device buffers are pitched: cell (j, i)
+ * lives at base[j * pitch + i + 3], so interior column 1 starts on a 16-byte
+ * boundary; pitch (in floats) is a multiple of 32 and at least nx + 8
+ * (pk_layout gives the values).  Sources are ny x nx interior arrays.
+ *
+ * Return codes: PK_OK (0) or a negative PK_E* code; pk_last_error(ctx)
+ * returns a message for the last failure on that context (or for the last
+ * failed pk_create* call when ctx is NULL).  A context is bound to one CUDA
+ * stream and is not thread-safe.
+ */
+#ifndef PK_H
+#define PK_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ------------------------------------------------------ */
+#define PK_OK 0
+#define PK_EINVAL (-1)      /* bad argument: size <= 0, overflow, NULL, non-finite input */
+#define PK_ECUDA (-2)       /* a CUDA runtime call failed (message in pk_last_error) */
+#define PK_ENORESIDENT (-3) /* cooperative launch refused: the grid cannot be co-resident */
+#define PK_ETIMEDOUT (-4)   /* a device spin limit or a host deadline expired */
+#define PK_EBUSY (-5)       /* the task kernel is live, or the mailbox ring is full */
+#define PK_ESHUTDOWN (-6)   /* the task kernel has stopped; the task will not run */
+#define PK_EDEVICE (-7)     /* the kernel reported an internal error status */
+
+/* ---- sweep variants ---------------------------------------------------- */
+#define PK_VARIANT_AUTO 0   /* STREAM when the two fields exceed half of L2, else DIRECT */
+#define PK_VARIANT_DIRECT 1 /* each thread loads its own float4 and neighbours (L2-resident grids) */
+#define PK_VARIANT_STREAM 2 /* TMA bulk row staging + register window down row bands (HBM grids) */
+
+/* ---- option flags ------------------------------------------------------ */
+#define PK_FLAG_LAUNCH_PROBLEM_GRID 0x1u /* pk_run_sweeps_launch: one thread per float4, not the persistent grid */
+#define PK_FLAG_ALTERNATE_DIRECTION 0x2u /* STREAM: odd sweeps walk each band bottom-up (reuses L2) */
+
+/* ---- task kinds for the mailbox ---------------------------------------- */
+#define PK_TASK_NOP 0
+#define PK_TASK_JACOBI 1 /* n_sweeps Laplace/Poisson sweeps of the context's field */
+#define PK_TASK_AXPY 2   /* y[q] = fl32(fl32(a * x[q]) + y[q]), q < len */
+#define PK_TASK_STOP 3   /* the task kernel finishes and exits */
+
+typedef struct pk_ctx pk_ctx;
+
+/* Result of one pk_run_sweeps / pk_run_sweeps_launch call. */
+typedef struct {
+    int64_t sweeps_done;  /* index k of the iterate now current (sweeps performed) */
+    double res0;          /* ||r(U_0)||_2, 0 when checks are off */
+    double res_last;      /* ||r(U_k)||_2 at the last check */
+    float res_max_last;   /* max |r(U_k)| at the last check */
+    int32_t status;       /* PK_OK or the device-reported error */
+    int32_t n_checks;     /* residual evaluations performed */
+    int32_t current;      /* buffer holding the current iterate: 0 = A, 1 = B */
+    int32_t grid;         /* CTAs the sweeps ran with */
+    int32_t variant;      /* PK_VARIANT_DIRECT or PK_VARIANT_STREAM */
+    double device_us;     /* device time of the call: CUDA events on the context's
+                             stream around its kernels (launch gaps included) */
+} pk_run_info;
+
+/* A mailbox task ([P1] "Base implementation": the host writes a task, the
+ * resident kernel polls for it).  x and y are DEVICE pointers owned by the
+ * caller and must stay valid until the task is done. */
+typedef struct {
+    int32_t kind;     /* PK_TASK_* */
+    int32_t n_sweeps; /* PK_TASK_JACOBI: sweeps to run (>= 1) */
+    float a;          /* PK_TASK_AXPY: scale */
+    int32_t reserved;
+    const float *x;   /* PK_TASK_AXPY */
+    float *y;         /* PK_TASK_AXPY */
+    int64_t len;      /* PK_TASK_AXPY: elements */
+} pk_task;
+
+typedef struct {
+    uint32_t struct_size;             /* sizeof(pk_options) */
+    int32_t variant;                  /* PK_VARIANT_* */
+    int32_t grid_override;            /* CTAs for sweeps; 0 = sized by occupancy and problem */
+    int32_t task_grid;                /* CTAs for the task kernel; 0 = auto */
+    double barrier_timeout_s;         /* device spin limit of one barrier wait (default 2.0) */
+    double mailbox_idle_timeout_s;    /* task kernel exits after this long with no task (default 10.0) */
+    double host_timeout_s;            /* pk_shutdown deadline (default 10.0) */
+    int32_t mailbox_depth;            /* task ring slots, 1..1024 (default 64) */
+    int32_t debug_skip_arrival_cta;   /* fault injection: this CTA leaves at barrier ... (-1 = off) */
+    int32_t debug_skip_arrival_at;    /* ... number debug_skip_arrival_at (0-based) without arriving */
+    uint32_t flags;                   /* PK_FLAG_* */
+    int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
+    int32_t reserved[7];
+} pk_options;
+
+/* Fill opt with the defaults above. */
+void pk_options_default(pk_options *opt);
+
+/* Device layout for an nx x ny problem: pitch of a field row in floats,
+ * bytes of one field buffer ((ny+2) * pitch * 4), and pitch of a source
+ * row in floats (interior cell (j, i) of g at g[(j-1) * gpitch + i-1]).
+ * Any output pointer may be NULL.  PK_EINVAL on nx or ny <= 0 or overflow. */
+int pk_layout(int nx, int ny, int64_t *pitch_floats, int64_t *field_bytes,
+              int64_t *gpitch_floats);
+
+/* Create a solver for [P1] "The problem": nx x ny interior, u0 the packed
+ * (ny+2) x (nx+2) HOST field (ring = Dirichlet values, interior = initial
+ * guess), f the packed ny x nx HOST source or NULL for Laplace.  Inputs are
+ * copied; the caller keeps ownership.  Allocates both ping-pong buffers,
+ * g = fl32(h^2 f) with h^2 = (float)(1/(nx+1)^2), the barrier words and the
+ * mapped-pinned mailbox ([P3] "Device Communication"), and sizes the
+ * persistent grid from the occupancy API ([P4] "What it promises").  opt may
+ * be NULL.  Uses the current CUDA device and a stream of its own.
+ * Errors: PK_EINVAL (sizes, non-finite inputs), PK_ECUDA. */
+int pk_create(int nx, int ny, const float *u0, const float *f, const pk_options *opt,
+              pk_ctx **out);
+
+/* As pk_create, but borrows caller-owned DEVICE buffers u_a and u_b in the
+ * pitched layout (16-byte aligned, pitch a multiple of 4 floats and at least
+ * nx + 8), both already holding the same ring; the interior of u_a is the
+ * initial iterate.  f_dev is a packed ny x nx DEVICE source or NULL.
+ * stream is a cudaStream_t (NULL = a stream created by libpk).  The buffers
+ * must outlive the context.  Errors: PK_EINVAL, PK_ECUDA. */
+int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, const float *f_dev,
+                     void *stream, const pk_options *opt, pk_ctx **out);
+
+/* Persistent path ([P2] "What the barrier buys"; [P4] "grid_barrier"): ONE
+ * cooperative launch whose resident grid loops over the domain grid-stride,
+ * with a release/acquire generation-counter grid barrier between sweeps.
+ * Runs up to n sweeps.  With tol > 0 and check_every > 0 the residual
+ * r = fl32(t - 4C) of iterate k (t as in the update, before the 1/4) is
+ * reduced in the kernel when k % check_every == 0 (L2 norm in fp64, and
+ * max|r|); the run stops at the first checked k > 0 with
+ * ||r_k|| < tol * ||r_0|| and keeps U_k, else it stops at k = n.  The
+ * current buffer afterwards holds U_{sweeps_done}.  Blocks until done.
+ * info may be NULL.  Errors: PK_EINVAL (n < 0), PK_EBUSY (task kernel live),
+ * PK_ENORESIDENT, PK_ETIMEDOUT (a barrier wait expired), PK_ECUDA. */
+int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
+
+/* Comparison path ([P2] "When a launch is the better barrier"): the same
+ * sweep code, one kernel launch per sweep (the launch boundary is the
+ * barrier), same grid unless PK_FLAG_LAUNCH_PROBLEM_GRID; on a check sweep a
+ * reduction kernel runs and the host reads the residual back and decides.
+ * Same results, bit for bit, as pk_run_sweeps.  Errors as pk_run_sweeps. */
+int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
+
+/* Copy the current iterate to / from a packed (ny+2) x (nx+2) HOST array.
+ * pk_set_field writes both buffers (ring included) and makes buffer A
+ * current.  Errors: PK_EINVAL, PK_EBUSY (task kernel live), PK_ECUDA. */
+int pk_get_field(pk_ctx *ctx, float *host_out);
+int pk_set_field(pk_ctx *ctx, const float *host_in);
+
+/* Device pointer and pitch (floats) of buffer `which` (0 = A, 1 = B), and
+ * the index of the current one.  Any output may be NULL. */
+int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *current);
+
+/* The launch plan chosen at creation: sweep variant (PK_VARIANT_DIRECT or
+ * PK_VARIANT_STREAM), persistent sweep grid (CTAs), task kernel grid, and
+ * the cooperative capacity (resident CTAs per SM x SMs) of the sweep
+ * kernel.  Any output may be NULL. */
+int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max);
+
+/* Post a task to the mapped-pinned mailbox ([P1] "Base implementation",
+ * "Thread synchronization", "Atomics and memory ordering"; [P3] "Device
+ * Communication").  Starts the resident task kernel on first use (on a
+ * stream of its own, [P3] "Stream concurrency").  The descriptor goes to
+ * slot seq % depth, then seq is published with a release store; one leader
+ * thread polls it, broadcasts it through device memory, the grid runs it,
+ * and the completion sequence is written with a system-scope release only
+ * after every CTA has finished ([P1] "Reflections": no early ACK).
+ * *seq_out (may be NULL) receives the task's sequence number (1, 2, ...).
+ * Errors: PK_EINVAL (bad task), PK_EBUSY (ring full), PK_ESHUTDOWN,
+ * PK_ENORESIDENT, PK_ECUDA. */
+int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out);
+
+/* Non-blocking: 1 if task seq is done, 0 if pending, <0 on error (the task
+ * kernel exited: PK_ETIMEDOUT after the idle limit, PK_ESHUTDOWN after STOP,
+ * or the device status). */
+int pk_poll(pk_ctx *ctx, uint64_t seq);
+
+/* Busy-poll until task seq is done or timeout_s passes (PK_ETIMEDOUT). */
+int pk_wait(pk_ctx *ctx, uint64_t seq, double timeout_s);
+
+/* Post STOP, wait (bounded by host_timeout_s) for the task kernel to exit,
+ * and return its final status (PK_OK if it was not running). */
+int pk_shutdown(pk_ctx *ctx);
+
+/* Shut down the task kernel if live, free everything libpk allocated. */
+void pk_destroy(pk_ctx *ctx);
+
+/* Message for the last failure (never NULL). */
+const char *pk_last_error(const pk_ctx *ctx);
+
+/* ---- measurement entry points ------------------------------------------ */
+
+/* Launch floors ([P1] "Small problem sizes"): an empty <<<1, 32>>> kernel
+ * launched `iters` times with a stream synchronize after each (us per
+ * launch+sync, host clock) and `iters` times back to back with one
+ * synchronize (us per queued launch).  Outputs may be NULL. */
+int pk_bench_launch_floor(pk_ctx *ctx, int iters, double *us_sync_each, double *us_queued);
+
+/* Barrier cost: a cooperative kernel with `grid` CTAs of 256 threads that
+ * only runs n_barriers barriers; kind 0 = libpk's generation-counter
+ * barrier, kind 1 = cooperative_groups grid.sync().  *us_total is the
+ * kernel's device time (CUDA events), launch included.  grid 0 = the
+ * persistent sweep grid. */
+int pk_bench_barrier(pk_ctx *ctx, int kind, int grid, int64_t n_barriers, double *us_total);
+
+/* Barrier stress ([P2] "Failure modes that only appear at this scale"):
+ * `rounds` rounds in which every CTA writes `words` (1..32) stamped words on
+ * its own 128-byte line, crosses the barrier, and reads three other CTAs'
+ * lines, counting stale words and summing what it saw.  checksums (host,
+ * grid entries, may be NULL) and *stale (may be NULL) are filled. */
+int pk_barrier_stress(pk_ctx *ctx, int grid, int rounds, int words, uint64_t *checksums,
+                      int64_t *stale);
+
+/* Round-trip timing of a task list, host clock (ns per task into
+ * samples[0..n_tasks-1]).  mode 0: through the mailbox (submit, then poll
+ * until done); mode 1: the same task as a standalone kernel launch followed
+ * by cudaStreamSynchronize.  Task t is tasks[t % n_kinds]. */
+int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int64_t n_tasks,
+                   int64_t *samples_ns);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PK_H */

@@ -1,0 +1,383 @@
+// pk_device.cuh -- device primitives of libpk (sm_103a): memory-ordering
+// PTX, the generation-counter grid barrier, mbarrier / TMA bulk copies, the
+// 4-cell Jacobi update, and block reductions.
+//
+// Sources (page title -- section):
+//   "Grid-Wide Barriers and Persistent Work Queues" -- "The barrier is a
+//     counter and a generation", "Failure modes that only appear at this
+//     scale" (single-writer reset; relaxed atomics do not order data).
+//   "Persistent Kernels: Bridging GPU-CPU Execution" -- "Reflections"
+//     (spin relaxed, then acquire; release before signalling; a real
+//     barrier, not a fence, to publish to the other threads of a block).
+//   "@persistent" -- "grid_barrier" (two 32-bit words, zeroed once).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pk {
+
+// ---------------------------------------------------------------------------
+// Status codes the kernels report (same values as include/pk.h).
+constexpr int kOk = 0;
+constexpr int kETimedOut = -4;
+constexpr int kEShutdown = -6;
+constexpr int kEDevice = -7;
+
+// Site ids recorded with a device error.
+constexpr int kSiteBarrier = 1;
+constexpr int kSitePipeline = 2;
+constexpr int kSiteMailboxIdle = 3;
+constexpr int kSiteTaskBroadcast = 4;
+constexpr int kSiteTaskGather = 5;
+constexpr int kSiteSkipInjected = 6;
+
+// ---------------------------------------------------------------------------
+// Barrier state: each word on its own 128-byte line so that spinning on the
+// generation does not contend with arrivals ("Persistent Kernels", section
+// "Reflections": pad flags to separate cache lines).
+struct alignas(128) Line {
+    unsigned v;
+    unsigned pad[31];
+};
+
+struct BarrierState {
+    Line count;       // arrivals in the current generation
+    Line generation;  // bumped by the last arriver
+    Line abort_flag;  // set by any CTA that gave up; every spin checks it
+    Line error;       // first error code (atomicCAS from 0)
+    Line site;        // where it happened
+    Line bad_cta;     // which CTA recorded it
+};
+
+// ---------------------------------------------------------------------------
+// Memory-ordering primitives (hand-written PTX).
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned ld_relaxed_gpu(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned *p, unsigned v) {
+    asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+__device__ __forceinline__ unsigned atom_add_release_gpu(unsigned *p, unsigned v) {
+    unsigned old;
+    asm volatile("atom.release.gpu.global.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+// System scope, for the mapped-pinned mailbox in host memory.
+__device__ __forceinline__ unsigned long long ld_relaxed_sys_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_sys_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.sys.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_sys_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.sys.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_release_sys_s32(int *p, int v) {
+    asm volatile("st.release.sys.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_sys_s32(const int *p) {
+    int v;
+    asm volatile("ld.relaxed.sys.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Generic-proxy writes -> later async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Error recording: the first error wins; every spin sees abort_flag.
+__device__ __forceinline__ void record_error(BarrierState *b, int code, int site) {
+    if (atomicCAS(reinterpret_cast<int *>(&b->error.v), 0, code) == 0) {
+        atomicExch(&b->site.v, (unsigned)site);
+        atomicExch(&b->bad_cta.v, blockIdx.x);
+    }
+    __threadfence();
+    atomicExch(&b->abort_flag.v, 1u);
+}
+
+__device__ __forceinline__ bool aborted(const BarrierState *b) {
+    return ld_relaxed_gpu(&b->abort_flag.v) != 0u;
+}
+
+// ---------------------------------------------------------------------------
+// Grid barrier ("Grid-Wide Barriers ...", section "The barrier is a counter
+// and a generation").  Called by every thread of every CTA.  Thread 0 of
+// each CTA reads the generation, arrives on the counter with an acq_rel
+// atomic (release: this CTA's writes, ordered before it by __syncthreads,
+// are published; acquire: the last arriver sees every CTA's writes).  The
+// last arriver resets the counter and then bumps the generation with a
+// release store -- the single writer does both, in that order.  The others
+// spin with acquire loads on the generation, bounded by timeout_ns on the
+// global timer; on expiry they record kETimedOut and raise abort_flag.
+// Returns false when the grid is aborting; the caller must then return.
+//
+// skip: fault injection -- this CTA leaves without arriving (host-driven
+// test of the timeout; it never faults the GPU).
+struct BarrierCtl {
+    BarrierState *state;
+    unsigned nblocks;
+    uint64_t timeout_ns;
+    int skip_cta;      // -1 = off
+    int skip_at;       // barrier index at which skip_cta leaves
+    int index;         // barriers passed so far by this CTA
+};
+
+__device__ __forceinline__ bool grid_barrier(BarrierCtl &ctl) {
+    __shared__ int s_ok;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        BarrierState *b = ctl.state;
+        if ((int)blockIdx.x == ctl.skip_cta && ctl.index == ctl.skip_at) {
+            ok = 0;  // leave without arriving; the others must time out
+        } else if (aborted(b)) {
+            ok = 0;
+        } else {
+            const unsigned gen = ld_relaxed_gpu(&b->generation.v);
+            const unsigned old = atom_add_acq_rel_gpu(&b->count.v, 1u);
+            if (old == ctl.nblocks - 1u) {
+                st_relaxed_gpu(&b->count.v, 0u);
+                st_release_gpu(&b->generation.v, gen + 1u);
+            } else {
+                const uint64_t t0 = globaltimer_ns();
+                unsigned spins = 0;
+                while (ld_acquire_gpu(&b->generation.v) == gen) {
+                    if ((++spins & 255u) == 0u) {
+                        if (aborted(b)) {
+                            ok = 0;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > ctl.timeout_ns) {
+                            record_error(b, kETimedOut, kSiteBarrier);
+                            ok = 0;
+                            break;
+                        }
+                    }
+                }
+            }
+        }
+        s_ok = ok;
+    }
+    __syncthreads();
+    ++ctl.index;
+    return s_ok != 0;
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier + TMA bulk copy (cp.async.bulk) helpers, CTA-local.
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0u;
+}
+// Bounded wait: false after timeout_ns, or as soon as the grid is aborting
+// (the caller records the error).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity,
+                                                  uint64_t timeout_ns, const BarrierState *gb) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++spins & 63u) == 0u) {
+            if (aborted(gb)) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) return false;
+        }
+    }
+}
+// 1-D bulk copy global -> this CTA's shared memory, completing on bar.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void tma_load_1d(void *dst, const void *src, unsigned bytes,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// The update ("Persistent Kernels ...", section "The problem (another PDE
+// solver)"): t = (W + E) + (S + N) [- g]; u' = 0.25 * t; residual
+// r = t - 4C.  Every operation is an explicit round-to-nearest intrinsic so
+// no FMA can be formed.
+__device__ __forceinline__ float cell_t(float w, float e, float s, float n) {
+    return __fadd_rn(__fadd_rn(w, e), __fadd_rn(s, n));
+}
+
+struct Quad {
+    float t0, t1, t2, t3;
+};
+
+// Four consecutive cells: row C = (c.x..c.w), left neighbour of c.x is w,
+// right neighbour of c.w is e; S and N rows above and below.
+template <bool POISSON>
+__device__ __forceinline__ Quad quad_t(float w, float4 c, float e, float4 s, float4 n, float4 g) {
+    Quad q;
+    q.t0 = cell_t(w, c.y, s.x, n.x);
+    q.t1 = cell_t(c.x, c.z, s.y, n.y);
+    q.t2 = cell_t(c.y, c.w, s.z, n.z);
+    q.t3 = cell_t(c.z, e, s.w, n.w);
+    if (POISSON) {
+        q.t0 = __fsub_rn(q.t0, g.x);
+        q.t1 = __fsub_rn(q.t1, g.y);
+        q.t2 = __fsub_rn(q.t2, g.z);
+        q.t3 = __fsub_rn(q.t3, g.w);
+    }
+    return q;
+}
+
+__device__ __forceinline__ float4 quad_update(const Quad &q) {
+    return make_float4(__fmul_rn(0.25f, q.t0), __fmul_rn(0.25f, q.t1), __fmul_rn(0.25f, q.t2),
+                       __fmul_rn(0.25f, q.t3));
+}
+
+// Residual accumulation over the first `valid` cells of the quad.
+__device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, double &s2,
+                                              float &rmax) {
+    const float tv[4] = {q.t0, q.t1, q.t2, q.t3};
+    const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < valid) {
+            const float r = __fsub_rn(tv[k], __fmul_rn(4.0f, cv[k]));
+            const double rd = (double)r;
+            s2 = __dadd_rn(s2, __dmul_rn(rd, rd));
+            rmax = fmaxf(rmax, fabsf(r));
+        }
+    }
+}
+
+// Store the first `valid` (1..4) cells of v at p (16-byte aligned).
+__device__ __forceinline__ void store_quad(float *p, float4 v, int valid) {
+    if (valid >= 4) {
+        *reinterpret_cast<float4 *>(p) = v;
+    } else {
+        if (valid > 0) p[0] = v.x;
+        if (valid > 1) p[1] = v.y;
+        if (valid > 2) p[2] = v.z;
+    }
+}
+
+__device__ __forceinline__ float4 ld4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+
+// ---------------------------------------------------------------------------
+// Residual partials: one per CTA, double-buffered by check parity.
+struct Partial {
+    double s2;
+    float rmax;
+    float pad;
+};
+
+// Deterministic block reduction of (s2, rmax); result valid in thread 0.
+// The tree is fixed for a given blockDim, so every CTA that reduces the same
+// inputs gets the same bits.
+__device__ __forceinline__ void block_reduce(double &s2, float &rmax) {
+    __shared__ double sh_s[32];
+    __shared__ float sh_m[32];
+    const unsigned lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        s2 = __dadd_rn(s2, __shfl_down_sync(0xffffffffu, s2, off));
+        rmax = fmaxf(rmax, __shfl_down_sync(0xffffffffu, rmax, off));
+    }
+    __syncthreads();  // sh_* may still be read by a previous call
+    if (lane == 0) {
+        sh_s[warp] = s2;
+        sh_m[warp] = rmax;
+    }
+    __syncthreads();
+    const unsigned nwarps = (blockDim.x + 31u) >> 5;
+    if (warp == 0) {
+        s2 = lane < nwarps ? sh_s[lane] : 0.0;
+        rmax = lane < nwarps ? sh_m[lane] : 0.0f;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            s2 = __dadd_rn(s2, __shfl_down_sync(0xffffffffu, s2, off));
+            rmax = fmaxf(rmax, __shfl_down_sync(0xffffffffu, rmax, off));
+        }
+    }
+}
+
+// Every CTA reduces all `count` partials in the same fixed order; the result
+// is broadcast to all threads of the CTA.
+__device__ __forceinline__ void reduce_partials(const Partial *parts, int count, double &s2_out,
+                                                float &rmax_out) {
+    __shared__ double s_s2;
+    __shared__ float s_rmax;
+    double s2 = 0.0;
+    float rmax = 0.0f;
+    for (int q = threadIdx.x; q < count; q += blockDim.x) {
+        // Plain loads: ordered after the barrier's acquire + __syncthreads.
+        s2 = __dadd_rn(s2, parts[q].s2);
+        rmax = fmaxf(rmax, parts[q].rmax);
+    }
+    block_reduce(s2, rmax);
+    if (threadIdx.x == 0) {
+        s_s2 = s2;
+        s_rmax = rmax;
+    }
+    __syncthreads();
+    s2_out = s_s2;
+    rmax_out = s_rmax;
+}
+
+}  // namespace pk

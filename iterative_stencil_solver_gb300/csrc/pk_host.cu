@@ -1,0 +1,916 @@
+// pk_host.cu -- the C ABI of libpk (include/pk.h): context, buffers, launch
+// sizing, the persistent and per-launch drivers, the mapped-pinned mailbox
+// and the measurement entry points.
+//
+// Sources (page title -- section):
+//   "Grid-Wide Barriers and Persistent Work Queues" -- "The residency
+//     requirement" (cooperative launch; a launch error is better than a
+//     hang; size the grid to the machine), "When a launch is the better
+//     barrier" (the per-launch path).
+//   "@persistent" -- "What it promises" (grid = CTAs per SM from the
+//     occupancy API x SMs, queried with the kernel's threads and dynamic
+//     shared bytes), "grid_barrier" (state zeroed once before the launch).
+//   "CUDA persist kernel" -- "Device Communication" (cudaHostAlloc mapped
+//     memory passed straight to the kernel), "Stream concurrency" (the
+//     resident kernel gets a stream of its own).
+//   "Persistent Kernels: Bridging GPU-CPU Execution" -- "Tuning sleep
+//     duration", "Reflections" (busy-poll rather than sleep; flags on
+//     separate cache lines; acquire/release, no early ACK).
+#include <atomic>
+#include <chrono>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <thread>
+
+#include "pk.h"
+#include "pk_internal.h"
+
+using namespace pk;
+
+namespace {
+
+thread_local std::string g_create_error = "no error";
+
+struct Scratch {
+    BarrierState bar_sweep;
+    BarrierState bar_task;
+    BarrierState bar_task_inner;
+    BarrierState bar_bench;
+    DeviceInfo info;
+    alignas(64) ResidualOut res;
+    alignas(64) TaskSlot desc;
+    alignas(128) unsigned long long stale;
+};
+
+inline uint64_t now_ns() {
+    return (uint64_t)std::chrono::duration_cast<std::chrono::nanoseconds>(
+               std::chrono::steady_clock::now().time_since_epoch())
+        .count();
+}
+
+inline long long round_up(long long v, long long m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+struct pk_ctx {
+    int nx = 0, ny = 0;
+    long long pitch = 0, gpitch = 0;
+    float h2 = 0.f;
+    bool poisson = false;
+    float *u[2] = {nullptr, nullptr};
+    bool own_u = false;
+    float *g = nullptr;
+    int cur = 0;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;
+    cudaStream_t task_stream = nullptr;
+    cudaEvent_t ev0 = nullptr, ev1 = nullptr, ev_sync = nullptr;
+    int device = 0, sms = 0;
+    long long l2_bytes = 0;
+    pk_options opt{};
+    int variant = kVariantDirect;
+    int grid = 1;        // persistent sweep grid
+    int coop_max = 1;    // occupancy x SMs for the sweep kernel
+    int part_cap = 0;    // partial slots per parity
+    Scratch *scratch = nullptr;
+    Partial *partials = nullptr;
+    unsigned *stress_lines = nullptr;
+    int stress_cap = 0;
+    unsigned long long *stress_out = nullptr;
+    // pinned host mirrors
+    DeviceInfo *h_info = nullptr;
+    ResidualOut *h_res = nullptr;
+    BarrierState *h_bar = nullptr;
+    // mailbox
+    Mailbox *mbox = nullptr;
+    Mailbox *mbox_dev = nullptr;
+    size_t mbox_bytes = 0;
+    bool task_live = false;
+    int task_grid = 1;
+    unsigned long long next_seq = 1;
+    int task_status = PK_OK;
+    int run_id = 0;
+    bool dirty_sweep = false;
+    std::string err = "no error";
+};
+
+namespace {
+
+int fail(pk_ctx *ctx, int code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    if (ctx)
+        ctx->err = buf;
+    else
+        g_create_error = buf;
+    return code;
+}
+
+int cuda_fail(pk_ctx *ctx, cudaError_t e, const char *what) {
+    (void)cudaGetLastError();  // clear a non-sticky error
+    const int code = (e == cudaErrorCooperativeLaunchTooLarge) ? PK_ENORESIDENT : PK_ECUDA;
+    return fail(ctx, code, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+#define PK_TRY(ctx, call)                                        \
+    do {                                                         \
+        cudaError_t e_ = (call);                                 \
+        if (e_ != cudaSuccess) return cuda_fail((ctx), e_, #call); \
+    } while (0)
+
+bool finite_array(const float *a, size_t n) {
+    for (size_t q = 0; q < n; ++q)
+        if (!std::isfinite(a[q])) return false;
+    return true;
+}
+
+int check_sizes(int nx, int ny) {
+    if (nx <= 0 || ny <= 0) return PK_EINVAL;
+    if (nx > (1 << 30) || ny > (1 << 30)) return PK_EINVAL;
+    const long long pitch = round_up((long long)nx + 8, 32);
+    const long double bytes = (long double)(ny + 2) * (long double)pitch * 4.0L;
+    if (bytes > (long double)(1LL << 46)) return PK_EINVAL;
+    return PK_OK;
+}
+
+void fill_default(pk_options *o) {
+    std::memset(o, 0, sizeof(*o));
+    o->struct_size = sizeof(pk_options);
+    o->variant = PK_VARIANT_AUTO;
+    o->barrier_timeout_s = 2.0;
+    o->mailbox_idle_timeout_s = 10.0;
+    o->host_timeout_s = 10.0;
+    o->mailbox_depth = 64;
+    o->debug_skip_arrival_cta = -1;
+    o->debug_skip_arrival_at = 0;
+}
+
+int read_options(pk_ctx *ctx, const pk_options *opt) {
+    fill_default(&ctx->opt);
+    if (!opt) return PK_OK;
+    if (opt->struct_size != sizeof(pk_options))
+        return fail(ctx, PK_EINVAL, "pk_options.struct_size is %u, expected %zu", opt->struct_size,
+                    sizeof(pk_options));
+    ctx->opt = *opt;
+    pk_options &o = ctx->opt;
+    if (o.variant < PK_VARIANT_AUTO || o.variant > PK_VARIANT_STREAM)
+        return fail(ctx, PK_EINVAL, "unknown variant %d", o.variant);
+    if (o.grid_override < 0 || o.task_grid < 0 || o.ctas_per_sm < 0)
+        return fail(ctx, PK_EINVAL, "negative grid option");
+    if (!(o.barrier_timeout_s > 0.0) || !(o.mailbox_idle_timeout_s > 0.0) ||
+        !(o.host_timeout_s > 0.0))
+        return fail(ctx, PK_EINVAL, "timeouts must be positive");
+    if (o.barrier_timeout_s > 3600.0 || o.mailbox_idle_timeout_s > 86400.0)
+        return fail(ctx, PK_EINVAL, "timeout too large");
+    if (o.mailbox_depth < 1 || o.mailbox_depth > 1024)
+        return fail(ctx, PK_EINVAL, "mailbox_depth must be in 1..1024");
+    return PK_OK;
+}
+
+unsigned long long ns_of(double s) { return (unsigned long long)(s * 1e9); }
+
+// Occupancy x SMs for a kernel ("@persistent", "What it promises").
+int coop_capacity(pk_ctx *ctx, const void *fn, int threads, size_t smem, int *per_sm) {
+    int nb = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, fn, threads, smem);
+    if (e != cudaSuccess) {
+        cuda_fail(ctx, e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+        return -1;
+    }
+    if (ctx->opt.ctas_per_sm > 0 && nb > ctx->opt.ctas_per_sm) nb = ctx->opt.ctas_per_sm;
+    if (per_sm) *per_sm = nb;
+    return nb * ctx->sms;
+}
+
+long long direct_units(const pk_ctx *ctx) { return (long long)ctx->ny * ((ctx->nx + 3) / 4); }
+
+long long stream_rows(const pk_ctx *ctx) {
+    return (long long)((ctx->nx + kTW - 1) / kTW) * ctx->ny;
+}
+
+int ensure_partials(pk_ctx *ctx, int grid) {
+    if (grid <= ctx->part_cap) return PK_OK;
+    if (ctx->partials) {
+        PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+        cudaFree(ctx->partials);
+        ctx->partials = nullptr;
+        ctx->part_cap = 0;
+    }
+    PK_TRY(ctx, cudaMalloc(&ctx->partials, sizeof(Partial) * 2 * (size_t)grid));
+    ctx->part_cap = grid;
+    return PK_OK;
+}
+
+// Variant and grid for the sweeps; also the task kernel's grid.
+int plan(pk_ctx *ctx) {
+    const long long field_bytes = (long long)(ctx->ny + 2) * ctx->pitch * 4;
+    long long resident = 2 * field_bytes + (ctx->poisson ? (long long)ctx->ny * ctx->gpitch * 4 : 0);
+    int v = ctx->opt.variant;
+    if (v == PK_VARIANT_AUTO) v = resident > ctx->l2_bytes / 2 ? kVariantStream : kVariantDirect;
+    if (v == kVariantDirect && direct_units(ctx) >= (1LL << 31))
+        return fail(ctx, PK_EINVAL, "grid too large for the DIRECT variant");
+    ctx->variant = v;
+    int per_sm = 0;
+    const int cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson), block_threads(v),
+                                  dyn_smem(v, ctx->poisson), &per_sm);
+    if (cap < 0) return PK_ECUDA;
+    if (cap == 0) return fail(ctx, PK_ENORESIDENT, "sweep kernel does not fit on an SM");
+    ctx->coop_max = cap;
+    long long need = v == kVariantStream ? stream_rows(ctx)
+                                         : (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+    if (need < 1) need = 1;
+    ctx->grid = (int)(need < cap ? need : cap);
+    if (ctx->opt.grid_override > 0) ctx->grid = ctx->opt.grid_override;
+    // task kernel (DIRECT sweep + axpy, 256 threads)
+    int tper = 0;
+    const int tcap = coop_capacity(ctx, kernel_task(ctx->poisson), kDirectThreads, 0, &tper);
+    if (tcap <= 0) return tcap < 0 ? PK_ECUDA : fail(ctx, PK_ENORESIDENT, "task kernel does not fit");
+    long long tneed = (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+    if (tneed < 1) tneed = 1;
+    ctx->task_grid = (int)(tneed < tcap ? tneed : tcap);
+    if (ctx->opt.task_grid > 0) ctx->task_grid = ctx->opt.task_grid;
+    int want = ctx->grid > cap ? ctx->grid : cap;
+    return ensure_partials(ctx, want);
+}
+
+SweepParams base_params(pk_ctx *ctx) {
+    SweepParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.u[0] = ctx->u[0];
+    p.u[1] = ctx->u[1];
+    p.g = ctx->g;
+    p.nx = ctx->nx;
+    p.ny = ctx->ny;
+    p.pitch = ctx->pitch;
+    p.gpitch = ctx->gpitch;
+    p.cur = ctx->cur;
+    p.bar = &ctx->scratch->bar_sweep;
+    p.partials = ctx->partials;
+    p.max_grid = ctx->part_cap;
+    p.info = &ctx->scratch->info;
+    p.timeout_ns = ns_of(ctx->opt.barrier_timeout_s);
+    p.skip_cta = ctx->opt.debug_skip_arrival_cta;
+    p.skip_at = ctx->opt.debug_skip_arrival_at;
+    p.alt_dir = (ctx->opt.flags & PK_FLAG_ALTERNATE_DIRECTION) ? 1 : 0;
+    p.run_id = ++ctx->run_id;
+    return p;
+}
+
+// Reads the barrier's error words after a kernel; returns PK_OK or the code.
+int bar_status(pk_ctx *ctx, BarrierState *dev_bar, const char *what) {
+    PK_TRY(ctx, cudaMemcpyAsync(ctx->h_bar, dev_bar, sizeof(BarrierState), cudaMemcpyDeviceToHost,
+                                ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    const int code = (int)ctx->h_bar->error.v;
+    if (code != 0) {
+        PK_TRY(ctx, cudaMemsetAsync(dev_bar, 0, sizeof(BarrierState), ctx->stream));
+        PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+        return fail(ctx, code, "%s: device reported %d at site %u (CTA %u)", what, code,
+                    ctx->h_bar->site.v, ctx->h_bar->bad_cta.v);
+    }
+    return PK_OK;
+}
+
+int write_field(pk_ctx *ctx, const float *host) {
+    const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
+    PK_TRY(ctx, cudaMemcpy2DAsync(ctx->u[0] + 3, sizeof(float) * (size_t)ctx->pitch, host, row, row,
+                                  (size_t)(ctx->ny + 2), cudaMemcpyHostToDevice, ctx->stream));
+    PK_TRY(ctx, cudaMemcpyAsync(ctx->u[1], ctx->u[0],
+                                sizeof(float) * (size_t)ctx->pitch * (size_t)(ctx->ny + 2),
+                                cudaMemcpyDeviceToDevice, ctx->stream));
+    ctx->cur = 0;
+    return PK_OK;
+}
+
+int common_setup(pk_ctx *ctx) {
+    PK_TRY(ctx, cudaGetDevice(&ctx->device));
+    PK_TRY(ctx, cudaDeviceGetAttribute(&ctx->sms, cudaDevAttrMultiProcessorCount, ctx->device));
+    int coop = 0, l2 = 0;
+    PK_TRY(ctx, cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx->device));
+    if (!coop) return fail(ctx, PK_ENORESIDENT, "device does not support cooperative launch");
+    PK_TRY(ctx, cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, ctx->device));
+    ctx->l2_bytes = l2;
+    PK_TRY(ctx, prepare_kernels());
+    if (!ctx->stream) {
+        PK_TRY(ctx, cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking));
+        ctx->own_stream = true;
+    }
+    PK_TRY(ctx, cudaStreamCreateWithFlags(&ctx->task_stream, cudaStreamNonBlocking));
+    PK_TRY(ctx, cudaEventCreate(&ctx->ev0));
+    PK_TRY(ctx, cudaEventCreate(&ctx->ev1));
+    PK_TRY(ctx, cudaEventCreateWithFlags(&ctx->ev_sync, cudaEventDisableTiming));
+    PK_TRY(ctx, cudaMalloc(&ctx->scratch, sizeof(Scratch)));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->scratch, 0, sizeof(Scratch), ctx->stream));
+    PK_TRY(ctx, cudaHostAlloc(&ctx->h_info, sizeof(DeviceInfo), cudaHostAllocDefault));
+    PK_TRY(ctx, cudaHostAlloc(&ctx->h_res, sizeof(ResidualOut), cudaHostAllocDefault));
+    PK_TRY(ctx, cudaHostAlloc(&ctx->h_bar, sizeof(BarrierState), cudaHostAllocDefault));
+    // Mailbox in mapped pinned host memory ("Device Communication").
+    ctx->mbox_bytes = sizeof(Mailbox) + sizeof(TaskSlot) * (size_t)(ctx->opt.mailbox_depth - 1);
+    PK_TRY(ctx, cudaHostAlloc(&ctx->mbox, ctx->mbox_bytes, cudaHostAllocMapped));
+    std::memset(ctx->mbox, 0, ctx->mbox_bytes);
+    PK_TRY(ctx, cudaHostGetDevicePointer((void **)&ctx->mbox_dev, ctx->mbox, 0));
+    return plan(ctx);
+}
+
+void release(pk_ctx *ctx) {
+    if (!ctx) return;
+    if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+    if (ctx->task_stream) cudaStreamSynchronize(ctx->task_stream);
+    if (ctx->own_u) {
+        cudaFree(ctx->u[0]);
+        cudaFree(ctx->u[1]);
+    }
+    cudaFree(ctx->g);
+    cudaFree(ctx->scratch);
+    cudaFree(ctx->partials);
+    cudaFree(ctx->stress_lines);
+    cudaFree(ctx->stress_out);
+    if (ctx->h_info) cudaFreeHost(ctx->h_info);
+    if (ctx->h_res) cudaFreeHost(ctx->h_res);
+    if (ctx->h_bar) cudaFreeHost(ctx->h_bar);
+    if (ctx->mbox) cudaFreeHost(ctx->mbox);
+    if (ctx->ev0) cudaEventDestroy(ctx->ev0);
+    if (ctx->ev1) cudaEventDestroy(ctx->ev1);
+    if (ctx->ev_sync) cudaEventDestroy(ctx->ev_sync);
+    if (ctx->task_stream) cudaStreamDestroy(ctx->task_stream);
+    if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
+    delete ctx;
+}
+
+double elapsed_us(pk_ctx *ctx) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, ctx->ev0, ctx->ev1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1.0;
+    }
+    return (double)ms * 1000.0;
+}
+
+void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
+               float rmax, int n_checks, int status, int grid) {
+    if (!info) return;
+    info->sweeps_done = sweeps;
+    info->res0 = res0;
+    info->res_last = res_last;
+    info->res_max_last = rmax;
+    info->status = status;
+    info->n_checks = n_checks;
+    info->current = ctx->cur;
+    info->grid = grid;
+    info->variant = ctx->variant;
+    info->device_us = elapsed_us(ctx);
+}
+
+int task_finish(pk_ctx *ctx) {
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->task_stream));
+    ctx->task_live = false;
+    PK_TRY(ctx, cudaMemcpy(ctx->h_info, &ctx->scratch->info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost));
+    ctx->cur = ctx->h_info->cur;
+    const long long st = (long long)__atomic_load_n(&ctx->mbox->status.v, __ATOMIC_ACQUIRE);
+    PK_TRY(ctx, cudaMemcpy(ctx->h_bar, &ctx->scratch->bar_task, sizeof(BarrierState), cudaMemcpyDeviceToHost));
+    int code = (int)ctx->h_bar->error.v;
+    if (code == 0) {
+        PK_TRY(ctx, cudaMemcpy(ctx->h_bar, &ctx->scratch->bar_task_inner, sizeof(BarrierState),
+                               cudaMemcpyDeviceToHost));
+        code = (int)ctx->h_bar->error.v;
+    }
+    if (code != 0) {
+        ctx->task_status = code;
+        return fail(ctx, code, "task kernel: device reported %d at site %u (CTA %u)", code,
+                    ctx->h_bar->site.v, ctx->h_bar->bad_cta.v);
+    }
+    ctx->task_status = (st == PK_ESHUTDOWN) ? PK_ESHUTDOWN : (int)st;
+    return PK_OK;
+}
+
+}  // namespace
+
+// ===========================================================================
+// Public ABI.
+extern "C" {
+
+void pk_options_default(pk_options *opt) {
+    if (opt) fill_default(opt);
+}
+
+int pk_layout(int nx, int ny, int64_t *pitch_floats, int64_t *field_bytes, int64_t *gpitch_floats) {
+    if (check_sizes(nx, ny) != PK_OK) return PK_EINVAL;
+    const long long pitch = round_up((long long)nx + 8, 32);
+    if (pitch_floats) *pitch_floats = pitch;
+    if (field_bytes) *field_bytes = (long long)(ny + 2) * pitch * 4;
+    if (gpitch_floats) *gpitch_floats = round_up(nx, 32);
+    return PK_OK;
+}
+
+int pk_create(int nx, int ny, const float *u0, const float *f, const pk_options *opt, pk_ctx **out) {
+    if (!out) return fail(nullptr, PK_EINVAL, "pk_create: out is NULL");
+    *out = nullptr;
+    if (check_sizes(nx, ny) != PK_OK)
+        return fail(nullptr, PK_EINVAL, "pk_create: bad sizes nx=%d ny=%d", nx, ny);
+    if (!u0) return fail(nullptr, PK_EINVAL, "pk_create: u0 is NULL");
+    const size_t cells = (size_t)(nx + 2) * (size_t)(ny + 2);
+    if (!finite_array(u0, cells)) return fail(nullptr, PK_EINVAL, "pk_create: u0 is not finite");
+    if (f && !finite_array(f, (size_t)nx * (size_t)ny))
+        return fail(nullptr, PK_EINVAL, "pk_create: f is not finite");
+    pk_ctx *ctx = new (std::nothrow) pk_ctx();
+    if (!ctx) return fail(nullptr, PK_ECUDA, "pk_create: out of host memory");
+    int rc = read_options(ctx, opt);
+    if (rc != PK_OK) {
+        g_create_error = ctx->err;
+        release(ctx);
+        return rc;
+    }
+    ctx->nx = nx;
+    ctx->ny = ny;
+    ctx->pitch = round_up((long long)nx + 8, 32);
+    ctx->gpitch = round_up(nx, 32);
+    ctx->h2 = (float)(1.0 / (((double)nx + 1.0) * ((double)nx + 1.0)));
+    ctx->poisson = f != nullptr;
+    auto bail = [&](int code) {
+        g_create_error = ctx->err;
+        release(ctx);
+        return code;
+    };
+    cudaError_t e;
+    const size_t fbytes = sizeof(float) * (size_t)ctx->pitch * (size_t)(ny + 2);
+    if ((e = cudaMalloc(&ctx->u[0], fbytes)) != cudaSuccess ||
+        (e = cudaMalloc(&ctx->u[1], fbytes)) != cudaSuccess)
+        return bail(cuda_fail(ctx, e, "cudaMalloc(field)"));
+    ctx->own_u = true;
+    if ((rc = common_setup(ctx)) != PK_OK) return bail(rc);
+    if ((e = cudaMemsetAsync(ctx->u[0], 0, fbytes, ctx->stream)) != cudaSuccess)
+        return bail(cuda_fail(ctx, e, "cudaMemsetAsync(field)"));
+    if ((rc = write_field(ctx, u0)) != PK_OK) return bail(rc);
+    if (f) {
+        float *fdev = nullptr;
+        const size_t gbytes = sizeof(float) * (size_t)ctx->gpitch * (size_t)ny;
+        if ((e = cudaMalloc(&ctx->g, gbytes)) != cudaSuccess)
+            return bail(cuda_fail(ctx, e, "cudaMalloc(g)"));
+        if ((e = cudaMalloc(&fdev, sizeof(float) * (size_t)nx * (size_t)ny)) != cudaSuccess)
+            return bail(cuda_fail(ctx, e, "cudaMalloc(f)"));
+        e = cudaMemcpyAsync(fdev, f, sizeof(float) * (size_t)nx * (size_t)ny, cudaMemcpyHostToDevice,
+                            ctx->stream);
+        if (e == cudaSuccess) e = launch_scale_source(fdev, ctx->g, nx, ny, ctx->gpitch, ctx->h2, ctx->stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+        cudaFree(fdev);
+        if (e != cudaSuccess) return bail(cuda_fail(ctx, e, "scale source"));
+    }
+    if ((e = cudaStreamSynchronize(ctx->stream)) != cudaSuccess)
+        return bail(cuda_fail(ctx, e, "cudaStreamSynchronize"));
+    *out = ctx;
+    return PK_OK;
+}
+
+int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, const float *f_dev,
+                     void *stream, const pk_options *opt, pk_ctx **out) {
+    if (!out) return fail(nullptr, PK_EINVAL, "pk_create_device: out is NULL");
+    *out = nullptr;
+    if (check_sizes(nx, ny) != PK_OK)
+        return fail(nullptr, PK_EINVAL, "pk_create_device: bad sizes nx=%d ny=%d", nx, ny);
+    if (!u_a || !u_b || u_a == u_b)
+        return fail(nullptr, PK_EINVAL, "pk_create_device: need two distinct buffers");
+    if ((((uintptr_t)u_a) | ((uintptr_t)u_b)) & 15u)
+        return fail(nullptr, PK_EINVAL, "pk_create_device: buffers must be 16-byte aligned");
+    if (pitch < (int64_t)nx + 8 || (pitch & 3))
+        return fail(nullptr, PK_EINVAL, "pk_create_device: pitch %lld must be >= nx+8 and a multiple of 4",
+                    (long long)pitch);
+    pk_ctx *ctx = new (std::nothrow) pk_ctx();
+    if (!ctx) return fail(nullptr, PK_ECUDA, "pk_create_device: out of host memory");
+    int rc = read_options(ctx, opt);
+    auto bail = [&](int code) {
+        g_create_error = ctx->err;
+        release(ctx);
+        return code;
+    };
+    if (rc != PK_OK) return bail(rc);
+    ctx->nx = nx;
+    ctx->ny = ny;
+    ctx->pitch = pitch;
+    ctx->gpitch = round_up(nx, 32);
+    ctx->h2 = (float)(1.0 / (((double)nx + 1.0) * ((double)nx + 1.0)));
+    ctx->poisson = f_dev != nullptr;
+    ctx->u[0] = u_a;
+    ctx->u[1] = u_b;
+    ctx->own_u = false;
+    ctx->stream = (cudaStream_t)stream;
+    if ((rc = common_setup(ctx)) != PK_OK) return bail(rc);
+    cudaError_t e;
+    if (f_dev) {
+        const size_t gbytes = sizeof(float) * (size_t)ctx->gpitch * (size_t)ny;
+        if ((e = cudaMalloc(&ctx->g, gbytes)) != cudaSuccess)
+            return bail(cuda_fail(ctx, e, "cudaMalloc(g)"));
+        if ((e = launch_scale_source(f_dev, ctx->g, nx, ny, ctx->gpitch, ctx->h2, ctx->stream)) !=
+            cudaSuccess)
+            return bail(cuda_fail(ctx, e, "scale source"));
+    }
+    if ((e = cudaStreamSynchronize(ctx->stream)) != cudaSuccess)
+        return bail(cuda_fail(ctx, e, "cudaStreamSynchronize"));
+    *out = ctx;
+    return PK_OK;
+}
+
+int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
+    if (!ctx) return PK_EINVAL;
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_sweeps: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_sweeps: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_sweeps: the task kernel is live");
+    SweepParams p = base_params(ctx);
+    p.n = n;
+    p.tol = tol;
+    p.check_every = check_every;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, ctx->grid, p, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
+                                ctx->stream));
+    int rc = bar_status(ctx, p.bar, "pk_run_sweeps");
+    if (rc != PK_OK) {
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, ctx->grid);
+        return rc;
+    }
+    if (ctx->h_info->run_id != p.run_id)
+        return fail(ctx, PK_EDEVICE, "pk_run_sweeps: kernel did not report its result");
+    ctx->cur = ctx->h_info->cur;
+    fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, ctx->grid);
+    return PK_OK;
+}
+
+int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
+    if (!ctx) return PK_EINVAL;
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_sweeps_launch: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_sweeps_launch: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_sweeps_launch: the task kernel is live");
+    int grid = ctx->grid;
+    if (ctx->opt.flags & PK_FLAG_LAUNCH_PROBLEM_GRID) {
+        long long need = ctx->variant == kVariantStream ? (stream_rows(ctx) + 31) / 32
+                                                        : (direct_units(ctx) + kDirectThreads - 1) /
+                                                              kDirectThreads;
+        if (need < 1) need = 1;
+        if (need > (1LL << 30)) need = 1LL << 30;
+        grid = (int)need;
+        int rc = ensure_partials(ctx, grid);
+        if (rc != PK_OK) return rc;
+    }
+    SweepParams p = base_params(ctx);
+    const bool checks = tol > 0.f && check_every > 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    int cur = ctx->cur;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    for (;;) {
+        const bool check = checks && (k % check_every) == 0;
+        if (k == n && !check) break;
+        p.cur = cur;
+        p.pass_check = check ? 1 : 0;
+        p.pass_store = k < n ? 1 : 0;
+        p.pass_parity = n_checks & 1;
+        p.pass_k = k;
+        cudaError_t e = launch_once(ctx->variant, ctx->poisson, grid, p, ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "sweep launch");
+        if (check) {
+            e = launch_finalize(ctx->variant, grid, p, &ctx->scratch->res, ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "residual launch");
+            PK_TRY(ctx, cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
+                                        cudaMemcpyDeviceToHost, ctx->stream));
+            PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+            const double res = ctx->h_res->res;
+            ++n_checks;
+            res_last = res;
+            rmax_last = ctx->h_res->rmax;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)tol * res0)
+                break;
+        }
+        if (k == n) break;
+        cur ^= 1;
+        ++k;
+    }
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    ctx->cur = cur;
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, grid);
+    return PK_OK;
+}
+
+int pk_get_field(pk_ctx *ctx, float *host_out) {
+    if (!ctx || !host_out) return ctx ? fail(ctx, PK_EINVAL, "pk_get_field: NULL output") : PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_get_field: the task kernel is live");
+    const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
+    PK_TRY(ctx, cudaMemcpy2DAsync(host_out, row, ctx->u[ctx->cur] + 3, sizeof(float) * (size_t)ctx->pitch,
+                                  row, (size_t)(ctx->ny + 2), cudaMemcpyDeviceToHost, ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    return PK_OK;
+}
+
+int pk_set_field(pk_ctx *ctx, const float *host_in) {
+    if (!ctx || !host_in) return ctx ? fail(ctx, PK_EINVAL, "pk_set_field: NULL input") : PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_set_field: the task kernel is live");
+    int rc = write_field(ctx, host_in);
+    if (rc != PK_OK) return rc;
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    return PK_OK;
+}
+
+int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *current) {
+    if (!ctx || which < 0 || which > 1) return PK_EINVAL;
+    if (ptr) *ptr = ctx->u[which];
+    if (pitch) *pitch = ctx->pitch;
+    if (current) *current = ctx->cur;
+    return PK_OK;
+}
+
+int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max) {
+    if (!ctx) return PK_EINVAL;
+    if (variant) *variant = ctx->variant;
+    if (grid) *grid = ctx->grid;
+    if (task_grid) *task_grid = ctx->task_grid;
+    if (coop_max) *coop_max = ctx->coop_max;
+    return PK_OK;
+}
+
+// ---- mailbox ----------------------------------------------------------------
+
+int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out) {
+    if (!ctx || !task) return ctx ? fail(ctx, PK_EINVAL, "pk_submit_task: NULL task") : PK_EINVAL;
+    if (seq_out) *seq_out = 0;
+    switch (task->kind) {
+        case PK_TASK_NOP:
+        case PK_TASK_STOP:
+            break;
+        case PK_TASK_JACOBI:
+            if (task->n_sweeps < 1 || task->n_sweeps > (1 << 24))
+                return fail(ctx, PK_EINVAL, "pk_submit_task: n_sweeps %d out of range", task->n_sweeps);
+            break;
+        case PK_TASK_AXPY:
+            if (!task->x || !task->y || task->len <= 0 || task->len > (1LL << 40) ||
+                !std::isfinite(task->a))
+                return fail(ctx, PK_EINVAL, "pk_submit_task: bad axpy task");
+            break;
+        default:
+            return fail(ctx, PK_EINVAL, "pk_submit_task: unknown kind %d", task->kind);
+    }
+    if (!ctx->task_live) {
+        if (task->kind == PK_TASK_STOP) return PK_OK;  // nothing to stop
+        // Fresh start: sequence numbers continue; state words zeroed.
+        const unsigned long long base = ctx->next_seq - 1;
+        ctx->mbox->done_seq.v = base;
+        ctx->mbox->status.v = 0;
+        __atomic_store_n(&ctx->mbox->seq.v, base, __ATOMIC_RELEASE);
+        PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_task, 0, sizeof(BarrierState), ctx->stream));
+        PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_task_inner, 0, sizeof(BarrierState), ctx->stream));
+        PK_TRY(ctx, cudaEventRecord(ctx->ev_sync, ctx->stream));
+        PK_TRY(ctx, cudaStreamWaitEvent(ctx->task_stream, ctx->ev_sync, 0));
+        TaskParams tp;
+        std::memset(&tp, 0, sizeof(tp));
+        tp.sp = base_params(ctx);
+        tp.sp.bar = &ctx->scratch->bar_task_inner;
+        tp.sp.skip_cta = -1;
+        tp.mbox = ctx->mbox_dev;
+        tp.dev_desc = &ctx->scratch->desc;
+        tp.tb = &ctx->scratch->bar_task;
+        tp.start_seq = base;
+        tp.depth = ctx->opt.mailbox_depth;
+        tp.idle_timeout_ns = ns_of(ctx->opt.mailbox_idle_timeout_s);
+        cudaError_t e = launch_task(ctx->poisson, ctx->task_grid, tp, ctx->task_stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(task kernel)");
+        ctx->task_live = true;
+        ctx->task_status = PK_OK;
+    }
+    const unsigned long long done = __atomic_load_n(&ctx->mbox->done_seq.v, __ATOMIC_ACQUIRE);
+    if (ctx->next_seq - 1 - done >= (unsigned long long)ctx->opt.mailbox_depth)
+        return fail(ctx, PK_EBUSY, "pk_submit_task: mailbox ring full");
+    const unsigned long long seq = ctx->next_seq++;
+    TaskSlot *slot = &ctx->mbox->slots[seq % (unsigned long long)ctx->opt.mailbox_depth];
+    slot->kind = task->kind;
+    slot->n_sweeps = task->n_sweeps;
+    slot->a = task->a;
+    slot->reserved = 0;
+    slot->x = (unsigned long long)(uintptr_t)task->x;
+    slot->y = (unsigned long long)(uintptr_t)task->y;
+    slot->len = task->len;
+    slot->pad = 0;
+    // Release: the descriptor is visible before the sequence number.
+    __atomic_store_n(&ctx->mbox->seq.v, seq, __ATOMIC_RELEASE);
+    if (seq_out) *seq_out = seq;
+    return PK_OK;
+}
+
+
+int pk_poll(pk_ctx *ctx, uint64_t seq) {
+    if (!ctx) return PK_EINVAL;
+    unsigned long long done = __atomic_load_n(&ctx->mbox->done_seq.v, __ATOMIC_ACQUIRE);
+    if (done >= seq) return 1;
+    if (!ctx->task_live) return ctx->task_status != PK_OK ? ctx->task_status : PK_ESHUTDOWN;
+    cudaError_t q = cudaStreamQuery(ctx->task_stream);
+    if (q == cudaErrorNotReady) return 0;
+    if (q != cudaSuccess) return cuda_fail(ctx, q, "cudaStreamQuery(task)");
+    int rc = task_finish(ctx);
+    done = __atomic_load_n(&ctx->mbox->done_seq.v, __ATOMIC_ACQUIRE);
+    if (done >= seq) return 1;
+    if (rc != PK_OK) return rc;
+    return ctx->task_status != PK_OK ? ctx->task_status : PK_ESHUTDOWN;
+}
+
+int pk_wait(pk_ctx *ctx, uint64_t seq, double timeout_s) {
+    if (!ctx) return PK_EINVAL;
+    const uint64_t t0 = now_ns();
+    const uint64_t limit = (uint64_t)(timeout_s * 1e9);
+    unsigned spins = 0;
+    for (;;) {
+        if (__atomic_load_n(&ctx->mbox->done_seq.v, __ATOMIC_ACQUIRE) >= seq) return PK_OK;
+        if ((++spins & 4095u) == 0u) {
+            int r = pk_poll(ctx, seq);
+            if (r == 1) return PK_OK;
+            if (r < 0) return r;
+            if (now_ns() - t0 > limit) return fail(ctx, PK_ETIMEDOUT, "pk_wait: deadline passed");
+        }
+    }
+}
+
+int pk_shutdown(pk_ctx *ctx) {
+    if (!ctx) return PK_EINVAL;
+    if (!ctx->task_live) {
+        const int st = ctx->task_status;
+        return (st == PK_ESHUTDOWN) ? PK_OK : st;
+    }
+    const uint64_t t0 = now_ns();
+    const uint64_t limit = (uint64_t)(ctx->opt.host_timeout_s * 1e9);
+    pk_task stop;
+    std::memset(&stop, 0, sizeof(stop));
+    stop.kind = PK_TASK_STOP;
+    uint64_t seq = 0;
+    for (;;) {
+        int rc = pk_submit_task(ctx, &stop, &seq);
+        if (rc == PK_OK) break;
+        if (rc != PK_EBUSY) return rc;
+        if (!ctx->task_live) break;
+        if (cudaStreamQuery(ctx->task_stream) == cudaSuccess) break;
+        if (now_ns() - t0 > limit) return fail(ctx, PK_ETIMEDOUT, "pk_shutdown: ring stayed full");
+    }
+    for (;;) {
+        if (!ctx->task_live) break;
+        cudaError_t q = cudaStreamQuery(ctx->task_stream);
+        if (q == cudaSuccess) break;
+        if (q != cudaErrorNotReady) return cuda_fail(ctx, q, "cudaStreamQuery(task)");
+        if (now_ns() - t0 > limit) return fail(ctx, PK_ETIMEDOUT, "pk_shutdown: task kernel still running");
+        std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+    if (ctx->task_live) {
+        int rc = task_finish(ctx);
+        if (rc != PK_OK) return rc;
+    }
+    return (ctx->task_status == PK_ESHUTDOWN || ctx->task_status == PK_OK) ? PK_OK : ctx->task_status;
+}
+
+void pk_destroy(pk_ctx *ctx) {
+    if (!ctx) return;
+    if (ctx->task_live) (void)pk_shutdown(ctx);
+    release(ctx);
+}
+
+const char *pk_last_error(const pk_ctx *ctx) {
+    return ctx ? ctx->err.c_str() : g_create_error.c_str();
+}
+
+// ---- measurement --------------------------------------------------------------
+
+int pk_bench_launch_floor(pk_ctx *ctx, int iters, double *us_sync_each, double *us_queued) {
+    if (!ctx || iters <= 0) return PK_EINVAL;
+    for (int w = 0; w < 8; ++w) PK_TRY(ctx, launch_empty(ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    uint64_t t0 = now_ns();
+    for (int i = 0; i < iters; ++i) {
+        PK_TRY(ctx, launch_empty(ctx->stream));
+        PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    }
+    uint64_t t1 = now_ns();
+    if (us_sync_each) *us_sync_each = (double)(t1 - t0) / 1e3 / iters;
+    t0 = now_ns();
+    for (int i = 0; i < iters; ++i) PK_TRY(ctx, launch_empty(ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    t1 = now_ns();
+    if (us_queued) *us_queued = (double)(t1 - t0) / 1e3 / iters;
+    return PK_OK;
+}
+
+int pk_bench_barrier(pk_ctx *ctx, int kind, int grid, int64_t n_barriers, double *us_total) {
+    if (!ctx || (kind != 0 && kind != 1) || grid < 0 || n_barriers < 0) return PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_bench_barrier: the task kernel is live");
+    if (grid == 0) grid = ctx->grid;
+    PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_bench, 0, sizeof(BarrierState), ctx->stream));
+    BarrierCtl ctl{&ctx->scratch->bar_bench, (unsigned)grid, ns_of(ctx->opt.barrier_timeout_s), -1, 0, 0};
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    cudaError_t e = launch_barrier_only(kind, grid, ctl, n_barriers, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(barrier)");
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    int rc = bar_status(ctx, &ctx->scratch->bar_bench, "pk_bench_barrier");
+    if (rc != PK_OK) return rc;
+    if (us_total) *us_total = elapsed_us(ctx);
+    return PK_OK;
+}
+
+int pk_barrier_stress(pk_ctx *ctx, int grid, int rounds, int words, uint64_t *checksums,
+                      int64_t *stale) {
+    if (!ctx || grid < 0 || rounds < 0 || words < 1 || words > kStressWords) return PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_barrier_stress: the task kernel is live");
+    if (grid == 0) grid = ctx->grid;
+    if (grid > ctx->stress_cap) {
+        cudaFree(ctx->stress_lines);
+        cudaFree(ctx->stress_out);
+        ctx->stress_lines = nullptr;
+        ctx->stress_out = nullptr;
+        ctx->stress_cap = 0;
+        PK_TRY(ctx, cudaMalloc(&ctx->stress_lines, sizeof(unsigned) * 2 * kStressWords * (size_t)grid));
+        PK_TRY(ctx, cudaMalloc(&ctx->stress_out, sizeof(unsigned long long) * ((size_t)grid + 1)));
+        ctx->stress_cap = grid;
+    }
+    PK_TRY(ctx, cudaMemsetAsync(ctx->stress_lines, 0, sizeof(unsigned) * 2 * kStressWords * (size_t)grid,
+                                ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->stress_out, 0, sizeof(unsigned long long) * ((size_t)grid + 1),
+                                ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_bench, 0, sizeof(BarrierState), ctx->stream));
+    BarrierCtl ctl{&ctx->scratch->bar_bench, (unsigned)grid, ns_of(ctx->opt.barrier_timeout_s), -1, 0, 0};
+    cudaError_t e = launch_stress(grid, ctl, rounds, words, ctx->stress_lines, ctx->stress_out + 1,
+                                  ctx->stress_out, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(stress)");
+    int rc = bar_status(ctx, &ctx->scratch->bar_bench, "pk_barrier_stress");
+    if (rc != PK_OK) return rc;
+    unsigned long long st = 0;
+    PK_TRY(ctx, cudaMemcpy(&st, ctx->stress_out, sizeof(st), cudaMemcpyDeviceToHost));
+    if (stale) *stale = (int64_t)st;
+    if (checksums)
+        PK_TRY(ctx, cudaMemcpy(checksums, ctx->stress_out + 1, sizeof(unsigned long long) * (size_t)grid,
+                               cudaMemcpyDeviceToHost));
+    return PK_OK;
+}
+
+int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int64_t n_tasks,
+                   int64_t *samples_ns) {
+    if (!ctx || !tasks || n_kinds <= 0 || n_tasks < 0 || (mode != 0 && mode != 1))
+        return ctx ? fail(ctx, PK_EINVAL, "pk_bench_tasks: bad arguments") : PK_EINVAL;
+    for (int q = 0; q < n_kinds; ++q)
+        if (tasks[q].kind == PK_TASK_STOP) return fail(ctx, PK_EINVAL, "pk_bench_tasks: STOP in list");
+    if (mode == 0) {
+        for (int64_t t = 0; t < n_tasks; ++t) {
+            const pk_task &task = tasks[t % n_kinds];
+            const uint64_t t0 = now_ns();
+            uint64_t seq = 0;
+            int rc = pk_submit_task(ctx, &task, &seq);
+            if (rc != PK_OK) return rc;
+            unsigned spins = 0;
+            while (__atomic_load_n(&ctx->mbox->done_seq.v, __ATOMIC_ACQUIRE) < seq) {
+                if ((++spins & 65535u) == 0u) {
+                    int r = pk_poll(ctx, seq);
+                    if (r == 1) break;
+                    if (r < 0) return r;
+                    if (now_ns() - t0 > (uint64_t)(ctx->opt.host_timeout_s * 1e9))
+                        return fail(ctx, PK_ETIMEDOUT, "pk_bench_tasks: task %lld not done",
+                                    (long long)t);
+                }
+            }
+            const uint64_t t1 = now_ns();
+            if (samples_ns) samples_ns[t] = (int64_t)(t1 - t0);
+        }
+        return PK_OK;
+    }
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_bench_tasks: the task kernel is live");
+    SweepParams p = base_params(ctx);
+    for (int64_t t = 0; t < n_tasks; ++t) {
+        const pk_task &task = tasks[t % n_kinds];
+        const uint64_t t0 = now_ns();
+        cudaError_t e = cudaSuccess;
+        if (task.kind == PK_TASK_JACOBI) {
+            for (int s = 0; s < task.n_sweeps && e == cudaSuccess; ++s) {
+                p.cur = ctx->cur;
+                p.pass_check = 0;
+                p.pass_store = 1;
+                p.pass_k = 0;
+                e = launch_once(kVariantDirect, ctx->poisson, ctx->task_grid, p, ctx->stream);
+                ctx->cur ^= 1;
+            }
+        } else if (task.kind == PK_TASK_AXPY) {
+            e = launch_axpy(ctx->task_grid, task.a, task.x, task.y, task.len, ctx->stream);
+        } else {
+            e = launch_empty(ctx->stream);
+        }
+        if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "pk_bench_tasks: launch");
+        const uint64_t t1 = now_ns();
+        if (samples_ns) samples_ns[t] = (int64_t)(t1 - t0);
+    }
+    return PK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,143 @@
+// pk_internal.h -- structures shared by libpk's kernel and host translation
+// units, and the launch wrappers the kernel unit exports to the host unit.
+// Not part of the public ABI (include/pk.h is).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "pk_device.cuh"
+
+namespace pk {
+
+// Per-run result the persistent kernel writes (CTA 0, thread 0, at exit).
+struct DeviceInfo {
+    long long sweeps_done;
+    double res0;
+    double res_last;
+    float rmax_last;
+    int n_checks;
+    int cur;       // buffer index holding the returned iterate
+    int run_id;    // equals SweepParams::run_id once written
+    long long task_sweeps;  // task kernel: sweeps run
+};
+
+// Residual result of the per-launch reduction kernel.
+struct ResidualOut {
+    double res;
+    float rmax;
+    float pad;
+};
+
+// Everything a sweep kernel needs.  Buffers are pitched: cell (j, i) of a
+// field at u[j * pitch + i + 3]; interior source cell (j, i) at
+// g[(j - 1) * gpitch + (i - 1)].
+struct SweepParams {
+    float *u[2];
+    const float *g;         // nullptr for Laplace
+    int nx, ny;
+    long long pitch, gpitch;
+    int cur;                // buffer holding U_0 when the kernel starts
+    // persistent loop
+    long long n;
+    float tol;
+    int check_every;
+    // single pass (per-launch path)
+    int pass_check, pass_store, pass_parity;
+    long long pass_k;       // sweep index (sets the STREAM direction)
+    // shared state
+    BarrierState *bar;
+    Partial *partials;      // 2 * max_grid entries (double-buffered by check parity)
+    int max_grid;
+    DeviceInfo *info;
+    unsigned long long timeout_ns;
+    int skip_cta, skip_at;
+    int alt_dir;            // STREAM: odd sweeps walk bands bottom-up
+    int run_id;             // echoed into DeviceInfo::run_id
+};
+
+// ---- mailbox in mapped pinned host memory ---------------------------------
+struct alignas(128) MboxWord {
+    unsigned long long v;
+    unsigned long long pad[15];
+};
+
+struct alignas(64) TaskSlot {
+    int kind;
+    int n_sweeps;
+    float a;
+    int reserved;
+    unsigned long long x;   // device address
+    unsigned long long y;   // device address
+    long long len;
+    long long pad;
+};
+
+struct Mailbox {
+    MboxWord seq;       // host: last posted sequence number (release store)
+    MboxWord done_seq;  // device: last completed sequence number (system-scope release)
+    MboxWord status;    // device: final status of the task kernel
+    MboxWord reserved;
+    TaskSlot slots[1];  // mailbox_depth entries
+};
+
+constexpr int kTaskExitIdle = 100;   // internal kind: idle timeout, exit
+
+struct TaskParams {
+    SweepParams sp;                 // field, source, inner grid barrier (sp.bar)
+    Mailbox *mbox;                  // device view of the mapped mailbox
+    TaskSlot *dev_desc;             // device-global broadcast copy
+    BarrierState *tb;               // gather (count) + broadcast (generation)
+    unsigned long long start_seq;   // last sequence number completed before launch
+    int depth;
+    unsigned long long idle_timeout_ns;
+};
+
+// ---- sizes -----------------------------------------------------------------
+constexpr int kDirectThreads = 256;
+constexpr int kConsumers = 256;                 // STREAM consumer threads
+constexpr int kStreamThreads = kConsumers + 32; // + one producer warp
+constexpr int kTW = 4 * kConsumers;             // interior columns per strip
+constexpr int kSlotU = kTW + 8;                 // floats of a staged row segment
+constexpr int kStages = 8;                      // TMA ring depth (power of two)
+constexpr int kStressWords = 32;
+
+inline size_t stream_smem_bytes(bool poisson) {
+    return 128 + (size_t)kStages * (size_t)(kSlotU + (poisson ? kTW : 0)) * sizeof(float);
+}
+
+// ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
+// Every wrapper returns the cudaError_t of its launch.
+enum Variant { kVariantDirect = 1, kVariantStream = 2 };
+
+// Once per device: kernel attributes (dynamic shared memory limits).
+cudaError_t prepare_kernels();
+
+// Kernel function pointers, for occupancy queries and attribute set-up.
+const void *kernel_persistent(int variant, bool poisson);
+const void *kernel_once(int variant, bool poisson);
+const void *kernel_task(bool poisson);
+const void *kernel_barrier_only(int kind);
+const void *kernel_stress();
+int block_threads(int variant);
+size_t dyn_smem(int variant, bool poisson);
+
+cudaError_t launch_persistent(int variant, bool poisson, int grid, const SweepParams &p,
+                              cudaStream_t s);
+cudaError_t launch_once(int variant, bool poisson, int grid, const SweepParams &p,
+                        cudaStream_t s);
+cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
+                            cudaStream_t s);
+cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long long gpitch,
+                                float h2, cudaStream_t s);
+cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s);
+cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,
+                        cudaStream_t s);
+cudaError_t launch_empty(cudaStream_t s);
+cudaError_t launch_barrier_only(int kind, int grid, BarrierCtl ctl, long long n,
+                                cudaStream_t s);
+cudaError_t launch_stress(int grid, BarrierCtl ctl, int rounds, int words, unsigned *lines,
+                          unsigned long long *checksums, unsigned long long *stale,
+                          cudaStream_t s);
+
+}  // namespace pk

@@ -1,0 +1,789 @@
+// pk_kernels.cu -- libpk's CUDA kernels for sm_103a and their launch wrappers.
+//
+// Sources (page title -- section):
+//   "Persistent Kernels: Bridging GPU-CPU Execution"
+//     -- "The problem (another PDE solver)": the 5-point update.
+//     -- "Implementation details and correctness": Jacobi into a separate
+//        result matrix.
+//     -- "Cache-line aware tiling and iteration": contiguous row bands, each
+//        thread walking down its columns with a three-row live window.
+//     -- "Base implementation" .. "Atomics and memory ordering",
+//        "Reflections": the host-flag task loop and how to do it correctly.
+//   "Grid-Wide Barriers and Persistent Work Queues"
+//     -- "The residency requirement": cooperative launch, grid sized to the
+//        machine, grid-stride loop.
+//     -- "What the barrier buys": in-kernel convergence check read by all
+//        blocks after the barrier.
+//     -- "When a launch is the better barrier": the per-launch path.
+//   "CUDA persist kernel" -- "Device Communication", "Ping-Pong Buffer":
+//     mapped pinned memory polled by the kernel; two buffers alternate.
+//   "@persistent" -- "A minimal kernel": a stage repeated with grid_barrier
+//     (reused as the barrier-only microbenchmark).
+#include <cooperative_groups.h>
+
+#include "pk_internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace pk {
+namespace {
+
+constexpr int kTaskNop = 0;
+constexpr int kTaskJacobi = 1;
+constexpr int kTaskAxpy = 2;
+constexpr int kTaskStop = 3;
+
+// ===========================================================================
+// DIRECT sweep: every thread owns float4 groups of a row and loads its own
+// centre, north, south and the two edge neighbours (they hit L1/L2: the
+// variant for grids that live in L2).  Units are (row, float4 group) pairs,
+// row-major, distributed grid-stride.
+template <bool POISSON, bool CHECK, bool STORE>
+__device__ __forceinline__ void pass_direct(const SweepParams &p, const float *__restrict__ src,
+                                            float *__restrict__ dst, unsigned first,
+                                            unsigned stride, double &s2, float &rmax) {
+    const unsigned nq = (unsigned)(p.nx + 3) >> 2;
+    const unsigned units = (unsigned)p.ny * nq;
+    for (unsigned u = first; u < units; u += stride) {
+        const unsigned jm1 = u / nq;
+        const unsigned q = u - jm1 * nq;
+        const long long off = (long long)(jm1 + 1u) * p.pitch + 4 + 4ll * q;
+        const float *c = src + off;
+        const float4 C = ld4(c);
+        const float4 S = ld4(c - p.pitch);
+        const float4 N = ld4(c + p.pitch);
+        const float W = c[-1];
+        const float E = c[4];
+        float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (POISSON) G = ld4(p.g + (long long)jm1 * p.gpitch + 4ll * q);
+        const int valid = min(4, p.nx - 4 * (int)q);
+        const Quad t = quad_t<POISSON>(W, C, E, S, N, G);
+        if (STORE) store_quad(dst + off, quad_update(t), valid);
+        if (CHECK) quad_residual(t, C, valid, s2, rmax);
+    }
+}
+
+template <bool POISSON>
+__device__ __forceinline__ void pass_direct_any(const SweepParams &p, const float *src, float *dst,
+                                                bool check, bool store, unsigned first,
+                                                unsigned stride, double &s2, float &rmax) {
+    if (check) {
+        if (store)
+            pass_direct<POISSON, true, true>(p, src, dst, first, stride, s2, rmax);
+        else
+            pass_direct<POISSON, true, false>(p, src, dst, first, stride, s2, rmax);
+    } else if (store) {
+        pass_direct<POISSON, false, true>(p, src, dst, first, stride, s2, rmax);
+    }
+}
+
+// ===========================================================================
+// STREAM sweep ("Cache-line aware tiling and iteration", the N = 10001
+// variant, rebuilt around TMA): the domain is cut into strips of kTW
+// interior columns; (strip, row) pairs are split evenly, in contiguous
+// runs, over the CTAs.  Each CTA walks its run row by row: one producer
+// thread streams every input row segment (with a 16-byte halo on each side)
+// into a kStages-deep shared-memory ring with cp.async.bulk, and 256
+// consumer threads keep a three-row window (previous, centre, next) in
+// registers, one float4 per thread, so each input row is read from HBM once
+// and from shared memory once.  Edge neighbours come from warp shuffles,
+// and at warp edges from the staged halo.
+struct StreamState {
+    uint64_t *full;
+    uint64_t *empty;
+    float *slots;
+    int slot_floats;
+    unsigned L;     // ring position; producer and consumers advance it alike
+    bool broken;    // a pipeline wait expired: stop waiting, finish quickly
+};
+
+__device__ __forceinline__ StreamState stream_setup(unsigned char *smem, bool poisson) {
+    StreamState st;
+    st.full = reinterpret_cast<uint64_t *>(smem);
+    st.empty = st.full + kStages;
+    st.slots = reinterpret_cast<float *>(smem + 128);
+    st.slot_floats = kSlotU + (poisson ? kTW : 0);
+    st.L = 0;
+    st.broken = false;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&st.full[i], 1);
+            mbar_init(&st.empty[i], kConsumers / 32);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+    return st;
+}
+
+__device__ __forceinline__ float4 lds4(const float *p) {
+    return *reinterpret_cast<const float4 *>(p);
+}
+
+// Producer: input rows ja - dir .. jb + dir of strip columns [col0, col0+cols).
+template <bool POISSON>
+__device__ __forceinline__ void produce_segment(const SweepParams &p, const float *src, int ja,
+                                                int jb, int dir, int cols, long long col0,
+                                                StreamState &st) {
+    const unsigned bytes_u = (unsigned)(((cols + 5 + 3) & ~3) * 4);
+    const unsigned bytes_g = (unsigned)(((cols + 3) & ~3) * 4);
+    const int r_last = jb + dir;
+    for (int r = ja - dir;; r += dir) {
+        const unsigned slot = st.L & (kStages - 1);
+        const unsigned ph = (st.L / kStages) & 1u;
+        if (!st.broken && !mbar_wait_bounded(&st.empty[slot], ph ^ 1u, p.timeout_ns, p.bar)) {
+            record_error(p.bar, kETimedOut, kSitePipeline);
+            st.broken = true;
+        }
+        const bool gneed = POISSON && (dir > 0 ? (r >= ja && r <= jb) : (r <= ja && r >= jb));
+        float *dst_u = st.slots + slot * st.slot_floats;
+        mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
+        tma_load_1d(dst_u, src + (long long)r * p.pitch + col0, bytes_u, &st.full[slot]);
+        if (gneed)
+            tma_load_1d(dst_u + kSlotU, p.g + (long long)(r - 1) * p.gpitch + col0, bytes_g,
+                        &st.full[slot]);
+        ++st.L;
+        if (r == r_last) break;
+    }
+}
+
+// Consumers: output rows ja .. jb (in walking order) of the same strip.
+template <bool POISSON, bool CHECK, bool STORE>
+__device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst, int ja, int jb,
+                                                int dir, int cols, long long col0,
+                                                StreamState &st, double &s2, float &rmax) {
+    const int t = threadIdx.x;
+    const unsigned lane = t & 31;
+    const int valid = max(0, min(4, cols - 4 * t));
+    const int nin = (dir > 0 ? jb - ja : ja - jb) + 3;
+    float4 prev = make_float4(0.f, 0.f, 0.f, 0.f), cur = prev, curg = prev;
+    float curw = 0.f, cure = 0.f;
+    int r = ja - dir;
+    for (int idx = 0; idx < nin; ++idx, r += dir) {
+        const unsigned slot = st.L & (kStages - 1);
+        const unsigned ph = (st.L / kStages) & 1u;
+        if (!st.broken && !mbar_wait_bounded(&st.full[slot], ph, p.timeout_ns, p.bar)) {
+            record_error(p.bar, kETimedOut, kSitePipeline);
+            st.broken = true;
+        }
+        const float *su = st.slots + slot * st.slot_floats;
+        const float4 x = lds4(su + 4 + 4 * t);
+        const float xw = lane == 0u ? su[3 + 4 * t] : 0.f;
+        const float xe = lane == 31u ? su[8 + 4 * t] : 0.f;
+        float4 xg = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (POISSON && idx >= 1 && idx <= nin - 2) xg = lds4(su + kSlotU + 4 * t);
+        __syncwarp();
+        if (lane == 0u) mbar_arrive(&st.empty[slot]);
+        ++st.L;
+        if (idx >= 2) {
+            float w = __shfl_up_sync(0xffffffffu, cur.w, 1);
+            float e = __shfl_down_sync(0xffffffffu, cur.x, 1);
+            if (lane == 0u) w = curw;
+            if (lane == 31u) e = cure;
+            // prev and x are the rows on either side of the centre; their sum
+            // is commutative, so walking up or down gives the same bits.
+            const Quad q = quad_t<POISSON>(w, cur, e, prev, x, curg);
+            if (STORE)
+                store_quad(dst + (long long)(r - dir) * p.pitch + col0 + 4 + 4 * t,
+                           quad_update(q), valid);
+            if (CHECK) quad_residual(q, cur, valid, s2, rmax);
+        }
+        prev = cur;
+        cur = x;
+        curw = xw;
+        cure = xe;
+        curg = xg;
+    }
+}
+
+template <bool POISSON, bool CHECK, bool STORE>
+__device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
+                                            int dir, StreamState &st, double &s2, float &rmax) {
+    const int nx = p.nx, ny = p.ny;
+    const int strips = (nx + kTW - 1) / kTW;
+    const long long R = (long long)strips * ny;
+    const long long L0 = R * blockIdx.x / gridDim.x;
+    const long long L1 = R * (blockIdx.x + 1) / gridDim.x;
+    const bool producer_warp = threadIdx.x >= kConsumers;
+    long long pos = dir > 0 ? L0 : L1 - 1;
+    long long remaining = L1 - L0;
+    while (remaining > 0) {
+        const int s = (int)(pos / ny);
+        const int jr = (int)(pos - (long long)s * ny) + 1;
+        long long len;
+        int jb;
+        if (dir > 0) {
+            len = min((long long)(ny - jr + 1), remaining);
+            jb = jr + (int)len - 1;
+        } else {
+            len = min((long long)jr, remaining);
+            jb = jr - (int)len + 1;
+        }
+        const int cols = min(kTW, nx - s * kTW);
+        const long long col0 = (long long)s * kTW;
+        if (producer_warp) {
+            if (threadIdx.x == kConsumers)
+                produce_segment<POISSON>(p, src, jr, jb, dir, cols, col0, st);
+        } else {
+            consume_segment<POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2, rmax);
+        }
+        pos += dir > 0 ? len : -len;
+        remaining -= len;
+    }
+    // Generic-proxy stores of this sweep -> TMA reads of the next one.
+    if (STORE && !producer_warp) fence_proxy_async_global();
+}
+
+template <bool POISSON>
+__device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
+                                                int dir, bool check, bool store, StreamState &st,
+                                                double &s2, float &rmax) {
+    if (check) {
+        if (store)
+            pass_stream<POISSON, true, true>(p, src, dst, dir, st, s2, rmax);
+        else
+            pass_stream<POISSON, true, false>(p, src, dst, dir, st, s2, rmax);
+    } else if (store) {
+        pass_stream<POISSON, false, true>(p, src, dst, dir, st, s2, rmax);
+    }
+}
+
+// ===========================================================================
+// The persistent loop ("What the barrier buys"): sweep k reads U_k and
+// writes U_{k+1}; on a check sweep the same pass reduces the residual of
+// U_k into per-CTA partials; after the grid barrier every CTA reduces all
+// partials in the same fixed order, so every CTA takes the same exit
+// decision without another barrier.  Partials are double-buffered by check
+// parity: a CTA can only overwrite a slot after the next barrier, by which
+// time every CTA has finished reading it.
+template <class PassFn>
+__device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
+    BarrierCtl ctl{p.bar, gridDim.x, p.timeout_ns, p.skip_cta, p.skip_at, 0};
+    const bool checks = p.tol > 0.f && p.check_every > 0;
+    int cur = p.cur;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    for (;;) {
+        const bool check = checks && (k % p.check_every) == 0;
+        if (k == p.n && !check) break;
+        const bool store = k < p.n;
+        double s2 = 0.0;
+        float rmax = 0.f;
+        pass(p.u[cur], p.u[cur ^ 1], check, store, k, s2, rmax);
+        Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+        if (check) {
+            block_reduce(s2, rmax);
+            if (threadIdx.x == 0) {
+                Partial pp;
+                pp.s2 = s2;
+                pp.rmax = rmax;
+                pp.pad = 0.f;
+                parts[blockIdx.x] = pp;
+            }
+        }
+        if (!grid_barrier(ctl)) return;  // aborting: the host reads the error
+        if (check) {
+            double S2;
+            float RM;
+            reduce_partials(parts, (int)gridDim.x, S2, RM);
+            const double res = sqrt(S2);
+            ++n_checks;
+            res_last = res;
+            rmax_last = RM;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)p.tol * res0)
+                break;
+        }
+        if (k == p.n) break;
+        cur ^= 1;
+        ++k;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = k;
+        d->res0 = res0;
+        d->res_last = res_last;
+        d->rmax_last = rmax_last;
+        d->n_checks = n_checks;
+        d->cur = cur;
+        d->task_sweeps = 0;
+        __threadfence();
+        d->run_id = p.run_id;
+    }
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParams p) {
+    const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned stride = gridDim.x * blockDim.x;
+    persistent_loop(p, [&](const float *src, float *dst, bool check, bool store, long long,
+                           double &s2, float &rmax) {
+        pass_direct_any<POISSON>(p, src, dst, check, store, first, stride, s2, rmax);
+    });
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    StreamState st = stream_setup(smem, POISSON);
+    persistent_loop(p, [&](const float *src, float *dst, bool check, bool store, long long k,
+                           double &s2, float &rmax) {
+        const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
+        // After the barrier: this producer's TMA reads must see the
+        // generic-proxy stores the whole grid made in the previous sweep.
+        if (threadIdx.x == kConsumers) fence_proxy_async_global();
+        pass_stream_any<POISSON>(p, src, dst, dir, check, store, st, s2, rmax);
+    });
+}
+
+// ===========================================================================
+// Per-launch path: one pass per launch (the launch boundary is the barrier).
+__device__ __forceinline__ void write_partial(const SweepParams &p, double s2, float rmax) {
+    block_reduce(s2, rmax);
+    if (threadIdx.x == 0) {
+        Partial pp;
+        pp.s2 = s2;
+        pp.rmax = rmax;
+        pp.pad = 0.f;
+        p.partials[(size_t)p.pass_parity * (size_t)p.max_grid + blockIdx.x] = pp;
+    }
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_once_direct(SweepParams p) {
+    double s2 = 0.0;
+    float rmax = 0.f;
+    pass_direct_any<POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], p.pass_check != 0, p.pass_store != 0,
+                             blockIdx.x * blockDim.x + threadIdx.x, gridDim.x * blockDim.x, s2,
+                             rmax);
+    if (p.pass_check) write_partial(p, s2, rmax);
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kStreamThreads) k_once_stream(SweepParams p) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    StreamState st = stream_setup(smem, POISSON);
+    double s2 = 0.0;
+    float rmax = 0.f;
+    const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;
+    pass_stream_any<POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
+                             p.pass_store != 0, st, s2, rmax);
+    if (p.pass_check) write_partial(p, s2, rmax);
+}
+
+// Reduction of the per-CTA partials, launched with the same block size as
+// the sweep kernel so the fixed reduction tree (and the result bits) match
+// the persistent kernel's.
+__global__ void k_finalize(SweepParams p, int count, ResidualOut *out) {
+    double S2;
+    float RM;
+    reduce_partials(p.partials + (size_t)p.pass_parity * (size_t)p.max_grid, count, S2, RM);
+    if (threadIdx.x == 0) {
+        out->res = sqrt(S2);
+        out->rmax = RM;
+        out->pad = 0.f;
+    }
+}
+
+// g = fl32(h^2 * f) into the pitched source layout; pad columns zeroed.
+__global__ void k_scale_source(const float *__restrict__ f, float *__restrict__ g, int nx, int ny,
+                               long long gpitch, float h2) {
+    const long long total = (long long)ny * gpitch;
+    for (long long q = blockIdx.x * (long long)blockDim.x + threadIdx.x; q < total;
+         q += (long long)gridDim.x * blockDim.x) {
+        const long long j = q / gpitch;
+        const long long i = q - j * gpitch;
+        g[q] = i < nx ? __fmul_rn(h2, f[j * nx + i]) : 0.f;
+    }
+}
+
+// ===========================================================================
+// y <- fl32(fl32(a * x) + y), grid-stride, float4 when both are aligned.
+__device__ __forceinline__ void axpy_range(float a, const float *__restrict__ x,
+                                           float *__restrict__ y, long long len, long long first,
+                                           long long stride) {
+    const bool vec = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(y)) & 15u) == 0;
+    long long done = 0;
+    if (vec) {
+        const long long n4 = len >> 2;
+        for (long long q = first; q < n4; q += stride) {
+            const float4 xv = ld4(x + 4 * q);
+            float4 yv = ld4(y + 4 * q);
+            yv.x = __fadd_rn(__fmul_rn(a, xv.x), yv.x);
+            yv.y = __fadd_rn(__fmul_rn(a, xv.y), yv.y);
+            yv.z = __fadd_rn(__fmul_rn(a, xv.z), yv.z);
+            yv.w = __fadd_rn(__fmul_rn(a, xv.w), yv.w);
+            *reinterpret_cast<float4 *>(y + 4 * q) = yv;
+        }
+        done = 4 * n4;
+    }
+    for (long long q = done + first; q < len; q += stride) y[q] = __fadd_rn(__fmul_rn(a, x[q]), y[q]);
+}
+
+__global__ void __launch_bounds__(kDirectThreads) k_axpy(float a, const float *x, float *y,
+                                                         long long len) {
+    axpy_range(a, x, y, len, blockIdx.x * (long long)blockDim.x + threadIdx.x,
+               (long long)gridDim.x * blockDim.x);
+}
+
+// ===========================================================================
+// Resident task loop ("Base implementation" rebuilt as the "Reflections"
+// ask).  CTA 0's thread 0 is the only poller of host memory.  Between two
+// tasks the grid does one gather + broadcast:
+//   * every other CTA, after __syncthreads, arrives on tb->count with a
+//     release atomic and spins (acquire) on tb->generation;
+//   * CTA 0's thread 0 waits (acquire) for gridDim.x - 1 arrivals, resets
+//     the count, publishes the finished task's sequence number to the host
+//     (__threadfence_system + st.release.sys: never before the work is
+//     done), polls the mailbox (relaxed loads, then one acquire), copies the
+//     descriptor to device memory and releases the next generation.
+// All spins are bounded (idle limit for the host poll, barrier limit for the
+// rest) and end on the abort flag.
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
+    __shared__ TaskSlot s_task;
+    const SweepParams &p = tp.sp;
+    BarrierState *tb = tp.tb;
+    BarrierCtl inner{p.bar, gridDim.x, p.timeout_ns, -1, 0, 0};
+    const unsigned G = gridDim.x;
+    const unsigned first_unit = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned stride = G * blockDim.x;
+    int cur = p.cur;
+    long long sweeps = 0;
+    unsigned long long last = tp.start_seq;
+    unsigned gen = 0;
+    bool first = true;
+    int final_status = kOk;
+    for (;;) {
+        __syncthreads();  // this CTA is done with the previous task
+        if (threadIdx.x == 0) {
+            if (blockIdx.x == 0) {
+                int kind_override = -1;
+                if (!first) {
+                    const uint64_t t0 = globaltimer_ns();
+                    unsigned spins = 0;
+                    while (ld_acquire_gpu(&tb->count.v) != G - 1u) {
+                        if ((++spins & 255u) == 0u) {
+                            if (aborted(tb) || aborted(p.bar)) {
+                                kind_override = kTaskExitIdle;
+                                break;
+                            }
+                            if (globaltimer_ns() - t0 > p.timeout_ns) {
+                                record_error(tb, kETimedOut, kSiteTaskGather);
+                                kind_override = kTaskExitIdle;
+                                break;
+                            }
+                        }
+                    }
+                    if (kind_override < 0) {
+                        st_relaxed_gpu(&tb->count.v, 0u);
+                        __threadfence_system();
+                        st_release_sys_u64(&tp.mbox->done_seq.v, last);
+                    }
+                }
+                if (kind_override < 0) {
+                    const uint64_t t0 = globaltimer_ns();
+                    unsigned spins = 0;
+                    for (;;) {
+                        if (ld_relaxed_sys_u64(&tp.mbox->seq.v) > last) break;
+                        if ((++spins & 63u) == 0u &&
+                            globaltimer_ns() - t0 > tp.idle_timeout_ns) {
+                            record_error(tb, kETimedOut, kSiteMailboxIdle);
+                            kind_override = kTaskExitIdle;
+                            break;
+                        }
+                    }
+                }
+                TaskSlot d;
+                if (kind_override < 0) {
+                    (void)ld_acquire_sys_u64(&tp.mbox->seq.v);
+                    const volatile TaskSlot *hs = &tp.mbox->slots[(last + 1ull) % (unsigned)tp.depth];
+                    d.kind = hs->kind;
+                    d.n_sweeps = hs->n_sweeps;
+                    d.a = hs->a;
+                    d.reserved = 0;
+                    d.x = hs->x;
+                    d.y = hs->y;
+                    d.len = hs->len;
+                    d.pad = 0;
+                } else {
+                    d.kind = kind_override;
+                    d.n_sweeps = 0;
+                    d.a = 0.f;
+                    d.reserved = 0;
+                    d.x = d.y = 0ull;
+                    d.len = 0;
+                    d.pad = 0;
+                }
+                *tp.dev_desc = d;
+                s_task = d;
+                st_release_gpu(&tb->generation.v, gen + 1u);
+            } else {
+                if (!first) atom_add_release_gpu(&tb->count.v, 1u);
+                const uint64_t t0 = globaltimer_ns();
+                const uint64_t limit = tp.idle_timeout_ns + p.timeout_ns;
+                unsigned spins = 0;
+                bool ok = true;
+                while (ld_acquire_gpu(&tb->generation.v) == gen) {
+                    if ((++spins & 255u) == 0u) {
+                        if (aborted(tb) || aborted(p.bar)) {
+                            ok = false;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > limit) {
+                            record_error(tb, kETimedOut, kSiteTaskBroadcast);
+                            ok = false;
+                            break;
+                        }
+                    }
+                }
+                if (ok) {
+                    const volatile TaskSlot *ds = tp.dev_desc;
+                    s_task.kind = ds->kind;
+                    s_task.n_sweeps = ds->n_sweeps;
+                    s_task.a = ds->a;
+                    s_task.x = ds->x;
+                    s_task.y = ds->y;
+                    s_task.len = ds->len;
+                } else {
+                    s_task.kind = kTaskExitIdle;
+                }
+            }
+        }
+        __syncthreads();
+        ++gen;
+        first = false;
+        const int kind = s_task.kind;
+        if (kind == kTaskStop) {
+            ++last;
+            final_status = kEShutdown;
+            break;
+        }
+        if (kind != kTaskNop && kind != kTaskJacobi && kind != kTaskAxpy) {
+            final_status = kETimedOut;
+            break;
+        }
+        ++last;
+        if (kind == kTaskJacobi) {
+            bool ok = true;
+            for (int s = 0; s < s_task.n_sweeps; ++s) {
+                if (s > 0 && !grid_barrier(inner)) {
+                    ok = false;
+                    break;
+                }
+                double d0 = 0.0;
+                float f0 = 0.f;
+                pass_direct<POISSON, false, true>(p, p.u[cur], p.u[cur ^ 1], first_unit, stride,
+                                                  d0, f0);
+                cur ^= 1;
+                ++sweeps;
+            }
+            if (!ok) {
+                final_status = kETimedOut;
+                break;
+            }
+        } else if (kind == kTaskAxpy) {
+            axpy_range(s_task.a, reinterpret_cast<const float *>(s_task.x),
+                       reinterpret_cast<float *>(s_task.y), s_task.len, first_unit, stride);
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = 0;
+        d->cur = cur;
+        d->task_sweeps = sweeps;
+        d->n_checks = 0;
+        __threadfence();
+        d->run_id = p.run_id;
+        __threadfence_system();
+        st_release_sys_u64(&tp.mbox->status.v, (unsigned long long)(long long)final_status);
+        if (final_status == kEShutdown) st_release_sys_u64(&tp.mbox->done_seq.v, last);
+    }
+}
+
+// ===========================================================================
+// Microbenchmarks and the barrier stress test.
+__global__ void k_empty() {}
+
+__global__ void __launch_bounds__(256) k_barrier_only(BarrierCtl ctl, long long n) {
+    for (long long i = 0; i < n; ++i)
+        if (!grid_barrier(ctl)) return;
+}
+
+__global__ void __launch_bounds__(256) k_cg_sync(BarrierCtl, long long n) {
+    cg::grid_group g = cg::this_grid();
+    for (long long i = 0; i < n; ++i) g.sync();
+}
+
+// SplitMix64 output function (Steele, Lea, Flood, OOPSLA 2014).
+__device__ __forceinline__ unsigned long long mix64(unsigned long long z) {
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__device__ __forceinline__ unsigned stamp(unsigned long long r, unsigned long long nb,
+                                          unsigned long long b, unsigned long long words,
+                                          unsigned long long w) {
+    return (unsigned)mix64(((r * nb + b) * words + w) + 1ull);
+}
+
+// Round r: CTA b writes `words` stamps on its own 128-byte line of buffer
+// r & 1, crosses the barrier, then reads the lines of CTAs b+1, b+G/2 and
+// b+r+1 (mod G) with ordinary loads, counting stale words and summing all.
+__global__ void __launch_bounds__(256) k_stress(BarrierCtl ctl, int rounds, int words,
+                                                unsigned *lines, unsigned long long *checksums,
+                                                unsigned long long *stale) {
+    const unsigned G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
+    unsigned long long acc = 0ull, bad = 0ull;
+    for (int r = 0; r < rounds; ++r) {
+        unsigned *buf = lines + (size_t)(r & 1) * G * kStressWords;
+        if (t < (unsigned)words) buf[b * kStressWords + t] = stamp(r, G, b, words, t);
+        if (!grid_barrier(ctl)) return;
+        if (t < (unsigned)words) {
+            const unsigned peers[3] = {(b + 1u) % G, (b + G / 2u) % G,
+                                       (unsigned)(((unsigned long long)b + r + 1ull) % G)};
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const unsigned v = buf[peers[k] * kStressWords + t];
+                acc += v;
+                if (v != stamp(r, G, peers[k], words, t)) ++bad;
+            }
+        }
+    }
+    if (t < 32) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc += __shfl_down_sync(0xffffffffu, acc, off);
+            bad += __shfl_down_sync(0xffffffffu, bad, off);
+        }
+        if (t == 0) {
+            checksums[b] = acc;
+            if (bad) atomicAdd(stale, bad);
+        }
+    }
+}
+
+}  // namespace
+
+// ===========================================================================
+// Launch wrappers.
+cudaError_t prepare_kernels() {
+    cudaError_t e;
+    e = cudaFuncSetAttribute(k_persistent_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem_bytes(false));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_persistent_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem_bytes(true));
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(k_once_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)stream_smem_bytes(false));
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(k_once_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)stream_smem_bytes(true));
+}
+
+const void *kernel_persistent(int variant, bool poisson) {
+    if (variant == kVariantStream)
+        return poisson ? (const void *)k_persistent_stream<true> : (const void *)k_persistent_stream<false>;
+    return poisson ? (const void *)k_persistent_direct<true> : (const void *)k_persistent_direct<false>;
+}
+
+const void *kernel_once(int variant, bool poisson) {
+    if (variant == kVariantStream)
+        return poisson ? (const void *)k_once_stream<true> : (const void *)k_once_stream<false>;
+    return poisson ? (const void *)k_once_direct<true> : (const void *)k_once_direct<false>;
+}
+
+const void *kernel_task(bool poisson) {
+    return poisson ? (const void *)k_task<true> : (const void *)k_task<false>;
+}
+
+const void *kernel_barrier_only(int kind) {
+    return kind == 1 ? (const void *)k_cg_sync : (const void *)k_barrier_only;
+}
+
+const void *kernel_stress() { return (const void *)k_stress; }
+
+int block_threads(int variant) { return variant == kVariantStream ? kStreamThreads : kDirectThreads; }
+
+size_t dyn_smem(int variant, bool poisson) {
+    return variant == kVariantStream ? stream_smem_bytes(poisson) : 0;
+}
+
+cudaError_t launch_persistent(int variant, bool poisson, int grid, const SweepParams &p,
+                              cudaStream_t s) {
+    SweepParams arg = p;
+    void *args[] = {&arg};
+    return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson), dim3(grid),
+                                       dim3(block_threads(variant)), args,
+                                       dyn_smem(variant, poisson), s);
+}
+
+cudaError_t launch_once(int variant, bool poisson, int grid, const SweepParams &p,
+                        cudaStream_t s) {
+    if (variant == kVariantStream) {
+        if (poisson)
+            k_once_stream<true><<<grid, kStreamThreads, stream_smem_bytes(true), s>>>(p);
+        else
+            k_once_stream<false><<<grid, kStreamThreads, stream_smem_bytes(false), s>>>(p);
+    } else {
+        if (poisson)
+            k_once_direct<true><<<grid, kDirectThreads, 0, s>>>(p);
+        else
+            k_once_direct<false><<<grid, kDirectThreads, 0, s>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
+                            cudaStream_t s) {
+    k_finalize<<<1, block_threads(variant), 0, s>>>(p, grid, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long long gpitch,
+                                float h2, cudaStream_t s) {
+    const long long total = (long long)ny * gpitch;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 65535) blocks = 65535;
+    if (blocks < 1) blocks = 1;
+    k_scale_source<<<(unsigned)blocks, 256, 0, s>>>(f, g, nx, ny, gpitch, h2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s) {
+    TaskParams arg = p;
+    void *args[] = {&arg};
+    return cudaLaunchCooperativeKernel(kernel_task(poisson), dim3(grid), dim3(kDirectThreads), args,
+                                       0, s);
+}
+
+cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,
+                        cudaStream_t s) {
+    k_axpy<<<grid, kDirectThreads, 0, s>>>(a, x, y, len);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_empty(cudaStream_t s) {
+    k_empty<<<1, 32, 0, s>>>();
+    return cudaGetLastError();
+}
+
+cudaError_t launch_barrier_only(int kind, int grid, BarrierCtl ctl, long long n,
+                                cudaStream_t s) {
+    void *args[] = {&ctl, &n};
+    return cudaLaunchCooperativeKernel(kernel_barrier_only(kind), dim3(grid), dim3(256), args, 0, s);
+}
+
+cudaError_t launch_stress(int grid, BarrierCtl ctl, int rounds, int words, unsigned *lines,
+                          unsigned long long *checksums, unsigned long long *stale,
+                          cudaStream_t s) {
+    void *args[] = {&ctl, &rounds, &words, &lines, &checksums, &stale};
+    return cudaLaunchCooperativeKernel(kernel_stress(), dim3(grid), dim3(256), args, 0, s);
+}
+
+}  // namespace pk

@@ -1,0 +1,120 @@
+"""libpk's C ABI on the CPU: the library loads, exports every symbol that
+include/pk.h declares, and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pk.h")
+
+
+@pytest.fixture(scope="module")
+def pk():
+    from iterative_stencil_solver_gb300 import build_ext
+    build_ext.build()
+    from iterative_stencil_solver_gb300 import pk as mod
+    return mod
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_ \t]*[\s*]+(pk_[a-z_0-9]+)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary_calls():
+    names = _declared_functions()
+    for required in ("pk_create", "pk_run_sweeps", "pk_run_sweeps_launch", "pk_submit_task",
+                     "pk_poll", "pk_shutdown", "pk_create_device", "pk_get_field",
+                     "pk_set_field", "pk_destroy", "pk_last_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the binding wraps each one under the same name
+    assert not [n for n in _declared_functions() if not hasattr(pk, n)]
+
+
+def test_struct_sizes_match_header(pk):
+    # pk_run_info: i64, f64, f64, f32, 5 x i32, f64 -> 56 bytes with natural alignment.
+    assert ctypes.sizeof(pk.pk_run_info) == 56
+    assert ctypes.sizeof(pk.pk_task) == 40
+    opt = pk.pk_options_default()
+    assert opt.struct_size == ctypes.sizeof(pk.pk_options) == 88
+
+
+def test_options_defaults(pk):
+    opt = pk.pk_options_default()
+    assert opt.variant == pk.PK_VARIANT_AUTO
+    assert opt.barrier_timeout_s == 2.0
+    assert opt.mailbox_idle_timeout_s == 10.0
+    assert opt.mailbox_depth == 64
+    assert opt.debug_skip_arrival_cta == -1
+
+
+@pytest.mark.parametrize("nx,ny", [(1, 1), (64, 64), (4096, 4096), (16384, 16384), (1030, 9)])
+def test_layout(pk, nx, ny):
+    pitch, fbytes, gpitch = pk.pk_layout(nx, ny)
+    assert pitch % 32 == 0 and pitch >= nx + 8
+    assert fbytes == (ny + 2) * pitch * 4
+    assert gpitch % 32 == 0 and gpitch >= nx
+
+
+def test_layout_rejects_bad_sizes(pk):
+    for nx, ny in ((0, 5), (5, 0), (-1, 3)):
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_layout(nx, ny)
+        assert e.value.code == pk.PK_EINVAL
+
+
+def test_create_rejects_bad_input_without_cuda(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    lib.pk_create.argtypes = pk._SIGS["pk_create"][1]
+    lib.pk_last_error.restype = ctypes.c_char_p
+    lib.pk_last_error.argtypes = [ctypes.c_void_p]
+    h = ctypes.c_void_p()
+    u = np.zeros((3, 3), np.float32)
+    fp = u.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+    assert lib.pk_create(0, 1, fp, None, None, ctypes.byref(h)) == pk.PK_EINVAL
+    assert b"bad sizes" in lib.pk_last_error(None)
+    assert lib.pk_create(1, 1, None, None, None, ctypes.byref(h)) == pk.PK_EINVAL
+    bad = u.copy()
+    bad[1, 1] = np.nan
+    assert lib.pk_create(1, 1, bad.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), None, None,
+                         ctypes.byref(h)) == pk.PK_EINVAL
+    assert b"not finite" in lib.pk_last_error(None)
+    f = np.array([[np.inf]], np.float32)
+    assert lib.pk_create(1, 1, fp, f.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), None,
+                         ctypes.byref(h)) == pk.PK_EINVAL
+    assert h.value is None
+
+
+def test_create_rejects_wrong_options_size(pk):
+    opt = pk.pk_options_default()
+    opt.struct_size = 12
+    u = np.zeros((3, 3), np.float32)
+    with pytest.raises(pk.PkError) as e:
+        pk.pk_create(1, 1, u, None, opt)
+    assert e.value.code == pk.PK_EINVAL
+
+
+def test_null_context_calls(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    for name in ("pk_run_sweeps", "pk_run_sweeps_launch"):
+        fn = getattr(lib, name)
+        fn.argtypes = pk._SIGS[name][1]
+        assert fn(None, 1, 0.0, 0, None) == pk.PK_EINVAL
+    lib.pk_poll.argtypes = pk._SIGS["pk_poll"][1]
+    assert lib.pk_poll(None, 1) == pk.PK_EINVAL
+    lib.pk_shutdown.argtypes = pk._SIGS["pk_shutdown"][1]
+    assert lib.pk_shutdown(None) == pk.PK_EINVAL
+    lib.pk_destroy.argtypes = pk._SIGS["pk_destroy"][1]
+    lib.pk_destroy(None)

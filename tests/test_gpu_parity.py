@@ -1,0 +1,402 @@
+"""GPU parity: libpk (through its C ABI) against the CPU oracle, bit for bit.
+
+Fields are compared element by element as raw binary32 bits.  Residual L2
+norms are compared at rel 1e-10 (the two sides sum in different orders);
+max|r| is order-free and must match exactly.
+"""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from iterative_stencil_solver_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+THREADS = os.cpu_count() or 1
+
+
+@pytest.fixture(scope="module")
+def pk():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from iterative_stencil_solver_gb300 import build_ext
+    build_ext.build()
+    from iterative_stencil_solver_gb300 import pk as mod
+    return mod
+
+
+def assert_same_bits(got, want, what="field"):
+    got = np.ascontiguousarray(got, np.float32)
+    want = np.ascontiguousarray(want, np.float32)
+    assert got.shape == want.shape, (got.shape, want.shape)
+    diff = got.view(np.uint32) != want.view(np.uint32)
+    if diff.any():
+        idx = np.argwhere(diff)
+        j, i = idx[0]
+        raise AssertionError("%s differs at %d cells; first (%d, %d): got %r want %r"
+                             % (what, len(idx), j, i, float(got[j, i]), float(want[j, i])))
+
+
+def run_pk(pk, u0, f, n, tol=0.0, ce=0, path="persistent", **opts):
+    ny, nx = u0.shape[0] - 2, u0.shape[1] - 2
+    opt = pk.pk_options_default(**opts)
+    ctx = pk.pk_create(nx, ny, u0, f, opt)
+    try:
+        fn = pk.pk_run_sweeps if path == "persistent" else pk.pk_run_sweeps_launch
+        info = fn(ctx, n, tol, ce)
+        out = pk.pk_get_field(ctx)
+    finally:
+        pk.pk_destroy(ctx)
+    return out, info
+
+
+def check_info(info, oinfo):
+    assert info["status"] == 0
+    assert info["sweeps_done"] == oinfo.sweeps_done
+    assert info["n_checks"] == oinfo.n_checks
+    if oinfo.n_checks:
+        assert info["res_max_last"] == oinfo.rmax_last
+        assert info["res0"] == pytest.approx(oinfo.res0, rel=1e-10, abs=0)
+        assert info["res_last"] == pytest.approx(oinfo.res_last, rel=1e-10, abs=1e-300)
+
+
+# ---- small and ragged grids, every variant and path -------------------------
+
+SIZES = [(1, 1), (1, 7), (7, 1), (2, 2), (5, 3), (63, 65), (129, 3), (300, 301), (1030, 9),
+         (2053, 5)]
+
+
+@pytest.mark.parametrize("nx,ny", SIZES, ids=["%dx%d" % s for s in SIZES])
+@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_small_grids_bit_exact(pk, nx, ny, variant, path, poisson):
+    u0 = inputs.random_field(nx, ny, seed=100 + nx + 7 * ny)
+    f = inputs.uniform_pm1(200 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    n, ce = 7, 3
+    want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=1e-30, check_every=ce)
+    got, info = run_pk(pk, u0, f, n, 1e-30, ce, path=path, variant=variant)
+    assert info["variant"] == variant
+    assert_same_bits(got, want)
+    check_info(info, oinfo)
+
+
+def test_worked_4x4(pk):
+    u0 = np.zeros((4, 4), np.float32)
+    u0[0] = [0, 4, 8, 0]
+    want = np.array([[0, 4, 8, 0], [0, 1.5, 2.25, 0], [0, 0.25, 0.5, 0], [0, 0, 0, 0]], np.float32)
+    for variant in (1, 2):
+        for path in ("persistent", "launch"):
+            got, info = run_pk(pk, u0, None, 2, 1e-30, 1, path=path, variant=variant)
+            assert_same_bits(got, want)
+            assert info["res0"] == np.sqrt(80.0) and info["n_checks"] == 3
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
+def test_flags_problem_grid_and_alternating_direction(pk, variant):
+    nx, ny = 2100, 37
+    u0 = inputs.random_field(nx, ny, seed=77)
+    f = inputs.uniform_pm1(78, nx * ny).reshape(ny, nx)
+    want, oinfo = oracle.jacobi_run(u0, f=f, n=12, tol=1e-30, check_every=4)
+    for flags in (pk.PK_FLAG_LAUNCH_PROBLEM_GRID, pk.PK_FLAG_ALTERNATE_DIRECTION, 3):
+        for path in ("persistent", "launch"):
+            got, info = run_pk(pk, u0, f, 12, 1e-30, 4, path=path, variant=variant, flags=flags)
+            assert_same_bits(got, want)
+            check_info(info, oinfo)
+
+
+def test_persistent_and_launch_residuals_identical(pk):
+    nx, ny = 700, 333
+    u0 = inputs.random_field(nx, ny, seed=5)
+    for variant in (1, 2):
+        _, a = run_pk(pk, u0, None, 30, 1e-30, 5, path="persistent", variant=variant)
+        _, b = run_pk(pk, u0, None, 30, 1e-30, 5, path="launch", variant=variant)
+        assert a["grid"] == b["grid"]
+        assert a["res0"] == b["res0"] and a["res_last"] == b["res_last"]
+        assert a["res_max_last"] == b["res_max_last"]
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+def test_early_exit_16x16_poisson(pk, variant, path):
+    n = 16
+    f = inputs.uniform_pm1(7, n * n).reshape(n, n)
+    u0 = np.zeros((n + 2, n + 2), np.float32)
+    want, oinfo = oracle.jacobi_run(u0, f=f, n=100000, tol=1e-4, check_every=10)
+    assert 0 < oinfo.sweeps_done < 100000
+    got, info = run_pk(pk, u0, f, 100000, 1e-4, 10, path=path, variant=variant)
+    check_info(info, oinfo)
+    assert_same_bits(got, want)
+
+
+def test_zero_sweeps_and_field_roundtrip(pk):
+    nx, ny = 33, 17
+    u0 = inputs.random_field(nx, ny, seed=3)
+    ctx = pk.pk_create(nx, ny, u0, None)
+    try:
+        info = pk.pk_run_sweeps(ctx, 0)
+        assert info["sweeps_done"] == 0 and info["n_checks"] == 0
+        assert_same_bits(pk.pk_get_field(ctx), u0)
+        info = pk.pk_run_sweeps(ctx, 0, 0.5, 4)
+        assert info["n_checks"] == 1 and info["sweeps_done"] == 0
+        assert info["res0"] == pytest.approx(oracle.residual(u0)[0], rel=1e-10)
+        u1 = inputs.random_field(nx, ny, seed=4)
+        pk.pk_set_field(ctx, u1)
+        assert_same_bits(pk.pk_get_field(ctx), u1)
+        # resume: 3 + 4 sweeps == 7 sweeps (Jacobi is memoryless)
+        pk.pk_run_sweeps(ctx, 3)
+        pk.pk_run_sweeps_launch(ctx, 4)
+        want, _ = oracle.jacobi_run(u1, n=7)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_create_device_with_torch_buffers(pk):
+    import torch
+    nx, ny, n = 1500, 40, 9
+    pitch, _, _ = pk.pk_layout(nx, ny)
+    u0 = inputs.random_field(nx, ny, seed=12)
+    f = inputs.uniform_pm1(13, nx * ny).reshape(ny, nx)
+    dev = torch.device("cuda", 0)
+    ua = torch.zeros((ny + 2, pitch), dtype=torch.float32, device=dev)
+    ub = torch.zeros_like(ua)
+    ua[:, 3:nx + 5] = torch.from_numpy(u0).to(dev)
+    ub[:, 3:nx + 5] = ua[:, 3:nx + 5]
+    fd = torch.from_numpy(f).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize()
+    for variant in (1, 2):
+        ua2, ub2 = ua.clone(), ub.clone()
+        torch.cuda.synchronize()
+        opt = pk.pk_options_default(variant=variant)
+        ctx = pk.pk_create_device(nx, ny, ua2.data_ptr(), ub2.data_ptr(), pitch, fd.data_ptr(),
+                                  stream.cuda_stream, opt)
+        try:
+            info = pk.pk_run_sweeps(ctx, n)
+            cur = info["current"]
+            got = (ua2, ub2)[cur][:, 3:nx + 5].cpu().numpy()
+        finally:
+            pk.pk_destroy(ctx)
+        want, _ = oracle.jacobi_run(u0, f=f, n=n)
+        assert_same_bits(got, want)
+
+
+# ---- the five workloads ------------------------------------------------------
+
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+def test_laplace_top_edge_64(pk, path):
+    w = inputs.workload_laplace_top_edge(64)
+    want, _ = oracle.jacobi_run(w["u0"], n=100)
+    got, info = run_pk(pk, w["u0"], None, 100, path=path)
+    assert info["sweeps_done"] == 100
+    assert_same_bits(got, want)
+
+
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+def test_laplace_random_512(pk, path):
+    w = inputs.workload_laplace_random(512, seed=1)
+    want, _ = oracle.jacobi_run(w["u0"], n=1000, threads=THREADS)
+    got, info = run_pk(pk, w["u0"], None, 1000, path=path)
+    assert info["sweeps_done"] == 1000
+    assert_same_bits(got, want)
+
+
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+def test_poisson_4096_residual_every_10(pk, path):
+    w = inputs.workload_poisson_random_source(4096, seed=2)
+    want, oinfo = oracle.jacobi_run(w["u0"], f=w["f"], n=2000, tol=1e-4, check_every=10,
+                                    threads=THREADS)
+    got, info = run_pk(pk, w["u0"], w["f"], 2000, 1e-4, 10, path=path)
+    check_info(info, oinfo)
+    assert_same_bits(got, want)
+
+
+def test_laplace_random_16384_full_field(pk):
+    w = inputs.workload_laplace_random(16384, seed=3)
+    got, info = run_pk(pk, w["u0"], None, 100)
+    assert info["sweeps_done"] == 100 and info["variant"] == 2
+    want, _ = oracle.jacobi_run(w["u0"], n=100, threads=THREADS)
+    assert_same_bits(got, want)
+
+
+def _task_setup(pk, w):
+    import torch
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(w["x"]).to(dev)
+    y = torch.from_numpy(w["y"]).to(dev)
+    torch.cuda.synchronize()
+    jac = pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=1)
+    ax = pk.make_task(pk.PK_TASK_AXPY, a=0.5, x=x.data_ptr(), y=y.data_ptr(), length=x.numel())
+    return x, y, [jac, ax]
+
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["mailbox", "launch"])
+def test_task_queue_10000(pk, mode):
+    w = inputs.workload_task_queue(256, 65536, seed=4)
+    x, y, tasks = _task_setup(pk, w)
+    ctx = pk.pk_create(256, 256, w["u0"], None)
+    try:
+        samples = pk.pk_bench_tasks(ctx, mode, tasks, 10000)
+        assert (samples > 0).all()
+        if mode == 0:
+            assert pk.pk_shutdown(ctx) == 0
+        field = pk.pk_get_field(ctx)
+    finally:
+        pk.pk_destroy(ctx)
+    import torch
+    torch.cuda.synchronize()
+    want_field, want_y = oracle.task_sequence(w["u0"], w["x"], w["y"], 10000)
+    assert_same_bits(field, want_field)
+    assert_same_bits(y.cpu().numpy()[None, :], want_y[None, :], "y")
+
+
+# ---- mailbox semantics -----------------------------------------------------------
+
+def test_mailbox_pipelined_ring_and_restart(pk):
+    nx = ny = 96
+    u0 = inputs.random_field(nx, ny, seed=21)
+    ctx = pk.pk_create(nx, ny, u0, None, pk.pk_options_default(mailbox_depth=4))
+    try:
+        seqs = []
+        for k in range(40):
+            t = pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=1 + (k % 3))
+            while True:
+                try:
+                    seqs.append(pk.pk_submit_task(ctx, t))
+                    break
+                except pk.PkError as e:
+                    assert e.code == pk.PK_EBUSY
+        assert seqs == list(range(1, 41))
+        pk.pk_wait(ctx, seqs[-1], 10.0)
+        assert pk.pk_poll(ctx, seqs[-1]) == 1
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 1)
+        assert e.value.code == pk.PK_EBUSY
+        assert pk.pk_shutdown(ctx) == 0
+        total = sum(1 + (k % 3) for k in range(40))
+        want, _ = oracle.jacobi_run(u0, n=total)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+        # restart: the task kernel relaunches on the next submit
+        s = pk.pk_submit_task(ctx, pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=5))
+        assert s == 42  # 41 was the STOP
+        pk.pk_wait(ctx, s, 10.0)
+        assert pk.pk_shutdown(ctx) == 0
+        want, _ = oracle.jacobi_run(u0, n=total + 5)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+        # the sweeps path works again once the task kernel is down
+        pk.pk_run_sweeps(ctx, 2)
+        want, _ = oracle.jacobi_run(u0, n=total + 7)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_mailbox_idle_timeout_reports_and_recovers(pk):
+    import time
+    nx = ny = 64
+    u0 = inputs.random_field(nx, ny, seed=22)
+    ctx = pk.pk_create(nx, ny, u0, None, pk.pk_options_default(mailbox_idle_timeout_s=0.2))
+    try:
+        s = pk.pk_submit_task(ctx, pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=3))
+        pk.pk_wait(ctx, s, 10.0)
+        time.sleep(0.6)  # longer than the idle limit: the kernel exits by itself
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_shutdown(ctx)
+        assert e.value.code == pk.PK_ETIMEDOUT
+        want, _ = oracle.jacobi_run(u0, n=3)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+        s = pk.pk_submit_task(ctx, pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=2))
+        pk.pk_wait(ctx, s, 10.0)
+        assert pk.pk_shutdown(ctx) == 0
+        want, _ = oracle.jacobi_run(u0, n=5)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_submit_rejects_bad_tasks(pk):
+    u0 = inputs.random_field(8, 8, seed=1)
+    ctx = pk.pk_create(8, 8, u0, None)
+    try:
+        for t in (pk.make_task(9), pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=0),
+                  pk.make_task(pk.PK_TASK_AXPY, a=1.0, x=None, y=None, length=4)):
+            with pytest.raises(pk.PkError) as e:
+                pk.pk_submit_task(ctx, t)
+            assert e.value.code == pk.PK_EINVAL
+        assert pk.pk_shutdown(ctx) == 0  # never started
+    finally:
+        pk.pk_destroy(ctx)
+
+
+# ---- barrier ------------------------------------------------------------------
+
+def test_barrier_stress_zero_stale(pk):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    u0 = inputs.random_field(512, 512, seed=1)
+    ctx = pk.pk_create(512, 512, u0, None)
+    try:
+        cap = pk.pk_get_plan(ctx)["coop_max"]
+        for grid in sorted({1, 2, 7, sms, 2 * sms, cap}):
+            rounds = 2000
+            sums, stale = pk.pk_barrier_stress(ctx, grid, rounds, 32)
+            assert stale == 0, "grid %d: %d stale words" % (grid, stale)
+            assert np.array_equal(sums, oracle.barrier_stress_expected(grid, rounds, 32)), grid
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_barrier_and_cg_sync_microbenchmarks(pk):
+    u0 = inputs.random_field(512, 512, seed=1)
+    ctx = pk.pk_create(512, 512, u0, None)
+    try:
+        ours = pk.pk_bench_barrier(ctx, 0, 0, 2000)
+        cgs = pk.pk_bench_barrier(ctx, 1, 0, 2000)
+        assert ours > 0 and cgs > 0
+        sync_each, queued = pk.pk_bench_launch_floor(ctx, 200)
+        assert sync_each > 0 and queued > 0
+    finally:
+        pk.pk_destroy(ctx)
+
+
+@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
+def test_barrier_timeout_is_reported_not_hung(pk, variant):
+    """Fault injection on the host's say-so: one CTA leaves without arriving;
+    the others give up after the (short) limit and the call returns
+    PK_ETIMEDOUT.  The device stays usable."""
+    nx, ny = (512, 512) if variant == 1 else (3000, 200)
+    u0 = inputs.random_field(nx, ny, seed=31)
+    opt = pk.pk_options_default(variant=variant, barrier_timeout_s=0.2, debug_skip_arrival_cta=1,
+                                debug_skip_arrival_at=3)
+    ctx = pk.pk_create(nx, ny, u0, None, opt)
+    try:
+        assert pk.pk_get_plan(ctx)["grid"] >= 2
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 50)
+        assert e.value.code == pk.PK_ETIMEDOUT
+    finally:
+        pk.pk_destroy(ctx)
+    want, _ = oracle.jacobi_run(u0, n=9)
+    got, _ = run_pk(pk, u0, None, 9, variant=variant)
+    assert_same_bits(got, want)
+
+
+def test_oversubscribed_grid_is_refused(pk):
+    u0 = inputs.random_field(256, 256, seed=2)
+    ctx = pk.pk_create(256, 256, u0, None)
+    cap = pk.pk_get_plan(ctx)["coop_max"]
+    pk.pk_destroy(ctx)
+    ctx = pk.pk_create(256, 256, u0, None, pk.pk_options_default(grid_override=cap + 1))
+    try:
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 3)
+        assert e.value.code == pk.PK_ENORESIDENT
+        # the per-launch path does not need co-residency
+        pk.pk_run_sweeps_launch(ctx, 3)
+        want, _ = oracle.jacobi_run(u0, n=3)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
