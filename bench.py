@@ -46,6 +46,8 @@ WORKLOADS = {
     "poisson-4096x4096-2000sweeps-res10": (4096, 2, 2000, True, 1e-4, 10),
     "laplace-512x512-1000sweeps": (512, 1, 1000, False, 0.0, 0),
     "laplace-64x64-topedge-100sweeps": (64, None, 100, False, 0.0, 0),
+    # profiling-sized case: two 268 MB buffers (> L2), short enough for ncu replays
+    "laplace-8192x8192-10sweeps": (8192, 3, 10, False, 0.0, 0),
 }
 DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 
@@ -325,7 +327,7 @@ def latency_extras(pk):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["pk", "reference"], default="pk")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)

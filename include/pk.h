@@ -63,6 +63,12 @@ extern "C" {
 /* ---- option flags ------------------------------------------------------ */
 #define PK_FLAG_LAUNCH_PROBLEM_GRID 0x1u /* pk_run_sweeps_launch: one thread per float4, not the persistent grid */
 #define PK_FLAG_ALTERNATE_DIRECTION 0x2u /* STREAM: odd sweeps walk each band bottom-up (reuses L2) */
+#define PK_FLAG_PROFILE_BARRIER 0x4u     /* record each CTA's total barrier wait (pk_barrier_wait_ns) */
+
+/* ---- grid barrier constructions ([P2] "The barrier is a counter and a
+ * generation") -------------------------------------------------------------- */
+#define PK_BARRIER_GENERATION 0 /* count word + generation word; last arriver resets and bumps */
+#define PK_BARRIER_COUNTER 1    /* one monotonic count word; generation = count / CTAs */
 
 /* ---- task kinds for the mailbox ---------------------------------------- */
 #define PK_TASK_NOP 0
@@ -111,9 +117,16 @@ typedef struct {
     int32_t mailbox_depth;            /* task ring slots, 1..1024 (default 64) */
     int32_t debug_skip_arrival_cta;   /* fault injection: this CTA leaves at barrier ... (-1 = off) */
     int32_t debug_skip_arrival_at;    /* ... number debug_skip_arrival_at (0-based) without arriving */
-    uint32_t flags;                   /* PK_FLAG_* */
+    uint32_t flags;                   /* PK_FLAG_* (default PK_FLAG_ALTERNATE_DIRECTION) */
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
-    int32_t reserved[7];
+    int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
+    int32_t stream_config;            /* STREAM shape, -1 = default (3).  Index into
+                                         {float4 groups per thread, TMA ring depth}:
+                                         0 {1,8}  1 {1,16}  2 {2,8}  3 {4,4}  4 {4,8}  5 {2,16};
+                                         a strip is 1024 x groups columns wide.  A shape
+                                         whose ring does not fit in shared memory is
+                                         refused with PK_EINVAL. */
+    int32_t reserved[5];
 } pk_options;
 
 /* Fill opt with the defaults above. */
@@ -223,19 +236,36 @@ const char *pk_last_error(const pk_ctx *ctx);
 int pk_bench_launch_floor(pk_ctx *ctx, int iters, double *us_sync_each, double *us_queued);
 
 /* Barrier cost: a cooperative kernel with `grid` CTAs of 256 threads that
- * only runs n_barriers barriers; kind 0 = libpk's generation-counter
- * barrier, kind 1 = cooperative_groups grid.sync().  *us_total is the
- * kernel's device time (CUDA events), launch included.  grid 0 = the
- * persistent sweep grid. */
+ * only runs n_barriers barriers; kind 0 = libpk's PK_BARRIER_GENERATION,
+ * kind 1 = cooperative_groups grid.sync(), kind 2 = libpk's
+ * PK_BARRIER_COUNTER.  *us_total is the kernel's device time (CUDA events),
+ * launch included.  grid 0 = the persistent sweep grid. */
 int pk_bench_barrier(pk_ctx *ctx, int kind, int grid, int64_t n_barriers, double *us_total);
+
+/* Per-CTA total barrier wait (ns, global timer) of the last pk_run_sweeps
+ * made with PK_FLAG_PROFILE_BARRIER; copies min(n, grid) entries to the HOST
+ * array per_cta and returns the count, or a negative code. */
+int pk_barrier_wait_ns(pk_ctx *ctx, int64_t *per_cta, int n);
 
 /* Barrier stress ([P2] "Failure modes that only appear at this scale"):
  * `rounds` rounds in which every CTA writes `words` (1..32) stamped words on
  * its own 128-byte line, crosses the barrier, and reads three other CTAs'
- * lines, counting stale words and summing what it saw.  checksums (host,
- * grid entries, may be NULL) and *stale (may be NULL) are filled. */
+ * lines, counting stale words and summing what it saw.  Uses the
+ * context's barrier construction.  checksums (host, grid entries, may be
+ * NULL) and *stale (may be NULL) are filled. */
 int pk_barrier_stress(pk_ctx *ctx, int grid, int rounds, int words, uint64_t *checksums,
                       int64_t *stale);
+
+/* The same rounds with 32 words per line, but each CTA fetches its peers'
+ * lines with TMA bulk copies (async proxy) into shared memory after the
+ * barrier -- the path the STREAM sweep uses to read rows its neighbours
+ * wrote with ordinary stores.  mode bit 0: the copying thread makes its own
+ * gpu-scope acquire before its proxy fence; bit 1: writers fence the
+ * generic proxy against the async proxy after their stores.  mode 3 is the
+ * protocol the STREAM sweep uses; the others are negative controls (they
+ * may count stale words; they cannot hang or fault). */
+int pk_barrier_stress_tma(pk_ctx *ctx, int grid, int rounds, int mode, uint64_t *checksums,
+                          int64_t *stale);
 
 /* Round-trip timing of a task list, host clock (ns per task into
  * samples[0..n_tasks-1]).  mode 0: through the mailbox (submit, then poll

@@ -115,6 +115,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
+// Generic-proxy reads of a shared-memory buffer -> a later async-proxy (TMA)
+// write of the same buffer.  Without it a pending ld.shared can be
+// overtaken by the refill that the mbarrier release allows.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // ---------------------------------------------------------------------------
 // Error recording: the first error wins; every spin sees abort_flag.
@@ -133,26 +139,75 @@ __device__ __forceinline__ bool aborted(const BarrierState *b) {
 
 // ---------------------------------------------------------------------------
 // Grid barrier ("Grid-Wide Barriers ...", section "The barrier is a counter
-// and a generation").  Called by every thread of every CTA.  Thread 0 of
-// each CTA reads the generation, arrives on the counter with an acq_rel
-// atomic (release: this CTA's writes, ordered before it by __syncthreads,
-// are published; acquire: the last arriver sees every CTA's writes).  The
-// last arriver resets the counter and then bumps the generation with a
-// release store -- the single writer does both, in that order.  The others
-// spin with acquire loads on the generation, bounded by timeout_ns on the
-// global timer; on expiry they record kETimedOut and raise abort_flag.
-// Returns false when the grid is aborting; the caller must then return.
+// and a generation"), called by every thread of every CTA.  After
+// __syncthreads, thread 0 arrives with a release atomic (its CTA's writes,
+// ordered before it by the block barrier, are published); a waiter spins on
+// relaxed loads and, once released, issues one acquire fence, so the reads
+// that follow see every CTA's writes.  Two constructions:
 //
+//   kBarrierGeneration -- a count word and a generation word.  The last
+//     arriver (its atomic returned nblocks-1) acquires, resets the count and
+//     then bumps the generation with a release store: one writer does both,
+//     in that order, so no arrival of the next round can be lost or counted
+//     twice ("Failure modes that only appear at this scale").  The others
+//     wait for the generation to change.  Each CTA keeps the generation it
+//     is in, read once at kernel start.
+//   kBarrierCounter -- one monotonic count word; barrier k of a launch is
+//     complete when count - base reaches (k+1) * nblocks (wrapping 32-bit
+//     arithmetic), so the generation is count / nblocks and nothing is ever
+//     reset.  base is the word's value at launch, tracked by the host.
+//
+// Every wait is bounded by timeout_ns on the global timer and ends early on
+// abort_flag; on expiry the CTA records kETimedOut and raises abort_flag.
+// Returns false when the grid is aborting; the caller must then return.
 // skip: fault injection -- this CTA leaves without arriving (host-driven
-// test of the timeout; it never faults the GPU).
+// test of the timeout path; it never faults the GPU).
+constexpr unsigned kBarrierGeneration = 0;
+constexpr unsigned kBarrierCounter = 1;
+
 struct BarrierCtl {
     BarrierState *state;
     unsigned nblocks;
+    unsigned kind;
     uint64_t timeout_ns;
-    int skip_cta;      // -1 = off
-    int skip_at;       // barrier index at which skip_cta leaves
-    int index;         // barriers passed so far by this CTA
+    int skip_cta;       // -1 = off
+    int skip_at;        // barrier index at which skip_cta leaves
+    int index;          // barriers completed by this CTA
+    unsigned base;      // kBarrierCounter: count at launch
+    unsigned gen;       // kBarrierGeneration: current generation (thread 0)
+    int profile;        // accumulate wait time in spin_ns
+    unsigned long long spin_ns;
 };
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Call once at kernel start, before the first grid_barrier.
+__device__ __forceinline__ void barrier_begin(BarrierCtl &ctl) {
+    if (threadIdx.x == 0 && ctl.kind == kBarrierGeneration)
+        ctl.gen = ld_relaxed_gpu(&ctl.state->generation.v);
+    ctl.spin_ns = 0ull;
+}
+
+// Spin until pred() holds; false on timeout (error recorded) or abort.
+template <class Pred>
+__device__ __forceinline__ bool bounded_spin(BarrierState *b, uint64_t timeout_ns, int site,
+                                             Pred pred) {
+    if (pred()) return true;
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    for (;;) {
+        if (pred()) return true;
+        if ((++spins & 31u) == 0u) {
+            if (aborted(b)) return false;
+            if (globaltimer_ns() - t0 > timeout_ns) {
+                record_error(b, kETimedOut, site);
+                return false;
+            }
+        }
+    }
+}
 
 __device__ __forceinline__ bool grid_barrier(BarrierCtl &ctl) {
     __shared__ int s_ok;
@@ -160,34 +215,34 @@ __device__ __forceinline__ bool grid_barrier(BarrierCtl &ctl) {
     if (threadIdx.x == 0) {
         int ok = 1;
         BarrierState *b = ctl.state;
+        const uint64_t t_in = ctl.profile ? globaltimer_ns() : 0ull;
         if ((int)blockIdx.x == ctl.skip_cta && ctl.index == ctl.skip_at) {
             ok = 0;  // leave without arriving; the others must time out
-        } else if (aborted(b)) {
-            ok = 0;
-        } else {
-            const unsigned gen = ld_relaxed_gpu(&b->generation.v);
-            const unsigned old = atom_add_acq_rel_gpu(&b->count.v, 1u);
-            if (old == ctl.nblocks - 1u) {
-                st_relaxed_gpu(&b->count.v, 0u);
-                st_release_gpu(&b->generation.v, gen + 1u);
-            } else {
-                const uint64_t t0 = globaltimer_ns();
-                unsigned spins = 0;
-                while (ld_acquire_gpu(&b->generation.v) == gen) {
-                    if ((++spins & 255u) == 0u) {
-                        if (aborted(b)) {
-                            ok = 0;
-                            break;
-                        }
-                        if (globaltimer_ns() - t0 > ctl.timeout_ns) {
-                            record_error(b, kETimedOut, kSiteBarrier);
-                            ok = 0;
-                            break;
-                        }
-                    }
-                }
+        } else if (ctl.kind == kBarrierCounter) {
+            const unsigned target = ctl.base + (unsigned)(ctl.index + 1) * ctl.nblocks;
+            const unsigned old = atom_add_release_gpu(&b->count.v, 1u);
+            if (old + 1u != target) {
+                ok = bounded_spin(b, ctl.timeout_ns, kSiteBarrier, [&] {
+                    return (int)(ld_relaxed_gpu(&b->count.v) - target) >= 0;
+                });
             }
+            fence_acq_rel_gpu();
+        } else {
+            const unsigned old = atom_add_release_gpu(&b->count.v, 1u);
+            if (old == ctl.nblocks - 1u) {
+                fence_acq_rel_gpu();
+                st_relaxed_gpu(&b->count.v, 0u);
+                st_release_gpu(&b->generation.v, ctl.gen + 1u);
+            } else {
+                const unsigned gen = ctl.gen;
+                ok = bounded_spin(b, ctl.timeout_ns, kSiteBarrier, [&] {
+                    return ld_relaxed_gpu(&b->generation.v) != gen;
+                });
+                fence_acq_rel_gpu();
+            }
+            ctl.gen += 1u;
         }
+        if (ctl.profile) ctl.spin_ns += globaltimer_ns() - t_in;
         s_ok = ok;
     }
     __syncthreads();

@@ -73,11 +73,15 @@ struct pk_ctx {
     long long l2_bytes = 0;
     pk_options opt{};
     int variant = kVariantDirect;
+    int stream_cfg = 0;  // STREAM configuration index
     int grid = 1;        // persistent sweep grid
     int coop_max = 1;    // occupancy x SMs for the sweep kernel
     int part_cap = 0;    // partial slots per parity
     Scratch *scratch = nullptr;
     Partial *partials = nullptr;
+    unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
+    int spin_valid = 0;                     // entries written by the last profiled run
+    unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
     unsigned *stress_lines = nullptr;
     int stress_cap = 0;
     unsigned long long *stress_out = nullptr;
@@ -150,6 +154,9 @@ void fill_default(pk_options *o) {
     o->mailbox_depth = 64;
     o->debug_skip_arrival_cta = -1;
     o->debug_skip_arrival_at = 0;
+    o->barrier_kind = PK_BARRIER_COUNTER;
+    o->stream_config = -1;
+    o->flags = PK_FLAG_ALTERNATE_DIRECTION;
 }
 
 int read_options(pk_ctx *ctx, const pk_options *opt) {
@@ -171,6 +178,10 @@ int read_options(pk_ctx *ctx, const pk_options *opt) {
         return fail(ctx, PK_EINVAL, "timeout too large");
     if (o.mailbox_depth < 1 || o.mailbox_depth > 1024)
         return fail(ctx, PK_EINVAL, "mailbox_depth must be in 1..1024");
+    if (o.barrier_kind != PK_BARRIER_GENERATION && o.barrier_kind != PK_BARRIER_COUNTER)
+        return fail(ctx, PK_EINVAL, "unknown barrier_kind %d", o.barrier_kind);
+    if (o.stream_config < -1 || o.stream_config >= kNumStreamConfigs)
+        return fail(ctx, PK_EINVAL, "stream_config %d out of range", o.stream_config);
     return PK_OK;
 }
 
@@ -192,18 +203,25 @@ int coop_capacity(pk_ctx *ctx, const void *fn, int threads, size_t smem, int *pe
 long long direct_units(const pk_ctx *ctx) { return (long long)ctx->ny * ((ctx->nx + 3) / 4); }
 
 long long stream_rows(const pk_ctx *ctx) {
-    return (long long)((ctx->nx + kTW - 1) / kTW) * ctx->ny;
+    const int tw = stream_tw(ctx->stream_cfg);
+    return (long long)((ctx->nx + tw - 1) / tw) * ctx->ny;
 }
+
+constexpr int kDefaultStreamConfig = 3;  // 4096-column strips, 4-deep ring, 1 CTA/SM
 
 int ensure_partials(pk_ctx *ctx, int grid) {
     if (grid <= ctx->part_cap) return PK_OK;
     if (ctx->partials) {
         PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
         cudaFree(ctx->partials);
+        cudaFree(ctx->spin_ns);
         ctx->partials = nullptr;
+        ctx->spin_ns = nullptr;
         ctx->part_cap = 0;
+        ctx->spin_valid = 0;
     }
     PK_TRY(ctx, cudaMalloc(&ctx->partials, sizeof(Partial) * 2 * (size_t)grid));
+    PK_TRY(ctx, cudaMalloc(&ctx->spin_ns, sizeof(unsigned long long) * (size_t)grid));
     ctx->part_cap = grid;
     return PK_OK;
 }
@@ -217,9 +235,13 @@ int plan(pk_ctx *ctx) {
     if (v == kVariantDirect && direct_units(ctx) >= (1LL << 31))
         return fail(ctx, PK_EINVAL, "grid too large for the DIRECT variant");
     ctx->variant = v;
+    ctx->stream_cfg = ctx->opt.stream_config >= 0 ? ctx->opt.stream_config : kDefaultStreamConfig;
+    if (v == kVariantStream && !stream_config_ok(ctx->stream_cfg, ctx->poisson))
+        return fail(ctx, PK_EINVAL, "stream_config %d does not fit in shared memory", ctx->stream_cfg);
     int per_sm = 0;
-    const int cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson), block_threads(v),
-                                  dyn_smem(v, ctx->poisson), &per_sm);
+    const int cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, ctx->stream_cfg),
+                                  block_threads(v), dyn_smem(v, ctx->poisson, ctx->stream_cfg),
+                                  &per_sm);
     if (cap < 0) return PK_ECUDA;
     if (cap == 0) return fail(ctx, PK_ENORESIDENT, "sweep kernel does not fit on an SM");
     ctx->coop_max = cap;
@@ -260,6 +282,10 @@ SweepParams base_params(pk_ctx *ctx) {
     p.skip_at = ctx->opt.debug_skip_arrival_at;
     p.alt_dir = (ctx->opt.flags & PK_FLAG_ALTERNATE_DIRECTION) ? 1 : 0;
     p.run_id = ++ctx->run_id;
+    p.barrier_kind = ctx->opt.barrier_kind;
+    p.bar_base = ctx->sweep_bar_base;
+    p.profile = (ctx->opt.flags & PK_FLAG_PROFILE_BARRIER) ? 1 : 0;
+    p.spin_ns = ctx->spin_ns;
     return p;
 }
 
@@ -526,18 +552,23 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.tol = tol;
     p.check_every = check_every;
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, ctx->grid, p, ctx->stream);
+    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, ctx->stream_cfg, ctx->grid, p,
+                                      ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
                                 ctx->stream));
+    ctx->spin_valid = 0;
     int rc = bar_status(ctx, p.bar, "pk_run_sweeps");
     if (rc != PK_OK) {
+        ctx->sweep_bar_base = 0;  // bar_status zeroed the barrier words
         fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, ctx->grid);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
         return fail(ctx, PK_EDEVICE, "pk_run_sweeps: kernel did not report its result");
+    ctx->sweep_bar_base = ctx->h_info->bar_count_end;
+    if (p.profile) ctx->spin_valid = ctx->grid;
     ctx->cur = ctx->h_info->cur;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
               ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, ctx->grid);
@@ -576,7 +607,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
         p.pass_store = k < n ? 1 : 0;
         p.pass_parity = n_checks & 1;
         p.pass_k = k;
-        cudaError_t e = launch_once(ctx->variant, ctx->poisson, grid, p, ctx->stream);
+        cudaError_t e = launch_once(ctx->variant, ctx->poisson, ctx->stream_cfg, grid, p, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "sweep launch");
         if (check) {
             e = launch_finalize(ctx->variant, grid, p, &ctx->scratch->res, ctx->stream);
@@ -677,6 +708,8 @@ int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out) {
         tp.sp = base_params(ctx);
         tp.sp.bar = &ctx->scratch->bar_task_inner;
         tp.sp.skip_cta = -1;
+        tp.sp.bar_base = 0;  // zeroed just above
+        tp.sp.profile = 0;
         tp.mbox = ctx->mbox_dev;
         tp.dev_desc = &ctx->scratch->desc;
         tp.tb = &ctx->scratch->bar_task;
@@ -805,14 +838,37 @@ int pk_bench_launch_floor(pk_ctx *ctx, int iters, double *us_sync_each, double *
     return PK_OK;
 }
 
+namespace {
+BarrierCtl bench_ctl(pk_ctx *ctx, int grid, int kind) {
+    BarrierCtl ctl;
+    std::memset(&ctl, 0, sizeof(ctl));
+    ctl.state = &ctx->scratch->bar_bench;
+    ctl.nblocks = (unsigned)grid;
+    ctl.kind = (unsigned)kind;
+    ctl.timeout_ns = ns_of(ctx->opt.barrier_timeout_s);
+    ctl.skip_cta = -1;
+    return ctl;
+}
+}  // namespace
+
+int pk_barrier_wait_ns(pk_ctx *ctx, int64_t *per_cta, int n) {
+    if (!ctx || n < 0 || (n > 0 && !per_cta)) return PK_EINVAL;
+    const int m = n < ctx->spin_valid ? n : ctx->spin_valid;
+    if (m > 0)
+        PK_TRY(ctx, cudaMemcpy(per_cta, ctx->spin_ns, sizeof(int64_t) * (size_t)m,
+                               cudaMemcpyDeviceToHost));
+    return m;
+}
+
 int pk_bench_barrier(pk_ctx *ctx, int kind, int grid, int64_t n_barriers, double *us_total) {
-    if (!ctx || (kind != 0 && kind != 1) || grid < 0 || n_barriers < 0) return PK_EINVAL;
+    if (!ctx || kind < 0 || kind > 2 || grid < 0 || n_barriers < 0) return PK_EINVAL;
     if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_bench_barrier: the task kernel is live");
     if (grid == 0) grid = ctx->grid;
     PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_bench, 0, sizeof(BarrierState), ctx->stream));
-    BarrierCtl ctl{&ctx->scratch->bar_bench, (unsigned)grid, ns_of(ctx->opt.barrier_timeout_s), -1, 0, 0};
+    const int bkind = kind == 2 ? (int)kBarrierCounter : (int)kBarrierGeneration;
+    BarrierCtl ctl = bench_ctl(ctx, grid, bkind);
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_barrier_only(kind, grid, ctl, n_barriers, ctx->stream);
+    cudaError_t e = launch_barrier_only(kind == 1 ? 1 : 0, grid, ctl, n_barriers, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(barrier)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     int rc = bar_status(ctx, &ctx->scratch->bar_bench, "pk_bench_barrier");
@@ -841,11 +897,46 @@ int pk_barrier_stress(pk_ctx *ctx, int grid, int rounds, int words, uint64_t *ch
     PK_TRY(ctx, cudaMemsetAsync(ctx->stress_out, 0, sizeof(unsigned long long) * ((size_t)grid + 1),
                                 ctx->stream));
     PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_bench, 0, sizeof(BarrierState), ctx->stream));
-    BarrierCtl ctl{&ctx->scratch->bar_bench, (unsigned)grid, ns_of(ctx->opt.barrier_timeout_s), -1, 0, 0};
+    BarrierCtl ctl = bench_ctl(ctx, grid, ctx->opt.barrier_kind);
     cudaError_t e = launch_stress(grid, ctl, rounds, words, ctx->stress_lines, ctx->stress_out + 1,
                                   ctx->stress_out, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(stress)");
     int rc = bar_status(ctx, &ctx->scratch->bar_bench, "pk_barrier_stress");
+    if (rc != PK_OK) return rc;
+    unsigned long long st = 0;
+    PK_TRY(ctx, cudaMemcpy(&st, ctx->stress_out, sizeof(st), cudaMemcpyDeviceToHost));
+    if (stale) *stale = (int64_t)st;
+    if (checksums)
+        PK_TRY(ctx, cudaMemcpy(checksums, ctx->stress_out + 1, sizeof(unsigned long long) * (size_t)grid,
+                               cudaMemcpyDeviceToHost));
+    return PK_OK;
+}
+
+int pk_barrier_stress_tma(pk_ctx *ctx, int grid, int rounds, int mode, uint64_t *checksums,
+                          int64_t *stale) {
+    if (!ctx || grid < 0 || rounds < 0 || mode < 0 || mode > 7) return PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_barrier_stress_tma: the task kernel is live");
+    if (grid == 0) grid = ctx->grid;
+    if (grid > ctx->stress_cap) {
+        cudaFree(ctx->stress_lines);
+        cudaFree(ctx->stress_out);
+        ctx->stress_lines = nullptr;
+        ctx->stress_out = nullptr;
+        ctx->stress_cap = 0;
+        PK_TRY(ctx, cudaMalloc(&ctx->stress_lines, sizeof(unsigned) * 2 * kStressWords * (size_t)grid));
+        PK_TRY(ctx, cudaMalloc(&ctx->stress_out, sizeof(unsigned long long) * ((size_t)grid + 1)));
+        ctx->stress_cap = grid;
+    }
+    PK_TRY(ctx, cudaMemsetAsync(ctx->stress_lines, 0, sizeof(unsigned) * 2 * kStressWords * (size_t)grid,
+                                ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->stress_out, 0, sizeof(unsigned long long) * ((size_t)grid + 1),
+                                ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_bench, 0, sizeof(BarrierState), ctx->stream));
+    BarrierCtl ctl = bench_ctl(ctx, grid, ctx->opt.barrier_kind);
+    cudaError_t e = launch_stress_tma(grid, ctl, rounds, ctx->stress_lines, ctx->stress_out + 1,
+                                      ctx->stress_out, mode, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(stress tma)");
+    int rc = bar_status(ctx, &ctx->scratch->bar_bench, "pk_barrier_stress_tma");
     if (rc != PK_OK) return rc;
     unsigned long long st = 0;
     PK_TRY(ctx, cudaMemcpy(&st, ctx->stress_out, sizeof(st), cudaMemcpyDeviceToHost));
@@ -897,7 +988,7 @@ int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int
                 p.pass_check = 0;
                 p.pass_store = 1;
                 p.pass_k = 0;
-                e = launch_once(kVariantDirect, ctx->poisson, ctx->task_grid, p, ctx->stream);
+                e = launch_once(kVariantDirect, ctx->poisson, 0, ctx->task_grid, p, ctx->stream);
                 ctx->cur ^= 1;
             }
         } else if (task.kind == PK_TASK_AXPY) {

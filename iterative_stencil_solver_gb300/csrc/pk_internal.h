@@ -20,6 +20,8 @@ struct DeviceInfo {
     int cur;       // buffer index holding the returned iterate
     int run_id;    // equals SweepParams::run_id once written
     long long task_sweeps;  // task kernel: sweeps run
+    int barriers;  // grid barriers completed (CTA 0)
+    unsigned bar_count_end;  // kBarrierCounter: count word after the last barrier
 };
 
 // Residual result of the per-launch reduction kernel.
@@ -54,6 +56,10 @@ struct SweepParams {
     int skip_cta, skip_at;
     int alt_dir;            // STREAM: odd sweeps walk bands bottom-up
     int run_id;             // echoed into DeviceInfo::run_id
+    int barrier_kind;       // kBarrierGeneration or kBarrierCounter
+    unsigned bar_base;      // kBarrierCounter: count word at launch
+    int profile;            // record per-CTA barrier wait time
+    unsigned long long *spin_ns;  // per-CTA barrier wait time (ns), when profiling
 };
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
@@ -97,13 +103,24 @@ struct TaskParams {
 constexpr int kDirectThreads = 256;
 constexpr int kConsumers = 256;                 // STREAM consumer threads
 constexpr int kStreamThreads = kConsumers + 32; // + one producer warp
-constexpr int kTW = 4 * kConsumers;             // interior columns per strip
-constexpr int kSlotU = kTW + 8;                 // floats of a staged row segment
-constexpr int kStages = 8;                      // TMA ring depth (power of two)
 constexpr int kStressWords = 32;
 
-inline size_t stream_smem_bytes(bool poisson) {
-    return 128 + (size_t)kStages * (size_t)(kSlotU + (poisson ? kTW : 0)) * sizeof(float);
+// STREAM configurations: float4 groups per consumer thread per row (the
+// strip is 4 * qpt * kConsumers columns wide) and TMA ring depth.
+struct StreamConfig {
+    int qpt;
+    int stages;
+};
+constexpr int kNumStreamConfigs = 6;
+constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
+    {1, 8}, {1, 16}, {2, 8}, {4, 4}, {4, 8}, {2, 16}};
+
+inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kConsumers; }
+
+inline size_t stream_smem_bytes(int cfg, bool poisson) {
+    const int tw = stream_tw(cfg);
+    const size_t slot = (size_t)(tw + 8 + (poisson ? tw : 0)) * sizeof(float);
+    return 256 + (size_t)kStreamConfigs[cfg].stages * slot;
 }
 
 // ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
@@ -111,20 +128,24 @@ inline size_t stream_smem_bytes(bool poisson) {
 enum Variant { kVariantDirect = 1, kVariantStream = 2 };
 
 // Once per device: kernel attributes (dynamic shared memory limits).
+// Configurations whose shared memory does not fit are left unset and
+// reported unusable by stream_config_ok.
 cudaError_t prepare_kernels();
+bool stream_config_ok(int cfg, bool poisson);
 
-// Kernel function pointers, for occupancy queries and attribute set-up.
-const void *kernel_persistent(int variant, bool poisson);
-const void *kernel_once(int variant, bool poisson);
+// Kernel function pointers, for occupancy queries.  cfg selects the STREAM
+// configuration (ignored for DIRECT).
+const void *kernel_persistent(int variant, bool poisson, int cfg);
+const void *kernel_once(int variant, bool poisson, int cfg);
 const void *kernel_task(bool poisson);
 const void *kernel_barrier_only(int kind);
 const void *kernel_stress();
 int block_threads(int variant);
-size_t dyn_smem(int variant, bool poisson);
+size_t dyn_smem(int variant, bool poisson, int cfg);
 
-cudaError_t launch_persistent(int variant, bool poisson, int grid, const SweepParams &p,
+cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                               cudaStream_t s);
-cudaError_t launch_once(int variant, bool poisson, int grid, const SweepParams &p,
+cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                         cudaStream_t s);
 cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
                             cudaStream_t s);
@@ -136,6 +157,9 @@ cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long l
 cudaError_t launch_empty(cudaStream_t s);
 cudaError_t launch_barrier_only(int kind, int grid, BarrierCtl ctl, long long n,
                                 cudaStream_t s);
+cudaError_t launch_stress_tma(int grid, BarrierCtl ctl, int rounds, unsigned *lines,
+                              unsigned long long *checksums, unsigned long long *stale, int mode,
+                              cudaStream_t s);
 cudaError_t launch_stress(int grid, BarrierCtl ctl, int rounds, int words, unsigned *lines,
                           unsigned long long *checksums, unsigned long long *stale,
                           cudaStream_t s);

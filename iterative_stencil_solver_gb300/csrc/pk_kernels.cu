@@ -79,34 +79,43 @@ __device__ __forceinline__ void pass_direct_any(const SweepParams &p, const floa
 
 // ===========================================================================
 // STREAM sweep ("Cache-line aware tiling and iteration", the N = 10001
-// variant, rebuilt around TMA): the domain is cut into strips of kTW
-// interior columns; (strip, row) pairs are split evenly, in contiguous
-// runs, over the CTAs.  Each CTA walks its run row by row: one producer
-// thread streams every input row segment (with a 16-byte halo on each side)
-// into a kStages-deep shared-memory ring with cp.async.bulk, and 256
-// consumer threads keep a three-row window (previous, centre, next) in
-// registers, one float4 per thread, so each input row is read from HBM once
-// and from shared memory once.  Edge neighbours come from warp shuffles,
-// and at warp edges from the staged halo.
+// variant, rebuilt around TMA): the domain is cut into strips of TW interior
+// columns; (strip, row) pairs are split evenly, in contiguous runs, over the
+// CTAs.  Each CTA walks its run row by row: one producer thread streams
+// every input row segment (with a 16-byte halo on each side) into a
+// STAGES-deep shared-memory ring with cp.async.bulk, and 256 consumer
+// threads keep a three-row window (previous, centre, next) in registers,
+// QPT float4 groups per thread, so each input row is read from HBM once and
+// from shared memory once.  Edge neighbours come from warp shuffles, and at
+// warp edges from the staged halo.
+template <int QPT, int STAGES, bool POISSON>
+struct SCfg {
+    static constexpr int kQPT = QPT;
+    static constexpr int kStages = STAGES;
+    static constexpr int TW = 4 * QPT * kConsumers;
+    static constexpr int SLOTU = TW + 8;
+    static constexpr int SLOT = SLOTU + (POISSON ? TW : 0);
+    static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
+};
+
 struct StreamState {
     uint64_t *full;
     uint64_t *empty;
     float *slots;
-    int slot_floats;
     unsigned L;     // ring position; producer and consumers advance it alike
     bool broken;    // a pipeline wait expired: stop waiting, finish quickly
 };
 
-__device__ __forceinline__ StreamState stream_setup(unsigned char *smem, bool poisson) {
+template <class C>
+__device__ __forceinline__ StreamState stream_setup(unsigned char *smem) {
     StreamState st;
     st.full = reinterpret_cast<uint64_t *>(smem);
-    st.empty = st.full + kStages;
-    st.slots = reinterpret_cast<float *>(smem + 128);
-    st.slot_floats = kSlotU + (poisson ? kTW : 0);
+    st.empty = st.full + C::kStages;
+    st.slots = reinterpret_cast<float *>(smem + 256);
     st.L = 0;
     st.broken = false;
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < C::kStages; ++i) {
             mbar_init(&st.full[i], 1);
             mbar_init(&st.empty[i], kConsumers / 32);
         }
@@ -121,86 +130,117 @@ __device__ __forceinline__ float4 lds4(const float *p) {
 }
 
 // Producer: input rows ja - dir .. jb + dir of strip columns [col0, col0+cols).
-template <bool POISSON>
+// Run by all 32 lanes of the producer warp, which stays converged: lane 0
+// waits and issues, every lane meets at __syncwarp each row, so the warp
+// reaches the CTA barriers that follow as one.
+template <class C, bool POISSON>
 __device__ __forceinline__ void produce_segment(const SweepParams &p, const float *src, int ja,
                                                 int jb, int dir, int cols, long long col0,
                                                 StreamState &st) {
+    const unsigned lane = threadIdx.x & 31u;
     const unsigned bytes_u = (unsigned)(((cols + 5 + 3) & ~3) * 4);
     const unsigned bytes_g = (unsigned)(((cols + 3) & ~3) * 4);
     const int r_last = jb + dir;
     for (int r = ja - dir;; r += dir) {
-        const unsigned slot = st.L & (kStages - 1);
-        const unsigned ph = (st.L / kStages) & 1u;
-        if (!st.broken && !mbar_wait_bounded(&st.empty[slot], ph ^ 1u, p.timeout_ns, p.bar)) {
-            record_error(p.bar, kETimedOut, kSitePipeline);
-            st.broken = true;
+        const unsigned slot = st.L & (C::kStages - 1);
+        const unsigned ph = (st.L / C::kStages) & 1u;
+        if (lane == 0u) {
+            if (!st.broken && !mbar_wait_bounded(&st.empty[slot], ph ^ 1u, p.timeout_ns, p.bar)) {
+                record_error(p.bar, kETimedOut, kSitePipeline);
+                st.broken = true;
+            }
+            const bool gneed =
+                POISSON && (dir > 0 ? (r >= ja && r <= jb) : (r <= ja && r >= jb));
+            float *dst_u = st.slots + slot * C::SLOT;
+            mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
+            tma_load_1d(dst_u, src + (long long)r * p.pitch + col0, bytes_u, &st.full[slot]);
+            if (gneed)
+                tma_load_1d(dst_u + C::SLOTU, p.g + (long long)(r - 1) * p.gpitch + col0,
+                            bytes_g, &st.full[slot]);
         }
-        const bool gneed = POISSON && (dir > 0 ? (r >= ja && r <= jb) : (r <= ja && r >= jb));
-        float *dst_u = st.slots + slot * st.slot_floats;
-        mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
-        tma_load_1d(dst_u, src + (long long)r * p.pitch + col0, bytes_u, &st.full[slot]);
-        if (gneed)
-            tma_load_1d(dst_u + kSlotU, p.g + (long long)(r - 1) * p.gpitch + col0, bytes_g,
-                        &st.full[slot]);
+        __syncwarp();
         ++st.L;
         if (r == r_last) break;
     }
 }
 
 // Consumers: output rows ja .. jb (in walking order) of the same strip.
-template <bool POISSON, bool CHECK, bool STORE>
+// Thread t owns float4 groups t + k * kConsumers, k < QPT, of the strip.
+template <class C, bool POISSON, bool CHECK, bool STORE>
 __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst, int ja, int jb,
                                                 int dir, int cols, long long col0,
                                                 StreamState &st, double &s2, float &rmax) {
+    constexpr int Q = C::kQPT;
     const int t = threadIdx.x;
     const unsigned lane = t & 31;
-    const int valid = max(0, min(4, cols - 4 * t));
+    int valid[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) valid[k] = max(0, min(4, cols - 4 * (t + k * kConsumers)));
     const int nin = (dir > 0 ? jb - ja : ja - jb) + 3;
-    float4 prev = make_float4(0.f, 0.f, 0.f, 0.f), cur = prev, curg = prev;
-    float curw = 0.f, cure = 0.f;
+    float4 prev[Q], cur[Q], curg[Q];
+    float curw[Q], cure[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        prev[k] = cur[k] = curg[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        curw[k] = cure[k] = 0.f;
+    }
     int r = ja - dir;
     for (int idx = 0; idx < nin; ++idx, r += dir) {
-        const unsigned slot = st.L & (kStages - 1);
-        const unsigned ph = (st.L / kStages) & 1u;
+        const unsigned slot = st.L & (C::kStages - 1);
+        const unsigned ph = (st.L / C::kStages) & 1u;
         if (!st.broken && !mbar_wait_bounded(&st.full[slot], ph, p.timeout_ns, p.bar)) {
             record_error(p.bar, kETimedOut, kSitePipeline);
             st.broken = true;
         }
-        const float *su = st.slots + slot * st.slot_floats;
-        const float4 x = lds4(su + 4 + 4 * t);
-        const float xw = lane == 0u ? su[3 + 4 * t] : 0.f;
-        const float xe = lane == 31u ? su[8 + 4 * t] : 0.f;
-        float4 xg = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (POISSON && idx >= 1 && idx <= nin - 2) xg = lds4(su + kSlotU + 4 * t);
+        const float *su = st.slots + slot * C::SLOT;
+        float4 x[Q], xg[Q];
+        float xw[Q], xe[Q];
+        const bool gin = POISSON && idx >= 1 && idx <= nin - 2;
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int o = 4 * (t + k * kConsumers);
+            x[k] = lds4(su + 4 + o);
+            xw[k] = lane == 0u ? su[3 + o] : 0.f;
+            xe[k] = lane == 31u ? su[8 + o] : 0.f;
+            xg[k] = gin ? lds4(su + C::SLOTU + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        // Release the slot only once this thread's reads of it are complete
+        // with respect to the async proxy that will refill it.
+        fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0u) mbar_arrive(&st.empty[slot]);
         ++st.L;
         if (idx >= 2) {
-            float w = __shfl_up_sync(0xffffffffu, cur.w, 1);
-            float e = __shfl_down_sync(0xffffffffu, cur.x, 1);
-            if (lane == 0u) w = curw;
-            if (lane == 31u) e = cure;
-            // prev and x are the rows on either side of the centre; their sum
-            // is commutative, so walking up or down gives the same bits.
-            const Quad q = quad_t<POISSON>(w, cur, e, prev, x, curg);
-            if (STORE)
-                store_quad(dst + (long long)(r - dir) * p.pitch + col0 + 4 + 4 * t,
-                           quad_update(q), valid);
-            if (CHECK) quad_residual(q, cur, valid, s2, rmax);
+            float *drow = dst + (long long)(r - dir) * p.pitch + col0 + 4;
+#pragma unroll
+            for (int k = 0; k < Q; ++k) {
+                float w = __shfl_up_sync(0xffffffffu, cur[k].w, 1);
+                float e = __shfl_down_sync(0xffffffffu, cur[k].x, 1);
+                if (lane == 0u) w = curw[k];
+                if (lane == 31u) e = cure[k];
+                // prev and x are the rows on either side of the centre; their
+                // sum is commutative, so walking up or down gives the same bits.
+                const Quad q = quad_t<POISSON>(w, cur[k], e, prev[k], x[k], curg[k]);
+                if (STORE) store_quad(drow + 4 * (t + k * kConsumers), quad_update(q), valid[k]);
+                if (CHECK) quad_residual(q, cur[k], valid[k], s2, rmax);
+            }
         }
-        prev = cur;
-        cur = x;
-        curw = xw;
-        cure = xe;
-        curg = xg;
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            prev[k] = cur[k];
+            cur[k] = x[k];
+            curw[k] = xw[k];
+            cure[k] = xe[k];
+            curg[k] = xg[k];
+        }
     }
 }
 
-template <bool POISSON, bool CHECK, bool STORE>
+template <class C, bool POISSON, bool CHECK, bool STORE>
 __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
                                             int dir, StreamState &st, double &s2, float &rmax) {
     const int nx = p.nx, ny = p.ny;
-    const int strips = (nx + kTW - 1) / kTW;
+    const int strips = (nx + C::TW - 1) / C::TW;
     const long long R = (long long)strips * ny;
     const long long L0 = R * blockIdx.x / gridDim.x;
     const long long L1 = R * (blockIdx.x + 1) / gridDim.x;
@@ -219,32 +259,33 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
             len = min((long long)jr, remaining);
             jb = jr - (int)len + 1;
         }
-        const int cols = min(kTW, nx - s * kTW);
-        const long long col0 = (long long)s * kTW;
+        const int cols = min(C::TW, nx - s * C::TW);
+        const long long col0 = (long long)s * C::TW;
         if (producer_warp) {
-            if (threadIdx.x == kConsumers)
-                produce_segment<POISSON>(p, src, jr, jb, dir, cols, col0, st);
+            produce_segment<C, POISSON>(p, src, jr, jb, dir, cols, col0, st);
         } else {
-            consume_segment<POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2, rmax);
+            consume_segment<C, POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
+                                                      rmax);
         }
         pos += dir > 0 ? len : -len;
         remaining -= len;
     }
     // Generic-proxy stores of this sweep -> TMA reads of the next one.
     if (STORE && !producer_warp) fence_proxy_async_global();
+    __syncwarp();
 }
 
-template <bool POISSON>
+template <class C, bool POISSON>
 __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
                                                 int dir, bool check, bool store, StreamState &st,
                                                 double &s2, float &rmax) {
     if (check) {
         if (store)
-            pass_stream<POISSON, true, true>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, true, true>(p, src, dst, dir, st, s2, rmax);
         else
-            pass_stream<POISSON, true, false>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, true, false>(p, src, dst, dir, st, s2, rmax);
     } else if (store) {
-        pass_stream<POISSON, false, true>(p, src, dst, dir, st, s2, rmax);
+        pass_stream<C, POISSON, false, true>(p, src, dst, dir, st, s2, rmax);
     }
 }
 
@@ -256,9 +297,26 @@ __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const floa
 // decision without another barrier.  Partials are double-buffered by check
 // parity: a CTA can only overwrite a slot after the next barrier, by which
 // time every CTA has finished reading it.
+__device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
+    BarrierCtl ctl;
+    ctl.state = p.bar;
+    ctl.nblocks = gridDim.x;
+    ctl.kind = (unsigned)p.barrier_kind;
+    ctl.timeout_ns = p.timeout_ns;
+    ctl.skip_cta = p.skip_cta;
+    ctl.skip_at = p.skip_at;
+    ctl.index = 0;
+    ctl.base = p.bar_base;
+    ctl.gen = 0u;
+    ctl.profile = p.profile;
+    ctl.spin_ns = 0ull;
+    barrier_begin(ctl);
+    return ctl;
+}
+
 template <class PassFn>
 __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
-    BarrierCtl ctl{p.bar, gridDim.x, p.timeout_ns, p.skip_cta, p.skip_at, 0};
+    BarrierCtl ctl = make_ctl(p);
     const bool checks = p.tol > 0.f && p.check_every > 0;
     int cur = p.cur;
     long long k = 0;
@@ -301,6 +359,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         cur ^= 1;
         ++k;
     }
+    if (threadIdx.x == 0 && p.profile) p.spin_ns[blockIdx.x] = ctl.spin_ns;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         DeviceInfo *d = p.info;
         d->sweeps_done = k;
@@ -310,6 +369,8 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         d->n_checks = n_checks;
         d->cur = cur;
         d->task_sweeps = 0;
+        d->barriers = ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;
     }
@@ -325,17 +386,22 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParam
     });
 }
 
-template <bool POISSON>
+template <class C, bool POISSON>
 __global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    StreamState st = stream_setup(smem, POISSON);
+    StreamState st = stream_setup<C>(smem);
     persistent_loop(p, [&](const float *src, float *dst, bool check, bool store, long long k,
                            double &s2, float &rmax) {
         const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
         // After the barrier: this producer's TMA reads must see the
         // generic-proxy stores the whole grid made in the previous sweep.
-        if (threadIdx.x == kConsumers) fence_proxy_async_global();
-        pass_stream_any<POISSON>(p, src, dst, dir, check, store, st, s2, rmax);
+        // The issuing thread acquires at gpu scope itself, then fences the
+        // generic proxy against the async proxy.
+        if (threadIdx.x == kConsumers) {
+            fence_acq_rel_gpu();
+            fence_proxy_async_global();
+        }
+        pass_stream_any<C, POISSON>(p, src, dst, dir, check, store, st, s2, rmax);
     });
 }
 
@@ -362,15 +428,15 @@ __global__ void __launch_bounds__(kDirectThreads) k_once_direct(SweepParams p) {
     if (p.pass_check) write_partial(p, s2, rmax);
 }
 
-template <bool POISSON>
+template <class C, bool POISSON>
 __global__ void __launch_bounds__(kStreamThreads) k_once_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    StreamState st = stream_setup(smem, POISSON);
+    StreamState st = stream_setup<C>(smem);
     double s2 = 0.0;
     float rmax = 0.f;
     const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;
-    pass_stream_any<POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
-                             p.pass_store != 0, st, s2, rmax);
+    pass_stream_any<C, POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
+                                p.pass_store != 0, st, s2, rmax);
     if (p.pass_check) write_partial(p, s2, rmax);
 }
 
@@ -447,7 +513,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
     __shared__ TaskSlot s_task;
     const SweepParams &p = tp.sp;
     BarrierState *tb = tp.tb;
-    BarrierCtl inner{p.bar, gridDim.x, p.timeout_ns, -1, 0, 0};
+    BarrierCtl inner = make_ctl(p);
     const unsigned G = gridDim.x;
     const unsigned first_unit = blockIdx.x * blockDim.x + threadIdx.x;
     const unsigned stride = G * blockDim.x;
@@ -609,6 +675,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
 __global__ void k_empty() {}
 
 __global__ void __launch_bounds__(256) k_barrier_only(BarrierCtl ctl, long long n) {
+    barrier_begin(ctl);
     for (long long i = 0; i < n; ++i)
         if (!grid_barrier(ctl)) return;
 }
@@ -639,6 +706,7 @@ __global__ void __launch_bounds__(256) k_stress(BarrierCtl ctl, int rounds, int 
                                                 unsigned long long *stale) {
     const unsigned G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
     unsigned long long acc = 0ull, bad = 0ull;
+    barrier_begin(ctl);
     for (int r = 0; r < rounds; ++r) {
         unsigned *buf = lines + (size_t)(r & 1) * G * kStressWords;
         if (t < (unsigned)words) buf[b * kStressWords + t] = stamp(r, G, b, words, t);
@@ -667,34 +735,144 @@ __global__ void __launch_bounds__(256) k_stress(BarrierCtl ctl, int rounds, int 
     }
 }
 
+// The same rounds, but every CTA reads its three peers' lines with one TMA
+// bulk copy each (async proxy) into shared memory, after the grid barrier,
+// as the STREAM sweep reads the rows its neighbours wrote.  mode bit 0: the
+// issuing thread makes its own gpu-scope acquire before its proxy fence;
+// bit 1: writers make a proxy fence after their stores.  With both bits set
+// this is the protocol the STREAM sweep uses.
+__global__ void __launch_bounds__(256) k_stress_tma(BarrierCtl ctl, int rounds, unsigned *lines,
+                                                    unsigned long long *checksums,
+                                                    unsigned long long *stale, int mode) {
+    __shared__ __align__(128) unsigned got[3][kStressWords];
+    __shared__ __align__(8) uint64_t bar;
+    const unsigned G = gridDim.x, b = blockIdx.x, t = threadIdx.x;
+    unsigned long long acc = 0ull, bad = 0ull;
+    bool broken = false;
+    if (t == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    barrier_begin(ctl);
+    for (int r = 0; r < rounds; ++r) {
+        unsigned *buf = lines + (size_t)(r & 1) * G * kStressWords;
+        const unsigned wt = t - (blockDim.x - kStressWords);  // writers: the last warp
+        if (t >= blockDim.x - kStressWords) {
+            buf[b * kStressWords + wt] = stamp(r, G, b, kStressWords, wt);
+            if (mode & 4) fence_acq_rel_gpu();
+            if (mode & 2) fence_proxy_async_global();
+        }
+        if (!grid_barrier(ctl)) return;
+        const unsigned peers[3] = {(b + 1u) % G, (b + G / 2u) % G,
+                                   (unsigned)(((unsigned long long)b + r + 1ull) % G)};
+        if (t == 0) {
+            if (mode & 1) fence_acq_rel_gpu();
+            fence_proxy_async_global();
+            mbar_arrive_expect_tx(&bar, 3u * kStressWords * 4u);
+            for (int k = 0; k < 3; ++k)
+                tma_load_1d(got[k], buf + (size_t)peers[k] * kStressWords, kStressWords * 4u, &bar);
+            if (!broken && !mbar_wait_bounded(&bar, (unsigned)(r & 1), ctl.timeout_ns, ctl.state)) {
+                record_error(ctl.state, kETimedOut, kSitePipeline);
+                broken = true;
+            }
+        }
+        __syncthreads();
+        if (t < (unsigned)kStressWords) {
+#pragma unroll
+            for (int k = 0; k < 3; ++k) {
+                const unsigned v = got[k][t];
+                acc += v;
+                if (v != stamp(r, G, peers[k], kStressWords, t)) ++bad;
+            }
+            fence_proxy_async_shared();  // got[] is refilled by TMA next round
+        }
+        __syncthreads();
+    }
+    if (t < 32) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc += __shfl_down_sync(0xffffffffu, acc, off);
+            bad += __shfl_down_sync(0xffffffffu, bad, off);
+        }
+        if (t == 0) {
+            checksums[b] = acc;
+            if (bad) atomicAdd(stale, bad);
+        }
+    }
+}
+
 }  // namespace
 
 // ===========================================================================
 // Launch wrappers.
-cudaError_t prepare_kernels() {
-    cudaError_t e;
-    e = cudaFuncSetAttribute(k_persistent_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem_bytes(false));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_persistent_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem_bytes(true));
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(k_once_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)stream_smem_bytes(false));
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(k_once_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)stream_smem_bytes(true));
+template <int CFG, bool POISSON>
+using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, POISSON>;
+
+template <int CFG, bool POISSON>
+const void *persistent_stream_fn() {
+    return (const void *)k_persistent_stream<CfgOf<CFG, POISSON>, POISSON>;
+}
+template <int CFG, bool POISSON>
+const void *once_stream_fn() {
+    return (const void *)k_once_stream<CfgOf<CFG, POISSON>, POISSON>;
 }
 
-const void *kernel_persistent(int variant, bool poisson) {
-    if (variant == kVariantStream)
-        return poisson ? (const void *)k_persistent_stream<true> : (const void *)k_persistent_stream<false>;
+template <bool POISSON>
+const void *stream_fn(int cfg, bool persistent) {
+    switch (cfg) {
+#define PK_CFG_CASE(c) \
+    case c:            \
+        return persistent ? persistent_stream_fn<c, POISSON>() : once_stream_fn<c, POISSON>();
+        PK_CFG_CASE(0)
+        PK_CFG_CASE(1)
+        PK_CFG_CASE(2)
+        PK_CFG_CASE(3)
+        PK_CFG_CASE(4)
+        PK_CFG_CASE(5)
+#undef PK_CFG_CASE
+        default:
+            return nullptr;
+    }
+}
+static_assert(kNumStreamConfigs == 6, "update stream_fn");
+
+bool g_cfg_ok[2][kNumStreamConfigs];
+
+cudaError_t prepare_kernels() {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    for (int poisson = 0; poisson < 2; ++poisson) {
+        for (int c = 0; c < kNumStreamConfigs; ++c) {
+            const size_t bytes = stream_smem_bytes(c, poisson != 0);
+            g_cfg_ok[poisson][c] = bytes <= (size_t)optin;
+            if (!g_cfg_ok[poisson][c]) continue;
+            for (int persistent = 0; persistent < 2; ++persistent) {
+                const void *fn = poisson ? stream_fn<true>(c, persistent != 0)
+                                         : stream_fn<false>(c, persistent != 0);
+                e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)bytes);
+                if (e != cudaSuccess) return e;
+            }
+        }
+    }
+    return cudaSuccess;
+}
+
+bool stream_config_ok(int cfg, bool poisson) {
+    return cfg >= 0 && cfg < kNumStreamConfigs && g_cfg_ok[poisson ? 1 : 0][cfg];
+}
+
+const void *kernel_persistent(int variant, bool poisson, int cfg) {
+    if (variant == kVariantStream) return poisson ? stream_fn<true>(cfg, true) : stream_fn<false>(cfg, true);
     return poisson ? (const void *)k_persistent_direct<true> : (const void *)k_persistent_direct<false>;
 }
 
-const void *kernel_once(int variant, bool poisson) {
-    if (variant == kVariantStream)
-        return poisson ? (const void *)k_once_stream<true> : (const void *)k_once_stream<false>;
+const void *kernel_once(int variant, bool poisson, int cfg) {
+    if (variant == kVariantStream) return poisson ? stream_fn<true>(cfg, false) : stream_fn<false>(cfg, false);
     return poisson ? (const void *)k_once_direct<true> : (const void *)k_once_direct<false>;
 }
 
@@ -710,33 +888,25 @@ const void *kernel_stress() { return (const void *)k_stress; }
 
 int block_threads(int variant) { return variant == kVariantStream ? kStreamThreads : kDirectThreads; }
 
-size_t dyn_smem(int variant, bool poisson) {
-    return variant == kVariantStream ? stream_smem_bytes(poisson) : 0;
+size_t dyn_smem(int variant, bool poisson, int cfg) {
+    return variant == kVariantStream ? stream_smem_bytes(cfg, poisson) : 0;
 }
 
-cudaError_t launch_persistent(int variant, bool poisson, int grid, const SweepParams &p,
+cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                               cudaStream_t s) {
     SweepParams arg = p;
     void *args[] = {&arg};
-    return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson), dim3(grid),
+    return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
                                        dim3(block_threads(variant)), args,
-                                       dyn_smem(variant, poisson), s);
+                                       dyn_smem(variant, poisson, cfg), s);
 }
 
-cudaError_t launch_once(int variant, bool poisson, int grid, const SweepParams &p,
+cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                         cudaStream_t s) {
-    if (variant == kVariantStream) {
-        if (poisson)
-            k_once_stream<true><<<grid, kStreamThreads, stream_smem_bytes(true), s>>>(p);
-        else
-            k_once_stream<false><<<grid, kStreamThreads, stream_smem_bytes(false), s>>>(p);
-    } else {
-        if (poisson)
-            k_once_direct<true><<<grid, kDirectThreads, 0, s>>>(p);
-        else
-            k_once_direct<false><<<grid, kDirectThreads, 0, s>>>(p);
-    }
-    return cudaGetLastError();
+    SweepParams arg = p;
+    void *args[] = {&arg};
+    return cudaLaunchKernel(kernel_once(variant, poisson, cfg), dim3(grid),
+                            dim3(block_threads(variant)), args, dyn_smem(variant, poisson, cfg), s);
 }
 
 cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
@@ -777,6 +947,13 @@ cudaError_t launch_barrier_only(int kind, int grid, BarrierCtl ctl, long long n,
                                 cudaStream_t s) {
     void *args[] = {&ctl, &n};
     return cudaLaunchCooperativeKernel(kernel_barrier_only(kind), dim3(grid), dim3(256), args, 0, s);
+}
+
+cudaError_t launch_stress_tma(int grid, BarrierCtl ctl, int rounds, unsigned *lines,
+                              unsigned long long *checksums, unsigned long long *stale, int mode,
+                              cudaStream_t s) {
+    void *args[] = {&ctl, &rounds, &lines, &checksums, &stale, &mode};
+    return cudaLaunchCooperativeKernel((const void *)k_stress_tma, dim3(grid), dim3(256), args, 0, s);
 }
 
 cudaError_t launch_stress(int grid, BarrierCtl ctl, int rounds, int words, unsigned *lines,

@@ -34,6 +34,10 @@ PK_VARIANT_STREAM = 2
 
 PK_FLAG_LAUNCH_PROBLEM_GRID = 0x1
 PK_FLAG_ALTERNATE_DIRECTION = 0x2
+PK_FLAG_PROFILE_BARRIER = 0x4
+
+PK_BARRIER_GENERATION = 0
+PK_BARRIER_COUNTER = 1
 
 PK_TASK_NOP = 0
 PK_TASK_JACOBI = 1
@@ -94,7 +98,9 @@ class pk_options(ctypes.Structure):
         ("debug_skip_arrival_at", ctypes.c_int32),
         ("flags", ctypes.c_uint32),
         ("ctas_per_sm", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 7),
+        ("barrier_kind", ctypes.c_int32),
+        ("stream_config", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 5),
     ]
 
 
@@ -130,8 +136,11 @@ _SIGS = {
                                              ctypes.POINTER(ctypes.c_double)]),
     "pk_bench_barrier": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
                                         ctypes.POINTER(ctypes.c_double)]),
+    "pk_barrier_wait_ns": (ctypes.c_int, [_VP, _I64P, ctypes.c_int]),
     "pk_barrier_stress": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.POINTER(ctypes.c_uint64), _I64P]),
+    "pk_barrier_stress_tma": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.POINTER(ctypes.c_uint64), _I64P]),
     "pk_bench_tasks": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(pk_task), ctypes.c_int,
                                       ctypes.c_int64, _I64P]),
 }
@@ -302,6 +311,12 @@ def pk_bench_barrier(ctx, kind, grid, n_barriers):
     return us.value
 
 
+def pk_barrier_wait_ns(ctx, n=1 << 16):
+    out = np.zeros(n, dtype=np.int64)
+    got = _check(_lib.pk_barrier_wait_ns(ctx, out.ctypes.data_as(_I64P), n), ctx)
+    return out[:got]
+
+
 def pk_barrier_stress(ctx, grid, rounds, words):
     """Returns (checksums uint64[grid_used], stale).  grid 0 = the sweep grid."""
     g = grid if grid > 0 else pk_get_plan(ctx)["grid"]
@@ -310,6 +325,17 @@ def pk_barrier_stress(ctx, grid, rounds, words):
     _check(_lib.pk_barrier_stress(ctx, g, rounds, words,
                                   sums.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
                                   ctypes.byref(stale)), ctx)
+    return sums, stale.value
+
+
+def pk_barrier_stress_tma(ctx, grid, rounds, mode=3):
+    """Returns (checksums uint64[grid_used], stale).  grid 0 = the sweep grid."""
+    g = grid if grid > 0 else pk_get_plan(ctx)["grid"]
+    sums = np.zeros(g, dtype=np.uint64)
+    stale = ctypes.c_int64()
+    _check(_lib.pk_barrier_stress_tma(ctx, g, rounds, mode,
+                                      sums.ctypes.data_as(ctypes.POINTER(ctypes.c_uint64)),
+                                      ctypes.byref(stale)), ctx)
     return sums, stale.value
 
 

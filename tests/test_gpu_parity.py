@@ -400,3 +400,126 @@ def test_oversubscribed_grid_is_refused(pk):
         assert_same_bits(pk.pk_get_field(ctx), want)
     finally:
         pk.pk_destroy(ctx)
+
+
+# ---- STREAM configurations and barrier constructions -------------------------------
+
+CFG_SIZES = [(1, 1), (5, 3), (300, 301), (2053, 5), (4100, 7), (8200, 3)]
+
+
+@pytest.mark.parametrize("cfg", range(6))
+@pytest.mark.parametrize("nx,ny", CFG_SIZES, ids=["%dx%d" % s for s in CFG_SIZES])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
+    u0 = inputs.random_field(nx, ny, seed=300 + cfg + nx)
+    f = inputs.uniform_pm1(400 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    want, oinfo = oracle.jacobi_run(u0, f=f, n=6, tol=1e-30, check_every=4)
+    for path in ("persistent", "launch"):
+        try:
+            got, info = run_pk(pk, u0, f, 6, 1e-30, 4, path=path, variant=2, stream_config=cfg,
+                               flags=pk.PK_FLAG_ALTERNATE_DIRECTION if cfg % 2 else 0)
+        except pk.PkError as e:
+            # a configuration whose ring does not fit in shared memory is refused
+            assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
+            return
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["generation", "counter"])
+def test_barrier_kinds_stress_and_parity(pk, kind):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    u0 = inputs.random_field(512, 512, seed=1)
+    ctx = pk.pk_create(512, 512, u0, None, pk.pk_options_default(barrier_kind=kind))
+    try:
+        cap = pk.pk_get_plan(ctx)["coop_max"]
+        for grid in sorted({1, 3, sms, cap}):
+            sums, stale = pk.pk_barrier_stress(ctx, grid, 1500, 32)
+            assert stale == 0, (kind, grid, stale)
+            assert np.array_equal(sums, oracle.barrier_stress_expected(grid, 1500, 32))
+        # several runs back to back: the counter construction carries its base
+        for _ in range(3):
+            pk.pk_run_sweeps(ctx, 17, 1e-30, 5)
+        pk.pk_run_sweeps_launch(ctx, 4)
+        want, _ = oracle.jacobi_run(u0, n=55)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+    for variant in (1, 2):
+        want, oinfo = oracle.jacobi_run(u0, n=40, tol=1e-30, check_every=7)
+        got, info = run_pk(pk, u0, None, 40, 1e-30, 7, variant=variant, barrier_kind=kind)
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+@pytest.mark.parametrize("kind", [0, 1], ids=["generation", "counter"])
+def test_barrier_kinds_timeout_then_recover(pk, kind):
+    u0 = inputs.random_field(512, 512, seed=31)
+    opt = pk.pk_options_default(barrier_kind=kind, barrier_timeout_s=0.2, debug_skip_arrival_cta=2,
+                                debug_skip_arrival_at=6)
+    ctx = pk.pk_create(512, 512, u0, None, opt)
+    try:
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 30)
+        assert e.value.code == pk.PK_ETIMEDOUT
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_barrier_wait_profile(pk):
+    u0 = inputs.random_field(700, 300, seed=8)
+    ctx = pk.pk_create(700, 300, u0, None,
+                       pk.pk_options_default(flags=pk.PK_FLAG_PROFILE_BARRIER))
+    try:
+        info = pk.pk_run_sweeps(ctx, 25)
+        waits = pk.pk_barrier_wait_ns(ctx)
+        assert len(waits) == info["grid"]
+        assert (waits > 0).all()
+        assert waits.max() < info["device_us"] * 1e3 * 1.05
+    finally:
+        pk.pk_destroy(ctx)
+
+
+def test_stream_ring_refill_race_regression(pk):
+    """One sweep per launch on the STREAM shape with three CTAs per SM,
+    checked after every sweep against the DIRECT path (bit-exact, generic
+    loads only).  Guards the shared-memory write-after-read ordering between
+    the consumers' ld.shared of a ring slot and the TMA refill of that slot:
+    without the proxy fence this configuration showed about one corrupted
+    row segment per 500 sweeps."""
+    import torch
+    dev = torch.device("cuda", 0)
+    n = 8192
+    pitch, _, _ = pk.pk_layout(n, n)
+    u0 = torch.from_numpy(inputs.random_field(n, n, 3)).to(dev)
+
+    def buffers():
+        a = torch.zeros((n + 2, pitch), dtype=torch.float32, device=dev)
+        a[:, 3:n + 5] = u0
+        return a, a.clone()
+
+    S, D = buffers(), buffers()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream(dev).cuda_stream
+    cs = pk.pk_create_device(n, n, S[0].data_ptr(), S[1].data_ptr(), pitch, None, st,
+                             pk.pk_options_default(variant=2, stream_config=1))
+    cd = pk.pk_create_device(n, n, D[0].data_ptr(), D[1].data_ptr(), pitch, None, st,
+                             pk.pk_options_default(variant=1))
+    try:
+        grid = pk.pk_get_plan(cs)["grid"]
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        assert grid > sms  # several CTAs share each SM
+        bad = 0
+        for k in range(2000):
+            a = pk.pk_run_sweeps_launch(cs, 1)
+            b = pk.pk_run_sweeps_launch(cd, 1)
+            assert a["current"] == b["current"]
+            if not torch.equal(S[a["current"]], D[b["current"]]):
+                bad += 1
+                S[0].copy_(D[0])
+                S[1].copy_(D[1])
+        assert bad == 0
+    finally:
+        pk.pk_destroy(cs)
+        pk.pk_destroy(cd)
