@@ -227,6 +227,36 @@ void pk_destroy(pk_ctx *ctx);
 /* Message for the last failure (never NULL). */
 const char *pk_last_error(const pk_ctx *ctx);
 
+/* The persistent sweep of pk_run_sweeps for callers that cannot allocate
+ * device memory: code running inside CUDA graph capture, under a framework
+ * or pool allocator that owns all device memory, or in a loop that cannot
+ * afford the device-wide synchronisation cudaMalloc/cudaFree may cause.
+ * (The pages have no counterpart; this is a library convenience.)
+ *
+ * It allocates nothing.  The caller passes the two pitched field buffers
+ * (layout as pk_create_device; `current` = 0 if u_a holds the starting
+ * iterate, 1 if u_b does), the optional DEVICE source already scaled,
+ * g = fl32(h^2 * f) with h^2 = (float)(1/(nx+1)^2), in the pitched source
+ * layout (g[(j-1) * gpitch + (i-1)], gpitch from pk_layout; NULL for
+ * Laplace), a cudaStream_t (NULL = the legacy default stream), and n, tol,
+ * check_every with pk_run_sweeps's meaning.  The result is bit for bit
+ * pk_run_sweeps's; info->current names the buffer holding it;
+ * info->device_us is 0 (no events are created).  Blocks until done.
+ *
+ * Scratch (grid-barrier words, residual partials, result record) lives in
+ * one file-scope device array of about 66 KB that every GPU loading libpk
+ * holds until the process exits; it serves grids of at most 2048 CTAs, and
+ * a larger plan is refused with PK_EINVAL.  All calls share that array:
+ * each call clears what must start at zero, and calls that overlap on the
+ * GPU (concurrent streams or threads on one device) race and must not be
+ * made.  The first call on a device looks up the array's device address
+ * and sets kernel attributes, so make it before any stream capture.
+ * Errors: PK_EINVAL, PK_ENORESIDENT, PK_ETIMEDOUT, PK_ECUDA; the message is
+ * in pk_last_error(NULL). */
+int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
+                          const float *g_dev, void *stream, int current, int64_t n, float tol,
+                          int check_every, pk_run_info *info);
+
 /* ---- measurement entry points ------------------------------------------ */
 
 /* Launch floors ([P1] "Small problem sizes"): an empty <<<1, 32>>> kernel

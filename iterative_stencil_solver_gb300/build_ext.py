@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpk.so")
-SOURCES = ["pk_kernels.cu", "pk_host.cu"]
+SOURCES = ["pk_kernels.cu", "pk_host.cu", "pk_noalloc.cu"]
 HEADERS = ["pk_device.cuh", "pk_internal.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

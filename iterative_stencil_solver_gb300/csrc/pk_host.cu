@@ -418,6 +418,8 @@ int task_finish(pk_ctx *ctx) {
 
 }  // namespace
 
+void pk::set_global_error(const char *msg) { g_create_error = msg; }
+
 // ===========================================================================
 // Public ABI.
 extern "C" {

@@ -123,6 +123,9 @@ inline size_t stream_smem_bytes(int cfg, bool poisson) {
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot;
 }
 
+// Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).
+void set_global_error(const char *msg);
+
 // ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
 // Every wrapper returns the cudaError_t of its launch.
 enum Variant { kVariantDirect = 1, kVariantStream = 2 };

@@ -119,6 +119,10 @@ _SIGS = {
                                      ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_launch": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
                                             ctypes.POINTER(pk_run_info)]),
+    "pk_run_sweeps_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int64,
+                                             _VP, _VP, ctypes.c_int, ctypes.c_int64,
+                                             ctypes.c_float, ctypes.c_int,
+                                             ctypes.POINTER(pk_run_info)]),
     "pk_get_field": (ctypes.c_int, [_VP, _F32P]),
     "pk_set_field": (ctypes.c_int, [_VP, _F32P]),
     "pk_device_field": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(_VP), _I64P,
@@ -235,6 +239,16 @@ def pk_run_sweeps(ctx, n, tol=0.0, check_every=0):
 def pk_run_sweeps_launch(ctx, n, tol=0.0, check_every=0):
     info = pk_run_info()
     _check(_lib.pk_run_sweeps_launch(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
+    return info.as_dict()
+
+
+def pk_run_sweeps_noalloc(nx, ny, u_a, u_b, pitch, g_dev=None, stream=None, current=0, n=0,
+                          tol=0.0, check_every=0):
+    """u_a, u_b, g_dev: device addresses (int); g_dev is the h^2-scaled source
+    in the pitched source layout, or None for Laplace."""
+    info = pk_run_info()
+    _check(_lib.pk_run_sweeps_noalloc(nx, ny, u_a, u_b, pitch, g_dev, stream, current, n, tol,
+                                      check_every, ctypes.byref(info)))
     return info.as_dict()
 
 
