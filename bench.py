@@ -55,7 +55,8 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum,
 # scaled to this workload's launch); valid only while the kernel source
 # hash matches.
-TRAFFIC = {"kernel_sha": None, "bytes_per_launch": None}
+TRAFFIC = {"kernel_sha": "cdeccbb51eee4d4c",
+           "bytes_per_launch": 103.94e9 + 107.38e9}  # 16384^2 x 100 sweeps, one launch
 
 
 def kernel_source_sha():
@@ -250,10 +251,14 @@ def latency_extras(pk):
         launch = [pk.pk_run_sweeps_launch(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
         sync_each, queued = pk.pk_bench_launch_floor(ctx, 2000)
         nb = 10000
-        b0 = pk.pk_bench_barrier(ctx, 0, 0, 0)
-        ours = (pk.pk_bench_barrier(ctx, 0, 0, nb) - b0) / nb
-        c0 = pk.pk_bench_barrier(ctx, 1, 0, 0)
-        cgs = (pk.pk_bench_barrier(ctx, 1, 0, nb) - c0) / nb
+
+        def per_barrier(kind):
+            b0 = pk.pk_bench_barrier(ctx, kind, 0, 0)
+            return (pk.pk_bench_barrier(ctx, kind, 0, nb) - b0) / nb
+
+        ours = per_barrier(2)          # monotonic-counter construction (default)
+        gen = per_barrier(0)           # count + generation words
+        cgs = per_barrier(1)           # cooperative_groups grid.sync
         p_med, l_med = statistics.median(pers), statistics.median(launch)
         out["laplace_512_1000sweeps"] = {
             "persistent_us_per_sweep": p_med, "launch_us_per_sweep": l_med,
@@ -261,7 +266,8 @@ def latency_extras(pk):
             "variant": "direct" if plan["variant"] == 1 else "stream",
             "persistent_cell_updates_per_s": 512 * 512 / (p_med * 1e-6),
             "floors_us": {"empty_launch_sync_each": sync_each, "empty_launch_queued": queued,
-                          "grid_barrier": ours, "cg_grid_sync": cgs},
+                          "grid_barrier_counter": ours, "grid_barrier_generation": gen,
+                          "cg_grid_sync": cgs},
             "persistent_sweep_in_barriers": p_med / ours if ours > 0 else None,
             "persistent_sweep_in_queued_launches": p_med / queued if queued > 0 else None,
         }
@@ -423,8 +429,8 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind,
-                     "kernel": "k_persistent_stream<laplace>" if plan["variant"] == 2
-                     else "k_persistent_direct",
+                     "kernel": "k_persistent_stream<{4 float4/thread, 4-deep ring}, laplace>"
+                     if plan["variant"] == 2 else "k_persistent_direct",
                      "algorithmic_bytes_per_launch": alg_bytes},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(w["u0"].nbytes),
