@@ -339,6 +339,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true", help="skip the supplementary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stream-config", type=int, default=-1,
+                    help="STREAM shape index (include/pk.h pk_options.stream_config), -1 = default")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -359,7 +361,8 @@ def main():
     w = make_workload(args.workload)
     nx, ny, sweeps = w["nx"], w["ny"], w["sweeps"]
     cells = nx * ny
-    ctx = pk.pk_create(nx, ny, w["u0"], w["f"])
+    ctx = pk.pk_create(nx, ny, w["u0"], w["f"],
+                       pk.pk_options_default(stream_config=args.stream_config))
     try:
         plan = pk.pk_get_plan(ctx)
         for _ in range(args.warmup):

@@ -121,11 +121,15 @@ typedef struct {
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
     int32_t stream_config;            /* STREAM shape, -1 = default (3).  Index into
-                                         {float4 groups per thread, TMA ring depth}:
-                                         0 {1,8}  1 {1,16}  2 {2,8}  3 {4,4}  4 {4,8}  5 {2,16};
-                                         a strip is 1024 x groups columns wide.  A shape
-                                         whose ring does not fit in shared memory is
-                                         refused with PK_EINVAL. */
+                                         {float4 groups per thread, TMA ring depth, sweeps
+                                         per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}
+                                         4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {2,4,2}
+                                         9 {4,4,2}; a strip is 1024 x groups columns wide.
+                                         Two sweeps per pass keep U_{k+1} on chip (temporal
+                                         blocking) whenever two sweeps are due and checks
+                                         are off or check_every is even; results are the
+                                         same bits.  A shape whose ring does not fit in
+                                         shared memory is refused with PK_EINVAL. */
     int32_t reserved[5];
 } pk_options;
 

@@ -106,20 +106,27 @@ constexpr int kStreamThreads = kConsumers + 32; // + one producer warp
 constexpr int kStressWords = 32;
 
 // STREAM configurations: float4 groups per consumer thread per row (the
-// strip is 4 * qpt * kConsumers columns wide) and TMA ring depth.
+// strip is 4 * qpt * kConsumers columns wide), TMA ring depth, and sweeps
+// per pass (2 = temporal blocking: U_{k+1} stays on chip, U_{k+2} is
+// written).
 struct StreamConfig {
     int qpt;
     int stages;
+    int depth;
 };
-constexpr int kNumStreamConfigs = 6;
+constexpr int kNumStreamConfigs = 10;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
-    {1, 8}, {1, 16}, {2, 8}, {4, 4}, {4, 8}, {2, 16}};
+    {1, 8, 1}, {1, 16, 1}, {2, 8, 1}, {4, 4, 1}, {4, 8, 1}, {2, 16, 1},
+    {1, 8, 2}, {2, 8, 2}, {2, 4, 2}, {4, 4, 2}};
 
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kConsumers; }
+inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 
+// A ring slot: the U row segment (4 halo floats each side) and, for
+// Poisson, the g row segment with a 4-float margin each side.
 inline size_t stream_smem_bytes(int cfg, bool poisson) {
     const int tw = stream_tw(cfg);
-    const size_t slot = (size_t)(tw + 8 + (poisson ? tw : 0)) * sizeof(float);
+    const size_t slot = (size_t)(tw + 8 + (poisson ? tw + 8 : 0)) * sizeof(float);
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot;
 }
 

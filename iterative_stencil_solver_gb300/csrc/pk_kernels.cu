@@ -88,14 +88,16 @@ __device__ __forceinline__ void pass_direct_any(const SweepParams &p, const floa
 // QPT float4 groups per thread, so each input row is read from HBM once and
 // from shared memory once.  Edge neighbours come from warp shuffles, and at
 // warp edges from the staged halo.
-template <int QPT, int STAGES, bool POISSON>
+template <int QPT, int STAGES, int DEPTH, bool POISSON>
 struct SCfg {
     static constexpr int kQPT = QPT;
     static constexpr int kStages = STAGES;
+    static constexpr int kDepth = DEPTH;
     static constexpr int TW = 4 * QPT * kConsumers;
     static constexpr int SLOTU = TW + 8;
-    static constexpr int SLOT = SLOTU + (POISSON ? TW : 0);
+    static constexpr int SLOT = SLOTU + (POISSON ? TW + 8 : 0);
     static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
+    static_assert(DEPTH == 1 || DEPTH == 2, "one or two sweeps per pass");
 };
 
 struct StreamState {
@@ -129,19 +131,30 @@ __device__ __forceinline__ float4 lds4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
 }
 
-// Producer: input rows ja - dir .. jb + dir of strip columns [col0, col0+cols).
+// Producer: input rows ja - D*dir .. jb + D*dir of strip columns
+// [col0, col0+cols), D = sweeps per pass; rows beyond the ring are clamped
+// to it (their products are never stored).  The g row (Poisson) comes with
+// every row that is a centre of the first stage: rows ja - (D-1)*dir ..
+// jb + (D-1)*dir inside 1..ny (the ring has no source).
 // Run by all 32 lanes of the producer warp, which stays converged: lane 0
 // waits and issues, every lane meets at __syncwarp each row, so the warp
 // reaches the CTA barriers that follow as one.
-template <class C, bool POISSON>
+template <class C, bool POISSON, int D>
 __device__ __forceinline__ void produce_segment(const SweepParams &p, const float *src, int ja,
                                                 int jb, int dir, int cols, long long col0,
                                                 StreamState &st) {
     const unsigned lane = threadIdx.x & 31u;
     const unsigned bytes_u = (unsigned)(((cols + 5 + 3) & ~3) * 4);
-    const unsigned bytes_g = (unsigned)(((cols + 3) & ~3) * 4);
-    const int r_last = jb + dir;
-    for (int r = ja - dir;; r += dir) {
+    const bool first_strip = col0 == 0;
+    const bool last_strip = col0 + cols >= p.nx;
+    // g segment: D == 1 needs [col0, col0+cols); D == 2 also one column on
+    // each side that lies inside the interior.
+    const int gl = (D == 2 && !first_strip) ? 4 : 0;
+    const int gr = (D == 2 && !last_strip) ? 4 : 0;
+    const unsigned bytes_g = (unsigned)((((cols + 3) & ~3) + gl + gr) * 4);
+    const int nin = (dir > 0 ? jb - ja : ja - jb) + 1 + 2 * D;
+    int r = ja - D * dir;
+    for (int idx = 0; idx < nin; ++idx, r += dir) {
         const unsigned slot = st.L & (C::kStages - 1);
         const unsigned ph = (st.L / C::kStages) & 1u;
         if (lane == 0u) {
@@ -149,18 +162,17 @@ __device__ __forceinline__ void produce_segment(const SweepParams &p, const floa
                 record_error(p.bar, kETimedOut, kSitePipeline);
                 st.broken = true;
             }
-            const bool gneed =
-                POISSON && (dir > 0 ? (r >= ja && r <= jb) : (r <= ja && r >= jb));
+            const int rr = r < 0 ? 0 : (r > p.ny + 1 ? p.ny + 1 : r);
+            const bool gneed = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= p.ny;
             float *dst_u = st.slots + slot * C::SLOT;
             mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
-            tma_load_1d(dst_u, src + (long long)r * p.pitch + col0, bytes_u, &st.full[slot]);
+            tma_load_1d(dst_u, src + (long long)rr * p.pitch + col0, bytes_u, &st.full[slot]);
             if (gneed)
-                tma_load_1d(dst_u + C::SLOTU, p.g + (long long)(r - 1) * p.gpitch + col0,
+                tma_load_1d(dst_u + C::SLOTU + 4 - gl, p.g + (long long)(r - 1) * p.gpitch + col0 - gl,
                             bytes_g, &st.full[slot]);
         }
         __syncwarp();
         ++st.L;
-        if (r == r_last) break;
     }
 }
 
@@ -202,7 +214,7 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
             x[k] = lds4(su + 4 + o);
             xw[k] = lane == 0u ? su[3 + o] : 0.f;
             xe[k] = lane == 31u ? su[8 + o] : 0.f;
-            xg[k] = gin ? lds4(su + C::SLOTU + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xg[k] = gin ? lds4(su + C::SLOTU + 4 + o) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // Release the slot only once this thread's reads of it are complete
         // with respect to the async proxy that will refill it.
@@ -236,7 +248,153 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
     }
 }
 
-template <class C, bool POISSON, bool CHECK, bool STORE>
+// Two sweeps per pass (temporal blocking; "Persistent Kernels...",
+// "Reflections": a wider halo lets a block run several steps per
+// synchronisation, trading a little redundant compute at the tile edges).
+// Input rows ja-2dir .. jb+2dir of U_k; stage 1 recomputes U_{k+1} on rows
+// ja-dir .. jb+dir and, at every warp edge, one column beyond it (lane 0 to
+// the left, lane 31 to the right); stage 2 writes U_{k+2} on rows ja .. jb.
+// U_{k+1} never leaves registers.  Ring cells of U_{k+1} keep their U_k
+// value; every other cell uses the single-sweep arithmetic, so the result
+// is bit for bit two single sweeps.  CHECK reduces the residual of U_k (the
+// loop only checks at the start of a pass).
+template <class C, bool POISSON, bool CHECK>
+__device__ __forceinline__ void consume_segment2(const SweepParams &p, float *dst, int ja, int jb,
+                                                 int dir, int cols, long long col0,
+                                                 StreamState &st, double &s2, float &rmax) {
+    constexpr int Q = C::kQPT;
+    const int t = threadIdx.x;
+    const unsigned lane = t & 31;
+    const bool lo = lane == 0u, hi = lane == 31u;
+    const int nx = p.nx, ny = p.ny;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    int valid[Q];
+    long long icol[Q];  // interior column of the quad's first cell
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        const int o = 4 * (t + k * kConsumers);
+        valid[k] = max(0, min(4, cols - o));
+        icol[k] = col0 + 1 + o;
+    }
+    const int nin = (dir > 0 ? jb - ja : ja - jb) + 5;
+    // U_k rows a (r - 2dir) and b (r - dir); U_{k+1} rows qa, qb.
+    float4 ka[Q], kb[Q], qa[Q], qb[Q], gb[Q], gq[Q];
+    float aw1[Q], bw1[Q], bw2[Q], ae1[Q], be1[Q], be2[Q], gbw[Q], gbe[Q];
+    float qaw[Q], qbw[Q], qae[Q], qbe[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        ka[k] = kb[k] = qa[k] = qb[k] = gb[k] = gq[k] = z4;
+        aw1[k] = bw1[k] = bw2[k] = ae1[k] = be1[k] = be2[k] = gbw[k] = gbe[k] = 0.f;
+        qaw[k] = qbw[k] = qae[k] = qbe[k] = 0.f;
+    }
+    int r = ja - 2 * dir;
+    for (int idx = 0; idx < nin; ++idx, r += dir) {
+        const unsigned slot = st.L & (C::kStages - 1);
+        const unsigned ph = (st.L / C::kStages) & 1u;
+        if (!st.broken && !mbar_wait_bounded(&st.full[slot], ph, p.timeout_ns, p.bar)) {
+            record_error(p.bar, kETimedOut, kSitePipeline);
+            st.broken = true;
+        }
+        const float *su = st.slots + slot * C::SLOT;
+        const float *sg = su + C::SLOTU + 4;
+        const bool gin = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= ny;
+        float4 x[Q], xg[Q];
+        float xw1[Q], xw2[Q], xe1[Q], xe2[Q], xgw[Q], xge[Q];
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int o = 4 * (t + k * kConsumers);
+            x[k] = lds4(su + 4 + o);
+            xw1[k] = lo ? su[3 + o] : 0.f;
+            xw2[k] = lo ? su[2 + o] : 0.f;
+            xe1[k] = hi ? su[8 + o] : 0.f;
+            xe2[k] = hi ? su[9 + o] : 0.f;
+            xg[k] = gin ? lds4(sg + o) : z4;
+            xgw[k] = (gin && lo) ? sg[o - 1] : 0.f;
+            xge[k] = (gin && hi) ? sg[o + 4] : 0.f;
+        }
+        fence_proxy_async_shared();
+        __syncwarp();
+        if (lane == 0u) mbar_arrive(&st.empty[slot]);
+        ++st.L;
+        float4 y[Q];
+        float yw[Q], ye[Q];
+        if (idx >= 2) {
+            // Stage 1: U_{k+1} on row r - dir (centre b).
+            const int o1 = r - dir;
+            const bool ring_row = o1 < 1 || o1 > ny;
+            const bool in_band = idx >= 3 && idx <= nin - 2;  // o1 in [ja, jb]
+#pragma unroll
+            for (int k = 0; k < Q; ++k) {
+                float w = __shfl_up_sync(0xffffffffu, kb[k].w, 1);
+                float e = __shfl_down_sync(0xffffffffu, kb[k].x, 1);
+                if (lo) w = bw1[k];
+                if (hi) e = be1[k];
+                const Quad q1 = quad_t<POISSON>(w, kb[k], e, ka[k], x[k], gb[k]);
+                if (CHECK && in_band) quad_residual(q1, kb[k], valid[k], s2, rmax);
+                float4 u1 = quad_update(q1);
+                if (ring_row) {
+                    u1 = kb[k];
+                } else if (icol[k] + 3 > nx) {
+                    if (icol[k] + 0 > nx) u1.x = kb[k].x;
+                    if (icol[k] + 1 > nx) u1.y = kb[k].y;
+                    if (icol[k] + 2 > nx) u1.z = kb[k].z;
+                    u1.w = kb[k].w;
+                }
+                y[k] = u1;
+                yw[k] = ye[k] = 0.f;
+                if (lo) {
+                    float tw = cell_t(bw2[k], kb[k].x, aw1[k], xw1[k]);
+                    if (POISSON) tw = __fsub_rn(tw, gbw[k]);
+                    yw[k] = (ring_row || icol[k] - 1 < 1) ? bw1[k] : __fmul_rn(0.25f, tw);
+                }
+                if (hi) {
+                    float te = cell_t(kb[k].w, be2[k], ae1[k], xe1[k]);
+                    if (POISSON) te = __fsub_rn(te, gbe[k]);
+                    ye[k] = (ring_row || icol[k] + 4 > nx) ? be1[k] : __fmul_rn(0.25f, te);
+                }
+            }
+            if (idx >= 4) {
+                // Stage 2: U_{k+2} on row r - 2dir (centre qb), inside the band.
+                float *drow = dst + (long long)(r - 2 * dir) * p.pitch + col0 + 4;
+#pragma unroll
+                for (int k = 0; k < Q; ++k) {
+                    float w = __shfl_up_sync(0xffffffffu, qb[k].w, 1);
+                    float e = __shfl_down_sync(0xffffffffu, qb[k].x, 1);
+                    if (lo) w = qbw[k];
+                    if (hi) e = qbe[k];
+                    const Quad q2 = quad_t<POISSON>(w, qb[k], e, qa[k], y[k], gq[k]);
+                    store_quad(drow + 4 * (t + k * kConsumers), quad_update(q2), valid[k]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < Q; ++k) {
+                qa[k] = qb[k];
+                qb[k] = y[k];
+                qaw[k] = qbw[k];
+                qbw[k] = yw[k];
+                qae[k] = qbe[k];
+                qbe[k] = ye[k];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            ka[k] = kb[k];
+            kb[k] = x[k];
+            aw1[k] = bw1[k];
+            bw1[k] = xw1[k];
+            bw2[k] = xw2[k];
+            ae1[k] = be1[k];
+            be1[k] = xe1[k];
+            be2[k] = xe2[k];
+            gq[k] = gb[k];
+            gb[k] = xg[k];
+            gbw[k] = xgw[k];
+            gbe[k] = xge[k];
+        }
+    }
+}
+
+template <class C, bool POISSON, bool CHECK, bool STORE, int D>
 __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
                                             int dir, StreamState &st, double &s2, float &rmax) {
     const int nx = p.nx, ny = p.ny;
@@ -262,7 +420,9 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
         const int cols = min(C::TW, nx - s * C::TW);
         const long long col0 = (long long)s * C::TW;
         if (producer_warp) {
-            produce_segment<C, POISSON>(p, src, jr, jb, dir, cols, col0, st);
+            produce_segment<C, POISSON, D>(p, src, jr, jb, dir, cols, col0, st);
+        } else if (D == 2) {
+            consume_segment2<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st, s2, rmax);
         } else {
             consume_segment<C, POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
                                                       rmax);
@@ -277,15 +437,20 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
 
 template <class C, bool POISSON>
 __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
-                                                int dir, bool check, bool store, StreamState &st,
-                                                double &s2, float &rmax) {
-    if (check) {
-        if (store)
-            pass_stream<C, POISSON, true, true>(p, src, dst, dir, st, s2, rmax);
+                                                int dir, bool check, bool store, bool two,
+                                                StreamState &st, double &s2, float &rmax) {
+    if (C::kDepth == 2 && two) {
+        if (check)
+            pass_stream<C, POISSON, true, true, 2>(p, src, dst, dir, st, s2, rmax);
         else
-            pass_stream<C, POISSON, true, false>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, false, true, 2>(p, src, dst, dir, st, s2, rmax);
+    } else if (check) {
+        if (store)
+            pass_stream<C, POISSON, true, true, 1>(p, src, dst, dir, st, s2, rmax);
+        else
+            pass_stream<C, POISSON, true, false, 1>(p, src, dst, dir, st, s2, rmax);
     } else if (store) {
-        pass_stream<C, POISSON, false, true>(p, src, dst, dir, st, s2, rmax);
+        pass_stream<C, POISSON, false, true, 1>(p, src, dst, dir, st, s2, rmax);
     }
 }
 
@@ -314,7 +479,11 @@ __device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
     return ctl;
 }
 
-template <class PassFn>
+// MAXD = 2: the pass may advance two sweeps at once (temporal blocking)
+// whenever two more sweeps are due and no check can fall between them
+// (checks are off, or check_every is even and the pass starts on a check
+// boundary's parity); otherwise it advances one.
+template <int MAXD, class PassFn>
 __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
     BarrierCtl ctl = make_ctl(p);
     const bool checks = p.tol > 0.f && p.check_every > 0;
@@ -327,9 +496,10 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         const bool check = checks && (k % p.check_every) == 0;
         if (k == p.n && !check) break;
         const bool store = k < p.n;
+        const bool two = MAXD >= 2 && store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0);
         double s2 = 0.0;
         float rmax = 0.f;
-        pass(p.u[cur], p.u[cur ^ 1], check, store, k, s2, rmax);
+        pass(p.u[cur], p.u[cur ^ 1], check, store, two, k, s2, rmax);
         Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
         if (check) {
             block_reduce(s2, rmax);
@@ -357,7 +527,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         }
         if (k == p.n) break;
         cur ^= 1;
-        ++k;
+        k += two ? 2 : 1;
     }
     if (threadIdx.x == 0 && p.profile) p.spin_ns[blockIdx.x] = ctl.spin_ns;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -380,8 +550,8 @@ template <bool POISSON>
 __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParams p) {
     const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
     const unsigned stride = gridDim.x * blockDim.x;
-    persistent_loop(p, [&](const float *src, float *dst, bool check, bool store, long long,
-                           double &s2, float &rmax) {
+    persistent_loop<1>(p, [&](const float *src, float *dst, bool check, bool store, bool,
+                              long long, double &s2, float &rmax) {
         pass_direct_any<POISSON>(p, src, dst, check, store, first, stride, s2, rmax);
     });
 }
@@ -390,8 +560,8 @@ template <class C, bool POISSON>
 __global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     StreamState st = stream_setup<C>(smem);
-    persistent_loop(p, [&](const float *src, float *dst, bool check, bool store, long long k,
-                           double &s2, float &rmax) {
+    persistent_loop<C::kDepth>(p, [&](const float *src, float *dst, bool check, bool store,
+                                      bool two, long long k, double &s2, float &rmax) {
         const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
         // After the barrier: this producer's TMA reads must see the
         // generic-proxy stores the whole grid made in the previous sweep.
@@ -401,7 +571,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParam
             fence_acq_rel_gpu();
             fence_proxy_async_global();
         }
-        pass_stream_any<C, POISSON>(p, src, dst, dir, check, store, st, s2, rmax);
+        pass_stream_any<C, POISSON>(p, src, dst, dir, check, store, two, st, s2, rmax);
     });
 }
 
@@ -436,7 +606,7 @@ __global__ void __launch_bounds__(kStreamThreads) k_once_stream(SweepParams p) {
     float rmax = 0.f;
     const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;
     pass_stream_any<C, POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
-                                p.pass_store != 0, st, s2, rmax);
+                                p.pass_store != 0, false, st, s2, rmax);
     if (p.pass_check) write_partial(p, s2, rmax);
 }
 
@@ -807,7 +977,8 @@ __global__ void __launch_bounds__(256) k_stress_tma(BarrierCtl ctl, int rounds, 
 // ===========================================================================
 // Launch wrappers.
 template <int CFG, bool POISSON>
-using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, POISSON>;
+using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, kStreamConfigs[CFG].depth,
+                   POISSON>;
 
 template <int CFG, bool POISSON>
 const void *persistent_stream_fn() {
@@ -830,12 +1001,16 @@ const void *stream_fn(int cfg, bool persistent) {
         PK_CFG_CASE(3)
         PK_CFG_CASE(4)
         PK_CFG_CASE(5)
+        PK_CFG_CASE(6)
+        PK_CFG_CASE(7)
+        PK_CFG_CASE(8)
+        PK_CFG_CASE(9)
 #undef PK_CFG_CASE
         default:
             return nullptr;
     }
 }
-static_assert(kNumStreamConfigs == 6, "update stream_fn");
+static_assert(kNumStreamConfigs == 10, "update stream_fn");
 
 bool g_cfg_ok[2][kNumStreamConfigs];
 

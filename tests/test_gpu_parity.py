@@ -407,23 +407,30 @@ def test_oversubscribed_grid_is_refused(pk):
 CFG_SIZES = [(1, 1), (5, 3), (300, 301), (2053, 5), (4100, 7), (8200, 3)]
 
 
-@pytest.mark.parametrize("cfg", range(6))
+# (sweeps, check_every): even intervals let depth-2 shapes take two sweeps per
+# pass; odd counts end with a single sweep; an odd interval forces single sweeps.
+CFG_RUNS = [(6, 4), (9, 0), (7, 3), (10, 2)]
+
+
+@pytest.mark.parametrize("cfg", range(10))
 @pytest.mark.parametrize("nx,ny", CFG_SIZES, ids=["%dx%d" % s for s in CFG_SIZES])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=300 + cfg + nx)
     f = inputs.uniform_pm1(400 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    want, oinfo = oracle.jacobi_run(u0, f=f, n=6, tol=1e-30, check_every=4)
-    for path in ("persistent", "launch"):
-        try:
-            got, info = run_pk(pk, u0, f, 6, 1e-30, 4, path=path, variant=2, stream_config=cfg,
-                               flags=pk.PK_FLAG_ALTERNATE_DIRECTION if cfg % 2 else 0)
-        except pk.PkError as e:
-            # a configuration whose ring does not fit in shared memory is refused
-            assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
-            return
-        assert_same_bits(got, want)
-        check_info(info, oinfo)
+    for n, ce in CFG_RUNS:
+        tol = 1e-30 if ce else 0.0
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        for path in ("persistent", "launch"):
+            try:
+                got, info = run_pk(pk, u0, f, n, tol, ce, path=path, variant=2, stream_config=cfg,
+                                   flags=pk.PK_FLAG_ALTERNATE_DIRECTION if (cfg + n) % 2 else 0)
+            except pk.PkError as e:
+                # a configuration whose ring does not fit in shared memory is refused
+                assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
+                return
+            assert_same_bits(got, want)
+            check_info(info, oinfo)
 
 
 @pytest.mark.parametrize("kind", [0, 1], ids=["generation", "counter"])
