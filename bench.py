@@ -311,6 +311,23 @@ def latency_extras(pk):
         }
     finally:
         pk.pk_destroy(ctx)
+    # Temporal blocking: two sweeps per HBM pass, same bits (16384^2, 100 sweeps)
+    w = make_workload(DEFAULT_WORKLOAD)
+    tb = {}
+    for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 6)):
+        ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
+        try:
+            for _ in range(2):
+                pk.pk_run_sweeps(ctx, 100)
+            us = statistics.median(pk.pk_run_sweeps(ctx, 100)["device_us"] / 100 for _ in range(5))
+            tb[name] = {"stream_config": cfg, "us_per_sweep": us,
+                        "cell_updates_per_s": 16384 * 16384 / (us * 1e-6),
+                        "dram_bytes_per_sweep_algorithmic": 8.0 * 16384 * 16384 / (1 if cfg == 3 else 2)}
+        finally:
+            pk.pk_destroy(ctx)
+    tb["speedup"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
+    out["temporal_blocking_16384_100sweeps"] = tb
+    del w
     # Poisson 4096^2 with the in-kernel residual every 10 sweeps
     w = make_workload("poisson-4096x4096-2000sweeps-res10")
     ctx = pk.pk_create(4096, 4096, w["u0"], w["f"])
