@@ -249,6 +249,8 @@ def latency_extras(pk):
             pk.pk_run_sweeps_launch(ctx, 1000)
         pers = [pk.pk_run_sweeps(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
         launch = [pk.pk_run_sweeps_launch(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
+        pk.pk_run_sweeps_graph(ctx, 1000)
+        graph = [pk.pk_run_sweeps_graph(ctx, 1000)["device_us"] / 1000 for _ in range(5)]
         sync_each, queued = pk.pk_bench_launch_floor(ctx, 2000)
         nb = 10000
 
@@ -262,8 +264,10 @@ def latency_extras(pk):
         p_med, l_med = statistics.median(pers), statistics.median(launch)
         out["laplace_512_1000sweeps"] = {
             "persistent_us_per_sweep": p_med, "launch_us_per_sweep": l_med,
-            "persistent_speedup": l_med / p_med, "grid": plan["grid"],
-            "variant": "direct" if plan["variant"] == 1 else "stream",
+            "graph_us_per_sweep": statistics.median(graph),
+            "persistent_speedup": l_med / p_med,
+            "persistent_speedup_vs_graph": statistics.median(graph) / p_med, "grid": plan["grid"],
+            "variant": {1: "direct", 2: "stream", 3: "local"}[plan["variant"]],
             "persistent_cell_updates_per_s": 512 * 512 / (p_med * 1e-6),
             "floors_us": {"empty_launch_sync_each": sync_each, "empty_launch_queued": queued,
                           "grid_barrier_counter": ours, "grid_barrier_generation": gen,
@@ -282,9 +286,14 @@ def latency_extras(pk):
         pers = statistics.median(pk.pk_run_sweeps(ctx, 100)["device_us"] / 100 for _ in range(5))
         launch = statistics.median(pk.pk_run_sweeps_launch(ctx, 100)["device_us"] / 100
                                    for _ in range(5))
+        pk.pk_run_sweeps_graph(ctx, 100)
+        graph = statistics.median(pk.pk_run_sweeps_graph(ctx, 100)["device_us"] / 100
+                                  for _ in range(5))
         out["laplace_64_topedge_100sweeps"] = {"persistent_us_per_sweep": pers,
                                                "launch_us_per_sweep": launch,
-                                               "persistent_speedup": launch / pers}
+                                               "graph_us_per_sweep": graph,
+                                               "persistent_speedup": launch / pers,
+                                               "persistent_speedup_vs_graph": graph / pers}
     finally:
         pk.pk_destroy(ctx)
     # task queue: 10,000 tasks alternating 1-sweep Jacobi (256^2) and axpy (65,536)
@@ -438,7 +447,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "nx": nx, "ny": ny, "sweeps_per_step": sweeps,
-                   "variant": "stream" if plan["variant"] == 2 else "direct",
+                   "variant": {1: "direct", 2: "stream", 3: "local"}[plan["variant"]],
                    "grid": plan["grid"], "l2": "inputs larger than L2 (2 x field > 129 MB)"
                    if 2 * 4 * cells > 129e6 else "L2-resident",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},

@@ -56,9 +56,14 @@ extern "C" {
 #define PK_EDEVICE (-7)     /* the kernel reported an internal error status */
 
 /* ---- sweep variants ---------------------------------------------------- */
-#define PK_VARIANT_AUTO 0   /* STREAM when the two fields exceed half of L2, else DIRECT */
+#define PK_VARIANT_AUTO 0   /* STREAM when the two fields exceed half of L2; else LOCAL for
+                               grids up to 2^20 cells whose tiles fit; else DIRECT */
 #define PK_VARIANT_DIRECT 1 /* each thread loads its own float4 and neighbours (L2-resident grids) */
 #define PK_VARIANT_STREAM 2 /* TMA bulk row staging + register window down row bands (HBM grids) */
+#define PK_VARIANT_LOCAL 3  /* each CTA keeps its row band in shared memory across sweeps and
+                               trades only boundary rows with its two neighbours, as tagged
+                               words, with no grid barrier between sweeps (small grids).  The
+                               per-launch and graph paths run DIRECT kernels for it. */
 
 /* ---- option flags ------------------------------------------------------ */
 #define PK_FLAG_LAUNCH_PROBLEM_GRID 0x1u /* pk_run_sweeps_launch: one thread per float4, not the persistent grid */
@@ -88,7 +93,7 @@ typedef struct {
     int32_t n_checks;     /* residual evaluations performed */
     int32_t current;      /* buffer holding the current iterate: 0 = A, 1 = B */
     int32_t grid;         /* CTAs the sweeps ran with */
-    int32_t variant;      /* PK_VARIANT_DIRECT or PK_VARIANT_STREAM */
+    int32_t variant;      /* PK_VARIANT_DIRECT, _STREAM or _LOCAL: the kernels that ran */
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
 } pk_run_info;
@@ -183,6 +188,17 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
  * reduction kernel runs and the host reads the residual back and decides.
  * Same results, bit for bit, as pk_run_sweeps.  Errors as pk_run_sweeps. */
 int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
+
+/* The per-launch path replayed from CUDA graphs ([P1] "Reflections and next
+ * steps": graphs record the launch sequence once and replay it, cutting the
+ * host-side launch cost while each kernel still pays its device-side set-up
+ * -- the fairer baseline for the persistent kernel).  The plain sweeps
+ * between two checks are captured once (segments of up to 1000 launches)
+ * and cached per context; a check sweep is its own small graph (sweep +
+ * reduction + residual readback) followed by a host decision.  Same grid,
+ * same kernels and the same bits as pk_run_sweeps_launch.  Errors as
+ * pk_run_sweeps_launch. */
+int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
 
 /* Copy the current iterate to / from a packed (ny+2) x (nx+2) HOST array.
  * pk_set_field writes both buffers (ring included) and makes buffer A

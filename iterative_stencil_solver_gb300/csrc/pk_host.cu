@@ -18,6 +18,8 @@
 //     separate cache lines; acquire/release, no early ACK).
 #include <atomic>
 #include <chrono>
+#include <map>
+#include <tuple>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -79,6 +81,8 @@ struct pk_ctx {
     int part_cap = 0;    // partial slots per parity
     Scratch *scratch = nullptr;
     Partial *partials = nullptr;
+    unsigned long long *halo = nullptr;     // LOCAL: tagged halo words
+    int local_rows = 0;                     // LOCAL: most rows per CTA
     unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
     int spin_valid = 0;                     // entries written by the last profiled run
     unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
@@ -99,6 +103,9 @@ struct pk_ctx {
     int task_status = PK_OK;
     int run_id = 0;
     bool dirty_sweep = false;
+    // pk_run_sweeps_graph: instantiated graphs keyed by
+    // (check sweep first, plain sweeps, buffer parity, direction parity, grid)
+    std::map<std::tuple<int, long long, int, int, int>, cudaGraphExec_t> graphs;
     std::string err = "no error";
 };
 
@@ -167,7 +174,7 @@ int read_options(pk_ctx *ctx, const pk_options *opt) {
                     sizeof(pk_options));
     ctx->opt = *opt;
     pk_options &o = ctx->opt;
-    if (o.variant < PK_VARIANT_AUTO || o.variant > PK_VARIANT_STREAM)
+    if (o.variant < PK_VARIANT_AUTO || o.variant > PK_VARIANT_LOCAL)
         return fail(ctx, PK_EINVAL, "unknown variant %d", o.variant);
     if (o.grid_override < 0 || o.task_grid < 0 || o.ctas_per_sm < 0)
         return fail(ctx, PK_EINVAL, "negative grid option");
@@ -226,30 +233,77 @@ int ensure_partials(pk_ctx *ctx, int grid) {
     return PK_OK;
 }
 
+// LOCAL plan: rows per CTA chosen so a CTA has about one float4 group per
+// thread, then the grid is capped by what is co-resident with the tile's
+// shared memory.  Returns false when the tile does not fit.
+bool plan_local(pk_ctx *ctx, int *grid_out, int *rows_out, int *cap_out) {
+    const int nq = (ctx->nx + 3) / 4;
+    long long rows = (kDirectThreads + nq - 1) / nq;
+    if (rows < 1) rows = 1;
+    long long grid = (ctx->ny + rows - 1) / rows;
+    if (ctx->opt.grid_override > 0) grid = ctx->opt.grid_override;
+    if (grid > ctx->ny) grid = ctx->ny;
+    for (int it = 0; it < 8; ++it) {
+        rows = (ctx->ny + grid - 1) / grid;
+        const size_t smem = local_smem_bytes(ctx->nx, (int)rows, ctx->poisson);
+        if (smem > g_local_smem_max) return false;
+        int per_sm = 0;
+        const int cap = coop_capacity(ctx, kernel_persistent(kVariantLocal, ctx->poisson, 0),
+                                      kDirectThreads, smem, &per_sm);
+        if (cap <= 0) return false;
+        if (grid <= cap || ctx->opt.grid_override > 0) {
+            *grid_out = (int)grid;
+            *rows_out = (int)rows;
+            *cap_out = cap;
+            return true;
+        }
+        grid = cap;
+    }
+    return false;
+}
+
 // Variant and grid for the sweeps; also the task kernel's grid.
 int plan(pk_ctx *ctx) {
     const long long field_bytes = (long long)(ctx->ny + 2) * ctx->pitch * 4;
     long long resident = 2 * field_bytes + (ctx->poisson ? (long long)ctx->ny * ctx->gpitch * 4 : 0);
     int v = ctx->opt.variant;
-    if (v == PK_VARIANT_AUTO) v = resident > ctx->l2_bytes / 2 ? kVariantStream : kVariantDirect;
+    int lgrid = 0, lrows = 0, lcap = 0;
+    if (v == PK_VARIANT_AUTO) {
+        if (resident > ctx->l2_bytes / 2)
+            v = kVariantStream;
+        else if ((long long)ctx->nx * ctx->ny <= (1LL << 20) && plan_local(ctx, &lgrid, &lrows, &lcap))
+            v = kVariantLocal;
+        else
+            v = kVariantDirect;
+    } else if (v == kVariantLocal && !plan_local(ctx, &lgrid, &lrows, &lcap)) {
+        return fail(ctx, PK_EINVAL, "the LOCAL tile does not fit in shared memory");
+    }
     if (v == kVariantDirect && direct_units(ctx) >= (1LL << 31))
         return fail(ctx, PK_EINVAL, "grid too large for the DIRECT variant");
     ctx->variant = v;
     ctx->stream_cfg = ctx->opt.stream_config >= 0 ? ctx->opt.stream_config : kDefaultStreamConfig;
     if (v == kVariantStream && !stream_config_ok(ctx->stream_cfg, ctx->poisson))
         return fail(ctx, PK_EINVAL, "stream_config %d does not fit in shared memory", ctx->stream_cfg);
-    int per_sm = 0;
-    const int cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, ctx->stream_cfg),
-                                  block_threads(v), dyn_smem(v, ctx->poisson, ctx->stream_cfg),
-                                  &per_sm);
-    if (cap < 0) return PK_ECUDA;
-    if (cap == 0) return fail(ctx, PK_ENORESIDENT, "sweep kernel does not fit on an SM");
+    int cap;
+    if (v == kVariantLocal) {
+        cap = lcap;
+        ctx->grid = lgrid;
+        ctx->local_rows = lrows;
+        const size_t words = (size_t)lgrid * local_halo_words(ctx->nx);
+        PK_TRY(ctx, cudaMalloc(&ctx->halo, words * sizeof(unsigned long long)));
+    } else {
+        int per_sm = 0;
+        cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, ctx->stream_cfg),
+                            block_threads(v), dyn_smem(v, ctx->poisson, ctx->stream_cfg), &per_sm);
+        if (cap < 0) return PK_ECUDA;
+        if (cap == 0) return fail(ctx, PK_ENORESIDENT, "sweep kernel does not fit on an SM");
+        long long need = v == kVariantStream ? stream_rows(ctx)
+                                             : (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+        if (need < 1) need = 1;
+        ctx->grid = (int)(need < cap ? need : cap);
+        if (ctx->opt.grid_override > 0) ctx->grid = ctx->opt.grid_override;
+    }
     ctx->coop_max = cap;
-    long long need = v == kVariantStream ? stream_rows(ctx)
-                                         : (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
-    if (need < 1) need = 1;
-    ctx->grid = (int)(need < cap ? need : cap);
-    if (ctx->opt.grid_override > 0) ctx->grid = ctx->opt.grid_override;
     // task kernel (DIRECT sweep + axpy, 256 threads)
     int tper = 0;
     const int tcap = coop_capacity(ctx, kernel_task(ctx->poisson), kDirectThreads, 0, &tper);
@@ -260,6 +314,13 @@ int plan(pk_ctx *ctx) {
     if (ctx->opt.task_grid > 0) ctx->task_grid = ctx->opt.task_grid;
     int want = ctx->grid > cap ? ctx->grid : cap;
     return ensure_partials(ctx, want);
+}
+
+// The per-launch and graph paths run the DIRECT kernels when the
+// persistent path is LOCAL (its shared-memory tile only lives inside one
+// launch).
+int launch_variant(const pk_ctx *ctx) {
+    return ctx->variant == kVariantLocal ? (int)kVariantDirect : ctx->variant;
 }
 
 SweepParams base_params(pk_ctx *ctx) {
@@ -286,6 +347,9 @@ SweepParams base_params(pk_ctx *ctx) {
     p.bar_base = ctx->sweep_bar_base;
     p.profile = (ctx->opt.flags & PK_FLAG_PROFILE_BARRIER) ? 1 : 0;
     p.spin_ns = ctx->spin_ns;
+    p.halo = ctx->halo;
+    p.local_rows = ctx->local_rows;
+    p.local_pitch = local_pitch(ctx->nx);
     return p;
 }
 
@@ -356,6 +420,7 @@ void release(pk_ctx *ctx) {
     cudaFree(ctx->g);
     cudaFree(ctx->scratch);
     cudaFree(ctx->partials);
+    cudaFree(ctx->halo);
     cudaFree(ctx->stress_lines);
     cudaFree(ctx->stress_out);
     if (ctx->h_info) cudaFreeHost(ctx->h_info);
@@ -365,6 +430,7 @@ void release(pk_ctx *ctx) {
     if (ctx->ev0) cudaEventDestroy(ctx->ev0);
     if (ctx->ev1) cudaEventDestroy(ctx->ev1);
     if (ctx->ev_sync) cudaEventDestroy(ctx->ev_sync);
+    for (auto &kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
     if (ctx->task_stream) cudaStreamDestroy(ctx->task_stream);
     if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
     delete ctx;
@@ -380,7 +446,7 @@ double elapsed_us(pk_ctx *ctx) {
 }
 
 void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
-               float rmax, int n_checks, int status, int grid) {
+               float rmax, int n_checks, int status, int grid, int variant = 0) {
     if (!info) return;
     info->sweeps_done = sweeps;
     info->res0 = res0;
@@ -390,7 +456,7 @@ void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, do
     info->n_checks = n_checks;
     info->current = ctx->cur;
     info->grid = grid;
-    info->variant = ctx->variant;
+    info->variant = variant ? variant : ctx->variant;
     info->device_us = elapsed_us(ctx);
 }
 
@@ -553,6 +619,10 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.n = n;
     p.tol = tol;
     p.check_every = check_every;
+    if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
+        PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0,
+                                    (size_t)ctx->grid * local_halo_words(ctx->nx) * sizeof(unsigned long long),
+                                    ctx->stream));
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, ctx->stream_cfg, ctx->grid, p,
                                       ctx->stream);
@@ -584,7 +654,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
     if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_sweeps_launch: the task kernel is live");
     int grid = ctx->grid;
     if (ctx->opt.flags & PK_FLAG_LAUNCH_PROBLEM_GRID) {
-        long long need = ctx->variant == kVariantStream ? (stream_rows(ctx) + 31) / 32
+        long long need = launch_variant(ctx) == kVariantStream ? (stream_rows(ctx) + 31) / 32
                                                         : (direct_units(ctx) + kDirectThreads - 1) /
                                                               kDirectThreads;
         if (need < 1) need = 1;
@@ -609,10 +679,10 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
         p.pass_store = k < n ? 1 : 0;
         p.pass_parity = n_checks & 1;
         p.pass_k = k;
-        cudaError_t e = launch_once(ctx->variant, ctx->poisson, ctx->stream_cfg, grid, p, ctx->stream);
+        cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, grid, p, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "sweep launch");
         if (check) {
-            e = launch_finalize(ctx->variant, grid, p, &ctx->scratch->res, ctx->stream);
+            e = launch_finalize(launch_variant(ctx), grid, p, &ctx->scratch->res, ctx->stream);
             if (e != cudaSuccess) return cuda_fail(ctx, e, "residual launch");
             PK_TRY(ctx, cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
                                         cudaMemcpyDeviceToHost, ctx->stream));
@@ -633,7 +703,139 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     ctx->cur = cur;
-    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, grid);
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, grid, launch_variant(ctx));
+    return PK_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+constexpr long long kGraphMaxSweeps = 1000;  // longest plain segment in one graph
+
+// A captured segment: [one check sweep + residual reduction + readback]
+// when `check`, else `plain` ordinary sweeps, starting from buffer `cur`
+// with direction parity `kpar`.
+int graph_for(pk_ctx *ctx, bool check, long long plain, int cur, int kpar, cudaGraphExec_t *out) {
+    const auto key = std::make_tuple(check ? 1 : 0, plain, cur, kpar, ctx->grid);
+    auto it = ctx->graphs.find(key);
+    if (it != ctx->graphs.end()) {
+        *out = it->second;
+        return PK_OK;
+    }
+    SweepParams p = base_params(ctx);
+    cudaGraph_t graph = nullptr;
+    PK_TRY(ctx, cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+    cudaError_t e = cudaSuccess;
+    long long k = kpar;
+    if (check) {
+        p.cur = cur;
+        p.pass_check = 1;
+        p.pass_store = 1;
+        p.pass_parity = 0;
+        p.pass_k = k;
+        e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->grid, p, ctx->stream);
+        if (e == cudaSuccess) e = launch_finalize(launch_variant(ctx), ctx->grid, p, &ctx->scratch->res, ctx->stream);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
+                                cudaMemcpyDeviceToHost, ctx->stream);
+    } else {
+        for (long long q = 0; q < plain && e == cudaSuccess; ++q, ++k) {
+            p.cur = (int)((cur + q) & 1);
+            p.pass_check = 0;
+            p.pass_store = 1;
+            p.pass_k = k;
+            e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->grid, p, ctx->stream);
+        }
+    }
+    cudaError_t e2 = cudaStreamEndCapture(ctx->stream, &graph);
+    if (e != cudaSuccess || e2 != cudaSuccess) {
+        if (graph) cudaGraphDestroy(graph);
+        return cuda_fail(ctx, e != cudaSuccess ? e : e2, "graph capture");
+    }
+    cudaGraphExec_t exec = nullptr;
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    cudaGraphDestroy(graph);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaGraphInstantiate");
+    ctx->graphs[key] = exec;
+    *out = exec;
+    return PK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
+    if (!ctx) return PK_EINVAL;
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_sweeps_graph: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_sweeps_graph: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_sweeps_graph: the task kernel is live");
+    const bool checks = tol > 0.f && check_every > 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    int cur = ctx->cur;
+    int rc;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    for (;;) {
+        const bool check = checks && (k % check_every) == 0;
+        if (k == n && !check) break;
+        cudaGraphExec_t g = nullptr;
+        if (check) {
+            if (k == n) {
+                // residual of the final iterate only: no store, not worth a graph
+                SweepParams p = base_params(ctx);
+                p.cur = cur;
+                p.pass_check = 1;
+                p.pass_store = 0;
+                p.pass_parity = 0;
+                p.pass_k = k;
+                cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg,
+                                            ctx->grid, p, ctx->stream);
+                if (e == cudaSuccess)
+                    e = launch_finalize(launch_variant(ctx), ctx->grid, p, &ctx->scratch->res,
+                                        ctx->stream);
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
+                                        cudaMemcpyDeviceToHost, ctx->stream);
+                if (e != cudaSuccess) return cuda_fail(ctx, e, "residual pass");
+            } else {
+                if ((rc = graph_for(ctx, true, 0, cur, (int)(k & 1), &g)) != PK_OK) return rc;
+                PK_TRY(ctx, cudaGraphLaunch(g, ctx->stream));
+            }
+            PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+            const double res = ctx->h_res->res;
+            ++n_checks;
+            res_last = res;
+            rmax_last = ctx->h_res->rmax;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)tol * res0)
+                break;  // U_k is intact in buffer cur
+            if (k == n) break;
+            cur ^= 1;
+            ++k;
+        }
+        // plain sweeps up to the next check (or n), in segments of at most kGraphMaxSweeps
+        long long stop = n;
+        if (checks) {
+            const long long next = (k + check_every - 1) / check_every * check_every;
+            if (next < stop) stop = next;
+        }
+        while (k < stop) {
+            const long long m = stop - k < kGraphMaxSweeps ? stop - k : kGraphMaxSweeps;
+            if ((rc = graph_for(ctx, false, m, cur, (int)(k & 1), &g)) != PK_OK) return rc;
+            PK_TRY(ctx, cudaGraphLaunch(g, ctx->stream));
+            cur ^= (int)(m & 1);
+            k += m;
+        }
+    }
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    ctx->cur = cur;
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->grid, launch_variant(ctx));
     return PK_OK;
 }
 

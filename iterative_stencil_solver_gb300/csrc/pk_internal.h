@@ -60,6 +60,11 @@ struct SweepParams {
     unsigned bar_base;      // kBarrierCounter: count word at launch
     int profile;            // record per-CTA barrier wait time
     unsigned long long *spin_ns;  // per-CTA barrier wait time (ns), when profiling
+    // LOCAL variant: tagged halo words (see k_persistent_local) and the
+    // shared-memory tile shape.
+    unsigned long long *halo;
+    int local_rows;         // most rows any CTA owns
+    int local_pitch;        // floats per tile row in shared memory
 };
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
@@ -135,13 +140,25 @@ void set_global_error(const char *msg);
 
 // ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
 // Every wrapper returns the cudaError_t of its launch.
-enum Variant { kVariantDirect = 1, kVariantStream = 2 };
+enum Variant { kVariantDirect = 1, kVariantStream = 2, kVariantLocal = 3 };
+
+// LOCAL variant: each CTA keeps its band (rows + one halo row each side) in
+// shared memory, twice (ping-pong), plus its source rows for Poisson.
+inline int local_pitch(int nx) { return (nx + 8 + 3) / 4 * 4; }
+inline size_t local_smem_bytes(int nx, int rows, bool poisson) {
+    const size_t tile = (size_t)2 * (rows + 2) * local_pitch(nx) * sizeof(float);
+    const size_t g = poisson ? (size_t)rows * ((nx + 3) / 4 * 4) * sizeof(float) : 0;
+    return tile + g;
+}
+// Halo words per CTA: 2 sides x 2 parities x (interior columns rounded to 4).
+inline size_t local_halo_words(int nx) { return (size_t)4 * ((nx + 3) / 4 * 4); }
 
 // Once per device: kernel attributes (dynamic shared memory limits).
 // Configurations whose shared memory does not fit are left unset and
 // reported unusable by stream_config_ok.
 cudaError_t prepare_kernels();
 bool stream_config_ok(int cfg, bool poisson);
+extern size_t g_local_smem_max;   // LOCAL: opt-in shared memory per CTA
 
 // Kernel function pointers, for occupancy queries.  cfg selects the STREAM
 // configuration (ignored for DIRECT).

@@ -576,6 +576,189 @@ __global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParam
 }
 
 // ===========================================================================
+// LOCAL: the band stays in shared memory; neighbours exchange only their
+// boundary rows, as tagged words, without a grid barrier between sweeps
+// ("Persistent Kernels...", "Reflections": GPU-side scheduling on the
+// neighbours' step counters instead of a round trip to the host; here the
+// step counter travels inside each data word).
+//
+// CTA b owns rows [r0, r1) in full width.  Its tile holds those rows plus
+// one halo row above and below, twice (ping-pong), in shared memory; the
+// ring columns and the ring rows are loaded once and never written.  After
+// computing U_{k+1} on its rows, a CTA writes its first row into the lower
+// halo area of CTA b-1 and its last row into the upper halo area of CTA b+1:
+// each cell as one 64-bit word (tag k+1 << 32 | value bits) with a relaxed
+// gpu-scope store, so value and tag arrive together.  Before sweep k+1 the
+// CTA polls its own halo areas with relaxed loads until every word carries
+// tag k+1.  A neighbour cannot run two sweeps ahead (it needs this CTA's
+// rows of the sweep in between), so double-buffering the halo areas by
+// parity is enough and the lag is at most one sweep: every cell sees the
+// same operands as in a synchronous sweep, bit for bit.  Residual checks
+// still reduce across the grid behind the grid barrier.
+__device__ __forceinline__ void st_tagged4(unsigned long long *p, float4 v, unsigned tag) {
+    const unsigned long long hi = (unsigned long long)tag << 32;
+    const unsigned long long a = hi | __float_as_uint(v.x), b = hi | __float_as_uint(v.y);
+    const unsigned long long c = hi | __float_as_uint(v.z), d = hi | __float_as_uint(v.w);
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p + 2), "l"(c), "l"(d) : "memory");
+}
+
+// Wait until the four tagged words at p carry `tag`; false on timeout/abort.
+__device__ __forceinline__ bool ld_tagged4(const unsigned long long *p, unsigned tag, float4 &v,
+                                           const SweepParams &sp) {
+    unsigned long long a, b, c, d;
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    for (;;) {
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+        asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(c), "=l"(d) : "l"(p + 2) : "memory");
+        if ((unsigned)(a >> 32) == tag && (unsigned)(b >> 32) == tag &&
+            (unsigned)(c >> 32) == tag && (unsigned)(d >> 32) == tag)
+            break;
+        if ((++spins & 31u) == 0u) {
+            if (aborted(sp.bar)) return false;
+            if (globaltimer_ns() - t0 > sp.timeout_ns) {
+                record_error(sp.bar, kETimedOut, kSiteBarrier);
+                return false;
+            }
+        }
+    }
+    v = make_float4(__uint_as_float((unsigned)a), __uint_as_float((unsigned)b),
+                    __uint_as_float((unsigned)c), __uint_as_float((unsigned)d));
+    return true;
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams p) {
+    extern __shared__ __align__(16) float tile[];
+    const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
+    const int nx = p.nx, ny = p.ny;
+    const int r0 = 1 + (int)((long long)ny * b / G);
+    const int r1 = 1 + (int)((long long)ny * (b + 1) / G);
+    const int B = r1 - r0;
+    const int sp = p.local_pitch, spq = sp / 4;
+    const int nq = (nx + 3) >> 2, gw = 4 * nq;
+    float *T[2] = {tile, tile + (size_t)(p.local_rows + 2) * sp};
+    float *gs = tile + (size_t)2 * (p.local_rows + 2) * sp;
+    const size_t hw = (size_t)4 * nq;  // words per (side, parity) area
+    unsigned long long *mine = p.halo + (size_t)b * 4 * hw;
+    unsigned long long *up = b > 0 ? p.halo + (size_t)(b - 1) * 4 * hw : nullptr;
+    unsigned long long *down = b < G - 1 ? p.halo + (size_t)(b + 1) * 4 * hw : nullptr;
+
+    const float *u0 = p.u[p.cur];
+    for (int q = tid; q < (B + 2) * spq; q += nthr) {
+        const int lr = q / spq, c4 = q - lr * spq;
+        const float4 v = ld4(u0 + (long long)(r0 - 1 + lr) * p.pitch + 4 * c4);
+        *reinterpret_cast<float4 *>(T[0] + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(T[1] + lr * sp + 4 * c4) = v;
+    }
+    if (POISSON) {
+        for (int q = tid; q < B * nq; q += nthr) {
+            const int lr = q / nq, c4 = q - lr * nq;
+            *reinterpret_cast<float4 *>(gs + lr * gw + 4 * c4) =
+                ld4(p.g + (long long)(r0 - 1 + lr) * p.gpitch + 4 * c4);
+        }
+    }
+    __syncthreads();
+
+    BarrierCtl ctl = make_ctl(p);
+    const bool checks = p.tol > 0.f && p.check_every > 0;
+    int c = 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    for (;;) {
+        const bool check = checks && (k % p.check_every) == 0;
+        if (k == p.n && !check) break;
+        // fault injection: this CTA leaves before sweep skip_at; its
+        // neighbours' tagged waits then expire (host-driven test only)
+        if (b == p.skip_cta && k == p.skip_at) return;
+        const bool store = k < p.n;
+        const float *Tc = T[c];
+        float *Tn = T[c ^ 1];
+        const unsigned tag = (unsigned)(k + 1);
+        const size_t par = (size_t)((k + 1) & 1);
+        double s2 = 0.0;
+        float rmax = 0.f;
+        for (int u = tid; u < B * nq; u += nthr) {
+            const int lr = u / nq + 1, q = u - (lr - 1) * nq;
+            const float *row = Tc + lr * sp + 4 + 4 * q;
+            const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
+            const float W = row[-1], E = row[4];
+            float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
+            const int valid = min(4, nx - 4 * q);
+            const Quad t = quad_t<POISSON>(W, C, E, S, N, G4);
+            if (check) quad_residual(t, C, valid, s2, rmax);
+            if (store) {
+                const float4 v = quad_update(t);
+                store_quad(Tn + lr * sp + 4 + 4 * q, v, valid);
+                if (lr == 1 && up) st_tagged4(up + (2 + par) * hw + 4 * q, v, tag);
+                if (lr == B && down) st_tagged4(down + par * hw + 4 * q, v, tag);
+            }
+        }
+        if (check) {
+            Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+            block_reduce(s2, rmax);
+            if (tid == 0) {
+                Partial pp;
+                pp.s2 = s2;
+                pp.rmax = rmax;
+                pp.pad = 0.f;
+                parts[b] = pp;
+            }
+            if (!grid_barrier(ctl)) return;
+            double S2;
+            float RM;
+            reduce_partials(parts, G, S2, RM);
+            const double res = sqrt(S2);
+            ++n_checks;
+            res_last = res;
+            rmax_last = RM;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)p.tol * res0)
+                break;
+        }
+        if (k == p.n) break;
+        // Halo rows of U_{k+1} from the neighbours (rows 0 and B+1 of Tn).
+        bool ok = true;
+        for (int q = tid; q < 2 * nq && ok; q += nthr) {
+            const int side = q < nq ? 0 : 1;
+            const int qq = side ? q - nq : q;
+            if (side == 0 ? b == 0 : b == G - 1) continue;
+            float4 v;
+            ok = ld_tagged4(mine + (side * 2 + par) * hw + 4 * qq, tag, v, p);
+            if (ok) store_quad(Tn + (side ? B + 1 : 0) * sp + 4 + 4 * qq, v, min(4, nx - 4 * qq));
+        }
+        if (__syncthreads_or(!ok)) return;  // a wait expired: the host reads the error
+        c ^= 1;
+        ++k;
+    }
+    float *dst = p.u[p.cur ^ (int)(k & 1)];
+    for (int u = tid; u < B * nq; u += nthr) {
+        const int lr = u / nq + 1, q = u - (lr - 1) * nq;
+        store_quad(dst + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q,
+                   ld4(T[c] + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+    }
+    if (b == 0 && tid == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = k;
+        d->res0 = res0;
+        d->res_last = res_last;
+        d->rmax_last = rmax_last;
+        d->n_checks = n_checks;
+        d->cur = p.cur ^ (int)(k & 1);
+        d->task_sweeps = 0;
+        d->barriers = ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
+        __threadfence();
+        d->run_id = p.run_id;
+    }
+}
+
+// ===========================================================================
 // Per-launch path: one pass per launch (the launch boundary is the barrier).
 __device__ __forceinline__ void write_partial(const SweepParams &p, double s2, float rmax) {
     block_reduce(s2, rmax);
@@ -1020,10 +1203,37 @@ cudaError_t prepare_kernels() {
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
     if (e != cudaSuccess) return e;
+    // Dynamic shared memory may use what the opt-in limit leaves after the
+    // kernel's static shared memory.
+    auto dyn_limit = [&](const void *fn, int *limit) -> cudaError_t {
+        cudaFuncAttributes a;
+        cudaError_t r = cudaFuncGetAttributes(&a, fn);
+        if (r != cudaSuccess) return r;
+        *limit = optin - (int)a.sharedSizeBytes;
+        return cudaSuccess;
+    };
+    size_t local_max = (size_t)optin;
+    for (int poisson = 0; poisson < 2; ++poisson) {
+        const void *fn = poisson ? (const void *)k_persistent_local<true>
+                                 : (const void *)k_persistent_local<false>;
+        int lim = 0;
+        if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+        if (e != cudaSuccess) return e;
+        if ((size_t)lim < local_max) local_max = (size_t)lim;
+    }
+    g_local_smem_max = local_max;
     for (int poisson = 0; poisson < 2; ++poisson) {
         for (int c = 0; c < kNumStreamConfigs; ++c) {
             const size_t bytes = stream_smem_bytes(c, poisson != 0);
-            g_cfg_ok[poisson][c] = bytes <= (size_t)optin;
+            g_cfg_ok[poisson][c] = true;
+            for (int persistent = 0; persistent < 2; ++persistent) {
+                const void *fn = poisson ? stream_fn<true>(c, persistent != 0)
+                                         : stream_fn<false>(c, persistent != 0);
+                int lim = 0;
+                if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
+                if (bytes > (size_t)lim) g_cfg_ok[poisson][c] = false;
+            }
             if (!g_cfg_ok[poisson][c]) continue;
             for (int persistent = 0; persistent < 2; ++persistent) {
                 const void *fn = poisson ? stream_fn<true>(c, persistent != 0)
@@ -1037,11 +1247,15 @@ cudaError_t prepare_kernels() {
     return cudaSuccess;
 }
 
+size_t g_local_smem_max = 0;
+
 bool stream_config_ok(int cfg, bool poisson) {
     return cfg >= 0 && cfg < kNumStreamConfigs && g_cfg_ok[poisson ? 1 : 0][cfg];
 }
 
 const void *kernel_persistent(int variant, bool poisson, int cfg) {
+    if (variant == kVariantLocal)
+        return poisson ? (const void *)k_persistent_local<true> : (const void *)k_persistent_local<false>;
     if (variant == kVariantStream) return poisson ? stream_fn<true>(cfg, true) : stream_fn<false>(cfg, true);
     return poisson ? (const void *)k_persistent_direct<true> : (const void *)k_persistent_direct<false>;
 }
@@ -1071,9 +1285,10 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
                               cudaStream_t s) {
     SweepParams arg = p;
     void *args[] = {&arg};
+    const size_t smem = variant == kVariantLocal ? local_smem_bytes(p.nx, p.local_rows, poisson)
+                                                 : dyn_smem(variant, poisson, cfg);
     return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
-                                       dim3(block_threads(variant)), args,
-                                       dyn_smem(variant, poisson, cfg), s);
+                                       dim3(block_threads(variant)), args, smem, s);
 }
 
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,

@@ -31,6 +31,7 @@ PK_EDEVICE = -7
 PK_VARIANT_AUTO = 0
 PK_VARIANT_DIRECT = 1
 PK_VARIANT_STREAM = 2
+PK_VARIANT_LOCAL = 3
 
 PK_FLAG_LAUNCH_PROBLEM_GRID = 0x1
 PK_FLAG_ALTERNATE_DIRECTION = 0x2
@@ -119,6 +120,8 @@ _SIGS = {
                                      ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_launch": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
                                             ctypes.POINTER(pk_run_info)]),
+    "pk_run_sweeps_graph": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+                                           ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int64,
                                              _VP, _VP, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_float, ctypes.c_int,
@@ -239,6 +242,12 @@ def pk_run_sweeps(ctx, n, tol=0.0, check_every=0):
 def pk_run_sweeps_launch(ctx, n, tol=0.0, check_every=0):
     info = pk_run_info()
     _check(_lib.pk_run_sweeps_launch(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
+    return info.as_dict()
+
+
+def pk_run_sweeps_graph(ctx, n, tol=0.0, check_every=0):
+    info = pk_run_info()
+    _check(_lib.pk_run_sweeps_graph(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
     return info.as_dict()
 
 

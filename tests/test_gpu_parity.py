@@ -44,7 +44,8 @@ def run_pk(pk, u0, f, n, tol=0.0, ce=0, path="persistent", **opts):
     opt = pk.pk_options_default(**opts)
     ctx = pk.pk_create(nx, ny, u0, f, opt)
     try:
-        fn = pk.pk_run_sweeps if path == "persistent" else pk.pk_run_sweeps_launch
+        fn = {"persistent": pk.pk_run_sweeps, "launch": pk.pk_run_sweeps_launch,
+              "graph": pk.pk_run_sweeps_graph}[path]
         info = fn(ctx, n, tol, ce)
         out = pk.pk_get_field(ctx)
     finally:
@@ -69,8 +70,8 @@ SIZES = [(1, 1), (1, 7), (7, 1), (2, 2), (5, 3), (63, 65), (129, 3), (300, 301),
 
 
 @pytest.mark.parametrize("nx,ny", SIZES, ids=["%dx%d" % s for s in SIZES])
-@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["direct", "stream", "local"])
+@pytest.mark.parametrize("path", ["persistent", "launch", "graph"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_small_grids_bit_exact(pk, nx, ny, variant, path, poisson):
     u0 = inputs.random_field(nx, ny, seed=100 + nx + 7 * ny)
@@ -78,7 +79,8 @@ def test_small_grids_bit_exact(pk, nx, ny, variant, path, poisson):
     n, ce = 7, 3
     want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=1e-30, check_every=ce)
     got, info = run_pk(pk, u0, f, n, 1e-30, ce, path=path, variant=variant)
-    assert info["variant"] == variant
+    # the per-launch and graph paths run DIRECT kernels for a LOCAL context
+    assert info["variant"] == (1 if variant == 3 and path != "persistent" else variant)
     assert_same_bits(got, want)
     check_info(info, oinfo)
 
@@ -112,14 +114,15 @@ def test_persistent_and_launch_residuals_identical(pk):
     u0 = inputs.random_field(nx, ny, seed=5)
     for variant in (1, 2):
         _, a = run_pk(pk, u0, None, 30, 1e-30, 5, path="persistent", variant=variant)
-        _, b = run_pk(pk, u0, None, 30, 1e-30, 5, path="launch", variant=variant)
-        assert a["grid"] == b["grid"]
-        assert a["res0"] == b["res0"] and a["res_last"] == b["res_last"]
-        assert a["res_max_last"] == b["res_max_last"]
+        for path in ("launch", "graph"):
+            _, b = run_pk(pk, u0, None, 30, 1e-30, 5, path=path, variant=variant)
+            assert a["grid"] == b["grid"]
+            assert a["res0"] == b["res0"] and a["res_last"] == b["res_last"]
+            assert a["res_max_last"] == b["res_max_last"]
 
 
-@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["direct", "stream", "local"])
+@pytest.mark.parametrize("path", ["persistent", "launch", "graph"])
 def test_early_exit_16x16_poisson(pk, variant, path):
     n = 16
     f = inputs.uniform_pm1(7, n * n).reshape(n, n)
@@ -186,7 +189,7 @@ def test_create_device_with_torch_buffers(pk):
 
 # ---- the five workloads ------------------------------------------------------
 
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("path", ["persistent", "launch", "graph"])
 def test_laplace_top_edge_64(pk, path):
     w = inputs.workload_laplace_top_edge(64)
     want, _ = oracle.jacobi_run(w["u0"], n=100)
@@ -195,7 +198,7 @@ def test_laplace_top_edge_64(pk, path):
     assert_same_bits(got, want)
 
 
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("path", ["persistent", "launch", "graph"])
 def test_laplace_random_512(pk, path):
     w = inputs.workload_laplace_random(512, seed=1)
     want, _ = oracle.jacobi_run(w["u0"], n=1000, threads=THREADS)
@@ -204,7 +207,7 @@ def test_laplace_random_512(pk, path):
     assert_same_bits(got, want)
 
 
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("path", ["persistent", "launch", "graph"])
 def test_poisson_4096_residual_every_10(pk, path):
     w = inputs.workload_poisson_random_source(4096, seed=2)
     want, oinfo = oracle.jacobi_run(w["u0"], f=w["f"], n=2000, tol=1e-4, check_every=10,
@@ -362,7 +365,7 @@ def test_barrier_and_cg_sync_microbenchmarks(pk):
         pk.pk_destroy(ctx)
 
 
-@pytest.mark.parametrize("variant", [1, 2], ids=["direct", "stream"])
+@pytest.mark.parametrize("variant", [1, 2, 3], ids=["direct", "stream", "local"])
 def test_barrier_timeout_is_reported_not_hung(pk, variant):
     """Fault injection on the host's say-so: one CTA leaves without arriving;
     the others give up after the (short) limit and the call returns
@@ -386,10 +389,10 @@ def test_barrier_timeout_is_reported_not_hung(pk, variant):
 
 def test_oversubscribed_grid_is_refused(pk):
     u0 = inputs.random_field(256, 256, seed=2)
-    ctx = pk.pk_create(256, 256, u0, None)
+    ctx = pk.pk_create(256, 256, u0, None, pk.pk_options_default(variant=1))
     cap = pk.pk_get_plan(ctx)["coop_max"]
     pk.pk_destroy(ctx)
-    ctx = pk.pk_create(256, 256, u0, None, pk.pk_options_default(grid_override=cap + 1))
+    ctx = pk.pk_create(256, 256, u0, None, pk.pk_options_default(variant=1, grid_override=cap + 1))
     try:
         with pytest.raises(pk.PkError) as e:
             pk.pk_run_sweeps(ctx, 3)
@@ -477,7 +480,7 @@ def test_barrier_kinds_timeout_then_recover(pk, kind):
 def test_barrier_wait_profile(pk):
     u0 = inputs.random_field(700, 300, seed=8)
     ctx = pk.pk_create(700, 300, u0, None,
-                       pk.pk_options_default(flags=pk.PK_FLAG_PROFILE_BARRIER))
+                       pk.pk_options_default(variant=1, flags=pk.PK_FLAG_PROFILE_BARRIER))
     try:
         info = pk.pk_run_sweeps(ctx, 25)
         waits = pk.pk_barrier_wait_ns(ctx)
@@ -530,3 +533,59 @@ def test_stream_ring_refill_race_regression(pk):
     finally:
         pk.pk_destroy(cs)
         pk.pk_destroy(cd)
+
+
+def test_graph_path_long_runs_and_reuse(pk):
+    """Segments longer than one graph (1000 launches), odd and even check
+    intervals, and cached graphs reused across calls from both buffer
+    parities."""
+    nx, ny = 130, 77
+    u0 = inputs.random_field(nx, ny, seed=91)
+    ctx = pk.pk_create(nx, ny, u0, None)
+    try:
+        total = 0
+        for n, tol, ce in ((2500, 0.0, 0), (37, 1e-30, 7), (40, 1e-30, 10), (2501, 0.0, 0),
+                           (9, 1e-30, 3)):
+            info = pk.pk_run_sweeps_graph(ctx, n, tol, ce)
+            assert info["sweeps_done"] == n
+            total += n
+        want, _ = oracle.jacobi_run(u0, n=total, threads=THREADS)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+# ---- LOCAL: shared-memory bands, tagged neighbour halos ---------------------------
+
+LOCAL_CASES = [(1030, 9, 0), (63, 65, 0), (512, 512, 0), (100, 100, 7), (300, 301, 0),
+               (64, 64, 0), (257, 50, 3), (5, 1000, 0)]
+
+
+@pytest.mark.parametrize("nx,ny,grid", LOCAL_CASES, ids=["%dx%d-g%d" % c for c in LOCAL_CASES])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_local_variant_bit_exact(pk, nx, ny, grid, poisson):
+    u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
+    f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, tol, ce in ((41, 0.0, 0), (33, 1e-30, 8), (12, 1e-30, 1)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, tol, ce, variant=3, grid_override=grid)
+        assert info["variant"] == 3
+        if grid:
+            assert info["grid"] == min(grid, ny)
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+def test_local_variant_repeated_runs(pk):
+    """Halo tags restart every run: many short runs in a row on one context."""
+    u0 = inputs.random_field(512, 512, seed=77)
+    ctx = pk.pk_create(512, 512, u0, None, pk.pk_options_default(variant=3))
+    try:
+        total = 0
+        for n in (1, 2, 3, 1, 5, 8, 13, 1, 1, 2):
+            pk.pk_run_sweeps(ctx, n)
+            total += n
+        want, _ = oracle.jacobi_run(u0, n=total)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
