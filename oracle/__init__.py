@@ -10,6 +10,8 @@ from .oracle import (  # noqa: F401
     sweep,
     residual,
     jacobi_run,
+    rb_half_sweep,
+    rb_run,
     axpy,
     task_sequence,
     barrier_stress_expected,

@@ -66,6 +66,12 @@ def _load():
     lib.oracle_barrier_stress.restype = None
     lib.oracle_barrier_stress.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.POINTER(ctypes.c_uint64)]
+    lib.oracle_rb_half_sweep.restype = None
+    lib.oracle_rb_half_sweep.argtypes = [ctypes.c_int, ctypes.c_int, _F32P, _F32P, ctypes.c_int]
+    lib.oracle_rb_run.restype = ctypes.c_int
+    lib.oracle_rb_run.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_float, _F32P, _F32P,
+                                  ctypes.c_int64, ctypes.c_float, ctypes.c_int, _F32P,
+                                  ctypes.POINTER(_CInfo)]
     lib.oracle_has_openmp.restype = ctypes.c_int
     lib.oracle_has_openmp.argtypes = []
     _lib = lib
@@ -145,6 +151,35 @@ def jacobi_run(u0, f=None, n=0, tol=0.0, check_every=0, h2v=None, threads=1):
                                    _ptr(out), ctypes.byref(info))
     if rc != 0:
         raise MemoryError("oracle_jacobi_run failed (%d)" % rc)
+    return out, OracleInfo(int(info.sweeps_done), float(info.res0), float(info.res_last),
+                           float(np.float32(info.rmax_last)), int(info.n_checks))
+
+
+def rb_half_sweep(u, colour, g=None):
+    """One red (colour 0: i+j even) or black (colour 1) half-sweep, in place
+    on a copy of u; returns the copy."""
+    u = _f32(u).copy()
+    ny, nx = u.shape[0] - 2, u.shape[1] - 2
+    if g is not None:
+        g = _f32(g, (ny, nx), "g")
+    _load().oracle_rb_half_sweep(nx, ny, _ptr(u), _ptr(g), int(colour))
+    return u
+
+
+def rb_run(u0, f=None, n=0, tol=0.0, check_every=0, h2v=None):
+    """Red-black Gauss-Seidel from u0 (n iterations of red then black)."""
+    u0 = _f32(u0)
+    ny, nx = u0.shape[0] - 2, u0.shape[1] - 2
+    if f is not None:
+        f = _f32(f, (ny, nx), "f")
+    if h2v is None:
+        h2v = h2(nx)
+    out = np.empty_like(u0)
+    info = _CInfo()
+    rc = _load().oracle_rb_run(nx, ny, ctypes.c_float(h2v), _ptr(u0), _ptr(f), int(n),
+                               ctypes.c_float(tol), int(check_every), _ptr(out), ctypes.byref(info))
+    if rc != 0:
+        raise MemoryError("oracle_rb_run failed (%d)" % rc)
     return out, OracleInfo(int(info.sweeps_done), float(info.res0), float(info.res_last),
                            float(np.float32(info.rmax_last)), int(info.n_checks))
 

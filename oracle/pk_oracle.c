@@ -214,6 +214,73 @@ int oracle_jacobi_run(int nx, int ny, float h2, const float *u0, const float *f,
     return 0;
 }
 
+/* ---- red-black Gauss-Seidel -------------------------------------------
+ * [P1] "Implementation details and correctness": first update every point
+ * whose i and j have the same parity (red), then every other point (black);
+ * a half-sweep reads only the other colour, so the update is in place and
+ * the black half-sweep sees the new red values.  Each point uses the same
+ * arithmetic as the Jacobi update. */
+void oracle_rb_half_sweep(int nx, int ny, float *u, const float *g, int colour)
+{
+    for (int j = 1; j <= ny; ++j) {
+        for (int i = 1; i <= nx; ++i) {
+            if (((i + j) & 1) != colour) continue;
+            float t = stencil_t(nx, u, g, j, i);
+            AT(u, nx, j, i) = 0.25f * t;
+        }
+    }
+}
+
+/* Full red-black run: iteration k = red half-sweep then black half-sweep.
+ * Checks, exit rule and returned iterate as oracle_jacobi_run (the residual
+ * of U_k is taken before iteration k). */
+int oracle_rb_run(int nx, int ny, float h2, const float *u0, const float *f, int64_t n, float tol,
+                  int check_every, float *out, oracle_info *info)
+{
+    if (nx <= 0 || ny <= 0 || n < 0) return -1;
+    size_t cells = (size_t)(nx + 2) * (size_t)(ny + 2);
+    float *g = NULL;
+    if (f) {
+        g = (float *)malloc(sizeof(float) * (size_t)nx * (size_t)ny);
+        if (!g) return -1;
+        oracle_scale_source(nx, ny, h2, f, g);
+    }
+    memcpy(out, u0, sizeof(float) * cells);
+    int checks = (tol > 0.0f && check_every > 0);
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.0f;
+    int32_t n_checks = 0;
+    int64_t k = 0;
+    for (;;) {
+        if (checks && (k % check_every) == 0) {
+            double res;
+            float rmax;
+            oracle_residual(nx, ny, out, g, &res, &rmax);
+            ++n_checks;
+            res_last = res;
+            rmax_last = rmax;
+            if (k == 0) {
+                res0 = res;
+            } else if (res < (double)tol * res0) {
+                break;
+            }
+        }
+        if (k == n) break;
+        oracle_rb_half_sweep(nx, ny, out, g, 0);
+        oracle_rb_half_sweep(nx, ny, out, g, 1);
+        ++k;
+    }
+    if (info) {
+        info->sweeps_done = k;
+        info->res0 = res0;
+        info->res_last = res_last;
+        info->rmax_last = rmax_last;
+        info->n_checks = n_checks;
+    }
+    free(g);
+    return 0;
+}
+
 /* y <- fl32(fl32(a * x) + y), element by element. */
 void oracle_axpy(int64_t len, float a, const float *x, float *y)
 {

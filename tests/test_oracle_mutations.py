@@ -28,14 +28,18 @@ MUTATIONS = [
     ("residual centre weight", "float c4 = 4.0f * AT(u, nx, j, i);",
      "float c4 = 3.0f * AT(u, nx, j, i);"),
     ("residual L1 norm", "double sq = (double)r * (double)r;", "double sq = fabs((double)r);"),
-    ("exit test", "} else if (res < (double)tol * res0) {",
-     "} else if (res < (double)tol * res0 * 2.0) {"),
+    ("exit test",
+     "} else if (res < (double)tol * res0) {\n                break;\n            }\n        }\n        if (k == n) break;\n        oracle_sweep(",
+     "} else if (res < (double)tol * res0 * 2.0) {\n                break;\n            }\n        }\n        if (k == n) break;\n        oracle_sweep("),
     ("returned iterate", "memcpy(out, buf[k & 1], sizeof(float) * cells);",
      "memcpy(out, buf[(k + 1) & 1], sizeof(float) * cells);"),
     ("ring not copied", "AT(dst, nx, j, nx + 1) = AT(src, nx, j, nx + 1);",
      "AT(dst, nx, j, nx + 1) = 0.0f;"),
     ("axpy operand", "float ax = a * x[q];", "float ax = a * y[q];"),
     ("stress peer", "peers[0] = (b + 1) % nblocks;", "peers[0] = (b + 2) % nblocks;"),
+    ("red-black colour order", "oracle_rb_half_sweep(nx, ny, out, g, 0);\n        oracle_rb_half_sweep(nx, ny, out, g, 1);",
+     "oracle_rb_half_sweep(nx, ny, out, g, 1);\n        oracle_rb_half_sweep(nx, ny, out, g, 0);"),
+    ("red-black colouring", "if (((i + j) & 1) != colour) continue;", "if ((i & 1) != colour) continue;"),
 ]
 
 

@@ -338,3 +338,77 @@ def test_barrier_stress_expected_brute_force():
                 for w in range(W):
                     acc += _mix64(((r * G + p) * W + w) + 1) & 0xFFFFFFFF
         assert int(got[b]) == acc % (1 << 64)
+
+
+# ---- red-black Gauss-Seidel ---------------------------------------------------
+
+def test_redblack_worked_4x4():
+    g = _read_golden("worked_4x4_redblack.txt")
+    u0 = _matrix(g["u0"])
+    red = oracle.rb_half_sweep(u0, 0)
+    assert _same_bits(red, _matrix(g["red1"]))
+    u1 = oracle.rb_half_sweep(red, 1)
+    assert _same_bits(u1, _matrix(g["u1"]))
+    out, info = oracle.rb_run(u0, n=2)
+    assert _same_bits(out, _matrix(g["u2"])) and info.sweeps_done == 2
+
+
+@pytest.mark.parametrize("nx,ny", [(13, 9), (1, 1), (6, 11)])
+def test_redblack_linear_field_fixed_point(nx, ny):
+    j, i = np.mgrid[0:ny + 2, 0:nx + 2]
+    u = (5 * i + 3 * j - 4).astype(np.float32)
+    out, _ = oracle.rb_run(u, n=25)
+    assert _same_bits(out, u)
+
+
+@pytest.mark.parametrize("poisson", [False, True])
+def test_redblack_3x3_converges_to_dense_solve(poisson):
+    u0 = inputs.random_field(3, 3, seed=15)
+    u0[1:-1, 1:-1] = 0.0
+    f = np.array([[40, -10, 3], [0, 25, -30], [7, 1, -2]], np.float32) if poisson else None
+    exact = _dense_solve(u0, f, oracle.h2(3))
+    out, _ = oracle.rb_run(u0, f=f, n=60)
+    assert np.abs(out - exact).max() <= 1e-6 * np.abs(exact).max()
+
+
+def test_redblack_transpose_bit_exact():
+    n = 15
+    u = inputs.random_field(n, n, seed=25)
+    f = inputs.uniform_pm1(26, n * n).reshape(n, n)
+    out, _ = oracle.rb_run(u, f=f, n=11)
+    outT, _ = oracle.rb_run(u.T.copy(), f=f.T.copy(), n=11)
+    assert _same_bits(outT, out.T)
+
+
+def test_redblack_asymptotic_rate_is_jacobi_squared():
+    """Gauss-Seidel with red-black ordering has spectral radius rho_J^2
+    (Young), rho_J = cos(pi h): per iteration the residual falls twice as
+    fast (in log) as Jacobi's."""
+    n = 24
+    f = inputs.uniform_pm1(9, n * n).reshape(n, n)
+    u0 = np.zeros((n + 2, n + 2), np.float32)
+    g = oracle.scale_source(n, n, oracle.h2(n), f)
+    cur = u0
+    res = []
+    for k in range(200):
+        res.append(oracle.residual(cur, g)[0])
+        cur = oracle.rb_half_sweep(oracle.rb_half_sweep(cur, 0, g), 1, g)
+    rho = math.cos(math.pi / (n + 1)) ** 2
+    got = (res[199] / res[149]) ** (1.0 / 50)
+    assert got == pytest.approx(rho, rel=2e-3)
+    # and Jacobi's rate over the same window is rho_J
+    cur = u0
+    rj = []
+    for k in range(400):
+        rj.append(oracle.residual(cur, g)[0])
+        cur = oracle.sweep(cur, g)
+    assert (rj[399] / rj[299]) ** (1.0 / 100) == pytest.approx(math.sqrt(rho), rel=2e-3)
+
+
+def test_redblack_check_schedule_matches_separate_runs():
+    n = 20
+    u = inputs.random_field(n, n, seed=35)
+    out, info = oracle.rb_run(u, n=25, tol=1e-30, check_every=10)
+    assert info.sweeps_done == 25 and info.n_checks == 3
+    u20, _ = oracle.rb_run(u, n=20)
+    assert info.res_last == oracle.residual(u20)[0]
