@@ -320,6 +320,34 @@ def latency_extras(pk):
         }
     finally:
         pk.pk_destroy(ctx)
+    # Red-black Gauss-Seidel: 512^2 time per iteration, and iterations to
+    # convergence against Jacobi sweeps on a 64^2 Poisson problem
+    w = inputs.workload_laplace_random(512, 1)
+    ctx = pk.pk_create(512, 512, w["u0"], None)
+    try:
+        for _ in range(2):
+            pk.pk_run_redblack(ctx, 500)
+            pk.pk_run_redblack_launch(ctx, 500)
+        rbp = statistics.median(pk.pk_run_redblack(ctx, 500)["device_us"] / 500 for _ in range(5))
+        rbl = statistics.median(pk.pk_run_redblack_launch(ctx, 500)["device_us"] / 500
+                                for _ in range(5))
+    finally:
+        pk.pk_destroy(ctx)
+    w = inputs.workload_poisson_random_source(64, 5)
+    ctx = pk.pk_create(64, 64, w["u0"], w["f"])
+    try:
+        jac = pk.pk_run_sweeps(ctx, 1000000, 1e-6, 10)
+        pk.pk_set_field(ctx, w["u0"])
+        rb = pk.pk_run_redblack(ctx, 1000000, 1e-6, 10)
+    finally:
+        pk.pk_destroy(ctx)
+    out["redblack"] = {
+        "laplace_512_us_per_iteration": {"persistent": rbp, "launch": rbl,
+                                         "persistent_speedup": rbl / rbp},
+        "poisson_64_tol1e-6_check10": {"jacobi_sweeps": jac["sweeps_done"],
+                                       "redblack_iterations": rb["sweeps_done"],
+                                       "jacobi_us": jac["device_us"], "redblack_us": rb["device_us"]},
+    }
     # Temporal blocking: two sweeps per HBM pass, same bits (16384^2, 100 sweeps)
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}

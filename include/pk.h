@@ -200,6 +200,21 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
  * pk_run_sweeps_launch. */
 int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
 
+/* Red-black Gauss-Seidel ([P1] "Implementation details and correctness"):
+ * each of n iterations updates every red point (i + j even) and then every
+ * black point, in place in the current buffer, each point with the Jacobi
+ * update's arithmetic; a half-sweep reads only the other colour.  One
+ * cooperative launch with a grid barrier after each half-sweep.  Checks,
+ * exit rule (the residual of U_k, taken before iteration k) and info as
+ * pk_run_sweeps; sweeps_done counts iterations and the current buffer does
+ * not change.  Errors as pk_run_sweeps. */
+int pk_run_redblack(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
+
+/* The same iterations with one launch per half-sweep (the launch boundary
+ * is the barrier) and a host decision on check iterations.  Same bits as
+ * pk_run_redblack. */
+int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
+
 /* Copy the current iterate to / from a packed (ny+2) x (nx+2) HOST array.
  * pk_set_field writes both buffers (ring included) and makes buffer A
  * current.  Errors: PK_EINVAL, PK_EBUSY (task kernel live), PK_ECUDA. */

@@ -86,6 +86,7 @@ struct pk_ctx {
     unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
     int spin_valid = 0;                     // entries written by the last profiled run
     unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
+    int rb_grid = 0;                        // red-black persistent grid (0 = not planned)
     unsigned *stress_lines = nullptr;
     int stress_cap = 0;
     unsigned long long *stress_out = nullptr;
@@ -836,6 +837,112 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     ctx->cur = cur;
     fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->grid, launch_variant(ctx));
+    return PK_OK;
+}
+
+}  // extern "C"
+
+namespace {
+int rb_plan(pk_ctx *ctx) {
+    if (ctx->rb_grid > 0) return PK_OK;
+    int per_sm = 0;
+    const int cap = coop_capacity(ctx, kernel_persistent_rb(ctx->poisson), kDirectThreads, 0, &per_sm);
+    if (cap < 0) return PK_ECUDA;
+    if (cap == 0) return fail(ctx, PK_ENORESIDENT, "red-black kernel does not fit on an SM");
+    long long need = (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+    if (need < 1) need = 1;
+    int grid = (int)(need < cap ? need : cap);
+    if (ctx->opt.grid_override > 0) grid = ctx->opt.grid_override;
+    int rc = ensure_partials(ctx, grid > cap ? grid : cap);
+    if (rc != PK_OK) return rc;
+    ctx->rb_grid = grid;
+    return PK_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int pk_run_redblack(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
+    if (!ctx) return PK_EINVAL;
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_redblack: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_redblack: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_redblack: the task kernel is live");
+    int rc = rb_plan(ctx);
+    if (rc != PK_OK) return rc;
+    SweepParams p = base_params(ctx);
+    p.n = n;
+    p.tol = tol;
+    p.check_every = check_every;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    cudaError_t e = launch_persistent_rb(ctx->poisson, ctx->rb_grid, p, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(red-black)");
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
+                                ctx->stream));
+    rc = bar_status(ctx, p.bar, "pk_run_redblack");
+    if (rc != PK_OK) {
+        ctx->sweep_bar_base = 0;
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, ctx->rb_grid, kVariantDirect);
+        return rc;
+    }
+    if (ctx->h_info->run_id != p.run_id)
+        return fail(ctx, PK_EDEVICE, "pk_run_redblack: kernel did not report its result");
+    ctx->sweep_bar_base = ctx->h_info->bar_count_end;
+    fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, ctx->rb_grid, kVariantDirect);
+    return PK_OK;
+}
+
+int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
+    if (!ctx) return PK_EINVAL;
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_redblack_launch: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_redblack_launch: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_redblack_launch: the task kernel is live");
+    int rc = rb_plan(ctx);
+    if (rc != PK_OK) return rc;
+    SweepParams p = base_params(ctx);
+    const bool checks = tol > 0.f && check_every > 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    for (;;) {
+        const bool check = checks && (k % check_every) == 0;
+        if (k == n && !check) break;
+        cudaError_t e = cudaSuccess;
+        if (check) {
+            p.pass_check = 1;
+            p.pass_parity = 0;
+            e = launch_once_rb(ctx->poisson, ctx->rb_grid, p, ctx->stream);
+            if (e == cudaSuccess)
+                e = launch_finalize(kVariantDirect, ctx->rb_grid, p, &ctx->scratch->res, ctx->stream);
+            if (e == cudaSuccess)
+                e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
+                                    cudaMemcpyDeviceToHost, ctx->stream);
+            if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+            if (e != cudaSuccess) return cuda_fail(ctx, e, "red-black residual");
+            const double res = ctx->h_res->res;
+            ++n_checks;
+            res_last = res;
+            rmax_last = ctx->h_res->rmax;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)tol * res0)
+                break;
+        }
+        if (k == n) break;
+        p.pass_check = 0;
+        for (int colour = 0; colour < 2 && e == cudaSuccess; ++colour) {
+            p.pass_k = colour;
+            e = launch_once_rb(ctx->poisson, ctx->rb_grid, p, ctx->stream);
+        }
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "red-black half-sweep");
+        ++k;
+    }
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->rb_grid, kVariantDirect);
     return PK_OK;
 }
 

@@ -176,6 +176,10 @@ cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const Swee
                         cudaStream_t s);
 cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
                             cudaStream_t s);
+// Red-black Gauss-Seidel (DIRECT-style passes, in place on p.u[p.cur]).
+const void *kernel_persistent_rb(bool poisson);
+cudaError_t launch_persistent_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s);
+cudaError_t launch_once_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s);
 cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long long gpitch,
                                 float h2, cudaStream_t s);
 cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s);

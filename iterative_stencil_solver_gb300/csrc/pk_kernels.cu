@@ -793,6 +793,118 @@ __global__ void __launch_bounds__(kStreamThreads) k_once_stream(SweepParams p) {
     if (p.pass_check) write_partial(p, s2, rmax);
 }
 
+// Red-black Gauss-Seidel ("Persistent Kernels...", "Implementation details
+// and correctness"): in place, red points (i+j even) first, then black
+// points; a half-sweep reads only the other colour, so it has no hazard
+// within itself, and a grid barrier separates the two.  Each point uses the
+// Jacobi arithmetic; a thread stores only the two points of its float4 group
+// that have the half-sweep's colour.
+template <bool POISSON>
+__device__ __forceinline__ void pass_rb(const SweepParams &p, float *u, int colour,
+                                        unsigned first, unsigned stride) {
+    const unsigned nq = (unsigned)(p.nx + 3) >> 2;
+    const unsigned units = (unsigned)p.ny * nq;
+    for (unsigned uu = first; uu < units; uu += stride) {
+        const unsigned jm1 = uu / nq;
+        const unsigned q = uu - jm1 * nq;
+        const long long off = (long long)(jm1 + 1u) * p.pitch + 4 + 4ll * q;
+        float *c = u + off;
+        const float4 C = ld4(c);
+        const float4 S = ld4(c - p.pitch);
+        const float4 N = ld4(c + p.pitch);
+        const float W = c[-1];
+        const float E = c[4];
+        float4 G = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (POISSON) G = ld4(p.g + (long long)jm1 * p.gpitch + 4ll * q);
+        const int valid = min(4, p.nx - 4 * (int)q);
+        const float4 v = quad_update(quad_t<POISSON>(W, C, E, S, N, G));
+        // point (j, i) with i = 1 + 4q + cell has colour (i + j) & 1
+        const int c0 = (colour + 1 + (int)(jm1 + 1u)) & 1;
+        if (c0 < valid) c[c0] = c0 ? v.y : v.x;
+        if (c0 + 2 < valid) c[c0 + 2] = c0 ? v.w : v.z;
+    }
+}
+
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_rb(SweepParams p) {
+    const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned stride = gridDim.x * blockDim.x;
+    float *u = p.u[p.cur];
+    BarrierCtl ctl = make_ctl(p);
+    const bool checks = p.tol > 0.f && p.check_every > 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    for (;;) {
+        const bool check = checks && (k % p.check_every) == 0;
+        if (k == p.n && !check) break;
+        if (check) {
+            double s2 = 0.0;
+            float rmax = 0.f;
+            pass_direct<POISSON, true, false>(p, u, u, first, stride, s2, rmax);
+            Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+            block_reduce(s2, rmax);
+            if (threadIdx.x == 0) {
+                Partial pp;
+                pp.s2 = s2;
+                pp.rmax = rmax;
+                pp.pad = 0.f;
+                parts[blockIdx.x] = pp;
+            }
+            if (!grid_barrier(ctl)) return;
+            double S2;
+            float RM;
+            reduce_partials(parts, (int)gridDim.x, S2, RM);
+            const double res = sqrt(S2);
+            ++n_checks;
+            res_last = res;
+            rmax_last = RM;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)p.tol * res0)
+                break;
+        }
+        if (k == p.n) break;
+        pass_rb<POISSON>(p, u, 0, first, stride);
+        if (!grid_barrier(ctl)) return;
+        pass_rb<POISSON>(p, u, 1, first, stride);
+        if (!grid_barrier(ctl)) return;
+        ++k;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = k;
+        d->res0 = res0;
+        d->res_last = res_last;
+        d->rmax_last = rmax_last;
+        d->n_checks = n_checks;
+        d->cur = p.cur;
+        d->task_sweeps = 0;
+        d->barriers = ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
+        __threadfence();
+        d->run_id = p.run_id;
+    }
+}
+
+// Per-launch red-black: one half-sweep (colour = pass_k) or, with
+// pass_check, the residual pass.
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_once_rb(SweepParams p) {
+    const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
+    const unsigned stride = gridDim.x * blockDim.x;
+    float *u = p.u[p.cur];
+    if (p.pass_check) {
+        double s2 = 0.0;
+        float rmax = 0.f;
+        pass_direct<POISSON, true, false>(p, u, u, first, stride, s2, rmax);
+        write_partial(p, s2, rmax);
+    } else {
+        pass_rb<POISSON>(p, u, (int)(p.pass_k & 1), first, stride);
+    }
+}
+
 // Reduction of the per-CTA partials, launched with the same block size as
 // the sweep kernel so the fixed reduction tree (and the result bits) match
 // the persistent kernel's.
@@ -1297,6 +1409,26 @@ cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const Swee
     void *args[] = {&arg};
     return cudaLaunchKernel(kernel_once(variant, poisson, cfg), dim3(grid),
                             dim3(block_threads(variant)), args, dyn_smem(variant, poisson, cfg), s);
+}
+
+cudaError_t launch_persistent_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s) {
+    SweepParams arg = p;
+    void *args[] = {&arg};
+    return cudaLaunchCooperativeKernel(poisson ? (const void *)k_persistent_rb<true>
+                                               : (const void *)k_persistent_rb<false>,
+                                       dim3(grid), dim3(kDirectThreads), args, 0, s);
+}
+
+cudaError_t launch_once_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s) {
+    if (poisson)
+        k_once_rb<true><<<grid, kDirectThreads, 0, s>>>(p);
+    else
+        k_once_rb<false><<<grid, kDirectThreads, 0, s>>>(p);
+    return cudaGetLastError();
+}
+
+const void *kernel_persistent_rb(bool poisson) {
+    return poisson ? (const void *)k_persistent_rb<true> : (const void *)k_persistent_rb<false>;
 }
 
 cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,

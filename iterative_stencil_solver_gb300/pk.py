@@ -120,6 +120,10 @@ _SIGS = {
                                      ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_launch": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
                                             ctypes.POINTER(pk_run_info)]),
+    "pk_run_redblack": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+                                       ctypes.POINTER(pk_run_info)]),
+    "pk_run_redblack_launch": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
+                                              ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_graph": (ctypes.c_int, [_VP, ctypes.c_int64, ctypes.c_float, ctypes.c_int,
                                            ctypes.POINTER(pk_run_info)]),
     "pk_run_sweeps_noalloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _VP, _VP, ctypes.c_int64,
@@ -242,6 +246,18 @@ def pk_run_sweeps(ctx, n, tol=0.0, check_every=0):
 def pk_run_sweeps_launch(ctx, n, tol=0.0, check_every=0):
     info = pk_run_info()
     _check(_lib.pk_run_sweeps_launch(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
+    return info.as_dict()
+
+
+def pk_run_redblack(ctx, n, tol=0.0, check_every=0):
+    info = pk_run_info()
+    _check(_lib.pk_run_redblack(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
+    return info.as_dict()
+
+
+def pk_run_redblack_launch(ctx, n, tol=0.0, check_every=0):
+    info = pk_run_info()
+    _check(_lib.pk_run_redblack_launch(ctx, n, tol, check_every, ctypes.byref(info)), ctx)
     return info.as_dict()
 
 

@@ -589,3 +589,71 @@ def test_local_variant_repeated_runs(pk):
         assert_same_bits(pk.pk_get_field(ctx), want)
     finally:
         pk.pk_destroy(ctx)
+
+
+# ---- red-black Gauss-Seidel --------------------------------------------------------
+
+def run_rb(pk, u0, f, n, tol=0.0, ce=0, path="persistent", **opts):
+    ny, nx = u0.shape[0] - 2, u0.shape[1] - 2
+    ctx = pk.pk_create(nx, ny, u0, f, pk.pk_options_default(**opts))
+    try:
+        fn = pk.pk_run_redblack if path == "persistent" else pk.pk_run_redblack_launch
+        info = fn(ctx, n, tol, ce)
+        out = pk.pk_get_field(ctx)
+    finally:
+        pk.pk_destroy(ctx)
+    return out, info
+
+
+@pytest.mark.parametrize("nx,ny", SIZES, ids=["%dx%d" % s for s in SIZES])
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_redblack_bit_exact(pk, nx, ny, path, poisson):
+    u0 = inputs.random_field(nx, ny, seed=700 + nx + ny)
+    f = inputs.uniform_pm1(800 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    want, oinfo = oracle.rb_run(u0, f=f, n=7, tol=1e-30, check_every=3)
+    got, info = run_rb(pk, u0, f, 7, 1e-30, 3, path=path)
+    assert_same_bits(got, want)
+    check_info(info, oinfo)
+
+
+def test_redblack_worked_4x4_and_mixed_methods(pk):
+    u0 = np.zeros((4, 4), np.float32)
+    u0[0] = [0, 4, 8, 0]
+    want = np.array([[0, 4, 8, 0], [0, 1.625, 2.5625, 0], [0, 0.5625, 0.625, 0], [0, 0, 0, 0]],
+                    np.float32)
+    got, info = run_rb(pk, u0, None, 2)
+    assert_same_bits(got, want) and info["sweeps_done"] == 2
+    # Jacobi, then red-black in place, then Jacobi again on one context
+    u = inputs.random_field(90, 70, seed=3)
+    ctx = pk.pk_create(90, 70, u, None)
+    try:
+        pk.pk_run_sweeps(ctx, 5)
+        pk.pk_run_redblack(ctx, 4)
+        pk.pk_run_sweeps_launch(ctx, 3)
+        pk.pk_run_redblack_launch(ctx, 2)
+        a, _ = oracle.jacobi_run(u, n=5)
+        b, _ = oracle.rb_run(a, n=4)
+        c, _ = oracle.jacobi_run(b, n=3)
+        d, _ = oracle.rb_run(c, n=2)
+        assert_same_bits(pk.pk_get_field(ctx), d)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+@pytest.mark.parametrize("path", ["persistent", "launch"])
+def test_redblack_early_exit_and_512(pk, path):
+    n = 16
+    f = inputs.uniform_pm1(7, n * n).reshape(n, n)
+    u0 = np.zeros((n + 2, n + 2), np.float32)
+    want, oinfo = oracle.rb_run(u0, f=f, n=100000, tol=1e-4, check_every=10)
+    jac, jinfo = oracle.jacobi_run(u0, f=f, n=100000, tol=1e-4, check_every=10)
+    assert oinfo.sweeps_done < jinfo.sweeps_done  # Gauss-Seidel converges faster
+    got, info = run_rb(pk, u0, f, 100000, 1e-4, 10, path=path)
+    check_info(info, oinfo)
+    assert_same_bits(got, want)
+    w = inputs.workload_laplace_random(512, seed=1)
+    want, _ = oracle.rb_run(w["u0"], n=300)
+    got, info = run_rb(pk, w["u0"], None, 300, path=path)
+    assert info["sweeps_done"] == 300
+    assert_same_bits(got, want)
