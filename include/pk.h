@@ -204,7 +204,9 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
  * each of n iterations updates every red point (i + j even) and then every
  * black point, in place in the current buffer, each point with the Jacobi
  * update's arithmetic; a half-sweep reads only the other colour.  One
- * cooperative launch with a grid barrier after each half-sweep.  Checks,
+ * cooperative launch: on a LOCAL context the bands stay in shared memory
+ * and neighbours trade tagged boundary rows after each half-sweep; else a
+ * grid barrier follows each half-sweep.  Checks,
  * exit rule (the residual of U_k, taken before iteration k) and info as
  * pk_run_sweeps; sweeps_done counts iterations and the current buffer does
  * not change.  Errors as pk_run_sweeps. */

@@ -873,23 +873,31 @@ int pk_run_redblack(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_i
     p.n = n;
     p.tol = tol;
     p.check_every = check_every;
+    const bool local = ctx->variant == kVariantLocal;
+    const int grid = local ? ctx->grid : ctx->rb_grid;
+    if (local)
+        PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0,
+                                    (size_t)ctx->grid * local_halo_words(ctx->nx) * sizeof(unsigned long long),
+                                    ctx->stream));
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_persistent_rb(ctx->poisson, ctx->rb_grid, p, ctx->stream);
+    cudaError_t e = local ? launch_persistent_local_rb(ctx->poisson, grid, p, ctx->stream)
+                          : launch_persistent_rb(ctx->poisson, grid, p, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(red-black)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
                                 ctx->stream));
+    const int used = local ? (int)kVariantLocal : (int)kVariantDirect;
     rc = bar_status(ctx, p.bar, "pk_run_redblack");
     if (rc != PK_OK) {
         ctx->sweep_bar_base = 0;
-        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, ctx->rb_grid, kVariantDirect);
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, used);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
         return fail(ctx, PK_EDEVICE, "pk_run_redblack: kernel did not report its result");
     ctx->sweep_bar_base = ctx->h_info->bar_count_end;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
-              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, ctx->rb_grid, kVariantDirect);
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid, used);
     return PK_OK;
 }
 

@@ -180,6 +180,9 @@ cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, Residua
 const void *kernel_persistent_rb(bool poisson);
 cudaError_t launch_persistent_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s);
 cudaError_t launch_once_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s);
+// Red-black on the LOCAL layout (shared-memory bands, tagged halo rows).
+cudaError_t launch_persistent_local_rb(bool poisson, int grid, const SweepParams &p,
+                                       cudaStream_t s);
 cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long long gpitch,
                                 float h2, cudaStream_t s);
 cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s);

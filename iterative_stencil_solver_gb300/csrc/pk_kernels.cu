@@ -888,6 +888,145 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_rb(SweepParams p)
     }
 }
 
+// Red-black on the LOCAL layout: the band stays in shared memory (one copy,
+// updated in place) and, after every half-sweep, each CTA sends its first
+// and last rows to its neighbours as tagged words (tag = half-sweep index
+// + 1) and waits for theirs before the next half-sweep.  No grid barrier
+// between half-sweeps; the residual check still uses it.
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_local_rb(SweepParams p) {
+    extern __shared__ __align__(16) float tile[];
+    const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
+    const int nx = p.nx, ny = p.ny;
+    const int r0 = 1 + (int)((long long)ny * b / G);
+    const int r1 = 1 + (int)((long long)ny * (b + 1) / G);
+    const int B = r1 - r0;
+    const int sp = p.local_pitch, spq = sp / 4;
+    const int nq = (nx + 3) >> 2, gw = 4 * nq;
+    float *T = tile;
+    float *gs = tile + (size_t)2 * (p.local_rows + 2) * sp;  // same layout as k_persistent_local
+    const size_t hw = (size_t)4 * nq;
+    unsigned long long *mine = p.halo + (size_t)b * 4 * hw;
+    unsigned long long *up = b > 0 ? p.halo + (size_t)(b - 1) * 4 * hw : nullptr;
+    unsigned long long *down = b < G - 1 ? p.halo + (size_t)(b + 1) * 4 * hw : nullptr;
+    float *u = p.u[p.cur];
+    for (int q = tid; q < (B + 2) * spq; q += nthr) {
+        const int lr = q / spq, c4 = q - lr * spq;
+        *reinterpret_cast<float4 *>(T + lr * sp + 4 * c4) =
+            ld4(u + (long long)(r0 - 1 + lr) * p.pitch + 4 * c4);
+    }
+    if (POISSON) {
+        for (int q = tid; q < B * nq; q += nthr) {
+            const int lr = q / nq, c4 = q - lr * nq;
+            *reinterpret_cast<float4 *>(gs + lr * gw + 4 * c4) =
+                ld4(p.g + (long long)(r0 - 1 + lr) * p.gpitch + 4 * c4);
+        }
+    }
+    __syncthreads();
+    BarrierCtl ctl = make_ctl(p);
+    const bool checks = p.tol > 0.f && p.check_every > 0;
+    long long k = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    for (;;) {
+        const bool check = checks && (k % p.check_every) == 0;
+        if (k == p.n && !check) break;
+        if (b == p.skip_cta && k == p.skip_at) return;  // fault injection (host-driven)
+        if (check) {
+            double s2 = 0.0;
+            float rmax = 0.f;
+            for (int uu = tid; uu < B * nq; uu += nthr) {
+                const int lr = uu / nq + 1, q = uu - (lr - 1) * nq;
+                const float *row = T + lr * sp + 4 + 4 * q;
+                float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
+                const float4 C = ld4(row);
+                const Quad t = quad_t<POISSON>(row[-1], C, row[4], ld4(row - sp), ld4(row + sp), G4);
+                quad_residual(t, C, min(4, nx - 4 * q), s2, rmax);
+            }
+            Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+            block_reduce(s2, rmax);
+            if (tid == 0) {
+                Partial pp;
+                pp.s2 = s2;
+                pp.rmax = rmax;
+                pp.pad = 0.f;
+                parts[b] = pp;
+            }
+            if (!grid_barrier(ctl)) return;
+            double S2;
+            float RM;
+            reduce_partials(parts, G, S2, RM);
+            const double res = sqrt(S2);
+            ++n_checks;
+            res_last = res;
+            rmax_last = RM;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)p.tol * res0)
+                break;
+        }
+        if (k == p.n) break;
+        for (int colour = 0; colour < 2; ++colour) {
+            const unsigned tag = (unsigned)(2 * k + colour + 1);
+            const size_t par = tag & 1u;
+            for (int uu = tid; uu < B * nq; uu += nthr) {
+                const int lr = uu / nq + 1, q = uu - (lr - 1) * nq;
+                float *row = T + lr * sp + 4 + 4 * q;
+                float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
+                float4 C = ld4(row);
+                const float4 v =
+                    quad_update(quad_t<POISSON>(row[-1], C, row[4], ld4(row - sp), ld4(row + sp), G4));
+                const int valid = min(4, nx - 4 * q);
+                const int c0 = (colour + 1 + (r0 - 1 + lr)) & 1;  // first point of the colour
+                if (c0 == 0) {
+                    C.x = v.x;
+                    C.z = v.z;
+                } else {
+                    C.y = v.y;
+                    C.w = v.w;
+                }
+                if (c0 < valid) row[c0] = c0 ? C.y : C.x;
+                if (c0 + 2 < valid) row[c0 + 2] = c0 ? C.w : C.z;
+                if (lr == 1 && up) st_tagged4(up + (2 + par) * hw + 4 * q, C, tag);
+                if (lr == B && down) st_tagged4(down + par * hw + 4 * q, C, tag);
+            }
+            bool ok = true;
+            for (int q = tid; q < 2 * nq && ok; q += nthr) {
+                const int side = q < nq ? 0 : 1;
+                const int qq = side ? q - nq : q;
+                if (side == 0 ? b == 0 : b == G - 1) continue;
+                float4 v;
+                ok = ld_tagged4(mine + (side * 2 + par) * hw + 4 * qq, tag, v, p);
+                if (ok) store_quad(T + (side ? B + 1 : 0) * sp + 4 + 4 * qq, v, min(4, nx - 4 * qq));
+            }
+            if (__syncthreads_or(!ok)) return;
+        }
+        ++k;
+    }
+    for (int uu = tid; uu < B * nq; uu += nthr) {
+        const int lr = uu / nq + 1, q = uu - (lr - 1) * nq;
+        store_quad(u + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q, ld4(T + lr * sp + 4 + 4 * q),
+                   min(4, nx - 4 * q));
+    }
+    if (b == 0 && tid == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = k;
+        d->res0 = res0;
+        d->res_last = res_last;
+        d->rmax_last = rmax_last;
+        d->n_checks = n_checks;
+        d->cur = p.cur;
+        d->task_sweeps = 0;
+        d->barriers = ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
+        __threadfence();
+        d->run_id = p.run_id;
+    }
+}
+
 // Per-launch red-black: one half-sweep (colour = pass_k) or, with
 // pass_check, the residual pass.
 template <bool POISSON>
@@ -1325,9 +1464,12 @@ cudaError_t prepare_kernels() {
         return cudaSuccess;
     };
     size_t local_max = (size_t)optin;
-    for (int poisson = 0; poisson < 2; ++poisson) {
-        const void *fn = poisson ? (const void *)k_persistent_local<true>
-                                 : (const void *)k_persistent_local<false>;
+    for (int which = 0; which < 4; ++which) {
+        const bool poisson = which & 1;
+        const void *fn = (which & 2) ? (poisson ? (const void *)k_persistent_local_rb<true>
+                                                : (const void *)k_persistent_local_rb<false>)
+                                     : (poisson ? (const void *)k_persistent_local<true>
+                                                : (const void *)k_persistent_local<false>);
         int lim = 0;
         if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
@@ -1417,6 +1559,16 @@ cudaError_t launch_persistent_rb(bool poisson, int grid, const SweepParams &p, c
     return cudaLaunchCooperativeKernel(poisson ? (const void *)k_persistent_rb<true>
                                                : (const void *)k_persistent_rb<false>,
                                        dim3(grid), dim3(kDirectThreads), args, 0, s);
+}
+
+cudaError_t launch_persistent_local_rb(bool poisson, int grid, const SweepParams &p,
+                                       cudaStream_t s) {
+    SweepParams arg = p;
+    void *args[] = {&arg};
+    return cudaLaunchCooperativeKernel(poisson ? (const void *)k_persistent_local_rb<true>
+                                               : (const void *)k_persistent_local_rb<false>,
+                                       dim3(grid), dim3(kDirectThreads), args,
+                                       local_smem_bytes(p.nx, p.local_rows, poisson), s);
 }
 
 cudaError_t launch_once_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s) {

@@ -606,15 +606,33 @@ def run_rb(pk, u0, f, n, tol=0.0, ce=0, path="persistent", **opts):
 
 
 @pytest.mark.parametrize("nx,ny", SIZES, ids=["%dx%d" % s for s in SIZES])
-@pytest.mark.parametrize("path", ["persistent", "launch"])
+@pytest.mark.parametrize("path", ["persistent-direct", "persistent-local", "launch"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_redblack_bit_exact(pk, nx, ny, path, poisson):
     u0 = inputs.random_field(nx, ny, seed=700 + nx + ny)
     f = inputs.uniform_pm1(800 + nx, nx * ny).reshape(ny, nx) if poisson else None
     want, oinfo = oracle.rb_run(u0, f=f, n=7, tol=1e-30, check_every=3)
-    got, info = run_rb(pk, u0, f, 7, 1e-30, 3, path=path)
+    variant = 3 if path == "persistent-local" else 1
+    got, info = run_rb(pk, u0, f, 7, 1e-30, 3, path=path.split("-")[0], variant=variant)
+    assert info["variant"] == (3 if path == "persistent-local" else 1)
     assert_same_bits(got, want)
     check_info(info, oinfo)
+
+
+RB_LOCAL_CASES = [(1030, 9, 0), (63, 65, 0), (512, 512, 0), (100, 100, 7), (300, 301, 0),
+                  (64, 64, 0), (257, 50, 3), (5, 1000, 0)]
+
+
+@pytest.mark.parametrize("nx,ny,grid", RB_LOCAL_CASES, ids=["%dx%d-g%d" % c for c in RB_LOCAL_CASES])
+def test_redblack_local_grids(pk, nx, ny, grid):
+    u0 = inputs.random_field(nx, ny, seed=900 + nx + ny)
+    f = inputs.uniform_pm1(901 + nx, nx * ny).reshape(ny, nx)
+    for n, tol, ce in ((23, 0.0, 0), (17, 1e-30, 5)):
+        want, oinfo = oracle.rb_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_rb(pk, u0, f, n, tol, ce, variant=3, grid_override=grid)
+        assert info["variant"] == 3
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
 
 
 def test_redblack_worked_4x4_and_mixed_methods(pk):
