@@ -309,13 +309,19 @@ def latency_extras(pk):
     ctx = pk.pk_create(256, 256, w["u0"], None)
     try:
         mb = pk.pk_bench_tasks(ctx, 0, tasks, 10100)[100:] / 1e3
+        nop = pk.pk_bench_tasks(ctx, 0, [pk.make_task(pk.PK_TASK_NOP)], 2100)[100:] / 1e3
         pk.pk_shutdown(ctx)
         ln = pk.pk_bench_tasks(ctx, 1, tasks, 10100)[100:] / 1e3
+        lnop = pk.pk_bench_tasks(ctx, 1, [pk.make_task(pk.PK_TASK_NOP)], 2100)[100:] / 1e3
         out["task_queue_10000"] = {
             "mailbox_round_trip_us": {"p50": float(np.percentile(mb, 50)),
                                       "p99": float(np.percentile(mb, 99))},
             "launch_sync_round_trip_us": {"p50": float(np.percentile(ln, 50)),
                                           "p99": float(np.percentile(ln, 99))},
+            "nop_mailbox_round_trip_us": {"p50": float(np.percentile(nop, 50)),
+                                          "p99": float(np.percentile(nop, 99))},
+            "nop_launch_sync_round_trip_us": {"p50": float(np.percentile(lnop, 50)),
+                                              "p99": float(np.percentile(lnop, 99))},
             "task_grid": pk.pk_get_plan(ctx)["task_grid"],
         }
     finally:

@@ -403,7 +403,7 @@ int common_setup(pk_ctx *ctx) {
     PK_TRY(ctx, cudaHostAlloc(&ctx->h_res, sizeof(ResidualOut), cudaHostAllocDefault));
     PK_TRY(ctx, cudaHostAlloc(&ctx->h_bar, sizeof(BarrierState), cudaHostAllocDefault));
     // Mailbox in mapped pinned host memory ("Device Communication").
-    ctx->mbox_bytes = sizeof(Mailbox) + sizeof(TaskSlot) * (size_t)(ctx->opt.mailbox_depth - 1);
+    ctx->mbox_bytes = sizeof(Mailbox) + sizeof(MboxSlot) * (size_t)(ctx->opt.mailbox_depth - 1);
     PK_TRY(ctx, cudaHostAlloc(&ctx->mbox, ctx->mbox_bytes, cudaHostAllocMapped));
     std::memset(ctx->mbox, 0, ctx->mbox_bytes);
     PK_TRY(ctx, cudaHostGetDevicePointer((void **)&ctx->mbox_dev, ctx->mbox, 0));
@@ -1044,16 +1044,27 @@ int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out) {
     if (ctx->next_seq - 1 - done >= (unsigned long long)ctx->opt.mailbox_depth)
         return fail(ctx, PK_EBUSY, "pk_submit_task: mailbox ring full");
     const unsigned long long seq = ctx->next_seq++;
-    TaskSlot *slot = &ctx->mbox->slots[seq % (unsigned long long)ctx->opt.mailbox_depth];
-    slot->kind = task->kind;
-    slot->n_sweeps = task->n_sweeps;
-    slot->a = task->a;
-    slot->reserved = 0;
-    slot->x = (unsigned long long)(uintptr_t)task->x;
-    slot->y = (unsigned long long)(uintptr_t)task->y;
-    slot->len = task->len;
-    slot->pad = 0;
-    // Release: the descriptor is visible before the sequence number.
+    MboxSlot *slot = &ctx->mbox->slots[seq % (unsigned long long)ctx->opt.mailbox_depth];
+    const unsigned long long x = (unsigned long long)(uintptr_t)task->x;
+    const unsigned long long y = (unsigned long long)(uintptr_t)task->y;
+    const unsigned long long len = task->kind == PK_TASK_AXPY ? (unsigned long long)task->len : 0ull;
+    unsigned a_bits;
+    std::memcpy(&a_bits, &task->a, sizeof(a_bits));
+    const unsigned data[8] = {
+        (unsigned)(task->kind & 0xff) | (unsigned)((len >> 32) << 8),
+        (unsigned)(task->kind == PK_TASK_JACOBI ? task->n_sweeps : 0),
+        a_bits,
+        (unsigned)x, (unsigned)(x >> 32),
+        (unsigned)y, (unsigned)(y >> 32),
+        (unsigned)len,
+    };
+    // Release fence: writes this thread made before posting (task buffers)
+    // are ordered before any word of the slot.  Each word is tagged, so the
+    // words themselves need no order among one another.
+    __atomic_thread_fence(__ATOMIC_RELEASE);
+    for (int k = 0; k < 8; ++k)
+        __atomic_store_n(&slot->w[k], mbox_word(seq, data[k]), __ATOMIC_RELAXED);
+    // The sequence word is informational for the device (it polls the tags).
     __atomic_store_n(&ctx->mbox->seq.v, seq, __ATOMIC_RELEASE);
     if (seq_out) *seq_out = seq;
     return PK_OK;

@@ -84,12 +84,28 @@ struct alignas(64) TaskSlot {
     long long pad;
 };
 
+// One posted task in the host ring.  Every 8-byte word carries the low 32
+// bits of the task's sequence number in its high half and 32 bits of the
+// descriptor in its low half, so the device learns that a slot is complete
+// from the words themselves: one poll over the interconnect reads readiness
+// and payload together, with no separate flag to acquire first.
+//   w[0] kind (bits 0-7) | len >> 32 (bits 8-16)   w[1] n_sweeps
+//   w[2] a (float bits)   w[3], w[4] x lo, hi       w[5], w[6] y lo, hi
+//   w[7] len lo
+struct alignas(64) MboxSlot {
+    unsigned long long w[8];
+};
+
+__host__ __device__ inline unsigned long long mbox_word(unsigned long long seq, unsigned data) {
+    return ((unsigned long long)(unsigned)seq << 32) | (unsigned long long)data;
+}
+
 struct Mailbox {
     MboxWord seq;       // host: last posted sequence number (release store)
     MboxWord done_seq;  // device: last completed sequence number (system-scope release)
     MboxWord status;    // device: final status of the task kernel
     MboxWord reserved;
-    TaskSlot slots[1];  // mailbox_depth entries
+    MboxSlot slots[1];  // mailbox_depth entries
 };
 
 constexpr int kTaskExitIdle = 100;   // internal kind: idle timeout, exit
@@ -118,11 +134,12 @@ struct StreamConfig {
     int qpt;
     int stages;
     int depth;
+    int min_ctas;  // CTAs per SM the register budget is sized for
 };
 constexpr int kNumStreamConfigs = 10;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
-    {1, 8, 1}, {1, 16, 1}, {2, 8, 1}, {4, 4, 1}, {4, 8, 1}, {2, 16, 1},
-    {1, 8, 2}, {2, 8, 2}, {2, 4, 2}, {4, 4, 2}};
+    {1, 8, 1, 1}, {1, 16, 1, 1}, {2, 8, 1, 1}, {4, 4, 1, 1}, {4, 8, 1, 1}, {2, 16, 1, 1},
+    {1, 8, 2, 2}, {2, 8, 2, 1}, {2, 4, 2, 1}, {4, 4, 2, 1}};
 
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kConsumers; }
 inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }

@@ -88,11 +88,12 @@ __device__ __forceinline__ void pass_direct_any(const SweepParams &p, const floa
 // QPT float4 groups per thread, so each input row is read from HBM once and
 // from shared memory once.  Edge neighbours come from warp shuffles, and at
 // warp edges from the staged halo.
-template <int QPT, int STAGES, int DEPTH, bool POISSON>
+template <int QPT, int STAGES, int DEPTH, int MINB, bool POISSON>
 struct SCfg {
     static constexpr int kQPT = QPT;
     static constexpr int kStages = STAGES;
     static constexpr int kDepth = DEPTH;
+    static constexpr int kMinBlocks = MINB;
     static constexpr int TW = 4 * QPT * kConsumers;
     static constexpr int SLOTU = TW + 8;
     static constexpr int SLOT = SLOTU + (POISSON ? TW + 8 : 0);
@@ -557,7 +558,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParam
 }
 
 template <class C, bool POISSON>
-__global__ void __launch_bounds__(kStreamThreads) k_persistent_stream(SweepParams p) {
+__global__ void __launch_bounds__(kStreamThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     StreamState st = stream_setup<C>(smem);
     persistent_loop<C::kDepth>(p, [&](const float *src, float *dst, bool check, bool store,
@@ -782,7 +783,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_once_direct(SweepParams p) {
 }
 
 template <class C, bool POISSON>
-__global__ void __launch_bounds__(kStreamThreads) k_once_stream(SweepParams p) {
+__global__ void __launch_bounds__(kStreamThreads, C::kMinBlocks) k_once_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     StreamState st = stream_setup<C>(smem);
     double s2 = 0.0;
@@ -1107,8 +1108,9 @@ __global__ void __launch_bounds__(kDirectThreads) k_axpy(float a, const float *x
 //     release atomic and spins (acquire) on tb->generation;
 //   * CTA 0's thread 0 waits (acquire) for gridDim.x - 1 arrivals, resets
 //     the count, publishes the finished task's sequence number to the host
-//     (__threadfence_system + st.release.sys: never before the work is
-//     done), polls the mailbox (relaxed loads, then one acquire), copies the
+//     (st.release.sys, cumulative over the arrivals it acquired: never
+//     before the work is done), polls the next tagged mailbox slot until
+//     all its words carry the task's tag (then one acquire fence), copies the
 //     descriptor to device memory and releases the next generation.
 // All spins are bounded (idle limit for the host poll, barrier limit for the
 // rest) and end on the abort flag.
@@ -1135,7 +1137,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                 if (!first) {
                     const uint64_t t0 = globaltimer_ns();
                     unsigned spins = 0;
-                    while (ld_acquire_gpu(&tb->count.v) != G - 1u) {
+                    while (ld_relaxed_gpu(&tb->count.v) != G - 1u) {
                         if ((++spins & 255u) == 0u) {
                             if (aborted(tb) || aborted(p.bar)) {
                                 kind_override = kTaskExitIdle;
@@ -1148,17 +1150,33 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                             }
                         }
                     }
+                    fence_acq_rel_gpu();  // acquire every CTA's release arrival
                     if (kind_override < 0) {
                         st_relaxed_gpu(&tb->count.v, 0u);
-                        __threadfence_system();
+                        // The system-scope release publishes, cumulatively, the
+                        // task's writes that this thread has acquired.
                         st_release_sys_u64(&tp.mbox->done_seq.v, last);
                     }
                 }
+                unsigned long long w[8];
                 if (kind_override < 0) {
+                    // Poll the whole tagged slot: the four 16-byte loads go
+                    // out together, and the slot is complete once every word
+                    // carries this task's tag.
+                    const unsigned long long *hw =
+                        tp.mbox->slots[(last + 1ull) % (unsigned)tp.depth].w;
+                    const unsigned tag = (unsigned)(last + 1ull);
                     const uint64_t t0 = globaltimer_ns();
                     unsigned spins = 0;
                     for (;;) {
-                        if (ld_relaxed_sys_u64(&tp.mbox->seq.v) > last) break;
+                        ld_relaxed_sys_v2_u64(hw + 0, w[0], w[1]);
+                        ld_relaxed_sys_v2_u64(hw + 2, w[2], w[3]);
+                        ld_relaxed_sys_v2_u64(hw + 4, w[4], w[5]);
+                        ld_relaxed_sys_v2_u64(hw + 6, w[6], w[7]);
+                        bool ready = true;
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) ready &= (unsigned)(w[k] >> 32) == tag;
+                        if (ready) break;
                         if ((++spins & 63u) == 0u &&
                             globaltimer_ns() - t0 > tp.idle_timeout_ns) {
                             record_error(tb, kETimedOut, kSiteMailboxIdle);
@@ -1166,18 +1184,20 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                             break;
                         }
                     }
+                    // Acquire: the host's writes before it posted the slot.
+                    if (kind_override < 0) fence_acq_rel_sys();
                 }
                 TaskSlot d;
                 if (kind_override < 0) {
-                    (void)ld_acquire_sys_u64(&tp.mbox->seq.v);
-                    const volatile TaskSlot *hs = &tp.mbox->slots[(last + 1ull) % (unsigned)tp.depth];
-                    d.kind = hs->kind;
-                    d.n_sweeps = hs->n_sweeps;
-                    d.a = hs->a;
+                    const unsigned w0 = (unsigned)w[0];
+                    d.kind = (int)(w0 & 0xffu);
+                    d.n_sweeps = (int)(unsigned)w[1];
+                    d.a = __uint_as_float((unsigned)w[2]);
                     d.reserved = 0;
-                    d.x = hs->x;
-                    d.y = hs->y;
-                    d.len = hs->len;
+                    d.x = (unsigned long long)(unsigned)w[3] | ((unsigned long long)(unsigned)w[4] << 32);
+                    d.y = (unsigned long long)(unsigned)w[5] | ((unsigned long long)(unsigned)w[6] << 32);
+                    d.len = (long long)((unsigned long long)(unsigned)w[7] |
+                                        ((unsigned long long)(w0 >> 8) << 32));
                     d.pad = 0;
                 } else {
                     d.kind = kind_override;
@@ -1197,7 +1217,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                 const uint64_t limit = tp.idle_timeout_ns + p.timeout_ns;
                 unsigned spins = 0;
                 bool ok = true;
-                while (ld_acquire_gpu(&tb->generation.v) == gen) {
+                while (ld_relaxed_gpu(&tb->generation.v) == gen) {
                     if ((++spins & 255u) == 0u) {
                         if (aborted(tb) || aborted(p.bar)) {
                             ok = false;
@@ -1210,6 +1230,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                         }
                     }
                 }
+                fence_acq_rel_gpu();  // acquire CTA 0's release of the descriptor
                 if (ok) {
                     const volatile TaskSlot *ds = tp.dev_desc;
                     s_task.kind = ds->kind;
@@ -1412,7 +1433,7 @@ __global__ void __launch_bounds__(256) k_stress_tma(BarrierCtl ctl, int rounds, 
 // Launch wrappers.
 template <int CFG, bool POISSON>
 using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, kStreamConfigs[CFG].depth,
-                   POISSON>;
+                   kStreamConfigs[CFG].min_ctas, POISSON>;
 
 template <int CFG, bool POISSON>
 const void *persistent_stream_fn() {
