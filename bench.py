@@ -10,9 +10,12 @@ CUDA events recorded on the launching stream around each kernel (libpk
 records them; pk_run_info.device_us); ``e2e`` is the same metric through the
 public C ABI with host buffers (pinned H2D copy of the field, the sweeps, a
 D2H copy of the result) on the host clock.  ``roofline`` reports the
-dominant kernel's algorithmic HBM bytes (8 B per cell-update: read the
-previous iterate once, write the new one once) per launch over its event
-time, against the measured copy bandwidth.  ``cpu_baseline`` times the CPU
+dominant kernel's algorithmic HBM bytes per launch over its event time,
+against the measured copy bandwidth.  Each pass over the field reads the
+current iterate once and writes the next one once (8 B per cell, 12 with a
+Poisson source); a pass of a two-sweep shape (temporal blocking) advances
+two sweeps for those 8 B, so the sweeps' compulsory traffic is 4 B per
+cell-update there.  ``cpu_baseline`` times the CPU
 oracle on a bounded sample of the same workload, single-threaded.
 
 ``--impl reference`` runs the CPU oracle arm instead (the only reference for
@@ -52,11 +55,47 @@ WORKLOADS = {
 DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 
 # DRAM traffic of one launch of the dominant kernel, from the ncu capture
-# summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum,
-# scaled to this workload's launch); valid only while the kernel source
-# hash matches.
-TRAFFIC = {"kernel_sha": "cdeccbb51eee4d4c",
-           "bytes_per_launch": 103.94e9 + 107.38e9}  # 16384^2 x 100 sweeps, one launch
+# summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
+# one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
+# source hash and the STREAM shape match.
+TRAFFIC = {"kernel_sha": "f97f488cbc722609", "stream_config": 6,
+           "bytes_per_launch": 54.00e9 + 53.69e9}
+
+
+# pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
+SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1), 5: (2, 16, 1),
+          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2)}
+
+
+def shape_label(info, poisson):
+    if info["variant"] != 2:
+        return {1: "k_persistent_direct", 3: "k_persistent_local"}[info["variant"]]
+    q, ring, depth = SHAPES[info["stream_config"]]
+    return "k_persistent_stream<{%d float4/thread, %d-deep ring, %d sweep%s/pass}, %s>" % (
+        q, ring, depth, "s" if depth > 1 else "", "poisson" if poisson else "laplace")
+
+
+def passes_of(info, sweeps, tol, check_every):
+    """Passes a persistent run over `sweeps` sweeps took (no early exit):
+    (passes that store, check-only passes).  A two-sweep shape takes two
+    sweeps per pass whenever no check can fall between them."""
+    checks = tol > 0 and check_every > 0
+    two = (info["variant"] == 2 and SHAPES[info["stream_config"]][2] == 2
+           and (not checks or check_every % 2 == 0))
+    k, store_passes = 0, 0
+    while k < sweeps:
+        k += 2 if two and k + 2 <= sweeps else 1
+        store_passes += 1
+    check_only = 1 if checks and sweeps % check_every == 0 else 0
+    return store_passes, check_only
+
+
+def algorithmic_bytes(info, cells, sweeps, poisson, tol, check_every):
+    """Compulsory HBM bytes of one persistent run: every pass reads U (and g)
+    once and, unless it only checks, writes U once."""
+    store_passes, check_only = passes_of(info, sweeps, tol, check_every)
+    src = 4.0 if poisson else 0.0
+    return cells * (store_passes * (8.0 + src) + check_only * (4.0 + src))
 
 
 def kernel_source_sha():
@@ -357,15 +396,18 @@ def latency_extras(pk):
     # Temporal blocking: two sweeps per HBM pass, same bits (16384^2, 100 sweeps)
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
-    for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 6)):
+    for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 6),
+                      ("two_sweeps_per_pass_16_deep_ring", 8)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):
                 pk.pk_run_sweeps(ctx, 100)
-            us = statistics.median(pk.pk_run_sweeps(ctx, 100)["device_us"] / 100 for _ in range(5))
+            runs = [pk.pk_run_sweeps(ctx, 100) for _ in range(5)]
+            us = statistics.median(r["device_us"] / 100 for r in runs)
             tb[name] = {"stream_config": cfg, "us_per_sweep": us,
                         "cell_updates_per_s": 16384 * 16384 / (us * 1e-6),
-                        "dram_bytes_per_sweep_algorithmic": 8.0 * 16384 * 16384 / (1 if cfg == 3 else 2)}
+                        "dram_bytes_per_sweep_algorithmic":
+                            algorithmic_bytes(runs[0], 16384 * 16384, 100, False, 0, 0) / 100}
         finally:
             pk.pk_destroy(ctx)
     tb["speedup"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
@@ -377,10 +419,13 @@ def latency_extras(pk):
     try:
         info = pk.pk_run_sweeps(ctx, 2000, 1e-4, 10)
         us = info["device_us"] / max(1, info["sweeps_done"])
+        done = info["sweeps_done"]
         out["poisson_4096_res10"] = {
-            "us_per_sweep": us, "sweeps_done": info["sweeps_done"],
+            "us_per_sweep": us, "sweeps_done": done,
             "res_ratio": info["res_last"] / info["res0"] if info["res0"] else None,
-            "hbm_gbs_algorithmic": 12.0 * 4096 * 4096 / (us * 1e-6) / 1e9,
+            "kernel": shape_label(info, True),
+            "hbm_gbs_algorithmic": algorithmic_bytes(info, 4096 * 4096, done, True, 1e-4, 10)
+                                   / (info["device_us"] * 1e-6) / 1e9,
             "n_checks": info["n_checks"],
         }
     finally:
@@ -435,6 +480,7 @@ def main():
         t0 = time.perf_counter()
         for _ in range(args.steps):
             info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+            run_info = info
             dev_us.append(info["device_us"])
             updates += cells * info["sweeps_done"]
         torch.cuda.synchronize()
@@ -470,19 +516,23 @@ def main():
     if rank != 0:
         return
     peak, peak_kind = measured_peaks()
-    bytes_per_update = 12.0 if w["f"] is not None else 8.0
     launch_us = statistics.median(dev_us)
-    alg_bytes = bytes_per_update * cells * sweeps
+    alg_bytes = algorithmic_bytes(run_info, cells, run_info["sweeps_done"], w["f"] is not None,
+                                  w["tol"], w["check_every"])
     achieved = alg_bytes / (launch_us * 1e-6) / 1e9
-    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["kernel_sha"] == kernel_source_sha() else None
+    traffic = (TRAFFIC["bytes_per_launch"]
+               if TRAFFIC["kernel_sha"] == kernel_source_sha()
+               and run_info["stream_config"] == TRAFFIC["stream_config"]
+               and args.workload == DEFAULT_WORKLOAD else None)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": args.workload, "nx": nx, "ny": ny, "sweeps_per_step": sweeps,
-                   "variant": {1: "direct", 2: "stream", 3: "local"}[plan["variant"]],
-                   "grid": plan["grid"], "l2": "inputs larger than L2 (2 x field > 129 MB)"
+                   "variant": {1: "direct", 2: "stream", 3: "local"}[run_info["variant"]],
+                   "stream_config": run_info["stream_config"],
+                   "grid": run_info["grid"], "l2": "inputs larger than L2 (2 x field > 129 MB)"
                    if 2 * 4 * cells > 129e6 else "L2-resident",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},
         "us_per_sweep": us_per_sweep,
@@ -492,8 +542,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": peak_kind,
-                     "kernel": "k_persistent_stream<{4 float4/thread, 4-deep ring}, laplace>"
-                     if plan["variant"] == 2 else "k_persistent_direct",
+                     "kernel": shape_label(run_info, w["f"] is not None),
                      "algorithmic_bytes_per_launch": alg_bytes},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(w["u0"].nbytes),

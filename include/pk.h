@@ -94,6 +94,9 @@ typedef struct {
     int32_t current;      /* buffer holding the current iterate: 0 = A, 1 = B */
     int32_t grid;         /* CTAs the sweeps ran with */
     int32_t variant;      /* PK_VARIANT_DIRECT, _STREAM or _LOCAL: the kernels that ran */
+    int32_t stream_config; /* STREAM shape the sweeps ran with (pk_options.stream_config
+                              index); -1 for the other variants */
+    int32_t reserved;
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
 } pk_run_info;
@@ -125,11 +128,15 @@ typedef struct {
     uint32_t flags;                   /* PK_FLAG_* (default PK_FLAG_ALTERNATE_DIRECTION) */
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
-    int32_t stream_config;            /* STREAM shape, -1 = default (3).  Index into
+    int32_t stream_config;            /* STREAM shape.  -1 = default: shape 6 for persistent
+                                         runs that can take two sweeps per pass (n >= 2 and
+                                         checks off or check_every even), shape 3 for the
+                                         rest and for the per-launch and graph paths
+                                         (pk_run_info.stream_config says which ran).  Index into
                                          {float4 groups per thread, TMA ring depth, sweeps
                                          per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}
-                                         4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {2,4,2}
-                                         9 {4,4,2}; a strip is 1024 x groups columns wide.
+                                         4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {1,16,2}
+                                         9 {2,16,2}; a strip is 1024 x groups columns wide.
                                          Two sweeps per pass keep U_{k+1} on chip (temporal
                                          blocking) whenever two sweeps are due and checks
                                          are off or check_every is even; results are the

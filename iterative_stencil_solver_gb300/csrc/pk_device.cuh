@@ -354,6 +354,36 @@ __device__ __forceinline__ float4 quad_update(const Quad &q) {
                        __fmul_rn(0.25f, q.t3));
 }
 
+// The same arithmetic with packed f32x2 operations: the S+N sums, the final
+// sums, the source and the quarter go two cells per instruction.  Each lane
+// of a packed operation rounds like its scalar form, and t - g is t + (-g)
+// under IEEE rules, so the results are bit for bit those of quad_t and
+// quad_update.
+template <bool POISSON>
+__device__ __forceinline__ Quad quad_t2(float w, float4 c, float e, float4 s, float4 n, float4 g) {
+    const float2 b01 = __fadd2_rn(make_float2(s.x, s.y), make_float2(n.x, n.y));
+    const float2 b23 = __fadd2_rn(make_float2(s.z, s.w), make_float2(n.z, n.w));
+    float2 t01 = __fadd2_rn(make_float2(__fadd_rn(w, c.y), __fadd_rn(c.x, c.z)), b01);
+    float2 t23 = __fadd2_rn(make_float2(__fadd_rn(c.y, c.w), __fadd_rn(c.z, e)), b23);
+    if (POISSON) {
+        t01 = __fadd2_rn(t01, make_float2(-g.x, -g.y));
+        t23 = __fadd2_rn(t23, make_float2(-g.z, -g.w));
+    }
+    Quad q;
+    q.t0 = t01.x;
+    q.t1 = t01.y;
+    q.t2 = t23.x;
+    q.t3 = t23.y;
+    return q;
+}
+
+__device__ __forceinline__ float4 quad_update2(const Quad &q) {
+    const float2 quarter = make_float2(0.25f, 0.25f);
+    const float2 u01 = __fmul2_rn(quarter, make_float2(q.t0, q.t1));
+    const float2 u23 = __fmul2_rn(quarter, make_float2(q.t2, q.t3));
+    return make_float4(u01.x, u01.y, u23.x, u23.y);
+}
+
 // Residual accumulation over the first `valid` cells of the quad.
 __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, double &s2,
                                               float &rmax) {

@@ -77,6 +77,8 @@ struct pk_ctx {
     int variant = kVariantDirect;
     int stream_cfg = 0;  // STREAM configuration index
     int grid = 1;        // persistent sweep grid
+    int stream_cfg2 = -1;  // two-sweep STREAM shape for persistent runs (-1 = none)
+    int grid2 = 0;         // its grid
     int coop_max = 1;    // occupancy x SMs for the sweep kernel
     int part_cap = 0;    // partial slots per parity
     Scratch *scratch = nullptr;
@@ -210,12 +212,14 @@ int coop_capacity(pk_ctx *ctx, const void *fn, int threads, size_t smem, int *pe
 
 long long direct_units(const pk_ctx *ctx) { return (long long)ctx->ny * ((ctx->nx + 3) / 4); }
 
-long long stream_rows(const pk_ctx *ctx) {
-    const int tw = stream_tw(ctx->stream_cfg);
+long long stream_rows(const pk_ctx *ctx, int cfg) {
+    const int tw = stream_tw(cfg);
     return (long long)((ctx->nx + tw - 1) / tw) * ctx->ny;
 }
+long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_cfg); }
 
-constexpr int kDefaultStreamConfig = 3;  // 4096-column strips, 4-deep ring, 1 CTA/SM
+constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
+constexpr int kDefaultStreamConfig2 = 6;  // two sweeps per pass, 1024-column strips, 2 CTAs/SM
 
 int ensure_partials(pk_ctx *ctx, int grid) {
     if (grid <= ctx->part_cap) return PK_OK;
@@ -285,6 +289,25 @@ int plan(pk_ctx *ctx) {
     ctx->stream_cfg = ctx->opt.stream_config >= 0 ? ctx->opt.stream_config : kDefaultStreamConfig;
     if (v == kVariantStream && !stream_config_ok(ctx->stream_cfg, ctx->poisson))
         return fail(ctx, PK_EINVAL, "stream_config %d does not fit in shared memory", ctx->stream_cfg);
+    // Default shape: persistent runs that can take two sweeps per pass use
+    // the two-sweep shape (same bits, half the HBM traffic per sweep).
+    ctx->stream_cfg2 = -1;
+    ctx->grid2 = 0;
+    if (v == kVariantStream && ctx->opt.stream_config < 0 &&
+        stream_config_ok(kDefaultStreamConfig2, ctx->poisson)) {
+        int per_sm2 = 0;
+        const int cap2 = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, kDefaultStreamConfig2),
+                                       block_threads(v),
+                                       dyn_smem(v, ctx->poisson, kDefaultStreamConfig2), &per_sm2);
+        if (cap2 < 0) return PK_ECUDA;
+        if (cap2 > 0) {
+            long long need2 = stream_rows(ctx, kDefaultStreamConfig2);
+            if (need2 < 1) need2 = 1;
+            ctx->stream_cfg2 = kDefaultStreamConfig2;
+            ctx->grid2 = (int)(need2 < cap2 ? need2 : cap2);
+            if (ctx->opt.grid_override > 0) ctx->grid2 = ctx->opt.grid_override;
+        }
+    }
     int cap;
     if (v == kVariantLocal) {
         cap = lcap;
@@ -314,6 +337,7 @@ int plan(pk_ctx *ctx) {
     ctx->task_grid = (int)(tneed < tcap ? tneed : tcap);
     if (ctx->opt.task_grid > 0) ctx->task_grid = ctx->opt.task_grid;
     int want = ctx->grid > cap ? ctx->grid : cap;
+    if (ctx->grid2 > want) want = ctx->grid2;
     return ensure_partials(ctx, want);
 }
 
@@ -447,7 +471,7 @@ double elapsed_us(pk_ctx *ctx) {
 }
 
 void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
-               float rmax, int n_checks, int status, int grid, int variant = 0) {
+               float rmax, int n_checks, int status, int grid, int variant = 0, int shape = -2) {
     if (!info) return;
     info->sweeps_done = sweeps;
     info->res0 = res0;
@@ -458,6 +482,9 @@ void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, do
     info->current = ctx->cur;
     info->grid = grid;
     info->variant = variant ? variant : ctx->variant;
+    if (shape == -2) shape = info->variant == kVariantStream ? ctx->stream_cfg : -1;
+    info->stream_config = info->variant == kVariantStream ? shape : -1;
+    info->reserved = 0;
     info->device_us = elapsed_us(ctx);
 }
 
@@ -624,9 +651,16 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
         PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0,
                                     (size_t)ctx->grid * local_halo_words(ctx->nx) * sizeof(unsigned long long),
                                     ctx->stream));
+    // The two-sweep shape pays off when its passes can advance two sweeps:
+    // at least two sweeps, and no check falling between the two.
+    const bool checks = tol > 0.f && check_every > 0;
+    int shape = ctx->stream_cfg, grid = ctx->grid;
+    if (ctx->stream_cfg2 >= 0 && n >= 2 && (!checks || check_every % 2 == 0)) {
+        shape = ctx->stream_cfg2;
+        grid = ctx->grid2;
+    }
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, ctx->stream_cfg, ctx->grid, p,
-                                      ctx->stream);
+    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, shape, grid, p, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
@@ -635,16 +669,16 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     int rc = bar_status(ctx, p.bar, "pk_run_sweeps");
     if (rc != PK_OK) {
         ctx->sweep_bar_base = 0;  // bar_status zeroed the barrier words
-        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, ctx->grid);
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, 0, shape);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
         return fail(ctx, PK_EDEVICE, "pk_run_sweeps: kernel did not report its result");
     ctx->sweep_bar_base = ctx->h_info->bar_count_end;
-    if (p.profile) ctx->spin_valid = ctx->grid;
+    if (p.profile) ctx->spin_valid = grid;
     ctx->cur = ctx->h_info->cur;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
-              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, ctx->grid);
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid, 0, shape);
     return PK_OK;
 }
 

@@ -139,17 +139,19 @@ struct StreamConfig {
 constexpr int kNumStreamConfigs = 10;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
     {1, 8, 1, 1}, {1, 16, 1, 1}, {2, 8, 1, 1}, {4, 4, 1, 1}, {4, 8, 1, 1}, {2, 16, 1, 1},
-    {1, 8, 2, 2}, {2, 8, 2, 1}, {2, 4, 2, 1}, {4, 4, 2, 1}};
+    {1, 8, 2, 2}, {2, 8, 2, 1}, {1, 16, 2, 2}, {2, 16, 2, 1}};
 
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kConsumers; }
 inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 
 // A ring slot: the U row segment (4 halo floats each side) and, for
-// Poisson, the g row segment with a 4-float margin each side.
+// Poisson, the g row segment with a 4-float margin each side.  Two-sweep
+// shapes add two shared U_{k+1} rows laid out like the U part of a slot.
 inline size_t stream_smem_bytes(int cfg, bool poisson) {
     const int tw = stream_tw(cfg);
     const size_t slot = (size_t)(tw + 8 + (poisson ? tw + 8 : 0)) * sizeof(float);
-    return 256 + (size_t)kStreamConfigs[cfg].stages * slot;
+    const size_t qrows = stream_depth(cfg) == 2 ? 2 * (size_t)(tw + 8) * sizeof(float) : 0;
+    return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 
 // Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).

@@ -252,146 +252,197 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
 // Two sweeps per pass (temporal blocking; "Persistent Kernels...",
 // "Reflections": a wider halo lets a block run several steps per
 // synchronisation, trading a little redundant compute at the tile edges).
-// Input rows ja-2dir .. jb+2dir of U_k; stage 1 recomputes U_{k+1} on rows
-// ja-dir .. jb+dir and, at every warp edge, one column beyond it (lane 0 to
-// the left, lane 31 to the right); stage 2 writes U_{k+2} on rows ja .. jb.
-// U_{k+1} never leaves registers.  Ring cells of U_{k+1} keep their U_k
-// value; every other cell uses the single-sweep arithmetic, so the result
-// is bit for bit two single sweeps.  CHECK reduces the residual of U_k (the
-// loop only checks at the start of a pass).
+// Input rows ja-2dir .. jb+2dir of U_k; stage 1 computes U_{k+1} on rows
+// ja-dir .. jb+dir, stage 2 writes U_{k+2} on rows ja .. jb.  U_{k+1} stays
+// on chip: each thread keeps its own quads of the last three U_{k+1} rows in
+// registers, and the CTA shares each new U_{k+1} row through a pair of
+// shared-memory rows (same indexing as a ring slot, plus one recomputed
+// cell beyond each strip edge), from which stage 2 takes its west and east
+// neighbours.  One named barrier among the consumer threads per input row
+// orders the writes of a shared row before its reads and before its reuse.
+// A ring slot is held for three input rows (S, centre and N of stage 1), so
+// both stages read their west/east U_k neighbours and the source straight
+// from the staged rows.  Ring cells of U_{k+1} keep their U_k value; every
+// other cell uses the single-sweep arithmetic, so the result is bit for bit
+// two single sweeps.  CHECK reduces the residual of U_k (the loop only
+// checks at the start of a pass).
+__device__ __forceinline__ void consumers_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");
+}
+
+template <int Q>
+struct Seg2 {
+    float *qbuf;       // two shared U_{k+1} rows
+    float *drow;       // stage-2 output row for the next step (+ quad offset)
+    long long dstep;   // dir * pitch
+    long long col0;
+    int dir, cols, nin, nx, ny;
+    int o[Q];          // float offset of quad k in the strip
+    int valid[Q];      // cells of quad k inside the strip (0..4)
+    int icol[Q];       // interior column of quad k's first cell
+};
+
+// One input row: idx is its position in the segment, r its row.  The three
+// U_k rows (KA = S, KB = centre, KX = N, the new row) and the three U_{k+1}
+// rows (QA, QB, QY = the new one) are passed in their current roles, so an
+// unrolled caller can rotate roles by renaming instead of moving registers.
+// STEADY: 4 <= idx <= nin-2, where both stages run, the stage-1 row lies in
+// the band and no ring row is involved.
+template <class C, bool POISSON, bool CHECK, bool STEADY>
+__device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c, StreamState &st,
+                                          int idx, int r, float4 (&KA)[C::kQPT],
+                                          float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
+                                          float4 (&QA)[C::kQPT], float4 (&QB)[C::kQPT],
+                                          float4 (&QY)[C::kQPT], double &s2, float &rmax) {
+    constexpr int Q = C::kQPT;
+    constexpr unsigned M = C::kStages - 1;
+    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+    const unsigned L = st.L;
+    if (!st.broken && !mbar_wait_bounded(&st.full[L & M], (L / C::kStages) & 1u, p.timeout_ns, p.bar)) {
+        record_error(p.bar, kETimedOut, kSitePipeline);
+        st.broken = true;
+    }
+    consumers_sync();
+    const float *sx = st.slots + (L & M) * C::SLOT;
+    const float *sb = st.slots + ((L - 1u) & M) * C::SLOT;
+    const float *sa = st.slots + ((L - 2u) & M) * C::SLOT;
+    float *qw = c.qbuf + (L & 1u) * C::SLOTU;
+    const float *qr = c.qbuf + ((L - 1u) & 1u) * C::SLOTU;
+#pragma unroll
+    for (int k = 0; k < Q; ++k) KX[k] = lds4(sx + 4 + c.o[k]);
+    if (STEADY || idx >= 2) {
+        // Stage 1: U_{k+1} on row r - dir (centre KB).
+        const int ob = r - c.dir;
+        const bool ring_row = !STEADY && (ob < 1 || ob > c.ny);
+        const bool in_band = STEADY || (idx >= 3 && idx <= c.nin - 2);
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int o = c.o[k];
+            const float4 g = POISSON ? lds4(sb + C::SLOTU + 4 + o) : z4;
+            const Quad q1 = quad_t2<POISSON>(sb[3 + o], KB[k], sb[8 + o], KA[k], KX[k], g);
+            if (CHECK && in_band) quad_residual(q1, KB[k], c.valid[k], s2, rmax);
+            float4 u1 = quad_update2(q1);
+            if (ring_row) {
+                u1 = KB[k];
+            } else if (c.icol[k] + 3 > c.nx) {
+                if (c.icol[k] + 0 > c.nx) u1.x = KB[k].x;
+                if (c.icol[k] + 1 > c.nx) u1.y = KB[k].y;
+                if (c.icol[k] + 2 > c.nx) u1.z = KB[k].z;
+                u1.w = KB[k].w;
+            }
+            QY[k] = u1;
+            if (c.valid[k] > 0) *reinterpret_cast<float4 *>(qw + 4 + o) = u1;
+        }
+        // The cell beyond each strip edge (the ring column keeps U_k).
+        if (threadIdx.x == 0) {
+            float v = sb[3];
+            if (!ring_row && c.col0 > 0) {
+                float t = cell_t(sb[2], sb[4], sa[3], sx[3]);
+                if (POISSON) t = __fsub_rn(t, sb[C::SLOTU + 3]);
+                v = __fmul_rn(0.25f, t);
+            }
+            qw[3] = v;
+        }
+        if (threadIdx.x == kConsumers - 1 && (c.cols & 3) == 0) {
+            const int m = 4 + c.cols;
+            float v = sb[m];
+            if (!ring_row && c.col0 + c.cols < c.nx) {
+                float t = cell_t(sb[m - 1], sb[m + 1], sa[m], sx[m]);
+                if (POISSON) t = __fsub_rn(t, sb[C::SLOTU + m]);
+                v = __fmul_rn(0.25f, t);
+            }
+            qw[m] = v;
+        }
+    }
+    if (STEADY || idx >= 4) {
+        // Stage 2: U_{k+2} on row r - 2dir (centre QB), inside the band.
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            const int o = c.o[k];
+            const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
+            const Quad q2 = quad_t2<POISSON>(qr[3 + o], QB[k], qr[8 + o], QA[k], QY[k], g);
+            store_quad(c.drow + o, quad_update2(q2), c.valid[k]);
+        }
+        c.drow += c.dstep;
+    }
+    if (STEADY || idx >= 2) {
+        // Row r - 2dir is no longer needed: hand its slot back to the TMA.
+        fence_proxy_async_shared();
+        __syncwarp();
+        if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 2u) & M]);
+    }
+    st.L = L + 1u;
+}
+
+template <int Q>
+__device__ __forceinline__ void rotate3(float4 (&A)[Q], float4 (&B)[Q], float4 (&X)[Q]) {
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        const float4 t = A[k];
+        A[k] = B[k];
+        B[k] = X[k];
+        X[k] = t;
+    }
+}
+
 template <class C, bool POISSON, bool CHECK>
 __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *dst, int ja, int jb,
                                                  int dir, int cols, long long col0,
-                                                 StreamState &st, double &s2, float &rmax) {
+                                                 StreamState &st, float *qbuf, double &s2,
+                                                 float &rmax) {
     constexpr int Q = C::kQPT;
-    const int t = threadIdx.x;
-    const unsigned lane = t & 31;
-    const bool lo = lane == 0u, hi = lane == 31u;
-    const int nx = p.nx, ny = p.ny;
+    Seg2<Q> c;
+    c.qbuf = qbuf;
+    c.dir = dir;
+    c.cols = cols;
+    c.col0 = col0;
+    c.nin = (dir > 0 ? jb - ja : ja - jb) + 5;
+    c.nx = p.nx;
+    c.ny = p.ny;
+    c.dstep = (long long)dir * p.pitch;
+    c.drow = dst + (long long)ja * p.pitch + col0 + 4;
+#pragma unroll
+    for (int k = 0; k < Q; ++k) {
+        c.o[k] = 4 * ((int)threadIdx.x + k * kConsumers);
+        c.valid[k] = max(0, min(4, cols - c.o[k]));
+        c.icol[k] = (int)col0 + 1 + c.o[k];
+    }
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    int valid[Q];
-    long long icol[Q];  // interior column of the quad's first cell
+    float4 ka[Q], kb[Q], kx[Q], qa[Q], qb[Q], qy[Q];
 #pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        const int o = 4 * (t + k * kConsumers);
-        valid[k] = max(0, min(4, cols - o));
-        icol[k] = col0 + 1 + o;
-    }
-    const int nin = (dir > 0 ? jb - ja : ja - jb) + 5;
-    // U_k rows a (r - 2dir) and b (r - dir); U_{k+1} rows qa, qb.
-    float4 ka[Q], kb[Q], qa[Q], qb[Q], gb[Q], gq[Q];
-    float aw1[Q], bw1[Q], bw2[Q], ae1[Q], be1[Q], be2[Q], gbw[Q], gbe[Q];
-    float qaw[Q], qbw[Q], qae[Q], qbe[Q];
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        ka[k] = kb[k] = qa[k] = qb[k] = gb[k] = gq[k] = z4;
-        aw1[k] = bw1[k] = bw2[k] = ae1[k] = be1[k] = be2[k] = gbw[k] = gbe[k] = 0.f;
-        qaw[k] = qbw[k] = qae[k] = qbe[k] = 0.f;
-    }
+    for (int k = 0; k < Q; ++k) ka[k] = kb[k] = kx[k] = qa[k] = qb[k] = qy[k] = z4;
+    int idx = 0;
     int r = ja - 2 * dir;
-    for (int idx = 0; idx < nin; ++idx, r += dir) {
-        const unsigned slot = st.L & (C::kStages - 1);
-        const unsigned ph = (st.L / C::kStages) & 1u;
-        if (!st.broken && !mbar_wait_bounded(&st.full[slot], ph, p.timeout_ns, p.bar)) {
-            record_error(p.bar, kETimedOut, kSitePipeline);
-            st.broken = true;
-        }
-        const float *su = st.slots + slot * C::SLOT;
-        const float *sg = su + C::SLOTU + 4;
-        const bool gin = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= ny;
-        float4 x[Q], xg[Q];
-        float xw1[Q], xw2[Q], xe1[Q], xe2[Q], xgw[Q], xge[Q];
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = 4 * (t + k * kConsumers);
-            x[k] = lds4(su + 4 + o);
-            xw1[k] = lo ? su[3 + o] : 0.f;
-            xw2[k] = lo ? su[2 + o] : 0.f;
-            xe1[k] = hi ? su[8 + o] : 0.f;
-            xe2[k] = hi ? su[9 + o] : 0.f;
-            xg[k] = gin ? lds4(sg + o) : z4;
-            xgw[k] = (gin && lo) ? sg[o - 1] : 0.f;
-            xge[k] = (gin && hi) ? sg[o + 4] : 0.f;
-        }
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0u) mbar_arrive(&st.empty[slot]);
-        ++st.L;
-        float4 y[Q];
-        float yw[Q], ye[Q];
-        if (idx >= 2) {
-            // Stage 1: U_{k+1} on row r - dir (centre b).
-            const int o1 = r - dir;
-            const bool ring_row = o1 < 1 || o1 > ny;
-            const bool in_band = idx >= 3 && idx <= nin - 2;  // o1 in [ja, jb]
-#pragma unroll
-            for (int k = 0; k < Q; ++k) {
-                float w = __shfl_up_sync(0xffffffffu, kb[k].w, 1);
-                float e = __shfl_down_sync(0xffffffffu, kb[k].x, 1);
-                if (lo) w = bw1[k];
-                if (hi) e = be1[k];
-                const Quad q1 = quad_t<POISSON>(w, kb[k], e, ka[k], x[k], gb[k]);
-                if (CHECK && in_band) quad_residual(q1, kb[k], valid[k], s2, rmax);
-                float4 u1 = quad_update(q1);
-                if (ring_row) {
-                    u1 = kb[k];
-                } else if (icol[k] + 3 > nx) {
-                    if (icol[k] + 0 > nx) u1.x = kb[k].x;
-                    if (icol[k] + 1 > nx) u1.y = kb[k].y;
-                    if (icol[k] + 2 > nx) u1.z = kb[k].z;
-                    u1.w = kb[k].w;
-                }
-                y[k] = u1;
-                yw[k] = ye[k] = 0.f;
-                if (lo) {
-                    float tw = cell_t(bw2[k], kb[k].x, aw1[k], xw1[k]);
-                    if (POISSON) tw = __fsub_rn(tw, gbw[k]);
-                    yw[k] = (ring_row || icol[k] - 1 < 1) ? bw1[k] : __fmul_rn(0.25f, tw);
-                }
-                if (hi) {
-                    float te = cell_t(kb[k].w, be2[k], ae1[k], xe1[k]);
-                    if (POISSON) te = __fsub_rn(te, gbe[k]);
-                    ye[k] = (ring_row || icol[k] + 4 > nx) ? be1[k] : __fmul_rn(0.25f, te);
-                }
-            }
-            if (idx >= 4) {
-                // Stage 2: U_{k+2} on row r - 2dir (centre qb), inside the band.
-                float *drow = dst + (long long)(r - 2 * dir) * p.pitch + col0 + 4;
-#pragma unroll
-                for (int k = 0; k < Q; ++k) {
-                    float w = __shfl_up_sync(0xffffffffu, qb[k].w, 1);
-                    float e = __shfl_down_sync(0xffffffffu, qb[k].x, 1);
-                    if (lo) w = qbw[k];
-                    if (hi) e = qbe[k];
-                    const Quad q2 = quad_t<POISSON>(w, qb[k], e, qa[k], y[k], gq[k]);
-                    store_quad(drow + 4 * (t + k * kConsumers), quad_update(q2), valid[k]);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < Q; ++k) {
-                qa[k] = qb[k];
-                qb[k] = y[k];
-                qaw[k] = qbw[k];
-                qbw[k] = yw[k];
-                qae[k] = qbe[k];
-                qbe[k] = ye[k];
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            ka[k] = kb[k];
-            kb[k] = x[k];
-            aw1[k] = bw1[k];
-            bw1[k] = xw1[k];
-            bw2[k] = xw2[k];
-            ae1[k] = be1[k];
-            be1[k] = xe1[k];
-            be2[k] = xe2[k];
-            gq[k] = gb[k];
-            gb[k] = xg[k];
-            gbw[k] = xgw[k];
-            gbe[k] = xge[k];
-        }
+    // Prologue: the first four input rows (stages start at idx 2 and 4).
+    for (; idx < 4; ++idx, r += dir) {
+        seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+        rotate3(ka, kb, kx);
+        rotate3(qa, qb, qy);
+    }
+    // Steady rows 4 .. nin-2, three per trip with the roles renamed.
+    int steady = c.nin - 5;
+    for (; steady >= 3; steady -= 3) {
+        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx + 1, r + dir, kb, kx, ka, qb, qy, qa, s2,
+                                           rmax);
+        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, qy, qa, qb,
+                                           s2, rmax);
+        idx += 3;
+        r += 3 * dir;
+    }
+    for (; steady > 0; --steady, ++idx, r += dir) {
+        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+        rotate3(ka, kb, kx);
+        rotate3(qa, qb, qy);
+    }
+    // Last input row: stage 1 on the row beyond the band (maybe the ring).
+    seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+    // The last two input rows' slots.
+    fence_proxy_async_shared();
+    __syncwarp();
+    if ((threadIdx.x & 31u) == 0u) {
+        mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
+        mbar_arrive(&st.empty[(st.L - 1u) & (C::kStages - 1)]);
     }
 }
 
@@ -423,7 +474,8 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
         if (producer_warp) {
             produce_segment<C, POISSON, D>(p, src, jr, jb, dir, cols, col0, st);
         } else if (D == 2) {
-            consume_segment2<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st, s2, rmax);
+            consume_segment2<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st,
+                                                st.slots + C::kStages * C::SLOT, s2, rmax);
         } else {
             consume_segment<C, POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
                                                       rmax);

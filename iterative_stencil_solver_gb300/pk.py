@@ -66,6 +66,8 @@ class pk_run_info(ctypes.Structure):
         ("current", ctypes.c_int32),
         ("grid", ctypes.c_int32),
         ("variant", ctypes.c_int32),
+        ("stream_config", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
         ("device_us", ctypes.c_double),
     ]
 

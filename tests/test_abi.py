@@ -44,11 +44,35 @@ def test_library_exports_every_declared_symbol(pk):
 
 
 def test_struct_sizes_match_header(pk):
-    # pk_run_info: i64, f64, f64, f32, 5 x i32, f64 -> 56 bytes with natural alignment.
-    assert ctypes.sizeof(pk.pk_run_info) == 56
+    # pk_run_info: i64, f64, f64, f32, 7 x i32, f64 -> 64 bytes with natural alignment.
+    assert ctypes.sizeof(pk.pk_run_info) == 64
     assert ctypes.sizeof(pk.pk_task) == 40
     opt = pk.pk_options_default()
     assert opt.struct_size == ctypes.sizeof(pk.pk_options) == 88
+
+
+def test_struct_layouts_match_the_c_compiler(pk, tmp_path):
+    # Compile a probe against include/pk.h with the host C compiler and compare
+    # every field's offset and the struct sizes with the ctypes mirrors.
+    structs = {"pk_run_info": pk.pk_run_info, "pk_task": pk.pk_task, "pk_options": pk.pk_options}
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "pk.h"', "int main(void) {"]
+    for cname, cls in structs.items():
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (cname, cname))
+        for field, _ in cls._fields_:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (cname, field, cname, field))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "probe"
+    import subprocess
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split("\n")
+    got = dict(l.split() for l in out if l.strip())
+    for cname, cls in structs.items():
+        assert int(got[cname]) == ctypes.sizeof(cls), cname
+        for field, _ in cls._fields_:
+            assert int(got["%s.%s" % (cname, field)]) == getattr(cls, field).offset, (cname, field)
 
 
 def test_options_defaults(pk):
