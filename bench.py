@@ -69,7 +69,8 @@ SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1),
 
 def shape_label(info, poisson):
     if info["variant"] != 2:
-        return {1: "k_persistent_direct", 3: "k_persistent_local"}[info["variant"]]
+        return {1: "k_persistent_direct", 3: "k_persistent_local"}[info["variant"]] + \
+            ("2" if info["variant"] == 3 and info["sweeps_per_pass"] == 2 else "")
     q, ring, depth = SHAPES[info["stream_config"]]
     return "k_persistent_stream<{%d float4/thread, %d-deep ring, %d sweep%s/pass}, %s>" % (
         q, ring, depth, "s" if depth > 1 else "", "poisson" if poisson else "laplace")
@@ -80,8 +81,7 @@ def passes_of(info, sweeps, tol, check_every):
     (passes that store, check-only passes).  A two-sweep shape takes two
     sweeps per pass whenever no check can fall between them."""
     checks = tol > 0 and check_every > 0
-    two = (info["variant"] == 2 and SHAPES[info["stream_config"]][2] == 2
-           and (not checks or check_every % 2 == 0))
+    two = info["sweeps_per_pass"] == 2 and (not checks or check_every % 2 == 0)
     k, store_passes = 0, 0
     while k < sweeps:
         k += 2 if two and k + 2 <= sweeps else 1

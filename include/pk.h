@@ -69,6 +69,8 @@ extern "C" {
 #define PK_FLAG_LAUNCH_PROBLEM_GRID 0x1u /* pk_run_sweeps_launch: one thread per float4, not the persistent grid */
 #define PK_FLAG_ALTERNATE_DIRECTION 0x2u /* STREAM: odd sweeps walk each band bottom-up (reuses L2) */
 #define PK_FLAG_PROFILE_BARRIER 0x4u     /* record each CTA's total barrier wait (pk_barrier_wait_ns) */
+#define PK_FLAG_ONE_SWEEP_PER_PASS 0x8u  /* pk_run_sweeps: no temporal blocking; every pass advances
+                                            one sweep (STREAM keeps stream_config's shape or 3) */
 
 /* ---- grid barrier constructions ([P2] "The barrier is a counter and a
  * generation") -------------------------------------------------------------- */
@@ -96,7 +98,9 @@ typedef struct {
     int32_t variant;      /* PK_VARIANT_DIRECT, _STREAM or _LOCAL: the kernels that ran */
     int32_t stream_config; /* STREAM shape the sweeps ran with (pk_options.stream_config
                               index); -1 for the other variants */
-    int32_t reserved;
+    int32_t sweeps_per_pass; /* 2 when the passes advanced two sweeps each wherever they
+                                could (temporal blocking: STREAM two-sweep shapes, LOCAL
+                                with two or more rows per CTA), else 1 */
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
 } pk_run_info;

@@ -79,6 +79,8 @@ struct pk_ctx {
     int grid = 1;        // persistent sweep grid
     int stream_cfg2 = -1;  // two-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
+    bool local2 = false;   // LOCAL: the two-sweep kernel fits (same grid and rows)
+    int launch_grid = 1;   // per-launch and graph paths: CTAs of their kernels
     int coop_max = 1;    // occupancy x SMs for the sweep kernel
     int part_cap = 0;    // partial slots per parity
     Scratch *scratch = nullptr;
@@ -210,6 +212,11 @@ int coop_capacity(pk_ctx *ctx, const void *fn, int threads, size_t smem, int *pe
     return nb * ctx->sms;
 }
 
+size_t local_halo_bytes(const pk_ctx *ctx) {
+    const size_t per = ctx->local2 ? local2_halo_words(ctx->nx) : local_halo_words(ctx->nx);
+    return (size_t)ctx->grid * per * sizeof(unsigned long long);
+}
+
 long long direct_units(const pk_ctx *ctx) { return (long long)ctx->ny * ((ctx->nx + 3) / 4); }
 
 long long stream_rows(const pk_ctx *ctx, int cfg) {
@@ -238,16 +245,45 @@ int ensure_partials(pk_ctx *ctx, int grid) {
     return PK_OK;
 }
 
-// LOCAL plan: rows per CTA chosen so a CTA has about one float4 group per
-// thread, then the grid is capped by what is co-resident with the tile's
-// shared memory.  Returns false when the tile does not fit.
+// Rows of width nx whose sweeps are bound by the neighbour round trip rather
+// than by the work of a band: there, two sweeps per exchange pay (measured
+// on GB300: equal at 768 columns, a loss above).
+constexpr int kLocal2MaxQuads = 128;  // 512 columns
+
+// LOCAL plan.  At the widths LOCAL serves, a sweep costs about one
+// neighbour round trip plus the band's work, so:
+//   * narrow rows (two sweeps per exchange): bands of two rows, as many as
+//     there are SMs;
+//   * wider rows: bands of one row or more, as many as there are SMs;
+//   * a grid above the SM count only as exactly two CTAs per SM (anything
+//     in between leaves some SMs with twice the work, and the neighbour
+//     chain runs at their pace), and only when a thread then still has at
+//     least two float4 groups per sweep to overlap.
+// The grid is then capped by what is co-resident with the tile's shared
+// memory.  Returns false when the tile does not fit.
 bool plan_local(pk_ctx *ctx, int *grid_out, int *rows_out, int *cap_out) {
     const int nq = (ctx->nx + 3) / 4;
-    long long rows = (kDirectThreads + nq - 1) / nq;
-    if (rows < 1) rows = 1;
-    long long grid = (ctx->ny + rows - 1) / rows;
-    if (ctx->opt.grid_override > 0) grid = ctx->opt.grid_override;
+    const long long sms = ctx->sms > 0 ? ctx->sms : 1;
+    long long grid;
+    if (ctx->opt.grid_override > 0) {
+        grid = ctx->opt.grid_override;
+    } else {
+        const bool narrow = nq <= kLocal2MaxQuads && ctx->ny >= 4;
+        const long long base = narrow ? ctx->ny / 2 : ctx->ny;
+        grid = base < sms ? base : sms;
+        const double per_thread = (double)ctx->ny / (double)sms * nq / kDirectThreads;
+        if (base >= 2 * sms && per_thread >= 2.0) grid = 2 * sms;
+    }
+    // Enough CTAs that a band's tile fits in shared memory.
+    const size_t per_row = local_smem_bytes(ctx->nx, 1, ctx->poisson) - local_smem_bytes(ctx->nx, 0, ctx->poisson);
+    const size_t fixed = local_smem_bytes(ctx->nx, 0, ctx->poisson);
+    if (fixed + per_row > g_local_smem_max) return false;
+    const long long rows_fit = (long long)((g_local_smem_max - fixed) / per_row);
+    const long long grid_min = (ctx->ny + rows_fit - 1) / rows_fit;
+    if (ctx->opt.grid_override <= 0 && grid < grid_min) grid = grid_min;
     if (grid > ctx->ny) grid = ctx->ny;
+    if (grid < 1) grid = 1;
+    long long rows;
     for (int it = 0; it < 8; ++it) {
         rows = (ctx->ny + grid - 1) / grid;
         const size_t smem = local_smem_bytes(ctx->nx, (int)rows, ctx->poisson);
@@ -313,8 +349,21 @@ int plan(pk_ctx *ctx) {
         cap = lcap;
         ctx->grid = lgrid;
         ctx->local_rows = lrows;
-        const size_t words = (size_t)lgrid * local_halo_words(ctx->nx);
-        PK_TRY(ctx, cudaMalloc(&ctx->halo, words * sizeof(unsigned long long)));
+        // Two sweeps per exchange need two rows in every CTA (both halo rows
+        // of a side come from one neighbour) and the wider tile co-resident;
+        // they are taken for narrow rows only, where they pay.
+        ctx->local2 = false;
+        if (ctx->ny / lgrid >= 2 && (ctx->nx + 3) / 4 <= kLocal2MaxQuads) {
+            const size_t smem2 = local2_smem_bytes(ctx->nx, lrows, ctx->poisson);
+            if (smem2 <= g_local_smem_max) {
+                int per2 = 0;
+                const int cap2 = coop_capacity(ctx, kernel_persistent(kVariantLocal2, ctx->poisson, 0),
+                                               kDirectThreads, smem2, &per2);
+                if (cap2 < 0) return PK_ECUDA;
+                ctx->local2 = cap2 >= lgrid;
+            }
+        }
+        PK_TRY(ctx, cudaMalloc(&ctx->halo, local_halo_bytes(ctx)));
     } else {
         int per_sm = 0;
         cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, ctx->stream_cfg),
@@ -336,8 +385,19 @@ int plan(pk_ctx *ctx) {
     if (tneed < 1) tneed = 1;
     ctx->task_grid = (int)(tneed < tcap ? tneed : tcap);
     if (ctx->opt.task_grid > 0) ctx->task_grid = ctx->opt.task_grid;
+    // The per-launch and graph paths run the persistent kernels' per-launch
+    // forms on the same grid, except for a LOCAL context: its launches run
+    // the DIRECT kernel, sized for one float4 group per thread.
+    ctx->launch_grid = ctx->grid;
+    if (v == kVariantLocal && ctx->opt.grid_override <= 0) {
+        long long need = (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+        if (need < 1) need = 1;
+        if (need > (1LL << 30)) need = 1LL << 30;
+        ctx->launch_grid = (int)need;
+    }
     int want = ctx->grid > cap ? ctx->grid : cap;
     if (ctx->grid2 > want) want = ctx->grid2;
+    if (ctx->launch_grid > want) want = ctx->launch_grid;
     return ensure_partials(ctx, want);
 }
 
@@ -375,6 +435,7 @@ SweepParams base_params(pk_ctx *ctx) {
     p.halo = ctx->halo;
     p.local_rows = ctx->local_rows;
     p.local_pitch = local_pitch(ctx->nx);
+    p.one_sweep = (ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS) ? 1 : 0;
     return p;
 }
 
@@ -471,7 +532,8 @@ double elapsed_us(pk_ctx *ctx) {
 }
 
 void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
-               float rmax, int n_checks, int status, int grid, int variant = 0, int shape = -2) {
+               float rmax, int n_checks, int status, int grid, int variant = 0, int shape = -2,
+               int depth = 1) {
     if (!info) return;
     info->sweeps_done = sweeps;
     info->res0 = res0;
@@ -484,7 +546,7 @@ void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, do
     info->variant = variant ? variant : ctx->variant;
     if (shape == -2) shape = info->variant == kVariantStream ? ctx->stream_cfg : -1;
     info->stream_config = info->variant == kVariantStream ? shape : -1;
-    info->reserved = 0;
+    info->sweeps_per_pass = depth;
     info->device_us = elapsed_us(ctx);
 }
 
@@ -648,19 +710,24 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.tol = tol;
     p.check_every = check_every;
     if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
-        PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0,
-                                    (size_t)ctx->grid * local_halo_words(ctx->nx) * sizeof(unsigned long long),
-                                    ctx->stream));
-    // The two-sweep shape pays off when its passes can advance two sweeps:
-    // at least two sweeps, and no check falling between the two.
+        PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0, local_halo_bytes(ctx), ctx->stream));
+    // Two sweeps per pass pay off when passes can advance two sweeps: at
+    // least two sweeps, and no check falling between the two.
     const bool checks = tol > 0.f && check_every > 0;
-    int shape = ctx->stream_cfg, grid = ctx->grid;
-    if (ctx->stream_cfg2 >= 0 && n >= 2 && (!checks || check_every % 2 == 0)) {
+    const bool two_ok = n >= 2 && (!checks || check_every % 2 == 0) &&
+                        !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
+    int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
+    if (ctx->stream_cfg2 >= 0 && two_ok) {
         shape = ctx->stream_cfg2;
         grid = ctx->grid2;
     }
+    if (ctx->variant == kVariantStream && stream_depth(shape) == 2 && two_ok) depth = 2;
+    if (ctx->variant == kVariantLocal && ctx->local2 && two_ok) {
+        kernel = kVariantLocal2;
+        depth = 2;
+    }
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_persistent(ctx->variant, ctx->poisson, shape, grid, p, ctx->stream);
+    cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
@@ -669,7 +736,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     int rc = bar_status(ctx, p.bar, "pk_run_sweeps");
     if (rc != PK_OK) {
         ctx->sweep_bar_base = 0;  // bar_status zeroed the barrier words
-        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, 0, shape);
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, 0, shape, depth);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
@@ -678,7 +745,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     if (p.profile) ctx->spin_valid = grid;
     ctx->cur = ctx->h_info->cur;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
-              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid, 0, shape);
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid, 0, shape, depth);
     return PK_OK;
 }
 
@@ -687,7 +754,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
     if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_sweeps_launch: n < 0");
     if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_sweeps_launch: tol is NaN");
     if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_sweeps_launch: the task kernel is live");
-    int grid = ctx->grid;
+    int grid = ctx->launch_grid;
     if (ctx->opt.flags & PK_FLAG_LAUNCH_PROBLEM_GRID) {
         long long need = launch_variant(ctx) == kVariantStream ? (stream_rows(ctx) + 31) / 32
                                                         : (direct_units(ctx) + kDirectThreads - 1) /
@@ -752,7 +819,7 @@ constexpr long long kGraphMaxSweeps = 1000;  // longest plain segment in one gra
 // when `check`, else `plain` ordinary sweeps, starting from buffer `cur`
 // with direction parity `kpar`.
 int graph_for(pk_ctx *ctx, bool check, long long plain, int cur, int kpar, cudaGraphExec_t *out) {
-    const auto key = std::make_tuple(check ? 1 : 0, plain, cur, kpar, ctx->grid);
+    const auto key = std::make_tuple(check ? 1 : 0, plain, cur, kpar, ctx->launch_grid);
     auto it = ctx->graphs.find(key);
     if (it != ctx->graphs.end()) {
         *out = it->second;
@@ -769,8 +836,8 @@ int graph_for(pk_ctx *ctx, bool check, long long plain, int cur, int kpar, cudaG
         p.pass_store = 1;
         p.pass_parity = 0;
         p.pass_k = k;
-        e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->grid, p, ctx->stream);
-        if (e == cudaSuccess) e = launch_finalize(launch_variant(ctx), ctx->grid, p, &ctx->scratch->res, ctx->stream);
+        e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->launch_grid, p, ctx->stream);
+        if (e == cudaSuccess) e = launch_finalize(launch_variant(ctx), ctx->launch_grid, p, &ctx->scratch->res, ctx->stream);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
                                 cudaMemcpyDeviceToHost, ctx->stream);
@@ -780,7 +847,7 @@ int graph_for(pk_ctx *ctx, bool check, long long plain, int cur, int kpar, cudaG
             p.pass_check = 0;
             p.pass_store = 1;
             p.pass_k = k;
-            e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->grid, p, ctx->stream);
+            e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->launch_grid, p, ctx->stream);
         }
     }
     cudaError_t e2 = cudaStreamEndCapture(ctx->stream, &graph);
@@ -828,9 +895,9 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
                 p.pass_parity = 0;
                 p.pass_k = k;
                 cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg,
-                                            ctx->grid, p, ctx->stream);
+                                            ctx->launch_grid, p, ctx->stream);
                 if (e == cudaSuccess)
-                    e = launch_finalize(launch_variant(ctx), ctx->grid, p, &ctx->scratch->res,
+                    e = launch_finalize(launch_variant(ctx), ctx->launch_grid, p, &ctx->scratch->res,
                                         ctx->stream);
                 if (e == cudaSuccess)
                     e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
@@ -870,7 +937,7 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     ctx->cur = cur;
-    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->grid, launch_variant(ctx));
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->launch_grid, launch_variant(ctx));
     return PK_OK;
 }
 

@@ -65,6 +65,7 @@ struct SweepParams {
     unsigned long long *halo;
     int local_rows;         // most rows any CTA owns
     int local_pitch;        // floats per tile row in shared memory
+    int one_sweep;          // 1: every pass advances one sweep (no temporal blocking)
 };
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
@@ -159,7 +160,8 @@ void set_global_error(const char *msg);
 
 // ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
 // Every wrapper returns the cudaError_t of its launch.
-enum Variant { kVariantDirect = 1, kVariantStream = 2, kVariantLocal = 3 };
+enum Variant { kVariantDirect = 1, kVariantStream = 2, kVariantLocal = 3,
+               kVariantLocal2 = 4 /* internal: LOCAL with two sweeps per exchange */ };
 
 // LOCAL variant: each CTA keeps its band (rows + one halo row each side) in
 // shared memory, twice (ping-pong), plus its source rows for Poisson.
@@ -171,6 +173,14 @@ inline size_t local_smem_bytes(int nx, int rows, bool poisson) {
 }
 // Halo words per CTA: 2 sides x 2 parities x (interior columns rounded to 4).
 inline size_t local_halo_words(int nx) { return (size_t)4 * ((nx + 3) / 4 * 4); }
+// Two sweeps per exchange: two halo rows each side, and the source rows of
+// the band plus one row on each side.
+inline size_t local2_smem_bytes(int nx, int rows, bool poisson) {
+    const size_t tile = (size_t)2 * (rows + 4) * local_pitch(nx) * sizeof(float);
+    const size_t g = poisson ? (size_t)(rows + 2) * ((nx + 3) / 4 * 4) * sizeof(float) : 0;
+    return tile + g;
+}
+inline size_t local2_halo_words(int nx) { return 2 * local_halo_words(nx); }
 
 // Once per device: kernel attributes (dynamic shared memory limits).
 // Configurations whose shared memory does not fit are left unset and

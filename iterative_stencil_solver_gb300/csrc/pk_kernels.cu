@@ -549,7 +549,8 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         const bool check = checks && (k % p.check_every) == 0;
         if (k == p.n && !check) break;
         const bool store = k < p.n;
-        const bool two = MAXD >= 2 && store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0);
+        const bool two = MAXD >= 2 && store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0) &&
+                         !p.one_sweep;
         double s2 = 0.0;
         float rmax = 0.f;
         pass(p.u[cur], p.u[cur ^ 1], check, store, two, k, s2, rmax);
@@ -681,6 +682,68 @@ __device__ __forceinline__ bool ld_tagged4(const unsigned long long *p, unsigned
     return true;
 }
 
+// Polls up to four tagged float4 units per thread at once (their loads are
+// in flight together, so a thread with several units pays one round trip,
+// not one per unit) until each carries `tag`, and stores it.  `unit(u, src,
+// dst, valid)` maps unit u < total to its tagged words and its destination,
+// or returns false when the unit has no neighbour.  False on timeout/abort.
+template <class UnitFn>
+__device__ __forceinline__ bool recv_tagged(int total, unsigned tag, const SweepParams &sp,
+                                            UnitFn &&unit) {
+    const int step = 4 * (int)blockDim.x;
+    for (int base = 0; base < total; base += step) {
+        const unsigned long long *src[4];
+        float *dst[4];
+        int valid[4];
+        unsigned pending = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int u = base + (int)threadIdx.x + j * (int)blockDim.x;
+            src[j] = nullptr;
+            dst[j] = nullptr;
+            valid[j] = 0;
+            if (u < total && unit(u, src[j], dst[j], valid[j])) pending |= 1u << j;
+        }
+        const uint64_t t0 = globaltimer_ns();
+        unsigned spins = 0;
+        while (pending) {
+            unsigned long long w[4][4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                w[j][0] = w[j][1] = w[j][2] = w[j][3] = 0ull;
+                if (pending & (1u << j)) {
+                    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+                                 : "=l"(w[j][0]), "=l"(w[j][1]) : "l"(src[j]) : "memory");
+                    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+                                 : "=l"(w[j][2]), "=l"(w[j][3]) : "l"(src[j] + 2) : "memory");
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                if (!(pending & (1u << j))) continue;
+                if ((unsigned)(w[j][0] >> 32) == tag && (unsigned)(w[j][1] >> 32) == tag &&
+                    (unsigned)(w[j][2] >> 32) == tag && (unsigned)(w[j][3] >> 32) == tag) {
+                    store_quad(dst[j],
+                               make_float4(__uint_as_float((unsigned)w[j][0]),
+                                           __uint_as_float((unsigned)w[j][1]),
+                                           __uint_as_float((unsigned)w[j][2]),
+                                           __uint_as_float((unsigned)w[j][3])),
+                               valid[j]);
+                    pending &= ~(1u << j);
+                }
+            }
+            if (pending && (++spins & 31u) == 0u) {
+                if (aborted(sp.bar)) return false;
+                if (globaltimer_ns() - t0 > sp.timeout_ns) {
+                    record_error(sp.bar, kETimedOut, kSiteBarrier);
+                    return false;
+                }
+            }
+        }
+    }
+    return true;
+}
+
 template <bool POISSON>
 __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams p) {
     extern __shared__ __align__(16) float tile[];
@@ -776,15 +839,16 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
         }
         if (k == p.n) break;
         // Halo rows of U_{k+1} from the neighbours (rows 0 and B+1 of Tn).
-        bool ok = true;
-        for (int q = tid; q < 2 * nq && ok; q += nthr) {
+        const bool ok = recv_tagged(2 * nq, tag, p,
+                                    [&](int q, const unsigned long long *&src, float *&dst, int &valid) {
             const int side = q < nq ? 0 : 1;
             const int qq = side ? q - nq : q;
-            if (side == 0 ? b == 0 : b == G - 1) continue;
-            float4 v;
-            ok = ld_tagged4(mine + (side * 2 + par) * hw + 4 * qq, tag, v, p);
-            if (ok) store_quad(Tn + (side ? B + 1 : 0) * sp + 4 + 4 * qq, v, min(4, nx - 4 * qq));
-        }
+            if (side == 0 ? b == 0 : b == G - 1) return false;
+            src = mine + (side * 2 + par) * hw + 4 * qq;
+            dst = Tn + (side ? B + 1 : 0) * sp + 4 + 4 * qq;
+            valid = min(4, nx - 4 * qq);
+            return true;
+        });
         if (__syncthreads_or(!ok)) return;  // a wait expired: the host reads the error
         c ^= 1;
         ++k;
@@ -793,6 +857,191 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
     for (int u = tid; u < B * nq; u += nthr) {
         const int lr = u / nq + 1, q = u - (lr - 1) * nq;
         store_quad(dst + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q,
+                   ld4(T[c] + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+    }
+    if (b == 0 && tid == 0) {
+        DeviceInfo *d = p.info;
+        d->sweeps_done = k;
+        d->res0 = res0;
+        d->res_last = res_last;
+        d->rmax_last = rmax_last;
+        d->n_checks = n_checks;
+        d->cur = p.cur ^ (int)(k & 1);
+        d->task_sweeps = 0;
+        d->barriers = ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
+        __threadfence();
+        d->run_id = p.run_id;
+    }
+}
+
+// Two sweeps per exchange on the LOCAL layout (temporal blocking as the
+// pages' "Reflections" suggest: a wider halo, several steps per
+// synchronisation).  Each CTA keeps TWO halo rows on each side of its band.
+// A two-sweep pass computes U_{k+1} on its rows and one row beyond each side
+// (from the two halo rows of U_k), then U_{k+2} on its rows, and sends its
+// first two and last two rows of U_{k+2} to the neighbours as tagged words;
+// so the neighbour wait, which bounds a sweep at small sizes, happens once
+// per two sweeps.  A pass that cannot advance two sweeps (a check would fall
+// between them, or one sweep is left) computes one and exchanges two rows
+// all the same.  Tags are the index of the iterate sent; the halo areas are
+// double-buffered by pass parity (a neighbour cannot run two passes ahead:
+// it needs this CTA's rows of the pass in between).  Every CTA owns at least
+// two rows, so both halo rows on a side come from the one neighbour (the
+// host checks this before choosing the kernel).
+//
+// Tile row lr holds grid row r0 - 2 + lr, lr = 0 .. B+3; rows beyond the
+// ring are never read.  The source rows cover r0-1 .. r1 (stage-1 rows).
+template <bool POISSON>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_local2(SweepParams p) {
+    extern __shared__ __align__(16) float tile[];
+    const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
+    const int nx = p.nx, ny = p.ny;
+    const int r0 = 1 + (int)((long long)ny * b / G);
+    const int r1 = 1 + (int)((long long)ny * (b + 1) / G);
+    const int B = r1 - r0;
+    const int sp = p.local_pitch, spq = sp / 4;
+    const int nq = (nx + 3) >> 2, gw = 4 * nq;
+    const size_t trows = (size_t)p.local_rows + 4;
+    float *T[2] = {tile, tile + trows * sp};
+    float *gs = tile + 2 * trows * sp;
+    const size_t rw = (size_t)4 * nq;  // words per halo row
+    const size_t hw = 2 * rw;          // words per (side, parity) area: two rows
+    unsigned long long *mine = p.halo + (size_t)b * 4 * hw;
+    unsigned long long *up = b > 0 ? p.halo + (size_t)(b - 1) * 4 * hw : nullptr;
+    unsigned long long *down = b < G - 1 ? p.halo + (size_t)(b + 1) * 4 * hw : nullptr;
+
+    const float *u0 = p.u[p.cur];
+    for (int q = tid; q < (B + 4) * spq; q += nthr) {
+        const int lr = q / spq, c4 = q - lr * spq;
+        const int gr = r0 - 2 + lr;
+        if (gr < 0 || gr > ny + 1) continue;
+        const float4 v = ld4(u0 + (long long)gr * p.pitch + 4 * c4);
+        *reinterpret_cast<float4 *>(T[0] + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(T[1] + lr * sp + 4 * c4) = v;
+    }
+    if (POISSON) {
+        for (int q = tid; q < (B + 2) * nq; q += nthr) {
+            const int lg = q / nq, c4 = q - lg * nq;
+            const int gr = r0 - 1 + lg;
+            if (gr < 1 || gr > ny) continue;
+            *reinterpret_cast<float4 *>(gs + lg * gw + 4 * c4) =
+                ld4(p.g + (long long)(gr - 1) * p.gpitch + 4 * c4);
+        }
+    }
+    __syncthreads();
+
+    // The new iterate's first two and last two band rows go to the neighbours.
+    auto send = [&](int lr, int q, float4 v, unsigned tag, size_t par) {
+        if (up && lr <= 3) st_tagged4(up + (2 + par) * hw + (lr - 2) * rw + 4 * q, v, tag);
+        if (down && lr >= B) st_tagged4(down + par * hw + (lr - B) * rw + 4 * q, v, tag);
+    };
+
+    BarrierCtl ctl = make_ctl(p);
+    const bool checks = p.tol > 0.f && p.check_every > 0;
+    int c = 0;
+    long long k = 0;
+    unsigned pass = 0;
+    double res0 = 0.0, res_last = 0.0;
+    float rmax_last = 0.f;
+    int n_checks = 0;
+    for (;;) {
+        const bool check = checks && (k % p.check_every) == 0;
+        if (k == p.n && !check) break;
+        // fault injection: this CTA leaves at the first pass from sweep
+        // skip_at on; its neighbours' tagged waits then expire (host-driven)
+        if (b == p.skip_cta && k >= p.skip_at) return;
+        const bool store = k < p.n;
+        const bool two = store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0) &&
+                         !p.one_sweep;
+        const float *Tc = T[c];
+        float *Tn = T[c ^ 1];
+        const unsigned tag = (unsigned)(k + (two ? 2 : 1));
+        const size_t par = (size_t)(pass & 1u);
+        double s2 = 0.0;
+        float rmax = 0.f;
+        // Stage 1: U_{k+1} (the residual of U_k on the band rows).
+        const int lo = two ? 1 : 2, hi = two ? B + 2 : B + 1;
+        for (int u = tid; u < (hi - lo + 1) * nq; u += nthr) {
+            const int lr = lo + u / nq, q = u - (lr - lo) * nq;
+            const int gr = r0 - 2 + lr;
+            if (gr < 1 || gr > ny) continue;  // ring rows keep their value in both tiles
+            const float *row = Tc + lr * sp + 4 + 4 * q;
+            const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
+            const float W = row[-1], E = row[4];
+            float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
+            const int valid = min(4, nx - 4 * q);
+            const Quad t = quad_t<POISSON>(W, C, E, S, N, G4);
+            if (check && lr >= 2 && lr <= B + 1) quad_residual(t, C, valid, s2, rmax);
+            if (store) {
+                const float4 v = quad_update(t);
+                store_quad(Tn + lr * sp + 4 + 4 * q, v, valid);
+                if (!two) send(lr, q, v, tag, par);
+            }
+        }
+        if (check) {
+            Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+            block_reduce(s2, rmax);
+            if (tid == 0) {
+                Partial pp;
+                pp.s2 = s2;
+                pp.rmax = rmax;
+                pp.pad = 0.f;
+                parts[b] = pp;
+            }
+            if (!grid_barrier(ctl)) return;
+            double S2;
+            float RM;
+            reduce_partials(parts, G, S2, RM);
+            const double res = sqrt(S2);
+            ++n_checks;
+            res_last = res;
+            rmax_last = RM;
+            if (k == 0)
+                res0 = res;
+            else if (res < (double)p.tol * res0)
+                break;  // U_k is still in T[c]
+        }
+        if (k == p.n) break;
+        float *Tout = Tn;
+        if (two) {
+            // Stage 2: U_{k+2} on the band rows, over U_k (no longer read).
+            __syncthreads();
+            Tout = T[c];
+            for (int u = tid; u < B * nq; u += nthr) {
+                const int lr = 2 + u / nq, q = u - (lr - 2) * nq;
+                const float *row = Tn + lr * sp + 4 + 4 * q;
+                const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
+                const float W = row[-1], E = row[4];
+                float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
+                const float4 v = quad_update(quad_t<POISSON>(W, C, E, S, N, G4));
+                store_quad(Tout + lr * sp + 4 + 4 * q, v, min(4, nx - 4 * q));
+                send(lr, q, v, tag, par);
+            }
+        }
+        // The neighbours' two rows on each side of the new iterate.
+        const bool ok = recv_tagged(4 * nq, tag, p,
+                                    [&](int q, const unsigned long long *&src, float *&dst, int &valid) {
+            const int side = q < 2 * nq ? 0 : 1;
+            const int rem = q - side * 2 * nq;
+            const int hr = rem / nq, qq = rem - hr * nq;
+            if (side == 0 ? b == 0 : b == G - 1) return false;
+            src = mine + (side * 2 + par) * hw + hr * rw + 4 * qq;
+            dst = Tout + (side ? B + 2 + hr : hr) * sp + 4 + 4 * qq;
+            valid = min(4, nx - 4 * qq);
+            return true;
+        });
+        if (__syncthreads_or(!ok)) return;  // a wait expired: the host reads the error
+        if (!two) c ^= 1;
+        k += two ? 2 : 1;
+        ++pass;
+    }
+    float *dst = p.u[p.cur ^ (int)(k & 1)];
+    for (int u = tid; u < B * nq; u += nthr) {
+        const int lr = 2 + u / nq, q = u - (lr - 2) * nq;
+        store_quad(dst + (long long)(r0 - 2 + lr) * p.pitch + 4 + 4 * q,
                    ld4(T[c] + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
@@ -1537,9 +1786,11 @@ cudaError_t prepare_kernels() {
         return cudaSuccess;
     };
     size_t local_max = (size_t)optin;
-    for (int which = 0; which < 4; ++which) {
+    for (int which = 0; which < 6; ++which) {
         const bool poisson = which & 1;
-        const void *fn = (which & 2) ? (poisson ? (const void *)k_persistent_local_rb<true>
+        const void *fn = (which & 4) ? (poisson ? (const void *)k_persistent_local2<true>
+                                                : (const void *)k_persistent_local2<false>)
+                       : (which & 2) ? (poisson ? (const void *)k_persistent_local_rb<true>
                                                 : (const void *)k_persistent_local_rb<false>)
                                      : (poisson ? (const void *)k_persistent_local<true>
                                                 : (const void *)k_persistent_local<false>);
@@ -1581,6 +1832,8 @@ bool stream_config_ok(int cfg, bool poisson) {
 }
 
 const void *kernel_persistent(int variant, bool poisson, int cfg) {
+    if (variant == kVariantLocal2)
+        return poisson ? (const void *)k_persistent_local2<true> : (const void *)k_persistent_local2<false>;
     if (variant == kVariantLocal)
         return poisson ? (const void *)k_persistent_local<true> : (const void *)k_persistent_local<false>;
     if (variant == kVariantStream) return poisson ? stream_fn<true>(cfg, true) : stream_fn<false>(cfg, true);
@@ -1612,8 +1865,9 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
                               cudaStream_t s) {
     SweepParams arg = p;
     void *args[] = {&arg};
-    const size_t smem = variant == kVariantLocal ? local_smem_bytes(p.nx, p.local_rows, poisson)
-                                                 : dyn_smem(variant, poisson, cfg);
+    const size_t smem = variant == kVariantLocal    ? local_smem_bytes(p.nx, p.local_rows, poisson)
+                        : variant == kVariantLocal2 ? local2_smem_bytes(p.nx, p.local_rows, poisson)
+                                                    : dyn_smem(variant, poisson, cfg);
     return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
                                        dim3(block_threads(variant)), args, smem, s);
 }

@@ -36,6 +36,7 @@ PK_VARIANT_LOCAL = 3
 PK_FLAG_LAUNCH_PROBLEM_GRID = 0x1
 PK_FLAG_ALTERNATE_DIRECTION = 0x2
 PK_FLAG_PROFILE_BARRIER = 0x4
+PK_FLAG_ONE_SWEEP_PER_PASS = 0x8
 
 PK_BARRIER_GENERATION = 0
 PK_BARRIER_COUNTER = 1
@@ -67,7 +68,7 @@ class pk_run_info(ctypes.Structure):
         ("grid", ctypes.c_int32),
         ("variant", ctypes.c_int32),
         ("stream_config", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("sweeps_per_pass", ctypes.c_int32),
         ("device_us", ctypes.c_double),
     ]
 

@@ -4,8 +4,10 @@ import bench
 CELLS = 16384 * 16384
 
 
-def info(variant, shape):
-    return {"variant": variant, "stream_config": shape}
+def info(variant, shape, depth=None):
+    if depth is None:
+        depth = bench.SHAPES[shape][2] if variant == 2 else 1
+    return {"variant": variant, "stream_config": shape, "sweeps_per_pass": depth}
 
 
 def test_single_sweep_shape_moves_8_bytes_per_cell_update():
@@ -32,4 +34,6 @@ def test_checks_between_pairs_force_single_sweeps():
 def test_other_variants_take_one_sweep_per_pass():
     assert bench.passes_of(info(1, -1), 10, 0.0, 0) == (10, 0)
     assert bench.passes_of(info(3, -1), 10, 0.0, 0) == (10, 0)
+    assert bench.passes_of(info(3, -1, 2), 10, 0.0, 0) == (5, 0)
+    assert bench.shape_label(info(3, -1, 2), False) == "k_persistent_local2"
     assert bench.shape_label(info(2, 6), False).startswith("k_persistent_stream<{1 float4/thread, 8-deep ring, 2 sweeps/pass}")

@@ -365,12 +365,13 @@ def test_barrier_and_cg_sync_microbenchmarks(pk):
         pk.pk_destroy(ctx)
 
 
-@pytest.mark.parametrize("variant", [1, 2, 3], ids=["direct", "stream", "local"])
-def test_barrier_timeout_is_reported_not_hung(pk, variant):
+@pytest.mark.parametrize("variant,nx,ny", [(1, 512, 512), (2, 3000, 200), (3, 3000, 200),
+                                           (3, 512, 512)],
+                         ids=["direct", "stream", "local", "local-two-sweeps"])
+def test_barrier_timeout_is_reported_not_hung(pk, variant, nx, ny):
     """Fault injection on the host's say-so: one CTA leaves without arriving;
     the others give up after the (short) limit and the call returns
     PK_ETIMEDOUT.  The device stays usable."""
-    nx, ny = (512, 512) if variant == 1 else (3000, 200)
     u0 = inputs.random_field(nx, ny, seed=31)
     opt = pk.pk_options_default(variant=variant, barrier_timeout_s=0.2, debug_skip_arrival_cta=1,
                                 debug_skip_arrival_at=3)
@@ -589,7 +590,7 @@ def test_graph_path_long_runs_and_reuse(pk):
 # ---- LOCAL: shared-memory bands, tagged neighbour halos ---------------------------
 
 LOCAL_CASES = [(1030, 9, 0), (63, 65, 0), (512, 512, 0), (100, 100, 7), (300, 301, 0),
-               (64, 64, 0), (257, 50, 3), (5, 1000, 0)]
+               (64, 64, 0), (257, 50, 3), (5, 1000, 0), (40, 50, 20), (37, 41, 20), (9, 4, 2)]
 
 
 @pytest.mark.parametrize("nx,ny,grid", LOCAL_CASES, ids=["%dx%d-g%d" % c for c in LOCAL_CASES])
@@ -597,12 +598,31 @@ LOCAL_CASES = [(1030, 9, 0), (63, 65, 0), (512, 512, 0), (100, 100, 7), (300, 30
 def test_local_variant_bit_exact(pk, nx, ny, grid, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    for n, tol, ce in ((41, 0.0, 0), (33, 1e-30, 8), (12, 1e-30, 1)):
+    for n, tol, ce in ((41, 0.0, 0), (33, 1e-30, 8), (12, 1e-30, 1), (30, 0.9, 2)):
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, variant=3, grid_override=grid)
         assert info["variant"] == 3
         if grid:
             assert info["grid"] == min(grid, ny)
+        # two sweeps per exchange whenever every band has two rows and no
+        # check falls between a pair
+        two_ok = n >= 2 and (ce == 0 or ce % 2 == 0)
+        narrow = nx <= 512
+        assert info["sweeps_per_pass"] == (2 if two_ok and narrow and ny // info["grid"] >= 2 else 1)
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+@pytest.mark.parametrize("nx,ny", [(512, 512), (64, 64), (130, 7)], ids=["512x512", "64x64", "130x7"])
+def test_local_context_launch_paths_use_direct_problem_grid(pk, nx, ny):
+    """A LOCAL context's per-launch and graph paths run the DIRECT kernel with
+    one float4 group per thread, whatever grid the LOCAL bands use."""
+    u0 = inputs.random_field(nx, ny, seed=nx + ny)
+    want, oinfo = oracle.jacobi_run(u0, n=9, tol=1e-30, check_every=3)
+    need = -(-((nx + 3) // 4) * ny // 256)
+    for path in ("launch", "graph"):
+        got, info = run_pk(pk, u0, None, 9, 1e-30, 3, path=path, variant=3)
+        assert info["variant"] == 1 and info["grid"] == need
         assert_same_bits(got, want)
         check_info(info, oinfo)
 
