@@ -132,10 +132,11 @@ typedef struct {
     uint32_t flags;                   /* PK_FLAG_* (default PK_FLAG_ALTERNATE_DIRECTION) */
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
-    int32_t stream_config;            /* STREAM shape.  -1 = default: shape 6 for persistent
-                                         runs that can take two sweeps per pass (n >= 2 and
-                                         checks off or check_every even), shape 3 for the
-                                         rest and for the per-launch and graph paths
+    int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs
+                                         that can take two sweeps per pass (n >= 2 and checks
+                                         off or check_every even) shape 8 (Laplace), 7
+                                         (Poisson, nx >= 8192) or 6 (Poisson); shape 3 for
+                                         the rest and for the per-launch and graph paths
                                          (pk_run_info.stream_config says which ran).  Index into
                                          {float4 groups per thread, TMA ring depth, sweeps
                                          per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}

@@ -226,7 +226,14 @@ long long stream_rows(const pk_ctx *ctx, int cfg) {
 long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_cfg); }
 
 constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
-constexpr int kDefaultStreamConfig2 = 6;  // two sweeps per pass, 1024-column strips, 2 CTAs/SM
+// Two-sweep shape for persistent runs, from measurements on GB300: Laplace
+// {1 float4/thread, 16-deep ring} (2 CTAs/SM); Poisson, whose ring slot also
+// holds the source row, {2, 8} (1 CTA/SM) from 8192 columns on and {1, 8}
+// (2 CTAs/SM) below.
+int default_two_sweep_shape(bool poisson, int nx) {
+    if (!poisson) return 8;
+    return nx >= 8192 ? 7 : 6;
+}
 
 int ensure_partials(pk_ctx *ctx, int grid) {
     if (grid <= ctx->part_cap) return PK_OK;
@@ -329,17 +336,16 @@ int plan(pk_ctx *ctx) {
     // the two-sweep shape (same bits, half the HBM traffic per sweep).
     ctx->stream_cfg2 = -1;
     ctx->grid2 = 0;
-    if (v == kVariantStream && ctx->opt.stream_config < 0 &&
-        stream_config_ok(kDefaultStreamConfig2, ctx->poisson)) {
+    const int shape2 = default_two_sweep_shape(ctx->poisson, ctx->nx);
+    if (v == kVariantStream && ctx->opt.stream_config < 0 && stream_config_ok(shape2, ctx->poisson)) {
         int per_sm2 = 0;
-        const int cap2 = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, kDefaultStreamConfig2),
-                                       block_threads(v),
-                                       dyn_smem(v, ctx->poisson, kDefaultStreamConfig2), &per_sm2);
+        const int cap2 = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, shape2),
+                                       block_threads(v), dyn_smem(v, ctx->poisson, shape2), &per_sm2);
         if (cap2 < 0) return PK_ECUDA;
         if (cap2 > 0) {
-            long long need2 = stream_rows(ctx, kDefaultStreamConfig2);
+            long long need2 = stream_rows(ctx, shape2);
             if (need2 < 1) need2 = 1;
-            ctx->stream_cfg2 = kDefaultStreamConfig2;
+            ctx->stream_cfg2 = shape2;
             ctx->grid2 = (int)(need2 < cap2 ? need2 : cap2);
             if (ctx->opt.grid_override > 0) ctx->grid2 = ctx->opt.grid_override;
         }

@@ -287,8 +287,9 @@ struct Seg2 {
 // rows (QA, QB, QY = the new one) are passed in their current roles, so an
 // unrolled caller can rotate roles by renaming instead of moving registers.
 // STEADY: 4 <= idx <= nin-2, where both stages run, the stage-1 row lies in
-// the band and no ring row is involved.
-template <class C, bool POISSON, bool CHECK, bool STEADY>
+// the band and no ring row is involved.  FULL: the strip is TW columns wide,
+// so every quad holds four interior cells and none holds the ring column.
+template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL = false>
 __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c, StreamState &st,
                                           int idx, int r, float4 (&KA)[C::kQPT],
                                           float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
@@ -320,18 +321,18 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
             const int o = c.o[k];
             const float4 g = POISSON ? lds4(sb + C::SLOTU + 4 + o) : z4;
             const Quad q1 = quad_t2<POISSON>(sb[3 + o], KB[k], sb[8 + o], KA[k], KX[k], g);
-            if (CHECK && in_band) quad_residual(q1, KB[k], c.valid[k], s2, rmax);
+            if (CHECK && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
             float4 u1 = quad_update2(q1);
             if (ring_row) {
                 u1 = KB[k];
-            } else if (c.icol[k] + 3 > c.nx) {
+            } else if (!FULL && c.icol[k] + 3 > c.nx) {
                 if (c.icol[k] + 0 > c.nx) u1.x = KB[k].x;
                 if (c.icol[k] + 1 > c.nx) u1.y = KB[k].y;
                 if (c.icol[k] + 2 > c.nx) u1.z = KB[k].z;
                 u1.w = KB[k].w;
             }
             QY[k] = u1;
-            if (c.valid[k] > 0) *reinterpret_cast<float4 *>(qw + 4 + o) = u1;
+            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(qw + 4 + o) = u1;
         }
         // The cell beyond each strip edge (the ring column keeps U_k).
         if (threadIdx.x == 0) {
@@ -361,7 +362,10 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
             const int o = c.o[k];
             const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
             const Quad q2 = quad_t2<POISSON>(qr[3 + o], QB[k], qr[8 + o], QA[k], QY[k], g);
-            store_quad(c.drow + o, quad_update2(q2), c.valid[k]);
+            if (FULL)
+                *reinterpret_cast<float4 *>(c.drow + o) = quad_update2(q2);
+            else
+                store_quad(c.drow + o, quad_update2(q2), c.valid[k]);
         }
         c.drow += c.dstep;
     }
@@ -372,6 +376,33 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
         if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 2u) & M]);
     }
     st.L = L + 1u;
+}
+
+template <int Q>
+__device__ __forceinline__ void rotate3(float4 (&A)[Q], float4 (&B)[Q], float4 (&X)[Q]);
+
+// Steady input rows of a segment, three per trip with the roles renamed.
+template <class C, bool POISSON, bool CHECK, bool FULL>
+__device__ __forceinline__ void seg2_steady(const SweepParams &p, Seg2<C::kQPT> &c, StreamState &st,
+                                            int &idx, int &r, int steady, float4 (&ka)[C::kQPT],
+                                            float4 (&kb)[C::kQPT], float4 (&kx)[C::kQPT],
+                                            float4 (&qa)[C::kQPT], float4 (&qb)[C::kQPT],
+                                            float4 (&qy)[C::kQPT], double &s2, float &rmax) {
+    const int dir = c.dir;
+    for (; steady >= 3; steady -= 3) {
+        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 1, r + dir, kb, kx, ka, qb, qy, qa,
+                                                 s2, rmax);
+        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, qy, qa,
+                                                 qb, s2, rmax);
+        idx += 3;
+        r += 3 * dir;
+    }
+    for (; steady > 0; --steady, ++idx, r += dir) {
+        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
+        rotate3(ka, kb, kx);
+        rotate3(qa, qb, qy);
+    }
 }
 
 template <int Q>
@@ -419,22 +450,13 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
         rotate3(ka, kb, kx);
         rotate3(qa, qb, qy);
     }
-    // Steady rows 4 .. nin-2, three per trip with the roles renamed.
-    int steady = c.nin - 5;
-    for (; steady >= 3; steady -= 3) {
-        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx + 1, r + dir, kb, kx, ka, qb, qy, qa, s2,
-                                           rmax);
-        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, qy, qa, qb,
-                                           s2, rmax);
-        idx += 3;
-        r += 3 * dir;
-    }
-    for (; steady > 0; --steady, ++idx, r += dir) {
-        seg2_step<C, POISSON, CHECK, true>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(qa, qb, qy);
-    }
+    // Steady rows 4 .. nin-2.
+    if (cols == C::TW)
+        seg2_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, c.nin - 5, ka, kb, kx, qa, qb, qy,
+                                             s2, rmax);
+    else
+        seg2_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, c.nin - 5, ka, kb, kx, qa, qb, qy,
+                                              s2, rmax);
     // Last input row: stage 1 on the row beyond the band (maybe the ring).
     seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
     // The last two input rows' slots.

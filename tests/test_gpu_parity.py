@@ -440,23 +440,28 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
 # The default STREAM plan: persistent runs whose passes can take two sweeps
 # use the two-sweep shape; the others, and the per-launch path, keep the
 # single-sweep shape.  Either way the bits are those of single sweeps.
+TWO = "two-sweep"
 DEFAULT_SHAPE_RUNS = [
     # (n, tol, check_every, expected shape)
-    (8, 0.0, 0, 6),
-    (9, 0.0, 0, 6),       # ends with one single sweep in the two-sweep shape
-    (10, 1e-30, 4, 6),
+    (8, 0.0, 0, TWO),
+    (9, 0.0, 0, TWO),     # ends with one single sweep in the two-sweep shape
+    (10, 1e-30, 4, TWO),
     (9, 1e-30, 3, 3),     # an odd interval puts checks between sweep pairs
     (1, 0.0, 0, 3),
-    (40, 0.5, 2, 6),      # early exit on a check at the start of a pass
+    (40, 0.5, 2, TWO),    # early exit on a check at the start of a pass
 ]
 
 
-@pytest.mark.parametrize("nx,ny", [(2053, 37), (1024, 5), (4100, 3)], ids=["2053x37", "1024x5", "4100x3"])
+@pytest.mark.parametrize("nx,ny", [(2053, 37), (1024, 5), (4100, 3), (8200, 3)],
+                         ids=["2053x37", "1024x5", "4100x3", "8200x3"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    # Laplace: {1 float4/thread, 16-deep ring}; Poisson: {2, 8} from 8192 columns, else {1, 8}
+    two = 8 if not poisson else (7 if nx >= 8192 else 6)
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
+        shape = two if shape == TWO else shape
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, path="persistent", variant=2)
         assert info["variant"] == 2 and info["stream_config"] == shape, (n, tol, ce, info)
