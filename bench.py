@@ -81,10 +81,13 @@ def passes_of(info, sweeps, tol, check_every):
     (passes that store, check-only passes).  A two-sweep shape takes two
     sweeps per pass whenever no check can fall between them."""
     checks = tol > 0 and check_every > 0
-    two = info["sweeps_per_pass"] == 2 and (not checks or check_every % 2 == 0)
+    depth = info["sweeps_per_pass"]
     k, store_passes = 0, 0
     while k < sweeps:
-        k += 2 if two and k + 2 <= sweeps else 1
+        dp = min(depth, sweeps - k)
+        if checks:
+            dp = min(dp, check_every - k % check_every)
+        k += dp
         store_passes += 1
     check_only = 1 if checks and sweeps % check_every == 0 else 0
     return store_passes, check_only
@@ -274,6 +277,27 @@ def reference_arm(args, world, rank):
 
 # ---- supplementary measurements (rank 0) ------------------------------------------
 
+def barrier_spin(pk, w, sweeps, **opts):
+    """Per-CTA time spent waiting in the grid barrier over one persistent run
+    (%globaltimer around each wait, PK_FLAG_PROFILE_BARRIER)."""
+    flags = opts.pop("flags", pk.PK_FLAG_ALTERNATE_DIRECTION) | pk.PK_FLAG_PROFILE_BARRIER
+    ctx = pk.pk_create(w["nx"], w["ny"], w["u0"], w["f"], pk.pk_options_default(flags=flags, **opts))
+    try:
+        pk.pk_run_sweeps(ctx, sweeps)
+        info = pk.pk_run_sweeps(ctx, sweeps)
+        waits = pk.pk_barrier_wait_ns(ctx).astype(np.float64)
+    finally:
+        pk.pk_destroy(ctx)
+    store_passes, check_only = passes_of(info, sweeps, 0.0, 0)
+    barriers = store_passes + check_only
+    run_ns = info["device_us"] * 1e3
+    return {"kernel": shape_label(info, w["f"] is not None), "grid": info["grid"],
+            "barriers": barriers, "run_us": info["device_us"],
+            "wait_us_per_barrier_mean": float(waits.mean()) / barriers / 1e3,
+            "wait_us_per_barrier_max_cta": float(waits.max()) / barriers / 1e3,
+            "wait_fraction_of_run_mean": float(waits.mean()) / run_ns}
+
+
 def latency_extras(pk):
     """512^2 persistent vs per-launch (1000 sweeps), floors, barrier costs, and
     the task-queue round trip (10,000 tasks)."""
@@ -396,8 +420,8 @@ def latency_extras(pk):
     # Temporal blocking: two sweeps per HBM pass, same bits (16384^2, 100 sweeps)
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
-    for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 6),
-                      ("two_sweeps_per_pass_16_deep_ring", 8)):
+    for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 8),
+                      ("two_sweeps_per_pass_8_deep_ring", 6)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):
@@ -412,6 +436,13 @@ def latency_extras(pk):
             pk.pk_destroy(ctx)
     tb["speedup"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
     out["temporal_blocking_16384_100sweeps"] = tb
+    # Barrier spin: the headline kernel (one barrier per two-sweep pass) and
+    # the barrier-per-sweep DIRECT kernel on the L2-resident 512^2 grid.
+    out["barrier_spin"] = {
+        "laplace_16384_100sweeps": barrier_spin(pk, w, 100),
+        "laplace_512_1000sweeps_direct": barrier_spin(pk, inputs.workload_laplace_random(512, 1),
+                                                      1000, variant=1),
+    }
     del w
     # Poisson 4096^2 with the in-kernel residual every 10 sweeps
     w = make_workload("poisson-4096x4096-2000sweeps-res10")

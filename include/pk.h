@@ -98,9 +98,10 @@ typedef struct {
     int32_t variant;      /* PK_VARIANT_DIRECT, _STREAM or _LOCAL: the kernels that ran */
     int32_t stream_config; /* STREAM shape the sweeps ran with (pk_options.stream_config
                               index); -1 for the other variants */
-    int32_t sweeps_per_pass; /* 2 when the passes advanced two sweeps each wherever they
-                                could (temporal blocking: STREAM two-sweep shapes, LOCAL
-                                with two or more rows per CTA), else 1 */
+    int32_t sweeps_per_pass; /* the most sweeps a pass advanced (temporal blocking): a pass
+                                takes that many, or fewer where n ends or a residual check
+                                would fall inside it.  STREAM two-sweep shapes: 2 (1 when
+                                check_every is odd); LOCAL: the plan's local_depth; else 1 */
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
 } pk_run_info;
@@ -147,7 +148,12 @@ typedef struct {
                                          are off or check_every is even; results are the
                                          same bits.  A shape whose ring does not fit in
                                          shared memory is refused with PK_EINVAL. */
-    int32_t reserved[5];
+    int32_t local_depth;              /* LOCAL: sweeps per neighbour exchange, 1..4 (temporal
+                                         blocking with that many halo rows a side); 0 = by
+                                         the plan.  The bands get at least that many rows;
+                                         where the tile cannot, the depth is lowered.  Same
+                                         bits at every depth. */
+    int32_t reserved[4];
 } pk_options;
 
 /* Fill opt with the defaults above. */

@@ -79,7 +79,7 @@ struct pk_ctx {
     int grid = 1;        // persistent sweep grid
     int stream_cfg2 = -1;  // two-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
-    bool local2 = false;   // LOCAL: the two-sweep kernel fits (same grid and rows)
+    int local_depth = 1;   // LOCAL: sweeps per neighbour exchange the plan allows
     int launch_grid = 1;   // per-launch and graph paths: CTAs of their kernels
     int coop_max = 1;    // occupancy x SMs for the sweep kernel
     int part_cap = 0;    // partial slots per parity
@@ -194,6 +194,8 @@ int read_options(pk_ctx *ctx, const pk_options *opt) {
         return fail(ctx, PK_EINVAL, "unknown barrier_kind %d", o.barrier_kind);
     if (o.stream_config < -1 || o.stream_config >= kNumStreamConfigs)
         return fail(ctx, PK_EINVAL, "stream_config %d out of range", o.stream_config);
+    if (o.local_depth < 0 || o.local_depth > kLocalMaxDepth)
+        return fail(ctx, PK_EINVAL, "local_depth %d out of range", o.local_depth);
     return PK_OK;
 }
 
@@ -213,7 +215,7 @@ int coop_capacity(pk_ctx *ctx, const void *fn, int threads, size_t smem, int *pe
 }
 
 size_t local_halo_bytes(const pk_ctx *ctx) {
-    const size_t per = ctx->local2 ? local2_halo_words(ctx->nx) : local_halo_words(ctx->nx);
+    const size_t per = local_d_halo_words(ctx->nx, ctx->local_depth);
     return (size_t)ctx->grid * per * sizeof(unsigned long long);
 }
 
@@ -252,14 +254,23 @@ int ensure_partials(pk_ctx *ctx, int grid) {
     return PK_OK;
 }
 
-// Rows of width nx whose sweeps are bound by the neighbour round trip rather
-// than by the work of a band: there, two sweeps per exchange pay (measured
-// on GB300: equal at 768 columns, a loss above).
-constexpr int kLocal2MaxQuads = 128;  // 512 columns
+// Sweeps per neighbour exchange the plan aims at: the option, else by row
+// width, as measured on GB300 (1000 sweeps, bands sized as below).  Up to
+// 128 columns a sweep is mostly the neighbour round trip and D = 4 is best
+// (64^2: 0.51 us/sweep against 1.03 at D = 1); up to 512 columns D = 3 is
+// within 7% of the best depth at every shape tried; from 768 columns the
+// band's work dominates and one sweep per exchange is best.
+int local_target_depth(const pk_ctx *ctx) {
+    if (ctx->opt.local_depth > 0) return ctx->opt.local_depth;
+    const int nq = (ctx->nx + 3) / 4;
+    if (nq <= 32) return 4;
+    if (nq <= 128) return 3;
+    return 1;
+}
 
 // LOCAL plan.  At the widths LOCAL serves, a sweep costs about one
 // neighbour round trip plus the band's work, so:
-//   * narrow rows (two sweeps per exchange): bands of two rows, as many as
+//   * narrow rows (D sweeps per exchange): bands of D rows, as many as
 //     there are SMs;
 //   * wider rows: bands of one row or more, as many as there are SMs;
 //   * a grid above the SM count only as exactly two CTAs per SM (anything
@@ -275,8 +286,9 @@ bool plan_local(pk_ctx *ctx, int *grid_out, int *rows_out, int *cap_out) {
     if (ctx->opt.grid_override > 0) {
         grid = ctx->opt.grid_override;
     } else {
-        const bool narrow = nq <= kLocal2MaxQuads && ctx->ny >= 4;
-        const long long base = narrow ? ctx->ny / 2 : ctx->ny;
+        const int depth = local_target_depth(ctx);
+        long long base = ctx->ny / depth;
+        if (base < 1) base = 1;
         grid = base < sms ? base : sms;
         const double per_thread = (double)ctx->ny / (double)sms * nq / kDirectThreads;
         if (base >= 2 * sms && per_thread >= 2.0) grid = 2 * sms;
@@ -355,20 +367,24 @@ int plan(pk_ctx *ctx) {
         cap = lcap;
         ctx->grid = lgrid;
         ctx->local_rows = lrows;
-        // Two sweeps per exchange need two rows in every CTA (both halo rows
-        // of a side come from one neighbour) and the wider tile co-resident;
-        // they are taken for narrow rows only, where they pay.
-        ctx->local2 = false;
-        if (ctx->ny / lgrid >= 2 && (ctx->nx + 3) / 4 <= kLocal2MaxQuads) {
-            const size_t smem2 = local2_smem_bytes(ctx->nx, lrows, ctx->poisson);
-            if (smem2 <= g_local_smem_max) {
-                int per2 = 0;
-                const int cap2 = coop_capacity(ctx, kernel_persistent(kVariantLocal2, ctx->poisson, 0),
-                                               kDirectThreads, smem2, &per2);
-                if (cap2 < 0) return PK_ECUDA;
-                ctx->local2 = cap2 >= lgrid;
+        // D sweeps per exchange need D rows in every CTA (all D halo rows of
+        // a side come from one neighbour) and the wider tile co-resident;
+        // the depth is lowered until both hold.
+        int depth = local_target_depth(ctx);
+        while (depth >= 2) {
+            if (ctx->ny / lgrid >= depth) {
+                const size_t smem_d = local_d_smem_bytes(ctx->nx, lrows, ctx->poisson, depth);
+                if (smem_d <= g_local_smem_max) {
+                    int per_d = 0;
+                    const int cap_d = coop_capacity(ctx, kernel_persistent(kVariantLocalD, ctx->poisson, depth),
+                                                    kDirectThreads, smem_d, &per_d);
+                    if (cap_d < 0) return PK_ECUDA;
+                    if (cap_d >= lgrid) break;
+                }
             }
+            --depth;
         }
+        ctx->local_depth = depth < 1 ? 1 : depth;
         PK_TRY(ctx, cudaMalloc(&ctx->halo, local_halo_bytes(ctx)));
     } else {
         int per_sm = 0;
@@ -728,9 +744,12 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
         grid = ctx->grid2;
     }
     if (ctx->variant == kVariantStream && stream_depth(shape) == 2 && two_ok) depth = 2;
-    if (ctx->variant == kVariantLocal && ctx->local2 && two_ok) {
-        kernel = kVariantLocal2;
-        depth = 2;
+    if (ctx->variant == kVariantLocal && ctx->local_depth >= 2 &&
+        !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS)) {
+        // passes take up to local_depth sweeps, never past a check
+        kernel = kVariantLocalD;
+        shape = ctx->local_depth;
+        depth = ctx->local_depth;
     }
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream);

@@ -161,7 +161,8 @@ void set_global_error(const char *msg);
 // ---- launch wrappers (defined in pk_kernels.cu) ----------------------------
 // Every wrapper returns the cudaError_t of its launch.
 enum Variant { kVariantDirect = 1, kVariantStream = 2, kVariantLocal = 3,
-               kVariantLocal2 = 4 /* internal: LOCAL with two sweeps per exchange */ };
+               kVariantLocalD = 4 /* internal: LOCAL with D sweeps per exchange */ };
+constexpr int kLocalMaxDepth = 4;  // sweeps per neighbour exchange, at most
 
 // LOCAL variant: each CTA keeps its band (rows + one halo row each side) in
 // shared memory, twice (ping-pong), plus its source rows for Poisson.
@@ -173,14 +174,14 @@ inline size_t local_smem_bytes(int nx, int rows, bool poisson) {
 }
 // Halo words per CTA: 2 sides x 2 parities x (interior columns rounded to 4).
 inline size_t local_halo_words(int nx) { return (size_t)4 * ((nx + 3) / 4 * 4); }
-// Two sweeps per exchange: two halo rows each side, and the source rows of
-// the band plus one row on each side.
-inline size_t local2_smem_bytes(int nx, int rows, bool poisson) {
-    const size_t tile = (size_t)2 * (rows + 4) * local_pitch(nx) * sizeof(float);
-    const size_t g = poisson ? (size_t)(rows + 2) * ((nx + 3) / 4 * 4) * sizeof(float) : 0;
+// D sweeps per exchange: D halo rows each side, and the source rows of the
+// band plus D-1 rows on each side.
+inline size_t local_d_smem_bytes(int nx, int rows, bool poisson, int depth) {
+    const size_t tile = (size_t)2 * (rows + 2 * depth) * local_pitch(nx) * sizeof(float);
+    const size_t g = poisson ? (size_t)(rows + 2 * depth - 2) * ((nx + 3) / 4 * 4) * sizeof(float) : 0;
     return tile + g;
 }
-inline size_t local2_halo_words(int nx) { return 2 * local_halo_words(nx); }
+inline size_t local_d_halo_words(int nx, int depth) { return (size_t)depth * local_halo_words(nx); }
 
 // Once per device: kernel attributes (dynamic shared memory limits).
 // Configurations whose shared memory does not fit are left unset and

@@ -776,7 +776,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
     const int B = r1 - r0;
     const int sp = p.local_pitch, spq = sp / 4;
     const int nq = (nx + 3) >> 2, gw = 4 * nq;
-    float *T[2] = {tile, tile + (size_t)(p.local_rows + 2) * sp};
+    float *const Ta = tile, *const Tb = tile + (size_t)(p.local_rows + 2) * sp;  // by parity c
     float *gs = tile + (size_t)2 * (p.local_rows + 2) * sp;
     const size_t hw = (size_t)4 * nq;  // words per (side, parity) area
     unsigned long long *mine = p.halo + (size_t)b * 4 * hw;
@@ -787,8 +787,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
     for (int q = tid; q < (B + 2) * spq; q += nthr) {
         const int lr = q / spq, c4 = q - lr * spq;
         const float4 v = ld4(u0 + (long long)(r0 - 1 + lr) * p.pitch + 4 * c4);
-        *reinterpret_cast<float4 *>(T[0] + lr * sp + 4 * c4) = v;
-        *reinterpret_cast<float4 *>(T[1] + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(Ta + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(Tb + lr * sp + 4 * c4) = v;
     }
     if (POISSON) {
         for (int q = tid; q < B * nq; q += nthr) {
@@ -813,8 +813,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
         // neighbours' tagged waits then expire (host-driven test only)
         if (b == p.skip_cta && k == p.skip_at) return;
         const bool store = k < p.n;
-        const float *Tc = T[c];
-        float *Tn = T[c ^ 1];
+        const float *Tc = c ? Tb : Ta;
+        float *Tn = c ? Ta : Tb;
         const unsigned tag = (unsigned)(k + 1);
         const size_t par = (size_t)((k + 1) & 1);
         double s2 = 0.0;
@@ -879,7 +879,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
     for (int u = tid; u < B * nq; u += nthr) {
         const int lr = u / nq + 1, q = u - (lr - 1) * nq;
         store_quad(dst + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q,
-                   ld4(T[c] + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+                   ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
         DeviceInfo *d = p.info;
@@ -897,25 +897,84 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams
     }
 }
 
-// Two sweeps per exchange on the LOCAL layout (temporal blocking as the
-// pages' "Reflections" suggest: a wider halo, several steps per
-// synchronisation).  Each CTA keeps TWO halo rows on each side of its band.
-// A two-sweep pass computes U_{k+1} on its rows and one row beyond each side
-// (from the two halo rows of U_k), then U_{k+2} on its rows, and sends its
-// first two and last two rows of U_{k+2} to the neighbours as tagged words;
-// so the neighbour wait, which bounds a sweep at small sizes, happens once
-// per two sweeps.  A pass that cannot advance two sweeps (a check would fall
-// between them, or one sweep is left) computes one and exchanges two rows
-// all the same.  Tags are the index of the iterate sent; the halo areas are
-// double-buffered by pass parity (a neighbour cannot run two passes ahead:
-// it needs this CTA's rows of the pass in between).  Every CTA owns at least
-// two rows, so both halo rows on a side come from the one neighbour (the
-// host checks this before choosing the kernel).
-//
-// Tile row lr holds grid row r0 - 2 + lr, lr = 0 .. B+3; rows beyond the
-// ring are never read.  The source rows cover r0-1 .. r1 (stage-1 rows).
+// Per-CTA constants of a depth-D LOCAL band, and this thread's walk over
+// a stage's float4 groups (row offset and column of its first group, and
+// the step between its groups), computed once per kernel: a division by the
+// run-time row width at every stage would cost every thread, working or not.
+struct LocalBand {
+    const float *gs;
+    unsigned long long *up, *down;
+    size_t rw, hw;
+    int r0, B, D, sp, nq, gw, nx, ny;
+    int t_row, t_col, dl, dq;
+};
+
+// One stage of a LOCAL pass: U_{k+s} from U_{k+s-1} (tile Ts to tile Td) on
+// tile rows lo .. lo+nrows-1; ring rows keep their value in both tiles.
+// resid reduces the residual of the source on the band rows, store writes
+// the update, and send also sends the band's first and last D rows to the
+// neighbours (the last stage of a pass).  The flags are run-time values on
+// purpose: one copy of the loop keeps the pass small in the instruction
+// cache, which measured faster than a copy per flag combination.  Threads
+// walk the rows' float4 groups in row-major order, stepping without a
+// division per group.
 template <bool POISSON>
-__global__ void __launch_bounds__(kDirectThreads) k_persistent_local2(SweepParams p) {
+__device__ __forceinline__ void local_stage(const LocalBand &lb, const float *Ts, float *Td, int lo,
+                                            int nrows, bool resid, bool store, bool send,
+                                            unsigned tag, size_t par, double &s2, float &rmax) {
+    const int nq = lb.nq, sp = lb.sp, dl = lb.dl, dq = lb.dq;
+    int lr = lo + lb.t_row, q = lb.t_col;
+    const int end = lo + nrows;
+    for (; lr < end;) {
+        const int gr = lb.r0 - lb.D + lr;
+        if (gr >= 1 && gr <= lb.ny) {
+            const float *row = Ts + lr * sp + 4 + 4 * q;
+            const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
+            const float W = row[-1], E = row[4];
+            float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (POISSON) G4 = ld4(lb.gs + (lr - 1) * lb.gw + 4 * q);
+            const int valid = min(4, lb.nx - 4 * q);
+            const Quad t = quad_t<POISSON>(W, C, E, S, N, G4);
+            if (resid && lr >= lb.D && lr < lb.D + lb.B) quad_residual(t, C, valid, s2, rmax);
+            if (store) {
+                const float4 v = quad_update(t);
+                store_quad(Td + lr * sp + 4 + 4 * q, v, valid);
+                if (send) {
+                    if (lb.up && lr < 2 * lb.D)
+                        st_tagged4(lb.up + (2 + par) * lb.hw + (lr - lb.D) * lb.rw + 4 * q, v, tag);
+                    if (lb.down && lr >= lb.B)
+                        st_tagged4(lb.down + par * lb.hw + (lr - lb.B) * lb.rw + 4 * q, v, tag);
+                }
+            }
+        }
+        lr += dl;
+        q += dq;
+        if (q >= nq) {
+            q -= nq;
+            ++lr;
+        }
+    }
+}
+
+// D sweeps per exchange on the LOCAL layout (temporal blocking as the
+// pages' "Reflections" suggest: a wider halo, several steps per
+// synchronisation).  Each CTA keeps D halo rows on each side of its band.
+// A pass of dp <= D sweeps computes U_{k+1} .. U_{k+dp} in shared memory,
+// stage s on the band widened by dp - s rows each side (the rows later
+// stages still read), and sends its first D and last D band rows of
+// U_{k+dp} to the neighbours as tagged words, so the neighbour wait, which
+// bounds a sweep at small sizes, happens once per dp sweeps.  A pass takes
+// as many sweeps as it may without a residual check falling inside it.
+// Tags are the index of the iterate sent; the halo areas are double-
+// buffered by pass parity (a neighbour cannot run two passes ahead: it
+// needs this CTA's rows of the pass in between).  Every CTA owns at least D
+// rows, so all D halo rows of a side come from one neighbour (the host
+// checks this before choosing the kernel).
+//
+// Tile row lr holds grid row r0 - D + lr, lr = 0 .. B+2D-1; rows beyond the
+// ring are never read.  Source row lg = lr - 1 covers the computed rows.
+template <bool POISSON, int D>
+__global__ void __launch_bounds__(kDirectThreads) k_persistent_local_d(SweepParams p) {
     extern __shared__ __align__(16) float tile[];
     const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
     const int nx = p.nx, ny = p.ny;
@@ -924,28 +983,30 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local2(SweepParam
     const int B = r1 - r0;
     const int sp = p.local_pitch, spq = sp / 4;
     const int nq = (nx + 3) >> 2, gw = 4 * nq;
-    const size_t trows = (size_t)p.local_rows + 4;
-    float *T[2] = {tile, tile + trows * sp};
+    const size_t trows = (size_t)p.local_rows + 2 * D;
+    // the two tiles, chosen by parity with a select (an indexed array would
+    // live in local memory)
+    float *const Ta = tile, *const Tb = tile + trows * sp;
     float *gs = tile + 2 * trows * sp;
     const size_t rw = (size_t)4 * nq;  // words per halo row
-    const size_t hw = 2 * rw;          // words per (side, parity) area: two rows
+    const size_t hw = D * rw;          // words per (side, parity) area
     unsigned long long *mine = p.halo + (size_t)b * 4 * hw;
     unsigned long long *up = b > 0 ? p.halo + (size_t)(b - 1) * 4 * hw : nullptr;
     unsigned long long *down = b < G - 1 ? p.halo + (size_t)(b + 1) * 4 * hw : nullptr;
 
     const float *u0 = p.u[p.cur];
-    for (int q = tid; q < (B + 4) * spq; q += nthr) {
+    for (int q = tid; q < (B + 2 * D) * spq; q += nthr) {
         const int lr = q / spq, c4 = q - lr * spq;
-        const int gr = r0 - 2 + lr;
+        const int gr = r0 - D + lr;
         if (gr < 0 || gr > ny + 1) continue;
         const float4 v = ld4(u0 + (long long)gr * p.pitch + 4 * c4);
-        *reinterpret_cast<float4 *>(T[0] + lr * sp + 4 * c4) = v;
-        *reinterpret_cast<float4 *>(T[1] + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(Ta + lr * sp + 4 * c4) = v;
+        *reinterpret_cast<float4 *>(Tb + lr * sp + 4 * c4) = v;
     }
     if (POISSON) {
-        for (int q = tid; q < (B + 2) * nq; q += nthr) {
+        for (int q = tid; q < (B + 2 * D - 2) * nq; q += nthr) {
             const int lg = q / nq, c4 = q - lg * nq;
-            const int gr = r0 - 1 + lg;
+            const int gr = r0 - D + 1 + lg;
             if (gr < 1 || gr > ny) continue;
             *reinterpret_cast<float4 *>(gs + lg * gw + 4 * c4) =
                 ld4(p.g + (long long)(gr - 1) * p.gpitch + 4 * c4);
@@ -953,11 +1014,24 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local2(SweepParam
     }
     __syncthreads();
 
-    // The new iterate's first two and last two band rows go to the neighbours.
-    auto send = [&](int lr, int q, float4 v, unsigned tag, size_t par) {
-        if (up && lr <= 3) st_tagged4(up + (2 + par) * hw + (lr - 2) * rw + 4 * q, v, tag);
-        if (down && lr >= B) st_tagged4(down + par * hw + (lr - B) * rw + 4 * q, v, tag);
-    };
+    LocalBand lb;
+    lb.gs = gs;
+    lb.up = up;
+    lb.down = down;
+    lb.rw = rw;
+    lb.hw = hw;
+    lb.r0 = r0;
+    lb.B = B;
+    lb.D = D;
+    lb.sp = sp;
+    lb.nq = nq;
+    lb.gw = gw;
+    lb.nx = nx;
+    lb.ny = ny;
+    lb.t_row = tid / nq;
+    lb.t_col = tid - lb.t_row * nq;
+    lb.dl = nthr / nq;
+    lb.dq = nthr - lb.dl * nq;
 
     BarrierCtl ctl = make_ctl(p);
     const bool checks = p.tol > 0.f && p.check_every > 0;
@@ -974,97 +1048,78 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local2(SweepParam
         // skip_at on; its neighbours' tagged waits then expire (host-driven)
         if (b == p.skip_cta && k >= p.skip_at) return;
         const bool store = k < p.n;
-        const bool two = store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0) &&
-                         !p.one_sweep;
-        const float *Tc = T[c];
-        float *Tn = T[c ^ 1];
-        const unsigned tag = (unsigned)(k + (two ? 2 : 1));
+        int dp = 1;  // sweeps this pass: up to D, none of them past a check
+        if (store && !p.one_sweep) {
+            long long m = p.n - k;
+            if (checks) {
+                const long long to_check = p.check_every - (k % p.check_every);
+                if (to_check < m) m = to_check;
+            }
+            dp = m < D ? (int)m : D;
+        }
+        const unsigned tag = (unsigned)(k + dp);
         const size_t par = (size_t)(pass & 1u);
+        // Stage s: U_{k+s} from U_{k+s-1}, on the band and dp-s rows beyond
+        // each side; stage 1 also reduces the residual of U_k on the band.
         double s2 = 0.0;
         float rmax = 0.f;
-        // Stage 1: U_{k+1} (the residual of U_k on the band rows).
-        const int lo = two ? 1 : 2, hi = two ? B + 2 : B + 1;
-        for (int u = tid; u < (hi - lo + 1) * nq; u += nthr) {
-            const int lr = lo + u / nq, q = u - (lr - lo) * nq;
-            const int gr = r0 - 2 + lr;
-            if (gr < 1 || gr > ny) continue;  // ring rows keep their value in both tiles
-            const float *row = Tc + lr * sp + 4 + 4 * q;
-            const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
-            const float W = row[-1], E = row[4];
-            float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
-            const int valid = min(4, nx - 4 * q);
-            const Quad t = quad_t<POISSON>(W, C, E, S, N, G4);
-            if (check && lr >= 2 && lr <= B + 1) quad_residual(t, C, valid, s2, rmax);
-            if (store) {
-                const float4 v = quad_update(t);
-                store_quad(Tn + lr * sp + 4 + 4 * q, v, valid);
-                if (!two) send(lr, q, v, tag, par);
+        bool exit_now = false;
+        for (int s = 1; s <= dp; ++s) {
+            if (s > 1) __syncthreads();
+            const int ext = store ? dp - s : 0;
+            local_stage<POISSON>(lb, ((c + s - 1) & 1) ? Tb : Ta, ((c + s) & 1) ? Tb : Ta, D - ext,
+                                 B + 2 * ext, s == 1 && check, store, store && s == dp, tag, par, s2,
+                                 rmax);
+            if (s == 1 && check) {
+                Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
+                block_reduce(s2, rmax);
+                if (tid == 0) {
+                    Partial pp;
+                    pp.s2 = s2;
+                    pp.rmax = rmax;
+                    pp.pad = 0.f;
+                    parts[b] = pp;
+                }
+                if (!grid_barrier(ctl)) return;
+                double S2;
+                float RM;
+                reduce_partials(parts, G, S2, RM);
+                const double res = sqrt(S2);
+                ++n_checks;
+                res_last = res;
+                rmax_last = RM;
+                if (k == 0) {
+                    res0 = res;
+                } else if (res < (double)p.tol * res0) {
+                    exit_now = true;  // U_k is still in tile c
+                    break;
+                }
             }
         }
-        if (check) {
-            Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
-            block_reduce(s2, rmax);
-            if (tid == 0) {
-                Partial pp;
-                pp.s2 = s2;
-                pp.rmax = rmax;
-                pp.pad = 0.f;
-                parts[b] = pp;
-            }
-            if (!grid_barrier(ctl)) return;
-            double S2;
-            float RM;
-            reduce_partials(parts, G, S2, RM);
-            const double res = sqrt(S2);
-            ++n_checks;
-            res_last = res;
-            rmax_last = RM;
-            if (k == 0)
-                res0 = res;
-            else if (res < (double)p.tol * res0)
-                break;  // U_k is still in T[c]
-        }
-        if (k == p.n) break;
-        float *Tout = Tn;
-        if (two) {
-            // Stage 2: U_{k+2} on the band rows, over U_k (no longer read).
-            __syncthreads();
-            Tout = T[c];
-            for (int u = tid; u < B * nq; u += nthr) {
-                const int lr = 2 + u / nq, q = u - (lr - 2) * nq;
-                const float *row = Tn + lr * sp + 4 + 4 * q;
-                const float4 C = ld4(row), S = ld4(row - sp), N = ld4(row + sp);
-                const float W = row[-1], E = row[4];
-                float4 G4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (POISSON) G4 = ld4(gs + (lr - 1) * gw + 4 * q);
-                const float4 v = quad_update(quad_t<POISSON>(W, C, E, S, N, G4));
-                store_quad(Tout + lr * sp + 4 + 4 * q, v, min(4, nx - 4 * q));
-                send(lr, q, v, tag, par);
-            }
-        }
-        // The neighbours' two rows on each side of the new iterate.
-        const bool ok = recv_tagged(4 * nq, tag, p,
+        if (exit_now || !store) break;  // early exit, or k == n: the residual of U_n only
+        // The neighbours' D rows on each side of the new iterate.
+        float *Tout = ((c + dp) & 1) ? Tb : Ta;
+        const bool ok = recv_tagged(2 * D * nq, tag, p,
                                     [&](int q, const unsigned long long *&src, float *&dst, int &valid) {
-            const int side = q < 2 * nq ? 0 : 1;
-            const int rem = q - side * 2 * nq;
+            const int side = q < D * nq ? 0 : 1;
+            const int rem = q - side * D * nq;
             const int hr = rem / nq, qq = rem - hr * nq;
             if (side == 0 ? b == 0 : b == G - 1) return false;
             src = mine + (side * 2 + par) * hw + hr * rw + 4 * qq;
-            dst = Tout + (side ? B + 2 + hr : hr) * sp + 4 + 4 * qq;
+            dst = Tout + (side ? B + D + hr : hr) * sp + 4 + 4 * qq;
             valid = min(4, nx - 4 * qq);
             return true;
         });
         if (__syncthreads_or(!ok)) return;  // a wait expired: the host reads the error
-        if (!two) c ^= 1;
-        k += two ? 2 : 1;
+        c = (c + dp) & 1;
+        k += dp;
         ++pass;
     }
     float *dst = p.u[p.cur ^ (int)(k & 1)];
     for (int u = tid; u < B * nq; u += nthr) {
-        const int lr = 2 + u / nq, q = u - (lr - 2) * nq;
-        store_quad(dst + (long long)(r0 - 2 + lr) * p.pitch + 4 + 4 * q,
-                   ld4(T[c] + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+        const int lr = D + u / nq, q = u - (lr - D) * nq;
+        store_quad(dst + (long long)(r0 - D + lr) * p.pitch + 4 + 4 * q,
+                   ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
         DeviceInfo *d = p.info;
@@ -1790,6 +1845,15 @@ const void *stream_fn(int cfg, bool persistent) {
 }
 static_assert(kNumStreamConfigs == 10, "update stream_fn");
 
+// The depth-D LOCAL kernel (2 <= D <= kLocalMaxDepth).
+const void *local_d_fn(bool poisson, int depth) {
+    switch (depth) {
+        case 3: return poisson ? (const void *)k_persistent_local_d<true, 3> : (const void *)k_persistent_local_d<false, 3>;
+        case 4: return poisson ? (const void *)k_persistent_local_d<true, 4> : (const void *)k_persistent_local_d<false, 4>;
+        default: return poisson ? (const void *)k_persistent_local_d<true, 2> : (const void *)k_persistent_local_d<false, 2>;
+    }
+}
+
 bool g_cfg_ok[2][kNumStreamConfigs];
 
 cudaError_t prepare_kernels() {
@@ -1808,14 +1872,13 @@ cudaError_t prepare_kernels() {
         return cudaSuccess;
     };
     size_t local_max = (size_t)optin;
-    for (int which = 0; which < 6; ++which) {
-        const bool poisson = which & 1;
-        const void *fn = (which & 4) ? (poisson ? (const void *)k_persistent_local2<true>
-                                                : (const void *)k_persistent_local2<false>)
-                       : (which & 2) ? (poisson ? (const void *)k_persistent_local_rb<true>
-                                                : (const void *)k_persistent_local_rb<false>)
-                                     : (poisson ? (const void *)k_persistent_local<true>
-                                                : (const void *)k_persistent_local<false>);
+    const void *local_fns[] = {
+        (const void *)k_persistent_local<false>,    (const void *)k_persistent_local<true>,
+        (const void *)k_persistent_local_rb<false>, (const void *)k_persistent_local_rb<true>,
+        local_d_fn(false, 2), local_d_fn(true, 2),   local_d_fn(false, 3), local_d_fn(true, 3),
+        local_d_fn(false, 4), local_d_fn(true, 4)};
+    static_assert(kLocalMaxDepth == 4, "list every depth kernel");
+    for (const void *fn : local_fns) {
         int lim = 0;
         if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
@@ -1854,8 +1917,8 @@ bool stream_config_ok(int cfg, bool poisson) {
 }
 
 const void *kernel_persistent(int variant, bool poisson, int cfg) {
-    if (variant == kVariantLocal2)
-        return poisson ? (const void *)k_persistent_local2<true> : (const void *)k_persistent_local2<false>;
+    if (variant == kVariantLocalD)
+        return local_d_fn(poisson, cfg);
     if (variant == kVariantLocal)
         return poisson ? (const void *)k_persistent_local<true> : (const void *)k_persistent_local<false>;
     if (variant == kVariantStream) return poisson ? stream_fn<true>(cfg, true) : stream_fn<false>(cfg, true);
@@ -1888,7 +1951,7 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
     SweepParams arg = p;
     void *args[] = {&arg};
     const size_t smem = variant == kVariantLocal    ? local_smem_bytes(p.nx, p.local_rows, poisson)
-                        : variant == kVariantLocal2 ? local2_smem_bytes(p.nx, p.local_rows, poisson)
+                        : variant == kVariantLocalD ? local_d_smem_bytes(p.nx, p.local_rows, poisson, cfg)
                                                     : dyn_smem(variant, poisson, cfg);
     return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
                                        dim3(block_threads(variant)), args, smem, s);

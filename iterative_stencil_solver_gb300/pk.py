@@ -104,7 +104,8 @@ class pk_options(ctypes.Structure):
         ("ctas_per_sm", ctypes.c_int32),
         ("barrier_kind", ctypes.c_int32),
         ("stream_config", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 5),
+        ("local_depth", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 4),
     ]
 
 

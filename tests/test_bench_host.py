@@ -23,8 +23,12 @@ def test_two_sweep_shape_moves_8_bytes_per_two_cell_updates():
 
 
 def test_checks_between_pairs_force_single_sweeps():
-    # odd interval: every pass is one sweep; the final iterate gets a check-only pass
-    assert bench.passes_of(info(2, 6), 9, 1e-4, 3) == (9, 1)
+    # odd interval on a STREAM two-sweep shape: the run reports one sweep per pass
+    assert bench.passes_of(info(2, 6, 1), 9, 1e-4, 3) == (9, 1)
+    # a depth-2 LOCAL run with an odd interval: passes of 2, 1, 2, 1, ... never past a check
+    assert bench.passes_of(info(3, -1, 2), 9, 1e-4, 3) == (6, 1)
+    # depth 3 and an interval of 10: 3, 3, 3, 1 per interval
+    assert bench.passes_of(info(3, -1, 3), 20, 1e-4, 10) == (8, 1)
     # even interval: pairs, plus the check-only pass when n is a multiple
     assert bench.passes_of(info(2, 6), 2000, 1e-4, 10) == (1000, 1)
     b = bench.algorithmic_bytes(info(2, 6), 4096 * 4096, 2000, True, 1e-4, 10)

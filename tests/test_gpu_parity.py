@@ -220,7 +220,8 @@ def test_poisson_4096_residual_every_10(pk, path):
 def test_laplace_random_16384_full_field(pk):
     w = inputs.workload_laplace_random(16384, seed=3)
     got, info = run_pk(pk, w["u0"], None, 100)
-    assert info["sweeps_done"] == 100 and info["variant"] == 2
+    # the launch configuration bench.py times: the default plan's two-sweep STREAM shape
+    assert info["sweeps_done"] == 100 and info["variant"] == 2 and info["sweeps_per_pass"] == 2
     want, _ = oracle.jacobi_run(w["u0"], n=100, threads=THREADS)
     assert_same_bits(got, want)
 
@@ -367,7 +368,7 @@ def test_barrier_and_cg_sync_microbenchmarks(pk):
 
 @pytest.mark.parametrize("variant,nx,ny", [(1, 512, 512), (2, 3000, 200), (3, 3000, 200),
                                            (3, 512, 512)],
-                         ids=["direct", "stream", "local", "local-two-sweeps"])
+                         ids=["direct", "stream", "local", "local-multi-sweep"])
 def test_barrier_timeout_is_reported_not_hung(pk, variant, nx, ny):
     """Fault injection on the host's say-so: one CTA leaves without arriving;
     the others give up after the (short) limit and the call returns
@@ -609,13 +610,63 @@ def test_local_variant_bit_exact(pk, nx, ny, grid, poisson):
         assert info["variant"] == 3
         if grid:
             assert info["grid"] == min(grid, ny)
-        # two sweeps per exchange whenever every band has two rows and no
-        # check falls between a pair
-        two_ok = n >= 2 and (ce == 0 or ce % 2 == 0)
-        narrow = nx <= 512
-        assert info["sweeps_per_pass"] == (2 if two_ok and narrow and ny // info["grid"] >= 2 else 1)
+        # the plan's depth by row width, lowered until every band has that
+        # many rows (passes shorten where a check or the end would fall inside)
+        depth = 4 if nx <= 128 else 3 if nx <= 512 else 1
+        while depth > 1 and ny // info["grid"] < depth:
+            depth -= 1
+        assert info["sweeps_per_pass"] == depth
         assert_same_bits(got, want)
         check_info(info, oinfo)
+
+
+# Deeper temporal blocking on the LOCAL layout: D halo rows a side, passes
+# of up to D sweeps that never straddle a residual check.
+DEPTH_CASES = [(40, 60, 20, 3), (17, 9, 3, 3), (33, 40, 10, 4), (64, 64, 16, 4), (512, 512, 0, 3),
+               (512, 512, 0, 4), (300, 301, 0, 3), (8, 8, 2, 4), (600, 100, 25, 4)]
+
+
+@pytest.mark.parametrize("nx,ny,grid,depth", DEPTH_CASES, ids=["%dx%d-g%d-d%d" % c for c in DEPTH_CASES])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_local_depth_bit_exact(pk, nx, ny, grid, depth, poisson):
+    u0 = inputs.random_field(nx, ny, seed=700 + nx + ny + depth)
+    f = inputs.uniform_pm1(800 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, tol, ce in ((41, 0.0, 0), (33, 1e-30, 8), (12, 1e-30, 1), (25, 1e-30, 3), (26, 1e-30, 10),
+                       (30, 0.9, 2), (3, 0.0, 0), (1, 0.0, 0)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, tol, ce, variant=3, grid_override=grid, local_depth=depth)
+        assert info["variant"] == 3
+        if grid:
+            assert info["grid"] == grid
+        # every band has at least `depth` rows in these cases
+        assert ny // info["grid"] >= depth and info["sweeps_per_pass"] == depth
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+def test_local_depth_lowered_when_bands_are_thin(pk):
+    """Bands of two rows cannot feed three halo rows: the plan lowers the depth."""
+    u0 = inputs.random_field(64, 64, seed=9)
+    got, info = run_pk(pk, u0, None, 20, variant=3, grid_override=32, local_depth=4)
+    assert info["sweeps_per_pass"] == 2
+    want, _ = oracle.jacobi_run(u0, n=20)
+    assert_same_bits(got, want)
+
+
+def test_local_depth_timeout_is_reported_not_hung(pk):
+    u0 = inputs.random_field(512, 512, seed=31)
+    opt = pk.pk_options_default(variant=3, local_depth=4, barrier_timeout_s=0.2,
+                                debug_skip_arrival_cta=1, debug_skip_arrival_at=5)
+    ctx = pk.pk_create(512, 512, u0, None, opt)
+    try:
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 50)
+        assert e.value.code == pk.PK_ETIMEDOUT
+    finally:
+        pk.pk_destroy(ctx)
+    want, _ = oracle.jacobi_run(u0, n=9)
+    got, _ = run_pk(pk, u0, None, 9, variant=3, local_depth=4)
+    assert_same_bits(got, want)
 
 
 @pytest.mark.parametrize("nx,ny", [(512, 512), (64, 64), (130, 7)], ids=["512x512", "64x64", "130x7"])
