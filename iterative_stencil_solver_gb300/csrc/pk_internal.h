@@ -187,6 +187,15 @@ inline size_t local_d_halo_words(int nx, int depth) { return (size_t)depth * loc
 // Configurations whose shared memory does not fit are left unset and
 // reported unusable by stream_config_ok.
 cudaError_t prepare_kernels();
+
+// Kernel entry points of the other translation units, as launchable
+// pointers: the STREAM kernels (pk_stream.cu; persistent or per-launch form
+// of shape cfg) and the LOCAL kernels (pk_local.cu; depth 2..kLocalMaxDepth
+// for local_d_kernel).
+const void *stream_kernel(bool poisson, int cfg, bool persistent);
+const void *local_kernel(bool poisson);
+const void *local_d_kernel(bool poisson, int depth);
+const void *local_rb_kernel(bool poisson);
 bool stream_config_ok(int cfg, bool poisson);
 extern size_t g_local_smem_max;   // LOCAL: opt-in shared memory per CTA
 
