@@ -58,13 +58,13 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "141f7985ac75ec2c", "stream_config": 8,
-           "bytes_per_launch": 53.99e9 + 53.67e9}
+TRAFFIC = {"kernel_sha": "8b108fe0c21ff37d", "stream_config": 11,
+           "bytes_per_launch": 35.58e9 + 36.50e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
 SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1), 5: (2, 16, 1),
-          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2)}
+          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3)}
 
 
 def shape_label(info, poisson):
@@ -421,7 +421,7 @@ def latency_extras(pk):
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
     for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 8),
-                      ("two_sweeps_per_pass_8_deep_ring", 6)):
+                      ("three_sweeps_per_pass", 11)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):
@@ -434,7 +434,8 @@ def latency_extras(pk):
                             algorithmic_bytes(runs[0], 16384 * 16384, 100, False, 0, 0) / 100}
         finally:
             pk.pk_destroy(ctx)
-    tb["speedup"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
+    tb["speedup_two"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
+    tb["speedup_three"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["three_sweeps_per_pass"]["us_per_sweep"]
     out["temporal_blocking_16384_100sweeps"] = tb
     # Barrier spin: the headline kernel (one barrier per two-sweep pass) and
     # the barrier-per-sweep DIRECT kernel on the L2-resident 512^2 grid.

@@ -100,8 +100,9 @@ typedef struct {
                               index); -1 for the other variants */
     int32_t sweeps_per_pass; /* the most sweeps a pass advanced (temporal blocking): a pass
                                 takes that many, or fewer where n ends or a residual check
-                                would fall inside it.  STREAM two-sweep shapes: 2 (1 when
-                                check_every is odd); LOCAL: the plan's local_depth; else 1 */
+                                would fall inside it.  STREAM: the shape's sweeps per pass;
+                                LOCAL: the plan's local_depth; else 1 (and 1 when n < 2 or
+                                PK_FLAG_ONE_SWEEP_PER_PASS is set) */
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
 } pk_run_info;
@@ -133,20 +134,21 @@ typedef struct {
     uint32_t flags;                   /* PK_FLAG_* (default PK_FLAG_ALTERNATE_DIRECTION) */
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
-    int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs
-                                         that can take two sweeps per pass (n >= 2 and checks
-                                         off or check_every even) shape 8 (Laplace), 7
-                                         (Poisson, nx >= 8192) or 6 (Poisson); shape 3 for
-                                         the rest and for the per-launch and graph paths
+    int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs of
+                                         two or more sweeps shape 11 (Laplace), 7 (Poisson,
+                                         nx >= 8192) or 6 (Poisson); shape 3 for the rest and
+                                         for the per-launch and graph paths
                                          (pk_run_info.stream_config says which ran).  Index into
                                          {float4 groups per thread, TMA ring depth, sweeps
                                          per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}
                                          4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {1,16,2}
-                                         9 {2,16,2}; a strip is 1024 x groups columns wide.
-                                         Two sweeps per pass keep U_{k+1} on chip (temporal
-                                         blocking) whenever two sweeps are due and checks
-                                         are off or check_every is even; results are the
-                                         same bits.  A shape whose ring does not fit in
+                                         9 {2,16,2} 10 {1,16,3} 11 {1,8,3}; a strip is 1024 x
+                                         groups columns wide (896 x groups for 10 and 11,
+                                         which run seven consumer warps).  A shape of D sweeps per pass
+                                         keeps U_{k+1} .. U_{k+D-1} on chip (temporal
+                                         blocking); a pass takes up to D sweeps, never past
+                                         the end or a residual check; results are the same
+                                         bits.  A shape whose ring does not fit in
                                          shared memory is refused with PK_EINVAL. */
     int32_t local_depth;              /* LOCAL: sweeps per neighbour exchange, 1..4 (temporal
                                          blocking with that many halo rows a side); 0 = by

@@ -183,7 +183,7 @@ struct BarrierCtl {
     uint64_t timeout_ns;
     int skip_cta;       // -1 = off
     int skip_at;        // barrier index at which skip_cta leaves
-    int index;          // barriers completed by this CTA
+    int index;          // barriers completed by this CTA (kept by thread 0)
     unsigned base;      // kBarrierCounter: count at launch
     unsigned gen;       // kBarrierGeneration: current generation (thread 0)
     int profile;        // accumulate wait time in spin_ns
@@ -254,10 +254,10 @@ __device__ __forceinline__ bool grid_barrier(BarrierCtl &ctl) {
             ctl.gen += 1u;
         }
         if (ctl.profile) ctl.spin_ns += globaltimer_ns() - t_in;
+        ++ctl.index;
         s_ok = ok;
     }
     __syncthreads();
-    ++ctl.index;
     return s_ok != 0;
 }
 

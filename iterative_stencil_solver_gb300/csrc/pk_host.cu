@@ -228,12 +228,14 @@ long long stream_rows(const pk_ctx *ctx, int cfg) {
 long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_cfg); }
 
 constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
-// Two-sweep shape for persistent runs, from measurements on GB300: Laplace
-// {1 float4/thread, 16-deep ring} (2 CTAs/SM); Poisson, whose ring slot also
-// holds the source row, {2, 8} (1 CTA/SM) from 8192 columns on and {1, 8}
-// (2 CTAs/SM) below.
-int default_two_sweep_shape(bool poisson, int nx) {
-    if (!poisson) return 8;
+// Multi-sweep shape for persistent runs, from measurements on GB300
+// (16384^2 and 8192^2): Laplace takes three sweeps per pass, {1 float4/
+// thread, 8-deep ring, 224 consumers} (145.6 us/sweep against 163.3 for the
+// best two-sweep shape).  Poisson, whose ring slots also carry the source
+// row, keeps two: {2, 8} (1 CTA/SM) from 8192 columns on, {1, 8} (2 CTAs/SM)
+// below; its three-sweep shapes ran 1.4x slower (too few rows in flight).
+int default_multi_sweep_shape(bool poisson, int nx) {
+    if (!poisson) return 11;
     return nx >= 8192 ? 7 : 6;
 }
 
@@ -348,11 +350,11 @@ int plan(pk_ctx *ctx) {
     // the two-sweep shape (same bits, half the HBM traffic per sweep).
     ctx->stream_cfg2 = -1;
     ctx->grid2 = 0;
-    const int shape2 = default_two_sweep_shape(ctx->poisson, ctx->nx);
+    const int shape2 = default_multi_sweep_shape(ctx->poisson, ctx->nx);
     if (v == kVariantStream && ctx->opt.stream_config < 0 && stream_config_ok(shape2, ctx->poisson)) {
         int per_sm2 = 0;
         const int cap2 = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, shape2),
-                                       block_threads(v), dyn_smem(v, ctx->poisson, shape2), &per_sm2);
+                                       block_threads(v, shape2), dyn_smem(v, ctx->poisson, shape2), &per_sm2);
         if (cap2 < 0) return PK_ECUDA;
         if (cap2 > 0) {
             long long need2 = stream_rows(ctx, shape2);
@@ -389,7 +391,7 @@ int plan(pk_ctx *ctx) {
     } else {
         int per_sm = 0;
         cap = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, ctx->stream_cfg),
-                            block_threads(v), dyn_smem(v, ctx->poisson, ctx->stream_cfg), &per_sm);
+                            block_threads(v, ctx->stream_cfg), dyn_smem(v, ctx->poisson, ctx->stream_cfg), &per_sm);
         if (cap < 0) return PK_ECUDA;
         if (cap == 0) return fail(ctx, PK_ENORESIDENT, "sweep kernel does not fit on an SM");
         long long need = v == kVariantStream ? stream_rows(ctx)
@@ -733,17 +735,16 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.check_every = check_every;
     if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
         PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0, local_halo_bytes(ctx), ctx->stream));
-    // Two sweeps per pass pay off when passes can advance two sweeps: at
-    // least two sweeps, and no check falling between the two.
-    const bool checks = tol > 0.f && check_every > 0;
-    const bool two_ok = n >= 2 && (!checks || check_every % 2 == 0) &&
-                        !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
+    // Several sweeps per pass pay off whenever a run has two or more: the
+    // kernels shorten a pass where the end or a residual check would fall
+    // inside it.
+    const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
     int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
-    if (ctx->stream_cfg2 >= 0 && two_ok) {
+    if (ctx->stream_cfg2 >= 0 && multi_ok) {
         shape = ctx->stream_cfg2;
         grid = ctx->grid2;
     }
-    if (ctx->variant == kVariantStream && stream_depth(shape) == 2 && two_ok) depth = 2;
+    if (ctx->variant == kVariantStream && multi_ok) depth = stream_depth(shape);
     if (ctx->variant == kVariantLocal && ctx->local_depth >= 2 &&
         !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS)) {
         // passes take up to local_depth sweeps, never past a check
@@ -809,7 +810,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
         cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, grid, p, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "sweep launch");
         if (check) {
-            e = launch_finalize(launch_variant(ctx), grid, p, &ctx->scratch->res, ctx->stream);
+            e = launch_finalize(launch_variant(ctx), ctx->stream_cfg, grid, p, &ctx->scratch->res, ctx->stream);
             if (e != cudaSuccess) return cuda_fail(ctx, e, "residual launch");
             PK_TRY(ctx, cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
                                         cudaMemcpyDeviceToHost, ctx->stream));
@@ -862,7 +863,7 @@ int graph_for(pk_ctx *ctx, bool check, long long plain, int cur, int kpar, cudaG
         p.pass_parity = 0;
         p.pass_k = k;
         e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, ctx->launch_grid, p, ctx->stream);
-        if (e == cudaSuccess) e = launch_finalize(launch_variant(ctx), ctx->launch_grid, p, &ctx->scratch->res, ctx->stream);
+        if (e == cudaSuccess) e = launch_finalize(launch_variant(ctx), ctx->stream_cfg, ctx->launch_grid, p, &ctx->scratch->res, ctx->stream);
         if (e == cudaSuccess)
             e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
                                 cudaMemcpyDeviceToHost, ctx->stream);
@@ -922,7 +923,7 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
                 cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg,
                                             ctx->launch_grid, p, ctx->stream);
                 if (e == cudaSuccess)
-                    e = launch_finalize(launch_variant(ctx), ctx->launch_grid, p, &ctx->scratch->res,
+                    e = launch_finalize(launch_variant(ctx), ctx->stream_cfg, ctx->launch_grid, p, &ctx->scratch->res,
                                         ctx->stream);
                 if (e == cudaSuccess)
                     e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
@@ -1050,7 +1051,7 @@ int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, p
             p.pass_parity = 0;
             e = launch_once_rb(ctx->poisson, ctx->rb_grid, p, ctx->stream);
             if (e == cudaSuccess)
-                e = launch_finalize(kVariantDirect, ctx->rb_grid, p, &ctx->scratch->res, ctx->stream);
+                e = launch_finalize(kVariantDirect, 0, ctx->rb_grid, p, &ctx->scratch->res, ctx->stream);
             if (e == cudaSuccess)
                 e = cudaMemcpyAsync(ctx->h_res, &ctx->scratch->res, sizeof(ResidualOut),
                                     cudaMemcpyDeviceToHost, ctx->stream);

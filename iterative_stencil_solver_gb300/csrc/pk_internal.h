@@ -123,35 +123,40 @@ struct TaskParams {
 
 // ---- sizes -----------------------------------------------------------------
 constexpr int kDirectThreads = 256;
-constexpr int kConsumers = 256;                 // STREAM consumer threads
-constexpr int kStreamThreads = kConsumers + 32; // + one producer warp
 constexpr int kStressWords = 32;
 
 // STREAM configurations: float4 groups per consumer thread per row (the
-// strip is 4 * qpt * kConsumers columns wide), TMA ring depth, and sweeps
-// per pass (2 = temporal blocking: U_{k+1} stays on chip, U_{k+2} is
-// written).
+// strip is 4 * qpt * consumers columns wide), TMA ring depth, sweeps per
+// pass (2 and 3 = temporal blocking: the intermediate iterates stay on
+// chip), CTAs per SM the register budget is sized for, and consumer threads
+// (a CTA adds one producer warp).  Seven consumer warps instead of eight
+// leave four warps per SM sub-partition at two CTAs per SM, which raises the
+// register cap from 96 to 128.
 struct StreamConfig {
     int qpt;
     int stages;
     int depth;
-    int min_ctas;  // CTAs per SM the register budget is sized for
+    int min_ctas;
+    int consumers;
 };
-constexpr int kNumStreamConfigs = 10;
+constexpr int kNumStreamConfigs = 12;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
-    {1, 8, 1, 1}, {1, 16, 1, 1}, {2, 8, 1, 1}, {4, 4, 1, 1}, {4, 8, 1, 1}, {2, 16, 1, 1},
-    {1, 8, 2, 2}, {2, 8, 2, 1}, {1, 16, 2, 2}, {2, 16, 2, 1}};
+    {1, 8, 1, 1, 256},  {1, 16, 1, 1, 256}, {2, 8, 1, 1, 256},  {4, 4, 1, 1, 256},
+    {4, 8, 1, 1, 256},  {2, 16, 1, 1, 256}, {1, 8, 2, 2, 256},  {2, 8, 2, 1, 256},
+    {1, 16, 2, 2, 256}, {2, 16, 2, 1, 256}, {1, 16, 3, 2, 224}, {1, 8, 3, 2, 224}};
 
-inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kConsumers; }
+inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kStreamConfigs[cfg].consumers; }
+inline int stream_threads(int cfg) { return kStreamConfigs[cfg].consumers + 32; }
 inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 
 // A ring slot: the U row segment (4 halo floats each side) and, for
-// Poisson, the g row segment with a 4-float margin each side.  Two-sweep
-// shapes add two shared U_{k+1} rows laid out like the U part of a slot.
+// Poisson, the g row segment with a 4-float margin each side.  A shape of
+// D sweeps per pass adds two shared rows for each of U_{k+1} .. U_{k+D-1},
+// laid out like the U part of a slot.
 inline size_t stream_smem_bytes(int cfg, bool poisson) {
     const int tw = stream_tw(cfg);
     const size_t slot = (size_t)(tw + 8 + (poisson ? tw + 8 : 0)) * sizeof(float);
-    const size_t qrows = stream_depth(cfg) == 2 ? 2 * (size_t)(tw + 8) * sizeof(float) : 0;
+    const size_t qrows = 2 * (size_t)(stream_depth(cfg) - 1) * (size_t)(tw + 8) * sizeof(float);
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 
@@ -206,14 +211,19 @@ const void *kernel_once(int variant, bool poisson, int cfg);
 const void *kernel_task(bool poisson);
 const void *kernel_barrier_only(int kind);
 const void *kernel_stress();
-int block_threads(int variant);
+// Threads per CTA of a sweep kernel (STREAM: of shape cfg; the default is
+// the single-sweep shape 3).
+int block_threads(int variant, int cfg = 3);
 size_t dyn_smem(int variant, bool poisson, int cfg);
 
 cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                               cudaStream_t s);
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                         cudaStream_t s);
-cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
+// Reduces the partials of a per-launch check pass with the thread count of
+// the kernel that wrote them (variant, shape cfg), so the order is the
+// persistent kernel's.
+cudaError_t launch_finalize(int variant, int cfg, int grid, const SweepParams &p, ResidualOut *out,
                             cudaStream_t s);
 // Red-black Gauss-Seidel (DIRECT-style passes, in place on p.u[p.cur]).
 const void *kernel_persistent_rb(bool poisson);

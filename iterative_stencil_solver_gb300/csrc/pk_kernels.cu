@@ -83,7 +83,7 @@ template <bool POISSON>
 __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParams p) {
     const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
     const unsigned stride = gridDim.x * blockDim.x;
-    persistent_loop<1>(p, [&](const float *src, float *dst, bool check, bool store, bool,
+    persistent_loop<1>(p, [&](const float *src, float *dst, bool check, bool store, int,
                               long long, double &s2, float &rmax) {
         pass_direct_any<POISSON>(p, src, dst, check, store, first, stride, s2, rmax);
     });
@@ -684,7 +684,9 @@ const void *kernel_barrier_only(int kind) {
 
 const void *kernel_stress() { return (const void *)k_stress; }
 
-int block_threads(int variant) { return variant == kVariantStream ? kStreamThreads : kDirectThreads; }
+int block_threads(int variant, int cfg) {
+    return variant == kVariantStream ? stream_threads(cfg) : kDirectThreads;
+}
 
 size_t dyn_smem(int variant, bool poisson, int cfg) {
     return variant == kVariantStream ? stream_smem_bytes(cfg, poisson) : 0;
@@ -698,7 +700,7 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
                         : variant == kVariantLocalD ? local_d_smem_bytes(p.nx, p.local_rows, poisson, cfg)
                                                     : dyn_smem(variant, poisson, cfg);
     return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
-                                       dim3(block_threads(variant)), args, smem, s);
+                                       dim3(block_threads(variant, cfg)), args, smem, s);
 }
 
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
@@ -706,7 +708,7 @@ cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const Swee
     SweepParams arg = p;
     void *args[] = {&arg};
     return cudaLaunchKernel(kernel_once(variant, poisson, cfg), dim3(grid),
-                            dim3(block_threads(variant)), args, dyn_smem(variant, poisson, cfg), s);
+                            dim3(block_threads(variant, cfg)), args, dyn_smem(variant, poisson, cfg), s);
 }
 
 cudaError_t launch_persistent_rb(bool poisson, int grid, const SweepParams &p, cudaStream_t s) {
@@ -738,9 +740,9 @@ const void *kernel_persistent_rb(bool poisson) {
     return poisson ? (const void *)k_persistent_rb<true> : (const void *)k_persistent_rb<false>;
 }
 
-cudaError_t launch_finalize(int variant, int grid, const SweepParams &p, ResidualOut *out,
+cudaError_t launch_finalize(int variant, int cfg, int grid, const SweepParams &p, ResidualOut *out,
                             cudaStream_t s) {
-    k_finalize<<<1, block_threads(variant), 0, s>>>(p, grid, out);
+    k_finalize<<<1, block_threads(variant, cfg), 0, s>>>(p, grid, out);
     return cudaGetLastError();
 }
 

@@ -40,28 +40,44 @@ __device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
     return ctl;
 }
 
-// MAXD = 2: the pass may advance two sweeps at once (temporal blocking)
-// whenever two more sweeps are due and no check can fall between them
-// (checks are off, or check_every is even and the pass starts on a check
-// boundary's parity); otherwise it advances one.
+// MAXD > 1: a pass may advance up to MAXD sweeps at once (temporal
+// blocking), as many as are due before the end or the next residual check.
 template <int MAXD, class PassFn>
 __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
-    BarrierCtl ctl = make_ctl(p);
+    // Loop state that only thread 0 uses (the barrier's bookkeeping) or that
+    // changes only on check sweeps (the residual history) lives in shared
+    // memory: the pass keeps the registers, which are what bounds the
+    // STREAM kernels' occupancy.
+    __shared__ BarrierCtl s_ctl;
+    __shared__ double s_res0, s_res_last;
+    __shared__ float s_rmax_last;
+    if (threadIdx.x == 0) {
+        s_ctl = make_ctl(p);
+        s_res0 = s_res_last = 0.0;
+        s_rmax_last = 0.f;
+    }
+    __syncthreads();
     const bool checks = p.tol > 0.f && p.check_every > 0;
     int cur = p.cur;
     long long k = 0;
-    double res0 = 0.0, res_last = 0.0;
-    float rmax_last = 0.f;
     int n_checks = 0;
     for (;;) {
         const bool check = checks && (k % p.check_every) == 0;
         if (k == p.n && !check) break;
         const bool store = k < p.n;
-        const bool two = MAXD >= 2 && store && k + 2 <= p.n && (!checks || (p.check_every % 2) == 0) &&
-                         !p.one_sweep;
+        // sweeps this pass: up to MAXD, none of them past the end or a check
+        int dp = 1;
+        if (MAXD >= 2 && store && !p.one_sweep) {
+            long long m = p.n - k;
+            if (checks) {
+                const long long to_check = p.check_every - (k % p.check_every);
+                if (to_check < m) m = to_check;
+            }
+            dp = m < MAXD ? (int)m : MAXD;
+        }
         double s2 = 0.0;
         float rmax = 0.f;
-        pass(p.u[cur], p.u[cur ^ 1], check, store, two, k, s2, rmax);
+        pass(p.u[cur], p.u[cur ^ 1], check, store, dp, k, s2, rmax);
         Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
         if (check) {
             block_reduce(s2, rmax);
@@ -73,36 +89,40 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
                 parts[blockIdx.x] = pp;
             }
         }
-        if (!grid_barrier(ctl)) return;  // aborting: the host reads the error
+        if (!grid_barrier(s_ctl)) return;  // aborting: the host reads the error
         if (check) {
             double S2;
             float RM;
             reduce_partials(parts, (int)gridDim.x, S2, RM);
             const double res = sqrt(S2);
             ++n_checks;
-            res_last = res;
-            rmax_last = RM;
-            if (k == 0)
-                res0 = res;
-            else if (res < (double)p.tol * res0)
+            if (threadIdx.x == 0) {
+                s_res_last = res;
+                s_rmax_last = RM;
+            }
+            // s_res0 was written at the first check, barriers ago
+            if (k == 0) {
+                if (threadIdx.x == 0) s_res0 = res;
+            } else if (res < (double)p.tol * s_res0) {
                 break;
+            }
         }
         if (k == p.n) break;
         cur ^= 1;
-        k += two ? 2 : 1;
+        k += dp;
     }
-    if (threadIdx.x == 0 && p.profile) p.spin_ns[blockIdx.x] = ctl.spin_ns;
+    if (threadIdx.x == 0 && p.profile) p.spin_ns[blockIdx.x] = s_ctl.spin_ns;
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         DeviceInfo *d = p.info;
         d->sweeps_done = k;
-        d->res0 = res0;
-        d->res_last = res_last;
-        d->rmax_last = rmax_last;
+        d->res0 = s_res0;
+        d->res_last = s_res_last;
+        d->rmax_last = s_rmax_last;
         d->n_checks = n_checks;
         d->cur = cur;
         d->task_sweeps = 0;
-        d->barriers = ctl.index;
-        d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
+        d->barriers = s_ctl.index;
+        d->bar_count_end = p.bar_base + (unsigned)s_ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;
     }

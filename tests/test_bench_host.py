@@ -22,9 +22,11 @@ def test_two_sweep_shape_moves_8_bytes_per_two_cell_updates():
     assert bench.passes_of(info(2, 8), 7, 0.0, 0) == (4, 0)
 
 
-def test_checks_between_pairs_force_single_sweeps():
-    # odd interval on a STREAM two-sweep shape: the run reports one sweep per pass
-    assert bench.passes_of(info(2, 6, 1), 9, 1e-4, 3) == (9, 1)
+def test_passes_never_straddle_a_check():
+    # odd interval on a STREAM two-sweep shape: passes of 2 and 1 sweeps
+    assert bench.passes_of(info(2, 6), 9, 1e-4, 3) == (6, 1)
+    # a three-sweep shape with an interval of 10: 3, 3, 3, 1
+    assert bench.passes_of(info(2, 10), 20, 1e-4, 10) == (8, 1)
     # a depth-2 LOCAL run with an odd interval: passes of 2, 1, 2, 1, ... never past a check
     assert bench.passes_of(info(3, -1, 2), 9, 1e-4, 3) == (6, 1)
     # depth 3 and an interval of 10: 3, 3, 3, 1 per interval

@@ -112,10 +112,13 @@ def test_flags_problem_grid_and_alternating_direction(pk, variant):
 def test_persistent_and_launch_residuals_identical(pk):
     nx, ny = 700, 333
     u0 = inputs.random_field(nx, ny, seed=5)
-    for variant in (1, 2):
-        _, a = run_pk(pk, u0, None, 30, 1e-30, 5, path="persistent", variant=variant)
+    # the same shape on every path (the per-CTA partials follow the shape);
+    # the persistent default would take a multi-sweep STREAM shape
+    for variant, shape in ((1, -1), (2, 3)):
+        _, a = run_pk(pk, u0, None, 30, 1e-30, 5, path="persistent", variant=variant,
+                      stream_config=shape)
         for path in ("launch", "graph"):
-            _, b = run_pk(pk, u0, None, 30, 1e-30, 5, path=path, variant=variant)
+            _, b = run_pk(pk, u0, None, 30, 1e-30, 5, path=path, variant=variant, stream_config=shape)
             assert a["grid"] == b["grid"]
             assert a["res0"] == b["res0"] and a["res_last"] == b["res_last"]
             assert a["res_max_last"] == b["res_max_last"]
@@ -221,7 +224,7 @@ def test_laplace_random_16384_full_field(pk):
     w = inputs.workload_laplace_random(16384, seed=3)
     got, info = run_pk(pk, w["u0"], None, 100)
     # the launch configuration bench.py times: the default plan's two-sweep STREAM shape
-    assert info["sweeps_done"] == 100 and info["variant"] == 2 and info["sweeps_per_pass"] == 2
+    assert info["sweeps_done"] == 100 and info["variant"] == 2 and info["sweeps_per_pass"] == 3
     want, _ = oracle.jacobi_run(w["u0"], n=100, threads=THREADS)
     assert_same_bits(got, want)
 
@@ -417,7 +420,7 @@ CFG_SIZES = [(1, 1), (5, 3), (300, 301), (2053, 5), (4100, 7), (8200, 3)]
 CFG_RUNS = [(6, 4), (9, 0), (7, 3), (10, 2)]
 
 
-@pytest.mark.parametrize("cfg", range(10))
+@pytest.mark.parametrize("cfg", range(12))
 @pytest.mark.parametrize("nx,ny", CFG_SIZES, ids=["%dx%d" % s for s in CFG_SIZES])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
@@ -441,15 +444,15 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
 # The default STREAM plan: persistent runs whose passes can take two sweeps
 # use the two-sweep shape; the others, and the per-launch path, keep the
 # single-sweep shape.  Either way the bits are those of single sweeps.
-TWO = "two-sweep"
+MULTI = "multi-sweep"
 DEFAULT_SHAPE_RUNS = [
     # (n, tol, check_every, expected shape)
-    (8, 0.0, 0, TWO),
-    (9, 0.0, 0, TWO),     # ends with one single sweep in the two-sweep shape
-    (10, 1e-30, 4, TWO),
-    (9, 1e-30, 3, 3),     # an odd interval puts checks between sweep pairs
+    (8, 0.0, 0, MULTI),
+    (9, 0.0, 0, MULTI),   # the last pass is shorter
+    (10, 1e-30, 4, MULTI),
+    (9, 1e-30, 3, MULTI),  # passes never straddle a check
     (1, 0.0, 0, 3),
-    (40, 0.5, 2, TWO),    # early exit on a check at the start of a pass
+    (40, 0.5, 2, MULTI),    # early exit on a check at the start of a pass
 ]
 
 
@@ -459,10 +462,10 @@ DEFAULT_SHAPE_RUNS = [
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    # Laplace: {1 float4/thread, 16-deep ring}; Poisson: {2, 8} from 8192 columns, else {1, 8}
-    two = 8 if not poisson else (7 if nx >= 8192 else 6)
+    # Laplace: three sweeps per pass, shape 11; Poisson: {2, 8} from 8192 columns, else {1, 8}
+    multi = 11 if not poisson else (7 if nx >= 8192 else 6)
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
-        shape = two if shape == TWO else shape
+        shape = multi if shape == MULTI else shape
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, path="persistent", variant=2)
         assert info["variant"] == 2 and info["stream_config"] == shape, (n, tol, ce, info)
