@@ -256,16 +256,18 @@ def reference_arm(args, world, rank):
     w = make_workload(args.workload)
     import oracle  # noqa: F401
     rows = min(w["ny"], max(1, int(4e7 // w["nx"])))  # ~4e7 cells per sweep sample
-    values = []
+    values, secs = [], []
     for step in range(args.warmup + args.steps):
-        v, desc, _ = oracle_sample(w, target_s=1.0, max_rows=rows)
+        v, desc, dt = oracle_sample(w, target_s=1.0, max_rows=rows)
         if step >= args.warmup:
             values.append(v)
+            secs.append(dt)
     value = statistics.median(values)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+        # a step here is one bounded sample (see cpu_baseline.sample)
+        "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
