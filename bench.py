@@ -64,7 +64,8 @@ TRAFFIC = {"kernel_sha": "8b108fe0c21ff37d", "stream_config": 11,
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
 SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1), 5: (2, 16, 1),
-          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3)}
+          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3), 12: (1, 16, 3),
+          13: (1, 16, 3), 14: (1, 16, 3)}
 
 
 def shape_label(info, poisson):

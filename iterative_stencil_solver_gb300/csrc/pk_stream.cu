@@ -669,10 +669,16 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     }
     // Steady rows 6 .. nin-3.
     const int steady = c.nin - 8 > 0 ? c.nin - 8 : 0;
+    // Full-width strips take the unrolled steady loop.  A ragged last strip
+    // takes its own unrolled copy for Laplace: the CTAs holding its rows would
+    // otherwise set the pace of every pass.  For Poisson the second copy
+    // makes the kernel too large for the compiler to keep the row windows in
+    // registers (they went to the stack, 1.45x slower), so there the ragged
+    // rows run through the rolled generic step below.
     if (cols == C::TW)
         seg3_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
                                              ry, s2, rmax);
-    else
+    else if constexpr (!POISSON)
         seg3_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
                                               rb, ry, s2, rmax);
     // The last input rows: stages 1 and 2 reach beyond the band (maybe the ring).
@@ -834,12 +840,15 @@ const void *stream_fn(int cfg, bool persistent) {
         PK_CFG_CASE(9)
         PK_CFG_CASE(10)
         PK_CFG_CASE(11)
+        PK_CFG_CASE(12)
+        PK_CFG_CASE(13)
+        PK_CFG_CASE(14)
 #undef PK_CFG_CASE
         default:
             return nullptr;
     }
 }
-static_assert(kNumStreamConfigs == 12, "update stream_fn");
+static_assert(kNumStreamConfigs == 15, "update stream_fn");
 
 }  // namespace
 
