@@ -58,14 +58,13 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "8b108fe0c21ff37d", "stream_config": 11,
+TRAFFIC = {"kernel_sha": "f51ce6685179d588", "stream_config": 11,
            "bytes_per_launch": 35.58e9 + 36.50e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
 SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1), 5: (2, 16, 1),
-          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3), 12: (1, 16, 3),
-          13: (1, 16, 3), 14: (1, 16, 3)}
+          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3), 12: (1, 16, 3)}
 
 
 def shape_label(info, poisson):
@@ -104,7 +103,7 @@ def algorithmic_bytes(info, cells, sweeps, poisson, tol, check_every):
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for name in ("pk_stream.cu", "pk_sweep.cuh", "pk_device.cuh", "pk_internal.h"):
+    for name in ("pk_stream.cuh", "pk_stream_d3.cu", "pk_sweep.cuh", "pk_device.cuh", "pk_internal.h"):
         with open(os.path.join(ROOT, "iterative_stencil_solver_gb300", "csrc", name), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

@@ -135,17 +135,16 @@ typedef struct {
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
     int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs of
-                                         two or more sweeps shape 11 (Laplace), 13 (Poisson,
+                                         two or more sweeps shape 11 (Laplace), 12 (Poisson,
                                          nx >= 8192) or 6 (Poisson); shape 3 for the rest and
                                          for the per-launch and graph paths
                                          (pk_run_info.stream_config says which ran).  Index into
                                          {float4 groups per thread, TMA ring depth, sweeps
                                          per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}
                                          4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {1,16,2}
-                                         9 {2,16,2} 10 {1,16,3} 11 {1,8,3} 12 {1,16,3} 13 {1,16,3}
-                                         14 {1,16,3}; a strip is 1024 x groups columns wide
-                                         (10, 11: 896, seven consumer warps; 12: 768, six; 14:
-                                         640, five; 13 runs one CTA per SM).  A shape of D sweeps per pass
+                                         9 {2,16,2} 10 {1,16,3} 11 {1,8,3} 12 {1,16,3}; a strip
+                                         is 1024 x groups columns wide (896 for 10 and 11, which
+                                         run seven consumer warps; 12 runs one CTA per SM).  A shape of D sweeps per pass
                                          keeps U_{k+1} .. U_{k+D-1} on chip (temporal
                                          blocking); a pass takes up to D sweeps, never past
                                          the end or a residual check; results are the same

@@ -15,8 +15,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpk.so")
-SOURCES = ["pk_stream.cu", "pk_local.cu", "pk_kernels.cu", "pk_host.cu", "pk_noalloc.cu"]
-HEADERS = ["pk_device.cuh", "pk_internal.h", "pk_sweep.cuh"]
+SOURCES = ["pk_stream_d3.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
+           "pk_host.cu", "pk_noalloc.cu", "pk_stream.cu"]
+HEADERS = ["pk_device.cuh", "pk_internal.h", "pk_sweep.cuh", "pk_stream.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-fmad=false", "-Xcompiler", "-fPIC",

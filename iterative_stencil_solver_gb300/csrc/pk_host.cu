@@ -237,7 +237,7 @@ constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 
 // with {1, 8} below, where the passes are short (4096^2: 24.4 against 25.0).
 int default_multi_sweep_shape(bool poisson, int nx) {
     if (!poisson) return 11;
-    return nx >= 8192 ? 13 : 6;
+    return nx >= 8192 ? 12 : 6;
 }
 
 int ensure_partials(pk_ctx *ctx, int grid) {

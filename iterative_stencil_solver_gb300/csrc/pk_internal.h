@@ -139,12 +139,12 @@ struct StreamConfig {
     int min_ctas;
     int consumers;
 };
-constexpr int kNumStreamConfigs = 15;
+constexpr int kNumStreamConfigs = 13;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
     {1, 8, 1, 1, 256},  {1, 16, 1, 1, 256}, {2, 8, 1, 1, 256},  {4, 4, 1, 1, 256},
     {4, 8, 1, 1, 256},  {2, 16, 1, 1, 256}, {1, 8, 2, 2, 256},  {2, 8, 2, 1, 256},
     {1, 16, 2, 2, 256}, {2, 16, 2, 1, 256}, {1, 16, 3, 2, 224}, {1, 8, 3, 2, 224},
-    {1, 16, 3, 2, 192}, {1, 16, 3, 1, 256}, {1, 16, 3, 2, 160}};
+    {1, 16, 3, 1, 256}};
 
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kStreamConfigs[cfg].consumers; }
 inline int stream_threads(int cfg) { return kStreamConfigs[cfg].consumers + 32; }

@@ -1,859 +1,22 @@
-// pk_stream.cu -- the STREAM sweep kernels (large grids): TMA-staged row
-// segments, a register window per thread, one or two sweeps per pass.
-//
-// Sources (page title -- section):
-//   "Persistent Kernels: Bridging GPU-CPU Execution"
-//     -- "The problem (another PDE solver)": the 5-point update.
-//     -- "Cache-line aware tiling and iteration": contiguous row bands, each
-//        thread walking down its columns with a three-row live window.
-//     -- "Reflections": a wider halo, several steps per synchronisation
-//        (the two-sweep pass).
-//   "Grid-Wide Barriers and Persistent Work Queues" -- "The residency
-//     requirement", "What the barrier buys", "When a launch is the better
-//     barrier".
-#include "pk_sweep.cuh"
+// pk_stream.cu -- picks the translation unit that instantiates a STREAM
+// shape: shapes of one, two and three sweeps per pass are compiled apart
+// (pk_stream_d1.cu, _d2.cu, _d3.cu) so the build runs them in parallel.
+#include "pk_internal.h"
 
 namespace pk {
-namespace {
 
-// ===========================================================================
-// STREAM sweep ("Cache-line aware tiling and iteration", the N = 10001
-// variant, rebuilt around TMA): the domain is cut into strips of TW interior
-// columns; (strip, row) pairs are split evenly, in contiguous runs, over the
-// CTAs.  Each CTA walks its run row by row: one producer thread streams
-// every input row segment (with a 16-byte halo on each side) into a
-// STAGES-deep shared-memory ring with cp.async.bulk, and 256 consumer
-// threads keep a three-row window (previous, centre, next) in registers,
-// QPT float4 groups per thread, so each input row is read from HBM once and
-// from shared memory once.  Edge neighbours come from warp shuffles, and at
-// warp edges from the staged halo.
-template <int QPT, int STAGES, int DEPTH, int MINB, int CONS, bool POISSON>
-struct SCfg {
-    static constexpr int kCons = CONS;       // consumer threads
-    static constexpr int kThreads = CONS + 32;  // + the producer warp
-    static_assert(CONS % 32 == 0 && CONS >= 64, "whole consumer warps");
-    static constexpr int kQPT = QPT;
-    static constexpr int kStages = STAGES;
-    static constexpr int kDepth = DEPTH;
-    static constexpr int kMinBlocks = MINB;
-    static constexpr int TW = 4 * QPT * CONS;
-    static constexpr int SLOTU = TW + 8;
-    static constexpr int SLOT = SLOTU + (POISSON ? TW + 8 : 0);
-    static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
-    static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three sweeps per pass");
-};
-
-struct StreamState {
-    uint64_t *full;
-    uint64_t *empty;
-    float *slots;
-    unsigned L;     // ring position; producer and consumers advance it alike
-    bool broken;    // a pipeline wait expired: stop waiting, finish quickly
-};
-
-template <class C>
-__device__ __forceinline__ StreamState stream_setup(unsigned char *smem) {
-    StreamState st;
-    st.full = reinterpret_cast<uint64_t *>(smem);
-    st.empty = st.full + C::kStages;
-    st.slots = reinterpret_cast<float *>(smem + 256);
-    st.L = 0;
-    st.broken = false;
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < C::kStages; ++i) {
-            mbar_init(&st.full[i], 1);
-            mbar_init(&st.empty[i], C::kCons / 32);
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-    return st;
-}
-
-__device__ __forceinline__ float4 lds4(const float *p) {
-    return *reinterpret_cast<const float4 *>(p);
-}
-
-// Producer: input rows ja - D*dir .. jb + D*dir of strip columns
-// [col0, col0+cols), D = sweeps per pass; rows beyond the ring are clamped
-// to it (their products are never stored).  The g row (Poisson) comes with
-// every row that is a centre of the first stage: rows ja - (D-1)*dir ..
-// jb + (D-1)*dir inside 1..ny (the ring has no source).
-// Run by all 32 lanes of the producer warp, which stays converged: lane 0
-// waits and issues, every lane meets at __syncwarp each row, so the warp
-// reaches the CTA barriers that follow as one.
-template <class C, bool POISSON, int D>
-__device__ __forceinline__ void produce_segment(const SweepParams &p, const float *src, int ja,
-                                                int jb, int dir, int cols, long long col0,
-                                                StreamState &st) {
-    const unsigned lane = threadIdx.x & 31u;
-    const unsigned bytes_u = (unsigned)(((cols + 5 + 3) & ~3) * 4);
-    const bool first_strip = col0 == 0;
-    const bool last_strip = col0 + cols >= p.nx;
-    // g segment: D == 1 needs [col0, col0+cols); D >= 2 also the D-1
-    // columns beyond each strip edge that lie inside the interior (the
-    // 4-float margin).
-    const int gl = (D >= 2 && !first_strip) ? 4 : 0;
-    const int gr = (D >= 2 && !last_strip) ? 4 : 0;
-    const unsigned bytes_g = (unsigned)((((cols + 3) & ~3) + gl + gr) * 4);
-    const int nin = (dir > 0 ? jb - ja : ja - jb) + 1 + 2 * D;
-    int r = ja - D * dir;
-    for (int idx = 0; idx < nin; ++idx, r += dir) {
-        const unsigned slot = st.L & (C::kStages - 1);
-        const unsigned ph = (st.L / C::kStages) & 1u;
-        if (lane == 0u) {
-            if (!st.broken && !mbar_wait_bounded(&st.empty[slot], ph ^ 1u, p.timeout_ns, p.bar)) {
-                record_error(p.bar, kETimedOut, kSitePipeline);
-                st.broken = true;
-            }
-            const int rr = r < 0 ? 0 : (r > p.ny + 1 ? p.ny + 1 : r);
-            const bool gneed = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= p.ny;
-            float *dst_u = st.slots + slot * C::SLOT;
-            mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
-            tma_load_1d(dst_u, src + (long long)rr * p.pitch + col0, bytes_u, &st.full[slot]);
-            if (gneed)
-                tma_load_1d(dst_u + C::SLOTU + 4 - gl, p.g + (long long)(r - 1) * p.gpitch + col0 - gl,
-                            bytes_g, &st.full[slot]);
-        }
-        __syncwarp();
-        ++st.L;
-    }
-}
-
-// Consumers: output rows ja .. jb (in walking order) of the same strip.
-// Thread t owns float4 groups t + k * C::kCons, k < QPT, of the strip.
-template <class C, bool POISSON, bool CHECK, bool STORE>
-__device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst, int ja, int jb,
-                                                int dir, int cols, long long col0,
-                                                StreamState &st, double &s2, float &rmax) {
-    constexpr int Q = C::kQPT;
-    const int t = threadIdx.x;
-    const unsigned lane = t & 31;
-    int valid[Q];
-#pragma unroll
-    for (int k = 0; k < Q; ++k) valid[k] = max(0, min(4, cols - 4 * (t + k * C::kCons)));
-    const int nin = (dir > 0 ? jb - ja : ja - jb) + 3;
-    float4 prev[Q], cur[Q], curg[Q];
-    float curw[Q], cure[Q];
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        prev[k] = cur[k] = curg[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-        curw[k] = cure[k] = 0.f;
-    }
-    int r = ja - dir;
-    for (int idx = 0; idx < nin; ++idx, r += dir) {
-        const unsigned slot = st.L & (C::kStages - 1);
-        const unsigned ph = (st.L / C::kStages) & 1u;
-        if (!st.broken && !mbar_wait_bounded(&st.full[slot], ph, p.timeout_ns, p.bar)) {
-            record_error(p.bar, kETimedOut, kSitePipeline);
-            st.broken = true;
-        }
-        const float *su = st.slots + slot * C::SLOT;
-        float4 x[Q], xg[Q];
-        float xw[Q], xe[Q];
-        const bool gin = POISSON && idx >= 1 && idx <= nin - 2;
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = 4 * (t + k * C::kCons);
-            x[k] = lds4(su + 4 + o);
-            xw[k] = lane == 0u ? su[3 + o] : 0.f;
-            xe[k] = lane == 31u ? su[8 + o] : 0.f;
-            xg[k] = gin ? lds4(su + C::SLOTU + 4 + o) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // Release the slot only once this thread's reads of it are complete
-        // with respect to the async proxy that will refill it.
-        fence_proxy_async_shared();
-        __syncwarp();
-        if (lane == 0u) mbar_arrive(&st.empty[slot]);
-        ++st.L;
-        if (idx >= 2) {
-            float *drow = dst + (long long)(r - dir) * p.pitch + col0 + 4;
-#pragma unroll
-            for (int k = 0; k < Q; ++k) {
-                float w = __shfl_up_sync(0xffffffffu, cur[k].w, 1);
-                float e = __shfl_down_sync(0xffffffffu, cur[k].x, 1);
-                if (lane == 0u) w = curw[k];
-                if (lane == 31u) e = cure[k];
-                // prev and x are the rows on either side of the centre; their
-                // sum is commutative, so walking up or down gives the same bits.
-                const Quad q = quad_t<POISSON>(w, cur[k], e, prev[k], x[k], curg[k]);
-                if (STORE) store_quad(drow + 4 * (t + k * C::kCons), quad_update(q), valid[k]);
-                if (CHECK) quad_residual(q, cur[k], valid[k], s2, rmax);
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            prev[k] = cur[k];
-            cur[k] = x[k];
-            curw[k] = xw[k];
-            cure[k] = xe[k];
-            curg[k] = xg[k];
-        }
-    }
-}
-
-// Two sweeps per pass (temporal blocking; "Persistent Kernels...",
-// "Reflections": a wider halo lets a block run several steps per
-// synchronisation, trading a little redundant compute at the tile edges).
-// Input rows ja-2dir .. jb+2dir of U_k; stage 1 computes U_{k+1} on rows
-// ja-dir .. jb+dir, stage 2 writes U_{k+2} on rows ja .. jb.  U_{k+1} stays
-// on chip: each thread keeps its own quads of the last three U_{k+1} rows in
-// registers, and the CTA shares each new U_{k+1} row through a pair of
-// shared-memory rows (same indexing as a ring slot, plus one recomputed
-// cell beyond each strip edge), from which stage 2 takes its west and east
-// neighbours.  One named barrier among the consumer threads per input row
-// orders the writes of a shared row before its reads and before its reuse.
-// A ring slot is held for three input rows (S, centre and N of stage 1), so
-// both stages read their west/east U_k neighbours and the source straight
-// from the staged rows.  Ring cells of U_{k+1} keep their U_k value; every
-// other cell uses the single-sweep arithmetic, so the result is bit for bit
-// two single sweeps.  CHECK reduces the residual of U_k (the loop only
-// checks at the start of a pass).
-template <int N>
-__device__ __forceinline__ void consumers_sync() {
-    asm volatile("bar.sync 1, %0;" ::"n"(N) : "memory");
-}
-
-template <int Q>
-struct Seg2 {
-    float *qbuf;       // two shared U_{k+1} rows
-    float *drow;       // stage-2 output row for the next step (+ quad offset)
-    long long dstep;   // dir * pitch
-    long long col0;
-    int dir, cols, nin, nx, ny;
-    int o[Q];          // float offset of quad k in the strip
-    int valid[Q];      // cells of quad k inside the strip (0..4)
-    int icol[Q];       // interior column of quad k's first cell
-};
-
-// One input row: idx is its position in the segment, r its row.  The three
-// U_k rows (KA = S, KB = centre, KX = N, the new row) and the three U_{k+1}
-// rows (QA, QB, QY = the new one) are passed in their current roles, so an
-// unrolled caller can rotate roles by renaming instead of moving registers.
-// STEADY: 4 <= idx <= nin-2, where both stages run, the stage-1 row lies in
-// the band and no ring row is involved.  FULL: the strip is TW columns wide,
-// so every quad holds four interior cells and none holds the ring column.
-template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL = false>
-__device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c, StreamState &st,
-                                          int idx, int r, float4 (&KA)[C::kQPT],
-                                          float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
-                                          float4 (&QA)[C::kQPT], float4 (&QB)[C::kQPT],
-                                          float4 (&QY)[C::kQPT], double &s2, float &rmax) {
-    constexpr int Q = C::kQPT;
-    constexpr unsigned M = C::kStages - 1;
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const unsigned L = st.L;
-    if (!st.broken && !mbar_wait_bounded(&st.full[L & M], (L / C::kStages) & 1u, p.timeout_ns, p.bar)) {
-        record_error(p.bar, kETimedOut, kSitePipeline);
-        st.broken = true;
-    }
-    consumers_sync<C::kCons>();
-    const float *sx = st.slots + (L & M) * C::SLOT;
-    const float *sb = st.slots + ((L - 1u) & M) * C::SLOT;
-    const float *sa = st.slots + ((L - 2u) & M) * C::SLOT;
-    float *qw = c.qbuf + (L & 1u) * C::SLOTU;
-    const float *qr = c.qbuf + ((L - 1u) & 1u) * C::SLOTU;
-#pragma unroll
-    for (int k = 0; k < Q; ++k) KX[k] = lds4(sx + 4 + c.o[k]);
-    if (STEADY || idx >= 2) {
-        // Stage 1: U_{k+1} on row r - dir (centre KB).
-        const int ob = r - c.dir;
-        const bool ring_row = !STEADY && (ob < 1 || ob > c.ny);
-        const bool in_band = STEADY || (idx >= 3 && idx <= c.nin - 2);
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sb + C::SLOTU + 4 + o) : z4;
-            const Quad q1 = quad_t2<POISSON>(sb[3 + o], KB[k], sb[8 + o], KA[k], KX[k], g);
-            if (CHECK && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
-            float4 u1 = quad_update2(q1);
-            if (ring_row) {
-                u1 = KB[k];
-            } else if (!FULL && c.icol[k] + 3 > c.nx) {
-                if (c.icol[k] + 0 > c.nx) u1.x = KB[k].x;
-                if (c.icol[k] + 1 > c.nx) u1.y = KB[k].y;
-                if (c.icol[k] + 2 > c.nx) u1.z = KB[k].z;
-                u1.w = KB[k].w;
-            }
-            QY[k] = u1;
-            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(qw + 4 + o) = u1;
-        }
-        // The cell beyond each strip edge (the ring column keeps U_k).
-        if (threadIdx.x == 0) {
-            float v = sb[3];
-            if (!ring_row && c.col0 > 0) {
-                float t = cell_t(sb[2], sb[4], sa[3], sx[3]);
-                if (POISSON) t = __fsub_rn(t, sb[C::SLOTU + 3]);
-                v = __fmul_rn(0.25f, t);
-            }
-            qw[3] = v;
-        }
-        if (threadIdx.x == C::kCons - 1 && (c.cols & 3) == 0) {
-            const int m = 4 + c.cols;
-            float v = sb[m];
-            if (!ring_row && c.col0 + c.cols < c.nx) {
-                float t = cell_t(sb[m - 1], sb[m + 1], sa[m], sx[m]);
-                if (POISSON) t = __fsub_rn(t, sb[C::SLOTU + m]);
-                v = __fmul_rn(0.25f, t);
-            }
-            qw[m] = v;
-        }
-    }
-    if (STEADY || idx >= 4) {
-        // Stage 2: U_{k+2} on row r - 2dir (centre QB), inside the band.
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
-            const Quad q2 = quad_t2<POISSON>(qr[3 + o], QB[k], qr[8 + o], QA[k], QY[k], g);
-            if (FULL)
-                *reinterpret_cast<float4 *>(c.drow + o) = quad_update2(q2);
-            else
-                store_quad(c.drow + o, quad_update2(q2), c.valid[k]);
-        }
-        c.drow += c.dstep;
-    }
-    if (STEADY || idx >= 2) {
-        // Row r - 2dir is no longer needed: hand its slot back to the TMA.
-        fence_proxy_async_shared();
-        __syncwarp();
-        if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 2u) & M]);
-    }
-    st.L = L + 1u;
-}
-
-template <int Q>
-__device__ __forceinline__ void rotate3(float4 (&A)[Q], float4 (&B)[Q], float4 (&X)[Q]);
-
-// Steady input rows of a segment, three per trip with the roles renamed.
-template <class C, bool POISSON, bool CHECK, bool FULL>
-__device__ __forceinline__ void seg2_steady(const SweepParams &p, Seg2<C::kQPT> &c, StreamState &st,
-                                            int &idx, int &r, int steady, float4 (&ka)[C::kQPT],
-                                            float4 (&kb)[C::kQPT], float4 (&kx)[C::kQPT],
-                                            float4 (&qa)[C::kQPT], float4 (&qb)[C::kQPT],
-                                            float4 (&qy)[C::kQPT], double &s2, float &rmax) {
-    const int dir = c.dir;
-    for (; steady >= 3; steady -= 3) {
-        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 1, r + dir, kb, kx, ka, qb, qy, qa,
-                                                 s2, rmax);
-        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, qy, qa,
-                                                 qb, s2, rmax);
-        idx += 3;
-        r += 3 * dir;
-    }
-    for (; steady > 0; --steady, ++idx, r += dir) {
-        seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(qa, qb, qy);
-    }
-}
-
-template <int Q>
-__device__ __forceinline__ void rotate3(float4 (&A)[Q], float4 (&B)[Q], float4 (&X)[Q]) {
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        const float4 t = A[k];
-        A[k] = B[k];
-        B[k] = X[k];
-        X[k] = t;
-    }
-}
-
-template <class C, bool POISSON, bool CHECK>
-__device__ __forceinline__ void consume_segment2(const SweepParams &p, float *dst, int ja, int jb,
-                                                 int dir, int cols, long long col0,
-                                                 StreamState &st, float *qbuf, double &s2,
-                                                 float &rmax) {
-    constexpr int Q = C::kQPT;
-    Seg2<Q> c;
-    c.qbuf = qbuf;
-    c.dir = dir;
-    c.cols = cols;
-    c.col0 = col0;
-    c.nin = (dir > 0 ? jb - ja : ja - jb) + 5;
-    c.nx = p.nx;
-    c.ny = p.ny;
-    c.dstep = (long long)dir * p.pitch;
-    c.drow = dst + (long long)ja * p.pitch + col0 + 4;
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        c.o[k] = 4 * ((int)threadIdx.x + k * C::kCons);
-        c.valid[k] = max(0, min(4, cols - c.o[k]));
-        c.icol[k] = (int)col0 + 1 + c.o[k];
-    }
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 ka[Q], kb[Q], kx[Q], qa[Q], qb[Q], qy[Q];
-#pragma unroll
-    for (int k = 0; k < Q; ++k) ka[k] = kb[k] = kx[k] = qa[k] = qb[k] = qy[k] = z4;
-    int idx = 0;
-    int r = ja - 2 * dir;
-    // Prologue: the first four input rows (stages start at idx 2 and 4).
-    for (; idx < 4; ++idx, r += dir) {
-        seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(qa, qb, qy);
-    }
-    // Steady rows 4 .. nin-2.
-    if (cols == C::TW)
-        seg2_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, c.nin - 5, ka, kb, kx, qa, qb, qy,
-                                             s2, rmax);
-    else
-        seg2_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, c.nin - 5, ka, kb, kx, qa, qb, qy,
-                                              s2, rmax);
-    // Last input row: stage 1 on the row beyond the band (maybe the ring).
-    seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
-    // The last two input rows' slots.
-    fence_proxy_async_shared();
-    __syncwarp();
-    if ((threadIdx.x & 31u) == 0u) {
-        mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
-        mbar_arrive(&st.empty[(st.L - 1u) & (C::kStages - 1)]);
-    }
-}
-
-// Three sweeps per pass: the two-sweep pass with one more level.  Input rows
-// ja-3dir .. jb+3dir of U_k; stage 1 computes U_{k+1} on rows ja-2dir ..
-// jb+2dir, stage 2 U_{k+2} on rows ja-dir .. jb+dir, stage 3 writes U_{k+3}
-// on rows ja .. jb.  Each thread keeps its quads of the last three rows of
-// U_k, U_{k+1} and U_{k+2} in registers; the CTA shares each new U_{k+1} and
-// U_{k+2} row through two shared rows per level, with the one named barrier
-// per input row.  The cells beyond a strip edge that later stages read are
-// U_{k+1} two columns out and U_{k+2} one column out; the thread that owns
-// the strip's first (last) quad computes them, from the staged U_k rows and
-// a three-row history of its own U_{k+1} edge cells.  A ring slot is held
-// for four input rows (stage 3 reads the source of its row from it).  Ring
-// cells of every level keep the U_k value; every other cell uses the
-// single-sweep arithmetic, so the result is bit for bit three single sweeps.
-template <int Q>
-struct Seg3 {
-    float *q1buf;      // two shared U_{k+1} rows
-    float *q2buf;      // two shared U_{k+2} rows
-    float *drow;       // stage-3 output row for the next step (+ quad offset)
-    long long dstep;   // dir * pitch
-    long long col0;
-    int dir, cols, nin, nx, ny;
-    bool first_strip, last_strip, right_edge;
-    int o[Q];
-    int valid[Q];
-    int icol[Q];
-    // Edge threads' U_{k+1} history: the cell just beyond the strip edge
-    // (column col0, or m = 4+cols on the right) at the last two stage-1
-    // rows, newest first, and the cell one further out at the last one.
-    float e_c0, e_c1;
-    float e_out;
-};
-
-// Replace the quad's cells beyond the right ring column (and the ring column
-// itself) by the previous level's value there.
-__device__ __forceinline__ float4 keep_ring_cols(float4 u, float4 prev, int icol, int nx) {
-    if (icol + 0 > nx) u.x = prev.x;
-    if (icol + 1 > nx) u.y = prev.y;
-    if (icol + 2 > nx) u.z = prev.z;
-    u.w = prev.w;
-    return u;
-}
-
-// One input row of a three-sweep segment: idx is its position, r its row.
-// K = U_k rows, P = U_{k+1} rows, R = U_{k+2} rows, each (two older rows,
-// the new row) in their current roles.  STEADY: 6 <= idx <= nin-3, where all
-// stages run, the stage-1 row lies in the band and no ring row is involved.
-// FULL: the strip is TW columns wide.
-template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL = false>
-__device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c, StreamState &st,
-                                          int idx, int r, float4 (&KA)[C::kQPT],
-                                          float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
-                                          float4 (&PA)[C::kQPT], float4 (&PB)[C::kQPT],
-                                          float4 (&PY)[C::kQPT], float4 (&RA)[C::kQPT],
-                                          float4 (&RB)[C::kQPT], float4 (&RY)[C::kQPT],
-                                          double &s2, float &rmax) {
-    constexpr int Q = C::kQPT;
-    constexpr unsigned M = C::kStages - 1;
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const unsigned L = st.L;
-    if (!st.broken && !mbar_wait_bounded(&st.full[L & M], (L / C::kStages) & 1u, p.timeout_ns, p.bar)) {
-        record_error(p.bar, kETimedOut, kSitePipeline);
-        st.broken = true;
-    }
-    consumers_sync<C::kCons>();
-    const float *sx = st.slots + (L & M) * C::SLOT;
-    const float *sb = st.slots + ((L - 1u) & M) * C::SLOT;
-    const float *sa = st.slots + ((L - 2u) & M) * C::SLOT;
-    const float *sz = st.slots + ((L - 3u) & M) * C::SLOT;
-    float *p1w = c.q1buf + (L & 1u) * C::SLOTU;
-    const float *p1r = c.q1buf + ((L - 1u) & 1u) * C::SLOTU;
-    float *p2w = c.q2buf + (L & 1u) * C::SLOTU;
-    const float *p2r = c.q2buf + ((L - 1u) & 1u) * C::SLOTU;
-#pragma unroll
-    for (int k = 0; k < Q; ++k) KX[k] = lds4(sx + 4 + c.o[k]);
-    const int r1 = r - c.dir, r2 = r - 2 * c.dir;
-    const bool act1 = STEADY || idx >= 2, act2 = STEADY || idx >= 4, act3 = STEADY || idx >= 6;
-    const bool ring1 = !STEADY && (r1 < 1 || r1 > c.ny);
-    const bool ring2 = !STEADY && (r2 < 1 || r2 > c.ny);
-    // The cells beyond each strip edge: U_{k+1} at row r1, one and two
-    // columns out, and U_{k+2} at row r2, one column out; a ring column (or
-    // ring row) keeps U_k at every level.  They need only the staged rows and
-    // the previous step's registers, so they come first and their loads
-    // overlap the stages; the branch is uniform per warp and the code inside
-    // it has no branches, so every lane of the warp runs it and only the
-    // edge lane's results are kept.
-    const unsigned lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    if (act1 && warp == 0) {
-        const bool keep1 = ring1 || c.first_strip, keep2 = ring2 || c.first_strip;
-        float t = cell_t(sb[2], sb[4], sa[3], sx[3]);
-        float t2 = cell_t(sb[1], sb[3], sa[2], sx[2]);
-        if (POISSON) {
-            t = __fsub_rn(t, sb[C::SLOTU + 3]);
-            t2 = __fsub_rn(t2, sb[C::SLOTU + 2]);
-        }
-        const float v1c = keep1 ? sb[3] : __fmul_rn(0.25f, t);
-        const float v1o = keep1 ? sb[2] : __fmul_rn(0.25f, t2);
-        float t3 = cell_t(c.e_out, PB[0].x, c.e_c1, v1c);
-        if (POISSON) t3 = __fsub_rn(t3, sa[C::SLOTU + 3]);
-        const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
-        if (lane == 0u) {
-            p1w[3] = v1c;
-            if (act2) p2w[3] = v2c;
-        }
-        c.e_c1 = c.e_c0;
-        c.e_c0 = v1c;
-        c.e_out = v1o;
-    }
-    if (act1 && warp == C::kCons / 32 - 1 && c.right_edge) {
-        const int m = 4 + c.cols;
-        const bool keep1 = ring1 || c.last_strip, keep2 = ring2 || c.last_strip;
-        float t = cell_t(sb[m - 1], sb[m + 1], sa[m], sx[m]);
-        float t2 = cell_t(sb[m], sb[m + 2], sa[m + 1], sx[m + 1]);
-        if (POISSON) {
-            t = __fsub_rn(t, sb[C::SLOTU + m]);
-            t2 = __fsub_rn(t2, sb[C::SLOTU + m + 1]);
-        }
-        const float v1c = keep1 ? sb[m] : __fmul_rn(0.25f, t);
-        const float v1o = keep1 ? sb[m + 1] : __fmul_rn(0.25f, t2);
-        float t3 = cell_t(PB[Q - 1].w, c.e_out, c.e_c1, v1c);
-        if (POISSON) t3 = __fsub_rn(t3, sa[C::SLOTU + m]);
-        const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
-        if (lane == 31u) {
-            p1w[m] = v1c;
-            if (act2) p2w[m] = v2c;
-        }
-        c.e_c1 = c.e_c0;
-        c.e_c0 = v1c;
-        c.e_out = v1o;
-    }
-    if (act1) {
-        // Stage 1: U_{k+1} on row r1 (centre KB).
-        const bool in_band = STEADY || (idx >= 4 && idx <= c.nin - 3);
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sb + C::SLOTU + 4 + o) : z4;
-            const Quad q1 = quad_t2<POISSON>(sb[3 + o], KB[k], sb[8 + o], KA[k], KX[k], g);
-            if (CHECK && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
-            float4 u1 = quad_update2(q1);
-            if (ring1)
-                u1 = KB[k];
-            else if (!FULL && c.icol[k] + 3 > c.nx)
-                u1 = keep_ring_cols(u1, KB[k], c.icol[k], c.nx);
-            PY[k] = u1;
-            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(p1w + 4 + o) = u1;
-        }
-    }
-    if (act2) {
-        // Stage 2: U_{k+2} on row r2 (centre PB); west/east from the shared
-        // U_{k+1} row written one step ago.
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
-            const Quad q2 = quad_t2<POISSON>(p1r[3 + o], PB[k], p1r[8 + o], PA[k], PY[k], g);
-            float4 u2 = quad_update2(q2);
-            if (ring2)
-                u2 = PB[k];
-            else if (!FULL && c.icol[k] + 3 > c.nx)
-                u2 = keep_ring_cols(u2, PB[k], c.icol[k], c.nx);
-            RY[k] = u2;
-            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(p2w + 4 + o) = u2;
-        }
-    }
-    if (act3) {
-        // Stage 3: U_{k+3} on row r - 3dir (centre RB), inside the band.
-#pragma unroll
-        for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sz + C::SLOTU + 4 + o) : z4;
-            const Quad q3 = quad_t2<POISSON>(p2r[3 + o], RB[k], p2r[8 + o], RA[k], RY[k], g);
-            if (FULL)
-                *reinterpret_cast<float4 *>(c.drow + o) = quad_update2(q3);
-            else
-                store_quad(c.drow + o, quad_update2(q3), c.valid[k]);
-        }
-        c.drow += c.dstep;
-    }
-    if (STEADY || idx >= 3) {
-        // Row r - 3dir is no longer needed: hand its slot back to the TMA.
-        fence_proxy_async_shared();
-        __syncwarp();
-        if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 3u) & M]);
-    }
-    st.L = L + 1u;
-}
-
-template <class C, bool POISSON, bool CHECK, bool FULL>
-__device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> &c, StreamState &st,
-                                            int &idx, int &r, int steady, float4 (&ka)[C::kQPT],
-                                            float4 (&kb)[C::kQPT], float4 (&kx)[C::kQPT],
-                                            float4 (&pa)[C::kQPT], float4 (&pb)[C::kQPT],
-                                            float4 (&py)[C::kQPT], float4 (&ra)[C::kQPT],
-                                            float4 (&rb)[C::kQPT], float4 (&ry)[C::kQPT],
-                                            double &s2, float &rmax) {
-    const int dir = c.dir;
-    for (; steady >= 3; steady -= 3) {
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry,
-                                                 s2, rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 1, r + dir, kb, kx, ka, pb, py, pa,
-                                                 rb, ry, ra, s2, rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, py, pa,
-                                                 pb, ry, ra, rb, s2, rmax);
-        idx += 3;
-        r += 3 * dir;
-    }
-    for (; steady > 0; --steady, ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry,
-                                                 s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(pa, pb, py);
-        rotate3(ra, rb, ry);
-    }
-}
-
-template <class C, bool POISSON, bool CHECK>
-__device__ __forceinline__ void consume_segment3(const SweepParams &p, float *dst, int ja, int jb,
-                                                 int dir, int cols, long long col0,
-                                                 StreamState &st, float *qbuf, double &s2,
-                                                 float &rmax) {
-    constexpr int Q = C::kQPT;
-    Seg3<Q> c;
-    c.q1buf = qbuf;
-    c.q2buf = qbuf + 2 * C::SLOTU;
-    c.dir = dir;
-    c.cols = cols;
-    c.col0 = col0;
-    c.nin = (dir > 0 ? jb - ja : ja - jb) + 7;
-    c.nx = p.nx;
-    c.ny = p.ny;
-    c.first_strip = col0 == 0;
-    c.last_strip = col0 + cols >= p.nx;
-    c.right_edge = (cols & 3) == 0;
-    c.dstep = (long long)dir * p.pitch;
-    c.drow = dst + (long long)ja * p.pitch + col0 + 4;
-    c.e_c0 = c.e_c1 = c.e_out = 0.f;
-#pragma unroll
-    for (int k = 0; k < Q; ++k) {
-        c.o[k] = 4 * ((int)threadIdx.x + k * C::kCons);
-        c.valid[k] = max(0, min(4, cols - c.o[k]));
-        c.icol[k] = (int)col0 + 1 + c.o[k];
-    }
-    const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 ka[Q], kb[Q], kx[Q], pa[Q], pb[Q], py[Q], ra[Q], rb[Q], ry[Q];
-#pragma unroll
-    for (int k = 0; k < Q; ++k) ka[k] = kb[k] = kx[k] = pa[k] = pb[k] = py[k] = ra[k] = rb[k] = ry[k] = z4;
-    int idx = 0;
-    int r = ja - 3 * dir;
-    // Prologue: the first six input rows (stages start at idx 2, 4 and 6).
-    for (; idx < 6; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry, s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(pa, pb, py);
-        rotate3(ra, rb, ry);
-    }
-    // Steady rows 6 .. nin-3.
-    const int steady = c.nin - 8 > 0 ? c.nin - 8 : 0;
-    // Full-width strips take the unrolled steady loop.  A ragged last strip
-    // takes its own unrolled copy for Laplace: the CTAs holding its rows would
-    // otherwise set the pace of every pass.  For Poisson the second copy
-    // makes the kernel too large for the compiler to keep the row windows in
-    // registers (they went to the stack, 1.45x slower), so there the ragged
-    // rows run through the rolled generic step below.
-    if (cols == C::TW)
-        seg3_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
-                                             ry, s2, rmax);
-    else if constexpr (!POISSON)
-        seg3_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
-                                              rb, ry, s2, rmax);
-    // The last input rows: stages 1 and 2 reach beyond the band (maybe the ring).
-    for (; idx < c.nin; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry, s2, rmax);
-        rotate3(ka, kb, kx);
-        rotate3(pa, pb, py);
-        rotate3(ra, rb, ry);
-    }
-    // The last three input rows' slots.
-    fence_proxy_async_shared();
-    __syncwarp();
-    if ((threadIdx.x & 31u) == 0u) {
-        mbar_arrive(&st.empty[(st.L - 3u) & (C::kStages - 1)]);
-        mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
-        mbar_arrive(&st.empty[(st.L - 1u) & (C::kStages - 1)]);
-    }
-}
-
-template <class C, bool POISSON, bool CHECK, bool STORE, int D>
-__device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
-                                            int dir, StreamState &st, double &s2, float &rmax) {
-    const int nx = p.nx, ny = p.ny;
-    const int strips = (nx + C::TW - 1) / C::TW;
-    const long long R = (long long)strips * ny;
-    const long long L0 = R * blockIdx.x / gridDim.x;
-    const long long L1 = R * (blockIdx.x + 1) / gridDim.x;
-    const bool producer_warp = threadIdx.x >= C::kCons;
-    long long pos = dir > 0 ? L0 : L1 - 1;
-    long long remaining = L1 - L0;
-    while (remaining > 0) {
-        const int s = (int)(pos / ny);
-        const int jr = (int)(pos - (long long)s * ny) + 1;
-        long long len;
-        int jb;
-        if (dir > 0) {
-            len = min((long long)(ny - jr + 1), remaining);
-            jb = jr + (int)len - 1;
-        } else {
-            len = min((long long)jr, remaining);
-            jb = jr - (int)len + 1;
-        }
-        const int cols = min(C::TW, nx - s * C::TW);
-        const long long col0 = (long long)s * C::TW;
-        if (producer_warp) {
-            produce_segment<C, POISSON, D>(p, src, jr, jb, dir, cols, col0, st);
-        } else if (D == 3) {
-            consume_segment3<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st,
-                                                st.slots + C::kStages * C::SLOT, s2, rmax);
-        } else if (D == 2) {
-            consume_segment2<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st,
-                                                st.slots + C::kStages * C::SLOT, s2, rmax);
-        } else {
-            consume_segment<C, POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
-                                                      rmax);
-        }
-        pos += dir > 0 ? len : -len;
-        remaining -= len;
-    }
-    // Generic-proxy stores of this sweep -> TMA reads of the next one.
-    if (STORE && !producer_warp) fence_proxy_async_global();
-    __syncwarp();
-}
-
-template <class C, bool POISSON>
-__device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
-                                                int dir, bool check, bool store, int dp,
-                                                StreamState &st, double &s2, float &rmax) {
-    // Only the depths this shape can take are compiled in.
-    if constexpr (C::kDepth >= 3) {
-        if (dp == 3) {
-            if (check)
-                pass_stream<C, POISSON, true, true, 3>(p, src, dst, dir, st, s2, rmax);
-            else
-                pass_stream<C, POISSON, false, true, 3>(p, src, dst, dir, st, s2, rmax);
-            return;
-        }
-    }
-    if constexpr (C::kDepth >= 2) {
-        if (dp == 2) {
-            if (check)
-                pass_stream<C, POISSON, true, true, 2>(p, src, dst, dir, st, s2, rmax);
-            else
-                pass_stream<C, POISSON, false, true, 2>(p, src, dst, dir, st, s2, rmax);
-            return;
-        }
-    }
-    if (check) {
-        if (store)
-            pass_stream<C, POISSON, true, true, 1>(p, src, dst, dir, st, s2, rmax);
-        else
-            pass_stream<C, POISSON, true, false, 1>(p, src, dst, dir, st, s2, rmax);
-    } else if (store) {
-        pass_stream<C, POISSON, false, true, 1>(p, src, dst, dir, st, s2, rmax);
-    }
-}
-
-// ===========================================================================
-// The persistent and per-launch STREAM kernels.
-template <class C, bool POISSON>
-__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    StreamState st = stream_setup<C>(smem);
-    persistent_loop<C::kDepth>(p, [&](const float *src, float *dst, bool check, bool store,
-                                      int dp, long long k, double &s2, float &rmax) {
-        const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
-        // After the barrier: this producer's TMA reads must see the
-        // generic-proxy stores the whole grid made in the previous sweep.
-        // The issuing thread acquires at gpu scope itself, then fences the
-        // generic proxy against the async proxy.
-        if (threadIdx.x == C::kCons) {
-            fence_acq_rel_gpu();
-            fence_proxy_async_global();
-        }
-        pass_stream_any<C, POISSON>(p, src, dst, dir, check, store, dp, st, s2, rmax);
-    });
-}
-
-template <class C, bool POISSON>
-__global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_once_stream(SweepParams p) {
-    extern __shared__ __align__(128) unsigned char smem[];
-    StreamState st = stream_setup<C>(smem);
-    double s2 = 0.0;
-    float rmax = 0.f;
-    const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;
-    pass_stream_any<C, POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
-                                p.pass_store != 0, 1, st, s2, rmax);
-    if (p.pass_check) write_partial(p, s2, rmax);
-}
-
-template <int CFG, bool POISSON>
-using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, kStreamConfigs[CFG].depth,
-                   kStreamConfigs[CFG].min_ctas, kStreamConfigs[CFG].consumers, POISSON>;
-
-template <int CFG, bool POISSON>
-const void *persistent_stream_fn() {
-    return (const void *)k_persistent_stream<CfgOf<CFG, POISSON>, POISSON>;
-}
-template <int CFG, bool POISSON>
-const void *once_stream_fn() {
-    return (const void *)k_once_stream<CfgOf<CFG, POISSON>, POISSON>;
-}
-
-template <bool POISSON>
-const void *stream_fn(int cfg, bool persistent) {
-    switch (cfg) {
-#define PK_CFG_CASE(c) \
-    case c:            \
-        return persistent ? persistent_stream_fn<c, POISSON>() : once_stream_fn<c, POISSON>();
-        PK_CFG_CASE(0)
-        PK_CFG_CASE(1)
-        PK_CFG_CASE(2)
-        PK_CFG_CASE(3)
-        PK_CFG_CASE(4)
-        PK_CFG_CASE(5)
-        PK_CFG_CASE(6)
-        PK_CFG_CASE(7)
-        PK_CFG_CASE(8)
-        PK_CFG_CASE(9)
-        PK_CFG_CASE(10)
-        PK_CFG_CASE(11)
-        PK_CFG_CASE(12)
-        PK_CFG_CASE(13)
-        PK_CFG_CASE(14)
-#undef PK_CFG_CASE
-        default:
-            return nullptr;
-    }
-}
-static_assert(kNumStreamConfigs == 15, "update stream_fn");
-
-}  // namespace
+const void *stream_kernel_d1(bool poisson, int cfg, bool persistent);
+const void *stream_kernel_d2(bool poisson, int cfg, bool persistent);
+const void *stream_kernel_d3(bool poisson, int cfg, bool persistent);
 
 const void *stream_kernel(bool poisson, int cfg, bool persistent) {
-    return poisson ? stream_fn<true>(cfg, persistent) : stream_fn<false>(cfg, persistent);
+    if (cfg < 0 || cfg >= kNumStreamConfigs) return nullptr;
+    switch (kStreamConfigs[cfg].depth) {
+        case 1: return stream_kernel_d1(poisson, cfg, persistent);
+        case 2: return stream_kernel_d2(poisson, cfg, persistent);
+        default: return stream_kernel_d3(poisson, cfg, persistent);
+    }
 }
+static_assert(kNumStreamConfigs == 13, "each shape must be instantiated in the unit of its depth");
 
 }  // namespace pk
