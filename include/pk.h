@@ -155,7 +155,8 @@ typedef struct {
                                          the plan.  The bands get at least that many rows;
                                          where the tile cannot, the depth is lowered.  Same
                                          bits at every depth. */
-    int32_t reserved[4];
+    int32_t local_threads;            /* LOCAL: threads per CTA, 256 or 512; 0 = by the plan */
+    int32_t reserved[3];
 } pk_options;
 
 /* Fill opt with the defaults above. */

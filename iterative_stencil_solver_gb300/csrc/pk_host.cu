@@ -80,6 +80,7 @@ struct pk_ctx {
     int stream_cfg2 = -1;  // two-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
     int local_depth = 1;   // LOCAL: sweeps per neighbour exchange the plan allows
+    int local_threads = kDirectThreads;  // LOCAL: threads per CTA
     int launch_grid = 1;   // per-launch and graph paths: CTAs of their kernels
     int coop_max = 1;    // occupancy x SMs for the sweep kernel
     int part_cap = 0;    // partial slots per parity
@@ -196,6 +197,8 @@ int read_options(pk_ctx *ctx, const pk_options *opt) {
         return fail(ctx, PK_EINVAL, "stream_config %d out of range", o.stream_config);
     if (o.local_depth < 0 || o.local_depth > kLocalMaxDepth)
         return fail(ctx, PK_EINVAL, "local_depth %d out of range", o.local_depth);
+    if (o.local_threads != 0 && o.local_threads != 256 && o.local_threads != 512)
+        return fail(ctx, PK_EINVAL, "local_threads %d must be 0, 256 or 512", o.local_threads);
     return PK_OK;
 }
 
@@ -257,19 +260,47 @@ int ensure_partials(pk_ctx *ctx, int grid) {
     return PK_OK;
 }
 
-// Sweeps per neighbour exchange the plan aims at: the option, else by row
-// width, as measured on GB300 (1000 sweeps, bands sized as below).  Up to
-// 128 columns a sweep is mostly the neighbour round trip and D = 4 is best
-// (64^2: 0.51 us/sweep against 1.03 at D = 1); up to 512 columns D = 3 is
-// within 7% of the best depth at every shape tried; from 768 columns the
-// band's work dominates and one sweep per exchange is best.
-int local_target_depth(const pk_ctx *ctx) {
-    if (ctx->opt.local_depth > 0) return ctx->opt.local_depth;
+// LOCAL shape by row width (nq float4 groups), as measured on GB300 over
+// 1000 sweeps for every combination of threads per CTA (256, 512), sweeps
+// per neighbour exchange (1..4) and grid:
+//   nq <= 32 (<= 128 columns):  256 threads, D = 4, bands of D rows
+//       (64^2: 0.49 us/sweep, 1.03 at D = 1);
+//   nq <= 96 (<= 384 columns):  512 threads, D = 3, bands of D rows
+//       (256^2: 0.72 against 0.82 with 256 threads);
+//   nq <= 128 (<= 512 columns): 256 threads, D = 3, bands of D rows
+//       (512^2: 1.14; 512 threads only matched it with bands of six rows);
+//   nq <= 256 (<= 1024 columns): 512 threads, D = 3, bands of 2D rows
+//       (1024^2: 1.76 against 2.17 with one sweep per exchange);
+//   wider: 256 threads, one sweep per exchange.
+// The options override threads and depth.
+struct LocalShape {
+    int threads;
+    int depth;
+    int rows_per_depth;  // band height the grid aims at, in units of depth
+};
+
+LocalShape local_shape(const pk_ctx *ctx) {
     const int nq = (ctx->nx + 3) / 4;
-    if (nq <= 32) return 4;
-    if (nq <= 128) return 3;
-    return 1;
+    LocalShape sh;
+    if (nq <= 32)
+        sh = {256, 4, 1};
+    else if (nq <= 96)
+        sh = {512, 3, 1};
+    else if (nq <= 128)
+        sh = {256, 3, 1};
+    else if (nq <= 256)
+        sh = {512, 3, 2};
+    else
+        sh = {256, 1, 1};
+    if (ctx->opt.local_threads > 0) sh.threads = ctx->opt.local_threads;
+    if (ctx->opt.local_depth > 0) {
+        sh.depth = ctx->opt.local_depth;
+        sh.rows_per_depth = 1;
+    }
+    return sh;
 }
+
+int local_target_depth(const pk_ctx *ctx) { return local_shape(ctx).depth; }
 
 // LOCAL plan.  At the widths LOCAL serves, a sweep costs about one
 // neighbour round trip plus the band's work, so:
@@ -283,17 +314,18 @@ int local_target_depth(const pk_ctx *ctx) {
 // The grid is then capped by what is co-resident with the tile's shared
 // memory.  Returns false when the tile does not fit.
 bool plan_local(pk_ctx *ctx, int *grid_out, int *rows_out, int *cap_out) {
+    const LocalShape shape = local_shape(ctx);
+    ctx->local_threads = shape.threads;
     const int nq = (ctx->nx + 3) / 4;
     const long long sms = ctx->sms > 0 ? ctx->sms : 1;
     long long grid;
     if (ctx->opt.grid_override > 0) {
         grid = ctx->opt.grid_override;
     } else {
-        const int depth = local_target_depth(ctx);
-        long long base = ctx->ny / depth;
+        long long base = ctx->ny / ((long long)shape.depth * shape.rows_per_depth);
         if (base < 1) base = 1;
         grid = base < sms ? base : sms;
-        const double per_thread = (double)ctx->ny / (double)sms * nq / kDirectThreads;
+        const double per_thread = (double)ctx->ny / (double)sms * nq / ctx->local_threads;
         if (base >= 2 * sms && per_thread >= 2.0) grid = 2 * sms;
     }
     // Enough CTAs that a band's tile fits in shared memory.
@@ -312,7 +344,7 @@ bool plan_local(pk_ctx *ctx, int *grid_out, int *rows_out, int *cap_out) {
         if (smem > g_local_smem_max) return false;
         int per_sm = 0;
         const int cap = coop_capacity(ctx, kernel_persistent(kVariantLocal, ctx->poisson, 0),
-                                      kDirectThreads, smem, &per_sm);
+                                      ctx->local_threads, smem, &per_sm);
         if (cap <= 0) return false;
         if (grid <= cap || ctx->opt.grid_override > 0) {
             *grid_out = (int)grid;
@@ -380,7 +412,7 @@ int plan(pk_ctx *ctx) {
                 if (smem_d <= g_local_smem_max) {
                     int per_d = 0;
                     const int cap_d = coop_capacity(ctx, kernel_persistent(kVariantLocalD, ctx->poisson, depth),
-                                                    kDirectThreads, smem_d, &per_d);
+                                                    ctx->local_threads, smem_d, &per_d);
                     if (cap_d < 0) return PK_ECUDA;
                     if (cap_d >= lgrid) break;
                 }
@@ -461,6 +493,7 @@ SweepParams base_params(pk_ctx *ctx) {
     p.local_rows = ctx->local_rows;
     p.local_pitch = local_pitch(ctx->nx);
     p.one_sweep = (ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS) ? 1 : 0;
+    p.local_threads = ctx->local_threads;
     return p;
 }
 

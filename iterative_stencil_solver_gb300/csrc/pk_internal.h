@@ -66,6 +66,7 @@ struct SweepParams {
     int local_rows;         // most rows any CTA owns
     int local_pitch;        // floats per tile row in shared memory
     int one_sweep;          // 1: every pass advances one sweep (no temporal blocking)
+    int local_threads;      // LOCAL: threads per CTA
 };
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
@@ -123,6 +124,7 @@ struct TaskParams {
 
 // ---- sizes -----------------------------------------------------------------
 constexpr int kDirectThreads = 256;
+constexpr int kLocalMaxThreads = 512;  // LOCAL kernels run 256 or 512 threads per CTA
 constexpr int kStressWords = 32;
 
 // STREAM configurations: float4 groups per consumer thread per row (the

@@ -696,11 +696,14 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
                               cudaStream_t s) {
     SweepParams arg = p;
     void *args[] = {&arg};
+    const int threads = (variant == kVariantLocal || variant == kVariantLocalD) && p.local_threads > 0
+                            ? p.local_threads
+                            : block_threads(variant, cfg);
     const size_t smem = variant == kVariantLocal    ? local_smem_bytes(p.nx, p.local_rows, poisson)
                         : variant == kVariantLocalD ? local_d_smem_bytes(p.nx, p.local_rows, poisson, cfg)
                                                     : dyn_smem(variant, poisson, cfg);
     return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
-                                       dim3(block_threads(variant, cfg)), args, smem, s);
+                                       dim3(threads), args, smem, s);
 }
 
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,

@@ -131,7 +131,7 @@ __device__ __forceinline__ bool recv_tagged(int total, unsigned tag, const Sweep
 }
 
 template <bool POISSON>
-__global__ void __launch_bounds__(kDirectThreads) k_persistent_local(SweepParams p) {
+__global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local(SweepParams p) {
     extern __shared__ __align__(16) float tile[];
     const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
     const int nx = p.nx, ny = p.ny;
@@ -338,7 +338,7 @@ __device__ __forceinline__ void local_stage(const LocalBand &lb, const float *Ts
 // Tile row lr holds grid row r0 - D + lr, lr = 0 .. B+2D-1; rows beyond the
 // ring are never read.  Source row lg = lr - 1 covers the computed rows.
 template <bool POISSON, int D>
-__global__ void __launch_bounds__(kDirectThreads) k_persistent_local_d(SweepParams p) {
+__global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local_d(SweepParams p) {
     extern __shared__ __align__(16) float tile[];
     const int G = gridDim.x, b = blockIdx.x, tid = threadIdx.x, nthr = blockDim.x;
     const int nx = p.nx, ny = p.ny;

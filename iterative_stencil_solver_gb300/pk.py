@@ -105,7 +105,8 @@ class pk_options(ctypes.Structure):
         ("barrier_kind", ctypes.c_int32),
         ("stream_config", ctypes.c_int32),
         ("local_depth", ctypes.c_int32),
-        ("reserved", ctypes.c_int32 * 4),
+        ("local_threads", ctypes.c_int32),
+        ("reserved", ctypes.c_int32 * 3),
     ]
 
 

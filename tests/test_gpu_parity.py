@@ -616,7 +616,7 @@ def test_local_variant_bit_exact(pk, nx, ny, grid, poisson):
             assert info["grid"] == min(grid, ny)
         # the plan's depth by row width, lowered until every band has that
         # many rows (passes shorten where a check or the end would fall inside)
-        depth = 4 if nx <= 128 else 3 if nx <= 512 else 1
+        depth = 4 if nx <= 128 else 3 if nx <= 1024 else 1
         while depth > 1 and ny // info["grid"] < depth:
             depth -= 1
         assert info["sweeps_per_pass"] == depth
