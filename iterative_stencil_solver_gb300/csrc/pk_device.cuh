@@ -128,7 +128,9 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 // Generic-proxy reads of a shared-memory buffer -> a later async-proxy (TMA)
 // write of the same buffer.  Without it a pending ld.shared can be
-// overtaken by the refill that the mbarrier release allows.
+// overtaken by the refill that the mbarrier release allows.  It waits for
+// the thread's outstanding memory operations, global stores included, so a
+// release is best placed before a step's stores.
 __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -278,34 +280,81 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned by
                  "r"(bytes)
                  : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+// The waits and arrivals take 32-bit shared-window addresses (smem_u32);
+// the pointer forms below convert.
+__device__ __forceinline__ void mbar_arrive_at(unsigned bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+__device__ __forceinline__ bool mbar_try_wait_at(unsigned bar, unsigned parity) {
     unsigned done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(bar), "r"(parity)
         : "memory");
     return done != 0u;
 }
+// The same test with an explicit suspend-time limit: a thread whose phase is
+// not complete sleeps until it completes or about hint_ns pass, instead of
+// returning at once and taking issue slots from the warps that work.
+__device__ __forceinline__ bool mbar_try_wait_sleep_at(unsigned bar, unsigned parity,
+                                                       unsigned hint_ns) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return done != 0u;
+}
+// Suspend limit of one wait round: the abort flag and the timeout are
+// checked after each round, so this is also their granularity.
+constexpr unsigned kMbarSleepNs = 20000u;
 // Bounded wait: false after timeout_ns, or as soon as the grid is aborting
 // (the caller records the error).
+__device__ __forceinline__ bool mbar_wait_bounded_at(unsigned bar, unsigned parity,
+                                                     uint64_t timeout_ns, const BarrierState *gb) {
+    if (mbar_try_wait_at(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_sleep_at(bar, parity, kMbarSleepNs)) return true;
+        if (aborted(gb)) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) { mbar_arrive_at(smem_u32(bar)); }
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity) {
+    return mbar_try_wait_at(smem_u32(bar), parity);
+}
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity,
                                                   uint64_t timeout_ns, const BarrierState *gb) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    unsigned spins = 0;
-    for (;;) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((++spins & 63u) == 0u) {
-            if (aborted(gb)) return false;
-            if (globaltimer_ns() - t0 > timeout_ns) return false;
-        }
-    }
+    return mbar_wait_bounded_at(smem_u32(bar), parity, timeout_ns, gb);
+}
+// Plain shared-memory loads and stores at 32-bit shared-window addresses
+// (volatile: they stay on their side of the barriers around them).
+__device__ __forceinline__ float lds_at(unsigned a) {
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 lds4_at(unsigned a) {
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(a));
+    return v;
+}
+__device__ __forceinline__ void sts_at(unsigned a, float v) {
+    asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v) : "memory");
+}
+__device__ __forceinline__ void sts4_at(unsigned a, float4 v) {
+    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v.x), "f"(v.y),
+                 "f"(v.z), "f"(v.w)
+                 : "memory");
 }
 // 1-D bulk copy global -> this CTA's shared memory, completing on bar.
 // dst, src 16-byte aligned; bytes a multiple of 16.

@@ -154,12 +154,14 @@ inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 
 // A ring slot: the U row segment (4 halo floats each side) and, for
 // Poisson, the g row segment with a 4-float margin each side.  A shape of
-// D sweeps per pass adds two shared rows for each of U_{k+1} .. U_{k+D-1},
-// laid out like the U part of a slot.
+// D sweeps per pass adds shared rows for each of U_{k+1} .. U_{k+D-1}, laid
+// out like the U part of a slot: two per level for D = 2, three for D = 3.
 inline size_t stream_smem_bytes(int cfg, bool poisson) {
     const int tw = stream_tw(cfg);
+    const int depth = stream_depth(cfg);
     const size_t slot = (size_t)(tw + 8 + (poisson ? tw + 8 : 0)) * sizeof(float);
-    const size_t qrows = 2 * (size_t)(stream_depth(cfg) - 1) * (size_t)(tw + 8) * sizeof(float);
+    const size_t per_level = depth >= 3 ? 3 : 2;
+    const size_t qrows = per_level * (size_t)(depth - 1) * (size_t)(tw + 8) * sizeof(float);
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 

@@ -44,6 +44,17 @@ struct SCfg {
     static constexpr int TW = 4 * QPT * CONS;
     static constexpr int SLOTU = TW + 8;
     static constexpr int SLOT = SLOTU + (POISSON ? TW + 8 : 0);
+    // Three-sweep passes: the consumer warp that computes the strip-edge
+    // cells (warps w and w + 4 share a scheduler; the producer is warp
+    // CONS / 32).
+    static constexpr int kEdgeWarp = 3;
+    // Where the generic-proxy reads of a ring slot are fenced against its
+    // TMA refill: in each consumer warp before it releases the slot, or once
+    // per row in the producer after it acquires the release.  Measured: the
+    // producer side is faster for the one-CTA-per-SM three-sweep shape, the
+    // consumer side for the two-CTA shapes.
+    static constexpr bool kProducerFence = DEPTH == 3 && MINB == 1;
+    static_assert(DEPTH < 3 || CONS / 32 > kEdgeWarp, "three-sweep shapes: at least four consumer warps");
     static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
     static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three sweeps per pass");
 };
@@ -79,6 +90,12 @@ __device__ __forceinline__ float4 lds4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
 }
 
+// The consumer half of the slot-release fencing (see SCfg::kProducerFence).
+template <class C>
+__device__ __forceinline__ void consumer_release_fence() {
+    if constexpr (!C::kProducerFence) fence_proxy_async_shared();
+}
+
 // Producer: input rows ja - D*dir .. jb + D*dir of strip columns
 // [col0, col0+cols), D = sweeps per pass; rows beyond the ring are clamped
 // to it (their products are never stored).  The g row (Poisson) comes with
@@ -111,6 +128,11 @@ __device__ __forceinline__ void produce_segment(const SweepParams &p, const floa
                 record_error(p.bar, kETimedOut, kSitePipeline);
                 st.broken = true;
             }
+            // Producer-side fencing: the consumers' reads of this slot
+            // precede their release arrivals, which this wait acquires, so
+            // a proxy fence here, on that path, orders them before the
+            // async-proxy refill.
+            if constexpr (C::kProducerFence) fence_proxy_async_shared();
             const int rr = r < 0 ? 0 : (r > p.ny + 1 ? p.ny + 1 : r);
             const bool gneed = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= p.ny;
             float *dst_u = st.slots + slot * C::SLOT;
@@ -167,7 +189,7 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
         }
         // Release the slot only once this thread's reads of it are complete
         // with respect to the async proxy that will refill it.
-        fence_proxy_async_shared();
+        consumer_release_fence<C>();
         __syncwarp();
         if (lane == 0u) mbar_arrive(&st.empty[slot]);
         ++st.L;
@@ -320,7 +342,7 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
     }
     if (STEADY || idx >= 2) {
         // Row r - 2dir is no longer needed: hand its slot back to the TMA.
-        fence_proxy_async_shared();
+        consumer_release_fence<C>();
         __syncwarp();
         if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 2u) & M]);
     }
@@ -409,7 +431,7 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
     // Last input row: stage 1 on the row beyond the band (maybe the ring).
     seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
     // The last two input rows' slots.
-    fence_proxy_async_shared();
+    consumer_release_fence<C>();
     __syncwarp();
     if ((threadIdx.x & 31u) == 0u) {
         mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
@@ -422,29 +444,42 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
 // jb+2dir, stage 2 U_{k+2} on rows ja-dir .. jb+dir, stage 3 writes U_{k+3}
 // on rows ja .. jb.  Each thread keeps its quads of the last three rows of
 // U_k, U_{k+1} and U_{k+2} in registers; the CTA shares each new U_{k+1} and
-// U_{k+2} row through two shared rows per level, with the one named barrier
-// per input row.  The cells beyond a strip edge that later stages read are
-// U_{k+1} two columns out and U_{k+2} one column out; the thread that owns
-// the strip's first (last) quad computes them, from the staged U_k rows and
-// a three-row history of its own U_{k+1} edge cells.  A ring slot is held
-// for four input rows (stage 3 reads the source of its row from it).  Ring
-// cells of every level keep the U_k value; every other cell uses the
-// single-sweep arithmetic, so the result is bit for bit three single sweeps.
+// U_{k+2} row through three shared rows per level (the row of input step i
+// in row i mod 3), with the one named barrier per input row.  The cells
+// beyond a strip edge that later stages read are U_{k+1} two columns out and
+// U_{k+2} one column out; one warp computes them from the staged U_k rows, a
+// shared U_{k+1} row and a short history.  A ring slot is held for three
+// input rows: stage 3 takes the source of its row from registers (stage 2
+// loaded it one step before).  Ring cells of every level keep the U_k value;
+// every other cell uses the single-sweep arithmetic, so the result is bit
+// for bit three single sweeps.
+//
+// The step keeps every shared-memory position as a 32-bit shared-window
+// address: this thread's quad in the three ring slots it reads, their full
+// barriers, and its quad in shared row 0.  The three-step unrolled loop
+// renames the slot roles and fixes each step's shared rows at compile time,
+// so a step spends a compare and two selects on ring bookkeeping.
 template <int Q>
 struct Seg3 {
-    float *q1buf;      // two shared U_{k+1} rows
-    float *q2buf;      // two shared U_{k+2} rows
-    float *drow;       // stage-3 output row for the next step (+ quad offset)
-    long long dstep;   // dir * pitch
-    long long col0;
+    unsigned q;           // this thread's first quad in shared row 0 (U_{k+1}
+                          // rows 0..2, U_{k+2} rows 3..5, SLOTU floats apart)
+    unsigned qe;          // edge warp: its lane's edge cell in shared row 0
+    int de;               // edge warp: that cell, in floats from this thread's first quad
+    int dd;               // edge warp: outward direction, -1 (left edge) or +1 (right)
+    unsigned slot_first;  // this thread's first quad in ring slot 0
+    unsigned slot_last;   // ... in ring slot kStages-1
+    unsigned full0;       // full barrier of slot 0 (its empty barrier is kStages words on)
+    unsigned ph;          // phase parity of the newest row's slot
+    int qj;               // rolled steps: shared row of this step (input step mod 3)
+    float *drow;          // stage-3 output, this thread's first quad, for the next step
+    long long dstep;      // dir * pitch
     int dir, cols, nin, nx, ny;
     bool first_strip, last_strip, right_edge;
-    int o[Q];
-    int valid[Q];
-    int icol[Q];
-    // Edge threads' U_{k+1} history: the cell just beyond the strip edge
-    // (column col0, or m = 4+cols on the right) at the last two stage-1
-    // rows, newest first, and the cell one further out at the last one.
+    int valid[Q];         // cells of quad k inside the strip (0..4)
+    int icol[Q];          // interior column of quad k's first cell
+    // Edge lanes' U_{k+1} history: the cell just beyond the strip edge at the
+    // last two stage-1 rows, newest first, and the cell one further out at
+    // the last one.
     float e_c0, e_c1;
     float e_out;
 };
@@ -459,88 +494,88 @@ __device__ __forceinline__ float4 keep_ring_cols(float4 u, float4 prev, int icol
     return u;
 }
 
+template <class T>
+__device__ __forceinline__ void rotate3v(T &a, T &b, T &x) {
+    const T t = a;
+    a = b;
+    b = x;
+    x = t;
+}
+
 // One input row of a three-sweep segment: idx is its position, r its row.
 // K = U_k rows, P = U_{k+1} rows, R = U_{k+2} rows, each (two older rows,
-// the new row) in their current roles.  STEADY: 6 <= idx <= nin-3, where all
-// stages run, the stage-1 row lies in the band and no ring row is involved.
-// FULL: the strip is TW columns wide.
-template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL = false>
+// the new row) in their current roles; sa, sb, sx: this thread's first quad
+// in the slots of input rows L-2, L-1, L, and fa, fb, fx their full
+// barriers.  On return sa and fa hold the slot and barrier of row L+1, so a
+// caller that rotates the roles (a, b, x) -> (b, x, a) is ready for the
+// next row.  G3 (Poisson): the source of stage 3's row on entry, of stage
+// 2's row on return.  STEADY: 6 <= idx <= nin-3, where all stages run, the
+// stage-1 row lies in the band and no ring row is involved.  FULL: the strip
+// is TW columns wide.  QJ: the step's shared row (idx mod 3) when the caller
+// knows it at compile time, else -1 (c.qj).
+template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL, int QJ>
 __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c, StreamState &st,
                                           int idx, int r, float4 (&KA)[C::kQPT],
                                           float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
                                           float4 (&PA)[C::kQPT], float4 (&PB)[C::kQPT],
                                           float4 (&PY)[C::kQPT], float4 (&RA)[C::kQPT],
                                           float4 (&RB)[C::kQPT], float4 (&RY)[C::kQPT],
+                                          unsigned &sa, unsigned &sb, unsigned &sx, unsigned &fa,
+                                          unsigned &fb, unsigned &fx, float4 (&G3)[C::kQPT],
                                           double &s2, float &rmax) {
     constexpr int Q = C::kQPT;
-    constexpr unsigned M = C::kStages - 1;
+    constexpr unsigned KO = 16u * C::kCons;  // bytes from one quad of a thread to its next
+    constexpr unsigned RW = 4u * C::SLOTU;   // bytes between shared rows
+    constexpr unsigned GO = 4u * C::SLOTU;   // bytes from a slot's U row to its g row
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    const unsigned L = st.L;
-    if (!st.broken && !mbar_wait_bounded(&st.full[L & M], (L / C::kStages) & 1u, p.timeout_ns, p.bar)) {
+    if (!st.broken && !mbar_wait_bounded_at(fx, c.ph, p.timeout_ns, p.bar)) {
         record_error(p.bar, kETimedOut, kSitePipeline);
         st.broken = true;
     }
     consumers_sync<C::kCons>();
-    const float *sx = st.slots + (L & M) * C::SLOT;
-    const float *sb = st.slots + ((L - 1u) & M) * C::SLOT;
-    const float *sa = st.slots + ((L - 2u) & M) * C::SLOT;
-    const float *sz = st.slots + ((L - 3u) & M) * C::SLOT;
-    float *p1w = c.q1buf + (L & 1u) * C::SLOTU;
-    const float *p1r = c.q1buf + ((L - 1u) & 1u) * C::SLOTU;
-    float *p2w = c.q2buf + (L & 1u) * C::SLOTU;
-    const float *p2r = c.q2buf + ((L - 1u) & 1u) * C::SLOTU;
 #pragma unroll
-    for (int k = 0; k < Q; ++k) KX[k] = lds4(sx + 4 + c.o[k]);
+    for (int k = 0; k < Q; ++k) KX[k] = lds4_at(sx + k * KO);
+    const unsigned qj = QJ >= 0 ? (unsigned)QJ : (unsigned)c.qj;
+    const unsigned qr = QJ >= 0 ? (unsigned)((QJ + 2) % 3) : (c.qj == 0 ? 2u : (unsigned)c.qj - 1u);
+    const unsigned p1w = c.q + qj * RW, p1r = c.q + qr * RW;
+    const unsigned p2w = p1w + 3u * RW, p2r = p1r + 3u * RW;
     const int r1 = r - c.dir, r2 = r - 2 * c.dir;
     const bool act1 = STEADY || idx >= 2, act2 = STEADY || idx >= 4, act3 = STEADY || idx >= 6;
     const bool ring1 = !STEADY && (r1 < 1 || r1 > c.ny);
     const bool ring2 = !STEADY && (r2 < 1 || r2 > c.ny);
     // The cells beyond each strip edge: U_{k+1} at row r1, one and two
     // columns out, and U_{k+2} at row r2, one column out; a ring column (or
-    // ring row) keeps U_k at every level.  They need only the staged rows and
-    // the previous step's registers, so they come first and their loads
-    // overlap the stages; the branch is uniform per warp and the code inside
-    // it has no branches, so every lane of the warp runs it and only the
-    // edge lane's results are kept.
+    // ring row) keeps U_k at every level.  They need only the staged rows,
+    // the shared U_{k+1} row of the previous step and a short history, so
+    // one warp computes both edges, the left in its even lanes and the right
+    // in its odd ones, with the same branch-free code; lanes 0 and 1 keep
+    // their results.  Its loads overlap the stages.  The warp is the
+    // consumer warp that shares its scheduler with the (mostly sleeping)
+    // producer warp rather than with another consumer warp.
     const unsigned lane = threadIdx.x & 31u, warp = threadIdx.x >> 5;
-    if (act1 && warp == 0) {
-        const bool keep1 = ring1 || c.first_strip, keep2 = ring2 || c.first_strip;
-        float t = cell_t(sb[2], sb[4], sa[3], sx[3]);
-        float t2 = cell_t(sb[1], sb[3], sa[2], sx[2]);
+    if (act1 && warp == C::kEdgeWarp) {
+        const bool right = c.dd > 0;
+        const unsigned xe = sx + 4 * c.de, be = sb + 4 * c.de, ae = sa + 4 * c.de;
+        const unsigned o4 = 4u * (unsigned)c.dd;  // one column outward, in bytes
+        const bool outer = right ? c.last_strip : c.first_strip;
+        const bool keep1 = ring1 || outer, keep2 = ring2 || outer;
+        float t = cell_t(lds_at(be - 4u), lds_at(be + 4u), lds_at(ae), lds_at(xe));
+        float t2 = cell_t(lds_at(be + o4 - 4u), lds_at(be + o4 + 4u), lds_at(ae + o4), lds_at(xe + o4));
         if (POISSON) {
-            t = __fsub_rn(t, sb[C::SLOTU + 3]);
-            t2 = __fsub_rn(t2, sb[C::SLOTU + 2]);
+            t = __fsub_rn(t, lds_at(be + GO));
+            t2 = __fsub_rn(t2, lds_at(be + o4 + GO));
         }
-        const float v1c = keep1 ? sb[3] : __fmul_rn(0.25f, t);
-        const float v1o = keep1 ? sb[2] : __fmul_rn(0.25f, t2);
-        float t3 = cell_t(c.e_out, PB[0].x, c.e_c1, v1c);
-        if (POISSON) t3 = __fsub_rn(t3, sa[C::SLOTU + 3]);
+        const float v1c = keep1 ? lds_at(be) : __fmul_rn(0.25f, t);
+        const float v1o = keep1 ? lds_at(be + o4) : __fmul_rn(0.25f, t2);
+        // U_{k+1} at row r2 beside the edge cell: the strip's outermost
+        // interior cell (shared row) and the cell two columns out (history).
+        const float in2 = lds_at(c.qe + qr * RW - o4);
+        float t3 = cell_t(right ? in2 : c.e_out, right ? c.e_out : in2, c.e_c1, v1c);
+        if (POISSON) t3 = __fsub_rn(t3, lds_at(ae + GO));
         const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
-        if (lane == 0u) {
-            p1w[3] = v1c;
-            if (act2) p2w[3] = v2c;
-        }
-        c.e_c1 = c.e_c0;
-        c.e_c0 = v1c;
-        c.e_out = v1o;
-    }
-    if (act1 && warp == C::kCons / 32 - 1 && c.right_edge) {
-        const int m = 4 + c.cols;
-        const bool keep1 = ring1 || c.last_strip, keep2 = ring2 || c.last_strip;
-        float t = cell_t(sb[m - 1], sb[m + 1], sa[m], sx[m]);
-        float t2 = cell_t(sb[m], sb[m + 2], sa[m + 1], sx[m + 1]);
-        if (POISSON) {
-            t = __fsub_rn(t, sb[C::SLOTU + m]);
-            t2 = __fsub_rn(t2, sb[C::SLOTU + m + 1]);
-        }
-        const float v1c = keep1 ? sb[m] : __fmul_rn(0.25f, t);
-        const float v1o = keep1 ? sb[m + 1] : __fmul_rn(0.25f, t2);
-        float t3 = cell_t(PB[Q - 1].w, c.e_out, c.e_c1, v1c);
-        if (POISSON) t3 = __fsub_rn(t3, sa[C::SLOTU + m]);
-        const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
-        if (lane == 31u) {
-            p1w[m] = v1c;
-            if (act2) p2w[m] = v2c;
+        if (lane < 2u && (!right || c.right_edge)) {
+            sts_at(c.qe + qj * RW, v1c);
+            if (act2) sts_at(c.qe + (3u + qj) * RW, v2c);
         }
         c.e_c1 = c.e_c0;
         c.e_c0 = v1c;
@@ -551,9 +586,10 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
         const bool in_band = STEADY || (idx >= 4 && idx <= c.nin - 3);
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sb + C::SLOTU + 4 + o) : z4;
-            const Quad q1 = quad_t2<POISSON>(sb[3 + o], KB[k], sb[8 + o], KA[k], KX[k], g);
+            const unsigned o = k * KO;
+            const float4 g = POISSON ? lds4_at(sb + GO + o) : z4;
+            const Quad q1 = quad_t2<POISSON>(lds_at(sb + o - 4u), KB[k], lds_at(sb + o + 16u), KA[k],
+                                             KX[k], g);
             if (CHECK && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
             float4 u1 = quad_update2(q1);
             if (ring1)
@@ -561,47 +597,69 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             else if (!FULL && c.icol[k] + 3 > c.nx)
                 u1 = keep_ring_cols(u1, KB[k], c.icol[k], c.nx);
             PY[k] = u1;
-            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(p1w + 4 + o) = u1;
+            if (FULL || c.valid[k] > 0) sts4_at(p1w + o, u1);
         }
     }
+    float4 g2[Q];
+#pragma unroll
+    for (int k = 0; k < Q; ++k) g2[k] = z4;
     if (act2) {
         // Stage 2: U_{k+2} on row r2 (centre PB); west/east from the shared
         // U_{k+1} row written one step ago.
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
-            const Quad q2 = quad_t2<POISSON>(p1r[3 + o], PB[k], p1r[8 + o], PA[k], PY[k], g);
+            const unsigned o = k * KO;
+            if (POISSON) g2[k] = lds4_at(sa + GO + o);
+            const Quad q2 = quad_t2<POISSON>(lds_at(p1r + o - 4u), PB[k], lds_at(p1r + o + 16u), PA[k],
+                                             PY[k], g2[k]);
             float4 u2 = quad_update2(q2);
             if (ring2)
                 u2 = PB[k];
             else if (!FULL && c.icol[k] + 3 > c.nx)
                 u2 = keep_ring_cols(u2, PB[k], c.icol[k], c.nx);
             RY[k] = u2;
-            if (FULL || c.valid[k] > 0) *reinterpret_cast<float4 *>(p2w + 4 + o) = u2;
+            if (FULL || c.valid[k] > 0) sts4_at(p2w + o, u2);
         }
     }
+    float4 u3[Q];
     if (act3) {
         // Stage 3: U_{k+3} on row r - 3dir (centre RB), inside the band.
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
-            const int o = c.o[k];
-            const float4 g = POISSON ? lds4(sz + C::SLOTU + 4 + o) : z4;
-            const Quad q3 = quad_t2<POISSON>(p2r[3 + o], RB[k], p2r[8 + o], RA[k], RY[k], g);
+            const unsigned o = k * KO;
+            const Quad q3 = quad_t2<POISSON>(lds_at(p2r + o - 4u), RB[k], lds_at(p2r + o + 16u), RA[k],
+                                             RY[k], G3[k]);
+            u3[k] = quad_update2(q3);
+        }
+    }
+    if (STEADY || idx >= 2) {
+        // Row r - 2dir (slot sa) is no longer needed: hand it back to the TMA.
+        // The proxy fence waits for this thread's outstanding memory
+        // operations, so it comes before the step's global stores.
+        consumer_release_fence<C>();
+        __syncwarp();
+        if (lane == 0u) mbar_arrive_at(fa + 8u * C::kStages);
+    }
+    if (act3) {
+#pragma unroll
+        for (int k = 0; k < Q; ++k) {
+            float *d = c.drow + 4 * k * C::kCons;
             if (FULL)
-                *reinterpret_cast<float4 *>(c.drow + o) = quad_update2(q3);
+                *reinterpret_cast<float4 *>(d) = u3[k];
             else
-                store_quad(c.drow + o, quad_update2(q3), c.valid[k]);
+                store_quad(d, u3[k], c.valid[k]);
         }
         c.drow += c.dstep;
     }
-    if (STEADY || idx >= 3) {
-        // Row r - 3dir is no longer needed: hand its slot back to the TMA.
-        fence_proxy_async_shared();
-        __syncwarp();
-        if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 3u) & M]);
+    if (POISSON) {
+#pragma unroll
+        for (int k = 0; k < Q; ++k) G3[k] = g2[k];
     }
-    st.L = L + 1u;
+    // The next row's slot and barrier take the roles just released.
+    const bool wrap = sx == c.slot_last;
+    sa = wrap ? c.slot_first : sx + 4u * C::SLOT;
+    fa = wrap ? c.full0 : fx + 8u;
+    c.ph ^= wrap ? 1u : 0u;
 }
 
 template <class C, bool POISSON, bool CHECK, bool FULL>
@@ -611,24 +669,33 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
                                             float4 (&pa)[C::kQPT], float4 (&pb)[C::kQPT],
                                             float4 (&py)[C::kQPT], float4 (&ra)[C::kQPT],
                                             float4 (&rb)[C::kQPT], float4 (&ry)[C::kQPT],
+                                            unsigned &sa, unsigned &sb, unsigned &sx, unsigned &fa,
+                                            unsigned &fb, unsigned &fx, float4 (&g3)[C::kQPT],
                                             double &s2, float &rmax) {
     const int dir = c.dir;
+    // The steady rows start at idx 6, so the unrolled steps' shared rows
+    // are 0, 1 and 2.
     for (; steady >= 3; steady -= 3) {
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry,
-                                                 s2, rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 1, r + dir, kb, kx, ka, pb, py, pa,
-                                                 rb, ry, ra, s2, rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, py, pa,
-                                                 pb, ry, ra, rb, s2, rmax);
+        seg3_step<C, POISSON, CHECK, true, FULL, 0>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
+                                                    ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
+        seg3_step<C, POISSON, CHECK, true, FULL, 1>(p, c, st, idx + 1, r + dir, kb, kx, ka, pb, py,
+                                                    pa, rb, ry, ra, sb, sx, sa, fb, fx, fa, g3, s2,
+                                                    rmax);
+        seg3_step<C, POISSON, CHECK, true, FULL, 2>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, py,
+                                                    pa, pb, ry, ra, rb, sx, sa, sb, fx, fa, fb, g3,
+                                                    s2, rmax);
         idx += 3;
         r += 3 * dir;
     }
     for (; steady > 0; --steady, ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry,
-                                                 s2, rmax);
+        seg3_step<C, POISSON, CHECK, true, FULL, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
+                                                     ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
         rotate3(ra, rb, ry);
+        rotate3v(sa, sb, sx);
+        rotate3v(fa, fb, fx);
+        c.qj = c.qj == 2 ? 0 : c.qj + 1;
     }
 }
 
@@ -638,12 +705,24 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
                                                  StreamState &st, float *qbuf, double &s2,
                                                  float &rmax) {
     constexpr int Q = C::kQPT;
+    constexpr unsigned M = C::kStages - 1;
+    const int t = (int)threadIdx.x;
+    const unsigned lane = threadIdx.x & 31u;
     Seg3<Q> c;
-    c.q1buf = qbuf;
-    c.q2buf = qbuf + 2 * C::SLOTU;
+    const unsigned qbase = smem_u32(qbuf);
+    const unsigned sbase = smem_u32(st.slots);
+    c.q = qbase + 4u * (4u + 4u * (unsigned)t);
+    const bool right = (lane & 1u) != 0u;
+    const int e = right ? 4 + cols : 3;
+    c.dd = right ? 1 : -1;
+    c.de = e - (4 + 4 * t);
+    c.qe = qbase + 4u * (unsigned)e;
+    c.slot_first = sbase + 4u * (4u + 4u * (unsigned)t);
+    c.slot_last = c.slot_first + 4u * C::SLOT * M;
+    c.full0 = smem_u32(st.full);
+    c.qj = 0;
     c.dir = dir;
     c.cols = cols;
-    c.col0 = col0;
     c.nin = (dir > 0 ? jb - ja : ja - jb) + 7;
     c.nx = p.nx;
     c.ny = p.ny;
@@ -651,26 +730,36 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     c.last_strip = col0 + cols >= p.nx;
     c.right_edge = (cols & 3) == 0;
     c.dstep = (long long)dir * p.pitch;
-    c.drow = dst + (long long)ja * p.pitch + col0 + 4;
+    c.drow = dst + (long long)ja * p.pitch + col0 + 4 + 4 * t;
     c.e_c0 = c.e_c1 = c.e_out = 0.f;
 #pragma unroll
     for (int k = 0; k < Q; ++k) {
-        c.o[k] = 4 * ((int)threadIdx.x + k * C::kCons);
-        c.valid[k] = max(0, min(4, cols - c.o[k]));
-        c.icol[k] = (int)col0 + 1 + c.o[k];
+        const int o = 4 * (t + k * C::kCons);
+        c.valid[k] = max(0, min(4, cols - o));
+        c.icol[k] = (int)col0 + 1 + o;
     }
+    // Ring cursor: the segment's first input row takes slot L0 & M.
+    const unsigned L0 = st.L;
+    unsigned sx = c.slot_first + 4u * C::SLOT * (L0 & M), sb = sx, sa = sx;
+    unsigned fx = c.full0 + 8u * (L0 & M), fb = fx, fa = fx;
+    c.ph = (L0 / C::kStages) & 1u;
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-    float4 ka[Q], kb[Q], kx[Q], pa[Q], pb[Q], py[Q], ra[Q], rb[Q], ry[Q];
+    float4 ka[Q], kb[Q], kx[Q], pa[Q], pb[Q], py[Q], ra[Q], rb[Q], ry[Q], g3[Q];
 #pragma unroll
-    for (int k = 0; k < Q; ++k) ka[k] = kb[k] = kx[k] = pa[k] = pb[k] = py[k] = ra[k] = rb[k] = ry[k] = z4;
+    for (int k = 0; k < Q; ++k)
+        ka[k] = kb[k] = kx[k] = pa[k] = pb[k] = py[k] = ra[k] = rb[k] = ry[k] = g3[k] = z4;
     int idx = 0;
     int r = ja - 3 * dir;
     // Prologue: the first six input rows (stages start at idx 2, 4 and 6).
     for (; idx < 6; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry, s2, rmax);
+        seg3_step<C, POISSON, CHECK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
+                                                       rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
         rotate3(ra, rb, ry);
+        rotate3v(sa, sb, sx);
+        rotate3v(fa, fb, fx);
+        c.qj = c.qj == 2 ? 0 : c.qj + 1;
     }
     // Steady rows 6 .. nin-3.
     const int steady = c.nin - 8 > 0 ? c.nin - 8 : 0;
@@ -682,25 +771,29 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     // rows run through the rolled generic step below.
     if (cols == C::TW)
         seg3_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
-                                             ry, s2, rmax);
+                                             ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
     else if constexpr (!POISSON)
         seg3_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
-                                              rb, ry, s2, rmax);
+                                              rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
     // The last input rows: stages 1 and 2 reach beyond the band (maybe the ring).
     for (; idx < c.nin; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb, ry, s2, rmax);
+        seg3_step<C, POISSON, CHECK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
+                                                       rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
         rotate3(ra, rb, ry);
+        rotate3v(sa, sb, sx);
+        rotate3v(fa, fb, fx);
+        c.qj = c.qj == 2 ? 0 : c.qj + 1;
     }
-    // The last three input rows' slots.
-    fence_proxy_async_shared();
+    // The last two input rows' slots (now in roles a and b).
+    consumer_release_fence<C>();
     __syncwarp();
-    if ((threadIdx.x & 31u) == 0u) {
-        mbar_arrive(&st.empty[(st.L - 3u) & (C::kStages - 1)]);
-        mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
-        mbar_arrive(&st.empty[(st.L - 1u) & (C::kStages - 1)]);
+    if (lane == 0u) {
+        mbar_arrive_at(fa + 8u * C::kStages);
+        mbar_arrive_at(fb + 8u * C::kStages);
     }
+    st.L = L0 + (unsigned)c.nin;
 }
 
 template <class C, bool POISSON, bool CHECK, bool STORE, int D>
