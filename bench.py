@@ -419,11 +419,11 @@ def latency_extras(pk):
                                        "redblack_iterations": rb["sweeps_done"],
                                        "jacobi_us": jac["device_us"], "redblack_us": rb["device_us"]},
     }
-    # Temporal blocking: two sweeps per HBM pass, same bits (16384^2, 100 sweeps)
+    # Temporal blocking: one, two and three sweeps per HBM pass, same bits (16384^2, 100 sweeps)
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
     for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 8),
-                      ("three_sweeps_per_pass", 11)):
+                      ("three_sweeps_per_pass", 10)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):

@@ -232,15 +232,14 @@ long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_c
 
 constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
 // Multi-sweep shape for persistent runs, from measurements on GB300
-// (16384^2 and 8192^2).  Laplace takes three sweeps per pass, {1 float4/
-// thread, 8-deep ring, 224 consumers, 2 CTAs/SM}: 145.6 us/sweep against
-// 163.3 for the best two-sweep shape.  Poisson, whose ring slots also carry
-// the source row, takes three sweeps with {1, 16-deep ring, 256 consumers,
-// 1 CTA/SM} from 8192 columns on (219.9 against 232.4 at 16384^2), and two
-// with {1, 8} below, where the passes are short (4096^2: 24.4 against 25.0).
-int default_multi_sweep_shape(bool poisson, int nx) {
-    if (!poisson) return 11;
-    return nx >= 8192 ? 12 : 6;
+// (16384^2, 8192^2 and 4096^2, 100 sweeps).  Both take three sweeps per pass.
+// Laplace: {1 float4/thread, 16-deep ring, 224 consumers, 2 CTAs/SM}, 123.9
+// us/sweep at 16384^2 against 128.2 with an 8-deep ring and 163.1 for the
+// best two-sweep shape.  Poisson, whose ring slots also carry the source
+// row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 175.9 at 16384^2 and 13.4
+// at 4096^2 (the best two-sweep shape: 249.1 and 17.0).
+int default_multi_sweep_shape(bool poisson, int /*nx*/) {
+    return poisson ? 12 : 10;
 }
 
 int ensure_partials(pk_ctx *ctx, int grid) {

@@ -50,10 +50,11 @@ struct SCfg {
     static constexpr int kEdgeWarp = 3;
     // Where the generic-proxy reads of a ring slot are fenced against its
     // TMA refill: in each consumer warp before it releases the slot, or once
-    // per row in the producer after it acquires the release.  Measured: the
-    // producer side is faster for the one-CTA-per-SM three-sweep shape, the
-    // consumer side for the two-CTA shapes.
-    static constexpr bool kProducerFence = DEPTH == 3 && MINB == 1;
+    // per row in the producer after it acquires the release.  Measured at
+    // 16384^2: for the three-sweep shapes the consumer-side fence costs 13%
+    // and the producer-side one about 1%; the two-sweep shape, which runs at
+    // the copy bandwidth, slows by 7% with the producer-side fence.
+    static constexpr bool kProducerFence = DEPTH == 3;
     static_assert(DEPTH < 3 || CONS / 32 > kEdgeWarp, "three-sweep shapes: at least four consumer warps");
     static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
     static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three sweeps per pass");
