@@ -49,11 +49,13 @@ struct SCfg {
     // CONS / 32).
     static constexpr int kEdgeWarp = 3;
     // Where the generic-proxy reads of a ring slot are fenced against its
-    // TMA refill: in each consumer warp before it releases the slot, or once
-    // per row in the producer after it acquires the release.  Measured at
-    // 16384^2: for the three-sweep shapes the consumer-side fence costs 13%
-    // and the producer-side one about 1%; the two-sweep shape, which runs at
-    // the copy bandwidth, slows by 7% with the producer-side fence.
+    // TMA refill.  The one- and two-sweep steps fence in each consumer warp
+    // before it releases the slot.  The three-sweep step releases a slot only
+    // after it has used every value it loaded from it, and the producer
+    // fences once per row after it acquires the release.  Measured at
+    // 16384^2: the consumer-side fence cost the three-sweep shapes 13%, the
+    // producer-side one about 1%; the two-sweep shape, which runs at the
+    // copy bandwidth, slows by 7% with a producer-side fence.
     static constexpr bool kProducerFence = DEPTH == 3;
     static_assert(DEPTH < 3 || CONS / 32 > kEdgeWarp, "three-sweep shapes: at least four consumer warps");
     static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
@@ -89,12 +91,6 @@ __device__ __forceinline__ StreamState stream_setup(unsigned char *smem) {
 
 __device__ __forceinline__ float4 lds4(const float *p) {
     return *reinterpret_cast<const float4 *>(p);
-}
-
-// The consumer half of the slot-release fencing (see SCfg::kProducerFence).
-template <class C>
-__device__ __forceinline__ void consumer_release_fence() {
-    if constexpr (!C::kProducerFence) fence_proxy_async_shared();
 }
 
 // Producer: input rows ja - D*dir .. jb + D*dir of strip columns
@@ -189,8 +185,10 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
             xg[k] = gin ? lds4(su + C::SLOTU + 4 + o) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         // Release the slot only once this thread's reads of it are complete
-        // with respect to the async proxy that will refill it.
-        consumer_release_fence<C>();
+        // with respect to the async proxy that will refill it.  The values
+        // just loaded are used only after the release, so this fence is
+        // what keeps a pending ld.shared from being overtaken by the refill.
+        fence_proxy_async_shared();
         __syncwarp();
         if (lane == 0u) mbar_arrive(&st.empty[slot]);
         ++st.L;
@@ -343,7 +341,7 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
     }
     if (STEADY || idx >= 2) {
         // Row r - 2dir is no longer needed: hand its slot back to the TMA.
-        consumer_release_fence<C>();
+        fence_proxy_async_shared();
         __syncwarp();
         if ((threadIdx.x & 31u) == 0u) mbar_arrive(&st.empty[(L - 2u) & M]);
     }
@@ -432,7 +430,7 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
     // Last input row: stage 1 on the row beyond the band (maybe the ring).
     seg2_step<C, POISSON, CHECK, false>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
     // The last two input rows' slots.
-    consumer_release_fence<C>();
+    fence_proxy_async_shared();
     __syncwarp();
     if ((threadIdx.x & 31u) == 0u) {
         mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
@@ -634,10 +632,11 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
         }
     }
     if (STEADY || idx >= 2) {
-        // Row r - 2dir (slot sa) is no longer needed: hand it back to the TMA.
-        // The proxy fence waits for this thread's outstanding memory
-        // operations, so it comes before the step's global stores.
-        consumer_release_fence<C>();
+        // Row r - 2dir (slot sa) is no longer needed: hand it back to the
+        // TMA.  Every value this thread loaded from the slot has been used
+        // by an instruction issued before this point, so no load from it is
+        // still pending; the producer's proxy fence orders the reads before
+        // the refill.
         __syncwarp();
         if (lane == 0u) mbar_arrive_at(fa + 8u * C::kStages);
     }
@@ -788,7 +787,6 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
         c.qj = c.qj == 2 ? 0 : c.qj + 1;
     }
     // The last two input rows' slots (now in roles a and b).
-    consumer_release_fence<C>();
     __syncwarp();
     if (lane == 0u) {
         mbar_arrive_at(fa + 8u * C::kStages);
