@@ -154,14 +154,17 @@ inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 
 // A ring slot: the U row segment (4 halo floats each side) and, for
 // Poisson, the g row segment with a 4-float margin each side.  A shape of
-// D sweeps per pass adds shared rows for each of U_{k+1} .. U_{k+D-1}, laid
-// out like the U part of a slot: two per level for D = 2, three for D = 3.
+// D sweeps per pass adds shared rows for each of U_{k+1} .. U_{k+D-1}: for
+// D = 2 two per level, laid out like the U part of a slot; for D = 3 three
+// per level, each the last and the first cell of every quad (two arrays of
+// tw/4 + 1 floats, rounded up to a multiple of four).
 inline size_t stream_smem_bytes(int cfg, bool poisson) {
     const int tw = stream_tw(cfg);
     const int depth = stream_depth(cfg);
     const size_t slot = (size_t)(tw + 8 + (poisson ? tw + 8 : 0)) * sizeof(float);
-    const size_t per_level = depth >= 3 ? 3 : 2;
-    const size_t qrows = per_level * (size_t)(depth - 1) * (size_t)(tw + 8) * sizeof(float);
+    const size_t nh = (size_t)((tw / 4 + 1 + 3) & ~3);
+    const size_t qrows = depth >= 3 ? 3 * (size_t)(depth - 1) * 2 * nh * sizeof(float)
+                                    : 2 * (size_t)(depth - 1) * (size_t)(tw + 8) * sizeof(float);
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 

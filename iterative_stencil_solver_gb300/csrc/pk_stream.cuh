@@ -44,6 +44,9 @@ struct SCfg {
     static constexpr int TW = 4 * QPT * CONS;
     static constexpr int SLOTU = TW + 8;
     static constexpr int SLOT = SLOTU + (POISSON ? TW + 8 : 0);
+    // Three-sweep passes share each U_{k+1} / U_{k+2} row as two arrays of
+    // NH floats: the last cell of every quad, then the first (see Seg3).
+    static constexpr int NH = (QPT * CONS + 1 + 3) & ~3;
     // Three-sweep passes: the consumer warp that computes the strip-edge
     // cells (warps w and w + 4 share a scheduler; the producer is warp
     // CONS / 32).
@@ -442,9 +445,11 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
 // ja-3dir .. jb+3dir of U_k; stage 1 computes U_{k+1} on rows ja-2dir ..
 // jb+2dir, stage 2 U_{k+2} on rows ja-dir .. jb+dir, stage 3 writes U_{k+3}
 // on rows ja .. jb.  Each thread keeps its quads of the last three rows of
-// U_k, U_{k+1} and U_{k+2} in registers; the CTA shares each new U_{k+1} and
-// U_{k+2} row through three shared rows per level (the row of input step i
-// in row i mod 3), with the one named barrier per input row.  The cells
+// U_k, U_{k+1} and U_{k+2} in registers; the CTA shares the first and last
+// cell of every quad of each new U_{k+1} and U_{k+2} row (the west and east
+// neighbours other threads need) through three shared rows per level (the
+// row of input step i in row i mod 3), with the one named barrier per input
+// row.  The cells
 // beyond a strip edge that later stages read are U_{k+1} two columns out and
 // U_{k+2} one column out; one warp computes them from the staged U_k rows, a
 // shared U_{k+1} row and a short history.  A ring slot is held for three
@@ -455,15 +460,17 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
 //
 // The step keeps every shared-memory position as a 32-bit shared-window
 // address: this thread's quad in the three ring slots it reads, their full
-// barriers, and its quad in shared row 0.  The three-step unrolled loop
+// barriers, and its cells in shared row 0.  The three-step unrolled loop
 // renames the slot roles and fixes each step's shared rows at compile time,
 // so a step spends a compare and two selects on ring bookkeeping.
 template <int Q>
 struct Seg3 {
-    unsigned q;           // this thread's first quad in shared row 0 (U_{k+1}
-                          // rows 0..2, U_{k+2} rows 3..5, SLOTU floats apart)
-    unsigned qe;          // edge warp: its lane's edge cell in shared row 0
-    int de;               // edge warp: that cell, in floats from this thread's first quad
+    unsigned h;           // shared row 0's last-cell array + 4 * (this thread's
+                          // first quad); U_{k+1} rows 0..2, U_{k+2} rows 3..5
+    unsigned he_w;        // edge warp: where its lane's edge cell goes in row 0
+    unsigned he_r;        // edge warp: the strip's outermost interior cell in row 0
+    int de;               // edge warp: its lane's edge cell in a ring slot, in floats
+                          // from this thread's first quad
     int dd;               // edge warp: outward direction, -1 (left edge) or +1 (right)
     unsigned slot_first;  // this thread's first quad in ring slot 0
     unsigned slot_last;   // ... in ring slot kStages-1
@@ -524,7 +531,8 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
                                           double &s2, float &rmax) {
     constexpr int Q = C::kQPT;
     constexpr unsigned KO = 16u * C::kCons;  // bytes from one quad of a thread to its next
-    constexpr unsigned RW = 4u * C::SLOTU;   // bytes between shared rows
+    constexpr unsigned NHB = 4u * C::NH;     // bytes from a row's last-cell to its first-cell array
+    constexpr unsigned RW = 2u * NHB;        // bytes between shared rows
     constexpr unsigned GO = 4u * C::SLOTU;   // bytes from a slot's U row to its g row
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!st.broken && !mbar_wait_bounded_at(fx, c.ph, p.timeout_ns, p.bar)) {
@@ -536,7 +544,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
     for (int k = 0; k < Q; ++k) KX[k] = lds4_at(sx + k * KO);
     const unsigned qj = QJ >= 0 ? (unsigned)QJ : (unsigned)c.qj;
     const unsigned qr = QJ >= 0 ? (unsigned)((QJ + 2) % 3) : (c.qj == 0 ? 2u : (unsigned)c.qj - 1u);
-    const unsigned p1w = c.q + qj * RW, p1r = c.q + qr * RW;
+    const unsigned p1w = c.h + qj * RW, p1r = c.h + qr * RW;
     const unsigned p2w = p1w + 3u * RW, p2r = p1r + 3u * RW;
     const int r1 = r - c.dir, r2 = r - 2 * c.dir;
     const bool act1 = STEADY || idx >= 2, act2 = STEADY || idx >= 4, act3 = STEADY || idx >= 6;
@@ -568,13 +576,13 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
         const float v1o = keep1 ? lds_at(be + o4) : __fmul_rn(0.25f, t2);
         // U_{k+1} at row r2 beside the edge cell: the strip's outermost
         // interior cell (shared row) and the cell two columns out (history).
-        const float in2 = lds_at(c.qe + qr * RW - o4);
+        const float in2 = lds_at(c.he_r + qr * RW);
         float t3 = cell_t(right ? in2 : c.e_out, right ? c.e_out : in2, c.e_c1, v1c);
         if (POISSON) t3 = __fsub_rn(t3, lds_at(ae + GO));
         const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
         if (lane < 2u && (!right || c.right_edge)) {
-            sts_at(c.qe + qj * RW, v1c);
-            if (act2) sts_at(c.qe + (3u + qj) * RW, v2c);
+            sts_at(c.he_w + qj * RW, v1c);
+            if (act2) sts_at(c.he_w + (3u + qj) * RW, v2c);
         }
         c.e_c1 = c.e_c0;
         c.e_c0 = v1c;
@@ -586,6 +594,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
             const unsigned o = k * KO;
+            const unsigned ho = 4u * k * C::kCons;
             const float4 g = POISSON ? lds4_at(sb + GO + o) : z4;
             const Quad q1 = quad_t2<POISSON>(lds_at(sb + o - 4u), KB[k], lds_at(sb + o + 16u), KA[k],
                                              KX[k], g);
@@ -596,7 +605,10 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             else if (!FULL && c.icol[k] + 3 > c.nx)
                 u1 = keep_ring_cols(u1, KB[k], c.icol[k], c.nx);
             PY[k] = u1;
-            if (FULL || c.valid[k] > 0) sts4_at(p1w + o, u1);
+            if (FULL || c.valid[k] > 0) {
+                sts_at(p1w + ho + 4u, u1.w);
+                sts_at(p1w + ho + NHB, u1.x);
+            }
         }
     }
     float4 g2[Q];
@@ -608,8 +620,9 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
             const unsigned o = k * KO;
+            const unsigned ho = 4u * k * C::kCons;
             if (POISSON) g2[k] = lds4_at(sa + GO + o);
-            const Quad q2 = quad_t2<POISSON>(lds_at(p1r + o - 4u), PB[k], lds_at(p1r + o + 16u), PA[k],
+            const Quad q2 = quad_t2<POISSON>(lds_at(p1r + ho), PB[k], lds_at(p1r + ho + NHB + 4u), PA[k],
                                              PY[k], g2[k]);
             float4 u2 = quad_update2(q2);
             if (ring2)
@@ -617,7 +630,10 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             else if (!FULL && c.icol[k] + 3 > c.nx)
                 u2 = keep_ring_cols(u2, PB[k], c.icol[k], c.nx);
             RY[k] = u2;
-            if (FULL || c.valid[k] > 0) sts4_at(p2w + o, u2);
+            if (FULL || c.valid[k] > 0) {
+                sts_at(p2w + ho + 4u, u2.w);
+                sts_at(p2w + ho + NHB, u2.x);
+            }
         }
     }
     float4 u3[Q];
@@ -625,8 +641,8 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
         // Stage 3: U_{k+3} on row r - 3dir (centre RB), inside the band.
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
-            const unsigned o = k * KO;
-            const Quad q3 = quad_t2<POISSON>(lds_at(p2r + o - 4u), RB[k], lds_at(p2r + o + 16u), RA[k],
+            const unsigned ho = 4u * k * C::kCons;
+            const Quad q3 = quad_t2<POISSON>(lds_at(p2r + ho), RB[k], lds_at(p2r + ho + NHB + 4u), RA[k],
                                              RY[k], G3[k]);
             u3[k] = quad_update2(q3);
         }
@@ -709,14 +725,22 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     const int t = (int)threadIdx.x;
     const unsigned lane = threadIdx.x & 31u;
     Seg3<Q> c;
-    const unsigned qbase = smem_u32(qbuf);
+    const unsigned hbase = smem_u32(qbuf);
     const unsigned sbase = smem_u32(st.slots);
-    c.q = qbase + 4u * (4u + 4u * (unsigned)t);
+    // A shared row: last[i + 1] = last cell of quad i (last[0]: the cell left
+    // of the strip), then first[i] = first cell of quad i (first[nq]: the
+    // cell right of the strip).  Quad i reads its west neighbour at last[i]
+    // and its east one at first[i + 1]: consecutive words across a warp.
+    c.h = hbase + 4u * (unsigned)t;
     const bool right = (lane & 1u) != 0u;
     const int e = right ? 4 + cols : 3;
     c.dd = right ? 1 : -1;
     c.de = e - (4 + 4 * t);
-    c.qe = qbase + 4u * (unsigned)e;
+    // The right edge cell is written only when cols is a multiple of 4; the
+    // odd lanes read and write at a 4-byte-aligned place either way.
+    const unsigned cq = (unsigned)(cols & ~3);
+    c.he_w = right ? hbase + 4u * C::NH + cq : hbase;
+    c.he_r = right ? hbase + cq : hbase + 4u * C::NH;
     c.slot_first = sbase + 4u * (4u + 4u * (unsigned)t);
     c.slot_last = c.slot_first + 4u * C::SLOT * M;
     c.full0 = smem_u32(st.full);
