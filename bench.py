@@ -423,7 +423,7 @@ def latency_extras(pk):
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
     for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 8),
-                      ("three_sweeps_per_pass", 10)):
+                      ("three_sweeps_per_pass", 11)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):

@@ -135,8 +135,8 @@ typedef struct {
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
     int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs of
-                                         two or more sweeps shape 10 (Laplace) or 12
-                                         (Poisson); shape 3 for the rest and
+                                         two or more sweeps shape 11 (Laplace, nx > 8192),
+                                         10 (Laplace) or 12 (Poisson); shape 3 for the rest and
                                          for the per-launch and graph paths
                                          (pk_run_info.stream_config says which ran).  Index into
                                          {float4 groups per thread, TMA ring depth, sweeps

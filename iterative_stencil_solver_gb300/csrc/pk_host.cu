@@ -231,15 +231,18 @@ long long stream_rows(const pk_ctx *ctx, int cfg) {
 long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_cfg); }
 
 constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
-// Multi-sweep shape for persistent runs, from measurements on GB300
-// (16384^2, 8192^2 and 4096^2, 100 sweeps).  Both take three sweeps per pass.
-// Laplace: {1 float4/thread, 16-deep ring, 224 consumers, 2 CTAs/SM}, 123.9
-// us/sweep at 16384^2 against 128.2 with an 8-deep ring and 163.1 for the
-// best two-sweep shape.  Poisson, whose ring slots also carry the source
-// row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 175.9 at 16384^2 and 13.4
-// at 4096^2 (the best two-sweep shape: 249.1 and 17.0).
-int default_multi_sweep_shape(bool poisson, int /*nx*/) {
-    return poisson ? 12 : 10;
+// Multi-sweep shape for persistent runs, from measurements on GB300 (100
+// sweeps, us/sweep).  Both take three sweeps per pass.  Laplace: {1 float4/
+// thread, 224 consumers, 2 CTAs/SM} with an 8-deep ring above 8192 columns
+// (16384^2: 121.5 against 123.4 with a 16-deep ring and 128.2 for one CTA of
+// 256 consumers per SM), the 16-deep ring up to 8192 (8192^2: 33.8 against
+// 34.3; 4096^2: 9.56 against 10.0).  Poisson, whose ring slots also carry the
+// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 170.3 at 16384^2,
+// 43.0 at 8192^2 and 12.8 at 4096^2 (the best two-sweep shape: 249.1 and
+// 17.0 at 16384^2 and 4096^2).
+int default_multi_sweep_shape(bool poisson, int nx) {
+    if (poisson) return 12;
+    return nx > 8192 ? 11 : 10;
 }
 
 int ensure_partials(pk_ctx *ctx, int grid) {

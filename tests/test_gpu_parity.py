@@ -462,8 +462,8 @@ DEFAULT_SHAPE_RUNS = [
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    # three sweeps per pass: shape 10 for Laplace, 12 for Poisson
-    multi = 12 if poisson else 10
+    # three sweeps per pass: shape 12 for Poisson; for Laplace 11 above 8192 columns, else 10
+    multi = 12 if poisson else (11 if nx > 8192 else 10)
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
         shape = multi if shape == MULTI else shape
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
