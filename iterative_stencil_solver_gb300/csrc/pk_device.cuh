@@ -449,6 +449,51 @@ __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid
     }
 }
 
+// Per-thread residual accumulator of the three-sweep STREAM step: the sum
+// of r^2 as an unevaluated pair of floats.  Each square is split exactly
+// into p + e (p = fl(r*r), e = fma(r, r, -p)); p joins hi through an
+// error-free two-sum whose error, with e, goes to lo.  Over the few hundred
+// cells a thread checks per segment the pair carries about 44 significant
+// bits, far inside the 1e-10 relative agreement the residual is held to,
+// and costs only fp32 arithmetic (fp64 runs at a small fraction of the fp32
+// rate on this GPU).  Squares whose split could underflow or overflow in
+// fp32 (0 < |r| < 2^-50, |r| >= 2^60) go to a double instead.
+struct ResFF {
+    float hi, lo;
+    double wide;
+};
+__device__ __forceinline__ void resff_add(ResFF &a, float r) {
+    const float m = fabsf(r);
+    if (m != 0.f && (m < 0x1p-50f || m >= 0x1p60f)) {
+        const double rd = (double)r;
+        a.wide = __dadd_rn(a.wide, __dmul_rn(rd, rd));
+        return;
+    }
+    const float p = __fmul_rn(r, r);
+    const float e = __fmaf_rn(r, r, -p);
+    const float s = __fadd_rn(a.hi, p);
+    const float bp = __fsub_rn(s, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    a.hi = s;
+    a.lo = __fadd_rn(a.lo, __fadd_rn(err, e));
+}
+__device__ __forceinline__ double resff_value(const ResFF &a) {
+    return __dadd_rn(__dadd_rn((double)a.hi, (double)a.lo), a.wide);
+}
+__device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, ResFF &acc,
+                                              float &rmax) {
+    const float tv[4] = {q.t0, q.t1, q.t2, q.t3};
+    const float cv[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        if (k < valid) {
+            const float r = __fsub_rn(tv[k], __fmul_rn(4.0f, cv[k]));
+            resff_add(acc, r);
+            rmax = fmaxf(rmax, fabsf(r));
+        }
+    }
+}
+
 // Store the first `valid` (1..4) cells of v at p (16-byte aligned).
 __device__ __forceinline__ void store_quad(float *p, float4 v, int valid) {
     if (valid >= 4) {

@@ -528,7 +528,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
                                           float4 (&RB)[C::kQPT], float4 (&RY)[C::kQPT],
                                           unsigned &sa, unsigned &sb, unsigned &sx, unsigned &fa,
                                           unsigned &fb, unsigned &fx, float4 (&G3)[C::kQPT],
-                                          double &s2, float &rmax) {
+                                          ResFF &s2, float &rmax) {
     constexpr int Q = C::kQPT;
     constexpr unsigned KO = 16u * C::kCons;  // bytes from one quad of a thread to its next
     constexpr unsigned NHB = 4u * C::NH;     // bytes from a row's last-cell to its first-cell array
@@ -687,7 +687,7 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
                                             float4 (&rb)[C::kQPT], float4 (&ry)[C::kQPT],
                                             unsigned &sa, unsigned &sb, unsigned &sx, unsigned &fa,
                                             unsigned &fb, unsigned &fx, float4 (&g3)[C::kQPT],
-                                            double &s2, float &rmax) {
+                                            ResFF &s2, float &rmax) {
     const int dir = c.dir;
     // The steady rows start at idx 6, so the unrolled steps' shared rows
     // are 0, 1 and 2.
@@ -718,8 +718,10 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
 template <class C, bool POISSON, bool CHECK>
 __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *dst, int ja, int jb,
                                                  int dir, int cols, long long col0,
-                                                 StreamState &st, float *qbuf, double &s2,
+                                                 StreamState &st, float *qbuf, double &s2_out,
                                                  float &rmax) {
+    // The residual of this segment's cells, added to s2_out at the end.
+    ResFF s2 = {0.f, 0.f, 0.0};
     constexpr int Q = C::kQPT;
     constexpr unsigned M = C::kStages - 1;
     const int t = (int)threadIdx.x;
@@ -817,6 +819,7 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
         mbar_arrive_at(fb + 8u * C::kStages);
     }
     st.L = L0 + (unsigned)c.nin;
+    if (CHECK) s2_out = __dadd_rn(s2_out, resff_value(s2));
 }
 
 template <class C, bool POISSON, bool CHECK, bool STORE, int D>

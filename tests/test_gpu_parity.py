@@ -441,6 +441,26 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
             check_info(info, oinfo)
 
 
+# The three-sweep step accumulates the residual's squares as a pair of floats
+# and sends squares that could underflow or overflow in fp32 to a double: a
+# field scaled far down puts every cell there, one scaled to the boundary of
+# the range mixes both kinds, and one scaled far up overflows r^2 in fp32.
+@pytest.mark.parametrize("cfg", [10, 11, 12])
+@pytest.mark.parametrize("scale", [1e-20, 3e-15, 1e25], ids=["tiny", "mixed", "huge"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_three_sweep_residual_extreme_scales(pk, cfg, scale, poisson):
+    nx, ny = 2053, 37
+    u0 = (inputs.random_field(nx, ny, seed=77) * np.float32(scale)).astype(np.float32)
+    f = (inputs.uniform_pm1(78, nx * ny).reshape(ny, nx) * np.float32(scale)).astype(np.float32) \
+        if poisson else None
+    for n, ce in [(9, 3), (12, 6)]:
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=1e-30, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, 1e-30, ce, variant=2, stream_config=cfg)
+        assert info["sweeps_per_pass"] == 3
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
 # The default STREAM plan: persistent runs whose passes can take two sweeps
 # use the two-sweep shape; the others, and the per-launch path, keep the
 # single-sweep shape.  Either way the bits are those of single sweeps.
