@@ -433,24 +433,8 @@ __device__ __forceinline__ float4 quad_update2(const Quad &q) {
     return make_float4(u01.x, u01.y, u23.x, u23.y);
 }
 
-// Residual accumulation over the first `valid` cells of the quad.
-__device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, double &s2,
-                                              float &rmax) {
-    const float tv[4] = {q.t0, q.t1, q.t2, q.t3};
-    const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (k < valid) {
-            const float r = __fsub_rn(tv[k], __fmul_rn(4.0f, cv[k]));
-            const double rd = (double)r;
-            s2 = __dadd_rn(s2, __dmul_rn(rd, rd));
-            rmax = fmaxf(rmax, fabsf(r));
-        }
-    }
-}
-
-// Per-thread residual accumulator of the three-sweep STREAM step: the sum
-// of r^2 as an unevaluated pair of floats.  Each square is split exactly
+// Per-thread residual accumulator of the sweep kernels: the sum of r^2 as an
+// unevaluated pair of floats.  Each square is split exactly
 // into p + e (p = fl(r*r), e = fma(r, r, -p)); p joins hi through an
 // error-free two-sum whose error, with e, goes to lo.  Over the few hundred
 // cells a thread checks per segment the pair carries about 44 significant
@@ -492,6 +476,15 @@ __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid
             rmax = fmaxf(rmax, fabsf(r));
         }
     }
+}
+
+// The same for one quad into a double (the small-grid kernels): the quad's
+// squares summed as a pair, then added once.
+__device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, double &s2,
+                                              float &rmax) {
+    ResFF a = {0.f, 0.f, 0.0};
+    quad_residual(q, c, valid, a, rmax);
+    s2 = __dadd_rn(s2, resff_value(a));
 }
 
 // Store the first `valid` (1..4) cells of v at p (16-byte aligned).

@@ -46,6 +46,7 @@ __device__ __forceinline__ void pass_direct(const SweepParams &p, const float *_
                                             unsigned stride, double &s2, float &rmax) {
     const unsigned nq = (unsigned)(p.nx + 3) >> 2;
     const unsigned units = (unsigned)p.ny * nq;
+    ResFF acc = {0.f, 0.f, 0.0};
     for (unsigned u = first; u < units; u += stride) {
         const unsigned jm1 = u / nq;
         const unsigned q = u - jm1 * nq;
@@ -61,8 +62,9 @@ __device__ __forceinline__ void pass_direct(const SweepParams &p, const float *_
         const int valid = min(4, p.nx - 4 * (int)q);
         const Quad t = quad_t<POISSON>(W, C, E, S, N, G);
         if (STORE) store_quad(dst + off, quad_update(t), valid);
-        if (CHECK) quad_residual(t, C, valid, s2, rmax);
+        if (CHECK) quad_residual(t, C, valid, acc, rmax);
     }
+    if (CHECK) s2 = __dadd_rn(s2, resff_value(acc));
 }
 
 template <bool POISSON>

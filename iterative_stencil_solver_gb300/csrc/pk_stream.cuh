@@ -152,10 +152,11 @@ __device__ __forceinline__ void produce_segment(const SweepParams &p, const floa
 template <class C, bool POISSON, bool CHECK, bool STORE>
 __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst, int ja, int jb,
                                                 int dir, int cols, long long col0,
-                                                StreamState &st, double &s2, float &rmax) {
+                                                StreamState &st, double &s2_out, float &rmax) {
     constexpr int Q = C::kQPT;
     const int t = threadIdx.x;
     const unsigned lane = t & 31;
+    ResFF s2 = {0.f, 0.f, 0.0};  // this segment's residual, added to s2_out at the end
     int valid[Q];
 #pragma unroll
     for (int k = 0; k < Q; ++k) valid[k] = max(0, min(4, cols - 4 * (t + k * C::kCons)));
@@ -219,6 +220,7 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
             curg[k] = xg[k];
         }
     }
+    if (CHECK) s2_out = __dadd_rn(s2_out, resff_value(s2));
 }
 
 // Two sweeps per pass (temporal blocking; "Persistent Kernels...",
@@ -267,7 +269,7 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
                                           int idx, int r, float4 (&KA)[C::kQPT],
                                           float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
                                           float4 (&QA)[C::kQPT], float4 (&QB)[C::kQPT],
-                                          float4 (&QY)[C::kQPT], double &s2, float &rmax) {
+                                          float4 (&QY)[C::kQPT], ResFF &s2, float &rmax) {
     constexpr int Q = C::kQPT;
     constexpr unsigned M = C::kStages - 1;
     const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -360,7 +362,7 @@ __device__ __forceinline__ void seg2_steady(const SweepParams &p, Seg2<C::kQPT> 
                                             int &idx, int &r, int steady, float4 (&ka)[C::kQPT],
                                             float4 (&kb)[C::kQPT], float4 (&kx)[C::kQPT],
                                             float4 (&qa)[C::kQPT], float4 (&qb)[C::kQPT],
-                                            float4 (&qy)[C::kQPT], double &s2, float &rmax) {
+                                            float4 (&qy)[C::kQPT], ResFF &s2, float &rmax) {
     const int dir = c.dir;
     for (; steady >= 3; steady -= 3) {
         seg2_step<C, POISSON, CHECK, true, FULL>(p, c, st, idx, r, ka, kb, kx, qa, qb, qy, s2, rmax);
@@ -392,8 +394,9 @@ __device__ __forceinline__ void rotate3(float4 (&A)[Q], float4 (&B)[Q], float4 (
 template <class C, bool POISSON, bool CHECK>
 __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *dst, int ja, int jb,
                                                  int dir, int cols, long long col0,
-                                                 StreamState &st, float *qbuf, double &s2,
+                                                 StreamState &st, float *qbuf, double &s2_out,
                                                  float &rmax) {
+    ResFF s2 = {0.f, 0.f, 0.0};  // this segment's residual, added to s2_out at the end
     constexpr int Q = C::kQPT;
     Seg2<Q> c;
     c.qbuf = qbuf;
@@ -439,6 +442,7 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
         mbar_arrive(&st.empty[(st.L - 2u) & (C::kStages - 1)]);
         mbar_arrive(&st.empty[(st.L - 1u) & (C::kStages - 1)]);
     }
+    if (CHECK) s2_out = __dadd_rn(s2_out, resff_value(s2));
 }
 
 // Three sweeps per pass: the two-sweep pass with one more level.  Input rows
