@@ -57,7 +57,9 @@ extern "C" {
 
 /* ---- sweep variants ---------------------------------------------------- */
 #define PK_VARIANT_AUTO 0   /* STREAM when the two fields exceed half of L2; else LOCAL for
-                               grids up to 2^20 cells whose tiles fit; else DIRECT */
+                               grids up to 2^20 cells whose tiles fit; else DIRECT, whose
+                               persistent runs of two or more sweeps take the multi-sweep
+                               STREAM shape (pk_run_info.variant says which ran) */
 #define PK_VARIANT_DIRECT 1 /* each thread loads its own float4 and neighbours (L2-resident grids) */
 #define PK_VARIANT_STREAM 2 /* TMA bulk row staging + register window down row bands (HBM grids) */
 #define PK_VARIANT_LOCAL 3  /* each CTA keeps its row band in shared memory across sweeps and
@@ -297,8 +299,11 @@ const char *pk_last_error(const pk_ctx *ctx);
  * g = fl32(h^2 * f) with h^2 = (float)(1/(nx+1)^2), in the pitched source
  * layout (g[(j-1) * gpitch + (i-1)], gpitch from pk_layout; NULL for
  * Laplace), a cudaStream_t (NULL = the legacy default stream), and n, tol,
- * check_every with pk_run_sweeps's meaning.  The result is bit for bit
- * pk_run_sweeps's; info->current names the buffer holding it;
+ * check_every with pk_run_sweeps's meaning.  The plan is pk_create's
+ * automatic one without LOCAL: runs of two or more sweeps take the
+ * multi-sweep STREAM shape, single sweeps STREAM or DIRECT by footprint.
+ * The result is bit for bit pk_run_sweeps's; info->current names the buffer
+ * holding it; info->variant, stream_config and sweeps_per_pass say what ran;
  * info->device_us is 0 (no events are created).  Blocks until done.
  *
  * Scratch (grid-barrier words, residual partials, result record) lives in

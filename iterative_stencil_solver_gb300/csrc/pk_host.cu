@@ -231,20 +231,6 @@ long long stream_rows(const pk_ctx *ctx, int cfg) {
 long long stream_rows(const pk_ctx *ctx) { return stream_rows(ctx, ctx->stream_cfg); }
 
 constexpr int kDefaultStreamConfig = 3;   // 4096-column strips, 4-deep ring, 1 CTA/SM
-// Multi-sweep shape for persistent runs, from measurements on GB300 (100
-// sweeps, us/sweep).  Both take three sweeps per pass.  Laplace: {1 float4/
-// thread, 224 consumers, 2 CTAs/SM} with an 8-deep ring above 8192 columns
-// (16384^2: 121.5 against 123.4 with a 16-deep ring and 128.2 for one CTA of
-// 256 consumers per SM), the 16-deep ring up to 8192 (8192^2: 33.8 against
-// 34.3; 4096^2: 9.56 against 10.0).  Poisson, whose ring slots also carry the
-// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 170.3 at 16384^2,
-// 43.0 at 8192^2 and 12.8 at 4096^2 (the best two-sweep shape: 249.1 and
-// 17.0 at 16384^2 and 4096^2).
-int default_multi_sweep_shape(bool poisson, int nx) {
-    if (poisson) return 12;
-    return nx > 8192 ? 11 : 10;
-}
-
 int ensure_partials(pk_ctx *ctx, int grid) {
     if (grid <= ctx->part_cap) return PK_OK;
     if (ctx->partials) {
@@ -381,15 +367,21 @@ int plan(pk_ctx *ctx) {
     ctx->stream_cfg = ctx->opt.stream_config >= 0 ? ctx->opt.stream_config : kDefaultStreamConfig;
     if (v == kVariantStream && !stream_config_ok(ctx->stream_cfg, ctx->poisson))
         return fail(ctx, PK_EINVAL, "stream_config %d does not fit in shared memory", ctx->stream_cfg);
-    // Default shape: persistent runs that can take two sweeps per pass use
-    // the two-sweep shape (same bits, half the HBM traffic per sweep).
+    // Persistent runs of two or more sweeps take the multi-sweep STREAM
+    // shape (several sweeps per pass, the same bits): on STREAM contexts
+    // without a chosen shape, and on DIRECT contexts the automatic plan
+    // chose (grids in L2 but too large for LOCAL), where it measured 1.5 to
+    // 1.8 times faster than DIRECT from 1536^2 to 2896^2.
     ctx->stream_cfg2 = -1;
     ctx->grid2 = 0;
     const int shape2 = default_multi_sweep_shape(ctx->poisson, ctx->nx);
-    if (v == kVariantStream && ctx->opt.stream_config < 0 && stream_config_ok(shape2, ctx->poisson)) {
+    const bool multi_stream = (v == kVariantStream && ctx->opt.stream_config < 0) ||
+                              (v == kVariantDirect && ctx->opt.variant == PK_VARIANT_AUTO);
+    if (multi_stream && stream_config_ok(shape2, ctx->poisson)) {
         int per_sm2 = 0;
-        const int cap2 = coop_capacity(ctx, kernel_persistent(v, ctx->poisson, shape2),
-                                       block_threads(v, shape2), dyn_smem(v, ctx->poisson, shape2), &per_sm2);
+        const int cap2 = coop_capacity(ctx, kernel_persistent(kVariantStream, ctx->poisson, shape2),
+                                       block_threads(kVariantStream, shape2),
+                                       dyn_smem(kVariantStream, ctx->poisson, shape2), &per_sm2);
         if (cap2 < 0) return PK_ECUDA;
         if (cap2 > 0) {
             long long need2 = stream_rows(ctx, shape2);
@@ -777,10 +769,11 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
     int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
     if (ctx->stream_cfg2 >= 0 && multi_ok) {
+        kernel = kVariantStream;
         shape = ctx->stream_cfg2;
         grid = ctx->grid2;
     }
-    if (ctx->variant == kVariantStream && multi_ok) depth = stream_depth(shape);
+    if (kernel == kVariantStream && multi_ok) depth = stream_depth(shape);
     if (ctx->variant == kVariantLocal && ctx->local_depth >= 2 &&
         !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS)) {
         // passes take up to local_depth sweeps, never past a check
@@ -798,7 +791,8 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     int rc = bar_status(ctx, p.bar, "pk_run_sweeps");
     if (rc != PK_OK) {
         ctx->sweep_bar_base = 0;  // bar_status zeroed the barrier words
-        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, 0, shape, depth);
+        fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, kernel == kVariantStream ? kernel : 0,
+                  shape, depth);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
@@ -807,7 +801,8 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     if (p.profile) ctx->spin_valid = grid;
     ctx->cur = ctx->h_info->cur;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
-              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid, 0, shape, depth);
+              ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid,
+              kernel == kVariantStream ? kernel : 0, shape, depth);
     return PK_OK;
 }
 

@@ -168,6 +168,20 @@ inline size_t stream_smem_bytes(int cfg, bool poisson) {
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 
+// Multi-sweep shape for persistent runs, from measurements on GB300 (100
+// sweeps, us/sweep).  Both take three sweeps per pass.  Laplace: {1 float4/
+// thread, 224 consumers, 2 CTAs/SM} with an 8-deep ring above 8192 columns
+// (16384^2: 121.5 against 123.4 with a 16-deep ring and 128.2 for one CTA of
+// 256 consumers per SM), the 16-deep ring up to 8192 (8192^2: 33.8 against
+// 34.3; 4096^2: 9.56 against 10.0).  Poisson, whose ring slots also carry the
+// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 170.3 at 16384^2,
+// 43.0 at 8192^2 and 12.8 at 4096^2 (the best two-sweep shape: 249.1 and
+// 17.0 at 16384^2 and 4096^2).
+inline int default_multi_sweep_shape(bool poisson, int nx) {
+    if (poisson) return 12;
+    return nx > 8192 ? 11 : 10;
+}
+
 // Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).
 void set_global_error(const char *msg);
 

@@ -114,16 +114,25 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     const bool poisson = g_dev != nullptr;
     const long long gpitch = (nx + 31LL) / 32 * 32;
 
-    // Plan: the same rules as pk_create's (variant by footprint, grid from
-    // the occupancy API and the problem size).
+    // Plan: pk_create's automatic rules without LOCAL (its halo areas would
+    // need an allocation).  A run of two or more sweeps takes the
+    // multi-sweep STREAM shape; otherwise grids larger than half of L2 take
+    // one sweep per STREAM pass and the others DIRECT.  The grid comes from
+    // the occupancy API and the problem size.
     const long long resident = 2LL * (ny + 2) * pitch * 4 + (poisson ? (long long)ny * gpitch * 4 : 0);
-    const int variant = resident > g_l2[dev] / 2 ? kVariantStream : kVariantDirect;
-    const int cfg = 3;
+    int variant = resident > g_l2[dev] / 2 ? kVariantStream : kVariantDirect;
+    int cfg = 3;
+    int depth = 1;
+    if (n >= 2 && stream_config_ok(default_multi_sweep_shape(poisson, nx), poisson)) {
+        variant = kVariantStream;
+        cfg = default_multi_sweep_shape(poisson, nx);
+        depth = stream_depth(cfg);
+    }
     if (variant == kVariantDirect && (long long)ny * ((nx + 3) / 4) >= (1LL << 31))
         return fail(PK_EINVAL, "pk_run_sweeps_noalloc: grid too large");
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_persistent(variant, poisson, cfg),
-                                                      block_threads(variant),
+                                                      block_threads(variant, cfg),
                                                       dyn_smem(variant, poisson, cfg));
     if (e != cudaSuccess) return fail(PK_ECUDA, "occupancy query", e);
     const long long cap = (long long)per_sm * g_sms[dev];
@@ -188,6 +197,8 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
         info->current = hi.cur;
         info->grid = (int)grid;
         info->variant = variant;
+        info->stream_config = variant == kVariantStream ? cfg : -1;
+        info->sweeps_per_pass = depth;
         info->device_us = 0.0;
     }
     return PK_OK;

@@ -461,6 +461,32 @@ def test_three_sweep_residual_extreme_scales(pk, cfg, scale, poisson):
         check_info(info, oinfo)
 
 
+# The automatic plan sends grids that live in L2 but are too large for LOCAL
+# to DIRECT; their persistent runs of two or more sweeps take the multi-sweep
+# STREAM shape, single sweeps and the per-launch path stay on DIRECT.
+@pytest.mark.parametrize("nx,ny", [(1536, 1536), (2100, 600)], ids=["1536x1536", "2100x600"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_auto_direct_context_takes_multi_sweep_stream(pk, nx, ny, poisson):
+    u0 = inputs.random_field(nx, ny, seed=900 + nx)
+    f = inputs.uniform_pm1(901 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    ctx = pk.pk_create(nx, ny, u0, f)
+    try:
+        assert pk.pk_get_plan(ctx)["variant"] == 1
+    finally:
+        pk.pk_destroy(ctx)
+    for n, tol, ce, want_variant in ((10, 1e-30, 4, 2), (1, 0.0, 0, 1)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, tol, ce)
+        assert info["variant"] == want_variant, info
+        if want_variant == 2:
+            assert info["stream_config"] == (12 if poisson else 10) and info["sweeps_per_pass"] == 3
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+        got, info = run_pk(pk, u0, f, n, tol, ce, path="launch")
+        assert info["variant"] == 1
+        assert_same_bits(got, want)
+
+
 # The default STREAM plan: persistent runs whose passes can take two sweeps
 # use the two-sweep shape; the others, and the per-launch path, keep the
 # single-sweep shape.  Either way the bits are those of single sweeps.
