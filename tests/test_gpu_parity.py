@@ -441,12 +441,12 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
             check_info(info, oinfo)
 
 
-# The three-sweep step accumulates the residual's squares as a pair of floats
-# and sends squares that could underflow or overflow in fp32 to a double: a
-# field scaled far down puts every cell there, one scaled to the boundary of
-# the range mixes both kinds, and one scaled far up overflows r^2 in fp32.
+# The sweep kernels accumulate the residual's squares as a pair of floats and
+# send squares that could underflow or overflow in fp32 to a double: a field
+# scaled far down puts every cell there, fields scaled near the boundary mix
+# both kinds, and one scaled far up overflows r^2 in fp32.
 @pytest.mark.parametrize("cfg", [10, 11, 12])
-@pytest.mark.parametrize("scale", [1e-20, 3e-15, 1e25], ids=["tiny", "mixed", "huge"])
+@pytest.mark.parametrize("scale", [1e-20, 3e-15, 1e-12, 1e25], ids=["tiny", "small", "mixed", "huge"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_three_sweep_residual_extreme_scales(pk, cfg, scale, poisson):
     nx, ny = 2053, 37
