@@ -27,11 +27,12 @@ namespace {
 // columns; (strip, row) pairs are split evenly, in contiguous runs, over the
 // CTAs.  Each CTA walks its run row by row: one producer thread streams
 // every input row segment (with a 16-byte halo on each side) into a
-// STAGES-deep shared-memory ring with cp.async.bulk, and 256 consumer
+// STAGES-deep shared-memory ring with cp.async.bulk, and CONS consumer
 // threads keep a three-row window (previous, centre, next) in registers,
 // QPT float4 groups per thread, so each input row is read from HBM once and
-// from shared memory once.  Edge neighbours come from warp shuffles, and at
-// warp edges from the staged halo.
+// from shared memory once.  In the one-sweep step edge neighbours come from
+// warp shuffles, and at warp edges from the staged halo; the two- and
+// three-sweep steps (below) read them from shared memory.
 template <int QPT, int STAGES, int DEPTH, int MINB, int CONS, bool POISSON>
 struct SCfg {
     static constexpr int kCons = CONS;       // consumer threads
@@ -453,10 +454,9 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
 // cell of every quad of each new U_{k+1} and U_{k+2} row (the west and east
 // neighbours other threads need) through three shared rows per level (the
 // row of input step i in row i mod 3), with the one named barrier per input
-// row.  The cells
-// beyond a strip edge that later stages read are U_{k+1} two columns out and
-// U_{k+2} one column out; one warp computes them from the staged U_k rows, a
-// shared U_{k+1} row and a short history.  A ring slot is held for three
+// row.  The cells beyond a strip edge that later stages read are U_{k+1} two
+// columns out and U_{k+2} one column out; one warp computes them from the
+// staged U_k rows, a shared U_{k+1} row and a short history.  A ring slot is held for three
 // input rows: stage 3 takes the source of its row from registers (stage 2
 // loaded it one step before).  Ring cells of every level keep the U_k value;
 // every other cell uses the single-sweep arithmetic, so the result is bit
