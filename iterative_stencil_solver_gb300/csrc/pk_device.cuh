@@ -434,27 +434,49 @@ __device__ __forceinline__ float4 quad_update2(const Quad &q) {
 }
 
 // Per-thread residual accumulator of the sweep kernels: the sum of r^2 as an
-// unevaluated pair of floats.  Each square is split exactly
-// into p + e (p = fl(r*r), e = fma(r, r, -p)); p joins hi through an
-// error-free two-sum whose error, with e, goes to lo.  Over the few hundred
-// cells a thread checks per segment the pair carries about 44 significant
-// bits, far inside the 1e-10 relative agreement the residual is held to,
-// and costs only fp32 arithmetic (fp64 runs at a small fraction of the fp32
-// rate on this GPU).  Squares whose split could underflow or overflow in
-// fp32 (0 < |r| < 2^-50, |r| >= 2^60) go to a double instead.
+// unevaluated pair of floats with a power-of-two exponent, sum = (hi + lo) *
+// 2^(2 * ex).  Each residual is scaled exactly by 2^-ex (held in `scale`) and
+// its square split exactly into p + e (p = fl(x*x), e = fma(x, x, -p)); p
+// joins hi through an error-free two-sum whose error, with e, goes to lo.
+// Over the few hundred cells a thread checks per pass the pair carries about
+// 44 significant bits, far inside the 1e-10 relative agreement the residual
+// is held to.  The exponent follows the largest residual seen: one whose
+// scaled value reaches 2^30 moves it up (the pair is scaled down exactly, or
+// to nothing where it is negligible next to the new term), so squares never
+// overflow; residuals far below the largest lose only bits that are far
+// below the sum.  All of it is fp32 and integer arithmetic: fp64 runs at a
+// small fraction of the fp32 rate on this GPU, and a double path for rare
+// values, even when no cell took it, kept the fp64 pipe busy on every
+// checked cell.
 struct ResFF {
     float hi, lo;
-    double wide;
+    float scale;  // 2^-ex
+    int ex;
 };
+__device__ __forceinline__ ResFF resff_zero() {
+    ResFF a;
+    a.hi = a.lo = 0.f;
+    a.ex = -126;
+    a.scale = 0x1p126f;
+    return a;
+}
 __device__ __forceinline__ void resff_add(ResFF &a, float r) {
-    const float m = fabsf(r);
-    if (m != 0.f && (m < 0x1p-50f || m >= 0x1p60f)) {
-        const double rd = (double)r;
-        a.wide = __dadd_rn(a.wide, __dmul_rn(rd, rd));
-        return;
+    float x = __fmul_rn(r, a.scale);
+    if (fabsf(x) >= 0x1p30f) {
+        // r's binary exponent (r * 2^-ne in [0.5, 1)); subnormals count as
+        // -126, and exponents above 126 as 126 (so 2^-ne stays a normal float)
+        const int eb = (__float_as_int(r) >> 23) & 0xff;
+        const int ne = eb == 0 ? -126 : min(eb - 126, 126);
+        const int d = 2 * (ne - a.ex);  // > 0: the pair shrinks by 2^-d
+        const float f = d < 127 ? __int_as_float((127 - d) << 23) : 0.f;
+        a.hi = __fmul_rn(a.hi, f);
+        a.lo = __fmul_rn(a.lo, f);
+        a.ex = ne;
+        a.scale = __int_as_float((127 - ne) << 23);
+        x = __fmul_rn(r, a.scale);
     }
-    const float p = __fmul_rn(r, r);
-    const float e = __fmaf_rn(r, r, -p);
+    const float p = __fmul_rn(x, x);
+    const float e = __fmaf_rn(x, x, -p);
     const float s = __fadd_rn(a.hi, p);
     const float bp = __fsub_rn(s, a.hi);
     const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
@@ -462,7 +484,8 @@ __device__ __forceinline__ void resff_add(ResFF &a, float r) {
     a.lo = __fadd_rn(a.lo, __fadd_rn(err, e));
 }
 __device__ __forceinline__ double resff_value(const ResFF &a) {
-    return __dadd_rn(__dadd_rn((double)a.hi, (double)a.lo), a.wide);
+    const double v = __dadd_rn((double)a.hi, (double)a.lo);
+    return ldexp(v, 2 * a.ex);
 }
 __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, ResFF &acc,
                                               float &rmax) {
@@ -482,7 +505,7 @@ __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid
 // squares summed as a pair, then added once.
 __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, double &s2,
                                               float &rmax) {
-    ResFF a = {0.f, 0.f, 0.0};
+    ResFF a = resff_zero();
     quad_residual(q, c, valid, a, rmax);
     s2 = __dadd_rn(s2, resff_value(a));
 }

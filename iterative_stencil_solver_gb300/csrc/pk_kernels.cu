@@ -46,7 +46,7 @@ __device__ __forceinline__ void pass_direct(const SweepParams &p, const float *_
                                             unsigned stride, double &s2, float &rmax) {
     const unsigned nq = (unsigned)(p.nx + 3) >> 2;
     const unsigned units = (unsigned)p.ny * nq;
-    ResFF acc = {0.f, 0.f, 0.0};
+    ResFF acc = resff_zero();
     for (unsigned u = first; u < units; u += stride) {
         const unsigned jm1 = u / nq;
         const unsigned q = u - jm1 * nq;

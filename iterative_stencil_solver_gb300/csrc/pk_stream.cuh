@@ -157,7 +157,7 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
     constexpr int Q = C::kQPT;
     const int t = threadIdx.x;
     const unsigned lane = t & 31;
-    ResFF s2 = {0.f, 0.f, 0.0};  // this segment's residual, added to s2_out at the end
+    ResFF s2 = resff_zero();  // this segment's residual, added to s2_out at the end
     int valid[Q];
 #pragma unroll
     for (int k = 0; k < Q; ++k) valid[k] = max(0, min(4, cols - 4 * (t + k * C::kCons)));
@@ -397,7 +397,7 @@ __device__ __forceinline__ void consume_segment2(const SweepParams &p, float *ds
                                                  int dir, int cols, long long col0,
                                                  StreamState &st, float *qbuf, double &s2_out,
                                                  float &rmax) {
-    ResFF s2 = {0.f, 0.f, 0.0};  // this segment's residual, added to s2_out at the end
+    ResFF s2 = resff_zero();  // this segment's residual, added to s2_out at the end
     constexpr int Q = C::kQPT;
     Seg2<Q> c;
     c.qbuf = qbuf;
@@ -725,7 +725,7 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
                                                  StreamState &st, float *qbuf, double &s2_out,
                                                  float &rmax) {
     // The residual of this segment's cells, added to s2_out at the end.
-    ResFF s2 = {0.f, 0.f, 0.0};
+    ResFF s2 = resff_zero();
     constexpr int Q = C::kQPT;
     constexpr unsigned M = C::kStages - 1;
     const int t = (int)threadIdx.x;
