@@ -197,8 +197,9 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
  * with a release/acquire generation-counter grid barrier between sweeps.
  * Runs up to n sweeps.  With tol > 0 and check_every > 0 the residual
  * r = fl32(t - 4C) of iterate k (t as in the update, before the 1/4) is
- * reduced in the kernel when k % check_every == 0 (L2 norm in fp64, and
- * max|r|); the run stops at the first checked k > 0 with
+ * reduced in the kernel when k % check_every == 0 (L2 norm: exact squares
+ * summed per thread as a float pair, across threads in fp64, to about 1e-12
+ * relative; and max|r| exactly); the run stops at the first checked k > 0 with
  * ||r_k|| < tol * ||r_0|| and keeps U_k, else it stops at k = n.  The
  * current buffer afterwards holds U_{sweeps_done}.  Blocks until done.
  * info may be NULL.  Errors: PK_EINVAL (n < 0), PK_EBUSY (task kernel live),
