@@ -59,8 +59,8 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "2b57a9d27dc85ce1", "stream_config": 11,
-           "bytes_per_launch": 35.584e9 + 36.492e9}
+TRAFFIC = {"kernel_sha": "9d87a1893e1f34b7", "stream_config": 11,
+           "bytes_per_launch": 35.587e9 + 36.490e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)

@@ -484,7 +484,12 @@ struct Seg3 {
     float *drow;          // stage-3 output, this thread's first quad, for the next step
     long long dstep;      // dir * pitch
     int dir, cols, nin, nx, ny;
-    bool first_strip, last_strip, right_edge;
+    // Edge warp, per lane: the cells beyond its edge are ring or pad columns
+    // (the first or last strip); the U_{k+1} cell two columns out is a ring
+    // column (that, or the next strip is the last one and one column wide);
+    // the lane stores its edge cells (lanes 0 and 1; the right one only when
+    // the strip width is a multiple of 4).
+    bool outer, outer2, write_edge;
     int valid[Q];         // cells of quad k inside the strip (0..4)
     int icol[Q];          // interior column of quad k's first cell
     // Edge lanes' U_{k+1} history: the cell just beyond the strip edge at the
@@ -568,8 +573,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
         const bool right = c.dd > 0;
         const unsigned xe = sx + 4 * c.de, be = sb + 4 * c.de, ae = sa + 4 * c.de;
         const unsigned o4 = 4u * (unsigned)c.dd;  // one column outward, in bytes
-        const bool outer = right ? c.last_strip : c.first_strip;
-        const bool keep1 = ring1 || outer, keep2 = ring2 || outer;
+        const bool keep1 = ring1 || c.outer, keep1o = ring1 || c.outer2, keep2 = ring2 || c.outer;
         float t = cell_t(lds_at(be - 4u), lds_at(be + 4u), lds_at(ae), lds_at(xe));
         float t2 = cell_t(lds_at(be + o4 - 4u), lds_at(be + o4 + 4u), lds_at(ae + o4), lds_at(xe + o4));
         if (POISSON) {
@@ -577,14 +581,14 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             t2 = __fsub_rn(t2, lds_at(be + o4 + GO));
         }
         const float v1c = keep1 ? lds_at(be) : __fmul_rn(0.25f, t);
-        const float v1o = keep1 ? lds_at(be + o4) : __fmul_rn(0.25f, t2);
+        const float v1o = keep1o ? lds_at(be + o4) : __fmul_rn(0.25f, t2);
         // U_{k+1} at row r2 beside the edge cell: the strip's outermost
         // interior cell (shared row) and the cell two columns out (history).
         const float in2 = lds_at(c.he_r + qr * RW);
         float t3 = cell_t(right ? in2 : c.e_out, right ? c.e_out : in2, c.e_c1, v1c);
         if (POISSON) t3 = __fsub_rn(t3, lds_at(ae + GO));
         const float v2c = keep2 ? c.e_c0 : __fmul_rn(0.25f, t3);
-        if (lane < 2u && (!right || c.right_edge)) {
+        if (c.write_edge) {
             sts_at(c.he_w + qj * RW, v1c);
             if (act2) sts_at(c.he_w + (3u + qj) * RW, v2c);
         }
@@ -756,9 +760,13 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     c.nin = (dir > 0 ? jb - ja : ja - jb) + 7;
     c.nx = p.nx;
     c.ny = p.ny;
-    c.first_strip = col0 == 0;
-    c.last_strip = col0 + cols >= p.nx;
-    c.right_edge = (cols & 3) == 0;
+    const bool first_strip = col0 == 0, last_strip = col0 + cols >= p.nx;
+    c.outer = right ? last_strip : first_strip;
+    // Two columns right of the strip lies the right ring column when the next
+    // strip is the last one and holds a single column (nx = col0 + cols + 1);
+    // two columns left of a strip that is not the first is always interior.
+    c.outer2 = c.outer || (right && col0 + cols + 1 == (long long)p.nx);
+    c.write_edge = lane < 2u && (!right || (cols & 3) == 0);
     c.dstep = (long long)dir * p.pitch;
     c.drow = dst + (long long)ja * p.pitch + col0 + 4 + 4 * t;
     c.e_c0 = c.e_c1 = c.e_out = 0.f;

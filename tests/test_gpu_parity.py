@@ -441,6 +441,51 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
             check_info(info, oinfo)
 
 
+# Strip width of each STREAM shape: 4 x (float4 groups per thread) x
+# (consumer threads), as in the shape table of the library.
+STREAM_TW = {0: 1024, 1: 1024, 2: 2048, 3: 4096, 4: 4096, 5: 2048, 6: 1024, 7: 2048, 8: 1024,
+             9: 2048, 10: 896, 11: 896, 12: 1024}
+
+
+# A last strip one to three columns wide.  With one column, the cell two
+# columns right of the strip before it is the ring column, which a three-sweep
+# pass must keep at U_k at every level.
+@pytest.mark.parametrize("cfg", range(13))
+@pytest.mark.parametrize("extra,strips", [(1, 1), (1, 2), (2, 1), (3, 1)],
+                         ids=["tw+1", "2tw+1", "tw+2", "tw+3"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_stream_narrow_last_strip(pk, cfg, extra, strips, poisson):
+    nx, ny = strips * STREAM_TW[cfg] + extra, 7
+    u0 = inputs.random_field(nx, ny, seed=500 + cfg + nx)
+    f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, ce in [(9, 0), (12, 6), (7, 3)]:
+        tol = 1e-30 if ce else 0.0
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        try:
+            got, info = run_pk(pk, u0, f, n, tol, ce, variant=2, stream_config=cfg,
+                               flags=pk.PK_FLAG_ALTERNATE_DIRECTION if n % 2 else 0)
+        except pk.PkError as e:
+            assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
+            return
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
+# The default three-sweep plans on grids whose last strip is one column wide:
+# 4097 columns for the 1024-wide Poisson shape, 1793 for the 896-wide Laplace
+# shape up to 8192 columns.
+@pytest.mark.parametrize("nx,ny", [(4097, 40), (1793, 33)], ids=["4097x40", "1793x33"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_stream_default_plan_one_column_strip(pk, nx, ny, poisson):
+    u0 = inputs.random_field(nx, ny, seed=nx + ny)
+    f = inputs.uniform_pm1(nx - ny, nx * ny).reshape(ny, nx) if poisson else None
+    want, oinfo = oracle.jacobi_run(u0, f=f, n=30, tol=1e-30, check_every=10)
+    got, info = run_pk(pk, u0, f, 30, 1e-30, 10, variant=2)
+    assert info["sweeps_per_pass"] == 3
+    assert_same_bits(got, want)
+    check_info(info, oinfo)
+
+
 # The sweep kernels accumulate the residual's squares as a pair of floats and
 # send squares that could underflow or overflow in fp32 to a double: a field
 # scaled far down puts every cell there, fields scaled near the boundary mix
