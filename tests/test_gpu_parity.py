@@ -738,6 +738,33 @@ def test_local_depth_bit_exact(pk, nx, ny, grid, depth, poisson):
         check_info(info, oinfo)
 
 
+# The automatic plan on grids that reach each LOCAL width class (256 threads
+# and four sweeps per exchange up to 128 columns; 512 threads and three up to
+# 384; 256 and three up to 512; 512, three, bands of six rows up to 1024;
+# wider rows one sweep per exchange) and the 2^20-cell limit of LOCAL.
+AUTO_LOCAL_CASES = [(128, 9), (129, 129), (384, 200), (385, 200), (520, 77), (768, 300),
+                    (1024, 1024), (1021, 1027), (1025, 1023)]
+
+
+@pytest.mark.parametrize("nx,ny", AUTO_LOCAL_CASES, ids=["%dx%d" % c for c in AUTO_LOCAL_CASES])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_local_default_plan_width_classes(pk, nx, ny, poisson):
+    u0 = inputs.random_field(nx, ny, seed=1100 + nx + ny)
+    f = inputs.uniform_pm1(1200 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, tol, ce in ((41, 0.0, 0), (33, 1e-30, 8), (12, 1e-30, 1), (30, 0.9, 2)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, tol, ce)
+        assert info["variant"] == 3
+        assert 1 <= info["sweeps_per_pass"] <= 4
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+    for n, tol, ce in ((9, 0.0, 0), (10, 1e-30, 4)):
+        want, oinfo = oracle.rb_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_rb(pk, u0, f, n, tol, ce)
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
 def test_local_depth_lowered_when_bands_are_thin(pk):
     """Bands of two rows cannot feed three halo rows: the plan lowers the depth."""
     u0 = inputs.random_field(64, 64, seed=9)

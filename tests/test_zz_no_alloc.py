@@ -41,8 +41,10 @@ def _info_matches(a, b):
     assert a["res_last"] == pytest.approx(b["res_last"], rel=1e-10, abs=0)
 
 
+# 4097 and 1793 columns: the three-sweep shapes' last strip is one column wide
+# (Poisson's 1024-wide strips, Laplace's 896-wide ones).
 @pytest.mark.parametrize("nx,ny,poisson", [(300, 301, True), (4096, 4096, False),
-                                           (2100, 37, True)])
+                                           (2100, 37, True), (4097, 33, True), (1793, 20, False)])
 def test_noalloc_matches_pk_run_sweeps_two_calls(env, nx, ny, poisson):
     pk, torch = env
     dev = torch.device("cuda", 0)
