@@ -142,3 +142,20 @@ def test_null_context_calls(pk):
     assert lib.pk_shutdown(None) == pk.PK_EINVAL
     lib.pk_destroy.argtypes = pk._SIGS["pk_destroy"][1]
     lib.pk_destroy(None)
+
+
+def test_gpu_tests_strip_widths_follow_the_shape_table():
+    """The GPU tests size their narrow-last-strip grids from a table of strip
+    widths (4 x float4 groups per thread x consumer threads); it must follow
+    the library's STREAM shape table."""
+    src = open(os.path.join(ROOT, "iterative_stencil_solver_gb300", "csrc", "pk_internal.h")).read()
+    body = re.search(r"kStreamConfigs\[kNumStreamConfigs\]\s*=\s*\{(.*?)\};", src, flags=re.S).group(1)
+    shapes = [tuple(int(v) for v in m.split(","))
+              for m in re.findall(r"\{\s*([0-9,\s]+?)\s*\}", body)]
+    assert all(len(s) == 5 for s in shapes)
+    widths = {cfg: 4 * qpt * consumers for cfg, (qpt, _, _, _, consumers) in enumerate(shapes)}
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("gpu_parity", os.path.join(ROOT, "tests", "test_gpu_parity.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert mod.STREAM_TW == widths
