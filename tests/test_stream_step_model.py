@@ -1,6 +1,6 @@
-"""A CPU model of the STREAM kernel's three-sweep step, and of the same step
-with a fourth level (the design of a four-sweep pass, which has no kernel in
-this tree yet).
+"""A CPU model of the STREAM kernel's two- and three-sweep steps, and of the
+three-sweep step with a fourth level (the design of a four-sweep pass, which
+has no kernel in this tree yet).
 
 The model follows the step's dataflow as the CUDA code does: per input row,
 an edge warp (left edge in even lanes, right edge in odd ones) computes the
@@ -133,7 +133,12 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
                     t = cell_t(sb[c - 1], sb[c + 1], sa[c], sx[c])
                     return F(t - gb[c]) if pois else t
 
-                if D == 3:
+                if D == 2:
+                    # the two-sweep step: one cell beyond each edge, by the
+                    # first and the last consumer thread
+                    v1c = sb[e] if (ring[1] or outer) else F(F(0.25) * t_at(0))
+                    vals = [v1c]
+                elif D == 3:
                     keep1 = ring[1] or outer
                     keep1o = keep1 if old_keep else (ring[1] or outer or (right and wr == 1))
                     keep2 = ring[2] or outer
@@ -211,11 +216,16 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
             last, first = sh[(D - 1, qr)]
             row = rs[D]
             for q in range(nq):
-                g = carry[D][q] if pois else None
+                if not pois:
+                    g = None
+                elif D == 2:
+                    g = ga[4 + 4 * q: 8 + 4 * q]
+                else:
+                    g = carry[D][q]
                 u = quad_stage(last[q], B[q], first[q + 1], A[q], Y[q], g)
                 for j in range(valid[q]):
                     out[row, st.col0 + 1 + 4 * q + j] = u[j]
-        if pois:
+        if pois and D >= 3:
             for s in range(D, 3, -1):
                 carry[s] = carry[s - 1].copy()
             carry[3] = g2 if g2 is not None else np.zeros((nq, 4), F)
@@ -252,7 +262,7 @@ CASES = [(16, 5, 1, 1), (17, 6, 2, 1), (18, 7, 1, -1), (19, 9, 3, 1), (33, 4, 1,
          (3, 5, 1, 1), (16, 1, 1, 1), (35, 11, 4, -1), (49, 3, 1, 1)]
 
 
-@pytest.mark.parametrize("D", [3, 4])
+@pytest.mark.parametrize("D", [2, 3, 4])
 @pytest.mark.parametrize("nx,ny,bands,d", CASES, ids=["%dx%d-b%d-d%d" % c for c in CASES])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_step_model_matches_single_sweeps(D, nx, ny, bands, d, poisson):
