@@ -63,8 +63,9 @@ class Strip:
         return row
 
 
-def quad_stage(W, C, E, S, N, g):
-    """The four cells of a quad: (W+E)+(S+N) [-g], times 1/4."""
+def quad_stage(W, C, E, S, N, g, ts=None):
+    """The four cells of a quad: (W+E)+(S+N) [-g], times 1/4 (the sums
+    before the quarter go to ts when given)."""
     out = np.empty(4, F)
     for j in range(4):
         w = W if j == 0 else C[j - 1]
@@ -72,6 +73,8 @@ def quad_stage(W, C, E, S, N, g):
         t = cell_t(w, e, S[j], N[j])
         if g is not None:
             t = F(t - g[j])
+        if ts is not None:
+            ts[j] = t
         out[j] = F(F(0.25) * t)
     return out
 
@@ -85,8 +88,10 @@ def keep_ring_cols(u, prev, icol, nx):
     return u
 
 
-def model_segment(st, ja, jb, d, out, old_keep=False):
-    """One segment (rows ja..jb, walking in direction d) of a D-sweep pass."""
+def model_segment(st, ja, jb, d, out, old_keep=False, resid=None):
+    """One segment (rows ja..jb, walking in direction d) of a D-sweep pass.
+    With resid (a list), stage 1 appends |r| = |fl32(t - 4C)| of U_k on the
+    segment's rows, as the kernel's check passes reduce it."""
     D, nx, ny, cols = st.D, st.nx, st.ny, st.cols
     pois = st.G is not None
     nq = (cols + 3) // 4
@@ -119,6 +124,10 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
         ring = [not (1 <= rs[s] <= ny) for s in range(D + 1)]
         KX = np.array([sx[4 + 4 * q: 8 + 4 * q] for q in range(nq)], F).reshape(nq, 4)
         win[0][2] = KX
+        # The kernels' test for a stage-1 row inside the segment (the residual
+        # is reduced there) must name exactly the segment's rows.
+        in_band = D + 1 <= idx <= nin - D
+        assert in_band == (act[1] and min(ja, jb) <= rs[1] <= max(ja, jb))
         if act[1]:
             for side in (0, 1):
                 h = hist[side]
@@ -189,6 +198,7 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
             A, B, Y = win[s - 1]
             new = np.empty((nq, 4), F)
             for q in range(nq):
+                ts = np.empty(4, F)
                 if s == 1:
                     W, E = sb[3 + 4 * q], sb[8 + 4 * q]
                     g = gb[4 + 4 * q: 8 + 4 * q] if pois else None
@@ -199,7 +209,10 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
                         g = ga[4 + 4 * q: 8 + 4 * q] if pois else None
                     else:
                         g = carry[s][q] if pois else None
-                u = quad_stage(W, B[q], E, A[q], Y[q], g)
+                u = quad_stage(W, B[q], E, A[q], Y[q], g, ts)
+                if s == 1 and resid is not None and in_band:
+                    for j in range(valid[q]):
+                        resid.append(abs(F(ts[j] - F(F(4) * B[q][j]))))
                 if ring[s]:
                     u = B[q].copy()
                 elif icol[q] + 3 > nx:
@@ -235,7 +248,7 @@ def model_segment(st, ja, jb, d, out, old_keep=False):
         r += d
 
 
-def model_pass(U, f, D, tw, bands, d, old_keep=False):
+def model_pass(U, f, D, tw, bands, d, old_keep=False, resid=None):
     """One D-sweep pass over the whole grid: strips of tw columns, each cut
     into the given number of row bands (segments walked in direction d)."""
     ny, nx = U.shape[0] - 2, U.shape[1] - 2
@@ -252,9 +265,9 @@ def model_pass(U, f, D, tw, bands, d, old_keep=False):
             if jb < ja:
                 continue
             if d > 0:
-                model_segment(st, ja, jb, 1, out, old_keep)
+                model_segment(st, ja, jb, 1, out, old_keep, resid)
             else:
-                model_segment(st, jb, ja, -1, out, old_keep)
+                model_segment(st, jb, ja, -1, out, old_keep, resid)
     return out
 
 
@@ -270,8 +283,16 @@ def test_step_model_matches_single_sweeps(D, nx, ny, bands, d, poisson):
     u0 = inputs.random_field(nx, ny, seed=40 + nx + ny)
     f = inputs.uniform_pm1(41 + nx, nx * ny).reshape(ny, nx) if poisson else None
     want, _ = oracle.jacobi_run(u0, f=f, n=D)
-    got = model_pass(u0, f, D, tw, bands, d)
+    resid = []
+    got = model_pass(u0, f, D, tw, bands, d, resid=resid)
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    # a check pass reduces every interior cell of U_k exactly once
+    assert len(resid) == nx * ny
+    g = None
+    if poisson:
+        g = (F(1.0 / ((nx + 1.0) * (nx + 1.0))) * f.astype(F)).astype(F)
+    _, rmax = oracle.residual(u0, g)
+    assert F(max(resid)) == F(rmax)
 
 
 def test_step_model_sees_the_one_column_strip_bug():
