@@ -34,7 +34,10 @@
  * Return codes: PK_OK (0) or a negative PK_E* code; pk_last_error(ctx)
  * returns a message for the last failure on that context (or for the last
  * failed pk_create* call when ctx is NULL).  A context is bound to one CUDA
- * stream and is not thread-safe.
+ * stream and is not thread-safe.  It belongs to the device that was current
+ * when it was created, and its calls run on the calling thread's current
+ * device: a thread that did not create it selects that device first
+ * (cudaSetDevice) before calling it.
  */
 #ifndef PK_H
 #define PK_H
