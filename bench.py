@@ -13,9 +13,10 @@ D2H copy of the result) on the host clock.  ``roofline`` reports the
 dominant kernel's algorithmic HBM bytes per launch over its event time,
 against the measured copy bandwidth.  Each pass over the field reads the
 current iterate once and writes the next one once (8 B per cell, 12 with a
-Poisson source); a pass of a two-sweep shape (temporal blocking) advances
-two sweeps for those 8 B, so the sweeps' compulsory traffic is 4 B per
-cell-update there.  ``cpu_baseline`` times the CPU
+Poisson source); a pass of a shape with D sweeps per pass (temporal
+blocking) advances D sweeps for those 8 B, so the sweeps' compulsory
+traffic is 8/D B per cell-update there (2.67 B at the default three).
+``cpu_baseline`` times the CPU
 oracle on a bounded sample of the same workload, single-threaded.
 
 ``--impl reference`` runs the CPU oracle arm instead (the only reference for
@@ -79,8 +80,8 @@ def shape_label(info, poisson):
 
 def passes_of(info, sweeps, tol, check_every):
     """Passes a persistent run over `sweeps` sweeps took (no early exit):
-    (passes that store, check-only passes).  A two-sweep shape takes two
-    sweeps per pass whenever no check can fall between them."""
+    (passes that store, check-only passes).  A shape of D sweeps per pass
+    takes up to D sweeps per pass, never past the end or a residual check."""
     checks = tol > 0 and check_every > 0
     depth = info["sweeps_per_pass"]
     k, store_passes = 0, 0
@@ -446,7 +447,7 @@ def latency_extras(pk):
     tb["speedup_two"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
     tb["speedup_three"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["three_sweeps_per_pass"]["us_per_sweep"]
     out["temporal_blocking_16384_100sweeps"] = tb
-    # Barrier spin: the headline kernel (one barrier per two-sweep pass) and
+    # Barrier spin: the headline kernel (one barrier per pass) and
     # the barrier-per-sweep DIRECT kernel on the L2-resident 512^2 grid.
     out["barrier_spin"] = {
         "laplace_16384_100sweeps": barrier_spin(pk, w, 100),

@@ -77,7 +77,7 @@ struct pk_ctx {
     int variant = kVariantDirect;
     int stream_cfg = 0;  // STREAM configuration index
     int grid = 1;        // persistent sweep grid
-    int stream_cfg2 = -1;  // two-sweep STREAM shape for persistent runs (-1 = none)
+    int stream_cfg2 = -1;  // multi-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
     int local_depth = 1;   // LOCAL: sweeps per neighbour exchange the plan allows
     int local_threads = kDirectThreads;  // LOCAL: threads per CTA
