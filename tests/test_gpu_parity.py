@@ -486,10 +486,11 @@ def test_stream_default_plan_one_column_strip(pk, nx, ny, poisson):
     check_info(info, oinfo)
 
 
-# The sweep kernels accumulate the residual's squares as a pair of floats and
-# send squares that could underflow or overflow in fp32 to a double: a field
-# scaled far down puts every cell there, fields scaled near the boundary mix
-# both kinds, and one scaled far up overflows r^2 in fp32.
+# The sweep kernels accumulate the residual's squares as a pair of floats
+# scaled by a power of two that follows the largest residual seen: a field
+# scaled far down has every r^2 below the fp32 normal range unscaled, fields
+# scaled near that boundary mix magnitudes, and one scaled far up would
+# overflow r^2 in fp32 without the scaling.
 @pytest.mark.parametrize("cfg", [10, 11, 12])
 @pytest.mark.parametrize("scale", [1e-20, 3e-15, 1e-12, 1e25], ids=["tiny", "small", "mixed", "huge"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
