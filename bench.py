@@ -8,8 +8,9 @@ as ONE persistent cooperative kernel per step (pk_run_sweeps).  The field is
 Prints one JSON line (rank 0).  ``value`` is whole-job cell-updates/s from
 CUDA events recorded on the launching stream around each kernel (libpk
 records them; pk_run_info.device_us); ``e2e`` is the same metric through the
-public C ABI with host buffers (pinned H2D copy of the field, the sweeps, a
-D2H copy of the result) on the host clock.  ``roofline`` reports the
+public C ABI with host buffers (pinned H2D copy of each step's field, the
+sweeps, a D2H copy of its result) on the host clock, the steps run through
+pk_run_batch, which overlaps one step's copies with the next one's sweeps.  ``roofline`` reports the
 dominant kernel's algorithmic HBM bytes per launch over its event time,
 against the measured copy bandwidth.  Each pass over the field reads the
 current iterate once and writes the next one once (8 B per cell, 12 with a
@@ -34,6 +35,7 @@ import re
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -192,9 +194,9 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % self.index)
-            self.fh = open(self.path, "w")
+            self.fh = tempfile.NamedTemporaryFile("w", prefix="pk_clocks_%d_" % self.index,
+                                                  suffix=".csv", delete=False)
+            self.path = self.fh.name
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
                  "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
@@ -211,6 +213,12 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
+        try:
+            return self._summary()
+        finally:
+            os.unlink(self.path)
+
+    def _summary(self):
         sm, smax, reasons = [], 0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
@@ -536,25 +544,41 @@ def main():
         ms_per_step = dev_s_max * 1e3 / args.steps
         us_per_sweep = dev_s * 1e6 / (updates / cells)
 
-        # e2e through the public API with pinned host buffers
-        # pinned host buffers; the tensors are kept so their pages stay pinned
+        # e2e through the public API with pinned host buffers: every step
+        # uploads its field, sweeps and downloads its result.  pk_run_batch
+        # runs the steps as a pipeline (step i+1's upload and step i-1's
+        # download overlap step i's sweeps); the tensors are kept so their
+        # pages stay pinned.
         host_in_t = torch.from_numpy(w["u0"]).pin_memory()
-        host_out_t = torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory()
-        assert host_in_t.is_pinned() and host_out_t.is_pinned()
-        host_in, host_out = host_in_t.numpy(), host_out_t.numpy()
+        host_out_t = [torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory()
+                      for _ in range(2)]
+        assert host_in_t.is_pinned() and all(t.is_pinned() for t in host_out_t)
+        host_in, host_out = host_in_t.numpy(), [t.numpy() for t in host_out_t]
+        pk.pk_run_batch(ctx, [host_in] * 2, host_out, sweeps, w["tol"], w["check_every"])
+        dist_barrier(world)
+        t0 = time.perf_counter()
+        infos = pk.pk_run_batch(ctx, [host_in] * args.steps,
+                                [host_out[q % 2] for q in range(args.steps)], sweeps, w["tol"],
+                                w["check_every"])
+        e2e_s = dist_max(world, time.perf_counter() - t0)
+        e2e_updates = sum(cells * info["sweeps_done"] for info in infos)
+        e2e_value = dist_sum(world, e2e_updates) / e2e_s
+        e2e_launches = len(infos) * 3  # per step: ring copy, persistent kernel, result record
+        # the same steps one call after another (set, run, get), for context
         pk.pk_set_field(ctx, host_in)
         pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
-        pk.pk_get_field(ctx, host_out)
+        pk.pk_get_field(ctx, host_out[0])
         dist_barrier(world)
-        e2e_updates = 0
+        serial_steps = min(args.steps, 10)
+        serial_updates = 0
         t0 = time.perf_counter()
-        for _ in range(args.steps):
+        for _ in range(serial_steps):
             pk.pk_set_field(ctx, host_in)
             info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
-            pk.pk_get_field(ctx, host_out)
-            e2e_updates += cells * info["sweeps_done"]
-        e2e_s = dist_max(world, time.perf_counter() - t0)
-        e2e_value = dist_sum(world, e2e_updates) / e2e_s
+            pk.pk_get_field(ctx, host_out[0])
+            serial_updates += cells * info["sweeps_done"]
+        serial_s = dist_max(world, time.perf_counter() - t0)
+        serial_value = dist_sum(world, serial_updates) / serial_s
     finally:
         pk.pk_destroy(ctx)
 
@@ -591,7 +615,12 @@ def main():
                      "algorithmic_bytes_per_launch": alg_bytes},
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": int(w["u0"].nbytes),
-                "d2h_bytes_per_step": int(w["u0"].nbytes)},
+                "d2h_bytes_per_step": int(w["u0"].nbytes),
+                "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps)",
+                "steps": args.steps, "seconds": e2e_s, "gpu_launches": e2e_launches,
+                "sweeps_ms_per_step_median": statistics.median(i["device_us"] for i in infos) / 1e3},
+        "e2e_serial": {"value": serial_value, "unit": UNIT, "steps": serial_steps,
+                       "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:

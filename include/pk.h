@@ -79,7 +79,8 @@ extern "C" {
 
 /* ---- grid barrier constructions ([P2] "The barrier is a counter and a
  * generation") -------------------------------------------------------------- */
-#define PK_BARRIER_GENERATION 0 /* count word + generation word; last arriver resets and bumps */
+#define PK_BARRIER_GENERATION 0 /* one word: arrival count in bits 0-30, generation in bit 31;
+                                   the last arrival of a barrier flips the generation */
 #define PK_BARRIER_COUNTER 1    /* one monotonic count word; generation = count / CTAs */
 
 /* ---- task kinds for the mailbox ---------------------------------------- */
@@ -203,8 +204,11 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
  * reduced in the kernel when k % check_every == 0 (L2 norm: exact squares
  * summed per thread as a float pair, across threads in fp64, to about 1e-12
  * relative; and max|r| exactly); the run stops at the first checked k > 0 with
- * ||r_k|| < tol * ||r_0|| and keeps U_k, else it stops at k = n.  The
- * current buffer afterwards holds U_{sweeps_done}.  Blocks until done.
+ * ||r_k|| < tol * ||r_0|| and keeps U_k, else it stops at k = n.  A residual
+ * that overflows (r = +-inf, where 4C or t is beyond the float range) makes
+ * that check's L2 norm NaN, as a compensated double sum gives too; max|r| is
+ * then +inf, and NaN never passes the exit test.  The current buffer
+ * afterwards holds U_{sweeps_done}.  Blocks until done.
  * info may be NULL.  Errors: PK_EINVAL (n < 0), PK_EBUSY (task kernel live),
  * PK_ENORESIDENT, PK_ETIMEDOUT (a barrier wait expired), PK_ECUDA. */
 int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
@@ -244,9 +248,33 @@ int pk_run_redblack(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_i
  * pk_run_redblack. */
 int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
 
+/* Pipelined independent problems ([P3] "Stream concurrency": copies on
+ * streams of their own, concurrent with the kernel).  Problem i starts from
+ * the packed (ny+2) x (nx+2) HOST field host_in[i] (ring and initial
+ * interior) with the context's size and source, runs pk_run_sweeps(n, tol,
+ * check_every) on it, and its result (the field pk_get_field would return)
+ * goes to the packed HOST array host_out[i]; infos[i] (may be NULL) gets its
+ * pk_run_info (current names the buffer of the problem's own pair).  The
+ * results are bit for bit those of pk_set_field + pk_run_sweeps +
+ * pk_get_field per problem.  While problem i sweeps, problem i+1's field
+ * goes up and problem i-1's result comes down, on two copy streams of the
+ * context; the sweeps themselves run one after another on the context's
+ * stream, so no two cooperative grids are ever in flight together.  Host
+ * arrays should be page-locked (cudaHostAlloc / cudaHostRegister) for the
+ * copies to overlap.  On first use the call allocates three field pairs of
+ * the context's layout (kept until pk_destroy); it neither reads nor
+ * changes the context's own field.  Blocks until every result is on the
+ * host.  Errors: PK_EINVAL, PK_EBUSY (task kernel live), PK_ENORESIDENT,
+ * PK_ETIMEDOUT (a barrier wait expired; later problems are not run),
+ * PK_ECUDA. */
+int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *const *host_out,
+                 int64_t n, float tol, int check_every, pk_run_info *infos);
+
 /* Copy the current iterate to / from a packed (ny+2) x (nx+2) HOST array.
- * pk_set_field writes both buffers (ring included) and makes buffer A
- * current.  Errors: PK_EINVAL, PK_EBUSY (task kernel live), PK_ECUDA. */
+ * pk_set_field writes buffer A (ring and interior), copies the ring into
+ * buffer B and makes A current; B's interior keeps whatever it held (every
+ * sweep writes all of it before any pass reads it).  Errors: PK_EINVAL,
+ * PK_EBUSY (task kernel live), PK_ECUDA. */
 int pk_get_field(pk_ctx *ctx, float *host_out);
 int pk_set_field(pk_ctx *ctx, const float *host_in);
 
@@ -292,10 +320,11 @@ void pk_destroy(pk_ctx *ctx);
 const char *pk_last_error(const pk_ctx *ctx);
 
 /* The persistent sweep of pk_run_sweeps for callers that cannot allocate
- * device memory: code running inside CUDA graph capture, under a framework
- * or pool allocator that owns all device memory, or in a loop that cannot
- * afford the device-wide synchronisation cudaMalloc/cudaFree may cause.
- * (The pages have no counterpart; this is a library convenience.)
+ * device memory: code under a framework or pool allocator that owns all of
+ * the device's memory and forbids allocations behind its back, and loops
+ * that cannot afford the device-wide synchronisation that cudaMalloc and
+ * cudaFree may cause.  (The pages have no counterpart; this is a library
+ * convenience.)
  *
  * It allocates nothing.  The caller passes the two pitched field buffers
  * (layout as pk_create_device; `current` = 0 if u_a holds the starting
@@ -308,7 +337,9 @@ const char *pk_last_error(const pk_ctx *ctx);
  * multi-sweep STREAM shape, single sweeps STREAM or DIRECT by footprint.
  * The result is bit for bit pk_run_sweeps's; info->current names the buffer
  * holding it; info->variant, stream_config and sweeps_per_pass say what ran;
- * info->device_us is 0 (no events are created).  Blocks until done.
+ * info->device_us is 0 (no events are created).  After the launch the call
+ * copies the result record to the host and synchronises the stream, so it
+ * blocks until the sweeps are done.
  *
  * Scratch (grid-barrier words, residual partials, result record) lives in
  * one file-scope device array of about 66 KB that every GPU loading libpk

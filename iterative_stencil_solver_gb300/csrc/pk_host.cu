@@ -58,6 +58,10 @@ inline long long round_up(long long v, long long m) { return (v + m - 1) / m * m
 
 }  // namespace
 
+// Problems in flight in pk_run_batch: one uploading, one sweeping, one
+// downloading.
+constexpr int kBatchSlots = 3;
+
 struct pk_ctx {
     int nx = 0, ny = 0;
     long long pitch = 0, gpitch = 0;
@@ -109,6 +113,14 @@ struct pk_ctx {
     int task_status = PK_OK;
     int run_id = 0;
     bool dirty_sweep = false;
+    // pk_run_batch: its own field pairs, one per pipeline slot (allocated on
+    // first use), the copy streams and the per-slot events and records.
+    float *bu[kBatchSlots][2] = {};
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t ev_in[kBatchSlots] = {}, ev_t0[kBatchSlots] = {}, ev_t1[kBatchSlots] = {},
+                ev_rec[kBatchSlots] = {}, ev_out[kBatchSlots] = {};
+    RunRecord *h_rec = nullptr;       // kBatchSlots records in mapped pinned memory
+    RunRecord *d_rec = nullptr;       // their device view
     // pk_run_sweeps_graph: instantiated graphs keyed by
     // (check sweep first, plain sweeps, buffer parity, direction parity, grid)
     std::map<std::tuple<int, long long, int, int, int>, cudaGraphExec_t> graphs;
@@ -506,13 +518,14 @@ int bar_status(pk_ctx *ctx, BarrierState *dev_bar, const char *what) {
     return PK_OK;
 }
 
+// The packed host field into buffer A, and its ring into buffer B.  B's
+// interior is left as it is: every sweep writes all of it before any pass
+// reads it, so only the ring (which sweeps never write) must match.
 int write_field(pk_ctx *ctx, const float *host) {
     const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
     PK_TRY(ctx, cudaMemcpy2DAsync(ctx->u[0] + 3, sizeof(float) * (size_t)ctx->pitch, host, row, row,
                                   (size_t)(ctx->ny + 2), cudaMemcpyHostToDevice, ctx->stream));
-    PK_TRY(ctx, cudaMemcpyAsync(ctx->u[1], ctx->u[0],
-                                sizeof(float) * (size_t)ctx->pitch * (size_t)(ctx->ny + 2),
-                                cudaMemcpyDeviceToDevice, ctx->stream));
+    PK_TRY(ctx, launch_copy_ring(ctx->u[0], ctx->u[1], ctx->nx, ctx->ny, ctx->pitch, ctx->stream));
     ctx->cur = 0;
     return PK_OK;
 }
@@ -569,6 +582,19 @@ void release(pk_ctx *ctx) {
     if (ctx->ev1) cudaEventDestroy(ctx->ev1);
     if (ctx->ev_sync) cudaEventDestroy(ctx->ev_sync);
     for (auto &kv : ctx->graphs) cudaGraphExecDestroy(kv.second);
+    if (ctx->s_in) cudaStreamSynchronize(ctx->s_in);
+    if (ctx->s_out) cudaStreamSynchronize(ctx->s_out);
+    for (int q = 0; q < kBatchSlots; ++q) {
+        cudaFree(ctx->bu[q][0]);
+        cudaFree(ctx->bu[q][1]);
+        cudaEvent_t *evs[] = {&ctx->ev_in[q], &ctx->ev_t0[q], &ctx->ev_t1[q], &ctx->ev_rec[q],
+                              &ctx->ev_out[q]};
+        for (cudaEvent_t *ev : evs)
+            if (*ev) cudaEventDestroy(*ev);
+    }
+    if (ctx->h_rec) cudaFreeHost(ctx->h_rec);
+    if (ctx->s_in) cudaStreamDestroy(ctx->s_in);
+    if (ctx->s_out) cudaStreamDestroy(ctx->s_out);
     if (ctx->task_stream) cudaStreamDestroy(ctx->task_stream);
     if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
     delete ctx;
@@ -622,6 +648,32 @@ int task_finish(pk_ctx *ctx) {
     }
     ctx->task_status = (st == PK_ESHUTDOWN) ? PK_ESHUTDOWN : (int)st;
     return PK_OK;
+}
+
+// The persistent kernel a run of n sweeps takes.  Several sweeps per pass
+// pay off whenever a run has two or more: the kernels shorten a pass where
+// the end or a residual check would fall inside it.
+void choose_persistent(const pk_ctx *ctx, int64_t n, int *kernel_out, int *shape_out,
+                       int *grid_out, int *depth_out) {
+    const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
+    int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
+    if (ctx->stream_cfg2 >= 0 && multi_ok) {
+        kernel = kVariantStream;
+        shape = ctx->stream_cfg2;
+        grid = ctx->grid2;
+    }
+    if (kernel == kVariantStream && multi_ok) depth = stream_depth(shape);
+    if (ctx->variant == kVariantLocal && ctx->local_depth >= 2 &&
+        !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS)) {
+        // passes take up to local_depth sweeps, never past a check
+        kernel = kVariantLocalD;
+        shape = ctx->local_depth;
+        depth = ctx->local_depth;
+    }
+    *kernel_out = kernel;
+    *shape_out = shape;
+    *grid_out = grid;
+    *depth_out = depth;
 }
 
 }  // namespace
@@ -681,7 +733,8 @@ int pk_create(int nx, int ny, const float *u0, const float *f, const pk_options 
         return bail(cuda_fail(ctx, e, "cudaMalloc(field)"));
     ctx->own_u = true;
     if ((rc = common_setup(ctx)) != PK_OK) return bail(rc);
-    if ((e = cudaMemsetAsync(ctx->u[0], 0, fbytes, ctx->stream)) != cudaSuccess)
+    if ((e = cudaMemsetAsync(ctx->u[0], 0, fbytes, ctx->stream)) != cudaSuccess ||
+        (e = cudaMemsetAsync(ctx->u[1], 0, fbytes, ctx->stream)) != cudaSuccess)
         return bail(cuda_fail(ctx, e, "cudaMemsetAsync(field)"));
     if ((rc = write_field(ctx, u0)) != PK_OK) return bail(rc);
     if (f) {
@@ -763,24 +816,8 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.check_every = check_every;
     if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
         PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0, local_halo_bytes(ctx), ctx->stream));
-    // Several sweeps per pass pay off whenever a run has two or more: the
-    // kernels shorten a pass where the end or a residual check would fall
-    // inside it.
-    const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
-    int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
-    if (ctx->stream_cfg2 >= 0 && multi_ok) {
-        kernel = kVariantStream;
-        shape = ctx->stream_cfg2;
-        grid = ctx->grid2;
-    }
-    if (kernel == kVariantStream && multi_ok) depth = stream_depth(shape);
-    if (ctx->variant == kVariantLocal && ctx->local_depth >= 2 &&
-        !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS)) {
-        // passes take up to local_depth sweeps, never past a check
-        kernel = kVariantLocalD;
-        shape = ctx->local_depth;
-        depth = ctx->local_depth;
-    }
+    int kernel, shape, grid, depth;
+    choose_persistent(ctx, n, &kernel, &shape, &grid, &depth);
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
@@ -805,6 +842,192 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
               kernel == kVariantStream ? kernel : 0, shape, depth);
     return PK_OK;
 }
+
+}  // extern "C"
+
+// ---- pipelined problems ---------------------------------------------------
+
+namespace {
+
+int ensure_batch(pk_ctx *ctx) {
+    if (ctx->s_in) return PK_OK;
+    const size_t fbytes = sizeof(float) * (size_t)ctx->pitch * (size_t)(ctx->ny + 2);
+    for (int q = 0; q < kBatchSlots; ++q) {
+        for (int b = 0; b < 2; ++b) {
+            PK_TRY(ctx, cudaMalloc(&ctx->bu[q][b], fbytes));
+            // pad columns hold defined values (no pass uses them)
+            PK_TRY(ctx, cudaMemsetAsync(ctx->bu[q][b], 0, fbytes, ctx->stream));
+        }
+        PK_TRY(ctx, cudaEventCreateWithFlags(&ctx->ev_in[q], cudaEventDisableTiming));
+        PK_TRY(ctx, cudaEventCreate(&ctx->ev_t0[q]));
+        PK_TRY(ctx, cudaEventCreate(&ctx->ev_t1[q]));
+        PK_TRY(ctx, cudaEventCreateWithFlags(&ctx->ev_rec[q], cudaEventDisableTiming));
+        PK_TRY(ctx, cudaEventCreateWithFlags(&ctx->ev_out[q], cudaEventDisableTiming));
+    }
+    PK_TRY(ctx, cudaHostAlloc(&ctx->h_rec, sizeof(RunRecord) * kBatchSlots, cudaHostAllocMapped));
+    std::memset(ctx->h_rec, 0, sizeof(RunRecord) * kBatchSlots);
+    PK_TRY(ctx, cudaHostGetDevicePointer((void **)&ctx->d_rec, ctx->h_rec, 0));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    cudaStream_t in = nullptr, out = nullptr;
+    PK_TRY(ctx, cudaStreamCreateWithFlags(&in, cudaStreamNonBlocking));
+    cudaError_t e = cudaStreamCreateWithFlags(&out, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+        cudaStreamDestroy(in);
+        return cuda_fail(ctx, e, "cudaStreamCreateWithFlags(batch)");
+    }
+    ctx->s_in = in;
+    ctx->s_out = out;
+    return PK_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *const *host_out,
+                 int64_t n, float tol, int check_every, pk_run_info *infos) {
+    if (!ctx) return PK_EINVAL;
+    if (count < 0 || (count > 0 && (!host_in || !host_out)))
+        return fail(ctx, PK_EINVAL, "pk_run_batch: bad count or NULL arrays");
+    for (int i = 0; i < count; ++i)
+        if (!host_in[i] || !host_out[i]) return fail(ctx, PK_EINVAL, "pk_run_batch: NULL field %d", i);
+    if (n < 0) return fail(ctx, PK_EINVAL, "pk_run_batch: n < 0");
+    if (!(tol == tol)) return fail(ctx, PK_EINVAL, "pk_run_batch: tol is NaN");
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_run_batch: the task kernel is live");
+    if (count == 0) return PK_OK;
+    int rc = ensure_batch(ctx);
+    if (rc != PK_OK) return rc;
+    int kernel, shape, grid, depth;
+    choose_persistent(ctx, n, &kernel, &shape, &grid, &depth);
+    const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
+    const size_t dpitch = sizeof(float) * (size_t)ctx->pitch;
+    const size_t rows = (size_t)(ctx->ny + 2);
+    cudaStream_t sc = ctx->stream;
+    BarrierState *dbar = &ctx->scratch->bar_sweep;
+    int run_ids[kBatchSlots] = {0, 0, 0};
+
+    // Problem j's field into slot j % kBatchSlots, once the download of the
+    // problem that used the slot before has finished with it.
+    auto upload = [&](int j) -> cudaError_t {
+        const int q = j % kBatchSlots;
+        cudaError_t e = cudaStreamWaitEvent(ctx->s_in, ctx->ev_out[q], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(ctx->bu[q][0] + 3, dpitch, host_in[j], row, row, rows,
+                                  cudaMemcpyHostToDevice, ctx->s_in);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_in[q], ctx->s_in);
+        return e;
+    };
+    // Problem j's sweeps on the context's stream: every cooperative launch
+    // goes to that one stream, so two are never in flight at once.  Only
+    // kernels run on that stream -- the ring copy (which also zeroes the
+    // barrier words, base 0, and the LOCAL halo tags), the sweeps, and a
+    // one-thread kernel that stores the result record into mapped host
+    // memory -- so nothing on it waits for a copy engine busy with another
+    // problem's field.
+    auto sweep = [&](int j) -> cudaError_t {
+        const int q = j % kBatchSlots;
+        cudaError_t e = cudaStreamWaitEvent(sc, ctx->ev_in[q], 0);
+        const bool local = ctx->variant == kVariantLocal;
+        if (e == cudaSuccess)
+            e = launch_copy_ring(ctx->bu[q][0], ctx->bu[q][1], ctx->nx, ctx->ny, ctx->pitch, sc, dbar,
+                                 sizeof(BarrierState), local ? ctx->halo : nullptr,
+                                 local ? local_halo_bytes(ctx) : 0);
+        SweepParams p = base_params(ctx);
+        p.u[0] = ctx->bu[q][0];
+        p.u[1] = ctx->bu[q][1];
+        p.cur = 0;
+        p.n = n;
+        p.tol = tol;
+        p.check_every = check_every;
+        p.bar_base = 0;
+        p.profile = 0;
+        run_ids[q] = p.run_id;
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t0[q], sc);
+        if (e == cudaSuccess) e = launch_persistent(kernel, ctx->poisson, shape, grid, p, sc);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t1[q], sc);
+        if (e == cudaSuccess) e = launch_publish_record(p.info, dbar, &ctx->d_rec[q], sc);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_rec[q], sc);
+        return e;
+    };
+    auto drain = [&]() {
+        cudaStreamSynchronize(sc);
+        cudaStreamSynchronize(ctx->s_in);
+        cudaStreamSynchronize(ctx->s_out);
+    };
+    cudaError_t e = cudaSuccess;
+    for (int j = 0; j < count && j < kBatchSlots && e == cudaSuccess; ++j) e = upload(j);
+    if (e == cudaSuccess) e = sweep(0);
+    if (e != cudaSuccess) {
+        drain();
+        return cuda_fail(ctx, e, "pk_run_batch: first problem");
+    }
+    unsigned last_count_end = 0;
+    for (int i = 0; i < count; ++i) {
+        const int q = i % kBatchSlots;
+        // queue the next problem's sweeps behind this one's before waiting
+        if (i + 1 < count && (e = sweep(i + 1)) != cudaSuccess) {
+            drain();
+            return cuda_fail(ctx, e, "pk_run_batch: sweep launch");
+        }
+        if ((e = cudaEventSynchronize(ctx->ev_rec[q])) != cudaSuccess) {
+            drain();
+            return cuda_fail(ctx, e, "pk_run_batch: sweeps");
+        }
+        const RunRecord &d = ctx->h_rec[q];
+        const int code = d.error;
+        if (code != 0 || d.run_id != run_ids[q]) {
+            drain();
+            cudaMemsetAsync(dbar, 0, sizeof(BarrierState), sc);
+            cudaStreamSynchronize(sc);
+            ctx->sweep_bar_base = 0;
+            if (code != 0)
+                return fail(ctx, code, "pk_run_batch: problem %d: device reported %d at site %u (CTA %u)",
+                            i, code, d.site, d.bad_cta);
+            return fail(ctx, PK_EDEVICE, "pk_run_batch: problem %d: kernel did not report", i);
+        }
+        last_count_end = d.bar_count_end;
+        const int cur = d.cur;
+        if (infos) {
+            pk_run_info &inf = infos[i];
+            inf.sweeps_done = d.sweeps_done;
+            inf.res0 = d.res0;
+            inf.res_last = d.res_last;
+            inf.res_max_last = d.rmax_last;
+            inf.status = PK_OK;
+            inf.n_checks = d.n_checks;
+            inf.current = cur;
+            inf.grid = grid;
+            inf.variant = kernel == kVariantStream ? (int)kVariantStream
+                          : kernel == kVariantLocalD ? (int)kVariantLocal : kernel;
+            inf.stream_config = kernel == kVariantStream ? shape : -1;
+            inf.sweeps_per_pass = depth;
+            float ms = 0.f;
+            inf.device_us = cudaEventElapsedTime(&ms, ctx->ev_t0[q], ctx->ev_t1[q]) == cudaSuccess
+                                ? (double)ms * 1000.0 : -1.0;
+        }
+        // the result down on the copy-out stream; the slot's next upload waits for it
+        e = cudaStreamWaitEvent(ctx->s_out, ctx->ev_rec[q], 0);
+        if (e == cudaSuccess)
+            e = cudaMemcpy2DAsync(host_out[i], row, ctx->bu[q][cur] + 3, dpitch, row, rows,
+                                  cudaMemcpyDeviceToHost, ctx->s_out);
+        if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_out[q], ctx->s_out);
+        if (e == cudaSuccess && i + kBatchSlots < count) e = upload(i + kBatchSlots);
+        if (e != cudaSuccess) {
+            drain();
+            return cuda_fail(ctx, e, "pk_run_batch: copies");
+        }
+    }
+    if ((e = cudaStreamSynchronize(ctx->s_out)) != cudaSuccess) {
+        drain();
+        return cuda_fail(ctx, e, "pk_run_batch: download");
+    }
+    ctx->sweep_bar_base = last_count_end;
+    return PK_OK;
+}
+
+}  // extern "C"
+
+extern "C" {
 
 int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info) {
     if (!ctx) return PK_EINVAL;

@@ -256,6 +256,23 @@ cudaError_t launch_persistent_local_rb(bool poisson, int grid, const SweepParams
                                        cudaStream_t s);
 cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long long gpitch,
                                 float h2, cudaStream_t s);
+// Copies the Dirichlet ring (two rows, two columns) of a pitched field, and
+// zeroes up to two byte ranges (multiples of 4 bytes; NULL/0 = none).
+cudaError_t launch_copy_ring(const float *src, float *dst, int nx, int ny, long long pitch,
+                             cudaStream_t s, void *zero0 = nullptr, size_t bytes0 = 0,
+                             void *zero1 = nullptr, size_t bytes1 = 0);
+// A run's result record, as the host reads it from mapped pinned memory.
+struct RunRecord {
+    long long sweeps_done;
+    double res0, res_last;
+    float rmax_last;
+    int n_checks, cur, run_id;
+    unsigned bar_count_end;
+    int error;
+    unsigned site, bad_cta;
+};
+cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
+                                  cudaStream_t s);
 cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s);
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,
                         cudaStream_t s);

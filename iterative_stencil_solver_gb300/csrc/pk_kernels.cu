@@ -23,6 +23,8 @@
 //     (reused as the barrier-only microbenchmark).
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "pk_sweep.cuh"
 
 namespace cg = cooperative_groups;
@@ -238,6 +240,36 @@ __global__ void k_scale_source(const float *__restrict__ f, float *__restrict__ 
         const long long j = q / gpitch;
         const long long i = q - j * gpitch;
         g[q] = i < nx ? __fmul_rn(h2, f[j * nx + i]) : 0.f;
+    }
+}
+
+// The Dirichlet ring of src (rows 0 and ny+1, columns 0 and nx+1) into dst:
+// the other buffer of a pair needs only the ring, since every sweep writes
+// the whole interior before a pass reads it.  Thread q < 2(nx+2) takes a
+// cell of the two ring rows, the rest the two ring columns of rows 1..ny.
+// The same launch zeroes up to two word ranges (a run's barrier words and
+// halo tags), so that a run queued behind copies needs no memset.
+__global__ void k_copy_ring(const float *__restrict__ src, float *__restrict__ dst, int nx, int ny,
+                            long long pitch, unsigned *z0, long long n0, unsigned *z1,
+                            long long n1) {
+    const long long rows_cells = 2LL * (nx + 2);
+    const long long total = rows_cells + 2LL * ny;
+    const long long first = blockIdx.x * (long long)blockDim.x + threadIdx.x;
+    const long long stride = (long long)gridDim.x * blockDim.x;
+    for (long long q = first; q < n0; q += stride) z0[q] = 0u;
+    for (long long q = first; q < n1; q += stride) z1[q] = 0u;
+    for (long long q = first; q < total; q += stride) {
+        long long off;
+        if (q < rows_cells) {
+            const long long j = q < nx + 2 ? 0 : ny + 1;
+            const long long i = q < nx + 2 ? q : q - (nx + 2);
+            off = j * pitch + i + 3;
+        } else {
+            const long long r = q - rows_cells;
+            const long long j = 1 + (r >> 1);
+            off = j * pitch + ((r & 1) ? nx + 1 : 0) + 3;
+        }
+        dst[off] = src[off];
     }
 }
 
@@ -603,7 +635,14 @@ __global__ void __launch_bounds__(256) k_stress_tma(BarrierCtl ctl, int rounds, 
 // Launch wrappers.
 bool g_cfg_ok[2][kNumStreamConfigs];
 
+// Contexts and the no-allocation entry point call this on whatever thread
+// creates them: one lock serialises the calls, and the tables are computed
+// into locals and published once, so a reader never sees a shape marked
+// usable that the call then clears.
+std::mutex g_prepare_mutex;
+
 cudaError_t prepare_kernels() {
+    std::lock_guard<std::mutex> lock(g_prepare_mutex);
     int dev = 0, optin = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -631,19 +670,20 @@ cudaError_t prepare_kernels() {
         if (e != cudaSuccess) return e;
         if ((size_t)lim < local_max) local_max = (size_t)lim;
     }
-    g_local_smem_max = local_max;
+    bool ok[2][kNumStreamConfigs];
     for (int poisson = 0; poisson < 2; ++poisson) {
         for (int c = 0; c < kNumStreamConfigs; ++c) {
             const size_t bytes = stream_smem_bytes(c, poisson != 0);
-            g_cfg_ok[poisson][c] = true;
+            bool fits = true;
             for (int persistent = 0; persistent < 2; ++persistent) {
                 const void *fn = poisson ? stream_kernel(true, c, persistent != 0)
                                          : stream_kernel(false, c, persistent != 0);
                 int lim = 0;
                 if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
-                if (bytes > (size_t)lim) g_cfg_ok[poisson][c] = false;
+                if (bytes > (size_t)lim) fits = false;
             }
-            if (!g_cfg_ok[poisson][c]) continue;
+            ok[poisson][c] = fits;
+            if (!fits) continue;
             for (int persistent = 0; persistent < 2; ++persistent) {
                 const void *fn = poisson ? stream_kernel(true, c, persistent != 0)
                                          : stream_kernel(false, c, persistent != 0);
@@ -653,6 +693,9 @@ cudaError_t prepare_kernels() {
             }
         }
     }
+    g_local_smem_max = local_max;
+    for (int poisson = 0; poisson < 2; ++poisson)
+        for (int c = 0; c < kNumStreamConfigs; ++c) g_cfg_ok[poisson][c] = ok[poisson][c];
     return cudaSuccess;
 }
 
@@ -758,6 +801,49 @@ cudaError_t launch_scale_source(const float *f, float *g, int nx, int ny, long l
     if (blocks > 65535) blocks = 65535;
     if (blocks < 1) blocks = 1;
     k_scale_source<<<(unsigned)blocks, 256, 0, s>>>(f, g, nx, ny, gpitch, h2);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_ring(const float *src, float *dst, int nx, int ny, long long pitch,
+                             cudaStream_t s, void *zero0, size_t bytes0, void *zero1,
+                             size_t bytes1) {
+    const long long n0 = (long long)(bytes0 / 4), n1 = (long long)(bytes1 / 4);
+    long long total = 2LL * (nx + 2) + 2LL * ny;
+    if (n0 > total) total = n0;
+    if (n1 > total) total = n1;
+    long long blocks = (total + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    k_copy_ring<<<(unsigned)blocks, 256, 0, s>>>(src, dst, nx, ny, pitch,
+                                                  static_cast<unsigned *>(zero0), n0,
+                                                  static_cast<unsigned *>(zero1), n1);
+    return cudaGetLastError();
+}
+
+// A run's result record and barrier status into mapped pinned host memory,
+// with plain stores over the interconnect (no copy engine).
+__global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar,
+                                 RunRecord *out) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        volatile const DeviceInfo *vi = info;
+        out->sweeps_done = vi->sweeps_done;
+        out->res0 = vi->res0;
+        out->res_last = vi->res_last;
+        out->rmax_last = vi->rmax_last;
+        out->n_checks = vi->n_checks;
+        out->cur = vi->cur;
+        out->run_id = vi->run_id;
+        out->bar_count_end = vi->bar_count_end;
+        volatile const BarrierState *vb = bar;
+        out->error = (int)vb->error.v;
+        out->site = vb->site.v;
+        out->bad_cta = vb->bad_cta.v;
+        __threadfence_system();
+    }
+}
+
+cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
+                                  cudaStream_t s) {
+    k_publish_record<<<1, 32, 0, s>>>(info, bar, out);
     return cudaGetLastError();
 }
 

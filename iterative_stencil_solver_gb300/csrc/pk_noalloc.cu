@@ -1,14 +1,14 @@
 // pk_noalloc.cu -- pk_run_sweeps_noalloc: the persistent sweep for callers
 // that cannot allocate device memory.
 //
-// Who needs it: code that runs where cudaMalloc is off limits -- inside a
-// region being captured into a CUDA graph (cudaMalloc is not a stream
-// operation and breaks or serialises capture), under an application memory
-// pool or framework allocator that owns all device memory and forbids
-// outside allocations, or in a latency-critical loop that cannot afford the
-// implicit device synchronisation cudaMalloc/cudaFree may cause.  Such a
-// caller owns the field buffers (and the optional source) and wants the
-// solver to run on them without any allocation of its own.
+// Who needs it: code that runs where cudaMalloc is off limits -- under an
+// application memory pool or framework allocator that owns all device
+// memory and forbids outside allocations, or in a latency-critical loop that
+// cannot afford the implicit device synchronisation cudaMalloc/cudaFree may
+// cause.  Such a caller owns the field buffers (and the optional source) and
+// wants the solver to run on them without any allocation of its own.  The
+// call reads its result record back and synchronises the stream before it
+// returns.
 //
 // The persistent kernel needs scratch memory besides its inputs and outputs:
 // the grid-barrier words, the per-CTA residual partials and the result

@@ -33,7 +33,6 @@ __device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
     ctl.skip_at = p.skip_at;
     ctl.index = 0;
     ctl.base = p.bar_base;
-    ctl.gen = 0u;
     ctl.profile = p.profile;
     ctl.spin_ns = 0ull;
     barrier_begin(ctl);

@@ -135,6 +135,9 @@ _SIGS = {
                                              _VP, _VP, ctypes.c_int, ctypes.c_int64,
                                              ctypes.c_float, ctypes.c_int,
                                              ctypes.POINTER(pk_run_info)]),
+    "pk_run_batch": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(_F32P),
+                                    ctypes.POINTER(_F32P), ctypes.c_int64, ctypes.c_float,
+                                    ctypes.c_int, ctypes.POINTER(pk_run_info)]),
     "pk_get_field": (ctypes.c_int, [_VP, _F32P]),
     "pk_set_field": (ctypes.c_int, [_VP, _F32P]),
     "pk_device_field": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(_VP), _I64P,
@@ -294,6 +297,27 @@ def pk_get_field(ctx, out=None):
 def pk_set_field(ctx, u):
     u = _f32c(u, (ctx.ny + 2, ctx.nx + 2), "u")
     _check(_lib.pk_set_field(ctx, u.ctypes.data_as(_F32P)), ctx)
+
+
+def pk_run_batch(ctx, fields_in, fields_out, n, tol=0.0, check_every=0):
+    """Runs one problem per entry of fields_in (packed (ny+2, nx+2) float32
+    host arrays, page-locked for the copies to overlap the sweeps); each
+    result is written into the matching entry of fields_out, which must be
+    C-contiguous float32 arrays of the same shape.  Returns the list of
+    per-problem info dicts."""
+    shape = (ctx.ny + 2, ctx.nx + 2)
+    count = len(fields_in)
+    if len(fields_out) != count:
+        raise ValueError("fields_in and fields_out differ in length")
+    ins = [_f32c(u, shape, "fields_in[%d]" % q) for q, u in enumerate(fields_in)]
+    for q, out in enumerate(fields_out):
+        if out.dtype != np.float32 or not out.flags.c_contiguous or out.shape != shape:
+            raise ValueError("fields_out[%d] must be a C-contiguous float32 %s array" % (q, shape))
+    in_ptrs = (_F32P * max(count, 1))(*[u.ctypes.data_as(_F32P) for u in ins])
+    out_ptrs = (_F32P * max(count, 1))(*[u.ctypes.data_as(_F32P) for u in fields_out])
+    infos = (pk_run_info * max(count, 1))()
+    _check(_lib.pk_run_batch(ctx, count, in_ptrs, out_ptrs, n, tol, check_every, infos), ctx)
+    return [infos[q].as_dict() for q in range(count)]
 
 
 def pk_device_field(ctx, which):

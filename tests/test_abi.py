@@ -136,6 +136,8 @@ def test_null_context_calls(pk):
         fn = getattr(lib, name)
         fn.argtypes = pk._SIGS[name][1]
         assert fn(None, 1, 0.0, 0, None) == pk.PK_EINVAL
+    lib.pk_run_batch.argtypes = pk._SIGS["pk_run_batch"][1]
+    assert lib.pk_run_batch(None, 1, None, None, 1, 0.0, 0, None) == pk.PK_EINVAL
     lib.pk_poll.argtypes = pk._SIGS["pk_poll"][1]
     assert lib.pk_poll(None, 1) == pk.PK_EINVAL
     lib.pk_shutdown.argtypes = pk._SIGS["pk_shutdown"][1]

@@ -160,6 +160,67 @@ def test_zero_sweeps_and_field_roundtrip(pk):
         pk.pk_destroy(ctx)
 
 
+# pk_set_field writes buffer A and only the ring of buffer B: a field whose
+# ring differs from the previous one must give the same bits on every
+# variant, whichever buffer the passes end in (odd and even sweep counts,
+# passes of one to four sweeps).
+@pytest.mark.parametrize("variant,nx,ny", [(0, 33, 17), (1, 300, 41), (2, 2100, 37),
+                                           (3, 300, 41)],
+                         ids=["auto-local", "direct", "stream", "local"])
+def test_set_field_new_ring_every_variant(pk, variant, nx, ny):
+    u0 = inputs.random_field(nx, ny, seed=21)
+    ctx = pk.pk_create(nx, ny, u0, None, pk.pk_options_default(variant=variant))
+    try:
+        pk.pk_run_sweeps(ctx, 5)
+        for seed, n in ((22, 7), (23, 8), (24, 1)):
+            u1 = inputs.random_field(nx, ny, seed=seed)
+            pk.pk_set_field(ctx, u1)
+            info = pk.pk_run_sweeps(ctx, n, 1e-30, 3)
+            want, oinfo = oracle.jacobi_run(u1, n=n, tol=1e-30, check_every=3)
+            assert_same_bits(pk.pk_get_field(ctx), want)
+            check_info(info, oinfo)
+            pk.pk_set_field(ctx, u1)
+            pk.pk_run_sweeps_launch(ctx, n)
+            want, _ = oracle.jacobi_run(u1, n=n)
+            assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
+# pk_run_batch: several problems with their own fields (rings included) run
+# through three pipeline slots; each result and its info must equal the
+# oracle's for that problem alone, and the context's own field is untouched.
+@pytest.mark.parametrize("nx,ny,poisson,n,tol,ce", [
+    (300, 41, False, 7, 1e-30, 3),      # LOCAL
+    (2100, 37, True, 9, 1e-30, 4),      # multi-sweep STREAM (Poisson)
+    (1793, 20, False, 11, 0.0, 0),      # Laplace, one-column last strip
+    (16, 16, True, 100000, 1e-4, 10),   # early exit
+], ids=["local", "stream-poisson", "stream-laplace", "early-exit"])
+def test_run_batch_matches_oracle(pk, nx, ny, poisson, n, tol, ce):
+    u0 = inputs.random_field(nx, ny, seed=31)
+    f = inputs.uniform_pm1(32, nx * ny).reshape(ny, nx) if poisson else None
+    count = 5
+    fields = [inputs.random_field(nx, ny, seed=40 + q) for q in range(count)]
+    if nx == 16:
+        fields = [np.zeros_like(u0) for _ in range(count)]
+    outs = [np.full((ny + 2, nx + 2), np.nan, dtype=np.float32) for _ in range(count)]
+    ctx = pk.pk_create(nx, ny, u0, f)
+    try:
+        for rep in range(2):
+            infos = pk.pk_run_batch(ctx, fields, outs, n, tol, ce)
+            for q in range(count):
+                want, oinfo = oracle.jacobi_run(fields[q], f=f, n=n, tol=tol, check_every=ce)
+                assert_same_bits(outs[q], want, "problem %d" % q)
+                check_info(infos[q], oinfo)
+        assert_same_bits(pk.pk_get_field(ctx), u0, "context field")
+        # the context still runs from its own field afterwards
+        pk.pk_run_sweeps(ctx, 3)
+        want, _ = oracle.jacobi_run(u0, f=f, n=3)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
 def test_create_device_with_torch_buffers(pk):
     import torch
     nx, ny, n = 1500, 40, 9
@@ -223,7 +284,7 @@ def test_poisson_4096_residual_every_10(pk, path):
 def test_laplace_random_16384_full_field(pk):
     w = inputs.workload_laplace_random(16384, seed=3)
     got, info = run_pk(pk, w["u0"], None, 100)
-    # the launch configuration bench.py times: the default plan's two-sweep STREAM shape
+    # the launch configuration bench.py times: the default plan's three-sweep STREAM shape
     assert info["sweeps_done"] == 100 and info["variant"] == 2 and info["sweeps_per_pass"] == 3
     want, _ = oracle.jacobi_run(w["u0"], n=100, threads=THREADS)
     assert_same_bits(got, want)
@@ -594,6 +655,56 @@ def test_barrier_kinds_stress_and_parity(pk, kind):
         got, info = run_pk(pk, u0, None, 40, 1e-30, 7, variant=variant, barrier_kind=kind)
         assert_same_bits(got, want)
         check_info(info, oinfo)
+
+
+# The ordering the STREAM sweep relies on between passes: rows written with
+# ordinary stores before the grid barrier are read after it through the
+# async proxy (TMA bulk copies).  Writers fence the generic proxy against the
+# async proxy; the copying thread acquires at gpu scope and fences the
+# proxies itself (mode 3, the only protocol run here).
+@pytest.mark.parametrize("kind", [0, 1], ids=["generation", "counter"])
+def test_barrier_stress_tma_readers(pk, kind):
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    u0 = inputs.random_field(512, 512, seed=1)
+    ctx = pk.pk_create(512, 512, u0, None, pk.pk_options_default(barrier_kind=kind))
+    try:
+        cap = pk.pk_get_plan(ctx)["coop_max"]
+        for grid in sorted({1, sms, 2 * sms, cap}):
+            rounds = 1500
+            sums, stale = pk.pk_barrier_stress_tma(ctx, grid, rounds, 3)
+            assert stale == 0, (kind, grid, stale)
+            assert np.array_equal(sums, oracle.barrier_stress_expected(grid, rounds, 32)), grid
+    finally:
+        pk.pk_destroy(ctx)
+
+
+# A residual that overflows: 4C is +inf for a cell of 1.5e38, so r = -inf
+# there.  The oracle's compensated sum then returns NaN, and so does the
+# kernels' float-pair sum; max|r| is +inf on both sides.  Later checks see
+# finite residuals again and must match as usual.
+@pytest.mark.parametrize("variant,path", [(0, "persistent"), (0, "launch"), (1, "persistent"),
+                                          (2, "persistent")],
+                         ids=["auto", "launch", "direct", "stream"])
+def test_residual_overflow_matches_oracle(pk, variant, path):
+    nx, ny = 300, 41
+    u0 = inputs.random_field(nx, ny, seed=91)
+    u0[20, 150] = np.float32(1.5e38)
+    u0[7, 299] = np.float32(-2.0e38)
+    want, oinfo = oracle.jacobi_run(u0, n=6, tol=1e-30, check_every=3)
+    got, info = run_pk(pk, u0, None, 6, 1e-30, 3, path=path, variant=variant)
+    assert_same_bits(got, want)
+    assert np.isnan(oinfo.res0) and np.isnan(info["res0"])
+    assert info["sweeps_done"] == oinfo.sweeps_done == 6
+    assert info["n_checks"] == oinfo.n_checks == 3
+    assert info["res_max_last"] == oinfo.rmax_last
+    assert info["res_last"] == pytest.approx(oinfo.res_last, rel=1e-10, abs=0)
+    # the first check alone: max|r| of U_0 is +inf on both sides
+    want0, oinfo0 = oracle.jacobi_run(u0, n=0, tol=1e-30, check_every=3)
+    got0, info0 = run_pk(pk, u0, None, 0, 1e-30, 3, path=path, variant=variant)
+    assert_same_bits(got0, want0)
+    assert oinfo0.rmax_last == np.inf and info0["res_max_last"] == np.inf
+    assert np.isnan(info0["res_last"]) and np.isnan(oinfo0.res_last)
 
 
 @pytest.mark.parametrize("kind", [0, 1], ids=["generation", "counter"])
