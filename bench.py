@@ -80,27 +80,46 @@ def shape_label(info, poisson):
         q, ring, depth, "s" if depth > 1 else "", "poisson" if poisson else "laplace")
 
 
-def passes_of(info, sweeps, tol, check_every):
-    """Passes a persistent run over `sweeps` sweeps took (no early exit):
-    (passes that store, check-only passes).  A shape of D sweeps per pass
-    takes up to D sweeps per pass, never past the end or a residual check."""
+def passes_of(info, sweeps, tol, check_every, exit_at=None):
+    """Passes a persistent run over `sweeps` sweeps takes: (passes that
+    store, check-only passes).  A shape of D sweeps per pass takes up to D
+    sweeps per pass, never past the end; a pass of fewer than three sweeps
+    stops at a residual check, while a three-sweep STREAM pass runs past one
+    (the check is taken in its stage 2 or 3) when no second check falls
+    inside it.  exit_at: the check at which the run stopped early (then a
+    straddled check costs one more pass, which sweeps again to that
+    iterate)."""
     checks = tol > 0 and check_every > 0
     depth = info["sweeps_per_pass"]
-    k, store_passes = 0, 0
-    while k < sweeps:
-        dp = min(depth, sweeps - k)
+    straddle = checks and bool(info.get("straddle"))
+    k, store_passes, check_only = 0, 0, 0
+    while True:
+        here = checks and k % check_every == 0
+        if k == sweeps:
+            check_only += 1 if here else 0
+            break
+        m, cs = sweeps - k, 1 if here else 0
         if checks:
-            dp = min(dp, check_every - k % check_every)
-        k += dp
+            to_check = check_every - k % check_every
+            if straddle and not here and to_check < depth and m >= depth \
+                    and to_check + check_every >= depth:
+                cs, m = to_check + 1, depth
+            elif to_check < m:
+                m = to_check
         store_passes += 1
-    check_only = 1 if checks and sweeps % check_every == 0 else 0
+        if cs and exit_at is not None and 0 < exit_at == k + cs - 1:
+            store_passes += 1 if cs >= 2 else 0
+            break
+        k += min(m, depth)
     return store_passes, check_only
 
 
 def algorithmic_bytes(info, cells, sweeps, poisson, tol, check_every):
     """Compulsory HBM bytes of one persistent run: every pass reads U (and g)
     once and, unless it only checks, writes U once."""
-    store_passes, check_only = passes_of(info, sweeps, tol, check_every)
+    done = info.get("sweeps_done", sweeps)
+    exit_at = done if done < sweeps else None
+    store_passes, check_only = passes_of(info, sweeps, tol, check_every, exit_at)
     src = 4.0 if poisson else 0.0
     return cells * (store_passes * (8.0 + src) + check_only * (4.0 + src))
 
@@ -463,23 +482,37 @@ def latency_extras(pk):
                                                       1000, variant=1),
     }
     del w
-    # Poisson 4096^2 with the in-kernel residual every 10 sweeps
+    # Poisson 4096^2 with the in-kernel residual every 10 sweeps: passes that
+    # straddle the checks (default) and passes that stop at them
     w = make_workload("poisson-4096x4096-2000sweeps-res10")
-    ctx = pk.pk_create(4096, 4096, w["u0"], w["f"])
-    try:
-        info = pk.pk_run_sweeps(ctx, 2000, 1e-4, 10)
-        us = info["device_us"] / max(1, info["sweeps_done"])
-        done = info["sweeps_done"]
-        out["poisson_4096_res10"] = {
-            "us_per_sweep": us, "sweeps_done": done,
-            "res_ratio": info["res_last"] / info["res0"] if info["res0"] else None,
-            "kernel": shape_label(info, True),
-            "hbm_gbs_algorithmic": algorithmic_bytes(info, 4096 * 4096, done, True, 1e-4, 10)
-                                   / (info["device_us"] * 1e-6) / 1e9,
-            "n_checks": info["n_checks"],
-        }
-    finally:
-        pk.pk_destroy(ctx)
+    res10 = {}
+    for name, flags in (("straddled", pk.PK_FLAG_ALTERNATE_DIRECTION),
+                        ("checks_end_passes",
+                         pk.PK_FLAG_ALTERNATE_DIRECTION | pk.PK_FLAG_CHECKS_END_PASSES)):
+        ctx = pk.pk_create(4096, 4096, w["u0"], w["f"], pk.pk_options_default(flags=flags))
+        try:
+            runs = []
+            for rep in range(4):  # the first is a warm-up; each run starts from the workload's field
+                pk.pk_set_field(ctx, w["u0"])
+                info = pk.pk_run_sweeps(ctx, 2000, 1e-4, 10)
+                if rep:
+                    runs.append(info)
+            info = min(runs, key=lambda r: r["device_us"])
+            done = info["sweeps_done"]
+            model = info
+            res10[name] = {
+                "us_per_sweep": info["device_us"] / max(1, done), "sweeps_done": done,
+                "res_ratio": info["res_last"] / info["res0"] if info["res0"] else None,
+                "kernel": shape_label(info, True), "passes": info["passes"],
+                "passes_model": sum(passes_of(model, 2000, 1e-4, 10,
+                                              done if done < 2000 else None)),
+                "hbm_gbs_algorithmic": algorithmic_bytes(model, 4096 * 4096, 2000, True, 1e-4, 10)
+                                       / (info["device_us"] * 1e-6) / 1e9,
+                "n_checks": info["n_checks"],
+            }
+        finally:
+            pk.pk_destroy(ctx)
+    out["poisson_4096_res10"] = res10
     return out
 
 
@@ -554,7 +587,8 @@ def main():
                       for _ in range(2)]
         assert host_in_t.is_pinned() and all(t.is_pinned() for t in host_out_t)
         host_in, host_out = host_in_t.numpy(), [t.numpy() for t in host_out_t]
-        pk.pk_run_batch(ctx, [host_in] * 2, host_out, sweeps, w["tol"], w["check_every"])
+        pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
+                        w["check_every"])
         dist_barrier(world)
         t0 = time.perf_counter()
         infos = pk.pk_run_batch(ctx, [host_in] * args.steps,

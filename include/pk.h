@@ -76,6 +76,10 @@ extern "C" {
 #define PK_FLAG_PROFILE_BARRIER 0x4u     /* record each CTA's total barrier wait (pk_barrier_wait_ns) */
 #define PK_FLAG_ONE_SWEEP_PER_PASS 0x8u  /* pk_run_sweeps: no temporal blocking; every pass advances
                                             one sweep (STREAM keeps stream_config's shape or 3) */
+#define PK_FLAG_CHECKS_END_PASSES 0x10u  /* pk_run_sweeps: a three-sweep pass stops at a residual
+                                            check instead of taking it in its stage 2 or 3 (the
+                                            same bits; passes of 3, 3, 3, 1 per check interval of
+                                            10 instead of 3 1/3) */
 
 /* ---- grid barrier constructions ([P2] "The barrier is a counter and a
  * generation") -------------------------------------------------------------- */
@@ -111,6 +115,14 @@ typedef struct {
                                 PK_FLAG_ONE_SWEEP_PER_PASS is set) */
     double device_us;     /* device time of the call: CUDA events on the context's
                              stream around its kernels (launch gaps included) */
+    int32_t passes;       /* passes over the field (each reads the current iterate once
+                             and, unless it only checks, writes the next once): the
+                             persistent DIRECT and STREAM kernels count theirs, the
+                             per-launch and graph paths count their sweep launches;
+                             0 where the kernels do not count them (LOCAL, red-black) */
+    int32_t straddle;     /* 1 when the run took the three-sweep kernel whose passes run past
+                             residual checks (a check inside a pass is taken in its stage 2
+                             or 3), else 0 */
 } pk_run_info;
 
 /* A mailbox task ([P1] "Base implementation": the host writes a task, the

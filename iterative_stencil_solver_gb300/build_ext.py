@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpk.so")
-SOURCES = ["pk_stream_d3.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
+SOURCES = ["pk_stream_d3.cu", "pk_stream_d3s.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
            "pk_host.cu", "pk_noalloc.cu", "pk_stream.cu"]
 HEADERS = ["pk_device.cuh", "pk_internal.h", "pk_sweep.cuh", "pk_stream.cuh"]
 

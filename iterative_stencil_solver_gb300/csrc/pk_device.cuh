@@ -431,75 +431,94 @@ __device__ __forceinline__ float4 quad_update2(const Quad &q) {
     return make_float4(u01.x, u01.y, u23.x, u23.y);
 }
 
-// Per-thread residual accumulator of the sweep kernels: the sum of r^2 as an
-// unevaluated pair of floats with a power-of-two exponent, sum = (hi + lo) *
-// 2^(2 * ex).  Each residual is scaled exactly by 2^-ex (held in `scale`) and
-// its square split exactly into p + e (p = fl(x*x), e = fma(x, x, -p)); p
-// joins hi through an error-free two-sum whose error, with e, goes to lo.
-// Over the few hundred cells a thread checks per pass the pair carries about
-// 44 significant bits, far inside the 1e-10 relative agreement the residual
-// is held to.  The exponent follows the largest residual seen: one whose
-// scaled value reaches 2^30 moves it up (the pair is scaled down exactly, or
-// to nothing where it is negligible next to the new term), so squares never
-// overflow; residuals far below the largest lose only bits that are far
-// below the sum.  A residual of +-inf (4C or t beyond the float range) turns
-// the pair into NaN (inf - inf in the two-sum), which is what a compensated
-// double sum of the same squares returns as well.  All of it is fp32 and
-// integer arithmetic: fp64 runs at a
-// small fraction of the fp32 rate on this GPU, and a double path for rare
-// values, even when no cell took it, kept the fp64 pipe busy on every
-// checked cell.
+// Per-thread residual accumulator of the sweep kernels: the sum of r^2 as two
+// unevaluated pairs of floats (two lanes: cells 0 and 2 of a quad go to one,
+// cells 1 and 3 to the other, so the two dependent chains run side by side)
+// with a power-of-two exponent shared by both, sum = (h0 + l0 + h1 + l1) *
+// 2^(2 * ex).  Each residual is scaled exactly by 2^-ex (held in `scale`)
+// and its square split exactly into p + e (p = fl(x*x), e = fma(x, x, -p));
+// p joins its lane's h through an error-free two-sum whose error, with e,
+// goes to l.  Over the few hundred cells a thread checks per pass each pair
+// carries about 44 significant bits, far inside the 1e-10 relative agreement
+// the residual is held to.  The exponent follows the largest residual seen:
+// a quad whose largest scaled residual reaches 2^30 moves it up (the pairs
+// are scaled down exactly, or to nothing where they are negligible next to
+// the new terms), so squares never overflow; residuals far below the largest
+// lose only bits that are far below the sum.  The test is made once per
+// quad, on the largest of its four residuals (which max|r| needs anyway).  A
+// residual of +-inf (4C or t beyond the float range) turns the pair into NaN
+// (inf - inf in the two-sum), which is what a compensated double sum of the
+// same squares returns as well.  All of it is fp32 and integer arithmetic:
+// fp64 runs at a small fraction of the fp32 rate on this GPU, and a double
+// path for rare values, even when no cell took it, kept the fp64 pipe busy on
+// every checked cell.  (Packed f32x2 forms of the same arithmetic, as
+// intrinsics or as PTX, pushed the three-sweep kernels' row windows onto a
+// stack frame.)
 struct ResFF {
-    float hi, lo;
-    float scale;  // 2^-ex
+    float h0, l0, h1, l1;  // the two lanes' pairs
+    float scale;           // 2^-ex
     int ex;
 };
 __device__ __forceinline__ ResFF resff_zero() {
     ResFF a;
-    a.hi = a.lo = 0.f;
+    a.h0 = a.l0 = a.h1 = a.l1 = 0.f;
     a.ex = -126;
     a.scale = 0x1p126f;
     return a;
 }
-__device__ __forceinline__ void resff_add(ResFF &a, float r) {
-    float x = __fmul_rn(r, a.scale);
-    if (fabsf(x) >= 0x1p30f) {
-        // r's binary exponent (r * 2^-ne in [0.5, 1)); subnormals count as
-        // -126, and exponents above 126 as 126 (so 2^-ne stays a normal float)
-        const int eb = (__float_as_int(r) >> 23) & 0xff;
-        const int ne = eb == 0 ? -126 : min(eb - 126, 126);
-        const int d = 2 * (ne - a.ex);  // > 0: the pair shrinks by 2^-d
-        const float f = d < 127 ? __int_as_float((127 - d) << 23) : 0.f;
-        a.hi = __fmul_rn(a.hi, f);
-        a.lo = __fmul_rn(a.lo, f);
-        a.ex = ne;
-        a.scale = __int_as_float((127 - ne) << 23);
-        x = __fmul_rn(r, a.scale);
-    }
+// Moves the exponent to that of m, a residual magnitude whose scaled value
+// reached 2^30: m * 2^-ne in [0.5, 1); subnormals count as -126, and
+// exponents above 126 as 126 (so 2^-ne stays a normal float).
+__device__ __forceinline__ void resff_rescale(ResFF &a, float m) {
+    const int eb = (__float_as_int(m) >> 23) & 0xff;
+    const int ne = eb == 0 ? -126 : min(eb - 126, 126);
+    const int d = 2 * (ne - a.ex);  // > 0: the pairs shrink by 2^-d
+    const float f = d < 127 ? __int_as_float((127 - d) << 23) : 0.f;
+    a.h0 = __fmul_rn(a.h0, f);
+    a.l0 = __fmul_rn(a.l0, f);
+    a.h1 = __fmul_rn(a.h1, f);
+    a.l1 = __fmul_rn(a.l1, f);
+    a.ex = ne;
+    a.scale = __int_as_float((127 - ne) << 23);
+}
+// The square of a scaled residual x into the pair (h, l).
+__device__ __forceinline__ void resff_add_lane(float &h, float &l, float x) {
     const float p = __fmul_rn(x, x);
     const float e = __fmaf_rn(x, x, -p);
-    const float s = __fadd_rn(a.hi, p);
-    const float bp = __fsub_rn(s, a.hi);
-    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bp)), __fsub_rn(p, bp));
-    a.hi = s;
-    a.lo = __fadd_rn(a.lo, __fadd_rn(err, e));
+    const float s = __fadd_rn(h, p);
+    const float bp = __fsub_rn(s, h);
+    const float err = __fadd_rn(__fsub_rn(h, __fsub_rn(s, bp)), __fsub_rn(p, bp));
+    h = s;
+    l = __fadd_rn(l, __fadd_rn(err, e));
 }
 __device__ __forceinline__ double resff_value(const ResFF &a) {
-    const double v = __dadd_rn((double)a.hi, (double)a.lo);
+    const double v = __dadd_rn(__dadd_rn((double)a.h0, (double)a.l0),
+                               __dadd_rn((double)a.h1, (double)a.l1));
     return ldexp(v, 2 * a.ex);
 }
+// The residuals r = fl32(t - 4C) of the first `valid` cells of a quad (the
+// others count as 0) into acc, and their largest magnitude into rmax.
 __device__ __forceinline__ void quad_residual(const Quad &q, float4 c, int valid, ResFF &acc,
                                               float &rmax) {
-    const float tv[4] = {q.t0, q.t1, q.t2, q.t3};
-    const float cv[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        if (k < valid) {
-            const float r = __fsub_rn(tv[k], __fmul_rn(4.0f, cv[k]));
-            resff_add(acc, r);
-            rmax = fmaxf(rmax, fabsf(r));
-        }
+    const float2 four = make_float2(4.0f, 4.0f);
+    const float2 c01 = __fmul2_rn(four, make_float2(c.x, c.y));  // exact
+    const float2 c23 = __fmul2_rn(four, make_float2(c.z, c.w));
+    const float2 r01 = __fadd2_rn(make_float2(q.t0, q.t1), make_float2(-c01.x, -c01.y));
+    const float2 r23 = __fadd2_rn(make_float2(q.t2, q.t3), make_float2(-c23.x, -c23.y));
+    float r0 = r01.x, r1 = r01.y, r2 = r23.x, r3 = r23.y;
+    if (valid < 4) {
+        if (valid < 1) r0 = 0.f;
+        if (valid < 2) r1 = 0.f;
+        if (valid < 3) r2 = 0.f;
+        r3 = 0.f;
     }
+    const float m = fmaxf(fmaxf(fabsf(r0), fabsf(r1)), fmaxf(fabsf(r2), fabsf(r3)));
+    rmax = fmaxf(rmax, m);
+    if (__fmul_rn(m, acc.scale) >= 0x1p30f) resff_rescale(acc, m);
+    resff_add_lane(acc.h0, acc.l0, __fmul_rn(r0, acc.scale));
+    resff_add_lane(acc.h1, acc.l1, __fmul_rn(r1, acc.scale));
+    resff_add_lane(acc.h0, acc.l0, __fmul_rn(r2, acc.scale));
+    resff_add_lane(acc.h1, acc.l1, __fmul_rn(r3, acc.scale));
 }
 
 // The same for one quad into a double (the small-grid kernels): the quad's

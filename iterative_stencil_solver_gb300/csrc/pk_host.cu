@@ -83,6 +83,8 @@ struct pk_ctx {
     int grid = 1;        // persistent sweep grid
     int stream_cfg2 = -1;  // multi-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
+    int grid_straddle = 0; // grid of the three-sweep kernel whose passes straddle
+                           // residual checks (0 = the multi-sweep shape has none)
     int local_depth = 1;   // LOCAL: sweeps per neighbour exchange the plan allows
     int local_threads = kDirectThreads;  // LOCAL: threads per CTA
     int launch_grid = 1;   // per-launch and graph paths: CTAs of their kernels
@@ -403,6 +405,35 @@ int plan(pk_ctx *ctx) {
             if (ctx->opt.grid_override > 0) ctx->grid2 = ctx->opt.grid_override;
         }
     }
+    // Runs with residual checks take the kernel of the same three-sweep
+    // shape whose passes straddle the checks; its occupancy is its own.
+    ctx->grid_straddle = 0;
+    {
+        const int shape_p = ctx->stream_cfg2 >= 0 ? ctx->stream_cfg2
+                            : v == kVariantStream ? ctx->stream_cfg : -1;
+        // A straddling kernel that compiled with a stack frame (local
+        // memory: its row windows left the registers) would run slower than
+        // passes that stop at the checks, so it is not used.
+        bool in_registers = false;
+        if (shape_p >= 0 && stream_depth(shape_p) == 3 && stream_config_ok(shape_p, ctx->poisson)) {
+            cudaFuncAttributes fa;
+            PK_TRY(ctx, cudaFuncGetAttributes(&fa, kernel_persistent(kVariantStream, ctx->poisson, shape_p, true)));
+            in_registers = fa.localSizeBytes == 0;
+        }
+        if (in_registers) {
+            int per_s = 0;
+            const int cap_s = coop_capacity(ctx, kernel_persistent(kVariantStream, ctx->poisson, shape_p, true),
+                                            block_threads(kVariantStream, shape_p),
+                                            dyn_smem(kVariantStream, ctx->poisson, shape_p), &per_s);
+            if (cap_s < 0) return PK_ECUDA;
+            if (cap_s > 0) {
+                long long need_s = stream_rows(ctx, shape_p);
+                if (need_s < 1) need_s = 1;
+                ctx->grid_straddle = (int)(need_s < cap_s ? need_s : cap_s);
+                if (ctx->opt.grid_override > 0) ctx->grid_straddle = ctx->opt.grid_override;
+            }
+        }
+    }
     int cap;
     if (v == kVariantLocal) {
         cap = lcap;
@@ -460,6 +491,7 @@ int plan(pk_ctx *ctx) {
     }
     int want = ctx->grid > cap ? ctx->grid : cap;
     if (ctx->grid2 > want) want = ctx->grid2;
+    if (ctx->grid_straddle > want) want = ctx->grid_straddle;
     if (ctx->launch_grid > want) want = ctx->launch_grid;
     return ensure_partials(ctx, want);
 }
@@ -611,8 +643,10 @@ double elapsed_us(pk_ctx *ctx) {
 
 void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
                float rmax, int n_checks, int status, int grid, int variant = 0, int shape = -2,
-               int depth = 1) {
+               int depth = 1, int passes = 0, bool straddle = false) {
     if (!info) return;
+    info->passes = passes;
+    info->straddle = straddle ? 1 : 0;
     info->sweeps_done = sweeps;
     info->res0 = res0;
     info->res_last = res_last;
@@ -652,9 +686,10 @@ int task_finish(pk_ctx *ctx) {
 
 // The persistent kernel a run of n sweeps takes.  Several sweeps per pass
 // pay off whenever a run has two or more: the kernels shorten a pass where
-// the end or a residual check would fall inside it.
-void choose_persistent(const pk_ctx *ctx, int64_t n, int *kernel_out, int *shape_out,
-                       int *grid_out, int *depth_out) {
+// the end would fall inside it, and a three-sweep pass runs past a residual
+// check (straddle) where a pass of fewer sweeps stops at it.
+void choose_persistent(const pk_ctx *ctx, int64_t n, float tol, int check_every, int *kernel_out,
+                       int *shape_out, int *grid_out, int *depth_out, bool *straddle_out) {
     const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
     int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
     if (ctx->stream_cfg2 >= 0 && multi_ok) {
@@ -670,10 +705,14 @@ void choose_persistent(const pk_ctx *ctx, int64_t n, int *kernel_out, int *shape
         shape = ctx->local_depth;
         depth = ctx->local_depth;
     }
+    const bool straddle = kernel == kVariantStream && depth == 3 && tol > 0.f && check_every > 0 &&
+                          ctx->grid_straddle > 0 && !(ctx->opt.flags & PK_FLAG_CHECKS_END_PASSES);
+    if (straddle) grid = ctx->grid_straddle;
     *kernel_out = kernel;
     *shape_out = shape;
     *grid_out = grid;
     *depth_out = depth;
+    *straddle_out = straddle;
 }
 
 }  // namespace
@@ -817,9 +856,10 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
         PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0, local_halo_bytes(ctx), ctx->stream));
     int kernel, shape, grid, depth;
-    choose_persistent(ctx, n, &kernel, &shape, &grid, &depth);
+    bool straddle;
+    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle);
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
-    cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream);
+    cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream, straddle);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaMemcpyAsync(ctx->h_info, p.info, sizeof(DeviceInfo), cudaMemcpyDeviceToHost,
@@ -839,7 +879,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     ctx->cur = ctx->h_info->cur;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
               ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid,
-              kernel == kVariantStream ? kernel : 0, shape, depth);
+              kernel == kVariantStream ? kernel : 0, shape, depth, ctx->h_info->passes, straddle);
     return PK_OK;
 }
 
@@ -898,7 +938,8 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
     int rc = ensure_batch(ctx);
     if (rc != PK_OK) return rc;
     int kernel, shape, grid, depth;
-    choose_persistent(ctx, n, &kernel, &shape, &grid, &depth);
+    bool straddle;
+    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle);
     const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
     const size_t dpitch = sizeof(float) * (size_t)ctx->pitch;
     const size_t rows = (size_t)(ctx->ny + 2);
@@ -943,7 +984,7 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
         p.profile = 0;
         run_ids[q] = p.run_id;
         if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t0[q], sc);
-        if (e == cudaSuccess) e = launch_persistent(kernel, ctx->poisson, shape, grid, p, sc);
+        if (e == cudaSuccess) e = launch_persistent(kernel, ctx->poisson, shape, grid, p, sc, straddle);
         if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t1[q], sc);
         if (e == cudaSuccess) e = launch_publish_record(p.info, dbar, &ctx->d_rec[q], sc);
         if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_rec[q], sc);
@@ -1001,6 +1042,8 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
                           : kernel == kVariantLocalD ? (int)kVariantLocal : kernel;
             inf.stream_config = kernel == kVariantStream ? shape : -1;
             inf.sweeps_per_pass = depth;
+            inf.passes = d.passes;
+            inf.straddle = straddle ? 1 : 0;
             float ms = 0.f;
             inf.device_us = cudaEventElapsedTime(&ms, ctx->ev_t0[q], ctx->ev_t1[q]) == cudaSuccess
                                 ? (double)ms * 1000.0 : -1.0;
@@ -1051,6 +1094,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
     double res0 = 0.0, res_last = 0.0;
     float rmax_last = 0.f;
     int n_checks = 0;
+    int passes = 0;
     int cur = ctx->cur;
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     for (;;) {
@@ -1063,6 +1107,7 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
         p.pass_k = k;
         cudaError_t e = launch_once(launch_variant(ctx), ctx->poisson, ctx->stream_cfg, grid, p, ctx->stream);
         if (e != cudaSuccess) return cuda_fail(ctx, e, "sweep launch");
+        ++passes;
         if (check) {
             e = launch_finalize(launch_variant(ctx), ctx->stream_cfg, grid, p, &ctx->scratch->res, ctx->stream);
             if (e != cudaSuccess) return cuda_fail(ctx, e, "residual launch");
@@ -1085,7 +1130,8 @@ int pk_run_sweeps_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     ctx->cur = cur;
-    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, grid, launch_variant(ctx));
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, grid, launch_variant(ctx),
+              -2, 1, passes);
     return PK_OK;
 }
 
@@ -1217,7 +1263,11 @@ int pk_run_sweeps_graph(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_r
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     ctx->cur = cur;
-    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->launch_grid, launch_variant(ctx));
+    // one sweep launch per sweep done, plus the launch of the check the run
+    // ended on (its sweep, or the residual-only launch at k == n)
+    const int passes = (int)k + ((checks && k % check_every == 0) ? 1 : 0);
+    fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->launch_grid, launch_variant(ctx),
+              -2, 1, passes);
     return PK_OK;
 }
 

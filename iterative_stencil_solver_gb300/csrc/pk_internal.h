@@ -22,6 +22,7 @@ struct DeviceInfo {
     long long task_sweeps;  // task kernel: sweeps run
     int barriers;  // grid barriers completed (CTA 0)
     unsigned bar_count_end;  // kBarrierCounter: count word after the last barrier
+    int passes;    // passes over the field (a pass advances one or more sweeps)
 };
 
 // Residual result of the per-launch reduction kernel.
@@ -219,7 +220,9 @@ cudaError_t prepare_kernels();
 // pointers: the STREAM kernels (pk_stream.cu; persistent or per-launch form
 // of shape cfg) and the LOCAL kernels (pk_local.cu; depth 2..kLocalMaxDepth
 // for local_d_kernel).
-const void *stream_kernel(bool poisson, int cfg, bool persistent);
+// straddle: the persistent three-sweep kernel whose passes run past residual
+// checks (shapes of depth 3 only; nullptr otherwise).
+const void *stream_kernel(bool poisson, int cfg, bool persistent, bool straddle = false);
 const void *local_kernel(bool poisson);
 const void *local_d_kernel(bool poisson, int depth);
 const void *local_rb_kernel(bool poisson);
@@ -228,7 +231,7 @@ extern size_t g_local_smem_max;   // LOCAL: opt-in shared memory per CTA
 
 // Kernel function pointers, for occupancy queries.  cfg selects the STREAM
 // configuration (ignored for DIRECT).
-const void *kernel_persistent(int variant, bool poisson, int cfg);
+const void *kernel_persistent(int variant, bool poisson, int cfg, bool straddle = false);
 const void *kernel_once(int variant, bool poisson, int cfg);
 const void *kernel_task(bool poisson);
 const void *kernel_barrier_only(int kind);
@@ -239,7 +242,7 @@ int block_threads(int variant, int cfg = 3);
 size_t dyn_smem(int variant, bool poisson, int cfg);
 
 cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
-                              cudaStream_t s);
+                              cudaStream_t s, bool straddle = false);
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
                         cudaStream_t s);
 // Reduces the partials of a per-launch check pass with the thread count of
@@ -270,6 +273,7 @@ struct RunRecord {
     unsigned bar_count_end;
     int error;
     unsigned site, bad_cta;
+    int passes;
 };
 cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
                                   cudaStream_t s);

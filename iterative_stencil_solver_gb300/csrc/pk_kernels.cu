@@ -87,9 +87,9 @@ template <bool POISSON>
 __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParams p) {
     const unsigned first = blockIdx.x * blockDim.x + threadIdx.x;
     const unsigned stride = gridDim.x * blockDim.x;
-    persistent_loop<1>(p, [&](const float *src, float *dst, bool check, bool store, int,
+    persistent_loop<1>(p, [&](const float *src, float *dst, int cs, bool store, int,
                               long long, double &s2, float &rmax) {
-        pass_direct_any<POISSON>(p, src, dst, check, store, first, stride, s2, rmax);
+        pass_direct_any<POISSON>(p, src, dst, cs != 0, store, first, stride, s2, rmax);
     });
 }
 
@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_rb(SweepParams p)
         d->cur = p.cur;
         d->task_sweeps = 0;
         d->barriers = ctl.index;
+        d->passes = 0;  // not counted by this kernel
         d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;
@@ -488,6 +489,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
         d->sweeps_done = 0;
         d->cur = cur;
         d->task_sweeps = sweeps;
+        d->passes = 0;
         d->n_checks = 0;
         __threadfence();
         d->run_id = p.run_id;
@@ -675,18 +677,18 @@ cudaError_t prepare_kernels() {
         for (int c = 0; c < kNumStreamConfigs; ++c) {
             const size_t bytes = stream_smem_bytes(c, poisson != 0);
             bool fits = true;
-            for (int persistent = 0; persistent < 2; ++persistent) {
-                const void *fn = poisson ? stream_kernel(true, c, persistent != 0)
-                                         : stream_kernel(false, c, persistent != 0);
+            for (int form = 0; form < 3; ++form) {  // per-launch, persistent, straddling
+                const void *fn = stream_kernel(poisson != 0, c, form != 0, form == 2);
+                if (!fn) continue;
                 int lim = 0;
                 if ((e = dyn_limit(fn, &lim)) != cudaSuccess) return e;
                 if (bytes > (size_t)lim) fits = false;
             }
             ok[poisson][c] = fits;
             if (!fits) continue;
-            for (int persistent = 0; persistent < 2; ++persistent) {
-                const void *fn = poisson ? stream_kernel(true, c, persistent != 0)
-                                         : stream_kernel(false, c, persistent != 0);
+            for (int form = 0; form < 3; ++form) {
+                const void *fn = stream_kernel(poisson != 0, c, form != 0, form == 2);
+                if (!fn) continue;
                 e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)bytes);
                 if (e != cudaSuccess) return e;
@@ -705,12 +707,12 @@ bool stream_config_ok(int cfg, bool poisson) {
     return cfg >= 0 && cfg < kNumStreamConfigs && g_cfg_ok[poisson ? 1 : 0][cfg];
 }
 
-const void *kernel_persistent(int variant, bool poisson, int cfg) {
+const void *kernel_persistent(int variant, bool poisson, int cfg, bool straddle) {
     if (variant == kVariantLocalD)
         return local_d_kernel(poisson, cfg);
     if (variant == kVariantLocal)
         return local_kernel(poisson);
-    if (variant == kVariantStream) return stream_kernel(poisson, cfg, true);
+    if (variant == kVariantStream) return stream_kernel(poisson, cfg, true, straddle);
     return poisson ? (const void *)k_persistent_direct<true> : (const void *)k_persistent_direct<false>;
 }
 
@@ -738,7 +740,7 @@ size_t dyn_smem(int variant, bool poisson, int cfg) {
 }
 
 cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool straddle) {
     SweepParams arg = p;
     void *args[] = {&arg};
     const int threads = (variant == kVariantLocal || variant == kVariantLocalD) && p.local_threads > 0
@@ -747,8 +749,9 @@ cudaError_t launch_persistent(int variant, bool poisson, int cfg, int grid, cons
     const size_t smem = variant == kVariantLocal    ? local_smem_bytes(p.nx, p.local_rows, poisson)
                         : variant == kVariantLocalD ? local_d_smem_bytes(p.nx, p.local_rows, poisson, cfg)
                                                     : dyn_smem(variant, poisson, cfg);
-    return cudaLaunchCooperativeKernel(kernel_persistent(variant, poisson, cfg), dim3(grid),
-                                       dim3(threads), args, smem, s);
+    const void *fn = kernel_persistent(variant, poisson, cfg, straddle);
+    if (!fn) return cudaErrorInvalidValue;
+    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(threads), args, smem, s);
 }
 
 cudaError_t launch_once(int variant, bool poisson, int cfg, int grid, const SweepParams &p,
@@ -833,6 +836,7 @@ __global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar
         out->cur = vi->cur;
         out->run_id = vi->run_id;
         out->bar_count_end = vi->bar_count_end;
+        out->passes = vi->passes;
         volatile const BarrierState *vb = bar;
         out->error = (int)vb->error.v;
         out->site = vb->site.v;

@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local(SweepPara
         d->cur = p.cur ^ (int)(k & 1);
         d->task_sweeps = 0;
         d->barriers = ctl.index;
+        d->passes = 0;  // not counted by this kernel
         d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;
@@ -495,6 +496,7 @@ __global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local_d(SweepPa
         d->cur = p.cur ^ (int)(k & 1);
         d->task_sweeps = 0;
         d->barriers = ctl.index;
+        d->passes = 0;  // not counted by this kernel
         d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;
@@ -634,6 +636,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local_rb(SweepPar
         d->cur = p.cur;
         d->task_sweeps = 0;
         d->barriers = ctl.index;
+        d->passes = 0;  // not counted by this kernel
         d->bar_count_end = p.bar_base + (unsigned)ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;

@@ -130,8 +130,17 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     }
     if (variant == kVariantDirect && (long long)ny * ((nx + 3) / 4) >= (1LL << 31))
         return fail(PK_EINVAL, "pk_run_sweeps_noalloc: grid too large");
+    // runs with checks on a three-sweep shape take the kernel whose passes
+    // straddle the checks, as pk_run_sweeps does
+    bool straddle = variant == kVariantStream && depth == 3 && tol > 0.f && check_every > 0;
+    if (straddle) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kernel_persistent(variant, poisson, cfg, true));
+        if (e != cudaSuccess) return fail(PK_ECUDA, "cudaFuncGetAttributes", e);
+        straddle = fa.localSizeBytes == 0;  // as pk_create's plan decides
+    }
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_persistent(variant, poisson, cfg),
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_persistent(variant, poisson, cfg, straddle),
                                                       block_threads(variant, cfg),
                                                       dyn_smem(variant, poisson, cfg));
     if (e != cudaSuccess) return fail(PK_ECUDA, "occupancy query", e);
@@ -177,7 +186,7 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     p.run_id = 1;
     p.barrier_kind = (int)kBarrierCounter;
     p.bar_base = 0;
-    e = launch_persistent(variant, poisson, cfg, (int)grid, p, s);
+    e = launch_persistent(variant, poisson, cfg, (int)grid, p, s, straddle);
     if (e != cudaSuccess) return fail(PK_ECUDA, "cudaLaunchCooperativeKernel(persistent sweep)", e);
     DeviceInfo hi;
     BarrierState hb;
@@ -200,6 +209,8 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
         info->stream_config = variant == kVariantStream ? cfg : -1;
         info->sweeps_per_pass = depth;
         info->device_us = 0.0;
+        info->passes = hi.passes;
+        info->straddle = straddle ? 1 : 0;
     }
     return PK_OK;
 }

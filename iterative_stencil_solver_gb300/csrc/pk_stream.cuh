@@ -484,6 +484,7 @@ struct Seg3 {
     float *drow;          // stage-3 output, this thread's first quad, for the next step
     long long dstep;      // dir * pitch
     int dir, cols, nin, nx, ny;
+    int cs;               // CHK = -1: the stage that reduces a residual, chosen at run time
     // Edge warp, per lane: the cells beyond its edge are ring or pad columns
     // (the first or last strip); the U_{k+1} cell two columns out is a ring
     // column (that, or the next strip is the last one and one column wide);
@@ -527,8 +528,12 @@ __device__ __forceinline__ void rotate3v(T &a, T &b, T &x) {
 // 2's row on return.  STEADY: 6 <= idx <= nin-3, where all stages run, the
 // stage-1 row lies in the band and no ring row is involved.  FULL: the strip
 // is TW columns wide.  QJ: the step's shared row (idx mod 3) when the caller
-// knows it at compile time, else -1 (c.qj).
-template <class C, bool POISSON, bool CHECK, bool STEADY, bool FULL, int QJ>
+// knows it at compile time, else -1 (c.qj).  CHK: the stage that reduces
+// the residual of the row it reads (0 = none; 1: U_k, 2: U_{k+1}, 3: U_{k+2}),
+// over the rows of the band only; -1: the stage is c.cs, chosen at run time
+// (one copy of the step serves every stage, which keeps a kernel that needs
+// all of them small enough for its row windows to stay in registers).
+template <class C, bool POISSON, int CHK, bool STEADY, bool FULL, int QJ>
 __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c, StreamState &st,
                                           int idx, int r, float4 (&KA)[C::kQPT],
                                           float4 (&KB)[C::kQPT], float4 (&KX)[C::kQPT],
@@ -557,6 +562,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
     const unsigned p2w = p1w + 3u * RW, p2r = p1r + 3u * RW;
     const int r1 = r - c.dir, r2 = r - 2 * c.dir;
     const bool act1 = STEADY || idx >= 2, act2 = STEADY || idx >= 4, act3 = STEADY || idx >= 6;
+    const int chk = CHK >= 0 ? CHK : c.cs;
     const bool ring1 = !STEADY && (r1 < 1 || r1 > c.ny);
     const bool ring2 = !STEADY && (r2 < 1 || r2 > c.ny);
     // The cells beyond each strip edge: U_{k+1} at row r1, one and two
@@ -606,7 +612,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             const float4 g = POISSON ? lds4_at(sb + GO + o) : z4;
             const Quad q1 = quad_t2<POISSON>(lds_at(sb + o - 4u), KB[k], lds_at(sb + o + 16u), KA[k],
                                              KX[k], g);
-            if (CHECK && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
+            if (chk == 1 && in_band) quad_residual(q1, KB[k], FULL ? 4 : c.valid[k], s2, rmax);
             float4 u1 = quad_update2(q1);
             if (ring1)
                 u1 = KB[k];
@@ -625,6 +631,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
     if (act2) {
         // Stage 2: U_{k+2} on row r2 (centre PB); west/east from the shared
         // U_{k+1} row written one step ago.
+        const bool in_band2 = STEADY || (idx >= 5 && idx <= c.nin - 2);
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
             const unsigned o = k * KO;
@@ -632,6 +639,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             if (POISSON) g2[k] = lds4_at(sa + GO + o);
             const Quad q2 = quad_t2<POISSON>(lds_at(p1r + ho), PB[k], lds_at(p1r + ho + NHB + 4u), PA[k],
                                              PY[k], g2[k]);
+            if (chk == 2 && in_band2) quad_residual(q2, PB[k], FULL ? 4 : c.valid[k], s2, rmax);
             float4 u2 = quad_update2(q2);
             if (ring2)
                 u2 = PB[k];
@@ -652,6 +660,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
             const unsigned ho = 4u * k * C::kCons;
             const Quad q3 = quad_t2<POISSON>(lds_at(p2r + ho), RB[k], lds_at(p2r + ho + NHB + 4u), RA[k],
                                              RY[k], G3[k]);
+            if (chk == 3) quad_residual(q3, RB[k], FULL ? 4 : c.valid[k], s2, rmax);
             u3[k] = quad_update2(q3);
         }
     }
@@ -686,7 +695,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
     c.ph ^= wrap ? 1u : 0u;
 }
 
-template <class C, bool POISSON, bool CHECK, bool FULL>
+template <class C, bool POISSON, int CHK, bool FULL>
 __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> &c, StreamState &st,
                                             int &idx, int &r, int steady, float4 (&ka)[C::kQPT],
                                             float4 (&kb)[C::kQPT], float4 (&kx)[C::kQPT],
@@ -700,19 +709,19 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
     // The steady rows start at idx 6, so the unrolled steps' shared rows
     // are 0, 1 and 2.
     for (; steady >= 3; steady -= 3) {
-        seg3_step<C, POISSON, CHECK, true, FULL, 0>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
+        seg3_step<C, POISSON, CHK, true, FULL, 0>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
                                                     ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL, 1>(p, c, st, idx + 1, r + dir, kb, kx, ka, pb, py,
+        seg3_step<C, POISSON, CHK, true, FULL, 1>(p, c, st, idx + 1, r + dir, kb, kx, ka, pb, py,
                                                     pa, rb, ry, ra, sb, sx, sa, fb, fx, fa, g3, s2,
                                                     rmax);
-        seg3_step<C, POISSON, CHECK, true, FULL, 2>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, py,
+        seg3_step<C, POISSON, CHK, true, FULL, 2>(p, c, st, idx + 2, r + 2 * dir, kx, ka, kb, py,
                                                     pa, pb, ry, ra, rb, sx, sa, sb, fx, fa, fb, g3,
                                                     s2, rmax);
         idx += 3;
         r += 3 * dir;
     }
     for (; steady > 0; --steady, ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, true, FULL, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
+        seg3_step<C, POISSON, CHK, true, FULL, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra, rb,
                                                      ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
@@ -723,11 +732,11 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
     }
 }
 
-template <class C, bool POISSON, bool CHECK>
+template <class C, bool POISSON, int CHK>
 __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *dst, int ja, int jb,
                                                  int dir, int cols, long long col0,
                                                  StreamState &st, float *qbuf, double &s2_out,
-                                                 float &rmax) {
+                                                 float &rmax, int cs) {
     // The residual of this segment's cells, added to s2_out at the end.
     ResFF s2 = resff_zero();
     constexpr int Q = C::kQPT;
@@ -755,6 +764,7 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     c.slot_last = c.slot_first + 4u * C::SLOT * M;
     c.full0 = smem_u32(st.full);
     c.qj = 0;
+    c.cs = cs;
     c.dir = dir;
     c.cols = cols;
     c.nin = (dir > 0 ? jb - ja : ja - jb) + 7;
@@ -790,8 +800,8 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     int r = ja - 3 * dir;
     // Prologue: the first six input rows (stages start at idx 2, 4 and 6).
     for (; idx < 6; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
-                                                       rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
+        seg3_step<C, POISSON, CHK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
+                                                     rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
         rotate3(ra, rb, ry);
@@ -808,15 +818,15 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     // registers (they went to the stack, 1.45x slower), so there the ragged
     // rows run through the rolled generic step below.
     if (cols == C::TW)
-        seg3_steady<C, POISSON, CHECK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
-                                             ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
+        seg3_steady<C, POISSON, CHK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
+                                           ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
     else if constexpr (!POISSON)
-        seg3_steady<C, POISSON, CHECK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
+        seg3_steady<C, POISSON, CHK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
                                               rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
     // The last input rows: stages 1 and 2 reach beyond the band (maybe the ring).
     for (; idx < c.nin; ++idx, r += dir) {
-        seg3_step<C, POISSON, CHECK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
-                                                       rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
+        seg3_step<C, POISSON, CHK, false, false, -1>(p, c, st, idx, r, ka, kb, kx, pa, pb, py, ra,
+                                                     rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
         rotate3(ka, kb, kx);
         rotate3(pa, pb, py);
         rotate3(ra, rb, ry);
@@ -831,12 +841,15 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
         mbar_arrive_at(fb + 8u * C::kStages);
     }
     st.L = L0 + (unsigned)c.nin;
-    if (CHECK) s2_out = __dadd_rn(s2_out, resff_value(s2));
+    if (CHK != 0) s2_out = __dadd_rn(s2_out, resff_value(s2));
 }
 
-template <class C, bool POISSON, bool CHECK, bool STORE, int D>
+// CHK: the stage that reduces a residual (0 = none; for D = 3 also 2 and 3,
+// or -1: the stage is cs, chosen at run time).
+template <class C, bool POISSON, int CHK, bool STORE, int D>
 __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
-                                            int dir, StreamState &st, double &s2, float &rmax) {
+                                            int dir, StreamState &st, double &s2, float &rmax,
+                                            int cs = 0) {
     const int nx = p.nx, ny = p.ny;
     const int strips = (nx + C::TW - 1) / C::TW;
     const long long R = (long long)strips * ny;
@@ -862,14 +875,14 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
         if (producer_warp) {
             produce_segment<C, POISSON, D>(p, src, jr, jb, dir, cols, col0, st);
         } else if (D == 3) {
-            consume_segment3<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st,
-                                                st.slots + C::kStages * C::SLOT, s2, rmax);
+            consume_segment3<C, POISSON, CHK>(p, dst, jr, jb, dir, cols, col0, st,
+                                              st.slots + C::kStages * C::SLOT, s2, rmax, cs);
         } else if (D == 2) {
-            consume_segment2<C, POISSON, CHECK>(p, dst, jr, jb, dir, cols, col0, st,
-                                                st.slots + C::kStages * C::SLOT, s2, rmax);
+            consume_segment2<C, POISSON, CHK == 1>(p, dst, jr, jb, dir, cols, col0, st,
+                                                   st.slots + C::kStages * C::SLOT, s2, rmax);
         } else {
-            consume_segment<C, POISSON, CHECK, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
-                                                      rmax);
+            consume_segment<C, POISSON, CHK == 1, STORE>(p, dst, jr, jb, dir, cols, col0, st, s2,
+                                                         rmax);
         }
         pos += dir > 0 ? len : -len;
         remaining -= len;
@@ -879,47 +892,64 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
     __syncwarp();
 }
 
-template <class C, bool POISSON>
+// cs: the stage that reduces a residual (0 = none).  Stages 2 and 3 come only
+// from a straddling loop, in full three-sweep passes, so only STRADDLE
+// kernels compile them, as one copy of the three-sweep step with the stage
+// chosen at run time (the passes without a check keep their own copy).  A
+// third copy (stage 1 on its own, or each stage on its own) pushed the
+// kernel past what the compiler keeps in registers: its row windows went to
+// a 248-byte stack frame.
+template <class C, bool POISSON, bool STRADDLE>
 __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
-                                                int dir, bool check, bool store, int dp,
+                                                int dir, int cs, bool store, int dp,
                                                 StreamState &st, double &s2, float &rmax) {
     // Only the depths this shape can take are compiled in.
     if constexpr (C::kDepth >= 3) {
         if (dp == 3) {
-            if (check)
-                pass_stream<C, POISSON, true, true, 3>(p, src, dst, dir, st, s2, rmax);
+            if constexpr (STRADDLE) {
+                if (cs)
+                    pass_stream<C, POISSON, -1, true, 3>(p, src, dst, dir, st, s2, rmax, cs);
+                else
+                    pass_stream<C, POISSON, 0, true, 3>(p, src, dst, dir, st, s2, rmax);
+                return;
+            }
+            if (cs)
+                pass_stream<C, POISSON, 1, true, 3>(p, src, dst, dir, st, s2, rmax);
             else
-                pass_stream<C, POISSON, false, true, 3>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 0, true, 3>(p, src, dst, dir, st, s2, rmax);
             return;
         }
     }
     if constexpr (C::kDepth >= 2) {
         if (dp == 2) {
-            if (check)
-                pass_stream<C, POISSON, true, true, 2>(p, src, dst, dir, st, s2, rmax);
+            if (cs)
+                pass_stream<C, POISSON, 1, true, 2>(p, src, dst, dir, st, s2, rmax);
             else
-                pass_stream<C, POISSON, false, true, 2>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 0, true, 2>(p, src, dst, dir, st, s2, rmax);
             return;
         }
     }
-    if (check) {
+    if (cs) {
         if (store)
-            pass_stream<C, POISSON, true, true, 1>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, 1, true, 1>(p, src, dst, dir, st, s2, rmax);
         else
-            pass_stream<C, POISSON, true, false, 1>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, 1, false, 1>(p, src, dst, dir, st, s2, rmax);
     } else if (store) {
-        pass_stream<C, POISSON, false, true, 1>(p, src, dst, dir, st, s2, rmax);
+        pass_stream<C, POISSON, 0, true, 1>(p, src, dst, dir, st, s2, rmax);
     }
 }
 
 // ===========================================================================
-// The persistent and per-launch STREAM kernels.
-template <class C, bool POISSON>
+// The persistent and per-launch STREAM kernels.  STRADDLE: the persistent
+// loop lets three-sweep passes run past residual checks (a separate
+// instantiation, taken for runs with checks, so that the kernel of runs
+// without them keeps its register budget).
+template <class C, bool POISSON, bool STRADDLE>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
     StreamState st = stream_setup<C>(smem);
-    persistent_loop<C::kDepth>(p, [&](const float *src, float *dst, bool check, bool store,
-                                      int dp, long long k, double &s2, float &rmax) {
+    persistent_loop<C::kDepth, STRADDLE>(p, [&](const float *src, float *dst, int cs, bool store,
+                                                int dp, long long k, double &s2, float &rmax) {
         const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
         // After the barrier: this producer's TMA reads must see the
         // generic-proxy stores the whole grid made in the previous sweep.
@@ -929,7 +959,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
             fence_acq_rel_gpu();
             fence_proxy_async_global();
         }
-        pass_stream_any<C, POISSON>(p, src, dst, dir, check, store, dp, st, s2, rmax);
+        pass_stream_any<C, POISSON, STRADDLE>(p, src, dst, dir, cs, store, dp, st, s2, rmax);
     });
 }
 
@@ -940,8 +970,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_once_stream(Swee
     double s2 = 0.0;
     float rmax = 0.f;
     const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;
-    pass_stream_any<C, POISSON>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0,
-                                p.pass_store != 0, 1, st, s2, rmax);
+    pass_stream_any<C, POISSON, false>(p, p.u[p.cur], p.u[p.cur ^ 1], dir, p.pass_check != 0 ? 1 : 0,
+                                       p.pass_store != 0, 1, st, s2, rmax);
     if (p.pass_check) write_partial(p, s2, rmax);
 }
 
@@ -949,9 +979,9 @@ template <int CFG, bool POISSON>
 using CfgOf = SCfg<kStreamConfigs[CFG].qpt, kStreamConfigs[CFG].stages, kStreamConfigs[CFG].depth,
                    kStreamConfigs[CFG].min_ctas, kStreamConfigs[CFG].consumers, POISSON>;
 
-template <int CFG, bool POISSON>
+template <int CFG, bool POISSON, bool STRADDLE>
 const void *persistent_stream_fn() {
-    return (const void *)k_persistent_stream<CfgOf<CFG, POISSON>, POISSON>;
+    return (const void *)k_persistent_stream<CfgOf<CFG, POISSON>, POISSON, STRADDLE>;
 }
 template <int CFG, bool POISSON>
 const void *once_stream_fn() {
@@ -961,8 +991,15 @@ const void *once_stream_fn() {
 // The persistent or per-launch kernel of shape CFG.
 template <int CFG>
 const void *stream_kernel_of(bool poisson, bool persistent) {
-    if (poisson) return persistent ? persistent_stream_fn<CFG, true>() : once_stream_fn<CFG, true>();
-    return persistent ? persistent_stream_fn<CFG, false>() : once_stream_fn<CFG, false>();
+    if (poisson)
+        return persistent ? persistent_stream_fn<CFG, true, false>() : once_stream_fn<CFG, true>();
+    return persistent ? persistent_stream_fn<CFG, false, false>() : once_stream_fn<CFG, false>();
+}
+
+// The persistent kernel of shape CFG whose passes straddle residual checks.
+template <int CFG>
+const void *straddle_stream_kernel_of(bool poisson) {
+    return poisson ? persistent_stream_fn<CFG, true, true>() : persistent_stream_fn<CFG, false, true>();
 }
 
 }  // namespace

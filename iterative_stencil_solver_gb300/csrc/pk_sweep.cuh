@@ -41,7 +41,21 @@ __device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
 
 // MAXD > 1: a pass may advance up to MAXD sweeps at once (temporal
 // blocking), as many as are due before the end or the next residual check.
-template <int MAXD, class PassFn>
+// The pass is called as pass(src, dst, cs, store, dp, k, s2, rmax): it
+// advances dp sweeps from U_k (src) into dst, and when cs > 0 its stage cs
+// also reduces the residual of the iterate it reads, U_{k+cs-1}.
+//
+// STRADDLE: a pass may run past a check ("What the barrier buys" wants the
+// check inside the kernel; nothing asks for a pass boundary there).  When
+// the next check c lies inside a full pass of MAXD sweeps (k < c < k+MAXD,
+// with no second check inside it), stage c-k+1 reduces the residual of U_c
+// and the pass runs on to U_{k+MAXD}.  If that check ends the run, U_c is
+// not in memory, but U_k still is (a pass only writes dst): the CTAs then
+// sweep c-k times from U_k into dst, the same sweeps with the same bits,
+// and stop there.  Without STRADDLE a pass always ends at the check, so a
+// check every 10 sweeps costs four passes of 3, 3, 3 and 1 sweeps instead
+// of three and a third.
+template <int MAXD, bool STRADDLE = false, class PassFn>
 __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
     // Loop state that only thread 0 uses (the barrier's bookkeeping) or that
     // changes only on check sweeps (the residual history) lives in shared
@@ -60,25 +74,48 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     int cur = p.cur;
     long long k = 0;
     int n_checks = 0;
+    // A straddled check that ends the run: the loop goes round once more to
+    // sweep from U_k to U_{k_exit} (the pass function keeps one call site, so
+    // the compiler inlines it and the row windows stay in registers).
+    bool redo = false;
+    long long k_exit = 0;
     for (;;) {
-        const bool check = checks && (k % p.check_every) == 0;
-        if (k == p.n && !check) break;
-        const bool store = k < p.n;
-        // sweeps this pass: up to MAXD, none of them past the end or a check
-        int dp = 1;
-        if (MAXD >= 2 && store && !p.one_sweep) {
-            long long m = p.n - k;
-            if (checks) {
-                const long long to_check = p.check_every - (k % p.check_every);
-                if (to_check < m) m = to_check;
+        int dp = 1, cs = 0;
+        bool store = true;
+        if (redo) {
+            dp = (int)(k_exit - k);
+        } else {
+            const bool check_here = checks && (k % p.check_every) == 0;
+            if (k == p.n && !check_here) break;
+            store = k < p.n;
+            // sweeps this pass: up to MAXD, none of them past the end or
+            // (unless the pass straddles it) a check
+            cs = check_here ? 1 : 0;
+            if (MAXD >= 2 && store && !p.one_sweep) {
+                long long m = p.n - k;
+                if (checks) {
+                    const long long to_check = p.check_every - (k % p.check_every);
+                    if (STRADDLE && !check_here && to_check < MAXD && m >= MAXD &&
+                        to_check + p.check_every >= MAXD) {
+                        cs = (int)to_check + 1;
+                        m = MAXD;
+                    } else if (to_check < m) {
+                        m = to_check;
+                    }
+                }
+                dp = m < MAXD ? (int)m : MAXD;
             }
-            dp = m < MAXD ? (int)m : MAXD;
         }
         double s2 = 0.0;
         float rmax = 0.f;
-        pass(p.u[cur], p.u[cur ^ 1], check, store, dp, k, s2, rmax);
+        pass(p.u[cur], p.u[cur ^ 1], cs, store, dp, k, s2, rmax);
+        if (redo) {  // no barrier: the kernel ends here
+            cur ^= 1;
+            k = k_exit;
+            break;
+        }
         Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
-        if (check) {
+        if (cs) {
             block_reduce(s2, rmax);
             if (threadIdx.x == 0) {
                 Partial pp;
@@ -89,7 +126,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
             }
         }
         if (!grid_barrier(s_ctl)) return;  // aborting: the host reads the error
-        if (check) {
+        if (cs) {
             double S2;
             float RM;
             reduce_partials(parts, (int)gridDim.x, S2, RM);
@@ -99,10 +136,18 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
                 s_res_last = res;
                 s_rmax_last = RM;
             }
+            const long long kc = k + cs - 1;  // the iterate this check measured
             // s_res0 was written at the first check, barriers ago
-            if (k == 0) {
+            if (kc == 0) {
                 if (threadIdx.x == 0) s_res0 = res;
             } else if (res < (double)p.tol * s_res0) {
+                if (STRADDLE && cs >= 2) {
+                    // U_kc again, from U_k, into dst (every CTA takes this
+                    // branch: the decision is the same everywhere)
+                    redo = true;
+                    k_exit = kc;
+                    continue;
+                }
                 break;
             }
         }
@@ -121,6 +166,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         d->cur = cur;
         d->task_sweeps = 0;
         d->barriers = s_ctl.index;
+        d->passes = s_ctl.index + (redo ? 1 : 0);  // every other pass ends at a barrier
         d->bar_count_end = p.bar_base + (unsigned)s_ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;

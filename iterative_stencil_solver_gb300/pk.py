@@ -37,6 +37,7 @@ PK_FLAG_LAUNCH_PROBLEM_GRID = 0x1
 PK_FLAG_ALTERNATE_DIRECTION = 0x2
 PK_FLAG_PROFILE_BARRIER = 0x4
 PK_FLAG_ONE_SWEEP_PER_PASS = 0x8
+PK_FLAG_CHECKS_END_PASSES = 0x10
 
 PK_BARRIER_GENERATION = 0
 PK_BARRIER_COUNTER = 1
@@ -70,6 +71,8 @@ class pk_run_info(ctypes.Structure):
         ("stream_config", ctypes.c_int32),
         ("sweeps_per_pass", ctypes.c_int32),
         ("device_us", ctypes.c_double),
+        ("passes", ctypes.c_int32),
+        ("straddle", ctypes.c_int32),
     ]
 
     def as_dict(self):

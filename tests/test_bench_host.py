@@ -4,10 +4,13 @@ import bench
 CELLS = 16384 * 16384
 
 
-def info(variant, shape, depth=None):
+def info(variant, shape, depth=None, straddle=None):
     if depth is None:
         depth = bench.SHAPES[shape][2] if variant == 2 else 1
-    return {"variant": variant, "stream_config": shape, "sweeps_per_pass": depth}
+    if straddle is None:  # the plan takes the straddling kernel for three-sweep STREAM shapes
+        straddle = variant == 2 and depth == 3
+    return {"variant": variant, "stream_config": shape, "sweeps_per_pass": depth,
+            "straddle": int(straddle)}
 
 
 def test_single_sweep_shape_moves_8_bytes_per_cell_update():
@@ -22,19 +25,46 @@ def test_two_sweep_shape_moves_8_bytes_per_two_cell_updates():
     assert bench.passes_of(info(2, 8), 7, 0.0, 0) == (4, 0)
 
 
-def test_passes_never_straddle_a_check():
+def test_passes_stop_at_checks_unless_three_sweep_stream():
     # odd interval on a STREAM two-sweep shape: passes of 2 and 1 sweeps
     assert bench.passes_of(info(2, 6), 9, 1e-4, 3) == (6, 1)
-    # a three-sweep shape with an interval of 10: 3, 3, 3, 1
-    assert bench.passes_of(info(2, 10), 20, 1e-4, 10) == (8, 1)
     # a depth-2 LOCAL run with an odd interval: passes of 2, 1, 2, 1, ... never past a check
     assert bench.passes_of(info(3, -1, 2), 9, 1e-4, 3) == (6, 1)
-    # depth 3 and an interval of 10: 3, 3, 3, 1 per interval
+    # LOCAL at depth 3 and an interval of 10: 3, 3, 3, 1 per interval
     assert bench.passes_of(info(3, -1, 3), 20, 1e-4, 10) == (8, 1)
     # even interval: pairs, plus the check-only pass when n is a multiple
     assert bench.passes_of(info(2, 6), 2000, 1e-4, 10) == (1000, 1)
     b = bench.algorithmic_bytes(info(2, 6), 4096 * 4096, 2000, True, 1e-4, 10)
     assert b == 4096 * 4096 * (1000 * 12.0 + 8.0)
+
+
+def test_three_sweep_stream_passes_straddle_checks():
+    # interval 10: passes from 0, 3, 6, 9 (check 10 in stage 2), 12, 15, 18
+    # (check 20 would be in stage 3, but only two sweeps are left: the pass
+    # stops at 20), then the check-only pass
+    assert bench.passes_of(info(2, 10), 20, 1e-4, 10) == (7, 1)
+    # 30 sweeps take ten passes: checks 10, 20 and 30 in stages 2, 3 and 1
+    assert bench.passes_of(info(2, 12), 30, 1e-4, 10) == (10, 1)
+    # the 4096^2 Poisson run: 667 passes instead of 800
+    assert bench.passes_of(info(2, 12), 2000, 1e-4, 10) == (667, 1)
+    b = bench.algorithmic_bytes(dict(info(2, 12), sweeps_done=2000), 4096 * 4096, 2000, True, 1e-4, 10)
+    assert b == 4096 * 4096 * (667 * 12.0 + 8.0)
+    # a run that did not take the straddling kernel stops its passes at checks
+    assert bench.passes_of(info(2, 11, straddle=False), 20, 1e-4, 10) == (8, 1)
+    # no straddling where a second check would fall inside the pass
+    assert bench.passes_of(info(2, 11), 10, 1e-4, 2) == (5, 1)
+    assert bench.passes_of(info(2, 11), 10, 1e-4, 1) == (10, 1)
+    # interval 4: 0..3 (check 0), 3..6 (check 4 in stage 2), 6..8 (stops at 8), ...
+    assert bench.passes_of(info(2, 11), 8, 1e-4, 4) == (3, 1)
+
+
+def test_exit_at_a_straddled_check_costs_one_more_pass():
+    # exit at check 10 (stage 2 of the pass from 9): 4 passes + the sweep again from 9
+    assert bench.passes_of(info(2, 12), 1000, 1e-4, 10, exit_at=10) == (5, 0)
+    # exit at 20 (stage 3 of the pass from 18)
+    assert bench.passes_of(info(2, 12), 1000, 1e-4, 10, exit_at=20) == (8, 0)
+    # exit at 30 (stage 1 of the pass from 30: U_30 is in memory)
+    assert bench.passes_of(info(2, 12), 1000, 1e-4, 10, exit_at=30) == (11, 0)
 
 
 def test_other_variants_take_one_sweep_per_pass():

@@ -547,6 +547,61 @@ def test_stream_default_plan_one_column_strip(pk, nx, ny, poisson):
     check_info(info, oinfo)
 
 
+# Runs with checks on a three-sweep shape take the kernel whose passes run
+# past a check (the check in stage 2 or 3 of a full pass) when no second
+# check falls inside the pass.  Intervals of 2, 4, 5, 7 and 10 put checks in
+# every stage; the kernel's pass count must follow the model in bench.py.
+STRADDLE_RUNS = [(20, 4), (23, 5), (31, 7), (40, 10), (17, 2)]
+
+
+@pytest.mark.parametrize("cfg", [10, 11, 12])
+@pytest.mark.parametrize("nx,ny", [(300, 41), (2053, 19), (1793, 9), (897, 5)],
+                         ids=["300x41", "2053x19", "1793x9", "897x5"])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_straddled_checks_bit_exact(pk, cfg, nx, ny, poisson):
+    import bench
+    u0 = inputs.random_field(nx, ny, seed=700 + cfg + nx)
+    f = inputs.uniform_pm1(800 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, ce in STRADDLE_RUNS:
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=1e-30, check_every=ce)
+        try:
+            got, info = run_pk(pk, u0, f, n, 1e-30, ce, variant=2, stream_config=cfg,
+                               flags=pk.PK_FLAG_ALTERNATE_DIRECTION if (n + cfg) % 2 else 0)
+        except pk.PkError as e:
+            assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
+            return
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+        assert info["passes"] == sum(bench.passes_of(info, n, 1e-30, ce))
+        if poisson and cfg == 12:  # the default Poisson shape's straddling kernel fits in registers
+            assert info["straddle"] == 1
+
+
+# An early exit at a check taken in stage 2 or 3: U_c is not in memory when
+# the check ends the run, so the kernel sweeps again from U_k to U_c.  With an
+# interval of 10 the checks at 10, 20, 30, 40 and 50 fall in stages 2, 3, 1,
+# 2 and 3; tol is set from the oracle's own residuals to stop at each one.
+@pytest.mark.parametrize("cfg", [10, 11, 12])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_straddled_exit_mid_pass(pk, cfg, poisson):
+    import bench
+    nx, ny = 1030, 37
+    u0 = inputs.random_field(nx, ny, seed=900 + cfg)
+    f = inputs.uniform_pm1(901, nx * ny).reshape(ny, nx) if poisson else None
+    g = oracle.scale_source(nx, ny, oracle.h2(nx), f) if poisson else None
+    res0 = oracle.residual(u0, g)[0]
+    for m in range(1, 6):
+        um, _ = oracle.jacobi_run(u0, f=f, n=10 * m)
+        ratio = oracle.residual(um, g)[0] / res0
+        tol = float(np.float32(ratio * (1.0 + 1e-5)))
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=1000, tol=tol, check_every=10)
+        assert oinfo.sweeps_done == 10 * m
+        got, info = run_pk(pk, u0, f, 1000, tol, 10, variant=2, stream_config=cfg)
+        assert_same_bits(got, want, "exit at %d" % (10 * m))
+        check_info(info, oinfo)
+        assert info["passes"] == sum(bench.passes_of(info, 1000, tol, 10, exit_at=10 * m))
+
+
 # The sweep kernels accumulate the residual's squares as a pair of floats
 # scaled by a power of two that follows the largest residual seen: a field
 # scaled far down has every r^2 below the fp32 normal range unscaled, fields

@@ -37,9 +37,11 @@ def _same_bits(a, b):
 
 
 def _info_matches(a, b):
+    # `current` may differ: the two plans can take different numbers of
+    # passes (LOCAL's passes stop at checks, STREAM's can straddle them), so
+    # each call's result is read from the buffer its own info names.
     assert a["sweeps_done"] == b["sweeps_done"]
     assert a["n_checks"] == b["n_checks"]
-    assert a["current"] == b["current"]
     assert a["res_max_last"] == b["res_max_last"]
     assert a["res0"] == pytest.approx(b["res0"], rel=1e-10, abs=0)
     assert a["res_last"] == pytest.approx(b["res_last"], rel=1e-10, abs=0)
