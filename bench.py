@@ -53,8 +53,11 @@ WORKLOADS = {
     "poisson-4096x4096-2000sweeps-res10": (4096, 2, 2000, True, 1e-4, 10),
     "laplace-512x512-1000sweeps": (512, 1, 1000, False, 0.0, 0),
     "laplace-64x64-topedge-100sweeps": (64, None, 100, False, 0.0, 0),
-    # profiling-sized case: two 268 MB buffers (> L2), short enough for ncu replays
+    # profiling-sized cases: inputs larger than L2, short enough for ncu replays
     "laplace-8192x8192-10sweeps": (8192, 3, 10, False, 0.0, 0),
+    # seven passes: checks at 0, 10 and 20 fall in stages 1, 2 and 3
+    "poisson-4096x4096-21sweeps-res10": (4096, 2, 21, True, 1e-4, 10),
+    "poisson-4096x4096-21sweeps": (4096, 2, 21, True, 0.0, 0),
 }
 DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 
@@ -62,8 +65,8 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "9d87a1893e1f34b7", "stream_config": 11,
-           "bytes_per_launch": 35.587e9 + 36.490e9}
+TRAFFIC = {"kernel_sha": "6ad435692fd7622a", "stream_config": 11,
+           "bytes_per_launch": 35.583e9 + 36.491e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
@@ -516,6 +519,52 @@ def latency_extras(pk):
     return out
 
 
+def e2e_steps(pk, ctx, w, args, world, torch):
+    """The bench steps end to end through the public API (host buffers in and
+    out); returns the e2e record and the serial set/run/get number."""
+    cells = w["nx"] * w["ny"]
+    sweeps = w["sweeps"]
+    # e2e through the public API with pinned host buffers: every step
+    # uploads its field, sweeps and downloads its result.  pk_run_batch
+    # runs the steps as a pipeline (step i+1's upload and step i-1's
+    # download overlap step i's sweeps); the tensors are kept so their
+    # pages stay pinned.
+    host_in_t = torch.from_numpy(w["u0"]).pin_memory()
+    host_out_t = [torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory()
+                  for _ in range(2)]
+    assert host_in_t.is_pinned() and all(t.is_pinned() for t in host_out_t)
+    host_in, host_out = host_in_t.numpy(), [t.numpy() for t in host_out_t]
+    pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
+                    w["check_every"])
+    dist_barrier(world)
+    t0 = time.perf_counter()
+    infos = pk.pk_run_batch(ctx, [host_in] * args.steps,
+                            [host_out[q % 2] for q in range(args.steps)], sweeps, w["tol"],
+                            w["check_every"])
+    e2e_s = dist_max(world, time.perf_counter() - t0)
+    e2e_updates = sum(cells * info["sweeps_done"] for info in infos)
+    e2e_value = dist_sum(world, e2e_updates) / e2e_s
+    e2e_launches = len(infos) * 3  # per step: ring copy, persistent kernel, result record
+    # the same steps one call after another (set, run, get), for context
+    pk.pk_set_field(ctx, host_in)
+    pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+    pk.pk_get_field(ctx, host_out[0])
+    dist_barrier(world)
+    serial_steps = min(args.steps, 10)
+    serial_updates = 0
+    t0 = time.perf_counter()
+    for _ in range(serial_steps):
+        pk.pk_set_field(ctx, host_in)
+        info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
+        pk.pk_get_field(ctx, host_out[0])
+        serial_updates += cells * info["sweeps_done"]
+    serial_s = dist_max(world, time.perf_counter() - t0)
+    serial_value = dist_sum(world, serial_updates) / serial_s
+    return {"value": e2e_value, "seconds": e2e_s, "launches": e2e_launches,
+            "sweeps_ms_median": statistics.median(i["device_us"] for i in infos) / 1e3,
+            "serial_value": serial_value, "serial_steps": serial_steps}
+
+
 # ---- main arm ----------------------------------------------------------------------
 
 def main():
@@ -527,6 +576,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true", help="skip the supplementary measurements")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true",
+                    help="skip the end-to-end measurement (profiling runs)")
     ap.add_argument("--stream-config", type=int, default=-1,
                     help="STREAM shape index (include/pk.h pk_options.stream_config), -1 = default")
     args = ap.parse_args()
@@ -576,43 +627,7 @@ def main():
         value = updates_all / dev_s_max
         ms_per_step = dev_s_max * 1e3 / args.steps
         us_per_sweep = dev_s * 1e6 / (updates / cells)
-
-        # e2e through the public API with pinned host buffers: every step
-        # uploads its field, sweeps and downloads its result.  pk_run_batch
-        # runs the steps as a pipeline (step i+1's upload and step i-1's
-        # download overlap step i's sweeps); the tensors are kept so their
-        # pages stay pinned.
-        host_in_t = torch.from_numpy(w["u0"]).pin_memory()
-        host_out_t = [torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory()
-                      for _ in range(2)]
-        assert host_in_t.is_pinned() and all(t.is_pinned() for t in host_out_t)
-        host_in, host_out = host_in_t.numpy(), [t.numpy() for t in host_out_t]
-        pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
-                        w["check_every"])
-        dist_barrier(world)
-        t0 = time.perf_counter()
-        infos = pk.pk_run_batch(ctx, [host_in] * args.steps,
-                                [host_out[q % 2] for q in range(args.steps)], sweeps, w["tol"],
-                                w["check_every"])
-        e2e_s = dist_max(world, time.perf_counter() - t0)
-        e2e_updates = sum(cells * info["sweeps_done"] for info in infos)
-        e2e_value = dist_sum(world, e2e_updates) / e2e_s
-        e2e_launches = len(infos) * 3  # per step: ring copy, persistent kernel, result record
-        # the same steps one call after another (set, run, get), for context
-        pk.pk_set_field(ctx, host_in)
-        pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
-        pk.pk_get_field(ctx, host_out[0])
-        dist_barrier(world)
-        serial_steps = min(args.steps, 10)
-        serial_updates = 0
-        t0 = time.perf_counter()
-        for _ in range(serial_steps):
-            pk.pk_set_field(ctx, host_in)
-            info = pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
-            pk.pk_get_field(ctx, host_out[0])
-            serial_updates += cells * info["sweeps_done"]
-        serial_s = dist_max(world, time.perf_counter() - t0)
-        serial_value = dist_sum(world, serial_updates) / serial_s
+        e2e = None if args.no_e2e else e2e_steps(pk, ctx, w, args, world, torch)
     finally:
         pk.pk_destroy(ctx)
 
@@ -647,14 +662,16 @@ def main():
                      "peak_source": peak_kind,
                      "kernel": shape_label(run_info, w["f"] is not None),
                      "algorithmic_bytes_per_launch": alg_bytes},
-        "e2e": {"value": e2e_value, "unit": UNIT,
-                "h2d_bytes_per_step": int(w["u0"].nbytes),
-                "d2h_bytes_per_step": int(w["u0"].nbytes),
-                "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps)",
-                "steps": args.steps, "seconds": e2e_s, "gpu_launches": e2e_launches,
-                "sweeps_ms_per_step_median": statistics.median(i["device_us"] for i in infos) / 1e3},
-        "e2e_serial": {"value": serial_value, "unit": UNIT, "steps": serial_steps,
-                       "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"},
+        "e2e": None if e2e is None else {
+            "value": e2e["value"], "unit": UNIT,
+            "h2d_bytes_per_step": int(w["u0"].nbytes),
+            "d2h_bytes_per_step": int(w["u0"].nbytes),
+            "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps)",
+            "steps": args.steps, "seconds": e2e["seconds"], "gpu_launches": e2e["launches"],
+            "sweeps_ms_per_step_median": e2e["sweeps_ms_median"]},
+        "e2e_serial": None if e2e is None else {
+            "value": e2e["serial_value"], "unit": UNIT, "steps": e2e["serial_steps"],
+            "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
