@@ -409,14 +409,34 @@ def latency_extras(pk):
     tasks = [pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=1),
              pk.make_task(pk.PK_TASK_AXPY, a=0.5, x=x.data_ptr(), y=y.data_ptr(),
                           length=x.numel())]
+    # Floors: a NOP on a task kernel of one CTA is the host<->device handshake
+    # alone (CTA 0 completes NOPs without the grid); the device-side
+    # hand-out (distributed shared memory) + gather of one task across the
+    # task kernel's cluster, no host involved.
+    ctx1 = pk.pk_create(256, 256, w["u0"], None, pk.pk_options_default(task_grid=1))
+    try:
+        echo = pk.pk_bench_tasks(ctx1, 0, [pk.make_task(pk.PK_TASK_NOP)], 5100)[100:] / 1e3
+    finally:
+        pk.pk_destroy(ctx1)
     ctx = pk.pk_create(256, 256, w["u0"], None)
     try:
+        n_h = 20000
+        pk.pk_bench_handoff(ctx, 0, n_h)
+        handoff = (pk.pk_bench_handoff(ctx, 0, n_h) - pk.pk_bench_handoff(ctx, 0, 0)) / n_h
+        bar = (pk.pk_bench_barrier(ctx, 2, pk.pk_get_plan(ctx)["task_grid"], 10000)
+               - pk.pk_bench_barrier(ctx, 2, pk.pk_get_plan(ctx)["task_grid"], 0)) / 10000
         mb = pk.pk_bench_tasks(ctx, 0, tasks, 10100)[100:] / 1e3
         nop = pk.pk_bench_tasks(ctx, 0, [pk.make_task(pk.PK_TASK_NOP)], 2100)[100:] / 1e3
         pk.pk_shutdown(ctx)
         ln = pk.pk_bench_tasks(ctx, 1, tasks, 10100)[100:] / 1e3
         lnop = pk.pk_bench_tasks(ctx, 1, [pk.make_task(pk.PK_TASK_NOP)], 2100)[100:] / 1e3
+        echo50 = float(np.percentile(echo, 50))
         out["task_queue_10000"] = {
+            "floors_us": {"echo_one_cta_p50": echo50,
+                          "echo_one_cta_p99": float(np.percentile(echo, 99)),
+                          "handout_gather_task_cluster": handoff,
+                          "grid_barrier_task_grid": bar},
+            "p50_over_echo_plus_barrier": float(np.percentile(mb, 50)) / (echo50 + bar),
             "mailbox_round_trip_us": {"p50": float(np.percentile(mb, 50)),
                                       "p99": float(np.percentile(mb, 99))},
             "launch_sync_round_trip_us": {"p50": float(np.percentile(ln, 50)),
@@ -425,7 +445,7 @@ def latency_extras(pk):
                                           "p99": float(np.percentile(nop, 99))},
             "nop_launch_sync_round_trip_us": {"p50": float(np.percentile(lnop, 50)),
                                               "p99": float(np.percentile(lnop, 99))},
-            "task_grid": pk.pk_get_plan(ctx)["task_grid"],
+            "task_cluster_ctas": pk.pk_get_plan(ctx)["task_grid"],
         }
     finally:
         pk.pk_destroy(ctx)

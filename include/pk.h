@@ -142,7 +142,9 @@ typedef struct {
     uint32_t struct_size;             /* sizeof(pk_options) */
     int32_t variant;                  /* PK_VARIANT_* */
     int32_t grid_override;            /* CTAs for sweeps; 0 = sized by occupancy and problem */
-    int32_t task_grid;                /* CTAs for the task kernel; 0 = auto */
+    int32_t task_grid;                /* CTAs of the task kernel, which runs as one thread-block
+                                         cluster of 1024-thread CTAs (1..16); 0 = auto (16, fewer
+                                         for small fields or where 16 does not fit) */
     double barrier_timeout_s;         /* device spin limit of one barrier wait (default 2.0) */
     double mailbox_idle_timeout_s;    /* task kernel exits after this long with no task (default 10.0) */
     double host_timeout_s;            /* pk_shutdown deadline (default 10.0) */
@@ -295,7 +297,8 @@ int pk_set_field(pk_ctx *ctx, const float *host_in);
 int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *current);
 
 /* The launch plan chosen at creation: sweep variant (PK_VARIANT_DIRECT or
- * PK_VARIANT_STREAM), persistent sweep grid (CTAs), task kernel grid, and
+ * PK_VARIANT_STREAM), persistent sweep grid (CTAs), task kernel grid (the
+ * CTAs of its one cluster), and
  * the cooperative capacity (resident CTAs per SM x SMs) of the sweep
  * kernel.  Any output may be NULL. */
 int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max);
@@ -304,10 +307,12 @@ int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_
  * "Thread synchronization", "Atomics and memory ordering"; [P3] "Device
  * Communication").  Starts the resident task kernel on first use (on a
  * stream of its own, [P3] "Stream concurrency").  The descriptor goes to
- * slot seq % depth, then seq is published with a release store; one leader
- * thread polls it, broadcasts it through device memory, the grid runs it,
- * and the completion sequence is written with a system-scope release only
- * after every CTA has finished ([P1] "Reflections": no early ACK).
+ * slot seq % depth (every word tagged with seq), after a release fence; one
+ * leader thread polls it, broadcasts it through device memory (a line of
+ * words tagged like the slot's), the grid runs it, and the completion
+ * sequence is written with a system-scope release only after every CTA has
+ * finished ([P1] "Reflections": no early ACK).  A NOP completes as soon as
+ * the leader reads it.
  * *seq_out (may be NULL) receives the task's sequence number (1, 2, ...).
  * Errors: PK_EINVAL (bad task), PK_EBUSY (ring full), PK_ESHUTDOWN,
  * PK_ENORESIDENT, PK_ECUDA. */
@@ -406,6 +411,17 @@ int pk_barrier_stress(pk_ctx *ctx, int grid, int rounds, int words, uint64_t *ch
  * may count stale words; they cannot hang or fault). */
 int pk_barrier_stress_tma(pk_ctx *ctx, int grid, int rounds, int mode, uint64_t *checksums,
                           int64_t *stale);
+
+/* The task kernel's device-side handoff alone ([P1] "Custom block
+ * scheduling" measures the cost per block of a handshake): a launch of the
+ * task kernel with `grid` CTAs (0 = the context's task grid) in which CTA 0
+ * makes up n_tasks empty tasks itself -- each broadcast to the grid and
+ * gathered back as a real task is, with no work and no host memory touched
+ * -- then stops.  *us_total is the launch's device time (CUDA events),
+ * launch included; the difference of two counts over their difference is
+ * the cost of one broadcast plus gather.  Errors: PK_EBUSY (task kernel
+ * live), PK_ENORESIDENT, PK_ETIMEDOUT, PK_ECUDA. */
+int pk_bench_handoff(pk_ctx *ctx, int grid, int64_t n_tasks, double *us_total);
 
 /* Round-trip timing of a task list, host clock (ns per task into
  * samples[0..n_tasks-1]).  mode 0: through the mailbox (submit, then poll

@@ -103,6 +103,19 @@ __device__ __forceinline__ void ld_relaxed_sys_v2_u64(const unsigned long long *
                  : "l"(p)
                  : "memory");
 }
+__device__ __forceinline__ void ld_relaxed_gpu_v2_u64(const unsigned long long *p,
+                                                      unsigned long long &a,
+                                                      unsigned long long &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];"
+                 : "=l"(a), "=l"(b)
+                 : "l"(p)
+                 : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu_v2_u64(unsigned long long *p, unsigned long long a,
+                                                      unsigned long long b) {
+    asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
+                 : "memory");
+}
 __device__ __forceinline__ void fence_acq_rel_sys() {
     asm volatile("fence.acq_rel.sys;" ::: "memory");
 }
@@ -354,6 +367,57 @@ __device__ __forceinline__ void sts4_at(unsigned a, float4 v) {
                  "f"(v.z), "f"(v.w)
                  : "memory");
 }
+// ---------------------------------------------------------------------------
+// Thread-block clusters: distributed shared memory and cluster-scope
+// mbarriers (the task kernel runs as one cluster).
+__device__ __forceinline__ unsigned cluster_ctarank() {
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// The shared::cluster address of this CTA's shared-window address `a` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ unsigned cluster_map(unsigned a, unsigned rank) {
+    unsigned r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void ld_cluster_v4(unsigned a, unsigned &x, unsigned &y, unsigned &z,
+                                              unsigned &w) {
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(x), "=r"(y), "=r"(z), "=r"(w)
+                 : "r"(a)
+                 : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(unsigned a, unsigned x, unsigned y, unsigned z,
+                                              unsigned w) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(x), "r"(y),
+                 "r"(z), "r"(w)
+                 : "memory");
+}
+// Arrive on an mbarrier of another CTA of the cluster (or this one), with
+// release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(unsigned a_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(a_cluster)
+                 : "memory");
+}
+// Test a phase of this CTA's mbarrier with acquire semantics at cluster scope.
+__device__ __forceinline__ bool mbar_try_wait_cluster(unsigned bar, unsigned parity) {
+    unsigned done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0u;
+}
+// Every thread of every CTA of the cluster (hardware barrier; all reach it).
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completing on bar.
 // dst, src 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void tma_load_1d(void *dst, const void *src, unsigned bytes,

@@ -44,7 +44,6 @@ struct Scratch {
     BarrierState bar_bench;
     DeviceInfo info;
     alignas(64) ResidualOut res;
-    alignas(64) TaskSlot desc;
     alignas(128) unsigned long long stale;
 };
 
@@ -110,7 +109,8 @@ struct pk_ctx {
     Mailbox *mbox_dev = nullptr;
     size_t mbox_bytes = 0;
     bool task_live = false;
-    int task_grid = 1;
+    int task_grid = 1;        // CTAs of the task kernel (its one cluster)
+    int task_launch_grid = 1; // CTAs of the launch-per-task comparison's kernels
     unsigned long long next_seq = 1;
     int task_status = PK_OK;
     int run_id = 0;
@@ -471,14 +471,29 @@ int plan(pk_ctx *ctx) {
         if (ctx->opt.grid_override > 0) ctx->grid = ctx->opt.grid_override;
     }
     ctx->coop_max = cap;
-    // task kernel (DIRECT sweep + axpy, 256 threads)
-    int tper = 0;
-    const int tcap = coop_capacity(ctx, kernel_task(ctx->poisson), kDirectThreads, 0, &tper);
-    if (tcap <= 0) return tcap < 0 ? PK_ECUDA : fail(ctx, PK_ENORESIDENT, "task kernel does not fit");
-    long long tneed = (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
-    if (tneed < 1) tneed = 1;
-    ctx->task_grid = (int)(tneed < tcap ? tneed : tcap);
-    if (ctx->opt.task_grid > 0) ctx->task_grid = ctx->opt.task_grid;
+    // Task kernel: one cluster of up to 16 CTAs of 1024 threads (fewer when
+    // the problem has fewer float4 groups, or when the option asks), the
+    // largest size the device schedules.  The launch-per-task comparison
+    // runs its kernels with one thread per float4 group.
+    {
+        long long tneed = (direct_units(ctx) + kTaskThreads - 1) / kTaskThreads;
+        int want = ctx->opt.task_grid > 0 ? ctx->opt.task_grid : kTaskMaxCluster;
+        if (want > kTaskMaxCluster) want = kTaskMaxCluster;
+        if (ctx->opt.task_grid <= 0 && tneed < want) want = tneed < 1 ? 1 : (int)tneed;
+        int fit = 0;
+        while (want >= 1) {
+            cudaError_t e = task_clusters_fit(ctx->poisson, want, &fit);
+            if (e != cudaSuccess) (void)cudaGetLastError();
+            if (e == cudaSuccess && fit > 0) break;
+            --want;
+        }
+        if (want < 1) return fail(ctx, PK_ENORESIDENT, "task kernel cluster does not fit");
+        ctx->task_grid = want;
+        long long lneed = (direct_units(ctx) + kDirectThreads - 1) / kDirectThreads;
+        if (lneed < 1) lneed = 1;
+        if (lneed > (1LL << 30)) lneed = 1LL << 30;
+        ctx->task_launch_grid = (int)lneed;
+    }
     // The per-launch and graph paths run the persistent kernels' per-launch
     // forms on the same grid, except for a LOCAL context: its launches run
     // the DIRECT kernel, sized for one float4 group per thread.
@@ -1461,7 +1476,7 @@ int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out) {
         tp.sp.bar_base = 0;  // zeroed just above
         tp.sp.profile = 0;
         tp.mbox = ctx->mbox_dev;
-        tp.dev_desc = &ctx->scratch->desc;
+        tp.synthetic = -1;
         tp.tb = &ctx->scratch->bar_task;
         tp.start_seq = base;
         tp.depth = ctx->opt.mailbox_depth;
@@ -1708,6 +1723,35 @@ int pk_barrier_stress_tma(pk_ctx *ctx, int grid, int rounds, int mode, uint64_t 
     return PK_OK;
 }
 
+int pk_bench_handoff(pk_ctx *ctx, int grid, int64_t n_tasks, double *us_total) {
+    if (!ctx || grid < 0 || n_tasks < 0) return PK_EINVAL;
+    if (ctx->task_live) return fail(ctx, PK_EBUSY, "pk_bench_handoff: the task kernel is live");
+    if (grid == 0) grid = ctx->task_grid;
+    if (grid > kTaskMaxCluster) return fail(ctx, PK_EINVAL, "pk_bench_handoff: at most %d CTAs", kTaskMaxCluster);
+    PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_task, 0, sizeof(BarrierState), ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(&ctx->scratch->bar_task_inner, 0, sizeof(BarrierState), ctx->stream));
+    TaskParams tp;
+    std::memset(&tp, 0, sizeof(tp));
+    tp.sp = base_params(ctx);
+    tp.sp.bar = &ctx->scratch->bar_task_inner;
+    tp.sp.skip_cta = -1;
+    tp.sp.bar_base = 0;
+    tp.sp.profile = 0;
+    tp.mbox = ctx->mbox_dev;
+    tp.tb = &ctx->scratch->bar_task;
+    tp.depth = ctx->opt.mailbox_depth;
+    tp.idle_timeout_ns = ns_of(ctx->opt.mailbox_idle_timeout_s);
+    tp.synthetic = n_tasks;
+    PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
+    cudaError_t e = launch_task(ctx->poisson, grid, tp, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(task kernel)");
+    PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
+    int rc = bar_status(ctx, &ctx->scratch->bar_task, "pk_bench_handoff");
+    if (rc != PK_OK) return rc;
+    if (us_total) *us_total = elapsed_us(ctx);
+    return PK_OK;
+}
+
 int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int64_t n_tasks,
                    int64_t *samples_ns) {
     if (!ctx || !tasks || n_kinds <= 0 || n_tasks < 0 || (mode != 0 && mode != 1))
@@ -1749,11 +1793,11 @@ int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int
                 p.pass_check = 0;
                 p.pass_store = 1;
                 p.pass_k = 0;
-                e = launch_once(kVariantDirect, ctx->poisson, 0, ctx->task_grid, p, ctx->stream);
+                e = launch_once(kVariantDirect, ctx->poisson, 0, ctx->task_launch_grid, p, ctx->stream);
                 ctx->cur ^= 1;
             }
         } else if (task.kind == PK_TASK_AXPY) {
-            e = launch_axpy(ctx->task_grid, task.a, task.x, task.y, task.len, ctx->stream);
+            e = launch_axpy(ctx->task_launch_grid, task.a, task.x, task.y, task.len, ctx->stream);
         } else {
             e = launch_empty(ctx->stream);
         }

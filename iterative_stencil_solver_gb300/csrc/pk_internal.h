@@ -114,17 +114,19 @@ struct Mailbox {
 constexpr int kTaskExitIdle = 100;   // internal kind: idle timeout, exit
 
 struct TaskParams {
-    SweepParams sp;                 // field, source, inner grid barrier (sp.bar)
+    SweepParams sp;                 // field and source
     Mailbox *mbox;                  // device view of the mapped mailbox
-    TaskSlot *dev_desc;             // device-global broadcast copy
-    BarrierState *tb;               // gather (count) + broadcast (generation)
+    BarrierState *tb;               // abort and error words of the task kernel
     unsigned long long start_seq;   // last sequence number completed before launch
     int depth;
     unsigned long long idle_timeout_ns;
+    long long synthetic;            // >= 0: that many empty tasks made up by CTA 0; -1 = off
 };
 
 // ---- sizes -----------------------------------------------------------------
 constexpr int kDirectThreads = 256;
+constexpr int kTaskThreads = 1024;   // threads per CTA of the task kernel (one cluster)
+constexpr int kTaskMaxCluster = 16;  // CTAs of the task kernel's cluster, at most
 constexpr int kLocalMaxThreads = 512;  // LOCAL kernels run 256 or 512 threads per CTA
 constexpr int kStressWords = 32;
 
@@ -277,7 +279,8 @@ struct RunRecord {
 };
 cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
                                   cudaStream_t s);
-cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s);
+cudaError_t launch_task(bool poisson, int cluster, const TaskParams &p, cudaStream_t s);
+cudaError_t task_clusters_fit(bool poisson, int cluster, int *n);
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,
                         cudaStream_t s);
 cudaError_t launch_empty(cudaStream_t s);

@@ -23,6 +23,7 @@
 //     (reused as the barrier-only microbenchmark).
 #include <cooperative_groups.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "pk_sweep.cuh"
@@ -305,169 +306,204 @@ __global__ void __launch_bounds__(kDirectThreads) k_axpy(float a, const float *x
 
 // ===========================================================================
 // Resident task loop ("Base implementation" rebuilt as the "Reflections"
-// ask).  CTA 0's thread 0 is the only poller of host memory.  Between two
-// tasks the grid does one gather + broadcast:
-//   * every other CTA, after __syncthreads, arrives on tb->count with a
-//     release atomic and spins (acquire) on tb->generation;
-//   * CTA 0's thread 0 waits (acquire) for gridDim.x - 1 arrivals, resets
-//     the count, publishes the finished task's sequence number to the host
-//     (st.release.sys, cumulative over the arrivals it acquired: never
-//     before the work is done), polls the next tagged mailbox slot until
-//     all its words carry the task's tag (then one acquire fence), copies the
-//     descriptor to device memory and releases the next generation.
-// All spins are bounded (idle limit for the host poll, barrier limit for the
-// rest) and end on the abort flag.
+// ask), run as ONE thread-block cluster of C CTAs (up to 16, co-scheduled by
+// the hardware, so no cooperative launch is needed).  CTA 0's thread 0 is the
+// only poller of host memory: with every CTA polling the slot itself, a
+// NOP's round trip grew from 2.6 to 3.4 us on a 64-CTA grid (the pages
+// measure the same effect, a cost per polled block and handshake).
+//   * A task is read from its mailbox slot: eight 8-byte words, each tagged
+//     with the task's sequence number, polled with four 16-byte relaxed
+//     system-scope loads until every tag matches, then one acquire fence.
+//   * A NOP needs no other CTA: CTA 0 publishes its completion at once.
+//   * Any other task: lane r of CTA 0's first warp writes it into the shared
+//     memory of CTA r of the cluster (distributed shared memory) and arrives,
+//     with release semantics at cluster scope, on CTA r's `go` mbarrier; each
+//     CTA's thread 0 waits on its own `go` (acquire, cluster scope) and reads
+//     the task from its own shared memory.  Global-memory flags took two L2
+//     round trips per task more (broadcast and gather, 2.6-3.0 us against
+//     1.2 us for a grid barrier).
+//   * After the task each CTA arrives on CTA 0's `done` mbarrier; CTA 0
+//     waits for all C arrivals (acquire) and only then publishes the task's
+//     sequence number to the host (st.release.sys, cumulative over what it
+//     acquired: never before the work is done).  CTA 0 writes the next task
+//     only after that wait, when no CTA reads the old one any more.
+// Every wait is a bounded try_wait loop (idle limit for the host poll and for
+// `go`, barrier limit for `done`); a CTA that gives up records the error,
+// which makes the leader hand out the exit.  The final cluster barrier keeps
+// every CTA resident (its shared memory valid for remote accesses) until all
+// have left the loop.
+// synthetic >= 0 (a measurement): CTA 0 makes up that many empty tasks, each
+// handed out and gathered like a real one, and touches no host memory.
+constexpr int kTaskEmpty = 101;   // internal: handed out and gathered, no work
+
+// Four 16-byte relaxed system-scope loads of a tagged slot; true when every
+// word carries tag.
+__device__ __forceinline__ bool load_tagged_sys(const unsigned long long *w8, unsigned tag,
+                                                unsigned long long (&w)[8]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) ld_relaxed_sys_v2_u64(w8 + 2 * q, w[2 * q], w[2 * q + 1]);
+    bool ready = true;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ready &= (unsigned)(w[k] >> 32) == tag;
+    return ready;
+}
+
+// A task from the data halves of a slot's words.
+__device__ __forceinline__ TaskSlot decode_task(const unsigned (&d)[8]) {
+    TaskSlot t;
+    t.kind = (int)(d[0] & 0xffu);
+    t.n_sweeps = (int)d[1];
+    t.a = __uint_as_float(d[2]);
+    t.reserved = 0;
+    t.x = (unsigned long long)d[3] | ((unsigned long long)d[4] << 32);
+    t.y = (unsigned long long)d[5] | ((unsigned long long)d[6] << 32);
+    t.len = (long long)((unsigned long long)d[7] | ((unsigned long long)(d[0] >> 8) << 32));
+    t.pad = 0;
+    return t;
+}
+
+// Bounded wait on a phase of this CTA's mbarrier (acquire, cluster scope);
+// false on expiry, or (watch_abort) when the task state is aborting.
+__device__ __forceinline__ bool wait_phase_cluster(unsigned bar, unsigned parity, uint64_t limit_ns,
+                                                   const BarrierState *tb, bool watch_abort) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    unsigned spins = 0;
+    for (;;) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((++spins & 63u) == 0u) {
+            if (watch_abort && aborted(tb)) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
+        }
+    }
+}
+
 template <bool POISSON>
-__global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
+__global__ void __launch_bounds__(kTaskThreads) k_task(TaskParams tp) {
+    __shared__ __align__(16) unsigned s_desc[8];  // the task, written by CTA 0's warp 0
+    __shared__ __align__(8) uint64_t s_go;        // one arrival (from CTA 0) per task
+    __shared__ __align__(8) uint64_t s_done;      // CTA 0: C arrivals per task
     __shared__ TaskSlot s_task;
     const SweepParams &p = tp.sp;
     BarrierState *tb = tp.tb;
-    BarrierCtl inner = make_ctl(p);
-    const unsigned G = gridDim.x;
-    const unsigned first_unit = blockIdx.x * blockDim.x + threadIdx.x;
-    const unsigned stride = G * blockDim.x;
+    const unsigned C = gridDim.x;  // the grid is one cluster
+    const unsigned rank = cluster_ctarank();
+    const bool leader = rank == 0u;
+    const unsigned first_unit = rank * blockDim.x + threadIdx.x;
+    const unsigned stride = C * blockDim.x;
+    const unsigned go_a = smem_u32(&s_go), done_a = smem_u32(&s_done), desc_a = smem_u32(s_desc);
+    if (threadIdx.x == 0) {
+        mbar_init(&s_go, 1);
+        mbar_init(&s_done, C);
+        mbar_fence_init();
+    }
+    cluster_sync();  // every CTA's barriers exist before any remote arrival
     int cur = p.cur;
     long long sweeps = 0;
-    unsigned long long last = tp.start_seq;
-    unsigned gen = 0;
-    bool first = true;
+    unsigned long long last = tp.start_seq;  // last host task taken (CTA 0)
+    long long made = 0;                      // synthetic tasks made (CTA 0)
+    unsigned phase = 0;                      // tasks handed out so far, mod 2
     int final_status = kOk;
     for (;;) {
-        __syncthreads();  // this CTA is done with the previous task
-        if (threadIdx.x == 0) {
-            if (blockIdx.x == 0) {
-                int kind_override = -1;
-                if (!first) {
-                    const uint64_t t0 = globaltimer_ns();
-                    unsigned spins = 0;
-                    while (ld_relaxed_gpu(&tb->count.v) != G - 1u) {
-                        if ((++spins & 255u) == 0u) {
-                            if (aborted(tb) || aborted(p.bar)) {
-                                kind_override = kTaskExitIdle;
-                                break;
-                            }
-                            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                                record_error(tb, kETimedOut, kSiteTaskGather);
-                                kind_override = kTaskExitIdle;
-                                break;
+        if (threadIdx.x < 32) {
+            const unsigned lane = threadIdx.x;
+            if (leader) {
+                // Lane 0 polls the host; then lane r hands the task to CTA r:
+                // it writes the task into CTA r's shared memory and arrives on
+                // CTA r's `go` barrier (its release covers its own stores), all
+                // lanes at once.  One thread arriving on sixteen CTAs in turn
+                // took 0.18 us per CTA.
+                unsigned long long w[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) w[k] = 0ull;
+                if (lane == 0) {
+                    int kind_override = -1;
+                    for (;;) {
+                        if (tp.synthetic >= 0) {
+                            w[0] = (unsigned long long)(made < tp.synthetic ? kTaskEmpty : kTaskStop);
+                            ++made;
+                            break;
+                        }
+                        // Poll the whole tagged slot: the four 16-byte loads
+                        // go out together, and the slot is complete once every
+                        // word carries this task's tag.
+                        const unsigned long long *hw = tp.mbox->slots[(last + 1ull) % (unsigned)tp.depth].w;
+                        const unsigned tag = (unsigned)(last + 1ull);
+                        const uint64_t t0 = globaltimer_ns();
+                        unsigned spins = 0;
+                        while (!load_tagged_sys(hw, tag, w)) {
+                            if ((++spins & 63u) == 0u) {
+                                if (aborted(tb)) {
+                                    kind_override = kTaskExitIdle;
+                                    break;
+                                }
+                                if (globaltimer_ns() - t0 > tp.idle_timeout_ns) {
+                                    record_error(tb, kETimedOut, kSiteMailboxIdle);
+                                    kind_override = kTaskExitIdle;
+                                    break;
+                                }
                             }
                         }
-                    }
-                    fence_acq_rel_gpu();  // acquire every CTA's release arrival
-                    if (kind_override < 0) {
-                        st_relaxed_gpu(&tb->count.v, 0u);
-                        // The system-scope release publishes, cumulatively, the
-                        // task's writes that this thread has acquired.
+                        if (kind_override >= 0) break;
+                        fence_acq_rel_sys();  // acquire: the host's writes before it posted the slot
+                        ++last;
+                        if ((w[0] & 0xffu) != (unsigned long long)kTaskNop) break;
+                        // A NOP is done as soon as it is taken (every task
+                        // before it was gathered): publish it and poll on.
                         st_release_sys_u64(&tp.mbox->done_seq.v, last);
                     }
-                }
-                unsigned long long w[8];
-                if (kind_override < 0) {
-                    // Poll the whole tagged slot: the four 16-byte loads go
-                    // out together, and the slot is complete once every word
-                    // carries this task's tag.
-                    const unsigned long long *hw =
-                        tp.mbox->slots[(last + 1ull) % (unsigned)tp.depth].w;
-                    const unsigned tag = (unsigned)(last + 1ull);
-                    const uint64_t t0 = globaltimer_ns();
-                    unsigned spins = 0;
-                    for (;;) {
-                        ld_relaxed_sys_v2_u64(hw + 0, w[0], w[1]);
-                        ld_relaxed_sys_v2_u64(hw + 2, w[2], w[3]);
-                        ld_relaxed_sys_v2_u64(hw + 4, w[4], w[5]);
-                        ld_relaxed_sys_v2_u64(hw + 6, w[6], w[7]);
-                        bool ready = true;
+                    if (kind_override >= 0) {
 #pragma unroll
-                        for (int k = 0; k < 8; ++k) ready &= (unsigned)(w[k] >> 32) == tag;
-                        if (ready) break;
-                        if ((++spins & 63u) == 0u &&
-                            globaltimer_ns() - t0 > tp.idle_timeout_ns) {
-                            record_error(tb, kETimedOut, kSiteMailboxIdle);
-                            kind_override = kTaskExitIdle;
-                            break;
-                        }
-                    }
-                    // Acquire: the host's writes before it posted the slot.
-                    if (kind_override < 0) fence_acq_rel_sys();
-                }
-                TaskSlot d;
-                if (kind_override < 0) {
-                    const unsigned w0 = (unsigned)w[0];
-                    d.kind = (int)(w0 & 0xffu);
-                    d.n_sweeps = (int)(unsigned)w[1];
-                    d.a = __uint_as_float((unsigned)w[2]);
-                    d.reserved = 0;
-                    d.x = (unsigned long long)(unsigned)w[3] | ((unsigned long long)(unsigned)w[4] << 32);
-                    d.y = (unsigned long long)(unsigned)w[5] | ((unsigned long long)(unsigned)w[6] << 32);
-                    d.len = (long long)((unsigned long long)(unsigned)w[7] |
-                                        ((unsigned long long)(w0 >> 8) << 32));
-                    d.pad = 0;
-                } else {
-                    d.kind = kind_override;
-                    d.n_sweeps = 0;
-                    d.a = 0.f;
-                    d.reserved = 0;
-                    d.x = d.y = 0ull;
-                    d.len = 0;
-                    d.pad = 0;
-                }
-                *tp.dev_desc = d;
-                s_task = d;
-                st_release_gpu(&tb->generation.v, gen + 1u);
-            } else {
-                if (!first) atom_add_release_gpu(&tb->count.v, 1u);
-                const uint64_t t0 = globaltimer_ns();
-                const uint64_t limit = tp.idle_timeout_ns + p.timeout_ns;
-                unsigned spins = 0;
-                bool ok = true;
-                while (ld_relaxed_gpu(&tb->generation.v) == gen) {
-                    if ((++spins & 255u) == 0u) {
-                        if (aborted(tb) || aborted(p.bar)) {
-                            ok = false;
-                            break;
-                        }
-                        if (globaltimer_ns() - t0 > limit) {
-                            record_error(tb, kETimedOut, kSiteTaskBroadcast);
-                            ok = false;
-                            break;
-                        }
+                        for (int k = 0; k < 8; ++k) w[k] = 0ull;
+                        w[0] = (unsigned long long)kind_override;
                     }
                 }
-                fence_acq_rel_gpu();  // acquire CTA 0's release of the descriptor
-                if (ok) {
-                    const volatile TaskSlot *ds = tp.dev_desc;
-                    s_task.kind = ds->kind;
-                    s_task.n_sweeps = ds->n_sweeps;
-                    s_task.a = ds->a;
-                    s_task.x = ds->x;
-                    s_task.y = ds->y;
-                    s_task.len = ds->len;
+                __syncwarp();
+                unsigned d[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) d[k] = __shfl_sync(0xffffffffu, (unsigned)w[k], 0);
+                if (lane < C) {
+                    const unsigned dst = cluster_map(desc_a, lane);
+                    st_cluster_v4(dst, d[0], d[1], d[2], d[3]);
+                    st_cluster_v4(dst + 16u, d[4], d[5], d[6], d[7]);
+                    mbar_arrive_cluster(cluster_map(go_a, lane));
+                }
+            }
+            if (lane == 0) {
+                // Every CTA: wait for the task, then read it from this CTA's
+                // shared memory.  A CTA that gives up records the error and
+                // waits once more: the leader hands out the exit as soon as it
+                // sees the abort flag, and a CTA must not leave the loop while
+                // the leader may still write to its shared memory.
+                bool got = wait_phase_cluster(go_a, phase, tp.idle_timeout_ns + p.timeout_ns, tb, true);
+                if (!got) {
+                    record_error(tb, kETimedOut, kSiteTaskBroadcast);
+                    got = wait_phase_cluster(go_a, phase, 2 * p.timeout_ns + 1000000000ull, tb, false);
+                }
+                if (got) {
+                    unsigned d[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) d[k] = s_desc[k];
+                    s_task = decode_task(d);
                 } else {
-                    s_task.kind = kTaskExitIdle;
+                    s_task.kind = kTaskExitIdle;  // the leader is gone too: last resort
                 }
             }
         }
         __syncthreads();
-        ++gen;
-        first = false;
+        phase ^= 1u;
         const int kind = s_task.kind;
         if (kind == kTaskStop) {
-            ++last;
             final_status = kEShutdown;
             break;
         }
-        if (kind != kTaskNop && kind != kTaskJacobi && kind != kTaskAxpy) {
+        if (kind != kTaskJacobi && kind != kTaskAxpy && kind != kTaskEmpty) {
             final_status = kETimedOut;
             break;
         }
-        ++last;
         if (kind == kTaskJacobi) {
-            bool ok = true;
             for (int s = 0; s < s_task.n_sweeps; ++s) {
-                if (s > 0 && !grid_barrier(inner)) {
-                    ok = false;
-                    break;
-                }
+                if (s > 0) cluster_sync();  // the previous sweep is complete in every CTA
                 double d0 = 0.0;
                 float f0 = 0.f;
                 pass_direct<POISSON, false, true>(p, p.u[cur], p.u[cur ^ 1], first_unit, stride,
@@ -475,16 +511,25 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
                 cur ^= 1;
                 ++sweeps;
             }
-            if (!ok) {
-                final_status = kETimedOut;
-                break;
-            }
         } else if (kind == kTaskAxpy) {
             axpy_range(s_task.a, reinterpret_cast<const float *>(s_task.x),
                        reinterpret_cast<float *>(s_task.y), s_task.len, first_unit, stride);
         }
+        __syncthreads();  // this CTA's part of the task is done
+        if (threadIdx.x == 0) {
+            mbar_arrive_cluster(cluster_map(done_a, 0));
+            if (leader) {
+                // Gather: every CTA has finished; then tell the host.
+                if (!wait_phase_cluster(done_a, phase ^ 1u, p.timeout_ns, tb, true)) {
+                    record_error(tb, kETimedOut, kSiteTaskGather);
+                } else if (tp.synthetic < 0) {
+                    st_release_sys_u64(&tp.mbox->done_seq.v, last);
+                }
+            }
+        }
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
+    cluster_sync();  // no CTA leaves while another may still arrive on its barriers
+    if (leader && threadIdx.x == 0) {
         DeviceInfo *d = p.info;
         d->sweeps_done = 0;
         d->cur = cur;
@@ -493,9 +538,11 @@ __global__ void __launch_bounds__(kDirectThreads) k_task(TaskParams tp) {
         d->n_checks = 0;
         __threadfence();
         d->run_id = p.run_id;
-        __threadfence_system();
-        st_release_sys_u64(&tp.mbox->status.v, (unsigned long long)(long long)final_status);
-        if (final_status == kEShutdown) st_release_sys_u64(&tp.mbox->done_seq.v, last);
+        if (tp.synthetic < 0) {
+            __threadfence_system();
+            st_release_sys_u64(&tp.mbox->status.v, (unsigned long long)(long long)final_status);
+            if (final_status == kEShutdown) st_release_sys_u64(&tp.mbox->done_seq.v, last);
+        }
     }
 }
 
@@ -671,6 +718,11 @@ cudaError_t prepare_kernels() {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
         if (e != cudaSuccess) return e;
         if ((size_t)lim < local_max) local_max = (size_t)lim;
+    }
+    for (int poisson = 0; poisson < 2; ++poisson) {
+        e = cudaFuncSetAttribute(kernel_task(poisson != 0),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
     }
     bool ok[2][kNumStreamConfigs];
     for (int poisson = 0; poisson < 2; ++poisson) {
@@ -851,11 +903,43 @@ cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *ba
     return cudaGetLastError();
 }
 
-cudaError_t launch_task(bool poisson, int grid, const TaskParams &p, cudaStream_t s) {
+// The task kernel is one cluster of `cluster` CTAs: the hardware schedules
+// a cluster's CTAs together, so they are co-resident without a cooperative
+// launch.
+cudaError_t launch_task(bool poisson, int cluster, const TaskParams &p, cudaStream_t s) {
     TaskParams arg = p;
     void *args[] = {&arg};
-    return cudaLaunchCooperativeKernel(kernel_task(poisson), dim3(grid), dim3(kDirectThreads), args,
-                                       0, s);
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3(kTaskThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, kernel_task(poisson), args);
+}
+
+// Clusters of the task kernel's size `cluster` that fit on the device at once
+// (0: the size is not schedulable).
+cudaError_t task_clusters_fit(bool poisson, int cluster, int *n) {
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)cluster);
+    cfg.blockDim = dim3(kTaskThreads);
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaOccupancyMaxActiveClusters(n, kernel_task(poisson), &cfg);
 }
 
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,

@@ -165,6 +165,8 @@ _SIGS = {
                                              ctypes.POINTER(ctypes.c_uint64), _I64P]),
     "pk_bench_tasks": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.POINTER(pk_task), ctypes.c_int,
                                       ctypes.c_int64, _I64P]),
+    "pk_bench_handoff": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_int64,
+                                        ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -416,3 +418,11 @@ def pk_bench_tasks(ctx, mode, tasks, n_tasks):
     _check(_lib.pk_bench_tasks(ctx, mode, arr, len(tasks), int(n_tasks),
                                out.ctypes.data_as(_I64P)), ctx)
     return out
+
+
+def pk_bench_handoff(ctx, grid, n_tasks):
+    """Device time (us) of a task-kernel launch that broadcasts and gathers
+    n_tasks empty tasks made up on the device (grid 0 = the task grid)."""
+    us = ctypes.c_double()
+    _check(_lib.pk_bench_handoff(ctx, grid, n_tasks, ctypes.byref(us)), ctx)
+    return us.value

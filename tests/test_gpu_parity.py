@@ -362,6 +362,61 @@ def test_mailbox_pipelined_ring_and_restart(pk):
         pk.pk_destroy(ctx)
 
 
+# NOPs are completed by CTA 0 alone (no broadcast, no gather); mixed with
+# Jacobi and axpy tasks through a small ring, every task still completes in
+# order and the field and y advance exactly by the other tasks.  Then the
+# device-side handoff measurement runs on the same context, and tasks run
+# again after it.
+def test_mailbox_nops_between_tasks_and_handoff_bench(pk):
+    import torch
+    nx = ny = 80
+    u0 = inputs.random_field(nx, ny, seed=23)
+    dev = torch.device("cuda", 0)
+    x = torch.from_numpy(inputs.uniform_pm1(24, 4099)).to(dev)
+    y = torch.from_numpy(inputs.uniform_pm1(25, 4099)).to(dev)
+    y0 = y.cpu().numpy()
+    torch.cuda.synchronize()
+    ctx = pk.pk_create(nx, ny, u0, None, pk.pk_options_default(mailbox_depth=3))
+    try:
+        seqs, sweeps, axpys = [], 0, 0
+        for k in range(60):
+            if k % 4 == 1:
+                t = pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=1 + (k % 3))
+                sweeps += 1 + (k % 3)
+            elif k % 4 == 3:
+                t = pk.make_task(pk.PK_TASK_AXPY, a=0.5, x=x.data_ptr(), y=y.data_ptr(),
+                                 length=x.numel())
+                axpys += 1
+            else:
+                t = pk.make_task(pk.PK_TASK_NOP)
+            while True:
+                try:
+                    seqs.append(pk.pk_submit_task(ctx, t))
+                    break
+                except pk.PkError as e:
+                    assert e.code == pk.PK_EBUSY
+        pk.pk_wait(ctx, seqs[-1], 10.0)
+        assert all(pk.pk_poll(ctx, s) == 1 for s in seqs)
+        assert pk.pk_shutdown(ctx) == 0
+        want, _ = oracle.jacobi_run(u0, n=sweeps)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+        yw = y0.copy()
+        for _ in range(axpys):
+            yw = oracle.axpy(0.5, x.cpu().numpy(), yw)
+        assert_same_bits(y.cpu().numpy(), yw, "y")
+        t0 = pk.pk_bench_handoff(ctx, 0, 0)
+        t1 = pk.pk_bench_handoff(ctx, 0, 2000)
+        t2 = pk.pk_bench_handoff(ctx, 1, 2000)
+        assert t1 > t0 > 0 and t2 > 0
+        s = pk.pk_submit_task(ctx, pk.make_task(pk.PK_TASK_JACOBI, n_sweeps=3))
+        pk.pk_wait(ctx, s, 10.0)
+        assert pk.pk_shutdown(ctx) == 0
+        want, _ = oracle.jacobi_run(u0, n=sweeps + 3)
+        assert_same_bits(pk.pk_get_field(ctx), want)
+    finally:
+        pk.pk_destroy(ctx)
+
+
 def test_mailbox_idle_timeout_reports_and_recovers(pk):
     import time
     nx = ny = 64
