@@ -65,7 +65,7 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "6ad435692fd7622a", "stream_config": 11,
+TRAFFIC = {"kernel_sha": "6ad435692fd7622a", "stream_config": 10,
            "bytes_per_launch": 35.583e9 + 36.491e9}
 
 
@@ -318,8 +318,9 @@ def reference_arm(args, world, rank):
 # ---- supplementary measurements (rank 0) ------------------------------------------
 
 def barrier_spin(pk, w, sweeps, **opts):
-    """Per-CTA time spent waiting in the grid barrier over one persistent run
-    (%globaltimer around each wait, PK_FLAG_PROFILE_BARRIER)."""
+    """Per-CTA time spent waiting between passes over one persistent run
+    (%globaltimer around each wait, PK_FLAG_PROFILE_BARRIER): at the grid
+    barrier, or for the pass counters of the CTAs a pass reads from."""
     flags = opts.pop("flags", pk.PK_FLAG_ALTERNATE_DIRECTION) | pk.PK_FLAG_PROFILE_BARRIER
     ctx = pk.pk_create(w["nx"], w["ny"], w["u0"], w["f"], pk.pk_options_default(flags=flags, **opts))
     try:
@@ -328,13 +329,13 @@ def barrier_spin(pk, w, sweeps, **opts):
         waits = pk.pk_barrier_wait_ns(ctx).astype(np.float64)
     finally:
         pk.pk_destroy(ctx)
-    store_passes, check_only = passes_of(info, sweeps, 0.0, 0)
-    barriers = store_passes + check_only
+    passes = info["passes"]
     run_ns = info["device_us"] * 1e3
     return {"kernel": shape_label(info, w["f"] is not None), "grid": info["grid"],
-            "barriers": barriers, "run_us": info["device_us"],
-            "wait_us_per_barrier_mean": float(waits.mean()) / barriers / 1e3,
-            "wait_us_per_barrier_max_cta": float(waits.max()) / barriers / 1e3,
+            "pass_order": "pass counters" if info["pass_counters"] else "grid barrier",
+            "passes": passes, "barriers": info["barriers"], "run_us": info["device_us"],
+            "wait_us_per_pass_mean": float(waits.mean()) / passes / 1e3,
+            "wait_us_per_pass_max_cta": float(waits.max()) / passes / 1e3,
             "wait_fraction_of_run_mean": float(waits.mean()) / run_ns}
 
 
@@ -481,7 +482,7 @@ def latency_extras(pk):
     w = make_workload(DEFAULT_WORKLOAD)
     tb = {}
     for name, cfg in (("one_sweep_per_pass", 3), ("two_sweeps_per_pass", 8),
-                      ("three_sweeps_per_pass", 11)):
+                      ("three_sweeps_per_pass", 10)):
         ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(stream_config=cfg))
         try:
             for _ in range(2):
@@ -497,6 +498,26 @@ def latency_extras(pk):
     tb["speedup_two"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["two_sweeps_per_pass"]["us_per_sweep"]
     tb["speedup_three"] = tb["one_sweep_per_pass"]["us_per_sweep"] / tb["three_sweeps_per_pass"]["us_per_sweep"]
     out["temporal_blocking_16384_100sweeps"] = tb
+    # Pass counters against a grid barrier after every pass (the same bits):
+    # the default three-sweep shape, and the 8-deep-ring shape that was the
+    # default with the barrier
+    pc = {}
+    for label, cfg in (("ring16", 10), ("ring8", 11)):
+        for mode, flags in (("pass_counters", pk.PK_FLAG_ALTERNATE_DIRECTION),
+                            ("barrier_every_pass",
+                             pk.PK_FLAG_ALTERNATE_DIRECTION | pk.PK_FLAG_BARRIER_EVERY_PASS)):
+            ctx = pk.pk_create(16384, 16384, w["u0"], None,
+                               pk.pk_options_default(stream_config=cfg, flags=flags))
+            try:
+                for _ in range(2):
+                    pk.pk_run_sweeps(ctx, 100)
+                runs = [pk.pk_run_sweeps(ctx, 100) for _ in range(5)]
+                pc["%s_%s" % (label, mode)] = {
+                    "stream_config": cfg, "us_per_sweep": statistics.median(r["device_us"] / 100 for r in runs),
+                    "barriers": runs[0]["barriers"], "passes": runs[0]["passes"]}
+            finally:
+                pk.pk_destroy(ctx)
+    out["pass_counters_laplace_16384_100sweeps"] = pc
     # Barrier spin: the headline kernel (one barrier per pass) and
     # the barrier-per-sweep DIRECT kernel on the L2-resident 512^2 grid.
     out["barrier_spin"] = {
@@ -670,6 +691,7 @@ def main():
         "config": {"workload": args.workload, "nx": nx, "ny": ny, "sweeps_per_step": sweeps,
                    "variant": {1: "direct", 2: "stream", 3: "local"}[run_info["variant"]],
                    "stream_config": run_info["stream_config"],
+                   "pass_order": "pass counters" if run_info["pass_counters"] else "grid barrier",
                    "grid": run_info["grid"], "l2": "inputs larger than L2 (2 x field > 129 MB)"
                    if 2 * 4 * cells > 129e6 else "L2-resident",
                    "parallelism": "replicas" if world > 1 else "single-gpu"},

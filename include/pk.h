@@ -80,6 +80,9 @@ extern "C" {
                                             check instead of taking it in its stage 2 or 3 (the
                                             same bits; passes of 3, 3, 3, 1 per check interval of
                                             10 instead of 3 1/3) */
+#define PK_FLAG_BARRIER_EVERY_PASS 0x20u /* persistent STREAM runs: every pass ends at the grid
+                                            barrier, also where pass counters would order it
+                                            (the same bits) */
 
 /* ---- grid barrier constructions ([P2] "The barrier is a counter and a
  * generation") -------------------------------------------------------------- */
@@ -123,6 +126,13 @@ typedef struct {
     int32_t straddle;     /* 1 when the run took the three-sweep kernel whose passes run past
                              residual checks (a check inside a pass is taken in its stage 2
                              or 3), else 0 */
+    int32_t pass_counters; /* 1 when the persistent STREAM kernel ordered its passes without a
+                              residual check by per-CTA pass counters: each CTA publishes the
+                              passes it has done and starts the next once the CTAs whose rows
+                              it reads (pk_stream_pass_deps) have done as many; else 0 */
+    int32_t barriers;     /* grid barriers the persistent DIRECT and STREAM kernels crossed
+                             (one per pass, or one per pass with a residual check when
+                             pass_counters is 1); 0 elsewhere */
 } pk_run_info;
 
 /* A mailbox task ([P1] "Base implementation": the host writes a task, the
@@ -149,8 +159,11 @@ typedef struct {
     double mailbox_idle_timeout_s;    /* task kernel exits after this long with no task (default 10.0) */
     double host_timeout_s;            /* pk_shutdown deadline (default 10.0) */
     int32_t mailbox_depth;            /* task ring slots, 1..1024 (default 64) */
-    int32_t debug_skip_arrival_cta;   /* fault injection: this CTA leaves at barrier ... (-1 = off) */
-    int32_t debug_skip_arrival_at;    /* ... number debug_skip_arrival_at (0-based) without arriving */
+    int32_t debug_skip_arrival_cta;   /* fault injection: this CTA leaves at grid barrier ... (-1 = off) */
+    int32_t debug_skip_arrival_at;    /* ... number debug_skip_arrival_at (0-based) without arriving;
+                                         in persistent DIRECT and STREAM sweeps, at the end of pass
+                                         number debug_skip_arrival_at, without arriving at the
+                                         barrier or publishing its pass count */
     uint32_t flags;                   /* PK_FLAG_* (default PK_FLAG_ALTERNATE_DIRECTION) */
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
@@ -211,9 +224,14 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
                      void *stream, const pk_options *opt, pk_ctx **out);
 
 /* Persistent path ([P2] "What the barrier buys"; [P4] "grid_barrier"): ONE
- * cooperative launch whose resident grid loops over the domain grid-stride,
- * with a release/acquire generation-counter grid barrier between sweeps.
- * Runs up to n sweeps.  With tol > 0 and check_every > 0 the residual
+ * cooperative launch whose resident grid loops over the domain, with a
+ * release/acquire grid barrier between passes (a pass advances one to three
+ * sweeps).  STREAM runs order the passes that take no residual check by
+ * per-CTA pass counters instead: a CTA starts a pass once the CTAs whose
+ * rows it reads (pk_stream_pass_deps) have finished the previous one; every
+ * check still ends at the grid barrier, behind which all CTAs reach the same
+ * exit decision (PK_FLAG_BARRIER_EVERY_PASS: a barrier after every pass;
+ * the same bits either way).  Runs up to n sweeps.  With tol > 0 and check_every > 0 the residual
  * r = fl32(t - 4C) of iterate k (t as in the update, before the 1/4) is
  * reduced in the kernel when k % check_every == 0 (L2 norm: exact squares
  * summed per thread as a float pair, across threads in fp64, to about 1e-12
@@ -224,7 +242,8 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
  * then +inf, and NaN never passes the exit test.  The current buffer
  * afterwards holds U_{sweeps_done}.  Blocks until done.
  * info may be NULL.  Errors: PK_EINVAL (n < 0), PK_EBUSY (task kernel live),
- * PK_ENORESIDENT, PK_ETIMEDOUT (a barrier wait expired), PK_ECUDA. */
+ * PK_ENORESIDENT, PK_ETIMEDOUT (a barrier or pass-counter wait expired),
+ * PK_ECUDA. */
 int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_info *info);
 
 /* Comparison path ([P2] "When a launch is the better barrier"): the same
@@ -303,6 +322,20 @@ int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *cu
  * kernel.  Any output may be NULL. */
 int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max);
 
+/* The CTAs whose pass counters CTA `cta` of a persistent STREAM kernel
+ * waits on before a pass (pk_run_info.pass_counters): the owners of the
+ * rows within D rows of its own (D = the shape's sweeps per pass) in its
+ * strip and in the strips on either side, the (strip, row) pairs of an
+ * nx x ny field being dealt out to `grid` CTAs of shape stream_config in
+ * contiguous runs of R*c/grid .. R*(c+1)/grid - 1.  They are also the CTAs
+ * that read `cta`'s rows.  The list is a concatenation of CTA ranges and may
+ * name a CTA twice.  Writes min(length, cap) entries to the HOST array out
+ * (NULL when cap is 0) and returns the length; a run uses pass counters only
+ * when every CTA's list has at most 32 entries.  Host arithmetic only (no
+ * device call).  Errors: PK_EINVAL (sizes, shape, grid or cta out of
+ * range, cap < 0). */
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int grid, int cta, int32_t *out, int cap);
+
 /* Post a task to the mapped-pinned mailbox ([P1] "Base implementation",
  * "Thread synchronization", "Atomics and memory ordering"; [P3] "Device
  * Communication").  Starts the resident task kernel on first use (on a
@@ -358,11 +391,13 @@ const char *pk_last_error(const pk_ctx *ctx);
  * copies the result record to the host and synchronises the stream, so it
  * blocks until the sweeps are done.
  *
- * Scratch (grid-barrier words, residual partials, result record) lives in
- * one file-scope device array of about 66 KB that every GPU loading libpk
- * holds until the process exits; it serves grids of at most 2048 CTAs, and
- * a larger plan is refused with PK_EINVAL.  All calls share that array:
- * each call clears what must start at zero, and calls that overlap on the
+ * Scratch (grid-barrier words, pass counters, residual partials, result
+ * record) lives in one file-scope device array of about 130 KB that every
+ * GPU loading libpk holds until the process exits; it serves grids of at
+ * most 2048 CTAs, and a larger plan is refused with PK_EINVAL.  All calls
+ * share that array: each call clears what must start at zero (the pass
+ * counters need not: every call takes a higher run id), and calls that
+ * overlap on the
  * GPU (concurrent streams or threads on one device) race and must not be
  * made.  The first call on a device looks up the array's device address
  * and sets kernel attributes, so make it before any stream capture.
@@ -387,9 +422,11 @@ int pk_bench_launch_floor(pk_ctx *ctx, int iters, double *us_sync_each, double *
  * launch included.  grid 0 = the persistent sweep grid. */
 int pk_bench_barrier(pk_ctx *ctx, int kind, int grid, int64_t n_barriers, double *us_total);
 
-/* Per-CTA total barrier wait (ns, global timer) of the last pk_run_sweeps
- * made with PK_FLAG_PROFILE_BARRIER; copies min(n, grid) entries to the HOST
- * array per_cta and returns the count, or a negative code. */
+/* Per-CTA total wait (ns, global timer) of the last pk_run_sweeps made with
+ * PK_FLAG_PROFILE_BARRIER: at the grid barrier, plus (STREAM runs with pass
+ * counters) before each pass for the counters it waits on; copies
+ * min(n, grid) entries to the HOST array per_cta and returns the count, or
+ * a negative code. */
 int pk_barrier_wait_ns(pk_ctx *ctx, int64_t *per_cta, int n);
 
 /* Barrier stress ([P2] "Failure modes that only appear at this scale"):

@@ -31,6 +31,7 @@ constexpr int kSiteMailboxIdle = 3;
 constexpr int kSiteTaskBroadcast = 4;
 constexpr int kSiteTaskGather = 5;
 constexpr int kSiteSkipInjected = 6;
+constexpr int kSitePassCounter = 7;
 
 // ---------------------------------------------------------------------------
 // Barrier state: each word on its own 128-byte line so that spinning on the
@@ -43,7 +44,7 @@ struct alignas(128) Line {
 
 struct BarrierState {
     Line count;       // arrivals in the current generation
-    Line generation;  // bumped by the last arriver
+    Line spare;       // unused (the generation barrier keeps its generation in count)
     Line abort_flag;  // set by any CTA that gave up; every spin checks it
     Line error;       // first error code (atomicCAS from 0)
     Line site;        // where it happened
@@ -115,6 +116,14 @@ __device__ __forceinline__ void st_relaxed_gpu_v2_u64(unsigned long long *p, uns
                                                       unsigned long long b) {
     asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b)
                  : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long *p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu_u64(unsigned long long *p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ void fence_acq_rel_sys() {
     asm volatile("fence.acq_rel.sys;" ::: "memory");

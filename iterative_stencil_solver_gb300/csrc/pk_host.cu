@@ -94,6 +94,8 @@ struct pk_ctx {
     unsigned long long *halo = nullptr;     // LOCAL: tagged halo words
     int local_rows = 0;                     // LOCAL: most rows per CTA
     unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
+    unsigned long long *pass_done = nullptr; // STREAM pass counters (4 words per CTA, part_cap CTAs)
+    std::map<std::pair<int, int>, bool> counters_fit;  // (shape, grid) -> every list fits
     int spin_valid = 0;                     // entries written by the last profiled run
     unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
     int rb_grid = 0;                        // red-black persistent grid (0 = not planned)
@@ -251,13 +253,19 @@ int ensure_partials(pk_ctx *ctx, int grid) {
         PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
         cudaFree(ctx->partials);
         cudaFree(ctx->spin_ns);
+        cudaFree(ctx->pass_done);
         ctx->partials = nullptr;
         ctx->spin_ns = nullptr;
+        ctx->pass_done = nullptr;
         ctx->part_cap = 0;
         ctx->spin_valid = 0;
     }
     PK_TRY(ctx, cudaMalloc(&ctx->partials, sizeof(Partial) * 2 * (size_t)grid));
     PK_TRY(ctx, cudaMalloc(&ctx->spin_ns, sizeof(unsigned long long) * (size_t)grid));
+    // Pass counters start at zero, below every run's (run_id << 32) targets.
+    const size_t pd_bytes = 4 * sizeof(unsigned long long) * (size_t)grid;
+    PK_TRY(ctx, cudaMalloc(&ctx->pass_done, pd_bytes));
+    PK_TRY(ctx, cudaMemset(ctx->pass_done, 0, pd_bytes));
     ctx->part_cap = grid;
     return PK_OK;
 }
@@ -547,6 +555,8 @@ SweepParams base_params(pk_ctx *ctx) {
     p.local_pitch = local_pitch(ctx->nx);
     p.one_sweep = (ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS) ? 1 : 0;
     p.local_threads = ctx->local_threads;
+    p.pass_done = ctx->pass_done;
+    p.pass_counters = 0;  // set per run by choose_persistent's answer
     return p;
 }
 
@@ -618,6 +628,8 @@ void release(pk_ctx *ctx) {
     cudaFree(ctx->g);
     cudaFree(ctx->scratch);
     cudaFree(ctx->partials);
+    cudaFree(ctx->spin_ns);
+    cudaFree(ctx->pass_done);
     cudaFree(ctx->halo);
     cudaFree(ctx->stress_lines);
     cudaFree(ctx->stress_out);
@@ -658,10 +670,13 @@ double elapsed_us(pk_ctx *ctx) {
 
 void fill_info(pk_ctx *ctx, pk_run_info *info, long long sweeps, double res0, double res_last,
                float rmax, int n_checks, int status, int grid, int variant = 0, int shape = -2,
-               int depth = 1, int passes = 0, bool straddle = false) {
+               int depth = 1, int passes = 0, bool straddle = false, bool counters = false,
+               int barriers = 0) {
     if (!info) return;
     info->passes = passes;
     info->straddle = straddle ? 1 : 0;
+    info->pass_counters = counters ? 1 : 0;
+    info->barriers = barriers;
     info->sweeps_done = sweeps;
     info->res0 = res0;
     info->res_last = res_last;
@@ -703,8 +718,14 @@ int task_finish(pk_ctx *ctx) {
 // pay off whenever a run has two or more: the kernels shorten a pass where
 // the end would fall inside it, and a three-sweep pass runs past a residual
 // check (straddle) where a pass of fewer sweeps stops at it.
-void choose_persistent(const pk_ctx *ctx, int64_t n, float tol, int check_every, int *kernel_out,
-                       int *shape_out, int *grid_out, int *depth_out, bool *straddle_out) {
+//
+// Pass counters (persistent STREAM kernels): passes without a residual check
+// wait only for the CTAs whose rows they read, unless
+// PK_FLAG_BARRIER_EVERY_PASS asks for the barrier or some CTA's list is too
+// long for the producer warp's lanes.
+void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *kernel_out,
+                       int *shape_out, int *grid_out, int *depth_out, bool *straddle_out,
+                       bool *counters_out) {
     const bool multi_ok = n >= 2 && !(ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS);
     int kernel = ctx->variant, shape = ctx->stream_cfg, grid = ctx->grid, depth = 1;
     if (ctx->stream_cfg2 >= 0 && multi_ok) {
@@ -723,6 +744,15 @@ void choose_persistent(const pk_ctx *ctx, int64_t n, float tol, int check_every,
     const bool straddle = kernel == kVariantStream && depth == 3 && tol > 0.f && check_every > 0 &&
                           ctx->grid_straddle > 0 && !(ctx->opt.flags & PK_FLAG_CHECKS_END_PASSES);
     if (straddle) grid = ctx->grid_straddle;
+    bool counters = false;
+    if (kernel == kVariantStream && !(ctx->opt.flags & PK_FLAG_BARRIER_EVERY_PASS)) {
+        const auto key = std::make_pair(shape, grid);
+        auto it = ctx->counters_fit.find(key);
+        if (it == ctx->counters_fit.end())
+            it = ctx->counters_fit.emplace(key, stream_counters_fit(ctx->nx, ctx->ny, shape, grid)).first;
+        counters = it->second;
+    }
+    *counters_out = counters;
     *kernel_out = kernel;
     *shape_out = shape;
     *grid_out = grid;
@@ -871,8 +901,9 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     if (ctx->variant == kVariantLocal)  // tags of an earlier run must not match
         PK_TRY(ctx, cudaMemsetAsync(ctx->halo, 0, local_halo_bytes(ctx), ctx->stream));
     int kernel, shape, grid, depth;
-    bool straddle;
-    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle);
+    bool straddle, counters;
+    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
+    p.pass_counters = counters ? 1 : 0;
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream, straddle);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
@@ -884,7 +915,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     if (rc != PK_OK) {
         ctx->sweep_bar_base = 0;  // bar_status zeroed the barrier words
         fill_info(ctx, info, 0, 0.0, 0.0, 0.f, 0, rc, grid, kernel == kVariantStream ? kernel : 0,
-                  shape, depth);
+                  shape, depth, 0, straddle, counters);
         return rc;
     }
     if (ctx->h_info->run_id != p.run_id)
@@ -892,9 +923,11 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     ctx->sweep_bar_base = ctx->h_info->bar_count_end;
     if (p.profile) ctx->spin_valid = grid;
     ctx->cur = ctx->h_info->cur;
+    const bool counts_barriers = kernel == kVariantStream || kernel == kVariantDirect;
     fill_info(ctx, info, ctx->h_info->sweeps_done, ctx->h_info->res0, ctx->h_info->res_last,
               ctx->h_info->rmax_last, ctx->h_info->n_checks, PK_OK, grid,
-              kernel == kVariantStream ? kernel : 0, shape, depth, ctx->h_info->passes, straddle);
+              kernel == kVariantStream ? kernel : 0, shape, depth, ctx->h_info->passes, straddle,
+              counters, counts_barriers ? ctx->h_info->barriers : 0);
     return PK_OK;
 }
 
@@ -953,8 +986,8 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
     int rc = ensure_batch(ctx);
     if (rc != PK_OK) return rc;
     int kernel, shape, grid, depth;
-    bool straddle;
-    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle);
+    bool straddle, counters;
+    choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
     const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
     const size_t dpitch = sizeof(float) * (size_t)ctx->pitch;
     const size_t rows = (size_t)(ctx->ny + 2);
@@ -997,6 +1030,7 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
         p.check_every = check_every;
         p.bar_base = 0;
         p.profile = 0;
+        p.pass_counters = counters ? 1 : 0;
         run_ids[q] = p.run_id;
         if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t0[q], sc);
         if (e == cudaSuccess) e = launch_persistent(kernel, ctx->poisson, shape, grid, p, sc, straddle);
@@ -1059,6 +1093,8 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
             inf.sweeps_per_pass = depth;
             inf.passes = d.passes;
             inf.straddle = straddle ? 1 : 0;
+            inf.pass_counters = counters ? 1 : 0;
+            inf.barriers = kernel == kVariantStream || kernel == kVariantDirect ? d.barriers : 0;
             float ms = 0.f;
             inf.device_us = cudaEventElapsedTime(&ms, ctx->ev_t0[q], ctx->ev_t1[q]) == cudaSuccess
                                 ? (double)ms * 1000.0 : -1.0;
@@ -1434,6 +1470,18 @@ int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_
     if (task_grid) *task_grid = ctx->task_grid;
     if (coop_max) *coop_max = ctx->coop_max;
     return PK_OK;
+}
+
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int grid, int cta, int32_t *out, int cap) {
+    if (nx <= 0 || ny <= 0 || stream_config < 0 || stream_config >= kNumStreamConfigs || grid <= 0 ||
+        cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out))
+        return PK_EINVAL;
+    const int tw = stream_tw(stream_config);
+    const int strips = (nx + tw - 1) / tw;
+    const int halo = stream_depth(stream_config);
+    const int n = stream_pass_ndeps(strips, ny, grid, cta, halo);
+    for (int i = 0; i < n && i < cap; ++i) out[i] = stream_pass_dep(strips, ny, grid, cta, halo, i);
+    return n;
 }
 
 // ---- mailbox ----------------------------------------------------------------

@@ -68,7 +68,76 @@ struct SweepParams {
     int local_pitch;        // floats per tile row in shared memory
     int one_sweep;          // 1: every pass advances one sweep (no temporal blocking)
     int local_threads;      // LOCAL: threads per CTA
+    // STREAM: pass counters instead of a grid barrier between passes that
+    // reduce no residual.  pass_done[4 * b] (a 32-byte sector per CTA) holds
+    // CTA b's run_id in the high half and its passes completed in the low
+    // half; before a pass a CTA waits for the CTAs whose rows it reads.
+    unsigned long long *pass_done;
+    int pass_counters;      // 1: use them (the plan checked every CTA's neighbour set fits)
 };
+
+// The CTAs whose rows CTA b of a STREAM pass reads, which are also the CTAs
+// that read b's rows (the relation is symmetric): the owners of the rows
+// within `halo` rows of b's rows, in b's strip and in the strips on either
+// side (a row segment carries four columns of each neighbouring strip).
+// Rows are dealt out as the STREAM kernel deals them: the R = strips * ny
+// (strip, row) pairs in strip-major order, CTA c taking [R c / G,
+// R (c + 1) / G).  The set is walked as a list of CTA ranges, one per
+// (segment of b's run, strip), b itself left out; a CTA can appear in two
+// ranges, and waiting on it twice is harmless, so the list is not reduced.
+__host__ __device__ inline long long stream_pair_owner(long long pos, long long R, int G) {
+    long long c = pos * G / R;
+    while (c + 1 < G && R * (c + 1) / G <= pos) ++c;
+    while (c > 0 && R * c / G > pos) --c;
+    return c;
+}
+// Calls visit(first, last) for each range; stops early when visit returns
+// false.
+template <class Visit>
+__host__ __device__ inline void stream_pass_dep_ranges(int strips, int ny, int G, int b, int halo,
+                                                       Visit &&visit) {
+    const long long R = (long long)strips * ny;
+    const long long L0 = R * b / G, L1 = R * (b + 1) / G;
+    for (long long pos = L0; pos < L1;) {
+        const int s = (int)(pos / ny);
+        const long long seg_end = ((long long)s + 1) * ny < L1 ? ((long long)s + 1) * ny : L1;
+        const int r0 = (int)(pos - (long long)s * ny), r1 = (int)(seg_end - 1 - (long long)s * ny);
+        const int lo = r0 - halo < 0 ? 0 : r0 - halo;
+        const int hi = r1 + halo > ny - 1 ? ny - 1 : r1 + halo;
+        for (int ss = s - 1; ss <= s + 1; ++ss) {
+            if (ss < 0 || ss >= strips) continue;
+            if (!visit(stream_pair_owner((long long)ss * ny + lo, R, G),
+                       stream_pair_owner((long long)ss * ny + hi, R, G)))
+                return;
+        }
+        pos = seg_end;
+    }
+}
+// Length of CTA b's list.
+__host__ __device__ inline int stream_pass_ndeps(int strips, int ny, int G, int b, int halo) {
+    int n = 0;
+    stream_pass_dep_ranges(strips, ny, G, b, halo, [&](long long c0, long long c1) {
+        n += (int)(c1 - c0 + 1) - (c0 <= b && b <= c1 ? 1 : 0);
+        return true;
+    });
+    return n;
+}
+// Entry i of CTA b's list, or -1 past its end.
+__host__ __device__ inline int stream_pass_dep(int strips, int ny, int G, int b, int halo, int i) {
+    int found = -1;
+    stream_pass_dep_ranges(strips, ny, G, b, halo, [&](long long c0, long long c1) {
+        for (long long c = c0; c <= c1; ++c) {
+            if (c == b) continue;
+            if (i-- == 0) {
+                found = (int)c;
+                return false;
+            }
+        }
+        return true;
+    });
+    return found;
+}
+constexpr int kMaxPassDeps = 32;  // one producer lane polls each entry
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
 struct alignas(128) MboxWord {
@@ -154,6 +223,15 @@ constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kStreamConfigs[cfg].consumers; }
 inline int stream_threads(int cfg) { return kStreamConfigs[cfg].consumers + 32; }
 inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
+// Whether every CTA of a persistent STREAM grid of shape cfg has at most
+// kMaxPassDeps entries in its pass-counter list (one producer lane each).
+inline bool stream_counters_fit(int nx, int ny, int cfg, int grid) {
+    const int tw = stream_tw(cfg);
+    const int strips = (nx + tw - 1) / tw;
+    for (int b = 0; b < grid; ++b)
+        if (stream_pass_ndeps(strips, ny, grid, b, stream_depth(cfg)) > kMaxPassDeps) return false;
+    return true;
+}
 
 // A ring slot: the U row segment (4 halo floats each side) and, for
 // Poisson, the g row segment with a 4-float margin each side.  A shape of
@@ -171,19 +249,21 @@ inline size_t stream_smem_bytes(int cfg, bool poisson) {
     return 256 + (size_t)kStreamConfigs[cfg].stages * slot + qrows;
 }
 
-// Multi-sweep shape for persistent runs, from measurements on GB300 (100
-// sweeps, us/sweep).  Both take three sweeps per pass.  Laplace: {1 float4/
-// thread, 224 consumers, 2 CTAs/SM} with an 8-deep ring above 8192 columns
-// (16384^2: 121.5 against 123.4 with a 16-deep ring and 128.2 for one CTA of
-// 256 consumers per SM), the 16-deep ring up to 8192 (8192^2: 33.8 against
-// 34.3; 4096^2: 9.56 against 10.0).  Poisson, whose ring slots also carry the
-// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 170.3 at 16384^2,
-// 43.0 at 8192^2 and 12.8 at 4096^2 (the best two-sweep shape: 249.1 and
-// 17.0 at 16384^2 and 4096^2).
-inline int default_multi_sweep_shape(bool poisson, int nx) {
-    if (poisson) return 12;
-    return nx > 8192 ? 11 : 10;
-}
+// Multi-sweep shape for persistent runs, from measurements on GB300 with
+// pass counters between passes (us/sweep; 100 sweeps at 8192^2 and above,
+// 300 below).  Both take three sweeps per pass.  Laplace: {1 float4/thread,
+// 16-deep ring, 224 consumers, 2 CTAs/SM} -- 16384^2: 113.3 against 122.8
+// with an 8-deep ring and 126.6 for one CTA of 256 consumers per SM; 8192^2:
+// 31.6 / 34.4 / 33.0; 4096^2: 9.59 / 9.72 / 9.92; 1536^2 to 6144^2 the best
+// or within 0.5% of it, except 2048^2 (4.59 against 3.76 for the 1024-wide
+// strips, which divide it exactly).  With a grid barrier after every pass
+// the two rings ran within 1% of each other at 16384^2 (120.9 and 122.2):
+// the counters take 7% off the 16-deep ring's time, whose CTAs waited
+// about 12% of a pass at the barrier.  Poisson, whose ring slots also carry the
+// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 169.0 at 16384^2,
+// 43.0 at 8192^2, 12.4 at 4096^2 and 4.33 at 2048^2 (the two-CTA shapes
+// 213.2, 58.3, 16.3 and 6.2).
+inline int default_multi_sweep_shape(bool poisson, int) { return poisson ? 12 : 10; }
 
 // Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).
 void set_global_error(const char *msg);
@@ -276,6 +356,7 @@ struct RunRecord {
     int error;
     unsigned site, bad_cta;
     int passes;
+    int barriers;
 };
 cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
                                   cudaStream_t s);

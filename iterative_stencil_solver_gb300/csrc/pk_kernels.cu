@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_direct(SweepParam
     persistent_loop<1>(p, [&](const float *src, float *dst, int cs, bool store, int,
                               long long, double &s2, float &rmax) {
         pass_direct_any<POISSON>(p, src, dst, cs != 0, store, first, stride, s2, rmax);
-    });
+    }, [](unsigned) { return true; });  // every DIRECT pass ends at the grid barrier
 }
 
 // ===========================================================================
@@ -889,6 +889,7 @@ __global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar
         out->run_id = vi->run_id;
         out->bar_count_end = vi->bar_count_end;
         out->passes = vi->passes;
+        out->barriers = vi->barriers;
         volatile const BarrierState *vb = bar;
         out->error = (int)vb->error.v;
         out->site = vb->site.v;

@@ -11,9 +11,10 @@
 // returns.
 //
 // The persistent kernel needs scratch memory besides its inputs and outputs:
-// the grid-barrier words, the per-CTA residual partials and the result
-// record.  Here that scratch is one file-scope __device__ array of fixed
-// size, which every GPU that loads libpk holds until the process exits.
+// the grid-barrier words, the per-CTA pass counters and residual partials,
+// and the result record.  Here that scratch is one file-scope __device__
+// array of fixed size, which every GPU that loads libpk holds until the
+// process exits.
 #include <cstddef>
 #include <cstring>
 #include <mutex>
@@ -35,9 +36,12 @@ struct NoAllocScratch {
     BarrierState bar;
     DeviceInfo info;
     alignas(16) Partial partials[2 * kNoAllocMaxGrid];
+    // STREAM pass counters (4 words per CTA).  Never cleared: each call
+    // takes a run id above every earlier one on the device (g_run_id).
+    alignas(32) unsigned long long pass_done[4 * kNoAllocMaxGrid];
 };
 
-// The scratch itself (about 66 KB per device).  In host code the name is a
+// The scratch itself (about 130 KB per device).  In host code the name is a
 // host-side stand-in, not a device address: only the address returned by
 // cudaGetSymbolAddress may be given to a kernel.
 __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
@@ -46,6 +50,7 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 NoAllocScratch *g_scratch_ptr[kMaxDevices];   // device address, per device
 bool g_ready[kMaxDevices];
+int g_run_id[kMaxDevices];   // the last call's run id (under g_setup_mutex)
 int g_sms[kMaxDevices];
 long long g_l2[kMaxDevices];
 
@@ -163,6 +168,14 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     e = cudaMemsetAsync(sc, 0, offsetof(NoAllocScratch, partials), s);
     if (e != cudaSuccess) return fail(PK_ECUDA, "cudaMemsetAsync(scratch)", e);
 
+    // pass counters as pk_run_sweeps uses them
+    const bool counters = variant == kVariantStream && stream_counters_fit(nx, ny, cfg, (int)grid);
+    int run_id;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        run_id = ++g_run_id[dev];
+    }
+
     SweepParams p;
     std::memset(&p, 0, sizeof(p));
     p.u[0] = u_a;
@@ -183,7 +196,9 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     p.timeout_ns = 2000000000ull;
     p.skip_cta = -1;
     p.alt_dir = 1;
-    p.run_id = 1;
+    p.run_id = run_id;
+    p.pass_done = sc->pass_done;
+    p.pass_counters = counters ? 1 : 0;
     p.barrier_kind = (int)kBarrierCounter;
     p.bar_base = 0;
     e = launch_persistent(variant, poisson, cfg, (int)grid, p, s, straddle);
@@ -195,7 +210,7 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     if (e == cudaSuccess) e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) return fail(PK_ECUDA, "reading the result", e);
     if (hb.error.v != 0u) return fail((int)hb.error.v, "pk_run_sweeps_noalloc: a device wait expired");
-    if (hi.run_id != 1) return fail(PK_EDEVICE, "pk_run_sweeps_noalloc: kernel did not report");
+    if (hi.run_id != run_id) return fail(PK_EDEVICE, "pk_run_sweeps_noalloc: kernel did not report");
     if (info) {
         info->sweeps_done = hi.sweeps_done;
         info->res0 = hi.res0;
@@ -211,6 +226,8 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
         info->device_us = 0.0;
         info->passes = hi.passes;
         info->straddle = straddle ? 1 : 0;
+        info->pass_counters = counters ? 1 : 0;
+        info->barriers = hi.barriers;
     }
     return PK_OK;
 }

@@ -939,28 +939,75 @@ __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const floa
     }
 }
 
+// Entry i of this CTA's pass-counter list, out of line: the lookup runs
+// once per launch, and inlined its 64-bit divisions cost the row windows
+// registers.
+__device__ __noinline__ int stream_pass_dep_of(const SweepParams &p, int tw, int depth, int i) {
+    return stream_pass_dep((p.nx + tw - 1) / tw, p.ny, (int)gridDim.x, (int)blockIdx.x, depth, i);
+}
+
 // ===========================================================================
 // The persistent and per-launch STREAM kernels.  STRADDLE: the persistent
 // loop lets three-sweep passes run past residual checks (a separate
 // instantiation, taken for runs with checks, so that the kernel of runs
 // without them keeps its register budget).
+//
+// Pass counters: producer lane i waits on entry i of this CTA's neighbour
+// list (stream_pass_dep: the CTAs whose rows the pass reads, which are the
+// CTAs that read this CTA's rows), or on nothing.  The lanes find their
+// entries after the first pass's row segments are issued, while the
+// consumers still work, and keep them in shared memory.
 template <class C, bool POISSON, bool STRADDLE>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int s_dep[32];
+    __shared__ int s_wait_ok;
+    __shared__ unsigned long long s_wait_ns;
     StreamState st = stream_setup<C>(smem);
+    if (threadIdx.x >= C::kCons) {
+        s_dep[threadIdx.x & 31u] = -2;  // not looked up yet
+        if (threadIdx.x == C::kCons) s_wait_ns = 0ull;
+    }
     persistent_loop<C::kDepth, STRADDLE>(p, [&](const float *src, float *dst, int cs, bool store,
                                                 int dp, long long k, double &s2, float &rmax) {
         const int dir = (p.alt_dir && (k & 1)) ? -1 : 1;
-        // After the barrier: this producer's TMA reads must see the
-        // generic-proxy stores the whole grid made in the previous sweep.
-        // The issuing thread acquires at gpu scope itself, then fences the
-        // generic proxy against the async proxy.
+        // After the barrier or the pass-counter wait: this producer's TMA
+        // reads must see the generic-proxy stores the grid made in the
+        // previous sweep.  The issuing thread acquires at gpu scope itself,
+        // then fences the generic proxy against the async proxy.
         if (threadIdx.x == C::kCons) {
             fence_acq_rel_gpu();
             fence_proxy_async_global();
         }
         pass_stream_any<C, POISSON, STRADDLE>(p, src, dst, dir, cs, store, dp, st, s2, rmax);
+        if (threadIdx.x >= C::kCons && p.pass_counters && s_dep[threadIdx.x & 31u] == -2)
+            s_dep[threadIdx.x & 31u] = stream_pass_dep_of(p, C::TW, C::kDepth, (int)(threadIdx.x & 31u));
+    }, [&](unsigned need) -> bool {
+        if (threadIdx.x >= C::kCons) {
+            const unsigned lane = threadIdx.x & 31u;
+            const uint64_t t0 = p.profile ? globaltimer_ns() : 0ull;
+            const int dep = s_dep[lane];
+            bool ok = true;
+            if (dep >= 0) {
+                const unsigned long long *w = p.pass_done + 4 * (size_t)dep;
+                const unsigned long long target = ((unsigned long long)(unsigned)p.run_id << 32) | need;
+                ok = bounded_spin(p.bar, p.timeout_ns, kSitePassCounter,
+                                  [&] { return ld_relaxed_gpu_u64(w) >= target; });
+                fence_acq_rel_gpu();  // each lane acquires what it observed
+            }
+            ok = __all_sync(0xffffffffu, ok);
+            __syncwarp();
+            if (lane == 0u) {
+                s_wait_ok = ok ? 1 : 0;
+                if (p.profile) s_wait_ns += globaltimer_ns() - t0;
+            }
+        }
+        __syncthreads();
+        return s_wait_ok != 0;
     });
+    // (a normal end: the loop has stored the barrier waits; the counter
+    // waits were made visible to thread 0 by the last wait's block barrier)
+    if (p.profile && threadIdx.x == 0 && p.pass_counters) p.spin_ns[blockIdx.x] += s_wait_ns;
 }
 
 template <class C, bool POISSON>

@@ -1,6 +1,7 @@
 // pk_sweep.cuh -- device code shared by libpk's sweep kernels: the
-// persistent sweep loop (grid barrier between passes, residual partials
-// reduced behind it) and the per-launch residual partial.
+// persistent sweep loop (a grid barrier or per-CTA pass counters between
+// passes, residual partials reduced behind the barrier) and the per-launch
+// residual partial.
 //
 // Sources (page title -- section):
 //   "Grid-Wide Barriers and Persistent Work Queues" -- "What the barrier
@@ -55,8 +56,23 @@ __device__ __forceinline__ BarrierCtl make_ctl(const SweepParams &p) {
 // and stop there.  Without STRADDLE a pass always ends at the check, so a
 // check every 10 sweeps costs four passes of 3, 3, 3 and 1 sweeps instead
 // of three and a third.
-template <int MAXD, bool STRADDLE = false, class PassFn>
-__device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass) {
+//
+// Pass counters (p.pass_counters): a pass that reduces no residual needs no
+// grid-wide agreement, only that the CTAs whose rows it reads have written
+// them and that the CTAs which read its target rows in the previous pass
+// have done so.  Such a pass ends with each CTA publishing its count of
+// passes done (a release store, thread 0, after the block barrier), and the
+// next pass starts once wait(count) -- called by every thread -- has seen
+// those CTAs reach the same count.  No CTA then runs more than one pass
+// ahead of a neighbour, and the passes' results are the same bits.  Passes
+// with a residual check still end at the grid barrier, behind which the
+// partials are reduced.  wait returns false when the grid is aborting.
+//
+// Fault injection (p.skip_cta >= 0): that CTA leaves at the end of pass
+// p.skip_at (0-based) without arriving at the barrier or publishing its
+// count; the others time out.
+template <int MAXD, bool STRADDLE = false, class PassFn, class WaitFn>
+__device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&pass, WaitFn &&wait) {
     // Loop state that only thread 0 uses (the barrier's bookkeeping) or that
     // changes only on check sweeps (the residual history) lives in shared
     // memory: the pass keeps the registers, which are what bounds the
@@ -66,6 +82,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     __shared__ float s_rmax_last;
     if (threadIdx.x == 0) {
         s_ctl = make_ctl(p);
+        s_ctl.skip_cta = -1;  // the loop injects the fault itself (see above)
         s_res0 = s_res_last = 0.0;
         s_rmax_last = 0.f;
     }
@@ -79,6 +96,8 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     // the compiler inlines it and the row windows stay in registers).
     bool redo = false;
     long long k_exit = 0;
+    unsigned passes = 0;       // passes this CTA has completed
+    bool counted = false;      // the last pass ended at the pass counters
     for (;;) {
         int dp = 1, cs = 0;
         bool store = true;
@@ -106,13 +125,28 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
                 dp = m < MAXD ? (int)m : MAXD;
             }
         }
+        if (counted && !wait(passes)) return;  // aborting: the host reads the error
         double s2 = 0.0;
         float rmax = 0.f;
         pass(p.u[cur], p.u[cur ^ 1], cs, store, dp, k, s2, rmax);
+        ++passes;
         if (redo) {  // no barrier: the kernel ends here
             cur ^= 1;
             k = k_exit;
             break;
+        }
+        if ((int)blockIdx.x == p.skip_cta && (int)passes - 1 == p.skip_at) return;
+        counted = p.pass_counters && !cs;
+        if (counted) {
+            // every thread's stores of this pass (fenced to the async proxy
+            // by the pass itself) are ordered before the count's release
+            __syncthreads();
+            if (threadIdx.x == 0)
+                st_release_gpu_u64(p.pass_done + 4 * (size_t)blockIdx.x,
+                                   ((unsigned long long)(unsigned)p.run_id << 32) | passes);
+            cur ^= 1;
+            k += dp;
+            continue;
         }
         Partial *parts = p.partials + (size_t)(n_checks & 1) * (size_t)p.max_grid;
         if (cs) {
@@ -166,7 +200,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         d->cur = cur;
         d->task_sweeps = 0;
         d->barriers = s_ctl.index;
-        d->passes = s_ctl.index + (redo ? 1 : 0);  // every other pass ends at a barrier
+        d->passes = (int)passes;
         d->bar_count_end = p.bar_base + (unsigned)s_ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;

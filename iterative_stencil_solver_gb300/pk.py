@@ -38,6 +38,7 @@ PK_FLAG_ALTERNATE_DIRECTION = 0x2
 PK_FLAG_PROFILE_BARRIER = 0x4
 PK_FLAG_ONE_SWEEP_PER_PASS = 0x8
 PK_FLAG_CHECKS_END_PASSES = 0x10
+PK_FLAG_BARRIER_EVERY_PASS = 0x20
 
 PK_BARRIER_GENERATION = 0
 PK_BARRIER_COUNTER = 1
@@ -73,6 +74,8 @@ class pk_run_info(ctypes.Structure):
         ("device_us", ctypes.c_double),
         ("passes", ctypes.c_int32),
         ("straddle", ctypes.c_int32),
+        ("pass_counters", ctypes.c_int32),
+        ("barriers", ctypes.c_int32),
     ]
 
     def as_dict(self):
@@ -147,6 +150,9 @@ _SIGS = {
                                        ctypes.POINTER(ctypes.c_int)]),
     "pk_get_plan": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
+    "pk_stream_pass_deps": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.c_int]),
     "pk_submit_task": (ctypes.c_int, [_VP, ctypes.POINTER(pk_task),
                                       ctypes.POINTER(ctypes.c_uint64)]),
     "pk_poll": (ctypes.c_int, [_VP, ctypes.c_uint64]),
@@ -337,6 +343,17 @@ def pk_get_plan(ctx):
     _check(_lib.pk_get_plan(ctx, ctypes.byref(v), ctypes.byref(g), ctypes.byref(tg),
                             ctypes.byref(cm)), ctx)
     return {"variant": v.value, "grid": g.value, "task_grid": tg.value, "coop_max": cm.value}
+
+
+def pk_stream_pass_deps(nx, ny, stream_config, grid, cta):
+    """The CTAs whose pass counters CTA `cta` of a persistent STREAM grid
+    waits on (host arithmetic; no device needed)."""
+    n = _lib.pk_stream_pass_deps(nx, ny, stream_config, grid, cta, None, 0)
+    if n < 0:
+        raise PkError(n, "pk_stream_pass_deps: bad arguments")
+    out = (ctypes.c_int32 * max(n, 1))()
+    _lib.pk_stream_pass_deps(nx, ny, stream_config, grid, cta, out, n)
+    return list(out[:n])
 
 
 def make_task(kind, n_sweeps=0, a=0.0, x=None, y=None, length=0):

@@ -44,8 +44,8 @@ def test_library_exports_every_declared_symbol(pk):
 
 
 def test_struct_sizes_match_header(pk):
-    # pk_run_info: i64, f64, f64, f32, 7 x i32, f64, 2 x i32 -> 72 bytes with natural alignment.
-    assert ctypes.sizeof(pk.pk_run_info) == 72
+    # pk_run_info: i64, f64, f64, f32, 7 x i32, f64, 4 x i32 -> 80 bytes with natural alignment.
+    assert ctypes.sizeof(pk.pk_run_info) == 80
     assert ctypes.sizeof(pk.pk_task) == 40
     opt = pk.pk_options_default()
     assert opt.struct_size == ctypes.sizeof(pk.pk_options) == 88

@@ -632,6 +632,80 @@ def test_straddled_checks_bit_exact(pk, cfg, nx, ny, poisson):
             assert info["straddle"] == 1
 
 
+# Pass counters: a persistent STREAM pass without a residual check starts
+# once the CTAs whose rows it reads have finished the pass before (the
+# lists are pinned on the CPU in test_pass_deps.py).  Shapes of one, two and
+# three sweeps per pass at the default grids, on fields whose CTAs own one
+# or two rows (so each waits on up to 20 others, across strips) and whose
+# last strip can be one column wide: the same bits as the oracle and as a
+# barrier after every pass, and the grid barrier only behind the checks.
+PASS_COUNTER_CASES = [(3, 3000, 200), (6, 2100, 37), (8, 1030, 300), (10, 1793, 60),
+                      (11, 4500, 90), (12, 4097, 50), (12, 300, 41)]
+
+
+@pytest.mark.parametrize("cfg,nx,ny", PASS_COUNTER_CASES,
+                         ids=["%d-%dx%d" % c for c in PASS_COUNTER_CASES])
+@pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
+def test_pass_counters_bit_exact(pk, cfg, nx, ny, poisson):
+    u0 = inputs.random_field(nx, ny, seed=1100 + cfg + ny)
+    f = inputs.uniform_pm1(1200 + nx, nx * ny).reshape(ny, nx) if poisson else None
+    for n, tol, ce in ((29, 0.0, 0), (31, 1e-30, 7)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        try:
+            got, info = run_pk(pk, u0, f, n, tol, ce, variant=2, stream_config=cfg)
+        except pk.PkError as e:
+            assert e.code == pk.PK_EINVAL and "shared memory" in str(e)
+            return
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+        assert info["pass_counters"] == 1
+        assert info["barriers"] == oinfo.n_checks
+        got2, info2 = run_pk(pk, u0, f, n, tol, ce, variant=2, stream_config=cfg,
+                             flags=pk.PK_FLAG_ALTERNATE_DIRECTION | pk.PK_FLAG_BARRIER_EVERY_PASS)
+        assert_same_bits(got2, want)
+        check_info(info2, oinfo)
+        assert info2["pass_counters"] == 0
+        assert info2["barriers"] == info2["passes"] == info["passes"]
+
+
+def test_pass_counters_off_when_a_list_is_too_long(pk):
+    # 300 CTAs of the two-sweep shape on 111 (strip, row) pairs: a CTA's list
+    # runs through the CTAs that own no rows and one reaches 35 entries, more
+    # than the producer warp's lanes, so the run keeps the barrier
+    nx, ny, cfg, grid = 2100, 37, 6, 300
+    assert max(len(pk.pk_stream_pass_deps(nx, ny, cfg, grid, b)) for b in range(grid)) > 32
+    u0 = inputs.random_field(nx, ny, seed=1300)
+    want, _ = oracle.jacobi_run(u0, n=12)
+    got, info = run_pk(pk, u0, None, 12, variant=2, stream_config=cfg, grid_override=grid)
+    assert info["grid"] == grid and info["pass_counters"] == 0
+    assert_same_bits(got, want)
+
+
+@pytest.mark.parametrize("counters", [True, False], ids=["pass-counters", "barrier"])
+def test_stream_timeout_names_the_wait(pk, counters):
+    """One CTA leaves after its fourth pass without publishing its count (or
+    arriving at the barrier); its neighbours' waits expire and the error
+    names the wait that gave up: site 7 (a pass counter) or 1 (the
+    barrier).  The context stays usable."""
+    nx, ny = 3000, 200
+    u0 = inputs.random_field(nx, ny, seed=41)
+    flags = pk.PK_FLAG_ALTERNATE_DIRECTION | (0 if counters else pk.PK_FLAG_BARRIER_EVERY_PASS)
+    opt = pk.pk_options_default(variant=2, stream_config=3, barrier_timeout_s=0.2, flags=flags,
+                                debug_skip_arrival_cta=5, debug_skip_arrival_at=3)
+    ctx = pk.pk_create(nx, ny, u0, None, opt)
+    try:
+        with pytest.raises(pk.PkError) as e:
+            pk.pk_run_sweeps(ctx, 40)
+        assert e.value.code == pk.PK_ETIMEDOUT
+        assert ("at site %d" % (7 if counters else 1)) in str(e.value)
+    finally:
+        pk.pk_destroy(ctx)
+    want, _ = oracle.jacobi_run(u0, n=9)
+    got, info = run_pk(pk, u0, None, 9, variant=2, stream_config=3, flags=flags)
+    assert_same_bits(got, want)
+    assert info["pass_counters"] == (1 if counters else 0)
+
+
 # An early exit at a check taken in stage 2 or 3: U_c is not in memory when
 # the check ends the run, so the kernel sweeps again from U_k to U_c.  With an
 # interval of 10 the checks at 10, 20, 30, 40 and 50 fall in stages 2, 3, 1,
@@ -725,8 +799,8 @@ DEFAULT_SHAPE_RUNS = [
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    # three sweeps per pass: shape 12 for Poisson; for Laplace 11 above 8192 columns, else 10
-    multi = 12 if poisson else (11 if nx > 8192 else 10)
+    # three sweeps per pass: shape 12 for Poisson, 10 for Laplace
+    multi = 12 if poisson else 10
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
         shape = multi if shape == MULTI else shape
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
