@@ -65,8 +65,8 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "6ad435692fd7622a", "stream_config": 10,
-           "bytes_per_launch": 35.583e9 + 36.491e9}
+TRAFFIC = {"kernel_sha": "f79dbb044f696a0d", "stream_config": 10,
+           "bytes_per_launch": 37.925e9 + 36.675e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
@@ -221,10 +221,24 @@ class ClockSampler:
             self.path = self.fh.name
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
-                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                 "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                 stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            return
+        # wait (up to 5 s) for the sampler's first line, so that it is
+        # running when the timed region starts
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
+        self.offset = 0
+
+    def mark(self):
+        """Start of the timed region: samples written before it are ignored."""
+        if self.proc is not None:
+            self.offset = os.path.getsize(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -243,23 +257,33 @@ class ClockSampler:
     def _summary(self):
         sm, smax, reasons = [], 0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        offset = getattr(self, "offset", 0)
         with open(self.path) as fh:
-            for line in fh:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 9:
-                    continue
-                try:
-                    sm.append(float(parts[1]))
-                    smax = max(smax, float(parts[2]))
-                except ValueError:
-                    continue
-                for name, flag in zip(names, parts[5:9]):
-                    if flag.lower() == "active":
-                        reasons.add(name)
+            before = fh.read(offset).splitlines()
+            lines = fh.read().splitlines()
+        # (a line the mark cut in two has fewer than nine fields on each side)
+        window = "timed region"
+        if not [l for l in lines if len(l.split(",")) >= 9]:
+            # no sample fell inside a short timed region: the last one taken
+            # before it, during the warm-up steps that ran just before
+            lines = [l for l in before if len(l.split(",")) >= 9][-1:]
+            window = "last warm-up sample (timed region shorter than the 50 ms period)"
+        for line in lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = max(smax, float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "window": window}
 
 
 # ---- CPU oracle timing ---------------------------------------------------------
@@ -621,6 +645,10 @@ def main():
                     help="skip the end-to-end measurement (profiling runs)")
     ap.add_argument("--stream-config", type=int, default=-1,
                     help="STREAM shape index (include/pk.h pk_options.stream_config), -1 = default")
+    ap.add_argument("--profile-handoff", action="store_true",
+                    help="only run the task kernel's device-side hand-out (pk_bench_handoff, "
+                         "10,000 made-up tasks) four times and print its cost per task: a "
+                         "small command to profile the task kernel with")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -638,6 +666,17 @@ def main():
     build_ext.build()
     from iterative_stencil_solver_gb300 import pk
 
+    if args.profile_handoff:
+        from iterative_stencil_solver_gb300 import inputs
+        hw = inputs.workload_laplace_random(512, 1)
+        ctx = pk.pk_create(512, 512, hw["u0"], None)
+        try:
+            us = [pk.pk_bench_handoff(ctx, 0, 10000) / 10000 for _ in range(4)]
+            print(json.dumps({"handoff_us_per_task": us, "task_cluster_ctas": pk.pk_get_plan(ctx)["task_grid"]}))
+        finally:
+            pk.pk_destroy(ctx)
+        return
+
     w = make_workload(args.workload)
     nx, ny, sweeps = w["nx"], w["ny"], w["sweeps"]
     cells = nx * ny
@@ -645,12 +684,13 @@ def main():
                        pk.pk_options_default(stream_config=args.stream_config))
     try:
         plan = pk.pk_get_plan(ctx)
+        clocks = ClockSampler(local)
+        clocks.start()  # samples the warm-up too: a short timed region may hold none
         for _ in range(args.warmup):
             pk.pk_run_sweeps(ctx, sweeps, w["tol"], w["check_every"])
-        clocks = ClockSampler(local)
-        clocks.start()
         dist_barrier(world)
         torch.cuda.synchronize()
+        clocks.mark()
         dev_us, updates = [], 0
         t0 = time.perf_counter()
         for _ in range(args.steps):

@@ -82,7 +82,7 @@ extern "C" {
                                             10 instead of 3 1/3) */
 #define PK_FLAG_BARRIER_EVERY_PASS 0x20u /* persistent STREAM runs: every pass ends at the grid
                                             barrier, also where pass counters would order it
-                                            (the same bits) */
+                                            (the same bits; the two-sweep shapes always do) */
 
 /* ---- grid barrier constructions ([P2] "The barrier is a counter and a
  * generation") -------------------------------------------------------------- */
@@ -226,8 +226,9 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
 /* Persistent path ([P2] "What the barrier buys"; [P4] "grid_barrier"): ONE
  * cooperative launch whose resident grid loops over the domain, with a
  * release/acquire grid barrier between passes (a pass advances one to three
- * sweeps).  STREAM runs order the passes that take no residual check by
- * per-CTA pass counters instead: a CTA starts a pass once the CTAs whose
+ * sweeps).  STREAM runs of the one- and three-sweep shapes (every default
+ * plan) order the passes that take no residual check by per-CTA pass
+ * counters instead: a CTA starts a pass once the CTAs whose
  * rows it reads (pk_stream_pass_deps) have finished the previous one; every
  * check still ends at the grid barrier, behind which all CTAs reach the same
  * exit decision (PK_FLAG_BARRIER_EVERY_PASS: a barrier after every pass;
@@ -340,12 +341,14 @@ int pk_stream_pass_deps(int nx, int ny, int stream_config, int grid, int cta, in
  * "Thread synchronization", "Atomics and memory ordering"; [P3] "Device
  * Communication").  Starts the resident task kernel on first use (on a
  * stream of its own, [P3] "Stream concurrency").  The descriptor goes to
- * slot seq % depth (every word tagged with seq), after a release fence; one
- * leader thread polls it, broadcasts it through device memory (a line of
- * words tagged like the slot's), the grid runs it, and the completion
- * sequence is written with a system-scope release only after every CTA has
- * finished ([P1] "Reflections": no early ACK).  A NOP completes as soon as
- * the leader reads it.
+ * slot seq % depth (every word tagged with seq), after a release fence.
+ * The task kernel is one thread-block cluster: one leader thread polls the
+ * slot and hands the task to every CTA of the cluster through distributed
+ * shared memory (a store into each CTA's descriptor and a remote arrive on
+ * its barrier); the CTAs run it, each arrives on the leader CTA's barrier
+ * when done, and the completion sequence is written with a system-scope
+ * release only after all have ([P1] "Reflections": no early ACK).  A NOP
+ * completes as soon as the leader reads it.
  * *seq_out (may be NULL) receives the task's sequence number (1, 2, ...).
  * Errors: PK_EINVAL (bad task), PK_EBUSY (ring full), PK_ESHUTDOWN,
  * PK_ENORESIDENT, PK_ECUDA. */
@@ -391,8 +394,9 @@ const char *pk_last_error(const pk_ctx *ctx);
  * copies the result record to the host and synchronises the stream, so it
  * blocks until the sweeps are done.
  *
- * Scratch (grid-barrier words, pass counters, residual partials, result
- * record) lives in one file-scope device array of about 130 KB that every
+ * Scratch (grid-barrier words, pass counters and their lists, residual
+ * partials, result record) lives in one file-scope device array of about
+ * 260 KB that every
  * GPU loading libpk holds until the process exits; it serves grids of at
  * most 2048 CTAs, and a larger plan is refused with PK_EINVAL.  All calls
  * share that array: each call clears what must start at zero (the pass
@@ -451,13 +455,14 @@ int pk_barrier_stress_tma(pk_ctx *ctx, int grid, int rounds, int mode, uint64_t 
 
 /* The task kernel's device-side handoff alone ([P1] "Custom block
  * scheduling" measures the cost per block of a handshake): a launch of the
- * task kernel with `grid` CTAs (0 = the context's task grid) in which CTA 0
- * makes up n_tasks empty tasks itself -- each broadcast to the grid and
- * gathered back as a real task is, with no work and no host memory touched
- * -- then stops.  *us_total is the launch's device time (CUDA events),
- * launch included; the difference of two counts over their difference is
- * the cost of one broadcast plus gather.  Errors: PK_EBUSY (task kernel
- * live), PK_ENORESIDENT, PK_ETIMEDOUT, PK_ECUDA. */
+ * task kernel with `grid` CTAs (0 = the context's task grid; one cluster,
+ * 1..16 CTAs) in which the leader makes up n_tasks empty tasks itself --
+ * each handed to the cluster's CTAs and gathered back as a real task is,
+ * with no work and no host memory touched -- then stops.  *us_total is the
+ * launch's device time (CUDA events), launch included; the difference of
+ * two counts over their difference is the cost of one hand-out plus
+ * gather.  Errors: PK_EINVAL (grid), PK_EBUSY (task kernel live),
+ * PK_ENORESIDENT, PK_ETIMEDOUT, PK_ECUDA. */
 int pk_bench_handoff(pk_ctx *ctx, int grid, int64_t n_tasks, double *us_total);
 
 /* Round-trip timing of a task list, host clock (ns per task into

@@ -95,6 +95,8 @@ struct pk_ctx {
     int local_rows = 0;                     // LOCAL: most rows per CTA
     unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
     unsigned long long *pass_done = nullptr; // STREAM pass counters (4 words per CTA, part_cap CTAs)
+    short *pass_deps = nullptr;              // their lists (32 entries per CTA, part_cap CTAs)
+    std::pair<int, int> deps_key{-1, 0};     // (shape, grid) whose lists pass_deps holds
     std::map<std::pair<int, int>, bool> counters_fit;  // (shape, grid) -> every list fits
     int spin_valid = 0;                     // entries written by the last profiled run
     unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
@@ -254,9 +256,12 @@ int ensure_partials(pk_ctx *ctx, int grid) {
         cudaFree(ctx->partials);
         cudaFree(ctx->spin_ns);
         cudaFree(ctx->pass_done);
+        cudaFree(ctx->pass_deps);
         ctx->partials = nullptr;
         ctx->spin_ns = nullptr;
         ctx->pass_done = nullptr;
+        ctx->pass_deps = nullptr;
+        ctx->deps_key = {-1, 0};
         ctx->part_cap = 0;
         ctx->spin_valid = 0;
     }
@@ -266,6 +271,7 @@ int ensure_partials(pk_ctx *ctx, int grid) {
     const size_t pd_bytes = 4 * sizeof(unsigned long long) * (size_t)grid;
     PK_TRY(ctx, cudaMalloc(&ctx->pass_done, pd_bytes));
     PK_TRY(ctx, cudaMemset(ctx->pass_done, 0, pd_bytes));
+    PK_TRY(ctx, cudaMalloc(&ctx->pass_deps, sizeof(short) * kMaxPassDeps * (size_t)grid));
     ctx->part_cap = grid;
     return PK_OK;
 }
@@ -556,8 +562,21 @@ SweepParams base_params(pk_ctx *ctx) {
     p.one_sweep = (ctx->opt.flags & PK_FLAG_ONE_SWEEP_PER_PASS) ? 1 : 0;
     p.local_threads = ctx->local_threads;
     p.pass_done = ctx->pass_done;
+    p.pass_deps = ctx->pass_deps;
     p.pass_counters = 0;  // set per run by choose_persistent's answer
     return p;
+}
+
+// The pass-counter lists for a persistent STREAM launch of `shape` on
+// `grid` CTAs, written on the context's stream unless they are already
+// there.
+int ensure_pass_deps(pk_ctx *ctx, int shape, int grid) {
+    const auto key = std::make_pair(shape, grid);
+    if (ctx->deps_key == key) return PK_OK;
+    cudaError_t e = launch_pass_deps(ctx->nx, ctx->ny, shape, grid, ctx->pass_deps, ctx->stream);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "k_pass_deps launch");
+    ctx->deps_key = key;
+    return PK_OK;
 }
 
 // Reads the barrier's error words after a kernel; returns PK_OK or the code.
@@ -630,6 +649,7 @@ void release(pk_ctx *ctx) {
     cudaFree(ctx->partials);
     cudaFree(ctx->spin_ns);
     cudaFree(ctx->pass_done);
+    cudaFree(ctx->pass_deps);
     cudaFree(ctx->halo);
     cudaFree(ctx->stress_lines);
     cudaFree(ctx->stress_out);
@@ -719,10 +739,16 @@ int task_finish(pk_ctx *ctx) {
 // the end would fall inside it, and a three-sweep pass runs past a residual
 // check (straddle) where a pass of fewer sweeps stops at it.
 //
-// Pass counters (persistent STREAM kernels): passes without a residual check
-// wait only for the CTAs whose rows they read, unless
-// PK_FLAG_BARRIER_EVERY_PASS asks for the barrier or some CTA's list is too
-// long for the producer warp's lanes.
+// Pass counters (persistent STREAM kernels of the one- and three-sweep
+// shapes): passes without a residual check wait only for the CTAs whose rows
+// they read, unless PK_FLAG_BARRIER_EVERY_PASS asks for the barrier or some
+// CTA's list is too long for the producer warp's lanes.  The two-sweep
+// shapes keep the barrier: they move their bytes at 0.97 of the copy
+// bandwidth with it, and with counters their CTAs drift apart and lose the
+// L2 reuse at band edges (16384^2, 100 sweeps: 168.6 against 163.1 us/sweep
+// for the 16-deep ring, 175.7 against 172.9 for the 8-deep one; the
+// three-sweep default 113.5 against 122.0, the one-sweep shape 314.1
+// against 314.9).
 void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *kernel_out,
                        int *shape_out, int *grid_out, int *depth_out, bool *straddle_out,
                        bool *counters_out) {
@@ -745,7 +771,8 @@ void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *
                           ctx->grid_straddle > 0 && !(ctx->opt.flags & PK_FLAG_CHECKS_END_PASSES);
     if (straddle) grid = ctx->grid_straddle;
     bool counters = false;
-    if (kernel == kVariantStream && !(ctx->opt.flags & PK_FLAG_BARRIER_EVERY_PASS)) {
+    if (kernel == kVariantStream && stream_depth(shape) != 2 &&
+        !(ctx->opt.flags & PK_FLAG_BARRIER_EVERY_PASS)) {
         const auto key = std::make_pair(shape, grid);
         auto it = ctx->counters_fit.find(key);
         if (it == ctx->counters_fit.end())
@@ -904,6 +931,10 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     bool straddle, counters;
     choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
     p.pass_counters = counters ? 1 : 0;
+    if (counters) {
+        const int rc = ensure_pass_deps(ctx, shape, grid);
+        if (rc != PK_OK) return rc;
+    }
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_persistent(kernel, ctx->poisson, shape, grid, p, ctx->stream, straddle);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(persistent sweep)");
@@ -988,6 +1019,7 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
     int kernel, shape, grid, depth;
     bool straddle, counters;
     choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
+    if (counters && (rc = ensure_pass_deps(ctx, shape, grid)) != PK_OK) return rc;
     const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
     const size_t dpitch = sizeof(float) * (size_t)ctx->pitch;
     const size_t rows = (size_t)(ctx->ny + 2);
@@ -1530,7 +1562,7 @@ int pk_submit_task(pk_ctx *ctx, const pk_task *task, uint64_t *seq_out) {
         tp.depth = ctx->opt.mailbox_depth;
         tp.idle_timeout_ns = ns_of(ctx->opt.mailbox_idle_timeout_s);
         cudaError_t e = launch_task(ctx->poisson, ctx->task_grid, tp, ctx->task_stream);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(task kernel)");
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchKernelExC(task kernel cluster)");
         ctx->task_live = true;
         ctx->task_status = PK_OK;
     }
@@ -1792,7 +1824,7 @@ int pk_bench_handoff(pk_ctx *ctx, int grid, int64_t n_tasks, double *us_total) {
     tp.synthetic = n_tasks;
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
     cudaError_t e = launch_task(ctx->poisson, grid, tp, ctx->stream);
-    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchCooperativeKernel(task kernel)");
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaLaunchKernelExC(task kernel cluster)");
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     int rc = bar_status(ctx, &ctx->scratch->bar_task, "pk_bench_handoff");
     if (rc != PK_OK) return rc;

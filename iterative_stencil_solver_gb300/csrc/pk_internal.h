@@ -73,7 +73,10 @@ struct SweepParams {
     // CTA b's run_id in the high half and its passes completed in the low
     // half; before a pass a CTA waits for the CTAs whose rows it reads.
     unsigned long long *pass_done;
-    int pass_counters;      // 1: use them (the plan checked every CTA's neighbour set fits)
+    // pass_deps[32 * b + i]: entry i of CTA b's list of CTAs to wait on, -1
+    // past its end (written by launch_pass_deps for this shape and grid)
+    const short *pass_deps;
+    int pass_counters;      // 1: use them (the plan checked every CTA's list fits)
 };
 
 // The CTAs whose rows CTA b of a STREAM pass reads, which are also the CTAs
@@ -138,6 +141,7 @@ __host__ __device__ inline int stream_pass_dep(int strips, int ny, int G, int b,
     return found;
 }
 constexpr int kMaxPassDeps = 32;  // one producer lane polls each entry
+constexpr int kMaxPassDepsGrid = 32767;  // the lists hold CTA indices as 16-bit integers
 
 // ---- mailbox in mapped pinned host memory ---------------------------------
 struct alignas(128) MboxWord {
@@ -226,6 +230,7 @@ inline int stream_depth(int cfg) { return kStreamConfigs[cfg].depth; }
 // Whether every CTA of a persistent STREAM grid of shape cfg has at most
 // kMaxPassDeps entries in its pass-counter list (one producer lane each).
 inline bool stream_counters_fit(int nx, int ny, int cfg, int grid) {
+    if (grid > kMaxPassDepsGrid) return false;
     const int tw = stream_tw(cfg);
     const int strips = (nx + tw - 1) / tw;
     for (int b = 0; b < grid; ++b)
@@ -360,6 +365,9 @@ struct RunRecord {
 };
 cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
                                   cudaStream_t s);
+// Writes the pass-counter lists of a persistent STREAM grid of shape cfg on
+// an nx x ny field into out (32 entries per CTA, grid * 32 shorts).
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, int grid, short *out, cudaStream_t s);
 cudaError_t launch_task(bool poisson, int cluster, const TaskParams &p, cudaStream_t s);
 cudaError_t task_clusters_fit(bool poisson, int cluster, int *n);
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,

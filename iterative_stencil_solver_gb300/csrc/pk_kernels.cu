@@ -898,6 +898,18 @@ __global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar
     }
 }
 
+// One CTA per sweep CTA, one thread per list entry.
+__global__ void __launch_bounds__(32) k_pass_deps(int strips, int ny, int halo, short *out) {
+    out[(size_t)blockIdx.x * kMaxPassDeps + threadIdx.x] =
+        (short)stream_pass_dep(strips, ny, (int)gridDim.x, (int)blockIdx.x, halo, (int)threadIdx.x);
+}
+
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, int grid, short *out, cudaStream_t s) {
+    const int tw = stream_tw(cfg);
+    k_pass_deps<<<grid, kMaxPassDeps, 0, s>>>((nx + tw - 1) / tw, ny, stream_depth(cfg), out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *bar, RunRecord *out,
                                   cudaStream_t s) {
     k_publish_record<<<1, 32, 0, s>>>(info, bar, out);

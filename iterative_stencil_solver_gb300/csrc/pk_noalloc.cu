@@ -11,8 +11,8 @@
 // returns.
 //
 // The persistent kernel needs scratch memory besides its inputs and outputs:
-// the grid-barrier words, the per-CTA pass counters and residual partials,
-// and the result record.  Here that scratch is one file-scope __device__
+// the grid-barrier words, the per-CTA pass counters and their neighbour
+// lists, the residual partials, and the result record.  Here that scratch is one file-scope __device__
 // array of fixed size, which every GPU that loads libpk holds until the
 // process exits.
 #include <cstddef>
@@ -39,9 +39,11 @@ struct NoAllocScratch {
     // STREAM pass counters (4 words per CTA).  Never cleared: each call
     // takes a run id above every earlier one on the device (g_run_id).
     alignas(32) unsigned long long pass_done[4 * kNoAllocMaxGrid];
+    // their lists (32 entries per CTA), written by each call that uses them
+    alignas(16) short pass_deps[kMaxPassDeps * kNoAllocMaxGrid];
 };
 
-// The scratch itself (about 130 KB per device).  In host code the name is a
+// The scratch itself (about 260 KB per device).  In host code the name is a
 // host-side stand-in, not a device address: only the address returned by
 // cudaGetSymbolAddress may be given to a kernel.
 __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
@@ -169,7 +171,8 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     if (e != cudaSuccess) return fail(PK_ECUDA, "cudaMemsetAsync(scratch)", e);
 
     // pass counters as pk_run_sweeps uses them
-    const bool counters = variant == kVariantStream && stream_counters_fit(nx, ny, cfg, (int)grid);
+    const bool counters = variant == kVariantStream && stream_depth(cfg) != 2 &&
+                          stream_counters_fit(nx, ny, cfg, (int)grid);
     int run_id;
     {
         std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -198,7 +201,12 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     p.alt_dir = 1;
     p.run_id = run_id;
     p.pass_done = sc->pass_done;
+    p.pass_deps = sc->pass_deps;
     p.pass_counters = counters ? 1 : 0;
+    if (counters) {
+        e = launch_pass_deps(nx, ny, cfg, (int)grid, sc->pass_deps, s);
+        if (e != cudaSuccess) return fail(PK_ECUDA, "k_pass_deps launch", e);
+    }
     p.barrier_kind = (int)kBarrierCounter;
     p.bar_base = 0;
     e = launch_persistent(variant, poisson, cfg, (int)grid, p, s, straddle);

@@ -939,13 +939,6 @@ __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const floa
     }
 }
 
-// Entry i of this CTA's pass-counter list, out of line: the lookup runs
-// once per launch, and inlined its 64-bit divisions cost the row windows
-// registers.
-__device__ __noinline__ int stream_pass_dep_of(const SweepParams &p, int tw, int depth, int i) {
-    return stream_pass_dep((p.nx + tw - 1) / tw, p.ny, (int)gridDim.x, (int)blockIdx.x, depth, i);
-}
-
 // ===========================================================================
 // The persistent and per-launch STREAM kernels.  STRADDLE: the persistent
 // loop lets three-sweep passes run past residual checks (a separate
@@ -954,9 +947,11 @@ __device__ __noinline__ int stream_pass_dep_of(const SweepParams &p, int tw, int
 //
 // Pass counters: producer lane i waits on entry i of this CTA's neighbour
 // list (stream_pass_dep: the CTAs whose rows the pass reads, which are the
-// CTAs that read this CTA's rows), or on nothing.  The lanes find their
-// entries after the first pass's row segments are issued, while the
-// consumers still work, and keep them in shared memory.
+// CTAs that read this CTA's rows), or on nothing.  A separate kernel writes
+// the lists (k_pass_deps; computed here, their 64-bit divisions cost the
+// two-CTA shapes' row windows registers); the lanes load their entries after
+// the first pass's row segments are issued, while the consumers still work,
+// and keep them in shared memory.
 template <class C, bool POISSON, bool STRADDLE>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -981,7 +976,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
         }
         pass_stream_any<C, POISSON, STRADDLE>(p, src, dst, dir, cs, store, dp, st, s2, rmax);
         if (threadIdx.x >= C::kCons && p.pass_counters && s_dep[threadIdx.x & 31u] == -2)
-            s_dep[threadIdx.x & 31u] = stream_pass_dep_of(p, C::TW, C::kDepth, (int)(threadIdx.x & 31u));
+            s_dep[threadIdx.x & 31u] = p.pass_deps[(size_t)blockIdx.x * kMaxPassDeps + (threadIdx.x & 31u)];
     }, [&](unsigned need) -> bool {
         if (threadIdx.x >= C::kCons) {
             const unsigned lane = threadIdx.x & 31u;

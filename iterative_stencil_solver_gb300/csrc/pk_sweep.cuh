@@ -80,11 +80,14 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     __shared__ BarrierCtl s_ctl;
     __shared__ double s_res0, s_res_last;
     __shared__ float s_rmax_last;
+    __shared__ unsigned s_passes;  // passes this CTA has completed (thread 0 counts)
+    __shared__ int s_leave;        // fault injection: leave at the end of this pass
     if (threadIdx.x == 0) {
         s_ctl = make_ctl(p);
         s_ctl.skip_cta = -1;  // the loop injects the fault itself (see above)
         s_res0 = s_res_last = 0.0;
         s_rmax_last = 0.f;
+        s_passes = 0;
     }
     __syncthreads();
     const bool checks = p.tol > 0.f && p.check_every > 0;
@@ -96,7 +99,6 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     // the compiler inlines it and the row windows stay in registers).
     bool redo = false;
     long long k_exit = 0;
-    unsigned passes = 0;       // passes this CTA has completed
     bool counted = false;      // the last pass ended at the pass counters
     for (;;) {
         int dp = 1, cs = 0;
@@ -125,17 +127,24 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
                 dp = m < MAXD ? (int)m : MAXD;
             }
         }
-        if (counted && !wait(passes)) return;  // aborting: the host reads the error
+        // (s_passes was last written before the block barrier that ended the
+        // previous pass)
+        if (counted && !wait(s_passes)) return;  // aborting: the host reads the error
         double s2 = 0.0;
         float rmax = 0.f;
         pass(p.u[cur], p.u[cur ^ 1], cs, store, dp, k, s2, rmax);
-        ++passes;
+        if (threadIdx.x == 0) ++s_passes;
         if (redo) {  // no barrier: the kernel ends here
             cur ^= 1;
             k = k_exit;
             break;
         }
-        if ((int)blockIdx.x == p.skip_cta && (int)passes - 1 == p.skip_at) return;
+        if (p.skip_cta >= 0) {  // fault injection (the condition is the same in every thread)
+            if (threadIdx.x == 0)
+                s_leave = (int)blockIdx.x == p.skip_cta && (int)s_passes - 1 == p.skip_at;
+            __syncthreads();
+            if (s_leave) return;
+        }
         counted = p.pass_counters && !cs;
         if (counted) {
             // every thread's stores of this pass (fenced to the async proxy
@@ -143,7 +152,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
             __syncthreads();
             if (threadIdx.x == 0)
                 st_release_gpu_u64(p.pass_done + 4 * (size_t)blockIdx.x,
-                                   ((unsigned long long)(unsigned)p.run_id << 32) | passes);
+                                   ((unsigned long long)(unsigned)p.run_id << 32) | s_passes);
             cur ^= 1;
             k += dp;
             continue;
@@ -200,7 +209,7 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
         d->cur = cur;
         d->task_sweeps = 0;
         d->barriers = s_ctl.index;
-        d->passes = (int)passes;
+        d->passes = (int)s_passes;
         d->bar_count_end = p.bar_base + (unsigned)s_ctl.index * gridDim.x;
         __threadfence();
         d->run_id = p.run_id;

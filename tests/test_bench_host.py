@@ -73,3 +73,22 @@ def test_other_variants_take_one_sweep_per_pass():
     assert bench.passes_of(info(3, -1, 2), 10, 0.0, 0) == (5, 0)
     assert bench.shape_label(info(3, -1, 2), False) == "k_persistent_local2"
     assert bench.shape_label(info(2, 6), False).startswith("k_persistent_stream<{1 float4/thread, 8-deep ring, 2 sweeps/pass}")
+
+
+def test_clock_summary_keeps_the_timed_region(tmp_path):
+    # samples after the mark are the timed region; with none there, the last
+    # warm-up sample stands in and the record says so
+    path = tmp_path / "clocks.csv"
+    idle = "0, 120, 2070, 90, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+    warm = "0, 2070, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active\n"
+    busy = "0, 2040, 2070, 950, 0x4, Not Active, Not Active, Not Active, Active\n"
+    path.write_text(idle + warm + busy + busy)
+    cs = bench.ClockSampler(0)
+    cs.path = str(path)
+    cs.offset = len(idle + warm)
+    got = cs._summary()
+    assert got["samples"] == 2 and got["sm_mhz"] == 2040 and got["reasons"] == ["sw_power_cap"]
+    assert got["window"] == "timed region"
+    cs.offset = len(idle + warm + busy + busy)
+    got = cs._summary()
+    assert got["samples"] == 1 and got["sm_mhz"] == 2040 and got["window"].startswith("last warm-up")

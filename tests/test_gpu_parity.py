@@ -634,13 +634,14 @@ def test_straddled_checks_bit_exact(pk, cfg, nx, ny, poisson):
 
 # Pass counters: a persistent STREAM pass without a residual check starts
 # once the CTAs whose rows it reads have finished the pass before (the
-# lists are pinned on the CPU in test_pass_deps.py).  Shapes of one, two and
-# three sweeps per pass at the default grids, on fields whose CTAs own one
-# or two rows (so each waits on up to 20 others, across strips) and whose
-# last strip can be one column wide: the same bits as the oracle and as a
-# barrier after every pass, and the grid barrier only behind the checks.
-PASS_COUNTER_CASES = [(3, 3000, 200), (6, 2100, 37), (8, 1030, 300), (10, 1793, 60),
-                      (11, 4500, 90), (12, 4097, 50), (12, 300, 41)]
+# lists are pinned on the CPU in test_pass_deps.py).  Shapes of one and three
+# sweeps per pass (the two-sweep shapes keep the barrier) at the default
+# grids, on fields whose CTAs own one or two rows (so each waits on up to 20
+# others, across strips) and whose last strip can be one column wide: the
+# same bits as the oracle and as a barrier after every pass, and the grid
+# barrier only behind the checks.
+PASS_COUNTER_CASES = [(3, 3000, 200), (3, 5000, 64), (10, 1793, 60), (11, 4500, 90),
+                      (11, 2053, 19), (12, 4097, 50), (12, 300, 41), (6, 2100, 37), (8, 1030, 300)]
 
 
 @pytest.mark.parametrize("cfg,nx,ny", PASS_COUNTER_CASES,
@@ -658,8 +659,11 @@ def test_pass_counters_bit_exact(pk, cfg, nx, ny, poisson):
             return
         assert_same_bits(got, want)
         check_info(info, oinfo)
-        assert info["pass_counters"] == 1
-        assert info["barriers"] == oinfo.n_checks
+        if cfg in (6, 8):  # two sweeps per pass: the barrier after every pass
+            assert info["pass_counters"] == 0 and info["barriers"] == info["passes"]
+        else:
+            assert info["pass_counters"] == 1
+            assert info["barriers"] == oinfo.n_checks
         got2, info2 = run_pk(pk, u0, f, n, tol, ce, variant=2, stream_config=cfg,
                              flags=pk.PK_FLAG_ALTERNATE_DIRECTION | pk.PK_FLAG_BARRIER_EVERY_PASS)
         assert_same_bits(got2, want)
@@ -669,10 +673,10 @@ def test_pass_counters_bit_exact(pk, cfg, nx, ny, poisson):
 
 
 def test_pass_counters_off_when_a_list_is_too_long(pk):
-    # 300 CTAs of the two-sweep shape on 111 (strip, row) pairs: a CTA's list
-    # runs through the CTAs that own no rows and one reaches 35 entries, more
-    # than the producer warp's lanes, so the run keeps the barrier
-    nx, ny, cfg, grid = 2100, 37, 6, 300
+    # 300 CTAs of a three-sweep shape on 100 (strip, row) pairs: a CTA's list
+    # runs through the CTAs that own no rows and reaches more entries than the
+    # producer warp's lanes, so the run keeps the barrier
+    nx, ny, cfg, grid = 1793, 50, 11, 300
     assert max(len(pk.pk_stream_pass_deps(nx, ny, cfg, grid, b)) for b in range(grid)) > 32
     u0 = inputs.random_field(nx, ny, seed=1300)
     want, _ = oracle.jacobi_run(u0, n=12)
