@@ -949,9 +949,7 @@ __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const floa
 // list (stream_pass_dep: the CTAs whose rows the pass reads, which are the
 // CTAs that read this CTA's rows), or on nothing.  A separate kernel writes
 // the lists (k_pass_deps; computed here, their 64-bit divisions cost the
-// two-CTA shapes' row windows registers); the lanes load their entries after
-// the first pass's row segments are issued, while the consumers still work,
-// and keep them in shared memory.
+// two-CTA shapes' row windows registers).
 template <class C, bool POISSON, bool STRADDLE>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
@@ -960,7 +958,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
     __shared__ unsigned long long s_wait_ns;
     StreamState st = stream_setup<C>(smem);
     if (threadIdx.x >= C::kCons) {
-        s_dep[threadIdx.x & 31u] = -2;  // not looked up yet
+        s_dep[threadIdx.x & 31u] = -2;  // not fetched yet
         if (threadIdx.x == C::kCons) s_wait_ns = 0ull;
     }
     persistent_loop<C::kDepth, STRADDLE>(p, [&](const float *src, float *dst, int cs, bool store,
@@ -975,31 +973,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
             fence_proxy_async_global();
         }
         pass_stream_any<C, POISSON, STRADDLE>(p, src, dst, dir, cs, store, dp, st, s2, rmax);
-        if (threadIdx.x >= C::kCons && p.pass_counters && s_dep[threadIdx.x & 31u] == -2)
-            s_dep[threadIdx.x & 31u] = p.pass_deps[(size_t)blockIdx.x * kMaxPassDeps + (threadIdx.x & 31u)];
-    }, [&](unsigned need) -> bool {
-        if (threadIdx.x >= C::kCons) {
-            const unsigned lane = threadIdx.x & 31u;
-            const uint64_t t0 = p.profile ? globaltimer_ns() : 0ull;
-            const int dep = s_dep[lane];
-            bool ok = true;
-            if (dep >= 0) {
-                const unsigned long long *w = p.pass_done + 4 * (size_t)dep;
-                const unsigned long long target = ((unsigned long long)(unsigned)p.run_id << 32) | need;
-                ok = bounded_spin(p.bar, p.timeout_ns, kSitePassCounter,
-                                  [&] { return ld_relaxed_gpu_u64(w) >= target; });
-                fence_acq_rel_gpu();  // each lane acquires what it observed
-            }
-            ok = __all_sync(0xffffffffu, ok);
-            __syncwarp();
-            if (lane == 0u) {
-                s_wait_ok = ok ? 1 : 0;
-                if (p.profile) s_wait_ns += globaltimer_ns() - t0;
-            }
-        }
-        __syncthreads();
-        return s_wait_ok != 0;
-    });
+        pass_counter_fetch<C::kCons>(p, s_dep);
+    }, [&](unsigned need) { return pass_counter_wait<C::kCons>(p, need, s_dep, s_wait_ok, s_wait_ns); });
     // (a normal end: the loop has stored the barrier waits; the counter
     // waits were made visible to thread 0 by the last wait's block barrier)
     if (p.profile && threadIdx.x == 0 && p.pass_counters) p.spin_ns[blockIdx.x] += s_wait_ns;

@@ -216,6 +216,50 @@ __device__ __forceinline__ void persistent_loop(const SweepParams &p, PassFn &&p
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pass counters, the kernel side: the 32 lanes of the warp whose first
+// thread is W0 hold this CTA's list in s_dep (entry i in lane i, -1 past the
+// end, -2 until fetched).  pass_counter_fetch loads it once, after the first
+// pass (by then that warp is idle: the list's load stays off the first
+// pass's critical path).  pass_counter_wait, called by every thread, lets
+// lane i spin (relaxed, bounded, abort-aware) until CTA s_dep[i] has
+// published `need` passes of this run, acquire it with its own fence, and
+// meets the CTA at a block barrier; false when a wait gave up or the grid is
+// aborting.  With profiling on, lane 0 adds the wait to s_wait_ns.
+template <unsigned W0>
+__device__ __forceinline__ void pass_counter_fetch(const SweepParams &p, int *s_dep) {
+    if (p.pass_counters && threadIdx.x >= W0 && threadIdx.x < W0 + 32u &&
+        s_dep[threadIdx.x - W0] == -2)
+        s_dep[threadIdx.x - W0] = p.pass_deps[(size_t)blockIdx.x * kMaxPassDeps + (threadIdx.x - W0)];
+}
+
+template <unsigned W0>
+__device__ __forceinline__ bool pass_counter_wait(const SweepParams &p, unsigned need,
+                                                  const int *s_dep, int &s_ok,
+                                                  unsigned long long &s_wait_ns) {
+    if (threadIdx.x >= W0 && threadIdx.x < W0 + 32u) {
+        const unsigned lane = threadIdx.x - W0;
+        const uint64_t t0 = p.profile ? globaltimer_ns() : 0ull;
+        const int dep = s_dep[lane];
+        bool ok = true;
+        if (dep >= 0) {
+            const unsigned long long *w = p.pass_done + 4 * (size_t)dep;
+            const unsigned long long target = ((unsigned long long)(unsigned)p.run_id << 32) | need;
+            ok = bounded_spin(p.bar, p.timeout_ns, kSitePassCounter,
+                              [&] { return ld_relaxed_gpu_u64(w) >= target; });
+            fence_acq_rel_gpu();  // each lane acquires what it observed
+        }
+        ok = __all_sync(0xffffffffu, ok);
+        __syncwarp();
+        if (lane == 0u) {
+            s_ok = ok ? 1 : 0;
+            if (p.profile) s_wait_ns += globaltimer_ns() - t0;
+        }
+    }
+    __syncthreads();
+    return s_ok != 0;
+}
+
 // Per-launch passes reduce their residual into this CTA's partial.
 __device__ __forceinline__ void write_partial(const SweepParams &p, double s2, float rmax) {
     block_reduce(s2, rmax);
