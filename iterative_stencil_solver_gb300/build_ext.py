@@ -1,7 +1,9 @@
 """Build libpk.so (the CUDA kernels and the C ABI) in-tree with nvcc for sm_103a.
 
-Two translation units are compiled in parallel and linked into
-``iterative_stencil_solver_gb300/libpk.so``.  Flags: ``-fmad=false`` (no FMA
+The translation units are compiled in parallel and linked into
+``iterative_stencil_solver_gb300/libpk.so``.  ``build(coverage=True)`` builds
+the coverage and bounds build (include/pk_debug.h) from the same sources with
+``-DPK_DEBUG_COVERAGE`` into ``libpk_coverage.so``; only its tests use it.  Flags: ``-fmad=false`` (no FMA
 contraction anywhere; the kernels also pin every operation with _rn
 intrinsics), default IEEE division/sqrt, no fast-math, no flush to zero.
 """
@@ -15,6 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpk.so")
+LIB_COVERAGE = os.path.join(HERE, "libpk_coverage.so")
 SOURCES = ["pk_stream_d3.cu", "pk_stream_d3s.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
            "pk_host.cu", "pk_noalloc.cu", "pk_stream.cu"]
 HEADERS = ["pk_device.cuh", "pk_internal.h", "pk_sweep.cuh", "pk_stream.cuh"]
@@ -34,25 +37,30 @@ def nvcc():
     raise RuntimeError("nvcc not found: libpk.so cannot be built")
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in SOURCES + HEADERS]
-    deps += [os.path.join(INCLUDE, "pk.h"), os.path.abspath(__file__)]
+    deps += [os.path.join(INCLUDE, "pk.h"), os.path.join(INCLUDE, "pk_debug.h"),
+             os.path.abspath(__file__)]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force=False, verbose=False, ptxas_verbose=False):
-    """Compile libpk.so if missing or older than its sources; return its path."""
-    if not force and not _stale():
-        return LIB
+def build(force=False, verbose=False, ptxas_verbose=False, coverage=False):
+    """Compile libpk.so (coverage=True: libpk_coverage.so) if missing or older
+    than its sources; return its path."""
+    lib = LIB_COVERAGE if coverage else LIB
+    if not force and not _stale(lib):
+        return lib
     exe = nvcc()
-    bdir = os.path.join(HERE, "_build")
+    bdir = os.path.join(HERE, "_build_coverage" if coverage else "_build")
     os.makedirs(bdir, exist_ok=True)
     procs = []
     objs = []
     extra = ["-Xptxas", "-v"] if ptxas_verbose else []
+    if coverage:
+        extra += ["-DPK_DEBUG_COVERAGE"]
     for src in SOURCES:
         obj = os.path.join(bdir, src.replace(".cu", ".o"))
         objs.append(obj)
@@ -70,13 +78,13 @@ def build(force=False, verbose=False, ptxas_verbose=False):
             failed.append(" ".join(cmd))
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
-    tmp = LIB + ".tmp%d" % os.getpid()
+    tmp = lib + ".tmp%d" % os.getpid()
     cmd = [exe] + ARCH + ["-shared", "-o", tmp] + objs
     if verbose:
         print(" ".join(cmd))
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

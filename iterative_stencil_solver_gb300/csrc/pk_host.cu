@@ -29,6 +29,7 @@
 #include <thread>
 
 #include "pk.h"
+#include "pk_debug.h"
 #include "pk_internal.h"
 
 using namespace pk;
@@ -96,6 +97,8 @@ struct pk_ctx {
     unsigned long long *spin_ns = nullptr;  // per-CTA barrier wait (part_cap entries)
     unsigned long long *pass_done = nullptr; // STREAM pass counters (4 words per CTA, part_cap CTAs)
     short *pass_deps = nullptr;              // their lists (32 entries per CTA, part_cap CTAs)
+    unsigned *cov = nullptr;                 // coverage build: a counter per float of both buffers
+    unsigned long long *cov_status = nullptr; // coverage build: bad accesses, first place
     std::pair<int, int> deps_key{-1, 0};     // (shape, grid) whose lists pass_deps holds
     std::map<std::pair<int, int>, bool> counters_fit;  // (shape, grid) -> every list fits
     int spin_valid = 0;                     // entries written by the last profiled run
@@ -564,6 +567,8 @@ SweepParams base_params(pk_ctx *ctx) {
     p.pass_done = ctx->pass_done;
     p.pass_deps = ctx->pass_deps;
     p.pass_counters = 0;  // set per run by choose_persistent's answer
+    p.cov = ctx->cov;  // null unless this is the coverage build
+    p.cov_status = ctx->cov_status;
     return p;
 }
 
@@ -633,6 +638,13 @@ int common_setup(pk_ctx *ctx) {
     PK_TRY(ctx, cudaHostAlloc(&ctx->mbox, ctx->mbox_bytes, cudaHostAllocMapped));
     std::memset(ctx->mbox, 0, ctx->mbox_bytes);
     PK_TRY(ctx, cudaHostGetDevicePointer((void **)&ctx->mbox_dev, ctx->mbox, 0));
+#ifdef PK_DEBUG_COVERAGE
+    const size_t cov_bytes = 2 * sizeof(unsigned) * (size_t)(ctx->ny + 2) * (size_t)ctx->pitch;
+    PK_TRY(ctx, cudaMalloc(&ctx->cov, cov_bytes));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->cov, 0, cov_bytes, ctx->stream));
+    PK_TRY(ctx, cudaMalloc(&ctx->cov_status, 2 * sizeof(unsigned long long)));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->cov_status, 0, 2 * sizeof(unsigned long long), ctx->stream));
+#endif
     return plan(ctx);
 }
 
@@ -650,6 +662,8 @@ void release(pk_ctx *ctx) {
     cudaFree(ctx->spin_ns);
     cudaFree(ctx->pass_done);
     cudaFree(ctx->pass_deps);
+    cudaFree(ctx->cov);
+    cudaFree(ctx->cov_status);
     cudaFree(ctx->halo);
     cudaFree(ctx->stress_lines);
     cudaFree(ctx->stress_out);
@@ -1890,3 +1904,31 @@ int pk_bench_tasks(pk_ctx *ctx, int mode, const pk_task *tasks, int n_kinds, int
 }
 
 }  // extern "C"
+
+#ifdef PK_DEBUG_COVERAGE
+// ---- the coverage and bounds build (include/pk_debug.h) ---------------------
+extern "C" {
+
+int pk_debug_coverage_reset(pk_ctx *ctx) {
+    if (!ctx) return PK_EINVAL;
+    const size_t cov_bytes = 2 * sizeof(unsigned) * (size_t)(ctx->ny + 2) * (size_t)ctx->pitch;
+    PK_TRY(ctx, cudaMemsetAsync(ctx->cov, 0, cov_bytes, ctx->stream));
+    PK_TRY(ctx, cudaMemsetAsync(ctx->cov_status, 0, 2 * sizeof(unsigned long long), ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    return PK_OK;
+}
+
+int pk_debug_coverage_read(pk_ctx *ctx, uint32_t *counts, int64_t n, uint64_t *status) {
+    if (!ctx) return PK_EINVAL;
+    const int64_t need = 2 * (int64_t)(ctx->ny + 2) * ctx->pitch;
+    if (counts && n < need) return fail(ctx, PK_EINVAL, "pk_debug_coverage_read: need %lld counters", (long long)need);
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
+    PK_TRY(ctx, cudaStreamSynchronize(ctx->task_stream));
+    if (counts) PK_TRY(ctx, cudaMemcpy(counts, ctx->cov, sizeof(uint32_t) * (size_t)need, cudaMemcpyDeviceToHost));
+    if (status) PK_TRY(ctx, cudaMemcpy(status, ctx->cov_status, 2 * sizeof(uint64_t), cudaMemcpyDeviceToHost));
+    return (int)(need > 0x7fffffff ? 0x7fffffff : need);
+}
+
+}  // extern "C"
+#endif
+

@@ -77,6 +77,12 @@ struct SweepParams {
     // past its end (written by launch_pass_deps for this shape and grid)
     const short *pass_deps;
     int pass_counters;      // 1: use them (the plan checked every CTA's list fits)
+    // The coverage and bounds build only (PK_DEBUG_COVERAGE), else null: one
+    // counter per float of each field buffer (buffer 0's (ny + 2) * pitch,
+    // then buffer 1's), and two status words: the bad accesses seen and the
+    // first one's place.
+    unsigned *cov;
+    unsigned long long *cov_status;
 };
 
 // The CTAs whose rows CTA b of a STREAM pass reads, which are also the CTAs

@@ -64,7 +64,7 @@ __device__ __forceinline__ void pass_direct(const SweepParams &p, const float *_
         if (POISSON) G = ld4(p.g + (long long)jm1 * p.gpitch + 4ll * q);
         const int valid = min(4, p.nx - 4 * (int)q);
         const Quad t = quad_t<POISSON>(W, C, E, S, N, G);
-        if (STORE) store_quad(dst + off, quad_update(t), valid);
+        if (STORE && PK_COV_STORE(p, dst + off, valid)) store_quad(dst + off, quad_update(t), valid);
         if (CHECK) quad_residual(t, C, valid, acc, rmax);
     }
     if (CHECK) s2 = __dadd_rn(s2, resff_value(acc));
@@ -133,8 +133,8 @@ __device__ __forceinline__ void pass_rb(const SweepParams &p, float *u, int colo
         const float4 v = quad_update(quad_t<POISSON>(W, C, E, S, N, G));
         // point (j, i) with i = 1 + 4q + cell has colour (i + j) & 1
         const int c0 = (colour + 1 + (int)(jm1 + 1u)) & 1;
-        if (c0 < valid) c[c0] = c0 ? v.y : v.x;
-        if (c0 + 2 < valid) c[c0 + 2] = c0 ? v.w : v.z;
+        if (c0 < valid && PK_COV_STORE(p, c + c0, 1)) c[c0] = c0 ? v.y : v.x;
+        if (c0 + 2 < valid && PK_COV_STORE(p, c + c0 + 2, 1)) c[c0 + 2] = c0 ? v.w : v.z;
     }
 }
 

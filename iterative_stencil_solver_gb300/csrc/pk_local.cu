@@ -242,8 +242,9 @@ __global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local(SweepPara
     float *dst = p.u[p.cur ^ (int)(k & 1)];
     for (int u = tid; u < B * nq; u += nthr) {
         const int lr = u / nq + 1, q = u - (lr - 1) * nq;
-        store_quad(dst + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q,
-                   ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+        float *d = dst + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q;
+        if (PK_COV_STORE(p, d, min(4, nx - 4 * q)))
+            store_quad(d, ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
         DeviceInfo *d = p.info;
@@ -483,8 +484,9 @@ __global__ void __launch_bounds__(kLocalMaxThreads) k_persistent_local_d(SweepPa
     float *dst = p.u[p.cur ^ (int)(k & 1)];
     for (int u = tid; u < B * nq; u += nthr) {
         const int lr = D + u / nq, q = u - (lr - D) * nq;
-        store_quad(dst + (long long)(r0 - D + lr) * p.pitch + 4 + 4 * q,
-                   ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
+        float *d = dst + (long long)(r0 - D + lr) * p.pitch + 4 + 4 * q;
+        if (PK_COV_STORE(p, d, min(4, nx - 4 * q)))
+            store_quad(d, ld4((c ? Tb : Ta) + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
         DeviceInfo *d = p.info;
@@ -623,8 +625,8 @@ __global__ void __launch_bounds__(kDirectThreads) k_persistent_local_rb(SweepPar
     }
     for (int uu = tid; uu < B * nq; uu += nthr) {
         const int lr = uu / nq + 1, q = uu - (lr - 1) * nq;
-        store_quad(u + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q, ld4(T + lr * sp + 4 + 4 * q),
-                   min(4, nx - 4 * q));
+        float *d = u + (long long)(r0 - 1 + lr) * p.pitch + 4 + 4 * q;
+        if (PK_COV_STORE(p, d, min(4, nx - 4 * q))) store_quad(d, ld4(T + lr * sp + 4 + 4 * q), min(4, nx - 4 * q));
     }
     if (b == 0 && tid == 0) {
         DeviceInfo *d = p.info;

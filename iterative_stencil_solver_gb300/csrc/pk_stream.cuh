@@ -138,9 +138,14 @@ __device__ __forceinline__ void produce_segment(const SweepParams &p, const floa
             const bool gneed = POISSON && idx >= 1 && idx <= nin - 2 && r >= 1 && r <= p.ny;
             float *dst_u = st.slots + slot * C::SLOT;
             mbar_arrive_expect_tx(&st.full[slot], bytes_u + (gneed ? bytes_g : 0u));
-            tma_load_1d(dst_u, src + (long long)rr * p.pitch + col0, bytes_u, &st.full[slot]);
+            tma_load_1d(dst_u,
+                        PK_COV_LOAD(p, src + (long long)rr * p.pitch + col0, bytes_u, src, p.pitch,
+                                    p.ny + 2, (p.u[1] == src ? 1ull : 0ull)),
+                        bytes_u, &st.full[slot]);
             if (gneed)
-                tma_load_1d(dst_u + C::SLOTU + 4 - gl, p.g + (long long)(r - 1) * p.gpitch + col0 - gl,
+                tma_load_1d(dst_u + C::SLOTU + 4 - gl,
+                            PK_COV_LOAD(p, p.g + (long long)(r - 1) * p.gpitch + col0 - gl, bytes_g,
+                                        p.g, p.gpitch, p.ny, 2ull),
                             bytes_g, &st.full[slot]);
         }
         __syncwarp();
@@ -208,7 +213,8 @@ __device__ __forceinline__ void consume_segment(const SweepParams &p, float *dst
                 // prev and x are the rows on either side of the centre; their
                 // sum is commutative, so walking up or down gives the same bits.
                 const Quad q = quad_t<POISSON>(w, cur[k], e, prev[k], x[k], curg[k]);
-                if (STORE) store_quad(drow + 4 * (t + k * C::kCons), quad_update(q), valid[k]);
+                if (STORE && PK_COV_STORE(p, drow + 4 * (t + k * C::kCons), valid[k]))
+                    store_quad(drow + 4 * (t + k * C::kCons), quad_update(q), valid[k]);
                 if (CHECK) quad_residual(q, cur[k], valid[k], s2, rmax);
             }
         }
@@ -338,6 +344,7 @@ __device__ __forceinline__ void seg2_step(const SweepParams &p, Seg2<C::kQPT> &c
             const int o = c.o[k];
             const float4 g = POISSON ? lds4(sa + C::SLOTU + 4 + o) : z4;
             const Quad q2 = quad_t2<POISSON>(qr[3 + o], QB[k], qr[8 + o], QA[k], QY[k], g);
+            if (!PK_COV_STORE(p, c.drow + o, FULL ? 4 : c.valid[k])) continue;
             if (FULL)
                 *reinterpret_cast<float4 *>(c.drow + o) = quad_update2(q2);
             else
@@ -677,6 +684,7 @@ __device__ __forceinline__ void seg3_step(const SweepParams &p, Seg3<C::kQPT> &c
 #pragma unroll
         for (int k = 0; k < Q; ++k) {
             float *d = c.drow + 4 * k * C::kCons;
+            if (!PK_COV_STORE(p, d, FULL ? 4 : c.valid[k])) continue;
             if (FULL)
                 *reinterpret_cast<float4 *>(d) = u3[k];
             else

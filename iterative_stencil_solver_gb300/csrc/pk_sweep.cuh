@@ -17,6 +17,63 @@ namespace pk {
 namespace {
 
 // ===========================================================================
+// The coverage and bounds build (compiled with PK_DEBUG_COVERAGE into a
+// library of its own; the release build compiles none of it).  It checks
+// what the kernels' index arithmetic otherwise leaves to the bit-exact
+// comparisons: that a pass stores each interior cell of its target once and
+// nothing else, and that every bulk copy reads inside one row of its buffer
+// ("Persistent Kernels: Bridging GPU-CPU Execution", "Implementation details
+// and correctness": the loops were checked to cover the domain exactly once).
+// A bad access is counted, its place recorded, and it is skipped (a store)
+// or redirected to the buffer's first row (a bulk copy, whose barrier must
+// still complete); nothing traps.  Status word 1 holds the first bad place:
+// bits 62-63 the buffer (0, 1; 2 the source; 3 none of them), bits 0-61 the
+// float offset.
+#ifdef PK_DEBUG_COVERAGE
+__device__ __noinline__ void cov_bad(const SweepParams &p, unsigned long long where) {
+    if (atomicAdd(&p.cov_status[0], 1ull) == 0ull) atomicExch(&p.cov_status[1], where);
+}
+// n consecutive floats stored at q: true (each counted) when all are
+// interior cells of one field buffer, else false (the caller skips the store).
+__device__ __noinline__ bool cov_store(const SweepParams &p, const float *q, int n) {
+    if (!p.cov || n <= 0) return true;
+    const long long elems = (long long)(p.ny + 2) * p.pitch;
+    for (int b = 0; b < 2; ++b) {
+        const long long off = q - p.u[b];
+        if (off < 0 || off + n > elems) continue;
+        const long long row = off / p.pitch, col = off - row * p.pitch;
+        if (row < 1 || row > p.ny || col < 4 || col + n - 1 > p.nx + 3) {
+            cov_bad(p, ((unsigned long long)b << 62) | (unsigned long long)off);
+            return false;
+        }
+        for (int i = 0; i < n; ++i) atomicAdd(&p.cov[(long long)b * elems + off + i], 1u);
+        return true;
+    }
+    cov_bad(p, 3ull << 62);
+    return false;
+}
+// A bulk copy of `bytes` from q, which must lie inside one row of the buffer
+// at base (rows of `pitch` floats, `rows` of them; `which` names it): q, or
+// base when it does not.
+__device__ __noinline__ const float *cov_load(const SweepParams &p, const float *q, unsigned bytes,
+                                              const float *base, long long pitch, long long rows,
+                                              unsigned long long which) {
+    if (!p.cov) return q;
+    const long long off = q - base;
+    const long long floats = (long long)(bytes + 3u) / 4;
+    if (off >= 0 && off / pitch < rows && off % pitch + floats <= pitch) return q;
+    cov_bad(p, (which << 62) | ((unsigned long long)off & 0x3fffffffffffffffull));
+    return base;
+}
+#define PK_COV_STORE(p, q, n) cov_store((p), (q), (n))
+#define PK_COV_LOAD(p, q, bytes, base, pitch, rows, which) \
+    cov_load((p), (q), (bytes), (base), (pitch), (rows), (which))
+#else
+#define PK_COV_STORE(p, q, n) true
+#define PK_COV_LOAD(p, q, bytes, base, pitch, rows, which) (q)
+#endif
+
+// ===========================================================================
 // The persistent loop ("What the barrier buys"): sweep k reads U_k and
 // writes U_{k+1}; on a check sweep the same pass reduces the residual of
 // U_k into per-CTA partials; after the grid barrier every CTA reduces all

@@ -17,7 +17,9 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libpk.so")
+# PK_LIBRARY names another build of the same ABI (the coverage build's
+# libpk_coverage.so, include/pk_debug.h); by default the release libpk.so.
+LIB_PATH = os.environ.get("PK_LIBRARY") or os.path.join(_HERE, "libpk.so")
 
 PK_OK = 0
 PK_EINVAL = -1
@@ -176,6 +178,14 @@ _SIGS = {
 }
 
 
+# Only the coverage build exports these (include/pk_debug.h).
+_DEBUG_SIGS = {
+    "pk_debug_coverage_reset": (ctypes.c_int, [_VP]),
+    "pk_debug_coverage_read": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int64,
+                                              ctypes.POINTER(ctypes.c_uint64)]),
+}
+
+
 def load_library(path=LIB_PATH):
     if not os.path.exists(path):
         raise ImportError("libpk.so not found at %s: build it first "
@@ -185,6 +195,11 @@ def load_library(path=LIB_PATH):
         fn = getattr(lib, name)
         fn.restype = res
         fn.argtypes = args
+    for name, (res, args) in _DEBUG_SIGS.items():
+        if hasattr(lib, name):
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
     return lib
 
 
@@ -354,6 +369,27 @@ def pk_stream_pass_deps(nx, ny, stream_config, grid, cta):
     out = (ctypes.c_int32 * max(n, 1))()
     _lib.pk_stream_pass_deps(nx, ny, stream_config, grid, cta, out, n)
     return list(out[:n])
+
+
+def has_coverage():
+    """True when the loaded library is the coverage build."""
+    return hasattr(_lib, "pk_debug_coverage_read")
+
+
+def pk_debug_coverage_reset(ctx):
+    _check(_lib.pk_debug_coverage_reset(ctx), ctx)
+
+
+def pk_debug_coverage_read(ctx):
+    """(counts, status): counts as a (2, ny + 2, pitch) uint32 array (buffer
+    A, then B, in the field layout), status as (bad accesses, first place)."""
+    pitch, _, _ = pk_layout(ctx.nx, ctx.ny)
+    n = 2 * (ctx.ny + 2) * pitch
+    counts = np.zeros(n, dtype=np.uint32)
+    status = (ctypes.c_uint64 * 2)()
+    _check(_lib.pk_debug_coverage_read(ctx, counts.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
+                                       n, status), ctx)
+    return counts.reshape(2, ctx.ny + 2, pitch), (int(status[0]), int(status[1]))
 
 
 def make_task(kind, n_sweeps=0, a=0.0, x=None, y=None, length=0):

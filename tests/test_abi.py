@@ -161,3 +161,16 @@ def test_gpu_tests_strip_widths_follow_the_shape_table():
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     assert mod.STREAM_TW == widths
+
+
+def test_coverage_build_exports_the_debug_calls():
+    """The coverage build is the same ABI plus include/pk_debug.h's calls; the
+    release library exports none of the latter."""
+    from iterative_stencil_solver_gb300 import build_ext
+    text = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", "pk_debug.h")).read(), flags=re.S)
+    debug = sorted(set(re.findall(r"\b(pk_debug_[a-z_]+)\s*\(", text)))
+    assert debug == ["pk_debug_coverage_read", "pk_debug_coverage_reset"]
+    cov = ctypes.CDLL(build_ext.build(coverage=True))
+    assert all(hasattr(cov, n) for n in debug + _declared_functions())
+    rel = ctypes.CDLL(build_ext.build())
+    assert not any(hasattr(rel, n) for n in debug)
