@@ -74,7 +74,8 @@ extern "C" {
 #define PK_FLAG_LAUNCH_PROBLEM_GRID 0x1u /* pk_run_sweeps_launch: one thread per float4, not the persistent grid */
 #define PK_FLAG_ALTERNATE_DIRECTION 0x2u /* STREAM: odd sweeps walk each band bottom-up (reuses L2);
                                             persistent three-sweep runs ordered by pass counters
-                                            walk every pass top-down regardless (faster there) */
+                                            on fields above four times L2 walk every pass
+                                            top-down regardless (faster there) */
 #define PK_FLAG_PROFILE_BARRIER 0x4u     /* record each CTA's total barrier wait (pk_barrier_wait_ns) */
 #define PK_FLAG_ONE_SWEEP_PER_PASS 0x8u  /* pk_run_sweeps: no temporal blocking; every pass advances
                                             one sweep (STREAM keeps stream_config's shape or 3) */

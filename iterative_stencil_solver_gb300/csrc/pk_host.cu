@@ -572,6 +572,11 @@ SweepParams base_params(pk_ctx *ctx) {
     return p;
 }
 
+// Bytes a STREAM pass touches: both field buffers and the source.
+long long working_set(const pk_ctx *ctx) {
+    return 2LL * (ctx->ny + 2) * ctx->pitch * 4 + (ctx->poisson ? (long long)ctx->ny * ctx->gpitch * 4 : 0);
+}
+
 // The pass-counter lists for a persistent STREAM launch of `shape` on
 // `grid` CTAs, written on the context's stream unless they are already
 // there.
@@ -752,16 +757,6 @@ int task_finish(pk_ctx *ctx) {
 // pay off whenever a run has two or more: the kernels shorten a pass where
 // the end would fall inside it, and a three-sweep pass runs past a residual
 // check (straddle) where a pass of fewer sweeps stops at it.
-//
-// Direction of the passes (PK_FLAG_ALTERNATE_DIRECTION): odd passes walk
-// their rows bottom-up so that a pass starts on the rows the previous one
-// wrote last, still in L2.  Three-sweep runs ordered by pass counters walk
-// every pass top-down instead (the flag is cleared for them where the
-// kernel is launched): their CTAs drift apart, the rows a CTA wrote last
-// are gone from L2 by the time it starts its next pass, and the same
-// direction measured 0.1-0.4% faster (16384^2 Laplace 113.1 against 113.6
-// us/sweep, 4096^2 Poisson checked every 10 sweeps 13.47 against 13.52);
-// the one-sweep shape keeps the alternation (313.6 against 314.6).
 //
 // Pass counters (persistent STREAM kernels of the one- and three-sweep
 // shapes): passes without a residual check wait only for the CTAs whose rows
@@ -955,7 +950,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     bool straddle, counters;
     choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
     p.pass_counters = counters ? 1 : 0;
-    if (counters && stream_depth(shape) == 3) p.alt_dir = 0;  // see choose_persistent's notes
+    if (stream_same_direction(counters, shape, working_set(ctx), ctx->l2_bytes)) p.alt_dir = 0;
     if (counters) {
         const int rc = ensure_pass_deps(ctx, shape, grid);
         if (rc != PK_OK) return rc;
@@ -1095,7 +1090,7 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
         p.bar_base = 0;
         p.profile = 0;
         p.pass_counters = counters ? 1 : 0;
-        if (counters && stream_depth(shape) == 3) p.alt_dir = 0;  // see choose_persistent's notes
+        if (stream_same_direction(counters, shape, working_set(ctx), ctx->l2_bytes)) p.alt_dir = 0;
         run_ids[q] = p.run_id;
         if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_t0[q], sc);
         if (e == cudaSuccess) e = launch_persistent(kernel, ctx->poisson, shape, grid, p, sc, straddle);

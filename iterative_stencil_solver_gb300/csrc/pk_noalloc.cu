@@ -203,7 +203,7 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     p.pass_done = sc->pass_done;
     p.pass_deps = sc->pass_deps;
     p.pass_counters = counters ? 1 : 0;
-    if (counters && depth == 3) p.alt_dir = 0;  // as pk_run_sweeps: every pass walks down
+    if (stream_same_direction(counters, cfg, resident, g_l2[dev])) p.alt_dir = 0;  // as pk_run_sweeps
     if (counters) {
         e = launch_pass_deps(nx, ny, cfg, (int)grid, sc->pass_deps, s);
         if (e != cudaSuccess) return fail(PK_ECUDA, "k_pass_deps launch", e);
