@@ -672,6 +672,23 @@ def test_pass_counters_bit_exact(pk, cfg, nx, ny, poisson):
         assert info2["barriers"] == info2["passes"] == info["passes"]
 
 
+def test_pass_counters_with_ctas_that_own_no_rows(pk):
+    # 100 CTAs of the one-sweep shape on 50 (strip, row) pairs: every other
+    # CTA owns nothing, passes through the loop all the same and publishes
+    # its counts, and the lists of the others run through it (a few entries)
+    nx, ny, cfg, grid = 3000, 50, 3, 100
+    lists = [pk.pk_stream_pass_deps(nx, ny, cfg, grid, b) for b in range(grid)]
+    assert max(len(l) for l in lists) <= 32 and min(len(l) for l in lists) == 0
+    u0 = inputs.random_field(nx, ny, seed=1310)
+    for n, tol, ce in ((13, 0.0, 0), (13, 1e-30, 4)):
+        want, oinfo = oracle.jacobi_run(u0, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, None, n, tol, ce, variant=2, stream_config=cfg, grid_override=grid)
+        assert info["grid"] == grid and info["pass_counters"] == 1
+        assert info["barriers"] == oinfo.n_checks
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
 def test_pass_counters_off_when_a_list_is_too_long(pk):
     # 300 CTAs of a three-sweep shape on 100 (strip, row) pairs: a CTA's list
     # runs through the CTAs that own no rows and reaches more entries than the
