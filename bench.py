@@ -589,16 +589,14 @@ def e2e_steps(pk, ctx, w, args, world, torch):
     out); returns the e2e record and the serial set/run/get number."""
     cells = w["nx"] * w["ny"]
     sweeps = w["sweeps"]
-    # e2e through the public API with pinned host buffers: every step
-    # uploads its field, sweeps and downloads its result.  pk_run_batch
-    # runs the steps as a pipeline (step i+1's upload and step i-1's
-    # download overlap step i's sweeps); the tensors are kept so their
-    # pages stay pinned.
-    host_in_t = torch.from_numpy(w["u0"]).pin_memory()
-    host_out_t = [torch.empty(w["u0"].shape, dtype=torch.float32).pin_memory()
-                  for _ in range(2)]
-    assert host_in_t.is_pinned() and all(t.is_pinned() for t in host_out_t)
-    host_in, host_out = host_in_t.numpy(), [t.numpy() for t in host_out_t]
+    # e2e through the public API with page-locked host buffers on 2 MB pages
+    # (pk_host_array): every step uploads its field, sweeps and downloads
+    # its result.  pk_run_batch runs the steps as a pipeline (step i+1's
+    # upload and step i-1's download overlap step i's sweeps).
+    host_in = pk.pk_host_array(w["u0"].shape)
+    host_in[...] = w["u0"]
+    host_out = [pk.pk_host_array(w["u0"].shape) for _ in range(2)]
+    host_in_t, host_out_t = torch.from_numpy(host_in), [torch.from_numpy(a) for a in host_out]
     pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
                     w["check_every"])
     dist_barrier(world)
@@ -625,9 +623,64 @@ def e2e_steps(pk, ctx, w, args, world, torch):
         serial_updates += cells * info["sweeps_done"]
     serial_s = dist_max(world, time.perf_counter() - t0)
     serial_value = dist_sum(world, serial_updates) / serial_s
+    link = host_link_gbs(torch, host_in_t, host_out_t[0])
+    link["huge_page_fraction"] = huge_page_fraction([host_in] + host_out)
+    sweeps_ms = statistics.median(i["device_us"] for i in infos) / 1e3
+    copy_ms = 2 * host_in_t.numel() * 4 / (link["both_gbs"] * 1e9) * 1e3
     return {"value": e2e_value, "seconds": e2e_s, "launches": e2e_launches,
-            "sweeps_ms_median": statistics.median(i["device_us"] for i in infos) / 1e3,
+            "sweeps_ms_median": sweeps_ms, "link": link,
+            # a step can go no faster than its sweeps or than both copies at
+            # this box's two-way link rate, whichever is longer
+            "bound_value": cells * sweeps / (max(sweeps_ms, copy_ms) * 1e-3),
             "serial_value": serial_value, "serial_steps": serial_steps}
+
+
+def huge_page_fraction(arrays):
+    """Share of the arrays' bytes that the kernel backs with transparent huge
+    pages (AnonHugePages of their mappings in /proc/self/smaps), or None
+    where that file cannot be read."""
+    spans = [(a.ctypes.data, a.ctypes.data + a.nbytes) for a in arrays]
+    total = sum(e - b for b, e in spans)
+    try:
+        huge, cur = 0, None
+        with open("/proc/self/smaps") as fh:
+            for line in fh:
+                head = line.split()[0]
+                if "-" in head and not head.endswith(":"):
+                    lo, hi = (int(x, 16) for x in head.split("-"))
+                    cur = (lo, hi) if any(lo < e and b < hi for b, e in spans) else None
+                elif cur and line.startswith("AnonHugePages:"):
+                    huge += int(line.split()[1]) * 1024
+        return min(1.0, huge / total) if total else None
+    except (OSError, ValueError):
+        return None
+
+
+def host_link_gbs(torch, host_in_t, host_out_t):
+    """This machine's host link with the e2e buffers: one field up, one down, and
+    both at once on two streams (GB/s, the best of three)."""
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d_in = torch.empty_like(host_in_t, device=dev)
+    d_out = torch.empty_like(host_out_t, device=dev)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    nbytes = host_in_t.numel() * 4
+    best = {"h2d_gbs": 0.0, "d2h_gbs": 0.0, "both_gbs": 0.0}
+    for _ in range(3):
+        for key in best:
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            if key in ("h2d_gbs", "both_gbs"):
+                with torch.cuda.stream(s1):
+                    d_in.copy_(host_in_t, non_blocking=True)
+            if key in ("d2h_gbs", "both_gbs"):
+                with torch.cuda.stream(s2):
+                    host_out_t.copy_(d_out, non_blocking=True)
+            torch.cuda.synchronize()
+            dt = time.perf_counter() - t0
+            moved = nbytes * (2 if key == "both_gbs" else 1)
+            best[key] = max(best[key], moved / dt / 1e9)
+    del d_in, d_out
+    return best
 
 
 # ---- main arm ----------------------------------------------------------------------
@@ -748,9 +801,12 @@ def main():
             "value": e2e["value"], "unit": UNIT,
             "h2d_bytes_per_step": int(w["u0"].nbytes),
             "d2h_bytes_per_step": int(w["u0"].nbytes),
-            "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps)",
+            "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps); "
+                   "host buffers from pk_host_alloc (page-locked, 2 MB pages)",
             "steps": args.steps, "seconds": e2e["seconds"], "gpu_launches": e2e["launches"],
-            "sweeps_ms_per_step_median": e2e["sweeps_ms_median"]},
+            "sweeps_ms_per_step_median": e2e["sweeps_ms_median"],
+            "host_link": e2e["link"], "bound_value": e2e["bound_value"],
+            "frac_of_bound": e2e["value"] / e2e["bound_value"]},
         "e2e_serial": None if e2e is None else {
             "value": e2e["serial_value"], "unit": UNIT, "steps": e2e["serial_steps"],
             "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"},

@@ -297,8 +297,9 @@ int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, p
  * goes up and problem i-1's result comes down, on two copy streams of the
  * context; the sweeps themselves run one after another on the context's
  * stream, so no two cooperative grids are ever in flight together.  Host
- * arrays should be page-locked (cudaHostAlloc / cudaHostRegister) for the
- * copies to overlap.  On first use the call allocates three field pairs of
+ * arrays should be page-locked (pk_host_alloc, or cudaHostAlloc /
+ * cudaHostRegister) for the copies to overlap, and on 2 MB pages
+ * (pk_host_alloc) for them to run at full rate in every batch.  On first use the call allocates three field pairs of
  * the context's layout (kept until pk_destroy); it neither reads nor
  * changes the context's own field.  Blocks until every result is on the
  * host.  Errors: PK_EINVAL, PK_EBUSY (task kernel live), PK_ENORESIDENT,
@@ -306,6 +307,24 @@ int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, p
  * PK_ECUDA. */
 int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *const *host_out,
                  int64_t n, float tol, int check_every, pk_run_info *infos);
+
+/* Page-locked HOST memory for the host arrays of pk_run_batch, pk_set_field
+ * and pk_get_field (a library convenience; the pages have no counterpart):
+ * `bytes` of zeroed memory.  Where the operating system backs all of it with
+ * 2 MB transparent huge pages (anonymous mmap on a 2 MB boundary, madvise
+ * MADV_HUGEPAGE, checked in /proc/self/smaps) the region is registered with
+ * cudaHostRegister; otherwise it comes from cudaHostAlloc.  On a GB300
+ * host, batches copying from cudaHostAlloc memory ran at full rate in some
+ * batches and 20-50% slower in others (the copy engines' translation of
+ * gigabytes of host pages); from 2 MB pages every batch ran at full rate,
+ * while registered small pages were slower than both.  *ptr receives the
+ * address; release it with pk_host_free only.  Needs a CUDA device.
+ * Errors: PK_EINVAL (bytes <= 0, ptr NULL), PK_ECUDA (*ptr is NULL). */
+int pk_host_alloc(int64_t bytes, void **ptr);
+
+/* Release memory from pk_host_alloc (NULL is a no-op).  Errors: PK_EINVAL
+ * (not an address pk_host_alloc returned), PK_ECUDA. */
+int pk_host_free(void *ptr);
 
 /* Copy the current iterate to / from a packed (ny+2) x (nx+2) HOST array.
  * pk_set_field writes buffer A (ring and interior), copies the ring into

@@ -23,10 +23,14 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <new>
+#include <mutex>
 #include <string>
 #include <thread>
+
+#include <sys/mman.h>
 
 #include "pk.h"
 #include "pk_debug.h"
@@ -1493,6 +1497,112 @@ int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, p
     PK_TRY(ctx, cudaEventRecord(ctx->ev1, ctx->stream));
     PK_TRY(ctx, cudaStreamSynchronize(ctx->stream));
     fill_info(ctx, info, k, res0, res_last, rmax_last, n_checks, PK_OK, ctx->rb_grid, kVariantDirect);
+    return PK_OK;
+}
+
+// ---- page-locked host memory on 2 MB pages --------------------------------
+
+namespace {
+// Regions handed out by pk_host_alloc: returned pointer -> (mapping, length),
+// mapping null for a cudaHostAlloc region.
+std::mutex g_host_mutex;
+std::map<void *, std::pair<void *, size_t>> g_host_regions;
+constexpr size_t kHugePage = size_t(2) << 20;
+
+// Bytes of [lo, hi) that the kernel backs with transparent huge pages
+// (AnonHugePages of the mappings that overlap it in /proc/self/smaps); -1
+// when the file cannot be read.
+long long huge_page_bytes(const char *lo, const char *hi) {
+    FILE *f = std::fopen("/proc/self/smaps", "r");
+    if (!f) return -1;
+    char line[512];
+    bool in = false;
+    long long huge = 0;
+    while (std::fgets(line, sizeof line, f)) {
+        unsigned long long a = 0, b = 0;
+        char dash = 0;
+        if (std::sscanf(line, "%llx%c%llx", &a, &dash, &b) == 3 && dash == '-') {
+            in = a < (unsigned long long)(uintptr_t)hi && (unsigned long long)(uintptr_t)lo < b;
+        } else if (in && std::strncmp(line, "AnonHugePages:", 14) == 0) {
+            huge += std::atoll(line + 14) * 1024;
+        }
+    }
+    std::fclose(f);
+    return huge;
+}
+}  // namespace
+
+int pk_host_alloc(int64_t bytes, void **ptr) {
+    if (!ptr) return PK_EINVAL;
+    *ptr = nullptr;
+    if (bytes <= 0) {
+        set_global_error("pk_host_alloc: bytes must be positive");
+        return PK_EINVAL;
+    }
+    const size_t len = ((size_t)bytes + kHugePage - 1) / kHugePage * kHugePage;
+    // First choice: anonymous memory on 2 MB pages, started on a 2 MB
+    // boundary (one huge page of slack), every page touched, then
+    // registered.  Kept only when the kernel backed all of it with huge
+    // pages: registered small pages copy far slower than cudaHostAlloc's.
+    void *map = mmap(nullptr, len + kHugePage, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    if (map != MAP_FAILED) {
+        char *base = static_cast<char *>(map);
+        char *start = base + (kHugePage - (reinterpret_cast<uintptr_t>(base) % kHugePage)) % kHugePage;
+        if (madvise(start, len, MADV_HUGEPAGE) == 0) {
+            std::memset(start, 0, len);
+            if (huge_page_bytes(start, start + len) >= (long long)len &&
+                cudaHostRegister(start, len, cudaHostRegisterDefault) == cudaSuccess) {
+                std::lock_guard<std::mutex> lock(g_host_mutex);
+                g_host_regions[start] = std::make_pair(map, len + kHugePage);
+                *ptr = start;
+                return PK_OK;
+            }
+            (void)cudaGetLastError();
+        }
+        munmap(map, len + kHugePage);
+    }
+    // Otherwise the driver's page-locked memory.
+    void *p = nullptr;
+    const cudaError_t e = cudaHostAlloc(&p, len, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        set_global_error((std::string("pk_host_alloc: cudaHostAlloc: ") + cudaGetErrorName(e)).c_str());
+        return PK_ECUDA;
+    }
+    std::memset(p, 0, len);
+    {
+        std::lock_guard<std::mutex> lock(g_host_mutex);
+        g_host_regions[p] = std::make_pair(nullptr, len);
+    }
+    *ptr = p;
+    return PK_OK;
+}
+
+int pk_host_free(void *ptr) {
+    if (!ptr) return PK_OK;
+    std::pair<void *, size_t> region;
+    {
+        std::lock_guard<std::mutex> lock(g_host_mutex);
+        auto it = g_host_regions.find(ptr);
+        if (it == g_host_regions.end()) {
+            set_global_error("pk_host_free: not a pointer pk_host_alloc returned");
+            return PK_EINVAL;
+        }
+        region = it->second;
+        g_host_regions.erase(it);
+    }
+    cudaError_t e;
+    if (region.first) {
+        e = cudaHostUnregister(ptr);
+        munmap(region.first, region.second);
+    } else {
+        e = cudaFreeHost(ptr);
+    }
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        set_global_error((std::string("pk_host_free: ") + cudaGetErrorName(e)).c_str());
+        return PK_ECUDA;
+    }
     return PK_OK;
 }
 

@@ -155,6 +155,8 @@ _SIGS = {
     "pk_stream_pass_deps": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
                                            ctypes.c_int]),
+    "pk_host_alloc": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(_VP)]),
+    "pk_host_free": (ctypes.c_int, [_VP]),
     "pk_submit_task": (ctypes.c_int, [_VP, ctypes.POINTER(pk_task),
                                       ctypes.POINTER(ctypes.c_uint64)]),
     "pk_poll": (ctypes.c_int, [_VP, ctypes.c_uint64]),
@@ -390,6 +392,28 @@ def pk_debug_coverage_read(ctx):
     _check(_lib.pk_debug_coverage_read(ctx, counts.ctypes.data_as(ctypes.POINTER(ctypes.c_uint32)),
                                        n, status), ctx)
     return counts.reshape(2, ctx.ny + 2, pitch), (int(status[0]), int(status[1]))
+
+
+def pk_host_alloc(nbytes):
+    """Address of `nbytes` of page-locked host memory on 2 MB pages."""
+    ptr = _VP()
+    _check(_lib.pk_host_alloc(nbytes, ctypes.byref(ptr)))
+    return ptr.value
+
+
+def pk_host_free(ptr):
+    _check(_lib.pk_host_free(ptr))
+
+
+def pk_host_array(shape, dtype=np.float32):
+    """A zeroed numpy array in pk_host_alloc memory; the memory is released
+    (pk_host_free) when the array and every view of it are gone."""
+    import weakref
+    nbytes = int(np.prod(shape)) * np.dtype(dtype).itemsize
+    ptr = pk_host_alloc(max(nbytes, 1))
+    buf = (ctypes.c_char * max(nbytes, 1)).from_address(ptr)
+    weakref.finalize(buf, _lib.pk_host_free, ptr)
+    return np.frombuffer(buf, dtype=dtype, count=int(np.prod(shape))).reshape(shape)
 
 
 def make_task(kind, n_sweeps=0, a=0.0, x=None, y=None, length=0):

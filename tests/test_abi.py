@@ -174,3 +174,16 @@ def test_coverage_build_exports_the_debug_calls():
     assert all(hasattr(cov, n) for n in debug + _declared_functions())
     rel = ctypes.CDLL(build_ext.build())
     assert not any(hasattr(rel, n) for n in debug)
+
+
+def test_host_alloc_refuses_bad_arguments(pk):
+    lib = ctypes.CDLL(pk.LIB_PATH)
+    lib.pk_host_alloc.argtypes = pk._SIGS["pk_host_alloc"][1]
+    lib.pk_host_free.argtypes = pk._SIGS["pk_host_free"][1]
+    ptr = ctypes.c_void_p(1)
+    assert lib.pk_host_alloc(0, ctypes.byref(ptr)) == pk.PK_EINVAL and not ptr.value
+    assert lib.pk_host_alloc(-5, ctypes.byref(ptr)) == pk.PK_EINVAL
+    assert lib.pk_host_alloc(64, None) == pk.PK_EINVAL
+    assert lib.pk_host_free(None) == pk.PK_OK
+    junk = ctypes.create_string_buffer(64)
+    assert lib.pk_host_free(ctypes.cast(junk, ctypes.c_void_p)) == pk.PK_EINVAL

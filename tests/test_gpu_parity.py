@@ -672,6 +672,35 @@ def test_pass_counters_bit_exact(pk, cfg, nx, ny, poisson):
         assert info2["barriers"] == info2["passes"] == info["passes"]
 
 
+def test_host_alloc_buffers_in_a_batch(pk):
+    """pk_host_alloc memory (page-locked, on 2 MB pages where granted) as the
+    host arrays of pk_run_batch: zeroed, results bit for bit the oracle's;
+    freed when the arrays go, and a second free is refused."""
+    import gc
+    nx, ny = 700, 300
+    fields = [inputs.random_field(nx, ny, seed=1500 + i) for i in range(4)]
+    ins = [pk.pk_host_array(f.shape) for f in fields]
+    outs = [pk.pk_host_array(f.shape) for f in fields]
+    for a in ins + outs:
+        assert a.ctypes.data % 4096 == 0 and not a.any()
+    for a, f in zip(ins, fields):
+        a[...] = f
+    ctx = pk.pk_create(nx, ny, fields[0], None)
+    try:
+        pk.pk_run_batch(ctx, ins, outs, 17, 0.0, 0)
+    finally:
+        pk.pk_destroy(ctx)
+    for f, o in zip(fields, outs):
+        assert_same_bits(o, oracle.jacobi_run(f, n=17)[0])
+    ptr = pk.pk_host_alloc(1000)
+    pk.pk_host_free(ptr)
+    with pytest.raises(pk.PkError) as e:
+        pk.pk_host_free(ptr)
+    assert e.value.code == pk.PK_EINVAL
+    del ins, outs
+    gc.collect()
+
+
 def test_pass_counters_with_ctas_that_own_no_rows(pk):
     # 100 CTAs of the one-sweep shape on 50 (strip, row) pairs: every other
     # CTA owns nothing, passes through the loop all the same and publishes
