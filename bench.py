@@ -288,8 +288,9 @@ class ClockSampler:
 
 # ---- CPU oracle timing ---------------------------------------------------------
 
-def oracle_sample(w, target_s=10.0, max_rows=None):
-    """Time the single-threaded oracle on a band of the workload's rows.
+def oracle_sample(w, target_s=10.0, max_rows=None, threads=1):
+    """Time the oracle (single-threaded unless `threads` > 1: its OpenMP split
+    of the row loop, bit-identical) on a band of the workload's rows.
 
     The band keeps the full row width; its top and bottom rows act as its
     ring.  Returns (cell-updates/s, description, seconds)."""
@@ -300,15 +301,15 @@ def oracle_sample(w, target_s=10.0, max_rows=None):
     f = None if w["f"] is None else np.ascontiguousarray(w["f"][:ny])
     h2 = oracle.h2(nx)
     t0 = time.perf_counter()
-    oracle.jacobi_run(band, f=f, n=2, h2v=h2, threads=1)
+    oracle.jacobi_run(band, f=f, n=2, h2v=h2, threads=threads)
     per_sweep = max((time.perf_counter() - t0) / 2.0, 1e-6)
     sweeps = int(max(1, min(w["sweeps"], target_s / per_sweep)))
     t0 = time.perf_counter()
-    oracle.jacobi_run(band, f=f, n=sweeps, h2v=h2, threads=1)
+    oracle.jacobi_run(band, f=f, n=sweeps, h2v=h2, threads=threads)
     dt = time.perf_counter() - t0
     updates = float(nx) * ny * sweeps
-    desc = "%d sweeps over a %d x %d band of the %d x %d workload, 1 thread" % (
-        sweeps, nx, ny, w["nx"], w["ny"])
+    desc = "%d sweeps over a %d x %d band of the %d x %d workload, %d thread%s" % (
+        sweeps, nx, ny, w["nx"], w["ny"], threads, "s" if threads > 1 else "")
     return updates / dt, desc, dt
 
 
@@ -816,6 +817,14 @@ def main():
         v, desc, dt = oracle_sample(w, target_s=10.0, max_rows=min(ny, 2048))
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": desc, "seconds": dt}
+        # context: the same oracle with its OpenMP split of the row loop on
+        # every host core (bit-identical per cell)
+        import oracle
+        ncpu = os.cpu_count() or 1
+        if oracle.has_openmp() and ncpu > 1:
+            va, desca, dta = oracle_sample(w, target_s=3.0, max_rows=min(ny, 2048), threads=ncpu)
+            line["cpu_baseline"]["all_cores"] = {"value": va, "cores": ncpu, "sample": desca,
+                                                 "seconds": dta}
     if not args.no_extras:
         line["extras"] = latency_extras(pk)
     print(json.dumps(line), flush=True)
