@@ -969,6 +969,28 @@ def test_barrier_wait_profile(pk):
         pk.pk_destroy(ctx)
 
 
+@pytest.mark.parametrize("counters", [True, False], ids=["pass-counters", "barrier"])
+def test_stream_wait_profile(pk, counters):
+    # the default three-sweep plan: waits at the pass counters (or at the
+    # barrier after every pass) are recorded per CTA; the field keeps its bits
+    nx, ny = 3000, 400
+    u0 = inputs.random_field(nx, ny, seed=18)
+    flags = pk.PK_FLAG_PROFILE_BARRIER | pk.PK_FLAG_ALTERNATE_DIRECTION | (
+        0 if counters else pk.PK_FLAG_BARRIER_EVERY_PASS)
+    ctx = pk.pk_create(nx, ny, u0, None, pk.pk_options_default(variant=2, flags=flags))
+    try:
+        info = pk.pk_run_sweeps(ctx, 30)
+        waits = pk.pk_barrier_wait_ns(ctx)
+        got = pk.pk_get_field(ctx)
+    finally:
+        pk.pk_destroy(ctx)
+    assert info["pass_counters"] == (1 if counters else 0) and info["passes"] == 10
+    assert len(waits) == info["grid"]
+    assert (waits >= 0).all() and waits.max() > 0
+    assert waits.max() < info["device_us"] * 1e3 * 1.05
+    assert_same_bits(got, oracle.jacobi_run(u0, n=30)[0])
+
+
 def test_stream_ring_refill_race_regression(pk):
     """One sweep per launch on the STREAM shape with three CTAs per SM,
     checked after every sweep against the DIRECT path (bit-exact, generic
