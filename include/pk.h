@@ -235,7 +235,8 @@ int pk_create_device(int nx, int ny, float *u_a, float *u_b, int64_t pitch, cons
  * rows it reads (pk_stream_pass_deps) have finished the previous one; every
  * check still ends at the grid barrier, behind which all CTAs reach the same
  * exit decision (PK_FLAG_BARRIER_EVERY_PASS: a barrier after every pass;
- * the same bits either way).  Runs up to n sweeps.  With tol > 0 and check_every > 0 the residual
+ * the same bits either way).  Runs up to n sweeps.  With tol > 0 and
+ * check_every > 0 the residual
  * r = fl32(t - 4C) of iterate k (t as in the update, before the 1/4) is
  * reduced in the kernel when k % check_every == 0 (L2 norm: exact squares
  * summed per thread as a float pair, across threads in fp64, to about 1e-12
@@ -345,19 +346,32 @@ int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *cu
  * kernel.  Any output may be NULL. */
 int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max);
 
+/* How a STREAM grid deals its rows out: the (strip, row) pairs of an
+ * nx x ny field (strips of the shape's width, the last one ragged when nx is
+ * not a multiple of it; R = strips * ny pairs, strip-major) go to `grid` CTAs
+ * of shape stream_config in contiguous runs, CTA c taking pairs
+ * starts[c] .. starts[c+1] - 1.  Every pair costs the same, except in
+ * three-sweep Poisson shapes, where a ragged last strip's pairs cost 38/20
+ * of a full strip's (their rolled generic step): starts[c] is the last pair
+ * whose cumulative cost C satisfies C * grid <= total cost * c, which for
+ * equal costs is floor(R c / grid).  Writes grid + 1 entries to the HOST
+ * array starts.  Host arithmetic only (no device call).  Errors: PK_EINVAL
+ * (sizes, shape or grid out of range, starts NULL). */
+int pk_stream_split(int nx, int ny, int stream_config, int poisson, int grid, int64_t *starts);
+
 /* The CTAs whose pass counters CTA `cta` of a persistent STREAM kernel
- * waits on before a pass (pk_run_info.pass_counters): the owners of the
- * rows within D rows of its own (D = the shape's sweeps per pass) in its
- * strip and in the strips on either side, the (strip, row) pairs of an
- * nx x ny field being dealt out to `grid` CTAs of shape stream_config in
- * contiguous runs of R*c/grid .. R*(c+1)/grid - 1.  They are also the CTAs
- * that read `cta`'s rows.  The list is a concatenation of CTA ranges and may
- * name a CTA twice.  Writes min(length, cap) entries to the HOST array out
- * (NULL when cap is 0) and returns the length; a run uses pass counters only
+ * waits on before a pass (pk_run_info.pass_counters): the owners, under
+ * pk_stream_split's runs (poisson as there), of the rows within D rows of
+ * its own (D = the shape's sweeps per pass) in its strip and in the strips
+ * on either side.  They are also the CTAs that read `cta`'s rows.  The list
+ * is a concatenation of CTA ranges and may name a CTA twice.  Writes
+ * min(length, cap) entries to the HOST array out (NULL when cap is 0) and
+ * returns the length; a run uses pass counters only
  * when every CTA's list has at most 32 entries.  Host arithmetic only (no
  * device call).  Errors: PK_EINVAL (sizes, shape, grid or cta out of
  * range, cap < 0). */
-int pk_stream_pass_deps(int nx, int ny, int stream_config, int grid, int cta, int32_t *out, int cap);
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int poisson, int grid, int cta, int32_t *out,
+                        int cap);
 
 /* Post a task to the mapped-pinned mailbox ([P1] "Base implementation",
  * "Thread synchronization", "Atomics and memory ordering"; [P3] "Device

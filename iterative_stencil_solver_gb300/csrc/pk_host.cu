@@ -587,7 +587,7 @@ long long working_set(const pk_ctx *ctx) {
 int ensure_pass_deps(pk_ctx *ctx, int shape, int grid) {
     const auto key = std::make_pair(shape, grid);
     if (ctx->deps_key == key) return PK_OK;
-    cudaError_t e = launch_pass_deps(ctx->nx, ctx->ny, shape, grid, ctx->pass_deps, ctx->stream);
+    cudaError_t e = launch_pass_deps(ctx->nx, ctx->ny, shape, ctx->poisson, grid, ctx->pass_deps, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "k_pass_deps launch");
     ctx->deps_key = key;
     return PK_OK;
@@ -799,7 +799,8 @@ void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *
         const auto key = std::make_pair(shape, grid);
         auto it = ctx->counters_fit.find(key);
         if (it == ctx->counters_fit.end())
-            it = ctx->counters_fit.emplace(key, stream_counters_fit(ctx->nx, ctx->ny, shape, grid)).first;
+            it = ctx->counters_fit.emplace(key, stream_counters_fit(ctx->nx, ctx->ny, shape, ctx->poisson,
+                                                                   grid)).first;
         counters = it->second;
     }
     *counters_out = counters;
@@ -1642,16 +1643,25 @@ int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_
     return PK_OK;
 }
 
-int pk_stream_pass_deps(int nx, int ny, int stream_config, int grid, int cta, int32_t *out, int cap) {
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int poisson, int grid, int cta, int32_t *out,
+                        int cap) {
     if (nx <= 0 || ny <= 0 || stream_config < 0 || stream_config >= kNumStreamConfigs || grid <= 0 ||
         cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out))
         return PK_EINVAL;
-    const int tw = stream_tw(stream_config);
-    const int strips = (nx + tw - 1) / tw;
+    const StreamSplit sp = stream_split_for(nx, ny, stream_config, poisson != 0, grid);
     const int halo = stream_depth(stream_config);
-    const int n = stream_pass_ndeps(strips, ny, grid, cta, halo);
-    for (int i = 0; i < n && i < cap; ++i) out[i] = stream_pass_dep(strips, ny, grid, cta, halo, i);
+    const int n = stream_pass_ndeps(sp, ny, cta, halo);
+    for (int i = 0; i < n && i < cap; ++i) out[i] = stream_pass_dep(sp, ny, cta, halo, i);
     return n;
+}
+
+int pk_stream_split(int nx, int ny, int stream_config, int poisson, int grid, int64_t *starts) {
+    if (nx <= 0 || ny <= 0 || stream_config < 0 || stream_config >= kNumStreamConfigs || grid <= 0 ||
+        !starts)
+        return PK_EINVAL;
+    const StreamSplit sp = stream_split_for(nx, ny, stream_config, poisson != 0, grid);
+    for (int c = 0; c <= grid; ++c) starts[c] = split_start(sp, c);
+    return PK_OK;
 }
 
 // ---- mailbox ----------------------------------------------------------------

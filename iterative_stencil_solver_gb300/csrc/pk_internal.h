@@ -85,28 +85,81 @@ struct SweepParams {
     unsigned long long *cov_status;
 };
 
+// How a STREAM grid deals out the R = strips * ny (strip, row) pairs, in
+// strip-major order: CTA c takes the contiguous run [start(c), start(c+1)).
+// Every pair costs w_full, except that the pairs of a ragged last strip
+// (one narrower than the shape's strip width) cost w_last; start(c) is the
+// last pair whose cumulative cost C satisfies C * G <= total * c, so that
+// equal costs give floor(R c / G) and unequal ones give the CTAs holding
+// costly pairs fewer of them.
+struct StreamSplit {
+    long long R;      // pairs
+    long long F;      // pairs before the ragged last strip's (R when there is none)
+    long long T;      // total cost: w_full F + w_last (R - F)
+    int G;
+    int w_full, w_last;
+};
+__host__ __device__ inline StreamSplit stream_split(int strips, int ny, int G, bool ragged_last,
+                                                    int w_full, int w_last) {
+    StreamSplit s;
+    s.R = (long long)strips * ny;
+    s.F = ragged_last ? s.R - ny : s.R;
+    s.G = G;
+    s.w_full = w_full;
+    s.w_last = w_last;
+    s.T = (long long)w_full * s.F + (long long)w_last * (s.R - s.F);
+    return s;
+}
+__host__ __device__ inline long long split_start(const StreamSplit &s, int c) {
+    const long long num = s.T * c;
+    const long long head = (long long)s.w_full * s.F * s.G;
+    if (num <= head) return num / ((long long)s.G * s.w_full);
+    return s.F + (num - head) / ((long long)s.G * s.w_last);
+}
+// The CTA whose run holds pair pos (one that owns at least one pair).
+__host__ __device__ inline long long split_owner(const StreamSplit &s, long long pos) {
+    const long long cost = pos < s.F ? (long long)s.w_full * pos
+                                     : (long long)s.w_full * s.F + (long long)s.w_last * (pos - s.F);
+    long long c = cost * s.G / s.T;
+    if (c > s.G - 1) c = s.G - 1;
+    while (c + 1 < s.G && split_start(s, (int)c + 1) <= pos) ++c;
+    while (c > 0 && split_start(s, (int)c) > pos) --c;
+    return c;
+}
+// The cost of a ragged last strip's pairs relative to full ones, in 20ths:
+// the Poisson three-sweep step takes its rolled generic form on a ragged
+// strip (an unrolled copy for it pushed the kernel's row windows onto the
+// stack).  Measured with pass counters on GB300 (us/sweep at 4000^2, 4097^2,
+// 3584^2, 8000^2): equal costs 20.4, 25.8, 18.4, 76.6; 29/20 15.9, 19.6,
+// 14.4, 56.6; 35/20 14.2, 17.6, 12.9, 49.2; 40/20 14.5, 17.2, 13.2, 46.9;
+// 46/20 15.1, 18.1, 13.8, 48.3.  The other shapes' ragged strips cost what
+// full ones do.
+constexpr int kSplitUnit = 20;
+constexpr int kSplitRaggedPoisson3 = 38;
+// The split of a STREAM grid of G CTAs and strips `tw` columns wide, the
+// same on the host and in the kernels.
+__host__ __device__ inline StreamSplit stream_split_of(int nx, int ny, int tw, int depth, bool poisson,
+                                                       int G) {
+    const bool ragged = nx % tw != 0;
+    const int w_last = poisson && depth == 3 && ragged ? kSplitRaggedPoisson3 : kSplitUnit;
+    return stream_split((nx + tw - 1) / tw, ny, G, ragged, kSplitUnit, w_last);
+}
+
 // The CTAs whose rows CTA b of a STREAM pass reads, which are also the CTAs
 // that read b's rows (the relation is symmetric): the owners of the rows
 // within `halo` rows of b's rows, in b's strip and in the strips on either
 // side (a row segment carries four columns of each neighbouring strip).
-// Rows are dealt out as the STREAM kernel deals them: the R = strips * ny
-// (strip, row) pairs in strip-major order, CTA c taking [R c / G,
-// R (c + 1) / G).  The set is walked as a list of CTA ranges, one per
-// (segment of b's run, strip), b itself left out; a CTA can appear in two
-// ranges, and waiting on it twice is harmless, so the list is not reduced.
-__host__ __device__ inline long long stream_pair_owner(long long pos, long long R, int G) {
-    long long c = pos * G / R;
-    while (c + 1 < G && R * (c + 1) / G <= pos) ++c;
-    while (c > 0 && R * c / G > pos) --c;
-    return c;
-}
+// Rows are dealt out as stream_split says.  The set is walked as a list of
+// CTA ranges, one per (segment of b's run, strip), b itself left out; a CTA
+// can appear in two ranges, and waiting on it twice is harmless, so the list
+// is not reduced.
 // Calls visit(first, last) for each range; stops early when visit returns
 // false.
 template <class Visit>
-__host__ __device__ inline void stream_pass_dep_ranges(int strips, int ny, int G, int b, int halo,
+__host__ __device__ inline void stream_pass_dep_ranges(const StreamSplit &sp, int ny, int b, int halo,
                                                        Visit &&visit) {
-    const long long R = (long long)strips * ny;
-    const long long L0 = R * b / G, L1 = R * (b + 1) / G;
+    const int strips = (int)(sp.R / ny);
+    const long long L0 = split_start(sp, b), L1 = split_start(sp, b + 1);
     for (long long pos = L0; pos < L1;) {
         const int s = (int)(pos / ny);
         const long long seg_end = ((long long)s + 1) * ny < L1 ? ((long long)s + 1) * ny : L1;
@@ -115,26 +168,25 @@ __host__ __device__ inline void stream_pass_dep_ranges(int strips, int ny, int G
         const int hi = r1 + halo > ny - 1 ? ny - 1 : r1 + halo;
         for (int ss = s - 1; ss <= s + 1; ++ss) {
             if (ss < 0 || ss >= strips) continue;
-            if (!visit(stream_pair_owner((long long)ss * ny + lo, R, G),
-                       stream_pair_owner((long long)ss * ny + hi, R, G)))
+            if (!visit(split_owner(sp, (long long)ss * ny + lo), split_owner(sp, (long long)ss * ny + hi)))
                 return;
         }
         pos = seg_end;
     }
 }
 // Length of CTA b's list.
-__host__ __device__ inline int stream_pass_ndeps(int strips, int ny, int G, int b, int halo) {
+__host__ __device__ inline int stream_pass_ndeps(const StreamSplit &sp, int ny, int b, int halo) {
     int n = 0;
-    stream_pass_dep_ranges(strips, ny, G, b, halo, [&](long long c0, long long c1) {
+    stream_pass_dep_ranges(sp, ny, b, halo, [&](long long c0, long long c1) {
         n += (int)(c1 - c0 + 1) - (c0 <= b && b <= c1 ? 1 : 0);
         return true;
     });
     return n;
 }
 // Entry i of CTA b's list, or -1 past its end.
-__host__ __device__ inline int stream_pass_dep(int strips, int ny, int G, int b, int halo, int i) {
+__host__ __device__ inline int stream_pass_dep(const StreamSplit &sp, int ny, int b, int halo, int i) {
     int found = -1;
-    stream_pass_dep_ranges(strips, ny, G, b, halo, [&](long long c0, long long c1) {
+    stream_pass_dep_ranges(sp, ny, b, halo, [&](long long c0, long long c1) {
         for (long long c = c0; c <= c1; ++c) {
             if (c == b) continue;
             if (i-- == 0) {
@@ -249,12 +301,14 @@ inline bool stream_same_direction(bool counters, int cfg, long long working_set,
 
 // Whether every CTA of a persistent STREAM grid of shape cfg has at most
 // kMaxPassDeps entries in its pass-counter list (one producer lane each).
-inline bool stream_counters_fit(int nx, int ny, int cfg, int grid) {
+inline StreamSplit stream_split_for(int nx, int ny, int cfg, bool poisson, int G) {
+    return stream_split_of(nx, ny, stream_tw(cfg), stream_depth(cfg), poisson, G);
+}
+inline bool stream_counters_fit(int nx, int ny, int cfg, bool poisson, int grid) {
     if (grid > kMaxPassDepsGrid) return false;
-    const int tw = stream_tw(cfg);
-    const int strips = (nx + tw - 1) / tw;
+    const StreamSplit sp = stream_split_for(nx, ny, cfg, poisson, grid);
     for (int b = 0; b < grid; ++b)
-        if (stream_pass_ndeps(strips, ny, grid, b, stream_depth(cfg)) > kMaxPassDeps) return false;
+        if (stream_pass_ndeps(sp, ny, b, stream_depth(cfg)) > kMaxPassDeps) return false;
     return true;
 }
 
@@ -387,7 +441,7 @@ cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *ba
                                   cudaStream_t s);
 // Writes the pass-counter lists of a persistent STREAM grid of shape cfg on
 // an nx x ny field into out (32 entries per CTA, grid * 32 shorts).
-cudaError_t launch_pass_deps(int nx, int ny, int cfg, int grid, short *out, cudaStream_t s);
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool poisson, int grid, short *out, cudaStream_t s);
 cudaError_t launch_task(bool poisson, int cluster, const TaskParams &p, cudaStream_t s);
 cudaError_t task_clusters_fit(bool poisson, int cluster, int *n);
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,

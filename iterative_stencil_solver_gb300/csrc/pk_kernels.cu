@@ -899,14 +899,16 @@ __global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar
 }
 
 // One CTA per sweep CTA, one thread per list entry.
-__global__ void __launch_bounds__(32) k_pass_deps(int strips, int ny, int halo, short *out) {
+__global__ void __launch_bounds__(32) k_pass_deps(int nx, int ny, int tw, int depth, int poisson,
+                                                  short *out) {
+    const StreamSplit sp = stream_split_of(nx, ny, tw, depth, poisson != 0, (int)gridDim.x);
     out[(size_t)blockIdx.x * kMaxPassDeps + threadIdx.x] =
-        (short)stream_pass_dep(strips, ny, (int)gridDim.x, (int)blockIdx.x, halo, (int)threadIdx.x);
+        (short)stream_pass_dep(sp, ny, (int)blockIdx.x, depth, (int)threadIdx.x);
 }
 
-cudaError_t launch_pass_deps(int nx, int ny, int cfg, int grid, short *out, cudaStream_t s) {
-    const int tw = stream_tw(cfg);
-    k_pass_deps<<<grid, kMaxPassDeps, 0, s>>>((nx + tw - 1) / tw, ny, stream_depth(cfg), out);
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool poisson, int grid, short *out, cudaStream_t s) {
+    k_pass_deps<<<grid, kMaxPassDeps, 0, s>>>(nx, ny, stream_tw(cfg), stream_depth(cfg), poisson ? 1 : 0,
+                                              out);
     return cudaGetLastError();
 }
 

@@ -24,8 +24,9 @@ namespace {
 // ===========================================================================
 // STREAM sweep ("Cache-line aware tiling and iteration", the N = 10001
 // variant, rebuilt around TMA): the domain is cut into strips of TW interior
-// columns; (strip, row) pairs are split evenly, in contiguous runs, over the
-// CTAs.  Each CTA walks its run row by row: one producer thread streams
+// columns; (strip, row) pairs are dealt out in contiguous runs over the CTAs,
+// by count or, where a ragged last strip's rows cost more, by cost
+// (stream_split).  Each CTA walks its run row by row: one producer thread streams
 // every input row segment (with a 16-byte halo on each side) into a
 // STAGES-deep shared-memory ring with cp.async.bulk, and CONS consumer
 // threads keep a three-row window (previous, centre, next) in registers,
@@ -65,6 +66,28 @@ struct SCfg {
     static_assert((STAGES & (STAGES - 1)) == 0 && STAGES <= 16, "stages: power of two <= 16");
     static_assert(DEPTH >= 1 && DEPTH <= 3, "one to three sweeps per pass");
 };
+
+// This CTA's run of (strip, row) pairs, [s_stream_run[0], s_stream_run[1]),
+// in the shapes whose split weighs a ragged last strip's rows (three-sweep
+// Poisson; stream_split_of): fixed for a launch, so thread 0 works it out
+// once, before the passes (stream_run_setup).  The other shapes split by
+// count, R c / G, in the pass itself, as before: reading the bounds from
+// shared memory there cost the Laplace three-sweep kernels a spill.
+__shared__ long long s_stream_run[2];
+
+__device__ __noinline__ void stream_run_bounds(int nx, int ny, int tw, int depth, bool poisson,
+                                               long long *run) {
+    const StreamSplit split = stream_split_of(nx, ny, tw, depth, poisson, (int)gridDim.x);
+    run[0] = split_start(split, (int)blockIdx.x);
+    run[1] = split_start(split, (int)blockIdx.x + 1);
+}
+
+template <class C, bool POISSON>
+__device__ __forceinline__ void stream_run_setup(const SweepParams &p) {
+    if constexpr (POISSON && C::kDepth == 3) {
+        if (threadIdx.x == 0) stream_run_bounds(p.nx, p.ny, C::TW, C::kDepth, POISSON, s_stream_run);
+    }
+}
 
 struct StreamState {
     uint64_t *full;
@@ -859,10 +882,16 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
                                             int dir, StreamState &st, double &s2, float &rmax,
                                             int cs = 0) {
     const int nx = p.nx, ny = p.ny;
-    const int strips = (nx + C::TW - 1) / C::TW;
-    const long long R = (long long)strips * ny;
-    const long long L0 = R * blockIdx.x / gridDim.x;
-    const long long L1 = R * (blockIdx.x + 1) / gridDim.x;
+    long long L0, L1;
+    if constexpr (POISSON && C::kDepth == 3) {
+        L0 = s_stream_run[0];
+        L1 = s_stream_run[1];
+    } else {  // split by count (stream_split_of gives the same for these shapes)
+        const int strips = (nx + C::TW - 1) / C::TW;
+        const long long R = (long long)strips * ny;
+        L0 = R * blockIdx.x / gridDim.x;
+        L1 = R * (blockIdx.x + 1) / gridDim.x;
+    }
     const bool producer_warp = threadIdx.x >= C::kCons;
     long long pos = dir > 0 ? L0 : L1 - 1;
     long long remaining = L1 - L0;
@@ -964,7 +993,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
     __shared__ int s_dep[32];
     __shared__ int s_wait_ok;
     __shared__ unsigned long long s_wait_ns;
-    StreamState st = stream_setup<C>(smem);
+    stream_run_setup<C, POISSON>(p);
+    StreamState st = stream_setup<C>(smem);  // (its block barrier publishes the run)
     if (threadIdx.x >= C::kCons) {
         s_dep[threadIdx.x & 31u] = -2;  // not fetched yet
         if (threadIdx.x == C::kCons) s_wait_ns = 0ull;
@@ -991,7 +1021,8 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
 template <class C, bool POISSON>
 __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_once_stream(SweepParams p) {
     extern __shared__ __align__(128) unsigned char smem[];
-    StreamState st = stream_setup<C>(smem);
+    stream_run_setup<C, POISSON>(p);
+    StreamState st = stream_setup<C>(smem);  // (its block barrier publishes the run)
     double s2 = 0.0;
     float rmax = 0.f;
     const int dir = (p.alt_dir && (p.pass_k & 1)) ? -1 : 1;

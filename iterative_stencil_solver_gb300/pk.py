@@ -153,8 +153,10 @@ _SIGS = {
     "pk_get_plan": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
                                    ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)]),
     "pk_stream_pass_deps": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                                           ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
+                                           ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32),
                                            ctypes.c_int]),
+    "pk_stream_split": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_int, _I64P]),
     "pk_host_alloc": (ctypes.c_int, [ctypes.c_int64, ctypes.POINTER(_VP)]),
     "pk_host_free": (ctypes.c_int, [_VP]),
     "pk_submit_task": (ctypes.c_int, [_VP, ctypes.POINTER(pk_task),
@@ -362,15 +364,26 @@ def pk_get_plan(ctx):
     return {"variant": v.value, "grid": g.value, "task_grid": tg.value, "coop_max": cm.value}
 
 
-def pk_stream_pass_deps(nx, ny, stream_config, grid, cta):
+def pk_stream_pass_deps(nx, ny, stream_config, grid, cta, poisson=False):
     """The CTAs whose pass counters CTA `cta` of a persistent STREAM grid
     waits on (host arithmetic; no device needed)."""
-    n = _lib.pk_stream_pass_deps(nx, ny, stream_config, grid, cta, None, 0)
+    n = _lib.pk_stream_pass_deps(nx, ny, stream_config, int(poisson), grid, cta, None, 0)
     if n < 0:
         raise PkError(n, "pk_stream_pass_deps: bad arguments")
     out = (ctypes.c_int32 * max(n, 1))()
-    _lib.pk_stream_pass_deps(nx, ny, stream_config, grid, cta, out, n)
+    _lib.pk_stream_pass_deps(nx, ny, stream_config, int(poisson), grid, cta, out, n)
     return list(out[:n])
+
+
+def pk_stream_split(nx, ny, stream_config, grid, poisson=False):
+    """First (strip, row) pair of each CTA's run, and R at the end (grid + 1
+    entries; host arithmetic)."""
+    starts = np.zeros(grid + 1, dtype=np.int64)
+    rc = _lib.pk_stream_split(nx, ny, stream_config, int(poisson), grid,
+                              starts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+    if rc < 0:
+        raise PkError(rc, "pk_stream_split: bad arguments")
+    return starts
 
 
 def has_coverage():

@@ -1,6 +1,7 @@
-"""The pass-counter neighbour lists of the persistent STREAM kernels, on the
-CPU: pk_stream_pass_deps against a brute-force walk over the (strip, row)
-partition.
+"""How the STREAM kernels deal out their rows, and the pass-counter
+neighbour lists that follow from it, on the CPU: pk_stream_split against the
+split's definition from per-pair costs (computed here with numpy), and
+pk_stream_pass_deps against a brute-force walk over that partition.
 
 A STREAM pass of CTA b reads the rows within D rows of its own (D = sweeps
 per pass of the shape) in its strip and, through the four columns a row
@@ -39,20 +40,34 @@ def _shapes():
 SHAPES = _shapes()
 
 
-def empty_ctas(nx, ny, cfg, grid):
-    tw, _ = SHAPES[cfg]
-    R = ((nx + tw - 1) // tw) * ny
-    return {c for c in range(grid) if R * c // grid == R * (c + 1) // grid}
+def brute_starts(nx, ny, cfg, grid, poisson=False):
+    """The split's definition, from costs: every (strip, row) pair costs 20,
+    a ragged last strip's pairs 38 in the three-sweep Poisson shapes; CTA
+    c's run starts at the last pair whose cumulative cost C has
+    C * grid <= total * c."""
+    tw, depth = SHAPES[cfg]
+    strips = (nx + tw - 1) // tw
+    cost = np.full(strips * ny, 20, dtype=np.int64)
+    if poisson and depth == 3 and nx % tw:
+        cost[(strips - 1) * ny:] = 38
+    cum = np.concatenate([[0], np.cumsum(cost)])
+    total = int(cum[-1])
+    return np.array([int(np.searchsorted(cum * grid, total * c, side="right")) - 1
+                     for c in range(grid + 1)], dtype=np.int64)
 
 
-def brute_deps(nx, ny, cfg, grid, b):
+def empty_ctas(nx, ny, cfg, grid, poisson=False):
+    b = brute_starts(nx, ny, cfg, grid, poisson)
+    return {c for c in range(grid) if b[c] == b[c + 1]}
+
+
+def brute_deps(nx, ny, cfg, grid, b, poisson=False):
     """Owners of every row within D rows of one of b's rows, in b's strip and
-    the strips beside it, b left out: from the partition's definition, CTA c
-    owning pairs R*c//grid .. R*(c+1)//grid - 1 of the strip-major order."""
+    the strips beside it, b left out, under the split's definition."""
     tw, depth = SHAPES[cfg]
     strips = (nx + tw - 1) // tw
     R = strips * ny
-    bounds = np.array([R * c // grid for c in range(grid + 1)], dtype=np.int64)
+    bounds = brute_starts(nx, ny, cfg, grid, poisson)
     owner = np.repeat(np.arange(grid), np.diff(bounds))
     assert owner.size == R
     out = set()
@@ -75,6 +90,49 @@ CASES = [(16384, 600, 10, 304), (16384, 700, 11, 304), (4096, 4096, 12, 152), (4
          (3000, 200, 3, 152),
          (1793, 20, 10, 100), (2100, 37, 6, 77), (130, 7, 3, 10), (5000, 3, 11, 9),
          (900, 1000, 10, 1)]
+
+
+# (nx, ny, shape, grid, poisson): three-sweep Poisson grids with a ragged
+# last strip (its rows weigh 38/20), one whose strips all are full, and a
+# Laplace one of the same size (equal weights).
+SPLIT_CASES = [(4097, 33, 12, 152, True), (3584, 64, 12, 152, True), (4000, 300, 12, 152, True),
+               (4096, 40, 12, 152, True), (1793, 50, 10, 300, True), (3584, 64, 12, 152, False),
+               (16384, 600, 10, 304, False), (2100, 37, 6, 77, True)]
+
+
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES)
+def test_split_follows_its_definition(pk, nx, ny, cfg, grid, poisson):
+    got = pk.pk_stream_split(nx, ny, cfg, grid, poisson)
+    want = brute_starts(nx, ny, cfg, grid, poisson)
+    assert np.array_equal(got, want)
+    tw, depth = SHAPES[cfg]
+    R = ((nx + tw - 1) // tw) * ny
+    assert got[0] == 0 and got[-1] == R and (np.diff(got) >= 0).all()
+    if not (poisson and depth == 3 and nx % tw):  # equal weights: floor(R c / grid)
+        assert np.array_equal(got, [R * c // grid for c in range(grid + 1)])
+
+
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES[:5])
+def test_weighted_split_balances_cost(pk, nx, ny, cfg, grid, poisson):
+    # the CTAs' costs differ by at most about one pair's cost (38)
+    tw, depth = SHAPES[cfg]
+    strips = (nx + tw - 1) // tw
+    cost = np.full(strips * ny, 20)
+    if poisson and depth == 3 and nx % tw:
+        cost[(strips - 1) * ny:] = 38
+    starts = pk.pk_stream_split(nx, ny, cfg, grid, poisson)
+    per = np.array([cost[starts[c]:starts[c + 1]].sum() for c in range(grid)])
+    assert per.max() - per.min() <= 2 * 38
+
+
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES)
+def test_weighted_lists_name_exactly_the_owners(pk, nx, ny, cfg, grid, poisson):
+    empty = empty_ctas(nx, ny, cfg, grid, poisson)
+    rng = np.random.default_rng(nx + ny)
+    for b in sorted(set([0, grid - 1, grid // 2] + rng.integers(0, grid, 10).tolist())):
+        got = pk.pk_stream_pass_deps(nx, ny, cfg, grid, b, poisson)
+        assert b not in got
+        assert set(got) - empty == brute_deps(nx, ny, cfg, grid, b, poisson), b
 
 
 @pytest.mark.parametrize("nx,ny,cfg,grid", CASES)
@@ -115,3 +173,6 @@ def test_bad_arguments_are_refused(pk):
                  (10, 10, 3, 4, 4), (10, 10, 3, 4, -1)]:
         with pytest.raises(pk.PkError):
             pk.pk_stream_pass_deps(*args)
+    for args in [(0, 10, 3, 4), (10, 10, -1, 4), (10, 10, 99, 4), (10, 10, 3, 0)]:
+        with pytest.raises(pk.PkError):
+            pk.pk_stream_split(*args)
