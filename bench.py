@@ -69,18 +69,21 @@ TRAFFIC = {"kernel_sha": "8d16aeb717d1253d", "stream_config": 10,
            "bytes_per_launch": 37.914e9 + 36.663e9}
 
 
-# pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass)
-SHAPES = {0: (1, 8, 1), 1: (1, 16, 1), 2: (2, 8, 1), 3: (4, 4, 1), 4: (4, 8, 1), 5: (2, 16, 1),
-          6: (1, 8, 2), 7: (2, 8, 2), 8: (1, 16, 2), 9: (2, 16, 2), 10: (1, 16, 3), 11: (1, 8, 3), 12: (1, 16, 3)}
+# pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass,
+# consumer threads per CTA)
+SHAPES = {0: (1, 8, 1, 256), 1: (1, 16, 1, 256), 2: (2, 8, 1, 256), 3: (4, 4, 1, 256), 4: (4, 8, 1, 256),
+          5: (2, 16, 1, 256), 6: (1, 8, 2, 256), 7: (2, 8, 2, 256), 8: (1, 16, 2, 256), 9: (2, 16, 2, 256),
+          10: (1, 16, 3, 224), 11: (1, 8, 3, 224), 12: (1, 16, 3, 256), 13: (1, 16, 3, 128),
+          14: (1, 16, 3, 128)}
 
 
 def shape_label(info, poisson):
     if info["variant"] != 2:
         return {1: "k_persistent_direct", 3: "k_persistent_local"}[info["variant"]] + \
             ("2" if info["variant"] == 3 and info["sweeps_per_pass"] == 2 else "")
-    q, ring, depth = SHAPES[info["stream_config"]]
-    return "k_persistent_stream<{%d float4/thread, %d-deep ring, %d sweep%s/pass}, %s>" % (
-        q, ring, depth, "s" if depth > 1 else "", "poisson" if poisson else "laplace")
+    q, ring, depth, cons = SHAPES[info["stream_config"]]
+    return "k_persistent_stream<{%d float4/thread, %d-deep ring, %d sweep%s/pass, %d consumers}, %s>" % (
+        q, ring, depth, "s" if depth > 1 else "", cons, "poisson" if poisson else "laplace")
 
 
 def passes_of(info, sweeps, tol, check_every, exit_at=None):

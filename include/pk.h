@@ -171,16 +171,21 @@ typedef struct {
     int32_t ctas_per_sm;              /* cap on resident CTAs per SM for sweeps (0 = occupancy) */
     int32_t barrier_kind;             /* PK_BARRIER_* (default PK_BARRIER_COUNTER) */
     int32_t stream_config;            /* STREAM shape.  -1 = default: for persistent runs of
-                                         two or more sweeps shape 11 (Laplace, nx > 8192),
-                                         10 (Laplace) or 12 (Poisson); shape 3 for the rest and
-                                         for the per-launch and graph paths
-                                         (pk_run_info.stream_config says which ran).  Index into
-                                         {float4 groups per thread, TMA ring depth, sweeps
-                                         per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1} 3 {4,4,1}
-                                         4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2} 8 {1,16,2}
-                                         9 {2,16,2} 10 {1,16,3} 11 {1,8,3} 12 {1,16,3}; a strip
-                                         is 1024 x groups columns wide (896 for 10 and 11, which
-                                         run seven consumer warps; 12 runs one CTA per SM).  A shape of D sweeps per pass
+                                         two or more sweeps shape 10 (Laplace) or, for
+                                         Poisson, 13 (12 where nx is a multiple of 1024 and at
+                                         least 8192), and for their runs with residual checks
+                                         shape 10 or 12 (their passes straddle the checks);
+                                         shape 3 for the rest and for the per-launch and graph
+                                         paths (pk_run_info.stream_config says which ran).
+                                         Index into {float4 groups per thread, TMA ring depth,
+                                         sweeps per pass}: 0 {1,8,1} 1 {1,16,1} 2 {2,8,1}
+                                         3 {4,4,1} 4 {4,8,1} 5 {2,16,1} 6 {1,8,2} 7 {2,8,2}
+                                         8 {1,16,2} 9 {2,16,2} 10 {1,16,3} 11 {1,8,3}
+                                         12 {1,16,3} 13 {1,16,3} 14 {1,16,3}; a strip is
+                                         1024 x groups columns wide (896 for 10 and 11, which
+                                         run seven consumer warps at two CTAs per SM; 12 runs
+                                         one CTA per SM; 13 and 14 run 512-column strips of
+                                         four consumer warps, three and two CTAs per SM).  A shape of D sweeps per pass
                                          keeps U_{k+1} .. U_{k+D-1} on chip (temporal
                                          blocking); a pass takes up to D sweeps, never past
                                          the end or a residual check; results are the same

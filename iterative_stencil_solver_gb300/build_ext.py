@@ -18,7 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libpk.so")
 LIB_COVERAGE = os.path.join(HERE, "libpk_coverage.so")
-SOURCES = ["pk_stream_d3.cu", "pk_stream_d3s.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
+SOURCES = ["pk_stream_d3.cu", "pk_stream_d3s.cu", "pk_stream_d3n.cu", "pk_stream_d2.cu", "pk_stream_d1.cu", "pk_local.cu", "pk_kernels.cu",
            "pk_host.cu", "pk_noalloc.cu", "pk_stream.cu"]
 HEADERS = ["pk_device.cuh", "pk_internal.h", "pk_sweep.cuh", "pk_stream.cuh"]
 

@@ -88,7 +88,8 @@ struct pk_ctx {
     int stream_cfg2 = -1;  // multi-sweep STREAM shape for persistent runs (-1 = none)
     int grid2 = 0;         // its grid
     int grid_straddle = 0; // grid of the three-sweep kernel whose passes straddle
-                           // residual checks (0 = the multi-sweep shape has none)
+                           // residual checks (0 = the plan has none)
+    int stream_cfg_s = -1; // its shape
     int local_depth = 1;   // LOCAL: sweeps per neighbour exchange the plan allows
     int local_threads = kDirectThreads;  // LOCAL: threads per CTA
     int launch_grid = 1;   // per-launch and graph paths: CTAs of their kernels
@@ -426,11 +427,13 @@ int plan(pk_ctx *ctx) {
             if (ctx->opt.grid_override > 0) ctx->grid2 = ctx->opt.grid_override;
         }
     }
-    // Runs with residual checks take the kernel of the same three-sweep
-    // shape whose passes straddle the checks; its occupancy is its own.
+    // Runs with residual checks take a three-sweep kernel whose passes
+    // straddle the checks, of the context's chosen shape or, in the
+    // automatic plan, of the check shape; its occupancy is its own.
     ctx->grid_straddle = 0;
+    ctx->stream_cfg_s = -1;
     {
-        const int shape_p = ctx->stream_cfg2 >= 0 ? ctx->stream_cfg2
+        const int shape_p = ctx->stream_cfg2 >= 0 ? default_check_shape(ctx->poisson, ctx->nx)
                             : v == kVariantStream ? ctx->stream_cfg : -1;
         // A straddling kernel that compiled with a stack frame (local
         // memory: its row windows left the registers) would run slower than
@@ -452,6 +455,7 @@ int plan(pk_ctx *ctx) {
                 if (need_s < 1) need_s = 1;
                 ctx->grid_straddle = (int)(need_s < cap_s ? need_s : cap_s);
                 if (ctx->opt.grid_override > 0) ctx->grid_straddle = ctx->opt.grid_override;
+                ctx->stream_cfg_s = shape_p;
             }
         }
     }
@@ -792,7 +796,10 @@ void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *
     }
     const bool straddle = kernel == kVariantStream && depth == 3 && tol > 0.f && check_every > 0 &&
                           ctx->grid_straddle > 0 && !(ctx->opt.flags & PK_FLAG_CHECKS_END_PASSES);
-    if (straddle) grid = ctx->grid_straddle;
+    if (straddle) {
+        shape = ctx->stream_cfg_s;
+        grid = ctx->grid_straddle;
+    }
     bool counters = false;
     if (kernel == kVariantStream && stream_depth(shape) != 2 &&
         !(ctx->opt.flags & PK_FLAG_BARRIER_EVERY_PASS)) {

@@ -267,7 +267,8 @@ constexpr int kStressWords = 32;
 // chip), CTAs per SM the register budget is sized for, and consumer threads
 // (a CTA adds one producer warp).  Seven consumer warps instead of eight
 // leave four warps per SM sub-partition at two CTAs per SM, which raises the
-// register cap from 96 to 128.
+// register cap from 96 to 128.  Shapes 13 and 14 run four consumer warps
+// (512-column strips) at three and two CTAs per SM.
 struct StreamConfig {
     int qpt;
     int stages;
@@ -275,12 +276,12 @@ struct StreamConfig {
     int min_ctas;
     int consumers;
 };
-constexpr int kNumStreamConfigs = 13;
+constexpr int kNumStreamConfigs = 15;
 constexpr StreamConfig kStreamConfigs[kNumStreamConfigs] = {
     {1, 8, 1, 1, 256},  {1, 16, 1, 1, 256}, {2, 8, 1, 1, 256},  {4, 4, 1, 1, 256},
     {4, 8, 1, 1, 256},  {2, 16, 1, 1, 256}, {1, 8, 2, 2, 256},  {2, 8, 2, 1, 256},
     {1, 16, 2, 2, 256}, {2, 16, 2, 1, 256}, {1, 16, 3, 2, 224}, {1, 8, 3, 2, 224},
-    {1, 16, 3, 1, 256}};
+    {1, 16, 3, 1, 256}, {1, 16, 3, 3, 128}, {1, 16, 3, 2, 128}};
 
 inline int stream_tw(int cfg) { return 4 * kStreamConfigs[cfg].qpt * kStreamConfigs[cfg].consumers; }
 inline int stream_threads(int cfg) { return kStreamConfigs[cfg].consumers + 32; }
@@ -338,11 +339,29 @@ inline size_t stream_smem_bytes(int cfg, bool poisson) {
 // strips, which divide it exactly).  With a grid barrier after every pass
 // the two rings ran within 1% of each other at 16384^2 (120.9 and 122.2):
 // the counters take 7% off the 16-deep ring's time, whose CTAs waited
-// about 12% of a pass at the barrier.  Poisson, whose ring slots also carry the
-// source row: {1, 16-deep ring, 256 consumers, 1 CTA/SM}, 169.0 at 16384^2,
-// 43.0 at 8192^2, 12.4 at 4096^2 and 4.33 at 2048^2 (the two-CTA shapes
-// 213.2, 58.3, 16.3 and 6.2).
-inline int default_multi_sweep_shape(bool poisson, int) { return poisson ? 12 : 10; }
+// about 12% of a pass at the barrier; the narrow three-CTA shape 13 below is
+// within a few per cent either way from 3072^2 to 12288^2 (5.67 against 6.12
+// at 3072^2, 7.71 against 6.54 at 3584^2, 25.2 against 22.6 at 7168^2), so
+// Laplace keeps shape 10.  Poisson, whose ring slots also carry the source
+// row, runs with one CTA of 256 consumers per SM or three CTAs of 128
+// consumers (shape 13: 512-column strips, 12 consumer warps per SM where
+// shape 12 has 8).  Shape 13 is faster below 8192^2 and on widths that are
+// not a multiple of 1024, where shape 12's last strip is ragged: 11.69
+// against 12.43 at 4096^2, 7.11 / 8.12 at 3072^2, 14.90 / 19.07 at 4608^2,
+// 9.65 / 13.27 at 3584^2, 23.7 / 25.0 at 6144^2, 40.6 / 46.5 at 8000^2.  On
+// the large multiples of 1024 shape 12 wins: 42.7 against 43.6 at 8192^2,
+// 66.3 / 66.7 at 10240^2, 165.9 / 175.4 at 16384^2 (12288^2: 95.0 / 94.3).
+inline int default_multi_sweep_shape(bool poisson, int nx) {
+    if (!poisson) return 10;
+    return nx >= 8192 && nx % 1024 == 0 ? 12 : 13;
+}
+// Shape of the automatic plan's runs with residual checks: the three-sweep
+// kernel whose passes straddle the checks must keep its row windows in
+// registers, which shape 13's does not (it compiles with a 16-byte stack
+// frame at its 128-register cap).  At 4096^2 Poisson with a check every 10
+// sweeps shape 12 ran 13.53 us/sweep, shape 13's straddling kernel 13.64,
+// and shape 13 with its passes stopping at the checks 15.34.
+inline int default_check_shape(bool poisson, int) { return poisson ? 12 : 10; }
 
 // Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).
 void set_global_error(const char *msg);

@@ -137,14 +137,19 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     }
     if (variant == kVariantDirect && (long long)ny * ((nx + 3) / 4) >= (1LL << 31))
         return fail(PK_EINVAL, "pk_run_sweeps_noalloc: grid too large");
-    // runs with checks on a three-sweep shape take the kernel whose passes
-    // straddle the checks, as pk_run_sweeps does
+    // runs with checks on a three-sweep shape take the check shape's kernel
+    // whose passes straddle the checks, as pk_run_sweeps does
     bool straddle = variant == kVariantStream && depth == 3 && tol > 0.f && check_every > 0;
     if (straddle) {
-        cudaFuncAttributes fa;
-        e = cudaFuncGetAttributes(&fa, kernel_persistent(variant, poisson, cfg, true));
-        if (e != cudaSuccess) return fail(PK_ECUDA, "cudaFuncGetAttributes", e);
-        straddle = fa.localSizeBytes == 0;  // as pk_create's plan decides
+        const int cs = default_check_shape(poisson, nx);
+        straddle = stream_depth(cs) == 3 && stream_config_ok(cs, poisson);
+        if (straddle) {
+            cudaFuncAttributes fa;
+            e = cudaFuncGetAttributes(&fa, kernel_persistent(variant, poisson, cs, true));
+            if (e != cudaSuccess) return fail(PK_ECUDA, "cudaFuncGetAttributes", e);
+            straddle = fa.localSizeBytes == 0;  // as pk_create's plan decides
+        }
+        if (straddle) cfg = cs;
     }
     int per_sm = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_persistent(variant, poisson, cfg, straddle),

@@ -90,7 +90,7 @@ def persistent_cases():
                 want, _ = oracle.jacobi_run(u0, f=ff, n=n, tol=tol, check_every=ce)
                 runs = [("direct", dict(variant=1)), ("local", dict(variant=3))]
                 runs += [("local-d%d" % d, dict(variant=3, local_depth=d)) for d in (2, 3, 4)]
-                runs += [("stream-%d" % s, dict(variant=2, stream_config=s)) for s in (3, 6, 8, 10, 11, 12)]
+                runs += [("stream-%d" % s, dict(variant=2, stream_config=s)) for s in (3, 6, 8, 10, 11, 12, 13, 14)]
                 runs += [("stream-auto", dict(variant=2)),
                          ("stream-one", dict(variant=2, flags=pk.PK_FLAG_ONE_SWEEP_PER_PASS)),
                          ("stream-barrier", dict(variant=2, flags=pk.PK_FLAG_ALTERNATE_DIRECTION

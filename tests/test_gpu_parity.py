@@ -536,7 +536,7 @@ CFG_SIZES = [(1, 1), (5, 3), (300, 301), (2053, 5), (4100, 7), (8200, 3)]
 CFG_RUNS = [(6, 4), (9, 0), (7, 3), (10, 2)]
 
 
-@pytest.mark.parametrize("cfg", range(13))
+@pytest.mark.parametrize("cfg", range(15))
 @pytest.mark.parametrize("nx,ny", CFG_SIZES, ids=["%dx%d" % s for s in CFG_SIZES])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
 def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
@@ -560,13 +560,13 @@ def test_stream_configs_bit_exact(pk, cfg, nx, ny, poisson):
 # Strip width of each STREAM shape: 4 x (float4 groups per thread) x
 # (consumer threads), as in the shape table of the library.
 STREAM_TW = {0: 1024, 1: 1024, 2: 2048, 3: 4096, 4: 4096, 5: 2048, 6: 1024, 7: 2048, 8: 1024,
-             9: 2048, 10: 896, 11: 896, 12: 1024}
+             9: 2048, 10: 896, 11: 896, 12: 1024, 13: 512, 14: 512}
 
 
 # A last strip one to three columns wide.  With one column, the cell two
 # columns right of the strip before it is the ring column, which a three-sweep
 # pass must keep at U_k at every level.
-@pytest.mark.parametrize("cfg", range(13))
+@pytest.mark.parametrize("cfg", range(15))
 @pytest.mark.parametrize("extra,strips", [(1, 1), (1, 2), (2, 1), (3, 1)],
                          ids=["tw+1", "2tw+1", "tw+2", "tw+3"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
@@ -609,7 +609,7 @@ def test_stream_default_plan_one_column_strip(pk, nx, ny, poisson):
 STRADDLE_RUNS = [(20, 4), (23, 5), (31, 7), (40, 10), (17, 2)]
 
 
-@pytest.mark.parametrize("cfg", [10, 11, 12])
+@pytest.mark.parametrize("cfg", [10, 11, 12, 13, 14])
 @pytest.mark.parametrize("nx,ny", [(300, 41), (2053, 19), (1793, 9), (897, 5)],
                          ids=["300x41", "2053x19", "1793x9", "897x5"])
 @pytest.mark.parametrize("poisson", [False, True], ids=["laplace", "poisson"])
@@ -641,7 +641,8 @@ def test_straddled_checks_bit_exact(pk, cfg, nx, ny, poisson):
 # same bits as the oracle and as a barrier after every pass, and the grid
 # barrier only behind the checks.
 PASS_COUNTER_CASES = [(3, 3000, 200), (3, 5000, 64), (10, 1793, 60), (11, 4500, 90),
-                      (11, 2053, 19), (12, 4097, 50), (12, 300, 41), (6, 2100, 37), (8, 1030, 300)]
+                      (11, 2053, 19), (12, 4097, 50), (12, 300, 41), (6, 2100, 37), (8, 1030, 300),
+                      (13, 1537, 40), (14, 4100, 70)]
 
 
 @pytest.mark.parametrize("cfg,nx,ny", PASS_COUNTER_CASES,
@@ -802,6 +803,25 @@ def test_three_sweep_residual_extreme_scales(pk, cfg, scale, poisson):
         check_info(info, oinfo)
 
 
+# The automatic plan's Poisson shapes: the narrow three-CTA shape 13 for runs
+# without checks, except on widths that are multiples of 1024 from 8192 up
+# (shape 12); runs with checks take shape 12, whose passes straddle them.
+# Short fields keep the oracle fast; the bits are the oracle's either way.
+@pytest.mark.parametrize("nx,want_plain", [(4096, 13), (4000, 13), (8192, 12), (8200, 13)],
+                         ids=["4096", "4000", "8192", "8200"])
+def test_poisson_plan_shapes(pk, nx, want_plain):
+    ny = 40
+    u0 = inputs.random_field(nx, ny, seed=950 + nx)
+    f = inputs.uniform_pm1(951 + nx, nx * ny).reshape(ny, nx)
+    for n, tol, ce, shape, straddle in ((12, 0.0, 0, want_plain, 0), (23, 1e-30, 5, 12, 1)):
+        want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
+        got, info = run_pk(pk, u0, f, n, tol, ce, variant=2)
+        assert info["variant"] == 2 and info["stream_config"] == shape, info
+        assert info["sweeps_per_pass"] == 3 and info["straddle"] == straddle
+        assert_same_bits(got, want)
+        check_info(info, oinfo)
+
+
 # The automatic plan sends grids that live in L2 but are too large for LOCAL
 # to DIRECT; their persistent runs of two or more sweeps take the multi-sweep
 # STREAM shape, single sweeps and the per-launch path stay on DIRECT.
@@ -815,12 +835,16 @@ def test_auto_direct_context_takes_multi_sweep_stream(pk, nx, ny, poisson):
         assert pk.pk_get_plan(ctx)["variant"] == 1
     finally:
         pk.pk_destroy(ctx)
-    for n, tol, ce, want_variant in ((10, 1e-30, 4, 2), (1, 0.0, 0, 1)):
+    # runs with checks take the check shape (12 or 10), runs without the
+    # multi-sweep shape (13 for Poisson below 8192 columns, else 10)
+    for n, tol, ce, want_variant, want_shape in ((10, 1e-30, 4, 2, 12 if poisson else 10),
+                                                 (10, 0.0, 0, 2, 13 if poisson else 10),
+                                                 (1, 0.0, 0, 1, None)):
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce)
         assert info["variant"] == want_variant, info
         if want_variant == 2:
-            assert info["stream_config"] == (12 if poisson else 10) and info["sweeps_per_pass"] == 3
+            assert info["stream_config"] == want_shape and info["sweeps_per_pass"] == 3
         assert_same_bits(got, want)
         check_info(info, oinfo)
         got, info = run_pk(pk, u0, f, n, tol, ce, path="launch")
@@ -849,10 +873,11 @@ DEFAULT_SHAPE_RUNS = [
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    # three sweeps per pass: shape 12 for Poisson, 10 for Laplace
-    multi = 12 if poisson else 10
+    # three sweeps per pass: for Poisson shape 13 without checks and 12 (the
+    # straddling kernel) with them, for Laplace shape 10
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
-        shape = multi if shape == MULTI else shape
+        if shape == MULTI:
+            shape = (12 if tol > 0 and ce > 0 else 13) if poisson else 10
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, path="persistent", variant=2)
         assert info["variant"] == 2 and info["stream_config"] == shape, (n, tol, ce, info)
