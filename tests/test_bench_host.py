@@ -72,7 +72,8 @@ def test_other_variants_take_one_sweep_per_pass():
     assert bench.passes_of(info(3, -1), 10, 0.0, 0) == (10, 0)
     assert bench.passes_of(info(3, -1, 2), 10, 0.0, 0) == (5, 0)
     assert bench.shape_label(info(3, -1, 2), False) == "k_persistent_local2"
-    assert bench.shape_label(info(2, 6), False).startswith("k_persistent_stream<{1 float4/thread, 8-deep ring, 2 sweeps/pass}")
+    assert bench.shape_label(info(2, 6), False).startswith(
+        "k_persistent_stream<{1 float4/thread, 8-deep ring, 2 sweeps/pass, 256 consumers}")
 
 
 def test_clock_summary_keeps_the_timed_region(tmp_path):
