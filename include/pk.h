@@ -351,31 +351,39 @@ int pk_device_field(pk_ctx *ctx, int which, float **ptr, int64_t *pitch, int *cu
  * kernel.  Any output may be NULL. */
 int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_max);
 
+/* kind: which persistent STREAM kernel a split or a pass-counter list is
+ * for -- PK_SPLIT_POISSON (a Poisson kernel), PK_SPLIT_STRADDLE (the kernel
+ * whose passes straddle residual checks: pk_run_info.straddle), both, or 0
+ * (a Laplace kernel without straddled checks). */
+#define PK_SPLIT_POISSON 1
+#define PK_SPLIT_STRADDLE 2
+
 /* How a STREAM grid deals its rows out: the (strip, row) pairs of an
  * nx x ny field (strips of the shape's width, the last one ragged when nx is
  * not a multiple of it; R = strips * ny pairs, strip-major) go to `grid` CTAs
  * of shape stream_config in contiguous runs, CTA c taking pairs
- * starts[c] .. starts[c+1] - 1.  Every pair costs the same, except in
- * three-sweep Poisson shapes, where a ragged last strip's pairs cost 38/20
- * of a full strip's (their rolled generic step): starts[c] is the last pair
- * whose cumulative cost C satisfies C * grid <= total cost * c, which for
- * equal costs is floor(R c / grid).  Writes grid + 1 entries to the HOST
- * array starts.  Host arithmetic only (no device call).  Errors: PK_EINVAL
- * (sizes, shape or grid out of range, starts NULL). */
-int pk_stream_split(int nx, int ny, int stream_config, int poisson, int grid, int64_t *starts);
+ * starts[c] .. starts[c+1] - 1.  Every pair costs the same, except in the
+ * three-sweep shapes' Poisson and straddling kernels (kind not 0), where a
+ * ragged last strip's pairs cost 38/20 of a full strip's (those kernels take
+ * a rolled generic step there): starts[c] is the last pair whose cumulative
+ * cost C satisfies C * grid <= total cost * c, which for equal costs is
+ * floor(R c / grid).  Writes grid + 1 entries to the HOST array starts.
+ * Host arithmetic only (no device call).  Errors: PK_EINVAL (sizes, shape,
+ * grid or kind out of range, starts NULL). */
+int pk_stream_split(int nx, int ny, int stream_config, int kind, int grid, int64_t *starts);
 
 /* The CTAs whose pass counters CTA `cta` of a persistent STREAM kernel
  * waits on before a pass (pk_run_info.pass_counters): the owners, under
- * pk_stream_split's runs (poisson as there), of the rows within D rows of
+ * pk_stream_split's runs (kind as there), of the rows within D rows of
  * its own (D = the shape's sweeps per pass) in its strip and in the strips
  * on either side.  They are also the CTAs that read `cta`'s rows.  The list
  * is a concatenation of CTA ranges and may name a CTA twice.  Writes
  * min(length, cap) entries to the HOST array out (NULL when cap is 0) and
  * returns the length; a run uses pass counters only
  * when every CTA's list has at most 32 entries.  Host arithmetic only (no
- * device call).  Errors: PK_EINVAL (sizes, shape, grid or cta out of
+ * device call).  Errors: PK_EINVAL (sizes, shape, grid, kind or cta out of
  * range, cap < 0). */
-int pk_stream_pass_deps(int nx, int ny, int stream_config, int poisson, int grid, int cta, int32_t *out,
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int kind, int grid, int cta, int32_t *out,
                         int cap);
 
 /* Post a task to the mapped-pinned mailbox ([P1] "Base implementation",

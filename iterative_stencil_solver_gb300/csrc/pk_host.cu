@@ -104,8 +104,10 @@ struct pk_ctx {
     short *pass_deps = nullptr;              // their lists (32 entries per CTA, part_cap CTAs)
     unsigned *cov = nullptr;                 // coverage build: a counter per float of both buffers
     unsigned long long *cov_status = nullptr; // coverage build: bad accesses, first place
-    std::pair<int, int> deps_key{-1, 0};     // (shape, grid) whose lists pass_deps holds
-    std::map<std::pair<int, int>, bool> counters_fit;  // (shape, grid) -> every list fits
+    // Pass-counter lists: keys (2 * shape + rolled, grid), rolled = the
+    // kernel deals its rows out by cost (stream_split_of)
+    std::pair<int, int> deps_key{-1, 0};     // the lists pass_deps holds
+    std::map<std::pair<int, int>, bool> counters_fit;  // -> every list fits
     int spin_valid = 0;                     // entries written by the last profiled run
     unsigned sweep_bar_base = 0;            // count word of bar_sweep (counter barrier)
     int rb_grid = 0;                        // red-black persistent grid (0 = not planned)
@@ -587,11 +589,12 @@ long long working_set(const pk_ctx *ctx) {
 
 // The pass-counter lists for a persistent STREAM launch of `shape` on
 // `grid` CTAs, written on the context's stream unless they are already
-// there.
-int ensure_pass_deps(pk_ctx *ctx, int shape, int grid) {
-    const auto key = std::make_pair(shape, grid);
+// there.  rolled: the kernel's split (the Poisson kernels and the ones whose
+// passes straddle checks weigh a ragged strip's rows).
+int ensure_pass_deps(pk_ctx *ctx, int shape, int grid, bool rolled) {
+    const auto key = std::make_pair(2 * shape + (rolled ? 1 : 0), grid);
     if (ctx->deps_key == key) return PK_OK;
-    cudaError_t e = launch_pass_deps(ctx->nx, ctx->ny, shape, ctx->poisson, grid, ctx->pass_deps, ctx->stream);
+    cudaError_t e = launch_pass_deps(ctx->nx, ctx->ny, shape, rolled, grid, ctx->pass_deps, ctx->stream);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "k_pass_deps launch");
     ctx->deps_key = key;
     return PK_OK;
@@ -803,10 +806,11 @@ void choose_persistent(pk_ctx *ctx, int64_t n, float tol, int check_every, int *
     bool counters = false;
     if (kernel == kVariantStream && stream_depth(shape) != 2 &&
         !(ctx->opt.flags & PK_FLAG_BARRIER_EVERY_PASS)) {
-        const auto key = std::make_pair(shape, grid);
+        const bool rolled = ctx->poisson || straddle;
+        const auto key = std::make_pair(2 * shape + (rolled ? 1 : 0), grid);
         auto it = ctx->counters_fit.find(key);
         if (it == ctx->counters_fit.end())
-            it = ctx->counters_fit.emplace(key, stream_counters_fit(ctx->nx, ctx->ny, shape, ctx->poisson,
+            it = ctx->counters_fit.emplace(key, stream_counters_fit(ctx->nx, ctx->ny, shape, rolled,
                                                                    grid)).first;
         counters = it->second;
     }
@@ -964,7 +968,7 @@ int pk_run_sweeps(pk_ctx *ctx, int64_t n, float tol, int check_every, pk_run_inf
     p.pass_counters = counters ? 1 : 0;
     if (stream_same_direction(counters, shape, working_set(ctx), ctx->l2_bytes)) p.alt_dir = 0;
     if (counters) {
-        const int rc = ensure_pass_deps(ctx, shape, grid);
+        const int rc = ensure_pass_deps(ctx, shape, grid, ctx->poisson || straddle);
         if (rc != PK_OK) return rc;
     }
     PK_TRY(ctx, cudaEventRecord(ctx->ev0, ctx->stream));
@@ -1051,7 +1055,7 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
     int kernel, shape, grid, depth;
     bool straddle, counters;
     choose_persistent(ctx, n, tol, check_every, &kernel, &shape, &grid, &depth, &straddle, &counters);
-    if (counters && (rc = ensure_pass_deps(ctx, shape, grid)) != PK_OK) return rc;
+    if (counters && (rc = ensure_pass_deps(ctx, shape, grid, ctx->poisson || straddle)) != PK_OK) return rc;
     const size_t row = sizeof(float) * (size_t)(ctx->nx + 2);
     const size_t dpitch = sizeof(float) * (size_t)ctx->pitch;
     const size_t rows = (size_t)(ctx->ny + 2);
@@ -1650,23 +1654,23 @@ int pk_get_plan(pk_ctx *ctx, int *variant, int *grid, int *task_grid, int *coop_
     return PK_OK;
 }
 
-int pk_stream_pass_deps(int nx, int ny, int stream_config, int poisson, int grid, int cta, int32_t *out,
+int pk_stream_pass_deps(int nx, int ny, int stream_config, int kind, int grid, int cta, int32_t *out,
                         int cap) {
     if (nx <= 0 || ny <= 0 || stream_config < 0 || stream_config >= kNumStreamConfigs || grid <= 0 ||
-        cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out))
+        cta < 0 || cta >= grid || cap < 0 || (cap > 0 && !out) || (kind & ~3))
         return PK_EINVAL;
-    const StreamSplit sp = stream_split_for(nx, ny, stream_config, poisson != 0, grid);
+    const StreamSplit sp = stream_split_for(nx, ny, stream_config, kind != 0, grid);
     const int halo = stream_depth(stream_config);
     const int n = stream_pass_ndeps(sp, ny, cta, halo);
     for (int i = 0; i < n && i < cap; ++i) out[i] = stream_pass_dep(sp, ny, cta, halo, i);
     return n;
 }
 
-int pk_stream_split(int nx, int ny, int stream_config, int poisson, int grid, int64_t *starts) {
+int pk_stream_split(int nx, int ny, int stream_config, int kind, int grid, int64_t *starts) {
     if (nx <= 0 || ny <= 0 || stream_config < 0 || stream_config >= kNumStreamConfigs || grid <= 0 ||
-        !starts)
+        !starts || (kind & ~3))
         return PK_EINVAL;
-    const StreamSplit sp = stream_split_for(nx, ny, stream_config, poisson != 0, grid);
+    const StreamSplit sp = stream_split_for(nx, ny, stream_config, kind != 0, grid);
     for (int c = 0; c <= grid; ++c) starts[c] = split_start(sp, c);
     return PK_OK;
 }

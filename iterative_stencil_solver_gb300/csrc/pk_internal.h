@@ -126,22 +126,23 @@ __host__ __device__ inline long long split_owner(const StreamSplit &s, long long
     while (c > 0 && split_start(s, (int)c) > pos) --c;
     return c;
 }
-// The cost of a ragged last strip's pairs relative to full ones, in 20ths:
-// the Poisson three-sweep step takes its rolled generic form on a ragged
-// strip (an unrolled copy for it pushed the kernel's row windows onto the
-// stack).  Measured with pass counters on GB300 (us/sweep at 4000^2, 4097^2,
-// 3584^2, 8000^2): equal costs 20.4, 25.8, 18.4, 76.6; 29/20 15.9, 19.6,
-// 14.4, 56.6; 35/20 14.2, 17.6, 12.9, 49.2; 40/20 14.5, 17.2, 13.2, 46.9;
-// 46/20 15.1, 18.1, 13.8, 48.3.  The other shapes' ragged strips cost what
-// full ones do.
+// The cost of a ragged last strip's pairs relative to full ones, in 20ths,
+// in the three-sweep kernels that take the rolled generic step on a ragged
+// strip (rolled: the Poisson kernels and the kernels whose passes straddle
+// residual checks; an unrolled copy for it pushed their row windows onto the
+// stack).  Measured with pass counters on GB300 (Poisson, us/sweep at
+// 4000^2, 4097^2, 3584^2, 8000^2): equal costs 20.4, 25.8, 18.4, 76.6;
+// 29/20 15.9, 19.6, 14.4, 56.6; 35/20 14.2, 17.6, 12.9, 49.2; 40/20 14.5,
+// 17.2, 13.2, 46.9; 46/20 15.1, 18.1, 13.8, 48.3.  The other kernels' ragged
+// strips cost what full ones do.
 constexpr int kSplitUnit = 20;
-constexpr int kSplitRaggedPoisson3 = 38;
+constexpr int kSplitRaggedRolled3 = 38;
 // The split of a STREAM grid of G CTAs and strips `tw` columns wide, the
 // same on the host and in the kernels.
-__host__ __device__ inline StreamSplit stream_split_of(int nx, int ny, int tw, int depth, bool poisson,
+__host__ __device__ inline StreamSplit stream_split_of(int nx, int ny, int tw, int depth, bool rolled,
                                                        int G) {
     const bool ragged = nx % tw != 0;
-    const int w_last = poisson && depth == 3 && ragged ? kSplitRaggedPoisson3 : kSplitUnit;
+    const int w_last = rolled && depth == 3 && ragged ? kSplitRaggedRolled3 : kSplitUnit;
     return stream_split((nx + tw - 1) / tw, ny, G, ragged, kSplitUnit, w_last);
 }
 
@@ -302,12 +303,12 @@ inline bool stream_same_direction(bool counters, int cfg, long long working_set,
 
 // Whether every CTA of a persistent STREAM grid of shape cfg has at most
 // kMaxPassDeps entries in its pass-counter list (one producer lane each).
-inline StreamSplit stream_split_for(int nx, int ny, int cfg, bool poisson, int G) {
-    return stream_split_of(nx, ny, stream_tw(cfg), stream_depth(cfg), poisson, G);
+inline StreamSplit stream_split_for(int nx, int ny, int cfg, bool rolled, int G) {
+    return stream_split_of(nx, ny, stream_tw(cfg), stream_depth(cfg), rolled, G);
 }
-inline bool stream_counters_fit(int nx, int ny, int cfg, bool poisson, int grid) {
+inline bool stream_counters_fit(int nx, int ny, int cfg, bool rolled, int grid) {
     if (grid > kMaxPassDepsGrid) return false;
-    const StreamSplit sp = stream_split_for(nx, ny, cfg, poisson, grid);
+    const StreamSplit sp = stream_split_for(nx, ny, cfg, rolled, grid);
     for (int b = 0; b < grid; ++b)
         if (stream_pass_ndeps(sp, ny, b, stream_depth(cfg)) > kMaxPassDeps) return false;
     return true;
@@ -460,7 +461,7 @@ cudaError_t launch_publish_record(const DeviceInfo *info, const BarrierState *ba
                                   cudaStream_t s);
 // Writes the pass-counter lists of a persistent STREAM grid of shape cfg on
 // an nx x ny field into out (32 entries per CTA, grid * 32 shorts).
-cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool poisson, int grid, short *out, cudaStream_t s);
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool rolled, int grid, short *out, cudaStream_t s);
 cudaError_t launch_task(bool poisson, int cluster, const TaskParams &p, cudaStream_t s);
 cudaError_t task_clusters_fit(bool poisson, int cluster, int *n);
 cudaError_t launch_axpy(int grid, float a, const float *x, float *y, long long len,

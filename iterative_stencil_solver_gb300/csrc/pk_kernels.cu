@@ -899,15 +899,15 @@ __global__ void k_publish_record(const DeviceInfo *info, const BarrierState *bar
 }
 
 // One CTA per sweep CTA, one thread per list entry.
-__global__ void __launch_bounds__(32) k_pass_deps(int nx, int ny, int tw, int depth, int poisson,
+__global__ void __launch_bounds__(32) k_pass_deps(int nx, int ny, int tw, int depth, int rolled,
                                                   short *out) {
-    const StreamSplit sp = stream_split_of(nx, ny, tw, depth, poisson != 0, (int)gridDim.x);
+    const StreamSplit sp = stream_split_of(nx, ny, tw, depth, rolled != 0, (int)gridDim.x);
     out[(size_t)blockIdx.x * kMaxPassDeps + threadIdx.x] =
         (short)stream_pass_dep(sp, ny, (int)blockIdx.x, depth, (int)threadIdx.x);
 }
 
-cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool poisson, int grid, short *out, cudaStream_t s) {
-    k_pass_deps<<<grid, kMaxPassDeps, 0, s>>>(nx, ny, stream_tw(cfg), stream_depth(cfg), poisson ? 1 : 0,
+cudaError_t launch_pass_deps(int nx, int ny, int cfg, bool rolled, int grid, short *out, cudaStream_t s) {
+    k_pass_deps<<<grid, kMaxPassDeps, 0, s>>>(nx, ny, stream_tw(cfg), stream_depth(cfg), rolled ? 1 : 0,
                                               out);
     return cudaGetLastError();
 }

@@ -177,7 +177,7 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
 
     // pass counters as pk_run_sweeps uses them
     const bool counters = variant == kVariantStream && stream_depth(cfg) != 2 &&
-                          stream_counters_fit(nx, ny, cfg, poisson, (int)grid);
+                          stream_counters_fit(nx, ny, cfg, poisson || straddle, (int)grid);
     int run_id;
     {
         std::lock_guard<std::mutex> lock(g_setup_mutex);
@@ -210,7 +210,7 @@ int pk_run_sweeps_noalloc(int nx, int ny, float *u_a, float *u_b, int64_t pitch,
     p.pass_counters = counters ? 1 : 0;
     if (stream_same_direction(counters, cfg, resident, g_l2[dev])) p.alt_dir = 0;  // as pk_run_sweeps
     if (counters) {
-        e = launch_pass_deps(nx, ny, cfg, poisson, (int)grid, sc->pass_deps, s);
+        e = launch_pass_deps(nx, ny, cfg, poisson || straddle, (int)grid, sc->pass_deps, s);
         if (e != cudaSuccess) return fail(PK_ECUDA, "k_pass_deps launch", e);
     }
     p.barrier_kind = (int)kBarrierCounter;

@@ -68,24 +68,26 @@ struct SCfg {
 };
 
 // This CTA's run of (strip, row) pairs, [s_stream_run[0], s_stream_run[1]),
-// in the shapes whose split weighs a ragged last strip's rows (three-sweep
-// Poisson; stream_split_of): fixed for a launch, so thread 0 works it out
-// once, before the passes (stream_run_setup).  The other shapes split by
-// count, R c / G, in the pass itself, as before: reading the bounds from
-// shared memory there cost the Laplace three-sweep kernels a spill.
+// in the kernels whose split weighs a ragged last strip's rows (three-sweep
+// kernels that take the rolled step there: Poisson, and the kernels whose
+// passes straddle checks; stream_split_of): fixed for a launch, so thread 0
+// works it out once, before the passes (stream_run_setup).  The other
+// kernels split by count, R c / G, in the pass itself, as before: reading
+// the bounds from shared memory there cost the Laplace three-sweep kernels a
+// spill.
 __shared__ long long s_stream_run[2];
 
-__device__ __noinline__ void stream_run_bounds(int nx, int ny, int tw, int depth, bool poisson,
+__device__ __noinline__ void stream_run_bounds(int nx, int ny, int tw, int depth, bool rolled,
                                                long long *run) {
-    const StreamSplit split = stream_split_of(nx, ny, tw, depth, poisson, (int)gridDim.x);
+    const StreamSplit split = stream_split_of(nx, ny, tw, depth, rolled, (int)gridDim.x);
     run[0] = split_start(split, (int)blockIdx.x);
     run[1] = split_start(split, (int)blockIdx.x + 1);
 }
 
-template <class C, bool POISSON>
+template <class C, bool ROLLED>
 __device__ __forceinline__ void stream_run_setup(const SweepParams &p) {
-    if constexpr (POISSON && C::kDepth == 3) {
-        if (threadIdx.x == 0) stream_run_bounds(p.nx, p.ny, C::TW, C::kDepth, POISSON, s_stream_run);
+    if constexpr (ROLLED && C::kDepth == 3) {
+        if (threadIdx.x == 0) stream_run_bounds(p.nx, p.ny, C::TW, C::kDepth, true, s_stream_run);
     }
 }
 
@@ -763,7 +765,7 @@ __device__ __forceinline__ void seg3_steady(const SweepParams &p, Seg3<C::kQPT> 
     }
 }
 
-template <class C, bool POISSON, int CHK>
+template <class C, bool POISSON, int CHK, bool ROLLED>
 __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *dst, int ja, int jb,
                                                  int dir, int cols, long long col0,
                                                  StreamState &st, float *qbuf, double &s2_out,
@@ -843,15 +845,15 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
     // Steady rows 6 .. nin-3.
     const int steady = c.nin - 8 > 0 ? c.nin - 8 : 0;
     // Full-width strips take the unrolled steady loop.  A ragged last strip
-    // takes its own unrolled copy for Laplace: the CTAs holding its rows would
-    // otherwise set the pace of every pass.  For Poisson the second copy
-    // makes the kernel too large for the compiler to keep the row windows in
-    // registers (they went to the stack, 1.45x slower), so there the ragged
-    // rows run through the rolled generic step below.
+    // takes its own unrolled copy in the Laplace kernels without straddled
+    // checks.  In the others (ROLLED) the second copy makes the kernel too
+    // large for the compiler to keep the row windows in registers (they went
+    // to the stack, 1.45x slower), so there the ragged rows run through the
+    // rolled generic step below, and the split gives their CTAs fewer rows.
     if (cols == C::TW)
         seg3_steady<C, POISSON, CHK, true>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra, rb,
                                            ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
-    else if constexpr (!POISSON)
+    else if constexpr (!ROLLED)
         seg3_steady<C, POISSON, CHK, false>(p, c, st, idx, r, steady, ka, kb, kx, pa, pb, py, ra,
                                               rb, ry, sa, sb, sx, fa, fb, fx, g3, s2, rmax);
     // The last input rows: stages 1 and 2 reach beyond the band (maybe the ring).
@@ -876,14 +878,16 @@ __device__ __forceinline__ void consume_segment3(const SweepParams &p, float *ds
 }
 
 // CHK: the stage that reduces a residual (0 = none; for D = 3 also 2 and 3,
-// or -1: the stage is cs, chosen at run time).
-template <class C, bool POISSON, int CHK, bool STORE, int D>
+// or -1: the stage is cs, chosen at run time).  ROLLED (a property of the
+// kernel, the same in all its passes): a three-sweep shape's ragged last
+// strip takes the rolled step, and the rows are dealt out by cost.
+template <class C, bool POISSON, int CHK, bool STORE, int D, bool ROLLED>
 __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *src, float *dst,
                                             int dir, StreamState &st, double &s2, float &rmax,
                                             int cs = 0) {
     const int nx = p.nx, ny = p.ny;
     long long L0, L1;
-    if constexpr (POISSON && C::kDepth == 3) {
+    if constexpr (ROLLED && C::kDepth == 3) {
         L0 = s_stream_run[0];
         L1 = s_stream_run[1];
     } else {  // split by count (stream_split_of gives the same for these shapes)
@@ -912,7 +916,7 @@ __device__ __forceinline__ void pass_stream(const SweepParams &p, const float *s
         if (producer_warp) {
             produce_segment<C, POISSON, D>(p, src, jr, jb, dir, cols, col0, st);
         } else if (D == 3) {
-            consume_segment3<C, POISSON, CHK>(p, dst, jr, jb, dir, cols, col0, st,
+            consume_segment3<C, POISSON, CHK, ROLLED>(p, dst, jr, jb, dir, cols, col0, st,
                                               st.slots + C::kStages * C::SLOT, s2, rmax, cs);
         } else if (D == 2) {
             consume_segment2<C, POISSON, CHK == 1>(p, dst, jr, jb, dir, cols, col0, st,
@@ -940,39 +944,42 @@ template <class C, bool POISSON, bool STRADDLE>
 __device__ __forceinline__ void pass_stream_any(const SweepParams &p, const float *src, float *dst,
                                                 int dir, int cs, bool store, int dp,
                                                 StreamState &st, double &s2, float &rmax) {
+    // The straddling kernels take the rolled step on ragged strips (a second
+    // unrolled copy put the Laplace ones' row windows on a stack frame).
+    constexpr bool R = POISSON || STRADDLE;
     // Only the depths this shape can take are compiled in.
     if constexpr (C::kDepth >= 3) {
         if (dp == 3) {
             if constexpr (STRADDLE) {
                 if (cs)
-                    pass_stream<C, POISSON, -1, true, 3>(p, src, dst, dir, st, s2, rmax, cs);
+                    pass_stream<C, POISSON, -1, true, 3, R>(p, src, dst, dir, st, s2, rmax, cs);
                 else
-                    pass_stream<C, POISSON, 0, true, 3>(p, src, dst, dir, st, s2, rmax);
+                    pass_stream<C, POISSON, 0, true, 3, R>(p, src, dst, dir, st, s2, rmax);
                 return;
             }
             if (cs)
-                pass_stream<C, POISSON, 1, true, 3>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 1, true, 3, R>(p, src, dst, dir, st, s2, rmax);
             else
-                pass_stream<C, POISSON, 0, true, 3>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 0, true, 3, R>(p, src, dst, dir, st, s2, rmax);
             return;
         }
     }
     if constexpr (C::kDepth >= 2) {
         if (dp == 2) {
             if (cs)
-                pass_stream<C, POISSON, 1, true, 2>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 1, true, 2, R>(p, src, dst, dir, st, s2, rmax);
             else
-                pass_stream<C, POISSON, 0, true, 2>(p, src, dst, dir, st, s2, rmax);
+                pass_stream<C, POISSON, 0, true, 2, R>(p, src, dst, dir, st, s2, rmax);
             return;
         }
     }
     if (cs) {
         if (store)
-            pass_stream<C, POISSON, 1, true, 1>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, 1, true, 1, R>(p, src, dst, dir, st, s2, rmax);
         else
-            pass_stream<C, POISSON, 1, false, 1>(p, src, dst, dir, st, s2, rmax);
+            pass_stream<C, POISSON, 1, false, 1, R>(p, src, dst, dir, st, s2, rmax);
     } else if (store) {
-        pass_stream<C, POISSON, 0, true, 1>(p, src, dst, dir, st, s2, rmax);
+        pass_stream<C, POISSON, 0, true, 1, R>(p, src, dst, dir, st, s2, rmax);
     }
 }
 
@@ -993,7 +1000,7 @@ __global__ void __launch_bounds__(C::kThreads, C::kMinBlocks) k_persistent_strea
     __shared__ int s_dep[32];
     __shared__ int s_wait_ok;
     __shared__ unsigned long long s_wait_ns;
-    stream_run_setup<C, POISSON>(p);
+    stream_run_setup<C, POISSON || STRADDLE>(p);
     StreamState st = stream_setup<C>(smem);  // (its block barrier publishes the run)
     if (threadIdx.x >= C::kCons) {
         s_dep[threadIdx.x & 31u] = -2;  // not fetched yet

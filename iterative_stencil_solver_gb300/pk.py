@@ -41,6 +41,8 @@ PK_FLAG_PROFILE_BARRIER = 0x4
 PK_FLAG_ONE_SWEEP_PER_PASS = 0x8
 PK_FLAG_CHECKS_END_PASSES = 0x10
 PK_FLAG_BARRIER_EVERY_PASS = 0x20
+PK_SPLIT_POISSON = 1
+PK_SPLIT_STRADDLE = 2
 
 PK_BARRIER_GENERATION = 0
 PK_BARRIER_COUNTER = 1
@@ -364,22 +366,28 @@ def pk_get_plan(ctx):
     return {"variant": v.value, "grid": g.value, "task_grid": tg.value, "coop_max": cm.value}
 
 
-def pk_stream_pass_deps(nx, ny, stream_config, grid, cta, poisson=False):
+def _split_kind(poisson, straddle):
+    return (PK_SPLIT_POISSON if poisson else 0) | (PK_SPLIT_STRADDLE if straddle else 0)
+
+
+def pk_stream_pass_deps(nx, ny, stream_config, grid, cta, poisson=False, straddle=False):
     """The CTAs whose pass counters CTA `cta` of a persistent STREAM grid
-    waits on (host arithmetic; no device needed)."""
-    n = _lib.pk_stream_pass_deps(nx, ny, stream_config, int(poisson), grid, cta, None, 0)
+    waits on (host arithmetic; no device needed); straddle: the kernel whose
+    passes straddle residual checks."""
+    kind = _split_kind(poisson, straddle)
+    n = _lib.pk_stream_pass_deps(nx, ny, stream_config, kind, grid, cta, None, 0)
     if n < 0:
         raise PkError(n, "pk_stream_pass_deps: bad arguments")
     out = (ctypes.c_int32 * max(n, 1))()
-    _lib.pk_stream_pass_deps(nx, ny, stream_config, int(poisson), grid, cta, out, n)
+    _lib.pk_stream_pass_deps(nx, ny, stream_config, kind, grid, cta, out, n)
     return list(out[:n])
 
 
-def pk_stream_split(nx, ny, stream_config, grid, poisson=False):
+def pk_stream_split(nx, ny, stream_config, grid, poisson=False, straddle=False):
     """First (strip, row) pair of each CTA's run, and R at the end (grid + 1
     entries; host arithmetic)."""
     starts = np.zeros(grid + 1, dtype=np.int64)
-    rc = _lib.pk_stream_split(nx, ny, stream_config, int(poisson), grid,
+    rc = _lib.pk_stream_split(nx, ny, stream_config, _split_kind(poisson, straddle), grid,
                               starts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
     if rc < 0:
         raise PkError(rc, "pk_stream_split: bad arguments")

@@ -146,6 +146,19 @@ def test_null_context_calls(pk):
     lib.pk_destroy(None)
 
 
+def test_binding_constants_match_the_header(pk):
+    # every PK_ constant the binding defines has the header's value, and the
+    # flag and split-kind constants are all there
+    hdr = open(os.path.join(ROOT, "include", "pk.h")).read()
+    defs = {m.group(1): int(m.group(2), 0)
+            for m in re.finditer(r"^#define (PK_\w+)\s+(0x[0-9a-fA-F]+|-?\d+)", hdr, flags=re.M)}
+    for name in [n for n in defs if n.startswith(("PK_FLAG_", "PK_SPLIT_"))]:
+        assert hasattr(pk, name), name
+    for name, value in defs.items():
+        if hasattr(pk, name):
+            assert getattr(pk, name) == value, name
+
+
 def test_gpu_tests_strip_widths_follow_the_shape_table():
     """The GPU tests size their narrow-last-strip grids from a table of strip
     widths (4 x float4 groups per thread x consumer threads); it must follow

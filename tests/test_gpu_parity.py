@@ -628,7 +628,7 @@ def test_straddled_checks_bit_exact(pk, cfg, nx, ny, poisson):
         assert_same_bits(got, want)
         check_info(info, oinfo)
         assert info["passes"] == sum(bench.passes_of(info, n, 1e-30, ce))
-        if poisson and cfg == 12:  # the default Poisson shape's straddling kernel fits in registers
+        if cfg != 13:  # every straddling kernel but shape 13's keeps its row windows in registers
             assert info["straddle"] == 1
 
 

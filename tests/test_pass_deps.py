@@ -40,15 +40,16 @@ def _shapes():
 SHAPES = _shapes()
 
 
-def brute_starts(nx, ny, cfg, grid, poisson=False):
+def brute_starts(nx, ny, cfg, grid, poisson=False, straddle=False):
     """The split's definition, from costs: every (strip, row) pair costs 20,
-    a ragged last strip's pairs 38 in the three-sweep Poisson shapes; CTA
+    a ragged last strip's pairs 38 in the three-sweep shapes' Poisson
+    kernels and straddling kernels (both take the rolled step there); CTA
     c's run starts at the last pair whose cumulative cost C has
     C * grid <= total * c."""
     tw, depth = SHAPES[cfg]
     strips = (nx + tw - 1) // tw
     cost = np.full(strips * ny, 20, dtype=np.int64)
-    if poisson and depth == 3 and nx % tw:
+    if (poisson or straddle) and depth == 3 and nx % tw:
         cost[(strips - 1) * ny:] = 38
     cum = np.concatenate([[0], np.cumsum(cost)])
     total = int(cum[-1])
@@ -56,18 +57,18 @@ def brute_starts(nx, ny, cfg, grid, poisson=False):
                      for c in range(grid + 1)], dtype=np.int64)
 
 
-def empty_ctas(nx, ny, cfg, grid, poisson=False):
-    b = brute_starts(nx, ny, cfg, grid, poisson)
+def empty_ctas(nx, ny, cfg, grid, poisson=False, straddle=False):
+    b = brute_starts(nx, ny, cfg, grid, poisson, straddle)
     return {c for c in range(grid) if b[c] == b[c + 1]}
 
 
-def brute_deps(nx, ny, cfg, grid, b, poisson=False):
+def brute_deps(nx, ny, cfg, grid, b, poisson=False, straddle=False):
     """Owners of every row within D rows of one of b's rows, in b's strip and
     the strips beside it, b left out, under the split's definition."""
     tw, depth = SHAPES[cfg]
     strips = (nx + tw - 1) // tw
     R = strips * ny
-    bounds = brute_starts(nx, ny, cfg, grid, poisson)
+    bounds = brute_starts(nx, ny, cfg, grid, poisson, straddle)
     owner = np.repeat(np.arange(grid), np.diff(bounds))
     assert owner.size == R
     out = set()
@@ -92,47 +93,57 @@ CASES = [(16384, 600, 10, 304), (16384, 700, 11, 304), (4096, 4096, 12, 152), (4
          (900, 1000, 10, 1)]
 
 
-# (nx, ny, shape, grid, poisson): three-sweep Poisson grids with a ragged
-# last strip (its rows weigh 38/20), one whose strips all are full, and a
-# Laplace one of the same size (equal weights).
-SPLIT_CASES = [(4097, 33, 12, 152, True), (3584, 64, 12, 152, True), (4000, 300, 12, 152, True),
-               (4096, 40, 12, 152, True), (1793, 50, 10, 300, True), (3584, 64, 12, 152, False),
-               (16384, 600, 10, 304, False), (2100, 37, 6, 77, True)]
+# (nx, ny, shape, grid, poisson, straddle): three-sweep Poisson grids with a
+# ragged last strip (its rows weigh 38/20), one whose strips all are full, a
+# Laplace one of the same size (equal weights), and the straddling kernels
+# of Laplace shapes on ragged widths (16384 columns in 896-wide strips; the
+# rolled step there, so weighted too).
+SPLIT_CASES = [(4097, 33, 12, 152, True, False), (3584, 64, 12, 152, True, False),
+               (4000, 300, 12, 152, True, False), (4096, 40, 12, 152, True, False),
+               (1793, 50, 10, 300, True, False), (16384, 600, 10, 304, False, True),
+               (4097, 33, 12, 152, False, True), (3000, 45, 13, 456, True, True),
+               (3584, 64, 12, 152, False, False), (16384, 600, 10, 304, False, False),
+               (2100, 37, 6, 77, True, False), (2100, 37, 6, 77, False, True)]
 
 
-@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES)
-def test_split_follows_its_definition(pk, nx, ny, cfg, grid, poisson):
-    got = pk.pk_stream_split(nx, ny, cfg, grid, poisson)
-    want = brute_starts(nx, ny, cfg, grid, poisson)
+def _weighted(nx, cfg, poisson, straddle):
+    tw, depth = SHAPES[cfg]
+    return (poisson or straddle) and depth == 3 and nx % tw != 0
+
+
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson,straddle", SPLIT_CASES)
+def test_split_follows_its_definition(pk, nx, ny, cfg, grid, poisson, straddle):
+    got = pk.pk_stream_split(nx, ny, cfg, grid, poisson, straddle)
+    want = brute_starts(nx, ny, cfg, grid, poisson, straddle)
     assert np.array_equal(got, want)
     tw, depth = SHAPES[cfg]
     R = ((nx + tw - 1) // tw) * ny
     assert got[0] == 0 and got[-1] == R and (np.diff(got) >= 0).all()
-    if not (poisson and depth == 3 and nx % tw):  # equal weights: floor(R c / grid)
+    if not _weighted(nx, cfg, poisson, straddle):  # equal weights: floor(R c / grid)
         assert np.array_equal(got, [R * c // grid for c in range(grid + 1)])
 
 
-@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES[:5])
-def test_weighted_split_balances_cost(pk, nx, ny, cfg, grid, poisson):
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson,straddle", SPLIT_CASES[:8])
+def test_weighted_split_balances_cost(pk, nx, ny, cfg, grid, poisson, straddle):
     # the CTAs' costs differ by at most about one pair's cost (38)
     tw, depth = SHAPES[cfg]
     strips = (nx + tw - 1) // tw
     cost = np.full(strips * ny, 20)
-    if poisson and depth == 3 and nx % tw:
+    if _weighted(nx, cfg, poisson, straddle):
         cost[(strips - 1) * ny:] = 38
-    starts = pk.pk_stream_split(nx, ny, cfg, grid, poisson)
+    starts = pk.pk_stream_split(nx, ny, cfg, grid, poisson, straddle)
     per = np.array([cost[starts[c]:starts[c + 1]].sum() for c in range(grid)])
     assert per.max() - per.min() <= 2 * 38
 
 
-@pytest.mark.parametrize("nx,ny,cfg,grid,poisson", SPLIT_CASES)
-def test_weighted_lists_name_exactly_the_owners(pk, nx, ny, cfg, grid, poisson):
-    empty = empty_ctas(nx, ny, cfg, grid, poisson)
+@pytest.mark.parametrize("nx,ny,cfg,grid,poisson,straddle", SPLIT_CASES)
+def test_weighted_lists_name_exactly_the_owners(pk, nx, ny, cfg, grid, poisson, straddle):
+    empty = empty_ctas(nx, ny, cfg, grid, poisson, straddle)
     rng = np.random.default_rng(nx + ny)
     for b in sorted(set([0, grid - 1, grid // 2] + rng.integers(0, grid, 10).tolist())):
-        got = pk.pk_stream_pass_deps(nx, ny, cfg, grid, b, poisson)
+        got = pk.pk_stream_pass_deps(nx, ny, cfg, grid, b, poisson, straddle)
         assert b not in got
-        assert set(got) - empty == brute_deps(nx, ny, cfg, grid, b, poisson), b
+        assert set(got) - empty == brute_deps(nx, ny, cfg, grid, b, poisson, straddle), b
 
 
 @pytest.mark.parametrize("nx,ny,cfg,grid", CASES)
@@ -176,3 +187,10 @@ def test_bad_arguments_are_refused(pk):
     for args in [(0, 10, 3, 4), (10, 10, -1, 4), (10, 10, 99, 4), (10, 10, 3, 0)]:
         with pytest.raises(pk.PkError):
             pk.pk_stream_split(*args)
+    # a kind outside PK_SPLIT_POISSON | PK_SPLIT_STRADDLE, through the C call
+    import ctypes
+    starts = np.zeros(5, dtype=np.int64)
+    ptr = starts.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    assert pk._lib.pk_stream_split(10, 10, 3, 4, 4, ptr) == pk.PK_EINVAL
+    assert pk._lib.pk_stream_split(10, 10, 3, 3, 4, ptr) == 0
+    assert pk._lib.pk_stream_pass_deps(10, 10, 3, 8, 4, 0, None, 0) == pk.PK_EINVAL
