@@ -281,6 +281,16 @@ def test_poisson_4096_residual_every_10(pk, path):
     assert_same_bits(got, want)
 
 
+def test_poisson_4096_no_checks_narrow_shape(pk):
+    # the same workload without checks takes the default plan's narrow
+    # three-CTA shape (512-column strips, 456 CTAs on 152 SMs)
+    w = inputs.workload_poisson_random_source(4096, seed=2)
+    want, _ = oracle.jacobi_run(w["u0"], f=w["f"], n=31, threads=THREADS)
+    got, info = run_pk(pk, w["u0"], w["f"], 31)
+    assert info["stream_config"] == 13 and info["sweeps_per_pass"] == 3 and info["pass_counters"] == 1
+    assert_same_bits(got, want)
+
+
 def test_laplace_random_16384_full_field(pk):
     w = inputs.workload_laplace_random(16384, seed=3)
     got, info = run_pk(pk, w["u0"], None, 100)
@@ -288,6 +298,18 @@ def test_laplace_random_16384_full_field(pk):
     assert info["sweeps_done"] == 100 and info["variant"] == 2 and info["sweeps_per_pass"] == 3
     want, _ = oracle.jacobi_run(w["u0"], n=100, threads=THREADS)
     assert_same_bits(got, want)
+    # the same sweeps with a residual check every 10 (the checks do not change
+    # the field): the kernel whose passes straddle the checks, at full size,
+    # its ragged last strip (16384 columns in 896-wide strips) on the rolled
+    # step; residuals against the oracle's of U_0 and U_100
+    got, info = run_pk(pk, w["u0"], None, 100, 1e-30, 10)
+    assert info["straddle"] == 1 and info["sweeps_done"] == 100 and info["n_checks"] == 11
+    assert_same_bits(got, want)
+    res0, _ = oracle.residual(w["u0"])
+    res_last, rmax_last = oracle.residual(want)
+    assert info["res0"] == pytest.approx(res0, rel=1e-10, abs=0)
+    assert info["res_last"] == pytest.approx(res_last, rel=1e-10, abs=0)
+    assert info["res_max_last"] == rmax_last
 
 
 def _task_setup(pk, w):
