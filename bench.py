@@ -546,6 +546,30 @@ def latency_extras(pk):
             finally:
                 pk.pk_destroy(ctx)
     out["pass_counters_laplace_16384_100sweeps"] = pc
+    # A residual check every 10 sweeps (11 checks; tol below any residual, so
+    # all 100 sweeps run): passes that straddle the checks (the default) and
+    # passes that stop at them; the same bits
+    lr = {}
+    for mode, flags in (("straddled", pk.PK_FLAG_ALTERNATE_DIRECTION),
+                        ("checks_end_passes",
+                         pk.PK_FLAG_ALTERNATE_DIRECTION | pk.PK_FLAG_CHECKS_END_PASSES)):
+        ctx = pk.pk_create(16384, 16384, w["u0"], None, pk.pk_options_default(flags=flags))
+        try:
+            runs = []
+            for rep in range(4):  # the first is a warm-up; each run starts from the workload's field
+                pk.pk_set_field(ctx, w["u0"])
+                info = pk.pk_run_sweeps(ctx, 100, 1e-30, 10)
+                if rep:
+                    runs.append(info)
+            info = min(runs, key=lambda r: r["device_us"])
+            lr[mode] = {"us_per_sweep": info["device_us"] / 100, "kernel": shape_label(info, False),
+                        "straddle": info["straddle"], "passes": info["passes"],
+                        "passes_model": sum(passes_of(info, 100, 1e-30, 10)),
+                        "barriers": info["barriers"], "n_checks": info["n_checks"],
+                        "res_last": info["res_last"]}
+        finally:
+            pk.pk_destroy(ctx)
+    out["laplace_16384_res10"] = lr
     # Barrier spin: the headline kernel (one barrier per pass) and
     # the barrier-per-sweep DIRECT kernel on the L2-resident 512^2 grid.
     out["barrier_spin"] = {

@@ -318,8 +318,9 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
  * and pk_get_field (a library convenience; the pages have no counterpart):
  * `bytes` of zeroed memory.  Where the operating system backs all of it with
  * 2 MB transparent huge pages (anonymous mmap on a 2 MB boundary, madvise
- * MADV_HUGEPAGE, checked in /proc/self/smaps) the region is registered with
- * cudaHostRegister; otherwise it comes from cudaHostAlloc.  On a GB300
+ * MADV_HUGEPAGE, and where the first touch left small pages a synchronous
+ * MADV_COLLAPSE of the range, checked in /proc/self/smaps) the region is
+ * registered with cudaHostRegister; otherwise it comes from cudaHostAlloc.  On a GB300
  * host, batches copying from cudaHostAlloc memory ran at full rate in some
  * batches and 20-50% slower in others (the copy engines' translation of
  * gigabytes of host pages); from 2 MB pages every batch ran at full rate,

@@ -1520,6 +1520,14 @@ namespace {
 std::mutex g_host_mutex;
 std::map<void *, std::pair<void *, size_t>> g_host_regions;
 constexpr size_t kHugePage = size_t(2) << 20;
+// madvise advice that collapses a populated range into huge pages at once,
+// compacting memory as needed (Linux 6.1 and later; older kernels refuse it
+// with EINVAL).  Spelled out where the C library's headers predate it.
+#ifdef MADV_COLLAPSE
+constexpr int kMadvCollapse = MADV_COLLAPSE;
+#else
+constexpr int kMadvCollapse = 25;
+#endif
 
 // Bytes of [lo, hi) that the kernel backs with transparent huge pages
 // (AnonHugePages of the mappings that overlap it in /proc/self/smaps); -1
@@ -1556,12 +1564,16 @@ int pk_host_alloc(int64_t bytes, void **ptr) {
     // boundary (one huge page of slack), every page touched, then
     // registered.  Kept only when the kernel backed all of it with huge
     // pages: registered small pages copy far slower than cudaHostAlloc's.
+    // Where the pages touched were not all huge (memory too fragmented for
+    // the fault path to find 2 MB blocks), the range is collapsed in place
+    // once before giving up.
     void *map = mmap(nullptr, len + kHugePage, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
     if (map != MAP_FAILED) {
         char *base = static_cast<char *>(map);
         char *start = base + (kHugePage - (reinterpret_cast<uintptr_t>(base) % kHugePage)) % kHugePage;
         if (madvise(start, len, MADV_HUGEPAGE) == 0) {
             std::memset(start, 0, len);
+            if (huge_page_bytes(start, start + len) < (long long)len) (void)madvise(start, len, kMadvCollapse);
             if (huge_page_bytes(start, start + len) >= (long long)len &&
                 cudaHostRegister(start, len, cudaHostRegisterDefault) == cudaSuccess) {
                 std::lock_guard<std::mutex> lock(g_host_mutex);
