@@ -617,7 +617,7 @@ def e2e_steps(pk, ctx, w, args, world, torch):
     out); returns the e2e record and the serial set/run/get number."""
     cells = w["nx"] * w["ny"]
     sweeps = w["sweeps"]
-    # e2e through the public API with page-locked host buffers on 2 MB pages
+    # e2e through the public API with page-locked host buffers on huge pages
     # (pk_host_array): every step uploads its field, sweeps and downloads
     # its result.  pk_run_batch runs the steps as a pipeline (step i+1's
     # upload and step i-1's download overlap step i's sweeps).
@@ -830,7 +830,7 @@ def main():
             "h2d_bytes_per_step": int(w["u0"].nbytes),
             "d2h_bytes_per_step": int(w["u0"].nbytes),
             "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps); "
-                   "host buffers from pk_host_alloc (page-locked, 2 MB pages)",
+                   "host buffers from pk_host_alloc (page-locked, on transparent huge pages where granted)",
             "steps": args.steps, "seconds": e2e["seconds"], "gpu_launches": e2e["launches"],
             "sweeps_ms_per_step_median": e2e["sweeps_ms_median"],
             "host_link": e2e["link"], "bound_value": e2e["bound_value"],

@@ -304,7 +304,7 @@ int pk_run_redblack_launch(pk_ctx *ctx, int64_t n, float tol, int check_every, p
  * context; the sweeps themselves run one after another on the context's
  * stream, so no two cooperative grids are ever in flight together.  Host
  * arrays should be page-locked (pk_host_alloc, or cudaHostAlloc /
- * cudaHostRegister) for the copies to overlap, and on 2 MB pages
+ * cudaHostRegister) for the copies to overlap, and on huge pages
  * (pk_host_alloc) for them to run at full rate in every batch.  On first use the call allocates three field pairs of
  * the context's layout (kept until pk_destroy); it neither reads nor
  * changes the context's own field.  Blocks until every result is on the
@@ -317,13 +317,16 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
 /* Page-locked HOST memory for the host arrays of pk_run_batch, pk_set_field
  * and pk_get_field (a library convenience; the pages have no counterpart):
  * `bytes` of zeroed memory.  Where the operating system backs all of it with
- * 2 MB transparent huge pages (anonymous mmap on a 2 MB boundary, madvise
- * MADV_HUGEPAGE, and where the first touch left small pages a synchronous
- * MADV_COLLAPSE of the range, checked in /proc/self/smaps) the region is
- * registered with cudaHostRegister; otherwise it comes from cudaHostAlloc.  On a GB300
+ * transparent huge pages of its size (hpage_pmd_size: 2 MB with 4 KB base
+ * pages, 512 MB with 64 KB ones; anonymous mmap on a huge-page boundary,
+ * madvise MADV_HUGEPAGE, and where the first touch left small pages a
+ * synchronous MADV_COLLAPSE of the range, checked in /proc/self/smaps) the
+ * region is registered with cudaHostRegister; otherwise, and for requests
+ * that whole huge pages would more than double, it comes from
+ * cudaHostAlloc.  On a GB300
  * host, batches copying from cudaHostAlloc memory ran at full rate in some
  * batches and 20-50% slower in others (the copy engines' translation of
- * gigabytes of host pages); from 2 MB pages every batch ran at full rate,
+ * gigabytes of host pages); from huge pages every batch ran at full rate,
  * while registered small pages were slower than both.  *ptr receives the
  * address; release it with pk_host_free only.  Needs a CUDA device.
  * Errors: PK_EINVAL (bytes <= 0, ptr NULL), PK_ECUDA (*ptr is NULL). */

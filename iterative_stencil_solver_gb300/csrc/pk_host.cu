@@ -1519,7 +1519,20 @@ namespace {
 // mapping null for a cudaHostAlloc region.
 std::mutex g_host_mutex;
 std::map<void *, std::pair<void *, size_t>> g_host_regions;
-constexpr size_t kHugePage = size_t(2) << 20;
+// The kernel's transparent huge page (PMD) size: 2 MB with 4 KB base pages,
+// 512 MB with 64 KB ones (as on GB300 hosts running a 64 KB-page kernel);
+// 2 MB where the kernel does not say.
+size_t thp_bytes() {
+    static const size_t v = [] {
+        unsigned long long x = 0;
+        if (FILE *f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+            if (std::fscanf(f, "%llu", &x) != 1) x = 0;
+            std::fclose(f);
+        }
+        return x >= 4096 && (x & (x - 1)) == 0 ? (size_t)x : size_t(2) << 20;
+    }();
+    return v;
+}
 // madvise advice that collapses a populated range into huge pages at once,
 // compacting memory as needed (Linux 6.1 and later; older kernels refuse it
 // with EINVAL).  Spelled out where the C library's headers predate it.
@@ -1559,33 +1572,38 @@ int pk_host_alloc(int64_t bytes, void **ptr) {
         set_global_error("pk_host_alloc: bytes must be positive");
         return PK_EINVAL;
     }
-    const size_t len = ((size_t)bytes + kHugePage - 1) / kHugePage * kHugePage;
-    // First choice: anonymous memory on 2 MB pages, started on a 2 MB
-    // boundary (one huge page of slack), every page touched, then
+    const size_t hp = thp_bytes();
+    size_t len = ((size_t)bytes + hp - 1) / hp * hp;
+    // First choice: anonymous memory on transparent huge pages, started on a
+    // huge-page boundary (one huge page of slack), every page touched, then
     // registered.  Kept only when the kernel backed all of it with huge
     // pages: registered small pages copy far slower than cudaHostAlloc's.
     // Where the pages touched were not all huge (memory too fragmented for
-    // the fault path to find 2 MB blocks), the range is collapsed in place
-    // once before giving up.
-    void *map = mmap(nullptr, len + kHugePage, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+    // the fault path to find the blocks), the range is collapsed in place
+    // once before giving up.  Not tried where rounding up to whole huge
+    // pages would more than double the request (small arrays).
+    void *map = len <= 2 * (size_t)bytes
+                    ? mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0)
+                    : MAP_FAILED;
     if (map != MAP_FAILED) {
         char *base = static_cast<char *>(map);
-        char *start = base + (kHugePage - (reinterpret_cast<uintptr_t>(base) % kHugePage)) % kHugePage;
+        char *start = base + (hp - (reinterpret_cast<uintptr_t>(base) % hp)) % hp;
         if (madvise(start, len, MADV_HUGEPAGE) == 0) {
             std::memset(start, 0, len);
             if (huge_page_bytes(start, start + len) < (long long)len) (void)madvise(start, len, kMadvCollapse);
             if (huge_page_bytes(start, start + len) >= (long long)len &&
                 cudaHostRegister(start, len, cudaHostRegisterDefault) == cudaSuccess) {
                 std::lock_guard<std::mutex> lock(g_host_mutex);
-                g_host_regions[start] = std::make_pair(map, len + kHugePage);
+                g_host_regions[start] = std::make_pair(map, len + hp);
                 *ptr = start;
                 return PK_OK;
             }
             (void)cudaGetLastError();
         }
-        munmap(map, len + kHugePage);
+        munmap(map, len + hp);
     }
     // Otherwise the driver's page-locked memory.
+    len = ((size_t)bytes + 4095) / 4096 * 4096;
     void *p = nullptr;
     const cudaError_t e = cudaHostAlloc(&p, len, cudaHostAllocDefault);
     if (e != cudaSuccess) {
