@@ -612,21 +612,68 @@ def latency_extras(pk):
     return out
 
 
-def e2e_steps(pk, ctx, w, args, world, torch):
+def e2e_buffers(pk, w):
+    """The e2e leg's page-locked host buffers (pk_host_array: on transparent
+    huge pages where the kernel grants them), one field in and two out.
+    Made before the device-timed steps: the huge-page faults can wake the
+    kernel's background memory compaction, which slows host-device copies
+    while it runs."""
+    host_in = pk.pk_host_array(w["u0"].shape)
+    host_in[...] = w["u0"]
+    host_out = [pk.pk_host_array(w["u0"].shape) for _ in range(2)]
+    return host_in, host_out
+
+
+def compaction_pages():
+    """Pages the kernel's memory compaction has scanned or isolated so far
+    (/proc/vmstat), or None where the file cannot be read."""
+    try:
+        total = 0
+        with open("/proc/vmstat") as fh:
+            for line in fh:
+                key, val = line.split()
+                if key in ("compact_migrate_scanned", "compact_free_scanned", "compact_isolated"):
+                    total += int(val)
+        return total
+    except (OSError, ValueError):
+        return None
+
+
+def wait_compaction_idle(limit_s=20.0, quiet_s=0.5):
+    """Wait until memory compaction has been idle for quiet_s (at most
+    limit_s); returns (seconds waited, idle reached)."""
+    t0 = time.perf_counter()
+    last = compaction_pages()
+    if last is None:
+        return 0.0, None
+    quiet_since = t0
+    while time.perf_counter() - t0 < limit_s:
+        time.sleep(0.1)
+        cur = compaction_pages()
+        now = time.perf_counter()
+        if cur != last:
+            last, quiet_since = cur, now
+        elif now - quiet_since >= quiet_s:
+            return now - t0, True
+    return time.perf_counter() - t0, False
+
+
+def e2e_steps(pk, ctx, w, args, world, torch, buffers):
     """The bench steps end to end through the public API (host buffers in and
     out); returns the e2e record and the serial set/run/get number."""
     cells = w["nx"] * w["ny"]
     sweeps = w["sweeps"]
     # e2e through the public API with page-locked host buffers on huge pages
-    # (pk_host_array): every step uploads its field, sweeps and downloads
-    # its result.  pk_run_batch runs the steps as a pipeline (step i+1's
-    # upload and step i-1's download overlap step i's sweeps).
-    host_in = pk.pk_host_array(w["u0"].shape)
-    host_in[...] = w["u0"]
-    host_out = [pk.pk_host_array(w["u0"].shape) for _ in range(2)]
+    # (e2e_buffers): every step uploads its field, sweeps and downloads its
+    # result.  pk_run_batch runs the steps as a pipeline (step i+1's upload
+    # and step i-1's download overlap step i's sweeps).
+    host_in, host_out = buffers
+    huge_before = huge_page_fraction([host_in] + host_out)
     host_in_t, host_out_t = torch.from_numpy(host_in), [torch.from_numpy(a) for a in host_out]
     pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
                     w["check_every"])
+    # the host quiet: no memory compaction running under the timed batches
+    settle_s, settled = wait_compaction_idle()
     dist_barrier(world)
     t0 = time.perf_counter()
     infos = pk.pk_run_batch(ctx, [host_in] * args.steps,
@@ -653,6 +700,7 @@ def e2e_steps(pk, ctx, w, args, world, torch):
     serial_value = dist_sum(world, serial_updates) / serial_s
     link = host_link_gbs(torch, host_in_t, host_out_t[0])
     link["huge_page_fraction"] = huge_page_fraction([host_in] + host_out)
+    link["huge_page_fraction_before"] = huge_before
     sweeps_ms = statistics.median(i["device_us"] for i in infos) / 1e3
     copy_ms = 2 * host_in_t.numel() * 4 / (link["both_gbs"] * 1e9) * 1e3
     return {"value": e2e_value, "seconds": e2e_s, "launches": e2e_launches,
@@ -660,7 +708,8 @@ def e2e_steps(pk, ctx, w, args, world, torch):
             # a step can go no faster than its sweeps or than both copies at
             # this box's two-way link rate, whichever is longer
             "bound_value": cells * sweeps / (max(sweeps_ms, copy_ms) * 1e-3),
-            "serial_value": serial_value, "serial_steps": serial_steps}
+            "serial_value": serial_value, "serial_steps": serial_steps,
+            "compaction_settle": {"waited_s": settle_s, "idle": settled}}
 
 
 def huge_page_fraction(arrays):
@@ -764,6 +813,7 @@ def main():
     ctx = pk.pk_create(nx, ny, w["u0"], w["f"],
                        pk.pk_options_default(stream_config=args.stream_config))
     try:
+        buffers = None if args.no_e2e else e2e_buffers(pk, w)
         plan = pk.pk_get_plan(ctx)
         clocks = ClockSampler(local)
         clocks.start()  # samples the warm-up too: a short timed region may hold none
@@ -789,12 +839,44 @@ def main():
         value = updates_all / dev_s_max
         ms_per_step = dev_s_max * 1e3 / args.steps
         us_per_sweep = dev_s * 1e6 / (updates / cells)
-        e2e = None if args.no_e2e else e2e_steps(pk, ctx, w, args, world, torch)
+        line = None if rank != 0 else result_line(args, w, world, value, ms_per_step, us_per_sweep,
+                                                  dev_us, run_info, host_s, clk)
+        # The end-to-end leg runs last, after the extras and the CPU
+        # baseline: the first run on a host that has just released a lot of
+        # page-locked memory (another process's exit) copied at about half
+        # speed for some seconds.
+        e2e = None if args.no_e2e else e2e_steps(pk, ctx, w, args, world, torch, buffers)
+        del buffers
     finally:
         pk.pk_destroy(ctx)
 
     if rank != 0:
         return
+    line["e2e"] = None if e2e is None else {
+        "value": e2e["value"], "unit": UNIT,
+        "h2d_bytes_per_step": int(w["u0"].nbytes),
+        "d2h_bytes_per_step": int(w["u0"].nbytes),
+        "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps); "
+               "host buffers from pk_host_alloc (page-locked, on transparent huge pages where granted)",
+        "steps": args.steps, "seconds": e2e["seconds"], "gpu_launches": e2e["launches"],
+        "sweeps_ms_per_step_median": e2e["sweeps_ms_median"],
+        "host_link": e2e["link"], "bound_value": e2e["bound_value"],
+        "frac_of_bound": e2e["value"] / e2e["bound_value"],
+        # untimed, before the timed batches: the host's memory compaction
+        # (which the huge-page faults of the buffers can start) idle
+        "host_compaction_settle": e2e["compaction_settle"]}
+    line["e2e_serial"] = None if e2e is None else {
+        "value": e2e["serial_value"], "unit": UNIT, "steps": e2e["serial_steps"],
+        "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"}
+    print(json.dumps(line), flush=True)
+
+
+def result_line(args, w, world, value, ms_per_step, us_per_sweep, dev_us, run_info, host_s, clk):
+    """Rank 0's JSON line without the end-to-end leg, with the CPU baseline
+    and the extras (both measured here)."""
+    from iterative_stencil_solver_gb300 import pk
+    nx, ny, sweeps = w["nx"], w["ny"], w["sweeps"]
+    cells = nx * ny
     peak, peak_kind = measured_peaks()
     launch_us = statistics.median(dev_us)
     alg_bytes = algorithmic_bytes(run_info, cells, run_info["sweeps_done"], w["f"] is not None,
@@ -825,19 +907,6 @@ def main():
                      "peak_source": peak_kind,
                      "kernel": shape_label(run_info, w["f"] is not None),
                      "algorithmic_bytes_per_launch": alg_bytes},
-        "e2e": None if e2e is None else {
-            "value": e2e["value"], "unit": UNIT,
-            "h2d_bytes_per_step": int(w["u0"].nbytes),
-            "d2h_bytes_per_step": int(w["u0"].nbytes),
-            "api": "pk_run_batch (pipelined: uploads and downloads overlap the sweeps); "
-                   "host buffers from pk_host_alloc (page-locked, on transparent huge pages where granted)",
-            "steps": args.steps, "seconds": e2e["seconds"], "gpu_launches": e2e["launches"],
-            "sweeps_ms_per_step_median": e2e["sweeps_ms_median"],
-            "host_link": e2e["link"], "bound_value": e2e["bound_value"],
-            "frac_of_bound": e2e["value"] / e2e["bound_value"]},
-        "e2e_serial": None if e2e is None else {
-            "value": e2e["serial_value"], "unit": UNIT, "steps": e2e["serial_steps"],
-            "api": "pk_set_field + pk_run_sweeps + pk_get_field per step"},
         "clocks": clk,
     }
     if not args.no_cpu_baseline:
@@ -854,7 +923,7 @@ def main():
                                                  "seconds": dta}
     if not args.no_extras:
         line["extras"] = latency_extras(pk)
-    print(json.dumps(line), flush=True)
+    return line
 
 
 if __name__ == "__main__":

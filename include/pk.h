@@ -319,9 +319,8 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
  * `bytes` of zeroed memory.  Where the operating system backs all of it with
  * transparent huge pages of its size (hpage_pmd_size: 2 MB with 4 KB base
  * pages, 512 MB with 64 KB ones; anonymous mmap on a huge-page boundary,
- * madvise MADV_HUGEPAGE, and where the first touch left small pages a
- * synchronous MADV_COLLAPSE of the range, checked in /proc/self/smaps) the
- * region is registered with cudaHostRegister; otherwise, and for requests
+ * madvise MADV_HUGEPAGE, checked in /proc/self/smaps) the region is
+ * registered with cudaHostRegister; otherwise, and for requests
  * that whole huge pages would more than double, it comes from
  * cudaHostAlloc.  On a GB300
  * host, batches copying from cudaHostAlloc memory ran at full rate in some

@@ -1533,14 +1533,6 @@ size_t thp_bytes() {
     }();
     return v;
 }
-// madvise advice that collapses a populated range into huge pages at once,
-// compacting memory as needed (Linux 6.1 and later; older kernels refuse it
-// with EINVAL).  Spelled out where the C library's headers predate it.
-#ifdef MADV_COLLAPSE
-constexpr int kMadvCollapse = MADV_COLLAPSE;
-#else
-constexpr int kMadvCollapse = 25;
-#endif
 
 // Bytes of [lo, hi) that the kernel backs with transparent huge pages
 // (AnonHugePages of the mappings that overlap it in /proc/self/smaps); -1
@@ -1578,10 +1570,8 @@ int pk_host_alloc(int64_t bytes, void **ptr) {
     // huge-page boundary (one huge page of slack), every page touched, then
     // registered.  Kept only when the kernel backed all of it with huge
     // pages: registered small pages copy far slower than cudaHostAlloc's.
-    // Where the pages touched were not all huge (memory too fragmented for
-    // the fault path to find the blocks), the range is collapsed in place
-    // once before giving up.  Not tried where rounding up to whole huge
-    // pages would more than double the request (small arrays).
+    // Not tried where rounding up to whole huge pages would more than double
+    // the request (small arrays).
     void *map = len <= 2 * (size_t)bytes
                     ? mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0)
                     : MAP_FAILED;
@@ -1590,7 +1580,6 @@ int pk_host_alloc(int64_t bytes, void **ptr) {
         char *start = base + (hp - (reinterpret_cast<uintptr_t>(base) % hp)) % hp;
         if (madvise(start, len, MADV_HUGEPAGE) == 0) {
             std::memset(start, 0, len);
-            if (huge_page_bytes(start, start + len) < (long long)len) (void)madvise(start, len, kMadvCollapse);
             if (huge_page_bytes(start, start + len) >= (long long)len &&
                 cudaHostRegister(start, len, cudaHostRegisterDefault) == cudaSuccess) {
                 std::lock_guard<std::mutex> lock(g_host_mutex);

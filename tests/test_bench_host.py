@@ -93,3 +93,17 @@ def test_clock_summary_keeps_the_timed_region(tmp_path):
     cs.offset = len(idle + warm + busy + busy)
     got = cs._summary()
     assert got["samples"] == 1 and got["sm_mhz"] == 2040 and got["window"].startswith("last warm-up")
+
+
+def test_compaction_settle_wait_is_bounded():
+    # the e2e leg's wait for the host's memory compaction to be idle ends
+    # within its limit whatever the host is doing, and says whether it saw
+    # the idle state (None where /proc/vmstat cannot be read)
+    import time
+    import bench
+    t0 = time.perf_counter()
+    waited, idle = bench.wait_compaction_idle(limit_s=1.0, quiet_s=0.2)
+    assert time.perf_counter() - t0 < 2.0 and 0.0 <= waited <= 1.5
+    assert idle in (True, False, None)
+    pages = bench.compaction_pages()
+    assert pages is None or pages >= 0
