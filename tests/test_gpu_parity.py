@@ -724,6 +724,31 @@ def test_host_alloc_buffers_in_a_batch(pk):
     gc.collect()
 
 
+def test_host_alloc_huge_page_buffers_in_a_batch(pk):
+    """Field-sized pk_host_alloc buffers (268 MB: within one huge page of the
+    request on both 4 KB- and 64 KB-page kernels, so the huge-page path is
+    tried) as the host arrays of pk_run_batch: zeroed, aligned, the oracle's
+    bits, freed with the arrays."""
+    import gc
+    nx = ny = 8190
+    fields = [inputs.random_field(nx, ny, seed=1600 + i) for i in range(2)]
+    ins = [pk.pk_host_array(f.shape) for f in fields]
+    outs = [pk.pk_host_array(f.shape) for f in fields]
+    for a in ins + outs:
+        assert a.ctypes.data % 4096 == 0 and not a.any()
+    for a, f in zip(ins, fields):
+        a[...] = f
+    ctx = pk.pk_create(nx, ny, fields[0], None)
+    try:
+        pk.pk_run_batch(ctx, ins, outs, 4, 0.0, 0)
+    finally:
+        pk.pk_destroy(ctx)
+    for f, o in zip(fields, outs):
+        assert_same_bits(o, oracle.jacobi_run(f, n=4, threads=THREADS)[0])
+    del ins, outs
+    gc.collect()
+
+
 def test_pass_counters_with_ctas_that_own_no_rows(pk):
     # 100 CTAs of the one-sweep shape on 50 (strip, row) pairs: every other
     # CTA owns nothing, passes through the loop all the same and publishes
