@@ -174,7 +174,9 @@ typedef struct {
                                          two or more sweeps shape 10 (Laplace) or, for
                                          Poisson, 13 (12 where nx is a multiple of 1024 and at
                                          least 8192), and for their runs with residual checks
-                                         shape 10 or 12 (their passes straddle the checks);
+                                         shape 10, or for Poisson 14 (nx not a multiple of
+                                         1024 and below 6144) or 12 (their passes straddle
+                                         the checks);
                                          shape 3 for the rest and for the per-launch and graph
                                          paths (pk_run_info.stream_config says which ran).
                                          Index into {float4 groups per thread, TMA ring depth,

@@ -363,8 +363,16 @@ inline int default_multi_sweep_shape(bool poisson, int nx) {
 // registers, which shape 13's does not (it compiles with a 16-byte stack
 // frame at its 128-register cap).  At 4096^2 Poisson with a check every 10
 // sweeps shape 12 ran 13.53 us/sweep, shape 13's straddling kernel 13.64,
-// and shape 13 with its passes stopping at the checks 15.34.
-inline int default_check_shape(bool poisson, int) { return poisson ? 12 : 10; }
+// and shape 13 with its passes stopping at the checks 15.34.  On widths
+// that are not a multiple of 1024 the two-CTA narrow shape 14 is faster up
+// to about 6000 columns (check every 10, us/sweep, 14 against 12): 3584^2
+// 11.90 / 14.93, 4097^2 17.13 / 19.27, 4000^2 15.86 / 16.28, 3000^2 10.32 /
+// 10.78; 6000^2 30.46 / 30.43, 8000^2 53.85 / 52.08, and on the multiples
+// of 1024 shape 12 (4096^2 13.70 / 13.89, 8192^2 47.91 / 48.65).
+inline int default_check_shape(bool poisson, int nx) {
+    if (!poisson) return 10;
+    return nx % 1024 != 0 && nx < 6144 ? 14 : 12;
+}
 
 // Sets the message pk_last_error(NULL) returns (defined in pk_host.cu).
 void set_global_error(const char *msg);

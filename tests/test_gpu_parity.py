@@ -852,15 +852,19 @@ def test_three_sweep_residual_extreme_scales(pk, cfg, scale, poisson):
 
 # The automatic plan's Poisson shapes: the narrow three-CTA shape 13 for runs
 # without checks, except on widths that are multiples of 1024 from 8192 up
-# (shape 12); runs with checks take shape 12, whose passes straddle them.
-# Short fields keep the oracle fast; the bits are the oracle's either way.
-@pytest.mark.parametrize("nx,want_plain", [(4096, 13), (4000, 13), (8192, 12), (8200, 13)],
-                         ids=["4096", "4000", "8192", "8200"])
-def test_poisson_plan_shapes(pk, nx, want_plain):
+# (shape 12); runs with checks take a shape whose passes straddle them, the
+# two-CTA narrow shape 14 on widths below 6144 that are not a multiple of
+# 1024, else shape 12.  Short fields keep the oracle fast; the bits are the
+# oracle's either way.
+PLAN_SHAPES = [(4096, 13, 12), (4000, 13, 14), (8192, 12, 12), (8200, 13, 12), (6000, 13, 14)]
+
+
+@pytest.mark.parametrize("nx,want_plain,want_check", PLAN_SHAPES, ids=[str(c[0]) for c in PLAN_SHAPES])
+def test_poisson_plan_shapes(pk, nx, want_plain, want_check):
     ny = 40
     u0 = inputs.random_field(nx, ny, seed=950 + nx)
     f = inputs.uniform_pm1(951 + nx, nx * ny).reshape(ny, nx)
-    for n, tol, ce, shape, straddle in ((12, 0.0, 0, want_plain, 0), (23, 1e-30, 5, 12, 1)):
+    for n, tol, ce, shape, straddle in ((12, 0.0, 0, want_plain, 0), (23, 1e-30, 5, want_check, 1)):
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, variant=2)
         assert info["variant"] == 2 and info["stream_config"] == shape, info
@@ -882,9 +886,10 @@ def test_auto_direct_context_takes_multi_sweep_stream(pk, nx, ny, poisson):
         assert pk.pk_get_plan(ctx)["variant"] == 1
     finally:
         pk.pk_destroy(ctx)
-    # runs with checks take the check shape (12 or 10), runs without the
-    # multi-sweep shape (13 for Poisson below 8192 columns, else 10)
-    for n, tol, ce, want_variant, want_shape in ((10, 1e-30, 4, 2, 12 if poisson else 10),
+    # runs with checks take the check shape (10, or 14 for Poisson on these
+    # widths), runs without the multi-sweep shape (13 for Poisson below 8192
+    # columns, else 10)
+    for n, tol, ce, want_variant, want_shape in ((10, 1e-30, 4, 2, 14 if poisson else 10),
                                                  (10, 0.0, 0, 2, 13 if poisson else 10),
                                                  (1, 0.0, 0, 1, None)):
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
@@ -920,11 +925,13 @@ DEFAULT_SHAPE_RUNS = [
 def test_default_stream_plan_takes_two_sweep_shape(pk, nx, ny, poisson):
     u0 = inputs.random_field(nx, ny, seed=500 + nx + ny)
     f = inputs.uniform_pm1(600 + nx, nx * ny).reshape(ny, nx) if poisson else None
-    # three sweeps per pass: for Poisson shape 13 without checks and 12 (the
-    # straddling kernel) with them, for Laplace shape 10
+    # three sweeps per pass: for Poisson shape 13 without checks and with
+    # them the straddling kernel of shape 14 (widths below 6144 that are not
+    # a multiple of 1024) or 12, for Laplace shape 10
+    check_shape = 14 if nx % 1024 and nx < 6144 else 12
     for n, tol, ce, shape in DEFAULT_SHAPE_RUNS:
         if shape == MULTI:
-            shape = (12 if tol > 0 and ce > 0 else 13) if poisson else 10
+            shape = (check_shape if tol > 0 and ce > 0 else 13) if poisson else 10
         want, oinfo = oracle.jacobi_run(u0, f=f, n=n, tol=tol, check_every=ce)
         got, info = run_pk(pk, u0, f, n, tol, ce, path="persistent", variant=2)
         assert info["variant"] == 2 and info["stream_config"] == shape, (n, tol, ce, info)
