@@ -65,8 +65,8 @@ DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 # summarised in profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of
 # one full-size launch: 16384^2, 100 sweeps); valid only while the kernel
 # source hash and the STREAM shape match.
-TRAFFIC = {"kernel_sha": "63d47287fbdf76a4", "stream_config": 10,
-           "bytes_per_launch": 37.931e9 + 36.667e9}
+TRAFFIC = {"kernel_sha": "c47dbabb6dba974d", "stream_config": 10,
+           "bytes_per_launch": 37.969e9 + 36.674e9}
 
 
 # pk_options.stream_config shapes: (float4 groups per thread, ring depth, sweeps per pass,
