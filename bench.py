@@ -658,6 +658,21 @@ def wait_compaction_idle(limit_s=20.0, quiet_s=0.5):
     return time.perf_counter() - t0, False
 
 
+def wait_huge_pages(arrays, target, limit_s=20.0):
+    """Wait until the arrays' huge-page share is back at `target` (their
+    share when made), at most limit_s; returns (seconds waited, reached)."""
+    t0 = time.perf_counter()
+    if not target:
+        return 0.0, None
+    while True:
+        cur = huge_page_fraction(arrays)
+        if cur is None or cur >= 0.999 * target:
+            return time.perf_counter() - t0, cur is not None
+        if time.perf_counter() - t0 >= limit_s:
+            return time.perf_counter() - t0, False
+        time.sleep(0.1)
+
+
 def e2e_steps(pk, ctx, w, args, world, torch, buffers):
     """The bench steps end to end through the public API (host buffers in and
     out); returns the e2e record and the serial set/run/get number."""
@@ -672,7 +687,13 @@ def e2e_steps(pk, ctx, w, args, world, torch, buffers):
     host_in_t, host_out_t = torch.from_numpy(host_in), [torch.from_numpy(a) for a in host_out]
     pk.pk_run_batch(ctx, [host_in] * 3, [host_out[q % 2] for q in range(3)], sweeps, w["tol"],
                     w["check_every"])
-    # the host quiet: no memory compaction running under the timed batches
+    # The host settled before the timed batches.  On the GB300 hosts the
+    # first batch call of a process (its device buffers and mapped records
+    # made after many other contexts came and went) has split every huge
+    # page of these buffers, which the kernel rebuilt within a second or
+    # so; timed in between, the copies ran at a third of their rate.  So:
+    # the buffers back on huge pages, then no memory compaction running.
+    huge_wait_s, huge_back = wait_huge_pages([host_in] + host_out, huge_before)
     settle_s, settled = wait_compaction_idle()
     dist_barrier(world)
     t0 = time.perf_counter()
@@ -709,7 +730,8 @@ def e2e_steps(pk, ctx, w, args, world, torch, buffers):
             # this box's two-way link rate, whichever is longer
             "bound_value": cells * sweeps / (max(sweeps_ms, copy_ms) * 1e-3),
             "serial_value": serial_value, "serial_steps": serial_steps,
-            "compaction_settle": {"waited_s": settle_s, "idle": settled}}
+            "compaction_settle": {"waited_s": settle_s, "idle": settled},
+            "huge_page_wait": {"waited_s": huge_wait_s, "restored": huge_back}}
 
 
 def huge_page_fraction(arrays):
@@ -862,8 +884,9 @@ def main():
         "sweeps_ms_per_step_median": e2e["sweeps_ms_median"],
         "host_link": e2e["link"], "bound_value": e2e["bound_value"],
         "frac_of_bound": e2e["value"] / e2e["bound_value"],
-        # untimed, before the timed batches: the host's memory compaction
-        # (which the huge-page faults of the buffers can start) idle
+        # untimed, before the timed batches: the buffers back on huge pages,
+        # then the host's memory compaction idle
+        "host_huge_page_wait": e2e["huge_page_wait"],
         "host_compaction_settle": e2e["compaction_settle"]}
     line["e2e_serial"] = None if e2e is None else {
         "value": e2e["serial_value"], "unit": UNIT, "steps": e2e["serial_steps"],

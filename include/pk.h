@@ -318,13 +318,14 @@ int pk_run_batch(pk_ctx *ctx, int count, const float *const *host_in, float *con
 
 /* Page-locked HOST memory for the host arrays of pk_run_batch, pk_set_field
  * and pk_get_field (a library convenience; the pages have no counterpart):
- * `bytes` of zeroed memory.  Where the operating system backs all of it with
- * transparent huge pages of its size (hpage_pmd_size: 2 MB with 4 KB base
- * pages, 512 MB with 64 KB ones; anonymous mmap on a huge-page boundary,
- * madvise MADV_HUGEPAGE, checked in /proc/self/smaps) the region is
- * registered with cudaHostRegister; otherwise, and for requests
- * that whole huge pages would more than double, it comes from
- * cudaHostAlloc.  On a GB300
+ * `bytes` of zeroed memory.  On kernels with 2 MB transparent huge pages
+ * (4 KB base pages), where the operating system backs all of it with them
+ * (anonymous mmap on a 2 MB boundary, madvise MADV_HUGEPAGE, checked in
+ * /proc/self/smaps), the region is registered with cudaHostRegister;
+ * otherwise, for requests that whole huge pages would more than double, and
+ * on kernels with larger huge pages (512 MB with 64 KB base pages, as on
+ * GB300 hosts: there registered 512 MB pages were split and rebuilt while
+ * batches ran, and the copies slowed), it comes from cudaHostAlloc.  On a GB300
  * host, batches copying from cudaHostAlloc memory ran at full rate in some
  * batches and 20-50% slower in others (the copy engines' translation of
  * gigabytes of host pages); from huge pages every batch ran at full rate,

@@ -1522,6 +1522,7 @@ std::map<void *, std::pair<void *, size_t>> g_host_regions;
 // The kernel's transparent huge page (PMD) size: 2 MB with 4 KB base pages,
 // 512 MB with 64 KB ones (as on GB300 hosts running a 64 KB-page kernel);
 // 2 MB where the kernel does not say.
+constexpr size_t kThpPreferred = size_t(2) << 20;
 size_t thp_bytes() {
     static const size_t v = [] {
         unsigned long long x = 0;
@@ -1566,13 +1567,18 @@ int pk_host_alloc(int64_t bytes, void **ptr) {
     }
     const size_t hp = thp_bytes();
     size_t len = ((size_t)bytes + hp - 1) / hp * hp;
-    // First choice: anonymous memory on transparent huge pages, started on a
-    // huge-page boundary (one huge page of slack), every page touched, then
-    // registered.  Kept only when the kernel backed all of it with huge
-    // pages: registered small pages copy far slower than cudaHostAlloc's.
-    // Not tried where rounding up to whole huge pages would more than double
-    // the request (small arrays).
-    void *map = len <= 2 * (size_t)bytes
+    // First choice, on kernels with 2 MB transparent huge pages: anonymous
+    // memory on them, started on a huge-page boundary (one huge page of
+    // slack), every page touched, then registered.  Kept only when the
+    // kernel backed all of it with huge pages: registered small pages copy
+    // far slower than cudaHostAlloc's.  Not tried where rounding up to whole
+    // huge pages would more than double the request (small arrays), nor on
+    // kernels whose huge pages are larger (512 MB with 64 KB base pages, as
+    // on the GB300 hosts): there the kernel split and rebuilt registered
+    // 512 MB pages while a process's batches ran, and the pipelined copies
+    // slowed to a quarter to a half of their rate, where cudaHostAlloc
+    // memory held its rate in most runs.
+    void *map = hp <= kThpPreferred && len <= 2 * (size_t)bytes
                     ? mmap(nullptr, len + hp, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0)
                     : MAP_FAILED;
     if (map != MAP_FAILED) {

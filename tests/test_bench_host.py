@@ -107,3 +107,18 @@ def test_compaction_settle_wait_is_bounded():
     assert idle in (True, False, None)
     pages = bench.compaction_pages()
     assert pages is None or pages >= 0
+
+
+def test_huge_page_wait_is_bounded():
+    # the e2e leg's wait for its buffers' huge pages: immediate where there
+    # is nothing to wait for, and never past its limit
+    import time
+    import numpy as np
+    import bench
+    a = np.zeros(1 << 20, dtype=np.float32)
+    assert bench.wait_huge_pages([a], 0.0) == (0.0, None)
+    t0 = time.perf_counter()
+    waited, reached = bench.wait_huge_pages([a], 1.0, limit_s=0.5)
+    assert time.perf_counter() - t0 < 1.5 and waited <= 1.0
+    frac = bench.huge_page_fraction([a])
+    assert reached == (frac is not None and frac >= 0.999)
