@@ -416,8 +416,8 @@ def pk_debug_coverage_read(ctx):
 
 
 def pk_host_alloc(nbytes):
-    """Address of `nbytes` of page-locked host memory (on transparent huge
-    pages where the kernel grants them)."""
+    """Address of `nbytes` of page-locked host memory (on 2 MB transparent
+    huge pages where the kernel grants them)."""
     ptr = _VP()
     _check(_lib.pk_host_alloc(nbytes, ctypes.byref(ptr)))
     return ptr.value

@@ -725,10 +725,10 @@ def test_host_alloc_buffers_in_a_batch(pk):
 
 
 def test_host_alloc_huge_page_buffers_in_a_batch(pk):
-    """Field-sized pk_host_alloc buffers (268 MB: within one huge page of the
-    request on both 4 KB- and 64 KB-page kernels, so the huge-page path is
-    tried) as the host arrays of pk_run_batch: zeroed, aligned, the oracle's
-    bits, freed with the arrays."""
+    """Field-sized pk_host_alloc buffers (268 MB: the huge-page path on kernels
+    with 2 MB huge pages, cudaHostAlloc on those with larger ones) as the host
+    arrays of pk_run_batch: zeroed, aligned, the oracle's bits, freed with the
+    arrays."""
     import gc
     nx = ny = 8190
     fields = [inputs.random_field(nx, ny, seed=1600 + i) for i in range(2)]
