@@ -58,6 +58,8 @@ WORKLOADS = {
     # seven passes: checks at 0, 10 and 20 fall in stages 1, 2 and 3
     "poisson-4096x4096-21sweeps-res10": (4096, 2, 21, True, 1e-4, 10),
     "poisson-4096x4096-21sweeps": (4096, 2, 21, True, 0.0, 0),
+    # the same for Laplace: checks at 0, 10 and 20 (tolerance below any residual)
+    "laplace-8192x8192-21sweeps-res10": (8192, 3, 21, False, 1e-30, 10),
 }
 DEFAULT_WORKLOAD = "laplace-16384x16384-100sweeps"
 
