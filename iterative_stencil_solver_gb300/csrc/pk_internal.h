@@ -133,8 +133,11 @@ __host__ __device__ inline long long split_owner(const StreamSplit &s, long long
 // stack).  Measured with pass counters on GB300 (Poisson, us/sweep at
 // 4000^2, 4097^2, 3584^2, 8000^2): equal costs 20.4, 25.8, 18.4, 76.6;
 // 29/20 15.9, 19.6, 14.4, 56.6; 35/20 14.2, 17.6, 12.9, 49.2; 40/20 14.5,
-// 17.2, 13.2, 46.9; 46/20 15.1, 18.1, 13.8, 48.3.  The other kernels' ragged
-// strips cost what full ones do.
+// 17.2, 13.2, 46.9; 46/20 15.1, 18.1, 13.8, 48.3.  The Laplace straddling
+// kernels, a check every 10 sweeps (16384^2, 8192^2, 4096^2, 6000^2): equal
+// costs 203.2, 56.7, 15.9, 29.8; 30/20 154.9, 44.1, 13.2, 23.9; 38/20 144.3,
+// 38.7, 12.7, 21.1; 46/20 143.5, 38.7, 12.4, 21.8.  The other kernels'
+// ragged strips cost what full ones do.
 constexpr int kSplitUnit = 20;
 constexpr int kSplitRaggedRolled3 = 38;
 // The split of a STREAM grid of G CTAs and strips `tw` columns wide, the
