@@ -161,8 +161,9 @@ def test_binding_constants_match_the_header(pk):
 
 def test_gpu_tests_strip_widths_follow_the_shape_table():
     """The GPU tests size their narrow-last-strip grids from a table of strip
-    widths (4 x float4 groups per thread x consumer threads); it must follow
-    the library's STREAM shape table."""
+    widths (4 x float4 groups per thread x consumer threads), and bench.py
+    keeps a table of the shapes; both must follow the library's STREAM shape
+    table."""
     src = open(os.path.join(ROOT, "iterative_stencil_solver_gb300", "csrc", "pk_internal.h")).read()
     body = re.search(r"kStreamConfigs\[kNumStreamConfigs\]\s*=\s*\{(.*?)\};", src, flags=re.S).group(1)
     shapes = [tuple(int(v) for v in m.split(","))
@@ -174,6 +175,10 @@ def test_gpu_tests_strip_widths_follow_the_shape_table():
     mod = importlib.util.module_from_spec(spec)
     spec.loader.exec_module(mod)
     assert mod.STREAM_TW == widths
+    # and bench.py labels and accounts its passes from its own copy
+    import bench
+    assert bench.SHAPES == {cfg: (qpt, stages, depth, consumers)
+                            for cfg, (qpt, stages, depth, _, consumers) in enumerate(shapes)}
 
 
 def test_coverage_build_exports_the_debug_calls():
